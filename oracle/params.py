@@ -1,0 +1,242 @@
+"""Parameter rules (S, t, M) of Prof-K, in fp64.
+
+Two versions of the paper disagree here; both are written out so that tests can
+hold each to its own page.
+
+Corrected version ("Prof-K: Probabilistic One-Pass Filtering for Efficient
+Top-k Selection", arXiv HTML):
+  * Theorem 4 (exact optimal parameters): t* = F^{-1}_{N,k-1,S}(1-eps_A) + 1,
+    M* = min{M >= k : F_{N,M,S}(t*-1) <= eps_B};  Propositions 2-3 give the
+    exact failure probabilities.
+  * Algorithm 1 (fast approximate parameters), Appendix B Eq 9-12: Acklam's
+    inverse normal, the Cornish-Fisher threshold rank (mu >= 15), the Poisson
+    quantile (mu < 15) and the Wilson-Hilferty buffer capacity.
+  * Proposition 7: S1 = (z/r)^(2/3) (kN)^(1/3), S2 = (kappa N / r)^(1/2).
+
+Older version (same title, mirrored page):
+  * Lemma 2 normal approximation, Eq 6 threshold rank, Corollary 4 buffer
+    size M = k + z sqrt(k(N-k)/S (1-S/N)) with z = z_A + z_B, Theorem 5
+    S* = (z tau_B log k / (2 tau_A))^(2/3) (k(N-k))^(1/3), and its Algorithm 1
+    (S clamped to [32768, 131072], "t <- 1 if alpha S < -ln(eps/2)").
+
+Default rule used by the library (a reading, because the two versions conflict):
+S from the older version's Theorem 5 with its clamp, rounding and log2 (its
+Algorithm 1, lines 1-4), and t, M from the corrected Algorithm 1 (lines 5-15)
+with z = Phi^{-1}(1 - eps/2), then 1 <= t <= S and k <= M <= N.  The older
+t-rule sets t = 1 exactly where recall failure is likely (its own text derives
+the bound in the wrong direction), so it is kept only as a named function and
+an optional mode.
+"""
+from __future__ import annotations
+
+import math
+
+from . import hypergeom
+
+# ---------------------------------------------------------------------------
+# Inverse standard normal: P. J. Acklam's rational approximation (relative
+# error below 1.15e-9), as the corrected paper prescribes (Appendix B).
+# Coefficients from Acklam's published algorithm.
+_A = (-3.969683028665376e+01, 2.209460984245205e+02, -2.759285104469687e+02,
+      1.383577518672690e+02, -3.066479806614716e+01, 2.506628277459239e+00)
+_B = (-5.447609879822406e+01, 1.615858368580409e+02, -1.556989798598866e+02,
+      6.680131188771972e+01, -1.328068155288572e+01)
+_C = (-7.784894002430293e-03, -3.223964580411365e-01, -2.400758277161838e+00,
+      -2.549732539343734e+00, 4.374664141464968e+00, 2.938163982698783e+00)
+_D = (7.784695709041462e-03, 3.224671290700398e-01, 2.445134137142996e+00,
+      3.754408661907416e+00)
+_P_LOW = 0.02425
+
+
+def norm_ppf(p: float) -> float:
+    """Phi^{-1}(p) for p in (0, 1) by Acklam's three-region rational fit."""
+    if not (0.0 < p < 1.0):
+        raise ValueError("p must be in (0, 1)")
+    if p < _P_LOW:
+        q = math.sqrt(-2.0 * math.log(p))
+        return ((((((_C[0] * q + _C[1]) * q + _C[2]) * q + _C[3]) * q + _C[4]) * q + _C[5])
+                / ((((_D[0] * q + _D[1]) * q + _D[2]) * q + _D[3]) * q + 1.0))
+    if p > 1.0 - _P_LOW:
+        q = math.sqrt(-2.0 * math.log1p(-p))
+        return -((((((_C[0] * q + _C[1]) * q + _C[2]) * q + _C[3]) * q + _C[4]) * q + _C[5])
+                 / ((((_D[0] * q + _D[1]) * q + _D[2]) * q + _D[3]) * q + 1.0))
+    q = p - 0.5
+    r = q * q
+    return ((((((_A[0] * r + _A[1]) * r + _A[2]) * r + _A[3]) * r + _A[4]) * r + _A[5]) * q
+            / (((((_B[0] * r + _B[1]) * r + _B[2]) * r + _B[3]) * r + _B[4]) * r + 1.0))
+
+
+# ---------------------------------------------------------------------------
+# Corrected version: exact analysis.
+
+def prob_recall_failure(N: int, k: int, S: int, t: int) -> float:
+    """Proposition 2: Pr(R < k) = 1 - F_{N,k-1,S}(t-1)."""
+    return hypergeom.sf(N, k - 1, S, t - 1)
+
+
+def prob_overflow(N: int, S: int, t: int, M: int) -> float:
+    """Proposition 3: Pr(R > M) = F_{N,M,S}(t-1)."""
+    return hypergeom.cdf(N, M, S, t - 1)
+
+
+def prob_fail(N: int, k: int, S: int, t: int, M: int) -> float:
+    """Eq 8: Pr(A or B) = Pr(R < k) + Pr(R > M) (disjoint because M >= k)."""
+    return prob_recall_failure(N, k, S, t) + prob_overflow(N, S, t, M)
+
+
+def params_exact(N: int, k: int, S: int, eps: float, eps_a: float | None = None,
+                 eps_b: float | None = None):
+    """Theorem 4: exact optimal (t*, M*) for a given S; default split eps/2."""
+    eps_a = eps / 2 if eps_a is None else eps_a
+    eps_b = eps / 2 if eps_b is None else eps_b
+    t = hypergeom.quantile(N, k - 1, S, 1.0 - eps_a) + 1
+    lo, hi = k, N  # G(M) = F_{N,M,S}(t-1) is nonincreasing in M and G(N) = 0
+    while lo < hi:
+        mid = (lo + hi) // 2
+        if hypergeom.cdf(N, mid, S, t - 1) <= eps_b:
+            hi = mid
+        else:
+            lo = mid + 1
+    return t, lo
+
+
+def threshold_rank_fast(N: int, k: int, S: int, eps: float) -> int:
+    """Algorithm 1 lines 5-14: Eq 10 (Cornish-Fisher) or Eq 11 (Poisson)."""
+    z = norm_ppf(1.0 - eps / 2)
+    mu = (k - 1) * S / N
+    if mu >= 15:
+        sigma = math.sqrt(mu * (1.0 - (k - 1) / N) * (N - S) / (N - 1))
+        return math.ceil(mu + z * sigma + (z * z - 1.0) / 6.0) + 1
+    p = math.exp(-mu)
+    c = p
+    j = 0
+    while c < 1.0 - eps / 2:
+        j += 1
+        p = p * mu / j
+        c = c + p
+    return j + 1
+
+
+def buffer_capacity_fast(N: int, S: int, t: int, eps: float) -> int:
+    """Algorithm 1 line 15: Eq 12, Wilson-Hilferty quantile of Gamma(t,1)."""
+    z = norm_ppf(1.0 - eps / 2)
+    h = 1.0 / (9.0 * t)
+    return math.ceil((N + 1) / (S + 1) * t * (1.0 - h + z * math.sqrt(h)) ** 3)
+
+
+def params_fast(N: int, k: int, S: int, eps: float):
+    """Algorithm 1 lines 5-15 for a given S, then 1 <= t <= S and k <= M <= N."""
+    t = min(max(threshold_rank_fast(N, k, S, eps), 1), S)
+    M = min(max(buffer_capacity_fast(N, S, t, eps), k), N)
+    return t, M
+
+
+def mean_rank(N: int, S: int, t: int) -> float:
+    """Lemma 6: E[R] = (N+1) t / (S+1)."""
+    return (N + 1) * t / (S + 1)
+
+
+def sample_size_prop7(N: int, k: int, eps: float, r: float):
+    """Proposition 7 candidates (S1, S2) for cost ratio r; kappa = z^2 + 1/2.
+
+    parity unpinned against the pages' Table 3 S column (that column also
+    depends on an unstated cap); the tests pin only Proposition 7's bracket.
+    """
+    z = norm_ppf(1.0 - eps / 2)
+    kappa = z * z + 0.5
+    S1 = (z / r) ** (2.0 / 3.0) * (k * N) ** (1.0 / 3.0)
+    S2 = math.sqrt(kappa * N / r)
+    return S1, S2
+
+
+# ---------------------------------------------------------------------------
+# Older version: closed forms.
+
+def lemma2_normal(N: int, S: int, t: int):
+    """Lemma 2 (Eq 4): R ~ Normal(N q, N^2 q (1-q) f / S), q = t/S, f = 1 - S/N."""
+    q = t / S
+    f = 1.0 - S / N
+    return N * q, N * N * q * (1.0 - q) * f / S
+
+
+def lemma1_nhg_moments(N: int, S: int, t: int):
+    """Older Lemma 1 (Eq 2): mean and variance of the negative hypergeometric R."""
+    mean = (N + 1) * t / (S + 1)
+    var = t * (S - t + 1) * (N + 1) * (N - S) / ((S + 1) ** 2 * (S + 2))
+    return mean, var
+
+
+def t_eq6(N: int, k: int, S: int, z_a: float) -> int:
+    """Eq 6: t = ceil(S alpha + z_A sqrt(S alpha (1-alpha) f))."""
+    alpha = k / N
+    f = 1.0 - S / N
+    return math.ceil(S * alpha + z_a * math.sqrt(S * alpha * (1.0 - alpha) * f))
+
+
+def m_cor4(N: int, k: int, S: int, z: float) -> float:
+    """Corollary 4 (Eq 12): M = k + z sqrt(k (N-k) / S * (1 - S/N)), z = z_A + z_B."""
+    return k + z * math.sqrt(k * (N - k) / S * (1.0 - S / N))
+
+
+def s_thm5(N: int, k: int, z: float, cost_ratio: float = 1.0, log=math.log2) -> float:
+    """Theorem 5 (Eq 14): S* = (z (tau_B/tau_A) log k / 2)^(2/3) (k (N-k))^(1/3)."""
+    return (z * cost_ratio * log(k) / 2.0) ** (2.0 / 3.0) * (k * (N - k)) ** (1.0 / 3.0)
+
+
+def s_star_scaling(N: int, k: int) -> float:
+    """Theorem 5's k << N scaling S* ~ (k (N-k))^(1/3) with unit prefactor."""
+    return (k * (N - k)) ** (1.0 / 3.0)
+
+
+S_MIN_OLD = 32768
+S_MAX_OLD = 131072
+
+
+def sample_size_old(N: int, k: int, eps: float, s_min: int = S_MIN_OLD,
+                    s_max: int = S_MAX_OLD, cost_ratio: float = 1.0) -> int:
+    """Older Algorithm 1 lines 1-4: z = 2 Phi^{-1}(1-eps/2), S* with log2, round, clamp."""
+    z = 2.0 * norm_ppf(1.0 - eps / 2)
+    s = s_thm5(N, k, z, cost_ratio) if k > 1 else 0.0
+    return int(min(s_max, max(s_min, math.floor(s + 0.5))))
+
+
+def params_old(N: int, k: int, eps: float, s_min: int = S_MIN_OLD, s_max: int = S_MAX_OLD,
+               cost_ratio: float = 1.0):
+    """Older Algorithm 1, literally (lines 1-9)."""
+    z = 2.0 * norm_ppf(1.0 - eps / 2)
+    alpha = k / N
+    S = sample_size_old(N, k, eps, s_min, s_max, cost_ratio)
+    f = 1.0 - S / N
+    t = max(1, math.ceil(S * alpha + z / 2.0 * math.sqrt(S * alpha * (1.0 - alpha) * f)))
+    M = math.ceil(k + z * math.sqrt(k * (N - k) / S * f))
+    if alpha * S < -math.log(eps / 2):
+        t = 1
+    return S, t, M
+
+
+# ---------------------------------------------------------------------------
+# The library's rule.
+
+MODE_DEFAULT = 0
+MODE_OLD = 1
+
+
+def params(N: int, k: int, eps: float, mode: int = MODE_DEFAULT):
+    """(S, t, M) as the library computes them (see the module docstring)."""
+    if mode == MODE_OLD:
+        S, t, M = params_old(N, k, eps)
+        S = min(S, N)
+        return S, min(max(t, 1), S), min(max(M, k), N)
+    S = min(sample_size_old(N, k, eps), N)
+    t, M = params_fast(N, k, S, eps)
+    return S, t, M
+
+
+def uses_filter(N: int, k: int, S: int) -> bool:
+    """Route: sample-and-filter only when S <= N/8 and k <= N/64.
+
+    Otherwise sampling buys nothing (the corrected paper's Appendix B keeps the
+    floor sample size once k/N exceeds about 2^-10, and a sample that is a
+    sizable share of the input is itself a full pass); the exact path runs.
+    """
+    return 8 * S <= N and 64 * k <= N

@@ -1,0 +1,155 @@
+"""Pins of the oracle's hypergeometric law and parameter rules.
+
+Sources: the corrected page's Table 3 (golden file), its stated error bound of
+Acklam's approximation, its Appendix B remarks (k = 1 gives t = 1; the
+Wilson-Hilferty quantile overestimates ln(1/eps_B) by about 3% at t = 1),
+Proposition 7's bracket, the older page's z ~ 6.58 and S* ~ 4,600 example, and
+the algebra of its Corollary 4.  scipy is an independent library check.
+"""
+import itertools
+import math
+from pathlib import Path
+
+import numpy as np
+import pytest
+from scipy import optimize, special, stats
+
+from oracle import hypergeom as HG
+from oracle import params as P
+
+GOLDEN = Path(__file__).parent / "golden" / "table3_fast_vs_exact.tsv"
+
+
+def table3_rows():
+    rows = []
+    for line in GOLDEN.read_text().splitlines():
+        if line.startswith("#") or line.startswith("log2N"):
+            continue
+        f = line.split("\t")
+        rows.append(dict(N=2 ** int(f[0]), k=2 ** int(f[1]), S=int(f[2]), t_star=int(f[3]), t=int(f[4]),
+                         M_star=int(f[5]), M=int(f[6]), pe=float(f[7]), pa=float(f[8])))
+    return rows
+
+
+ROWS = table3_rows()
+
+
+def test_golden_has_21_rows():
+    assert len(ROWS) == 21
+
+
+@pytest.mark.parametrize("r", ROWS, ids=lambda r: f"N2^{int(math.log2(r['N']))}-k2^{int(math.log2(r['k']))}")
+def test_table3_exact_and_fast(r):
+    t_star, M_star = P.params_exact(r["N"], r["k"], r["S"], 1e-3)
+    t, M = P.params_fast(r["N"], r["k"], r["S"], 1e-3)
+    assert (t_star, M_star) == (r["t_star"], r["M_star"])
+    assert (t, M) == (r["t"], r["M"])
+    # printed to three significant digits
+    assert P.prob_fail(r["N"], r["k"], r["S"], t_star, M_star) == pytest.approx(r["pe"], rel=1e-2, abs=0.006e-4)
+    assert P.prob_fail(r["N"], r["k"], r["S"], t, M) == pytest.approx(r["pa"], rel=1e-2, abs=0.006e-4)
+
+
+def test_acklam_within_stated_bound():
+    p = np.concatenate([np.logspace(-15, -1, 300), np.linspace(0.02, 0.98, 301), 1 - np.logspace(-15, -1, 300)])
+    for q in p:
+        ref = special.ndtri(q)
+        assert abs(P.norm_ppf(q) - ref) <= 1.15e-9 * abs(ref) + 1e-15
+
+
+def test_z_values():
+    assert P.norm_ppf(1 - 5e-4) == pytest.approx(3.2905267, abs=1e-6)
+    assert 2 * P.norm_ppf(1 - 5e-4) == pytest.approx(6.58, abs=0.005)  # older Algorithm 1, line 1
+
+
+def test_wilson_hilferty_at_t1_overestimates_by_about_3_percent():
+    z = P.norm_ppf(1 - 5e-4)
+    wh = (1 - 1 / 9 + z * math.sqrt(1 / 9)) ** 3
+    assert wh / math.log(1 / 5e-4) == pytest.approx(1.03, abs=0.005)
+
+
+def test_k1_gives_t1_and_no_recall_failure():
+    for N, S in [(2**20, 8192), (2**30, 32768)]:
+        assert P.threshold_rank_fast(N, 1, S, 1e-3) == 1
+        assert P.prob_recall_failure(N, 1, S, 1) == 0.0
+
+
+def test_sstar_example_of_the_older_page():
+    assert P.s_star_scaling(1e9, 100) == pytest.approx(4600, rel=0.01)
+
+
+def test_older_page_corollary4_algebra():
+    # M = c k with c = c0 + z_B sqrt((1-a) f / (a S)), c0 = 1 + z_A/sqrt(S) sqrt((1-a)/a f)  (Eq 8, 11)
+    for N, k, S in [(2**30, 1024, 105985), (2**20, 64, 32768), (50331648, 131072, 131072)]:
+        zA = zB = P.norm_ppf(1 - 5e-4)
+        a = k / N
+        f = 1 - S / N
+        c0 = 1 + zA / math.sqrt(S) * math.sqrt((1 - a) / a * f)
+        c = c0 + zB * math.sqrt((1 - a) * f / (a * S))
+        assert c * k == pytest.approx(P.m_cor4(N, k, S, zA + zB), rel=1e-12)
+
+
+def test_proposition7_bracket():
+    for N, k, r in [(2**24, 2**11, 0.5), (2**28, 2**17, 0.1), (2**31, 32, 2.0), (2**20, 2**14, 0.05)]:
+        S1, S2 = P.sample_size_prop7(N, k, 1e-3, r)
+        z = P.norm_ppf(1 - 5e-4)
+        kappa = z * z + 0.5
+        C = lambda S: r * S + 2 * z * math.sqrt(k * N / S) + kappa * N / S
+        res = optimize.minimize_scalar(C, bounds=(1.0, 1e9), method="bounded", options={"xatol": 1e-6})
+        lo = max(S1, S2)
+        assert lo * (1 - 1e-6) <= res.x <= 2 ** (2 / 3) * lo * (1 + 1e-6)
+
+
+def test_hypergeom_matches_enumeration():
+    N, K, S = 10, 4, 5
+    counts = np.zeros(S + 1)
+    for c in itertools.combinations(range(N), S):
+        counts[sum(1 for i in c if i < K)] += 1
+    pmf = counts / counts.sum()
+    assert np.allclose(HG.pmf_upto(N, K, S, S), pmf, atol=1e-15)
+    for j in range(-1, S + 1):
+        assert HG.cdf(N, K, S, j) == pytest.approx(pmf[: max(j + 1, 0)].sum(), abs=1e-15)
+    for p in (0.01, 0.3, 0.5, 0.9, 1.0):
+        assert HG.quantile(N, K, S, p) == min(j for j in range(S + 1) if pmf[: j + 1].sum() >= p - 1e-15)
+
+
+def mp_cdf(N, K, S, j):
+    """F(j) summed term by term in 40-digit arithmetic (log-gamma binomials)."""
+    mp = pytest.importorskip("mpmath")
+
+    mp.mp.dps = 40
+    lc = lambda a, b: mp.loggamma(a + 1) - mp.loggamma(b + 1) - mp.loggamma(a - b + 1)
+    lo = max(0, S - (N - K))
+    tot = mp.fsum(mp.exp(lc(K, i) + lc(N - K, S - i) - lc(N, S)) for i in range(lo, j + 1))
+    return float(tot)
+
+
+@pytest.mark.parametrize("N,K,S,j", [(2**20, 31, 8192, 3), (2**24, 2047, 20650, 9), (2**31, 996031, 16384, 0),
+                                     (2**28, 224429, 234231, 151), (1000, 990, 500, 495)])
+def test_hypergeom_matches_high_precision(N, K, S, j):
+    assert HG.cdf(N, K, S, j) == pytest.approx(mp_cdf(N, K, S, j), rel=1e-10, abs=1e-300)
+
+
+@pytest.mark.parametrize("N,K,S,j", [(2**20, 31, 8192, 3), (2**24, 2047, 20650, 9), (1000, 990, 500, 495)])
+def test_hypergeom_matches_scipy(N, K, S, j):
+    assert HG.cdf(N, K, S, j) == pytest.approx(stats.hypergeom.cdf(j, N, K, S), rel=1e-6)
+
+
+def test_older_rule_literal_and_its_budget():
+    # The older Algorithm 1 at N = 2^20, k = 64: alpha S = 2 < -ln(eps/2) = 7.6, so t = 1,
+    # which makes recall failure likely (the reading that keeps it off by default).
+    S, t, M = P.params_old(2**20, 64, 1e-3)
+    assert (S, t) == (32768, 1)
+    assert P.prob_recall_failure(2**20, 64, S, t) > 0.8
+    S2, t2, M2 = P.params(2**20, 64, 1e-3)
+    assert S2 == S and P.prob_fail(2**20, 64, S2, t2, M2) <= 1e-3
+
+
+def test_default_rule_invariants():
+    for N in (2**20, 2**22, 2**26, 2**30, 50331648, 2**32):
+        for k in (1, 2, 32, 1024, 4096, 2**19):
+            if k * 64 > N:
+                continue
+            S, t, M = P.params(N, k, 1e-3)
+            assert 32768 <= S <= 131072 and 1 <= t <= S and k <= M <= N
+            if P.uses_filter(N, k, S):
+                assert P.prob_fail(N, k, S, t, M) <= 1e-3
