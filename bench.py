@@ -1,0 +1,346 @@
+"""Benchmark of Prof-K exact top-k on GB300.
+
+One step = one exact top-k call (sample, threshold, filter, check, refine) on
+a 2^30-element float32 standard-normal vector with k = 1024, eps = 1e-3, the
+input already resident in HBM.  The input (4 GiB) is far larger than L2
+(129 MB), so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  Keys beyond the base contract:
+  roofline      filter kernel: algorithmic bytes 4n per launch / its mean
+                device time (CUDA events the library records on the launch
+                stream), against the measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle (full sort) on a bounded prefix of the input
+  e2e           the same metric through the C-ABI with host buffers: each step
+                copies x host->device from pinned memory, runs the call and
+                copies the k results back
+  sweep         the other k and distributions at 2^30 (fewer steps each)
+
+--impl reference times the CPU oracle itself (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+N_DEFAULT = 1 << 30
+K_DEFAULT = 1024
+EPS = 1e-3
+METRIC = "top-k Gelem/s and HBM GB/s vs peak, N=2^30 fp32, k∈{32,1024,2^19}"
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def filter_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("filter.cu", "common.cuh", "kernels.h"):
+        h.update((ROOT / "streaming_selection_primitive_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(n: int):
+    """DRAM bytes per filter launch from the committed ncu summary, scaled to n;
+    None when absent or when the filter source changed since the capture."""
+    p = ROOT / "profiles" / "filter_normal_2p28.md"
+    if not p.exists():
+        return None
+    text = p.read_text()
+    m_hash = re.search(r"filter_source_hash:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_element:\s*([0-9.]+)", text)
+    if not m_hash or not m_b or m_hash.group(1) != filter_source_hash():
+        return None
+    return float(m_b.group(1)) * n
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(x_host_prefix, k, budget_s=12.0):
+    """The oracle (full sort) on a bounded prefix of the same input."""
+    from oracle.topk import topk_sort
+
+    elems, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        topk_sort(x_host_prefix, k)
+        reps += 1
+        elems += x_host_prefix.size
+        if time.perf_counter() - t0 >= budget_s or reps >= 50:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": elems / dt / 1e9, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+            "sample": f"oracle.topk_sort (numpy lexsort, one thread) on the first {x_host_prefix.size} elements "
+                      f"of the same normal input, k={k}, {reps} calls in {dt:.1f} s"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    import workloads
+    from oracle.topk import topk_sort
+
+    n_sample = 1 << 22
+    x = workloads.normal(n_sample, 1, "cpu").numpy()
+    for _ in range(args.warmup):
+        topk_sort(x, args.k)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        topk_sort(x, args.k)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = n_sample * args.steps / tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "Gelem/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"normal_2^30_k{args.k}", "n": args.n, "k": args.k, "eps": EPS,
+                   "sample_elems": n_sample},
+        "cpu_baseline": {"value": value, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: oracle.topk_sort (full sort, one thread) on a {n_sample}-element "
+                                   f"prefix-sized sample of the normal workload, k={args.k}"},
+        "e2e": {"value": value, "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="profk", choices=["profk", "reference"])
+    ap.add_argument("--n", type=int, default=N_DEFAULT)
+    ap.add_argument("--k", type=int, default=K_DEFAULT)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+
+    import streaming_selection_primitive_gb300 as pk
+    import workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk.lib()
+    pk.reset_options()
+    n, k = args.n, args.k
+
+    x = workloads.normal(n, 1 + rank, dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    out = (torch.empty(k, dtype=torch.float32, device=dev), torch.empty(k, dtype=torch.int64, device=dev))
+    pk.set_option(pk.OPT_TIMING, 1)
+    for w in range(args.warmup):
+        pk.topk(x, k, EPS, 10_000 + w, out=out)
+    barrier()
+    filter_ms, attempts, launches, paths, Rs = [], [], 0, [], []
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(dev.index)
+    with ClockSampler(gpu_id) as clk:
+        barrier()
+        ev0.record(stream)
+        for s in range(args.steps):
+            _, _, st = pk.topk(x, k, EPS, 1000 + s, out=out)
+            filter_ms.append(st["filter_ms"])
+            attempts.append(st["attempts"])
+            launches += st["launches"]
+            paths.append(st["path"])
+            Rs.append(st["R_first"])
+        ev1.record(stream)
+        barrier()
+    total_ms = ev0.elapsed_time(ev1)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clocks = clk.summary()
+    ms_step = total_ms / args.steps
+    value = n * args.steps * ws / (total_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+    f_ms = statistics.mean(filter_ms)
+    achieved = 4.0 * n / (f_ms / 1e3) / 1e9
+    traffic = traffic_from_profile(n)
+    aux = pk.topk(x, k, EPS, 7, out=out)[2]["aux_bytes"]
+
+    # End to end through the C-ABI with host buffers.
+    pk.set_option(pk.OPT_TIMING, 0)
+    xh = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    xh.copy_(x)
+    xd = torch.empty_like(x)
+    vh = torch.empty(k, dtype=torch.float32, pin_memory=True)
+    ih = torch.empty(k, dtype=torch.int64, pin_memory=True)
+    for w in range(2):
+        xd.copy_(xh, non_blocking=True)
+        pk.topk(xd, k, EPS, 20_000 + w, out=out)
+        vh.copy_(out[0], non_blocking=True)
+        ih.copy_(out[1], non_blocking=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(args.e2e_steps):
+        xd.copy_(xh, non_blocking=True)
+        pk.topk(xd, k, EPS, 30_000 + s, out=out)
+        vh.copy_(out[0], non_blocking=True)
+        ih.copy_(out[1], non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_value = n * args.e2e_steps * ws / (e2e_ms / 1e3) / 1e9
+    del xh, xd
+
+    sweep = {}
+    if not args.no_sweep:
+        for gen in ("uniform", "normal", "pareto"):
+            xs = x if gen == "normal" else workloads.GENERATORS[gen](n, 1 + rank, dev)
+            for kk in (32, 1024, 1 << 19):
+                o2 = (torch.empty(kk, dtype=torch.float32, device=dev), torch.empty(kk, dtype=torch.int64, device=dev))
+                for w in range(2):
+                    pk.topk(xs, kk, EPS, 40_000 + w, out=o2)
+                torch.cuda.synchronize()
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 5
+                a0.record(stream)
+                for s in range(reps):
+                    _, _, st = pk.topk(xs, kk, EPS, 50_000 + s, out=o2)
+                a1.record(stream)
+                torch.cuda.synchronize()
+                ms = a0.elapsed_time(a1) / reps
+                sweep[f"{gen}_k{kk}"] = {"ms": round(ms, 4), "gelem_s": round(n / ms / 1e6, 2),
+                                         "hbm_frac_of_8TBs": round(4 * n / (ms / 1e3) / 8e12, 3)}
+            if gen != "normal":
+                del xs
+                torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and ws >= 1 and not args.no_cpu and args.gpus == 1:
+        cpu = cpu_baseline(x[: 1 << 24].cpu().numpy(), k)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "Gelem/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"normal_2^30_k{k}", "n": n, "k": k, "eps": EPS, "input": "float32 N(0,1)",
+                       "l2": "input 4 GiB > L2 129 MB: no flush between steps", "parallelism": f"replicas x{ws}"},
+            "hbm_gbs_end_to_end": round(4 * n / (ms_step / 1e3) / 1e9, 1),
+            "hbm_frac_of_8TBs": round(4 * n / (ms_step / 1e3) / 8e12, 4),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_kind,
+                         "kernel": "k_filter", "bytes_per_launch": 4 * n, "mean_launch_ms": round(f_ms, 4)},
+            "e2e": {"value": round(e2e_value, 3), "unit": "Gelem/s", "h2d_bytes_per_step": 4 * n,
+                    "d2h_bytes_per_step": 12 * k, "ms_per_step": round(e2e_ms / args.e2e_steps, 3)},
+            "gpu_launches": launches,
+            "retries": int(sum(a - 1 for a in attempts if a > 0)),
+            "aux_bytes": aux,
+            "R_first_mean": round(float(np.mean(Rs)), 1),
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

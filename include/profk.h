@@ -1,0 +1,202 @@
+/*
+ * profk.h -- Prof-K exact top-k selection for NVIDIA GB300 (sm_103a).
+ *
+ * Prof-K ("Prof-K: Probabilistic One-Pass Filtering for Efficient Top-k
+ * Selection") returns the k largest entries of a vector with their indices.
+ * It draws a uniform sample of S indices without replacement, takes the t-th
+ * largest sampled value as a threshold tau, streams the input once keeping
+ * every x_i >= tau in a buffer of capacity M while counting them exactly (R),
+ * and selects the exact top-k from the buffer.  When the run-time check
+ * k <= R <= M fails it redraws, and after a fixed number of attempts it runs
+ * an exact selection over the whole input, so the result is always exact
+ * (paper, Section 3 "The Prof-K Algorithm" and Section 4 "Failure Modes").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Order.  Values descending under IEEE-754 comparison (-0.0 == +0.0, +-inf
+ *   are ordinary values); equal values by ascending index.  The pages assume
+ *   distinct values (Section 4 "Notation and Conventions"); this tie rule is
+ *   the library's reading.  Returned values keep their original bits.
+ * NaN.  An input containing NaN is rejected with PROFK_ERR_NAN; the output
+ *   buffers are then unspecified.
+ * Pointers.  x, out_vals, out_idx and every array documented as "device" are
+ *   device pointers owned by the caller; x is only read.  stats is a host
+ *   pointer and may be NULL.
+ * Indices.  int64, relative to the row (0 .. n-1).  n must be <= 2^32.
+ * Streams.  All device work is ordered on `stream` (0 = legacy default).
+ *   profk_topk / profk_topk_batched synchronize `stream` once per filter
+ *   attempt to read the exact count R (the pages' run-time check); outputs
+ *   are complete once `stream` is synchronized after the call returns, and
+ *   *stats is complete when the call returns.
+ * Workspace.  The library allocates its workspace stream-ordered from a
+ *   memory pool it owns (cudaMallocAsync) and returns it before the call
+ *   returns; its size is O(M + S) per row, never O(n) (stats->aux_bytes).
+ * Errors.  Every entry point returns PROFK_OK (0) or a negative
+ *   profk_status; no exception crosses the ABI and there is no CPU fallback.
+ * Threads.  Calls from several host threads are safe; profk_set_option
+ *   changes process-wide settings and should not race with running calls.
+ */
+#ifndef PROFK_H_
+#define PROFK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum profk_status {
+  PROFK_OK = 0,
+  PROFK_ERR_INVALID = -1,        /* an argument is out of range or NULL */
+  PROFK_ERR_CUDA = -2,           /* a CUDA call failed; stats->cuda_error has the code */
+  PROFK_ERR_NAN = -3,            /* the input holds a NaN */
+  PROFK_ERR_UNSUPPORTED = -4,    /* e.g. n > 2^32 or a misaligned input */
+  PROFK_ERR_DEVICE_TIMEOUT = -5  /* a bounded device-side wait gave up */
+} profk_status;
+
+/* How a row's result was produced. */
+typedef enum profk_path {
+  PROFK_PATH_FILTER = 0,    /* sample -> threshold -> filter -> refine (k <= R <= M) */
+  PROFK_PATH_TIE = 1,       /* R > M but R_gt < k: tau is the k-th largest value; the
+                               library emits x > tau plus the lowest-index copies of tau */
+  PROFK_PATH_FALLBACK = 2,  /* every attempt failed: exact selection over the row */
+  PROFK_PATH_EXACT = 3      /* no sampling (S > n/8 or k > n/64): exact selection */
+} profk_path;
+
+/* Per-row report.  Counts of attempts that did not run are -1. */
+typedef struct profk_stats {
+  int64_t S, t, M;           /* sample size, threshold rank, buffer capacity */
+  int64_t R_first;           /* |{x >= tau}| of the first attempt */
+  int64_t R_gt_first;        /* |{x >  tau}| of the first attempt */
+  int64_t R_final;           /* the same counts for the last attempt */
+  int64_t R_gt_final;
+  float tau_first;           /* threshold of the first attempt */
+  float tau_final;
+  int32_t attempts;          /* filter passes run for this row (0 on the exact path) */
+  int32_t path;              /* a profk_path */
+  int32_t draw_doublings;    /* times the draw budget had to grow (see profk_sample) */
+  int32_t cuda_error;        /* cudaError_t of the failing call, else 0 */
+  uint64_t aux_bytes;        /* device workspace of the whole call, bytes */
+  float filter_ms;           /* device time of the first filter pass over all rows when
+                                PROFK_OPT_TIMING is on, else -1 */
+  int32_t launches;          /* kernels the whole call launched (all rows) */
+} profk_stats;
+
+/* ---- the method -------------------------------------------------------- */
+
+/* Exact top-k of one row x[0..n) (problem statement: paper Section 3).
+ *   x         device, n floats, 16-byte aligned for the vectorised filter
+ *             (other alignments return PROFK_ERR_UNSUPPORTED)
+ *   n         1 <= n <= 2^32
+ *   k         1 <= k <= n
+ *   eps       failure budget of one attempt, 0 < eps < 1, split eps/2 + eps/2
+ *             between recall failure and overflow (Theorem 4's default split)
+ *   seed      seeds every sample; the same (x, k, eps, seed) reproduces the
+ *             same samples, counts and stats
+ *   out_vals  device, k floats, sorted in the library order
+ *   out_idx   device, k int64 indices into x
+ */
+int profk_topk(const float* x, int64_t n, int64_t k, double eps, uint64_t seed,
+               float* out_vals, int64_t* out_idx, cudaStream_t stream,
+               profk_stats* stats);
+
+/* Exact top-k of each of `rows` rows; row r is x[r*ld .. r*ld + n).  The
+ * paper applies the procedure to each batch element (Section 3) with a
+ * per-row threshold, buffer and counter (Appendix C "The Filter Kernel").
+ * Each row gets the budget eps / rows, so one attempt of the whole call fails
+ * with probability <= eps (union bound, Appendix E.2).  Rows that fail the
+ * check are redrawn alone.
+ *   ld        row stride in elements, ld >= n, ld % 4 == 0
+ *   out_vals  device, rows*k floats, row-major (row r at r*k)
+ *   out_idx   device, rows*k int64, row-relative indices
+ *   stats     host array of `rows` entries, or NULL
+ */
+int profk_topk_batched(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
+                       double eps, uint64_t seed, float* out_vals, int64_t* out_idx,
+                       cudaStream_t stream, profk_stats* stats);
+
+/* Parameters (S, t, M) for one row of length n at budget eps.
+ *   mode PROFK_PARAMS_DEFAULT: S from the older version's Theorem 5,
+ *     S* = (z log2(k) / 2)^(2/3) (k(n-k))^(1/3) with z = 2 Phi^{-1}(1-eps/2),
+ *     rounded and clamped to [32768, 131072] (its Algorithm 1, lines 1-4);
+ *     t and M from the corrected Algorithm 1 (Eq 10 or 11, then Eq 12) with
+ *     z = Phi^{-1}(1-eps/2); then 1 <= t <= S and k <= M <= n.
+ *   mode PROFK_PARAMS_OLD: the older Algorithm 1 literally (Eq 6 t,
+ *     Corollary 4 M, and t = 1 when (k/n) S < -ln(eps/2)).
+ * Pure host arithmetic (fp64), no device work. */
+#define PROFK_PARAMS_DEFAULT 0
+#define PROFK_PARAMS_OLD 1
+int profk_params(int64_t n, int64_t k, double eps, int mode,
+                 int64_t* S, int64_t* t, int64_t* M);
+
+/* Device bytes one call of profk_topk_batched(rows, n, k, eps) allocates at
+ * most (profk_topk is rows = 1).  0 on invalid arguments. */
+size_t profk_workspace_size(int64_t rows, int64_t n, int64_t k, double eps);
+
+/* Process-wide options (defaults in brackets). */
+typedef enum profk_option {
+  PROFK_OPT_PARAM_MODE = 0,    /* PROFK_PARAMS_DEFAULT [0] or PROFK_PARAMS_OLD */
+  PROFK_OPT_MAX_ATTEMPTS = 1,  /* filter attempts before the exact fallback [6]; 0 = fallback at once */
+  PROFK_OPT_TIE_EXIT = 2,      /* take PROFK_PATH_TIE when R > M and R_gt < k [1] */
+  PROFK_OPT_FORCE_S = 3,       /* >0 overrides S (and disables the exact-path routing) [0] */
+  PROFK_OPT_FORCE_T = 4,       /* >0 overrides t [0] */
+  PROFK_OPT_FORCE_M = 5,       /* >0 overrides M [0] */
+  PROFK_OPT_TIMING = 6,        /* record stats.filter_ms with CUDA events [0] */
+  PROFK_OPT_FILTER_CTAS_PER_SM = 7, /* persistent filter grid = SMs x this; 0 = auto [0] */
+  PROFK_OPT__COUNT = 8
+} profk_option;
+int profk_set_option(int option, int64_t value);
+int64_t profk_get_option(int option);
+
+/* Static description of a status code. */
+const char* profk_strerror(int code);
+
+/* ---- the individual steps (for testing and composition) ---------------- */
+
+/* Step 1, sampling (paper Section 3, stage 1).  The sample is the first S
+ * distinct values of the draw stream u_0, u_1, ... in order of first
+ * appearance, where draw i is
+ *   w = Philox4x64-10(counter = (i / 4, attempt, j, 0), key = (seed, row))[i % 4]
+ * accepted by Lemire's method for the range n (128-bit product m = w * n,
+ * reject while (m mod 2^64) < (2^64 - n) mod n, retrying with j = 1, 2, ...),
+ * u_i = m >> 64.  Writes out_sidx[0..S) (device int64) and
+ * out_vals[0..S) = x[out_sidx] (device float).  Requires 1 <= S <= n/2. */
+int profk_sample(const float* x, int64_t n, int64_t S, uint64_t seed, int64_t row,
+                 int32_t attempt, int64_t* out_sidx, float* out_vals, cudaStream_t stream);
+
+/* Step 2, threshold (Section 3, stage 2): *out_tau (device float) = the t-th
+ * largest of vals[0..S) (device), 1 <= t <= S.  A zero is returned as +0.0. */
+int profk_threshold(const float* vals, int64_t S, int64_t t, float* out_tau,
+                    cudaStream_t stream);
+
+/* Step 3, filter (Section 3, stage 3; Appendix C): one pass over x[0..n)
+ * (device, 16-byte aligned) counting out_counts[0] = R = |{x_i >= tau}|,
+ * out_counts[1] = |{x_i > tau}|, out_counts[2] = |{x_i is NaN}| (device
+ * uint64[3]), and storing min(R, M) passers into out_keys[0..M) (device) in
+ * an unspecified order.  A passer (v, i) is stored as the 64-bit key
+ *   (ord(v) << 32) | (0xFFFFFFFF - i),
+ * ord(v) = bits(v) ^ 0x80000000 for v >= +0.0 (with -0.0 read as +0.0) and
+ * ~bits(v) for v < 0, so that keys compare like the library order. */
+int profk_filter(const float* x, int64_t n, float tau, int64_t M, uint64_t* out_keys,
+                 uint64_t* out_counts, cudaStream_t stream);
+
+/* Step 4, refinement (Section 3, stage 4): exact top-k of the R keys
+ * keys[0..R) (device, the profk_filter encoding, distinct), 1 <= k <= R;
+ * values are read back from x[0..n) (device) at the decoded indices.  A key
+ * whose index is >= n yields the output entry (NaN, -1) instead of a read. */
+int profk_refine(const uint64_t* keys, int64_t R, int64_t k, const float* x, int64_t n,
+                 float* out_vals, int64_t* out_idx, cudaStream_t stream);
+
+/* Exact top-k over the whole row without sampling (the fallback of Section 3,
+ * stage 4): multi-pass radix selection of the k-th largest key, compaction
+ * and sort.  Returns PROFK_ERR_NAN if x holds a NaN (synchronizes stream). */
+int profk_exact(const float* x, int64_t n, int64_t k, float* out_vals, int64_t* out_idx,
+                cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PROFK_H_ */

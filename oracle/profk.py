@@ -96,7 +96,9 @@ def tie_path(x: np.ndarray, tau, k: int):
 
 def profk(x: np.ndarray, k: int, eps: float, seed: int, row: int = 0, *, max_attempts: int = 6,
           mode: int = P.MODE_DEFAULT, tie_exit: bool = True, force=None):
-    """One row of Prof-K.  ``force`` may override (S, t, M) as a dict."""
+    """One row of Prof-K.  ``force`` may override (S, t, M) as a dict; a forced
+    S recomputes t and M from it (Algorithm 1 lines 5-15) unless those are
+    forced as well.  Any override routes through sampling."""
     x = np.asarray(x, dtype=np.float32)
     if np.isnan(x).any():
         raise ValueError("NaN in input")
@@ -104,7 +106,10 @@ def profk(x: np.ndarray, k: int, eps: float, seed: int, row: int = 0, *, max_att
     st = Stats()
     S, t, M = P.params(N, k, eps, mode)
     if force:
-        S, t, M = force.get("S", S), force.get("t", t), force.get("M", M)
+        if "S" in force:  # a forced S gets the fast t and M of that S unless they are forced too
+            S = force["S"]
+            t, M = P.params_fast(N, k, S, eps)
+        t, M = force.get("t", t), force.get("M", M)
     st.S, st.t, st.M = S, t, M
     if not P.uses_filter(N, k, S) and not force:
         st.path = PATH_EXACT

@@ -1,0 +1,158 @@
+"""Prof-K exact top-k selection on GB300: Python binding of libprofk.so.
+
+Every step runs in the library's CUDA kernels; this module only marshals
+arguments.  PyTorch supplies device memory and the current CUDA stream.  There
+is no CPU fallback: a missing library or a non-CUDA tensor raises.
+
+    import streaming_selection_primitive_gb300 as pk
+    vals, idx, stats = pk.topk(x, k=1024, eps=1e-3, seed=0)   # x: 1-D float32 CUDA tensor
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+from . import _abi
+from ._abi import (OPT_FILTER_CTAS_PER_SM, OPT_FORCE_M, OPT_FORCE_S, OPT_FORCE_T, OPT_MAX_ATTEMPTS,
+                   OPT_PARAM_MODE, OPT_TIE_EXIT, OPT_TIMING, PARAMS_DEFAULT, PARAMS_OLD, PATH_EXACT,
+                   PATH_FALLBACK, PATH_FILTER, PATH_TIE, ProfkError, ProfkStats)
+
+__all__ = ["topk", "topk_batched", "params", "workspace_size", "set_option", "get_option", "reset_options",
+           "sample", "threshold", "filter_pass", "refine", "exact", "ProfkError", "ProfkStats", "lib"]
+
+
+def lib():
+    return _abi.lib()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream=None) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _need_cuda_f32(x, name="x"):
+    torch = _torch()
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float32:
+        raise TypeError(f"{name} must be a float32 CUDA tensor")
+
+
+def params(n: int, k: int, eps: float = 1e-3, mode: int = PARAMS_DEFAULT):
+    """(S, t, M) as the library computes them (host arithmetic, no GPU needed)."""
+    S, t, M = C.c_int64(), C.c_int64(), C.c_int64()
+    _abi.check(lib().profk_params(int(n), int(k), float(eps), int(mode), C.byref(S), C.byref(t), C.byref(M)))
+    return S.value, t.value, M.value
+
+
+def workspace_size(rows: int, n: int, k: int, eps: float = 1e-3) -> int:
+    return int(lib().profk_workspace_size(int(rows), int(n), int(k), float(eps)))
+
+
+def set_option(option: int, value: int) -> None:
+    _abi.check(lib().profk_set_option(int(option), int(value)))
+
+
+def get_option(option: int) -> int:
+    return int(lib().profk_get_option(int(option)))
+
+
+def reset_options() -> None:
+    for o, v in _abi.OPT_DEFAULTS.items():
+        set_option(o, v)
+
+
+def topk(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=None):
+    """Exact top-k of a 1-D float32 CUDA tensor: (values, int64 indices, stats dict)."""
+    torch = _torch()
+    _need_cuda_f32(x)
+    if x.dim() != 1 or not x.is_contiguous():
+        raise ValueError("x must be 1-D and contiguous")
+    n = x.numel()
+    if out is None:
+        vals = torch.empty(k, dtype=torch.float32, device=x.device)
+        idx = torch.empty(k, dtype=torch.int64, device=x.device)
+    else:
+        vals, idx = out
+    st = ProfkStats()
+    code = lib().profk_topk(x.data_ptr(), n, int(k), float(eps), int(seed) & (2**64 - 1), vals.data_ptr(),
+                            idx.data_ptr(), _stream_handle(stream), C.byref(st))
+    _abi.check(code)
+    return vals, idx, st.as_dict()
+
+
+def topk_batched(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=None):
+    """Exact top-k of each row of a 2-D float32 CUDA tensor (row stride x.stride(0))."""
+    torch = _torch()
+    _need_cuda_f32(x)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    rows, n = x.shape
+    if out is None:
+        vals = torch.empty((rows, k), dtype=torch.float32, device=x.device)
+        idx = torch.empty((rows, k), dtype=torch.int64, device=x.device)
+    else:
+        vals, idx = out
+    sts = (ProfkStats * rows)()
+    code = lib().profk_topk_batched(x.data_ptr(), rows, n, x.stride(0), int(k), float(eps),
+                                    int(seed) & (2**64 - 1), vals.data_ptr(), idx.data_ptr(),
+                                    _stream_handle(stream), sts)
+    _abi.check(code)
+    return vals, idx, [s.as_dict() for s in sts]
+
+
+def sample(x, S: int, seed: int, row: int = 0, attempt: int = 0, stream=None):
+    """Step 1 alone: the sample's indices (int64, draw order) and values."""
+    torch = _torch()
+    _need_cuda_f32(x)
+    sidx = torch.empty(S, dtype=torch.int64, device=x.device)
+    svals = torch.empty(S, dtype=torch.float32, device=x.device)
+    _abi.check(lib().profk_sample(x.data_ptr(), x.numel(), int(S), int(seed) & (2**64 - 1), int(row),
+                                  int(attempt), sidx.data_ptr(), svals.data_ptr(), _stream_handle(stream)))
+    return sidx, svals
+
+
+def threshold(vals, t: int, stream=None):
+    """Step 2 alone: the t-th largest of a float32 CUDA tensor, as a 1-element tensor."""
+    torch = _torch()
+    _need_cuda_f32(vals, "vals")
+    out = torch.empty(1, dtype=torch.float32, device=vals.device)
+    _abi.check(lib().profk_threshold(vals.data_ptr(), vals.numel(), int(t), out.data_ptr(),
+                                     _stream_handle(stream)))
+    return out
+
+
+def filter_pass(x, tau: float, M: int, stream=None):
+    """Step 3 alone: (candidate keys[M] as int64 bit patterns, counts[3] = R, R_gt, NaNs)."""
+    torch = _torch()
+    _need_cuda_f32(x)
+    keys = torch.zeros(max(int(M), 1), dtype=torch.int64, device=x.device)
+    counts = torch.zeros(3, dtype=torch.int64, device=x.device)
+    _abi.check(lib().profk_filter(x.data_ptr(), x.numel(), float(tau), int(M), keys.data_ptr(),
+                                  counts.data_ptr(), _stream_handle(stream)))
+    return keys[: int(M)], counts
+
+
+def refine(keys, k: int, x, stream=None):
+    """Step 4 alone: exact top-k of candidate keys (profk_filter encoding)."""
+    torch = _torch()
+    _need_cuda_f32(x)
+    vals = torch.empty(k, dtype=torch.float32, device=x.device)
+    idx = torch.empty(k, dtype=torch.int64, device=x.device)
+    _abi.check(lib().profk_refine(keys.data_ptr(), keys.numel(), int(k), x.data_ptr(), x.numel(),
+                                  vals.data_ptr(), idx.data_ptr(), _stream_handle(stream)))
+    return vals, idx
+
+
+def exact(x, k: int, stream=None):
+    """Exact top-k without sampling (the fallback)."""
+    torch = _torch()
+    _need_cuda_f32(x)
+    vals = torch.empty(k, dtype=torch.float32, device=x.device)
+    idx = torch.empty(k, dtype=torch.int64, device=x.device)
+    _abi.check(lib().profk_exact(x.data_ptr(), x.numel(), int(k), vals.data_ptr(), idx.data_ptr(),
+                                 _stream_handle(stream)))
+    return vals, idx

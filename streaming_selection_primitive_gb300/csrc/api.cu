@@ -1,0 +1,752 @@
+// C-ABI of the Prof-K library and the host control of the method
+// ("Prof-K: Probabilistic One-Pass Filtering for Efficient Top-k Selection",
+// Section 3 "The Prof-K Algorithm": sample -> threshold -> filter -> check ->
+// refine, redraw on failure, exact fallback after a fixed number of attempts).
+//
+// The host does what the pages' host does: it computes (S, t, M) once per
+// configuration (memoized, Section 4 "Fast Approximate Parameter
+// Computation"), launches the steps on the caller's stream, and reads the
+// exact counts back after the filter (the run-time check, Appendix D "Cost of
+// the Run-Time Check").  All arithmetic on the data happens in the kernels.
+#include <algorithm>
+#include <atomic>
+#include <cstddef>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "../../include/profk.h"
+#include "kernels.h"
+#include "params.h"
+
+namespace profk {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Options.
+std::atomic<int64_t> g_opt[PROFK_OPT__COUNT] = {
+    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}};
+
+// ---------------------------------------------------------------------------
+// Memoized parameters per (n, k, eps, mode).
+Params cached_params(int64_t n, int64_t k, double eps, int mode) {
+  static std::mutex mu;
+  static std::map<std::tuple<int64_t, int64_t, double, int>, Params> cache;
+  const auto key = std::make_tuple(n, k, eps, mode);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const Params p = compute_params(n, k, eps, mode);
+  std::lock_guard<std::mutex> g(mu);
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = p;
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// Device memory: one stream-ordered pool per device, owned by the library.
+cudaError_t pool_for_current_device(cudaMemPool_t* out) {
+  static std::mutex mu;
+  static std::map<int, cudaMemPool_t> pools;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> g(mu);
+  auto it = pools.find(dev);
+  if (it != pools.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  cudaMemPoolProps props;
+  std::memset(&props, 0, sizeof(props));
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = dev;
+  cudaMemPool_t pool;
+  e = cudaMemPoolCreate(&pool, &props);
+  if (e != cudaSuccess) return e;
+  uint64_t keep = ~0ull;
+  cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  pools[dev] = pool;
+  *out = pool;
+  return cudaSuccess;
+}
+
+// Small pinned host scratch per host thread (row lists and count read-back).
+struct Pinned {
+  void* p = nullptr;
+  size_t cap = 0;
+};
+thread_local Pinned t_pinned;
+
+cudaError_t pinned(size_t bytes, void** out) {
+  if (t_pinned.cap < bytes) {
+    if (t_pinned.p) cudaFreeHost(t_pinned.p);
+    t_pinned.p = nullptr;
+    t_pinned.cap = 0;
+    const size_t cap = std::max<size_t>(bytes, 1 << 16);
+    cudaError_t e = cudaHostAlloc(&t_pinned.p, cap, cudaHostAllocDefault);
+    if (e != cudaSuccess) return e;
+    t_pinned.cap = cap;
+  }
+  *out = t_pinned.p;
+  return cudaSuccess;
+}
+
+struct Events {
+  cudaEvent_t a = nullptr, b = nullptr;
+};
+thread_local Events t_events;
+
+// ---------------------------------------------------------------------------
+// Small kernels of the control flow.
+__global__ void k_attempt_init(RowState* st, const int* rows) {
+  const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
+  RowState& S = st[row];
+  S.R_ge = 0;
+  S.R_gt = 0;
+  S.nan = 0;
+  S.distinct = 0;
+  S.error = 0;
+}
+
+// Hash tables of the listed rows back to "empty".
+__global__ void k_reset_tables(unsigned long long* table, int log2H, const int* rows) {
+  const int row = launch_row(rows);
+  unsigned long long* t = table + (static_cast<int64_t>(row) << log2H);
+  const int64_t H = 1ll << log2H;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < H;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    t[i] = ~0ull;
+}
+
+__global__ void k_set_tau(RowState* st, float tau) {
+  st->tau_key = ord_key(tau);
+  st->R_ge = 0;
+  st->R_gt = 0;
+  st->nan = 0;
+}
+
+__global__ void k_set_count(RowState* st, unsigned long long R) { st->R_ge = R; }
+
+__global__ void k_vals_to_keys(const float* v, int64_t S, uint32_t* keys) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < S;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    keys[i] = ord_key(v[i]);
+}
+
+__global__ void k_tau_out(const RowState* st, float* out) { *out = key_to_float(st->tau_key); }
+
+__global__ void k_sample_out(const uint32_t* sidx, int64_t S, const float* x, int64_t* out_sidx, float* out_vals) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < S;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint32_t u = sidx[i];
+    out_sidx[i] = static_cast<int64_t>(u);
+    out_vals[i] = x[u];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Workspace layout.
+size_t align_up(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  int64_t rows = 0, n = 0, k = 0, S = 0, D = 0, M = 0, nbD = 0, kstride = 0;
+  int log2H = 0;
+  bool sampling = false;
+  size_t off_state = 0, off_lists = 0, off_table = 0, off_draws = 0, off_blockcnt = 0, off_sidx = 0, off_skeys = 0,
+         off_buf = 0, off_sel = 0, total = 0;
+};
+
+int64_t draw_budget(int64_t n, int64_t S) {
+  // Expected repeats among the first ~S draws are about S^2 / (2n); ask for
+  // twice that plus 8 standard deviations and a margin, so that growing D
+  // is practically never needed (the result does not depend on D).
+  const double rep = static_cast<double>(S) * static_cast<double>(S) / (2.0 * static_cast<double>(n));
+  int64_t D = S + static_cast<int64_t>(2.0 * rep + 8.0 * std::sqrt(rep) + 256.0);
+  return (D + 3) & ~3ll;
+}
+
+Layout make_layout(int64_t rows, int64_t n, int64_t k, int64_t S, int64_t D, int64_t M, bool sampling) {
+  Layout L;
+  L.rows = rows;
+  L.n = n;
+  L.k = k;
+  L.S = S;
+  L.D = D;
+  L.M = M;
+  L.sampling = sampling;
+  L.kstride = sort_stride(k);
+  size_t off = 0;
+  L.off_state = off;
+  off = align_up(off + sizeof(RowState) * rows);
+  L.off_lists = off;
+  off = align_up(off + sizeof(int) * rows * 4);
+  if (sampling) {
+    L.log2H = 1;
+    while ((1ll << L.log2H) < 2 * D) ++L.log2H;
+    L.nbD = (D + 1023) / 1024;
+    L.off_table = off;
+    off = align_up(off + sizeof(unsigned long long) * (static_cast<size_t>(rows) << L.log2H));
+    L.off_draws = off;
+    off = align_up(off + sizeof(uint32_t) * rows * D);
+    L.off_blockcnt = off;
+    off = align_up(off + sizeof(uint32_t) * rows * L.nbD);
+    L.off_sidx = off;
+    off = align_up(off + sizeof(uint32_t) * rows * S);
+    L.off_skeys = off;
+    off = align_up(off + sizeof(uint32_t) * rows * S);
+    L.off_buf = off;
+    off = align_up(off + sizeof(unsigned long long) * rows * M);
+  }
+  L.off_sel = off;
+  off = align_up(off + sizeof(unsigned long long) * rows * L.kstride);
+  L.total = off;
+  return L;
+}
+
+template <class T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+// Per-row counters read back after each filter pass (the head of RowState).
+constexpr size_t REPORT_BYTES = offsetof(RowState, hist);
+
+struct Call {
+  cudaStream_t stream;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  cudaError_t err = cudaSuccess;
+  int status = PROFK_OK;
+};
+
+#define PK_CHECK(expr)                      \
+  do {                                      \
+    cudaError_t e_ = (expr);                \
+    if (e_ != cudaSuccess) {                \
+      c.err = e_;                           \
+      c.status = PROFK_ERR_CUDA;            \
+      goto done;                            \
+    }                                       \
+  } while (0)
+
+cudaError_t ws_alloc(Call& c, size_t bytes) {
+  cudaMemPool_t pool;
+  cudaError_t e = pool_for_current_device(&pool);
+  if (e != cudaSuccess) return e;
+  e = cudaMallocFromPoolAsync(&c.ws, bytes, pool, c.stream);
+  if (e == cudaSuccess) c.ws_bytes = bytes;
+  return e;
+}
+
+void ws_free(Call& c) {
+  if (c.ws) cudaFreeAsync(c.ws, c.stream);
+  c.ws = nullptr;
+}
+
+// Copies a row list into list slot `slot` of the workspace (through the
+// pinned scratch at `hbuf`); *dev_out is nullptr for the list 0..rows-1.
+cudaError_t upload_rows(const Layout& L, void* ws, void* hbuf, int slot, const std::vector<int>& rows,
+                        cudaStream_t stream, int** dev_out) {
+  bool identity = static_cast<int64_t>(rows.size()) == L.rows;
+  for (size_t i = 0; identity && i < rows.size(); ++i) identity = rows[i] == static_cast<int>(i);
+  *dev_out = nullptr;
+  if (identity) return cudaSuccess;
+  int* hs = static_cast<int*>(hbuf) + slot * L.rows;
+  std::copy(rows.begin(), rows.end(), hs);
+  int* d = at<int>(ws, L.off_lists) + slot * L.rows;
+  *dev_out = d;
+  return cudaMemcpyAsync(d, hs, sizeof(int) * rows.size(), cudaMemcpyHostToDevice, stream);
+}
+
+// Exact selection over whole rows (fallback / exact path).
+void launch_exact(const Layout& L, void* ws, const float* x, int64_t ld, int nrows, const int* rows,
+                  float* out_vals, int64_t* out_idx, cudaStream_t stream) {
+  RowState* st = at<RowState>(ws, L.off_state);
+  unsigned long long* sel = at<unsigned long long>(ws, L.off_sel);
+  SelectArgs a{KeySource::Input, x, ld, L.n, nrows, rows, st};
+  launch_select(a, static_cast<uint64_t>(L.k), false, 0, stream);
+  launch_compact(a, reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, stream);
+  launch_sort_emit(reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, nrows, rows, x, ld, L.n, out_vals, out_idx, stream);
+}
+
+// SM count and the filter's persistent grid, cached per device.
+struct DeviceInfo {
+  int sms = 0;
+  int filter_grid = 0;
+};
+DeviceInfo g_dev[64];
+std::mutex g_dev_mu;
+
+int filter_grid(int64_t ctas_per_sm) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.sms) {
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (d.sms <= 0) d.sms = 1;
+    d.filter_grid = filter_default_grid(d.sms);
+  }
+  return ctas_per_sm > 0 ? static_cast<int>(d.sms * ctas_per_sm) : d.filter_grid;
+}
+
+void fill_stats_params(profk_stats* s, const Params& P) {
+  std::memset(s, 0, sizeof(*s));
+  s->S = P.S;
+  s->t = P.t;
+  s->M = P.M;
+  s->R_first = s->R_gt_first = s->R_final = s->R_gt_final = -1;
+  s->filter_ms = -1.f;
+}
+
+
+int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,
+             float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_stats* stats) {
+  if (!x || !out_vals || !out_idx) return PROFK_ERR_INVALID;
+  if (rows < 1 || n < 1 || k < 1 || k > n || ld < n || !(eps > 0.0 && eps < 1.0)) return PROFK_ERR_INVALID;
+  if (rows > (1 << 20)) return PROFK_ERR_INVALID;
+  if (n > (1ll << 32)) return PROFK_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) != 0 || (rows > 1 && (ld & 3) != 0)) return PROFK_ERR_UNSUPPORTED;
+
+  const int mode = static_cast<int>(g_opt[PROFK_OPT_PARAM_MODE].load());
+  const int max_attempts = static_cast<int>(std::max<int64_t>(0, g_opt[PROFK_OPT_MAX_ATTEMPTS].load()));
+  const bool tie_exit = g_opt[PROFK_OPT_TIE_EXIT].load() != 0;
+  const int64_t fS = g_opt[PROFK_OPT_FORCE_S].load(), ft = g_opt[PROFK_OPT_FORCE_T].load(),
+                fM = g_opt[PROFK_OPT_FORCE_M].load();
+  const bool timing = g_opt[PROFK_OPT_TIMING].load() != 0;
+  const int64_t cps = g_opt[PROFK_OPT_FILTER_CTAS_PER_SM].load();
+
+  const double eps_row = eps / static_cast<double>(rows);
+  Params P = cached_params(n, k, eps_row, mode);
+  const bool forced = fS > 0 || ft > 0 || fM > 0;
+  if (fS > 0) {
+    P.S = std::min<int64_t>(fS, std::max<int64_t>(1, n / 2));
+    P.t = std::min<int64_t>(std::max<int64_t>(threshold_rank_fast(n, k, P.S, eps_row), 1), P.S);
+    P.M = std::min<int64_t>(std::max<int64_t>(buffer_capacity_fast(n, P.S, P.t, eps_row), k), n);
+  }
+  if (ft > 0) P.t = std::min<int64_t>(ft, P.S);
+  if (fM > 0) P.M = std::min<int64_t>(std::max<int64_t>(fM, k), n);
+  if (forced && 2 * P.S > n) return PROFK_ERR_INVALID;
+
+  const bool sampling = forced ? true : uses_filter(n, k, P.S);
+  std::vector<profk_stats> st_host(static_cast<size_t>(rows));
+  for (auto& s : st_host) fill_stats_params(&s, P);
+
+  Call c;
+  c.stream = stream;
+  const int64_t launches0 = launch_count();
+  int64_t D = sampling ? draw_budget(n, P.S) : 0;
+  Layout L = make_layout(rows, n, k, P.S, D, P.M, sampling);
+  std::vector<int> pending, fallback, attempt(static_cast<size_t>(rows), 0);
+  bool exact_ran = false, first_filter = true;
+  float filter_ms = -1.f;
+  void* hbuf = nullptr;
+  RowState* st = nullptr;
+
+  PK_CHECK(ws_alloc(c, L.total));
+  st = at<RowState>(c.ws, L.off_state);
+  PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState) * rows, stream));
+  PK_CHECK(pinned(sizeof(int) * rows * 4 + REPORT_BYTES * rows, &hbuf));
+
+  if (!sampling) {
+    for (int64_t r = 0; r < rows; ++r) st_host[r].path = PROFK_PATH_EXACT;
+    launch_exact(L, c.ws, x, ld, static_cast<int>(rows), nullptr, out_vals, out_idx, stream);
+    PK_CHECK(cudaGetLastError());
+    exact_ran = true;
+  } else {
+    for (int64_t r = 0; r < rows; ++r) pending.push_back(static_cast<int>(r));
+  }
+
+  while (!pending.empty()) {
+    // Rows advance in groups that share an attempt number (the draw stream of
+    // an attempt is keyed by it).
+    int a = attempt[pending[0]];
+    for (int r : pending) a = std::min(a, attempt[r]);
+    std::vector<int> group, next;
+    for (int r : pending) (attempt[r] == a ? group : next).push_back(r);
+    if (a >= max_attempts) {
+      for (int r : group) fallback.push_back(r);
+      pending = next;
+      continue;
+    }
+    const int ng = static_cast<int>(group.size());
+    int* gl = nullptr;
+    PK_CHECK(upload_rows(L, c.ws, hbuf, 0, group, stream, &gl));
+    {
+      const int64_t H = 1ll << L.log2H;
+      const unsigned rb = static_cast<unsigned>(std::min<int64_t>((H + 1023) / 1024, 256));
+      ++launch_count();
+      k_reset_tables<<<dim3(rb, ng), 1024, 0, stream>>>(at<unsigned long long>(c.ws, L.off_table), L.log2H, gl);
+      ++launch_count();
+      k_attempt_init<<<ng, 1, 0, stream>>>(st, gl);
+      SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, a, ng, gl, st,
+                    at<unsigned long long>(c.ws, L.off_table), at<uint32_t>(c.ws, L.off_draws),
+                    at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
+                    at<uint32_t>(c.ws, L.off_skeys)};
+      launch_sample(sa, stream);
+      SelectArgs ta{KeySource::SampleKeys, at<uint32_t>(c.ws, L.off_skeys), P.S, P.S, ng, gl, st};
+      launch_select(ta, static_cast<uint64_t>(P.t), true, 0, stream);
+      launch_store_tau(ng, gl, st, stream);
+      const bool time_it = timing && first_filter;
+      if (time_it) {
+        if (!t_events.a) {
+          PK_CHECK(cudaEventCreate(&t_events.a));
+          PK_CHECK(cudaEventCreate(&t_events.b));
+        }
+        PK_CHECK(cudaEventRecord(t_events.a, stream));
+      }
+      FilterArgs fa{x, ld, n, P.M, ng, gl, st, at<unsigned long long>(c.ws, L.off_buf), filter_grid(cps)};
+      launch_filter(fa, stream);
+      if (time_it) PK_CHECK(cudaEventRecord(t_events.b, stream));
+      PK_CHECK(cudaGetLastError());
+      // Run-time check: read the exact counts of every row.
+      char* rep = static_cast<char*>(hbuf) + sizeof(int) * rows * 4;
+      PK_CHECK(cudaMemcpy2DAsync(rep, REPORT_BYTES, st, sizeof(RowState), REPORT_BYTES, rows,
+                                 cudaMemcpyDeviceToHost, stream));
+      PK_CHECK(cudaStreamSynchronize(stream));
+      if (time_it) {
+        PK_CHECK(cudaEventElapsedTime(&filter_ms, t_events.a, t_events.b));
+        first_filter = false;
+      }
+      std::vector<int> ok, tie;
+      bool grow = false;
+      for (int r : group) {
+        const char* h = rep + REPORT_BYTES * r;
+        unsigned long long Rg = 0, Rt = 0, nanc = 0;
+        unsigned distinct = 0, tau_key = 0, errf = 0;
+        std::memcpy(&Rg, h + offsetof(RowState, R_ge), 8);
+        std::memcpy(&Rt, h + offsetof(RowState, R_gt), 8);
+        std::memcpy(&nanc, h + offsetof(RowState, nan), 8);
+        std::memcpy(&distinct, h + offsetof(RowState, distinct), 4);
+        std::memcpy(&tau_key, h + offsetof(RowState, tau_key), 4);
+        std::memcpy(&errf, h + offsetof(RowState, error), 4);
+        if (nanc > 0) {
+          c.status = PROFK_ERR_NAN;
+          goto done;
+        }
+        if (errf) {
+          c.status = PROFK_ERR_CUDA;
+          goto done;
+        }
+        if (static_cast<int64_t>(distinct) < P.S) {
+          // Fewer than S distinct values among the D draws: the same attempt
+          // runs again with more draws (same stream, so the same sample).
+          if (st_host[r].draw_doublings >= 24) {  // cannot happen for S <= n/2
+            c.status = PROFK_ERR_CUDA;
+            goto done;
+          }
+          st_host[r].draw_doublings += 1;
+          grow = true;
+          next.push_back(r);
+          continue;
+        }
+        profk_stats& s = st_host[r];
+        s.attempts = a + 1;
+        const float tau = key_to_float(tau_key);
+        if (a == 0) {
+          s.R_first = static_cast<int64_t>(Rg);
+          s.R_gt_first = static_cast<int64_t>(Rt);
+          s.tau_first = tau;
+        }
+        s.R_final = static_cast<int64_t>(Rg);
+        s.R_gt_final = static_cast<int64_t>(Rt);
+        s.tau_final = tau;
+        if (static_cast<uint64_t>(k) <= Rg && Rg <= static_cast<uint64_t>(P.M)) {
+          s.path = PROFK_PATH_FILTER;
+          ok.push_back(r);
+        } else if (tie_exit && Rg > static_cast<uint64_t>(P.M) && Rt < static_cast<uint64_t>(k)) {
+          s.path = PROFK_PATH_TIE;
+          tie.push_back(r);
+        } else {
+          attempt[r] = a + 1;
+          next.push_back(r);
+        }
+      }
+      if (!ok.empty()) {
+        int* ol = nullptr;
+        PK_CHECK(upload_rows(L, c.ws, hbuf, 1, ok, stream, &ol));
+        SelectArgs ra{KeySource::Buffer, at<unsigned long long>(c.ws, L.off_buf), P.M, P.M,
+                      static_cast<int>(ok.size()), ol, st};
+        uint64_t* sel = at<uint64_t>(c.ws, L.off_sel);
+        launch_select(ra, static_cast<uint64_t>(k), false, 0, stream);
+        launch_compact(ra, sel, L.kstride, k, stream);
+        launch_sort_emit(sel, L.kstride, k, static_cast<int>(ok.size()), ol, x, ld, n, out_vals, out_idx, stream);
+      }
+      if (!tie.empty()) {
+        int* tl = nullptr;
+        PK_CHECK(upload_rows(L, c.ws, hbuf, 2, tie, stream, &tl));
+        launch_tie_init(static_cast<int>(tie.size()), tl, st, k, stream);
+        SelectArgs ia{KeySource::Input, x, ld, n, static_cast<int>(tie.size()), tl, st};
+        uint64_t* sel = at<uint64_t>(c.ws, L.off_sel);
+        launch_select(ia, 0, false, 3, stream);
+        launch_compact(ia, sel, L.kstride, k, stream);
+        launch_sort_emit(sel, L.kstride, k, static_cast<int>(tie.size()), tl, x, ld, n, out_vals, out_idx, stream);
+      }
+      PK_CHECK(cudaGetLastError());
+      if (grow) {
+        // Grow the draw budget.  Everything enqueued so far uses the old
+        // workspace, whose release is stream-ordered behind it; per-row state
+        // is rebuilt by the next attempt's initialisation.
+        ws_free(c);
+        D *= 2;
+        L = make_layout(rows, n, k, P.S, D, P.M, true);
+        PK_CHECK(ws_alloc(c, L.total));
+        st = at<RowState>(c.ws, L.off_state);
+        PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState) * rows, stream));
+      }
+    }
+    pending = next;
+  }
+
+  if (!fallback.empty()) {
+    int* fl = nullptr;
+    PK_CHECK(upload_rows(L, c.ws, hbuf, 3, fallback, stream, &fl));
+    for (int r : fallback) st_host[r].path = PROFK_PATH_FALLBACK;
+    launch_exact(L, c.ws, x, ld, static_cast<int>(fallback.size()), fl, out_vals, out_idx, stream);
+    PK_CHECK(cudaGetLastError());
+    exact_ran = true;
+  }
+  if (exact_ran) {
+    // The exact selection's first pass counted NaN keys of its rows.
+    char* rep = static_cast<char*>(hbuf) + sizeof(int) * rows * 4;
+    PK_CHECK(cudaMemcpy2DAsync(rep, REPORT_BYTES, st, sizeof(RowState), REPORT_BYTES, rows, cudaMemcpyDeviceToHost,
+                               stream));
+    PK_CHECK(cudaStreamSynchronize(stream));
+    for (int64_t r = 0; r < rows; ++r) {
+      unsigned long long q = 0;
+      std::memcpy(&q, rep + REPORT_BYTES * r + offsetof(RowState, sel_nan), 8);
+      if (q) {
+        c.status = PROFK_ERR_NAN;
+        goto done;
+      }
+    }
+  }
+
+done:
+  ws_free(c);
+  if (stats) {
+    for (int64_t r = 0; r < rows; ++r) {
+      st_host[r].aux_bytes = c.ws_bytes;
+      st_host[r].filter_ms = filter_ms;
+      st_host[r].cuda_error = static_cast<int32_t>(c.err);
+      st_host[r].launches = static_cast<int32_t>(launch_count() - launches0);
+      stats[r] = st_host[r];
+    }
+  }
+  return c.status;
+}
+
+}  // namespace
+}  // namespace profk
+
+using namespace profk;
+
+extern "C" {
+
+int profk_topk(const float* x, int64_t n, int64_t k, double eps, uint64_t seed, float* out_vals, int64_t* out_idx,
+               cudaStream_t stream, profk_stats* stats) {
+  return run_topk(x, 1, n, n, k, eps, seed, out_vals, out_idx, stream, stats);
+}
+
+int profk_topk_batched(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,
+                       float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_stats* stats) {
+  return run_topk(x, rows, n, ld, k, eps, seed, out_vals, out_idx, stream, stats);
+}
+
+int profk_params(int64_t n, int64_t k, double eps, int mode, int64_t* S, int64_t* t, int64_t* M) {
+  if (n < 1 || k < 1 || k > n || !(eps > 0.0 && eps < 1.0) || (mode != 0 && mode != 1) || !S || !t || !M)
+    return PROFK_ERR_INVALID;
+  const Params p = cached_params(n, k, eps, mode);
+  *S = p.S;
+  *t = p.t;
+  *M = p.M;
+  return PROFK_OK;
+}
+
+size_t profk_workspace_size(int64_t rows, int64_t n, int64_t k, double eps) {
+  if (rows < 1 || n < 1 || k < 1 || k > n || !(eps > 0.0 && eps < 1.0)) return 0;
+  const Params P = cached_params(n, k, eps / static_cast<double>(rows), static_cast<int>(g_opt[0].load()));
+  const bool sampling = uses_filter(n, k, P.S);
+  return make_layout(rows, n, k, P.S, sampling ? draw_budget(n, P.S) : 0, P.M, sampling).total;
+}
+
+int profk_set_option(int option, int64_t value) {
+  if (option < 0 || option >= PROFK_OPT__COUNT) return PROFK_ERR_INVALID;
+  if (option == PROFK_OPT_PARAM_MODE && value != 0 && value != 1) return PROFK_ERR_INVALID;
+  if (value < 0) return PROFK_ERR_INVALID;
+  g_opt[option].store(value);
+  return PROFK_OK;
+}
+
+int64_t profk_get_option(int option) {
+  if (option < 0 || option >= PROFK_OPT__COUNT) return PROFK_ERR_INVALID;
+  return g_opt[option].load();
+}
+
+const char* profk_strerror(int code) {
+  switch (code) {
+    case PROFK_OK: return "ok";
+    case PROFK_ERR_INVALID: return "invalid argument";
+    case PROFK_ERR_CUDA: return "CUDA error";
+    case PROFK_ERR_NAN: return "input contains NaN";
+    case PROFK_ERR_UNSUPPORTED: return "unsupported input (n > 2^32 or misaligned pointer / stride)";
+    case PROFK_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int profk_sample(const float* x, int64_t n, int64_t S, uint64_t seed, int64_t row, int32_t attempt,
+                 int64_t* out_sidx, float* out_vals, cudaStream_t stream) {
+  if (!x || !out_sidx || !out_vals || n < 2 || S < 1 || 2 * S > n || n > (1ll << 32) || row < 0 || attempt < 0)
+    return PROFK_ERR_INVALID;
+  Call c;
+  c.stream = stream;
+  int64_t D = draw_budget(n, S);
+  Layout L;
+  void* hbuf = nullptr;
+  for (int iter = 0; iter < 40; ++iter) {
+    L = make_layout(1, n, 1, S, D, 1, true);
+    PK_CHECK(ws_alloc(c, L.total));
+    {
+      RowState* st = at<RowState>(c.ws, L.off_state);
+      PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
+      ++launch_count();
+      k_reset_tables<<<dim3(256, 1), 1024, 0, stream>>>(at<unsigned long long>(c.ws, L.off_table), L.log2H, nullptr);
+      SampleArgs sa{x, n, static_cast<uint64_t>(n), S, D, L.log2H, seed, attempt, 1, nullptr, st,
+                    at<unsigned long long>(c.ws, L.off_table), at<uint32_t>(c.ws, L.off_draws),
+                    at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
+                    at<uint32_t>(c.ws, L.off_skeys)};
+      launch_sample_rows(sa, row, stream);
+      PK_CHECK(cudaGetLastError());
+      PK_CHECK(pinned(REPORT_BYTES, &hbuf));
+      PK_CHECK(cudaMemcpyAsync(hbuf, st, REPORT_BYTES, cudaMemcpyDeviceToHost, stream));
+      PK_CHECK(cudaStreamSynchronize(stream));
+      unsigned distinct = 0, errf = 0;
+      std::memcpy(&distinct, static_cast<char*>(hbuf) + offsetof(RowState, distinct), 4);
+      std::memcpy(&errf, static_cast<char*>(hbuf) + offsetof(RowState, error), 4);
+      if (errf) {
+        c.status = PROFK_ERR_CUDA;
+        goto done;
+      }
+      if (static_cast<int64_t>(distinct) >= S) {
+        const unsigned b = static_cast<unsigned>(std::min<int64_t>((S + 255) / 256, 1024));
+        ++launch_count();
+        k_sample_out<<<b, 256, 0, stream>>>(at<uint32_t>(c.ws, L.off_sidx), S, x, out_sidx, out_vals);
+        PK_CHECK(cudaGetLastError());
+        goto done;
+      }
+    }
+    ws_free(c);
+    D *= 2;
+  }
+  c.status = PROFK_ERR_CUDA;
+done:
+  ws_free(c);
+  return c.status;
+}
+
+int profk_threshold(const float* vals, int64_t S, int64_t t, float* out_tau, cudaStream_t stream) {
+  if (!vals || !out_tau || S < 1 || t < 1 || t > S || S > (1ll << 31)) return PROFK_ERR_INVALID;
+  Call c;
+  c.stream = stream;
+  const size_t bytes = align_up(sizeof(RowState)) + align_up(sizeof(uint32_t) * S);
+  PK_CHECK(ws_alloc(c, bytes));
+  {
+    RowState* st = at<RowState>(c.ws, 0);
+    uint32_t* keys = at<uint32_t>(c.ws, align_up(sizeof(RowState)));
+    PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
+    const unsigned b = static_cast<unsigned>(std::min<int64_t>((S + 255) / 256, 1024));
+    ++launch_count();
+    k_vals_to_keys<<<b, 256, 0, stream>>>(vals, S, keys);
+    SelectArgs ta{KeySource::SampleKeys, keys, S, S, 1, nullptr, st};
+    launch_select(ta, static_cast<uint64_t>(t), true, 0, stream);
+    launch_store_tau(1, nullptr, st, stream);
+    ++launch_count();
+    k_tau_out<<<1, 1, 0, stream>>>(st, out_tau);
+    PK_CHECK(cudaGetLastError());
+  }
+done:
+  ws_free(c);
+  return c.status;
+}
+
+int profk_filter(const float* x, int64_t n, float tau, int64_t M, uint64_t* out_keys, uint64_t* out_counts,
+                 cudaStream_t stream) {
+  if (!x || !out_counts || n < 1 || M < 0 || (M > 0 && !out_keys) || n > (1ll << 32)) return PROFK_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) != 0) return PROFK_ERR_UNSUPPORTED;
+  Call c;
+  c.stream = stream;
+  PK_CHECK(ws_alloc(c, align_up(sizeof(RowState))));
+  {
+    RowState* st = at<RowState>(c.ws, 0);
+    PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
+    ++launch_count();
+    k_set_tau<<<1, 1, 0, stream>>>(st, tau);
+    const int64_t cps = g_opt[PROFK_OPT_FILTER_CTAS_PER_SM].load();
+    FilterArgs fa{x, n, n, M, 1, nullptr, st, reinterpret_cast<unsigned long long*>(out_keys), filter_grid(cps)};
+    launch_filter(fa, stream);
+    PK_CHECK(cudaMemcpyAsync(out_counts, &st->R_ge, 3 * sizeof(unsigned long long), cudaMemcpyDeviceToDevice, stream));
+    PK_CHECK(cudaGetLastError());
+  }
+done:
+  ws_free(c);
+  return c.status;
+}
+
+int profk_refine(const uint64_t* keys, int64_t R, int64_t k, const float* x, int64_t n, float* out_vals,
+                 int64_t* out_idx, cudaStream_t stream) {
+  if (!keys || !x || !out_vals || !out_idx || k < 1 || R < k || n < 1) return PROFK_ERR_INVALID;
+  Call c;
+  c.stream = stream;
+  const int64_t ks = sort_stride(k);
+  PK_CHECK(ws_alloc(c, align_up(sizeof(RowState)) + align_up(sizeof(unsigned long long) * ks)));
+  {
+    RowState* st = at<RowState>(c.ws, 0);
+    unsigned long long* sel = at<unsigned long long>(c.ws, align_up(sizeof(RowState)));
+    PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
+    ++launch_count();
+    k_set_count<<<1, 1, 0, stream>>>(st, static_cast<unsigned long long>(R));
+    SelectArgs ra{KeySource::Buffer, keys, R, R, 1, nullptr, st};
+    launch_select(ra, static_cast<uint64_t>(k), false, 0, stream);
+    launch_compact(ra, reinterpret_cast<uint64_t*>(sel), ks, k, stream);
+    launch_sort_emit(reinterpret_cast<uint64_t*>(sel), ks, k, 1, nullptr, x, 0, n, out_vals, out_idx, stream);
+    PK_CHECK(cudaGetLastError());
+  }
+done:
+  ws_free(c);
+  return c.status;
+}
+
+int profk_exact(const float* x, int64_t n, int64_t k, float* out_vals, int64_t* out_idx, cudaStream_t stream) {
+  if (!x || !out_vals || !out_idx || n < 1 || k < 1 || k > n) return PROFK_ERR_INVALID;
+  if (n > (1ll << 32)) return PROFK_ERR_UNSUPPORTED;
+  Call c;
+  c.stream = stream;
+  Layout L = make_layout(1, n, k, 0, 0, 0, false);
+  void* hbuf = nullptr;
+  PK_CHECK(ws_alloc(c, L.total));
+  {
+    RowState* st = at<RowState>(c.ws, L.off_state);
+    PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
+    launch_exact(L, c.ws, x, n, 1, nullptr, out_vals, out_idx, stream);
+    PK_CHECK(cudaGetLastError());
+    PK_CHECK(pinned(REPORT_BYTES, &hbuf));
+    PK_CHECK(cudaMemcpyAsync(hbuf, st, REPORT_BYTES, cudaMemcpyDeviceToHost, stream));
+    PK_CHECK(cudaStreamSynchronize(stream));
+    unsigned long long q = 0;
+    std::memcpy(&q, static_cast<char*>(hbuf) + offsetof(RowState, sel_nan), 8);
+    if (q) c.status = PROFK_ERR_NAN;
+  }
+done:
+  ws_free(c);
+  return c.status;
+}
+
+}  // extern "C"

@@ -1,0 +1,138 @@
+// Shared device definitions of the Prof-K library (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace profk {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+constexpr int HIST_BITS = 11;
+constexpr int HIST_BINS = 1 << HIST_BITS;  // 2048-bin radix histograms
+
+// ---------------------------------------------------------------------------
+// Order keys.  ord(v) maps a float to a uint32 whose unsigned order is the
+// IEEE order of the values, with -0.0 folded onto +0.0 so that they compare
+// equal.  A candidate (v, i) is the 64-bit key (ord(v) << 32) | ~i: larger key
+// = larger value, and for equal values the lower index.  NaN maps above
+// ord(+inf) (positive NaN) or below ord(-inf) (negative NaN).
+__host__ __device__ __forceinline__ uint32_t ord_key(float v) {
+#ifdef __CUDA_ARCH__
+  uint32_t b = __float_as_uint(v);
+#else
+  uint32_t b;
+  __builtin_memcpy(&b, &v, 4);
+#endif
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__host__ __device__ __forceinline__ float key_to_float(uint32_t k) {
+  uint32_t b = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+#ifdef __CUDA_ARCH__
+  return __uint_as_float(b);
+#else
+  float v;
+  __builtin_memcpy(&v, &b, 4);
+  return v;
+#endif
+}
+
+constexpr uint32_t KEY_POS_INF = 0xff800000u;  // ord(+inf)
+constexpr uint32_t KEY_NEG_INF = 0x007fffffu;  // ord(-inf)
+
+__host__ __device__ __forceinline__ bool key_is_nan(uint32_t k) {
+  return k > KEY_POS_INF || k < KEY_NEG_INF;
+}
+
+__device__ __forceinline__ uint64_t cand_key(float v, uint32_t idx) {
+  return (static_cast<uint64_t>(ord_key(v)) << 32) | static_cast<uint32_t>(~idx);
+}
+
+__device__ __forceinline__ uint32_t cand_index(uint64_t key) {
+  return ~static_cast<uint32_t>(key & 0xffffffffull);
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds; each round
+// multiplies counter words 0 and 2 by two odd constants (128-bit products)
+// and mixes with words 1, 3 and the key; the key is bumped by two Weyl
+// constants between rounds.
+constexpr uint64_t PHILOX_M0 = 0xD2E7470EE14C6C93ull;
+constexpr uint64_t PHILOX_M1 = 0xCA5A826395121157ull;
+constexpr uint64_t PHILOX_W0 = 0x9E3779B97F4A7C15ull;
+constexpr uint64_t PHILOX_W1 = 0xBB67AE8584CAA73Bull;
+
+__device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += PHILOX_W0;
+      k1 += PHILOX_W1;
+    }
+    const uint64_t lo0 = PHILOX_M0 * c[0], hi0 = __umul64hi(PHILOX_M0, c[0]);
+    const uint64_t lo1 = PHILOX_M1 * c[2], hi1 = __umul64hi(PHILOX_M1, c[2]);
+    const uint64_t n0 = hi1 ^ c[1] ^ k0;
+    const uint64_t n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+}
+
+// Lemire's multiply-shift bounded integer: accept w for range n unless the
+// low half of w*n falls in the (2^64 mod n) rejection zone.
+__device__ __forceinline__ bool lemire64(uint64_t w, uint64_t n, uint64_t* out) {
+  const uint64_t lo = w * n;
+  if (lo < n) {
+    const uint64_t thr = (0ull - n) % n;
+    if (lo < thr) return false;
+  }
+  *out = __umul64hi(w, n);
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Per-row device state of one call.  Zeroed by the host before use.
+struct RowState {
+  // Filter counters of the current attempt.  R_ge is also the slot cursor
+  // of the candidate buffer: it counts every passer, stores stop at M.
+  unsigned long long R_ge;
+  unsigned long long R_gt;
+  unsigned long long nan;
+  // Sampling.
+  unsigned int distinct;  // distinct draws among the D examined
+  unsigned int tau_key;   // ord(tau)
+  // Radix selection of the r-th largest key (r = 1 is the maximum).
+  unsigned long long sel_prefix;  // resolved high bits (right-aligned)
+  unsigned long long sel_rank;    // rank still to find inside the prefix bucket
+  unsigned long long sel_above;   // keys strictly above the prefix bucket
+  unsigned long long sel_bucket;  // population of the last chosen bucket
+  unsigned long long sel_thresh;  // final threshold key (valid when sel_done)
+  unsigned long long sel_nan;     // NaN keys seen by the first pass (float sources)
+  int sel_bits;                   // number of resolved high bits
+  int sel_done;                   // 1 once the threshold is known
+  unsigned int done_blocks;       // last-block-done ticket
+  unsigned int compact_count;     // output cursor of the compaction
+  unsigned int error;             // nonzero: a device-side check failed
+  unsigned int pad;
+  unsigned int hist[HIST_BINS];
+};
+
+// Row of a launch: identity unless a row list is given.
+__device__ __forceinline__ int launch_row(const int* rows) {
+  return rows ? rows[blockIdx.y] : static_cast<int>(blockIdx.y);
+}
+
+// Warp-aggregated shared-memory histogram increment.
+__device__ __forceinline__ void hist_add(unsigned int* h, uint32_t bin, bool valid) {
+  const unsigned act = __ballot_sync(FULL_MASK, valid);
+  if (valid) {
+    const unsigned peers = __match_any_sync(act, bin);
+    const int lane = threadIdx.x & 31;
+    if (lane == __ffs(peers) - 1) atomicAdd(h + bin, static_cast<unsigned>(__popc(peers)));
+  }
+}
+
+}  // namespace profk

@@ -1,0 +1,21 @@
+// Host parameter rules of Prof-K (see params.cpp).
+#pragma once
+
+#include <cstdint>
+
+namespace profk {
+
+struct Params {
+  int64_t S, t, M;
+};
+
+double inv_norm_cdf(double p);
+int64_t sample_size_thm5(int64_t n, int64_t k, double eps);
+int64_t threshold_rank_fast(int64_t n, int64_t k, int64_t S, double eps);
+int64_t buffer_capacity_fast(int64_t n, int64_t S, int64_t t, double eps);
+// mode 0: default rule, mode 1: the older version's Algorithm 1 literally.
+Params compute_params(int64_t n, int64_t k, double eps, int mode);
+// Sampling pays off only when S <= n/8 and k <= n/64; otherwise the exact path runs.
+bool uses_filter(int64_t n, int64_t k, int64_t S);
+
+}  // namespace profk

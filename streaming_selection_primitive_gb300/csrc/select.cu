@@ -1,0 +1,473 @@
+// Exact selection machinery shared by Prof-K's steps 2 and 4 and by the exact
+// fallback ("Prof-K: Probabilistic One-Pass Filtering for Efficient Top-k
+// Selection", Section 3, stages 2 and 4).
+//
+// * Radix selection of the r-th largest key, most significant digit first:
+//   one launch per 11/11/10-bit digit.  Every block histograms the keys that
+//   match the prefix resolved so far; the last block to finish (a ticket
+//   counter, no spin-wait) picks the digit that holds rank r, narrows the
+//   prefix and clears the histogram for the next launch.  Composite
+//   (value, index) keys are distinct, so six digits give the exact k-th key;
+//   the selection stops early once a whole bucket falls inside the top-k.
+// * Compaction of the keys >= the selected threshold (exactly k of them).
+// * Bitonic sort of the k keys (descending) and emission of values/indices.
+#include <algorithm>
+
+#include "kernels.h"
+
+namespace profk {
+namespace {
+
+constexpr int SEL_THREADS = 512;
+constexpr int SMALL_SORT_MAX = 8192;    // keys sorted by one CTA in shared memory
+constexpr int CHUNK = 8192;             // shared-memory chunk of the multi-CTA sort
+constexpr int SORT_THREADS = 1024;
+
+struct SrcSample {
+  static constexpr bool kFloat = false;
+  const uint32_t* k;
+  int64_t stride, len;
+  __device__ int64_t length(const RowState&) const { return len; }
+  __device__ uint64_t key(int row, int64_t i) const {
+    return static_cast<uint64_t>(k[row * stride + i]) << 32;
+  }
+};
+
+struct SrcInput {
+  static constexpr bool kFloat = true;
+  const float* x;
+  int64_t ld, n;
+  __device__ int64_t length(const RowState&) const { return n; }
+  __device__ uint64_t key(int row, int64_t i) const {
+    return cand_key(x[row * ld + i], static_cast<uint32_t>(i));
+  }
+};
+
+struct SrcBuffer {
+  static constexpr bool kFloat = false;
+  const unsigned long long* b;
+  int64_t stride, cap;
+  __device__ int64_t length(const RowState& s) const {
+    return s.R_ge < static_cast<unsigned long long>(cap) ? static_cast<int64_t>(s.R_ge) : cap;
+  }
+  __device__ uint64_t key(int row, int64_t i) const { return b[row * stride + i]; }
+};
+
+__global__ void k_sel_init(RowState* st, const int* rows, unsigned long long rank) {
+  const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
+  RowState& S = st[row];
+  for (int b = threadIdx.x; b < HIST_BINS; b += blockDim.x) S.hist[b] = 0;
+  if (threadIdx.x == 0) {
+    S.sel_prefix = 0;
+    S.sel_rank = rank;
+    S.sel_above = 0;
+    S.sel_bucket = 0;
+    S.sel_thresh = 0;
+    S.sel_nan = 0;
+    S.sel_bits = 0;
+    S.sel_done = 0;
+    S.done_blocks = 0;
+    S.compact_count = 0;
+  }
+}
+
+__global__ void k_tie_init(RowState* st, const int* rows, unsigned long long k) {
+  const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
+  RowState& S = st[row];
+  for (int b = threadIdx.x; b < HIST_BINS; b += blockDim.x) S.hist[b] = 0;
+  if (threadIdx.x == 0) {
+    S.sel_prefix = S.tau_key;
+    S.sel_above = S.R_gt;
+    S.sel_rank = k - S.R_gt;  // 1 <= rank because R_gt < k on this path
+    S.sel_bucket = 0;
+    S.sel_thresh = 0;
+    S.sel_nan = 0;
+    S.sel_bits = 32;
+    S.sel_done = 0;
+    S.done_blocks = 0;
+    S.compact_count = 0;
+  }
+}
+
+__global__ void k_store_tau(RowState* st, const int* rows) {
+  const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
+  if (threadIdx.x == 0) st[row].tau_key = static_cast<uint32_t>(st[row].sel_prefix);
+}
+
+// Block-wide exclusive scan of one u64 per thread (thread order).
+__device__ __forceinline__ unsigned long long block_excl_scan(unsigned long long v, unsigned long long* sw) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned long long incl = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(FULL_MASK, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sw[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long w = lane < nw ? sw[lane] : 0ull;
+    unsigned long long wi = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(FULL_MASK, wi, o);
+      if (lane >= o) wi += t;
+    }
+    if (lane < nw) sw[lane] = wi - w;
+  }
+  __syncthreads();
+  return sw[warp] + incl - v;
+}
+
+template <class Src>
+__global__ void __launch_bounds__(SEL_THREADS) k_radix_pass(Src src, RowState* st, const int* rows, int shift,
+                                                           int width, int final_shift, int value_only,
+                                                           int count_nan) {
+  __shared__ unsigned h[HIST_BINS];
+  __shared__ unsigned long long sw[32];
+  __shared__ unsigned s_nan;
+  __shared__ int s_last;
+  const int row = launch_row(rows);
+  RowState& S = st[row];
+  if (S.sel_done) return;
+  const unsigned long long prefix = S.sel_prefix;
+  const int bits = S.sel_bits;
+  const int hi_shift = shift + width;
+  const unsigned nb = 1u << width;
+  for (unsigned b = threadIdx.x; b < nb; b += blockDim.x) h[b] = 0;
+  if (threadIdx.x == 0) s_nan = 0;
+  __syncthreads();
+  const int64_t len = src.length(S);
+  const int lane = threadIdx.x & 31;
+  unsigned nan_local = 0;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); w0 < len; w0 += step) {
+    const int64_t i = w0 + lane;
+    const bool valid = i < len;
+    const uint64_t key = valid ? src.key(row, i) : 0ull;
+    if (Src::kFloat && count_nan && valid && key_is_nan(static_cast<uint32_t>(key >> 32))) ++nan_local;
+    const bool match = valid && (bits == 0 || (key >> hi_shift) == prefix);
+    hist_add(h, static_cast<uint32_t>(key >> shift) & (nb - 1), match);
+  }
+  if (nan_local) atomicAdd(&s_nan, nan_local);
+  __syncthreads();
+  for (unsigned b = threadIdx.x; b < nb; b += blockDim.x)
+    if (h[b]) atomicAdd(&S.hist[b], h[b]);
+  if (threadIdx.x == 0 && s_nan) atomicAdd(&S.sel_nan, static_cast<unsigned long long>(s_nan));
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(&S.done_blocks, 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (unsigned b = threadIdx.x; b < nb; b += blockDim.x) h[b] = __ldcg(&S.hist[b]);
+  __syncthreads();
+  // Thread t owns `per` consecutive bins counted down from the top digit.
+  const int per = (nb + blockDim.x - 1) / blockDim.x;
+  const int top = static_cast<int>(nb) - 1 - static_cast<int>(threadIdx.x) * per;
+  unsigned long long local = 0;
+  for (int q = 0; q < per; ++q)
+    if (top - q >= 0) local += h[top - q];
+  const unsigned long long rank = S.sel_rank;  // read before any thread updates it
+  const unsigned long long excl = block_excl_scan(local, sw);
+  if (excl < rank && rank <= excl + local) {
+    unsigned long long acc = excl;
+    for (int q = 0; q < per; ++q) {
+      const int b = top - q;
+      if (b < 0) break;
+      const unsigned long long c = h[b];
+      if (rank <= acc + c) {
+        const unsigned long long np = (prefix << width) | static_cast<unsigned long long>(b);
+        S.sel_above += acc;
+        S.sel_rank = rank - acc;
+        S.sel_prefix = np;
+        S.sel_bits = bits + width;
+        S.sel_bucket = c;
+        if (shift == final_shift || (!value_only && c == rank - acc)) {
+          S.sel_done = 1;
+          S.sel_thresh = np << shift;
+        }
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+  for (unsigned b = threadIdx.x; b < nb; b += blockDim.x) S.hist[b] = 0;
+  if (threadIdx.x == 0) {
+    if (S.sel_bits == bits) {  // no digit was chosen
+      atomicOr(&S.error, 4u);
+      S.sel_done = 1;
+      S.sel_thresh = ~0ull;
+    }
+    S.done_blocks = 0;
+  }
+}
+
+template <class Src>
+__global__ void __launch_bounds__(SEL_THREADS) k_compact(Src src, RowState* st, const int* rows,
+                                                        unsigned long long* out, int64_t out_stride, int64_t k) {
+  const int row = launch_row(rows);
+  RowState& S = st[row];
+  if (!S.sel_done) return;
+  const unsigned long long thresh = S.sel_thresh;
+  const int64_t len = src.length(S);
+  const int lane = threadIdx.x & 31;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); w0 < len; w0 += step) {
+    const int64_t i = w0 + lane;
+    const bool valid = i < len;
+    const uint64_t key = valid ? src.key(row, i) : 0ull;
+    const bool sel = valid && key >= thresh;
+    const unsigned m = __ballot_sync(FULL_MASK, sel);
+    if (m) {
+      unsigned base = 0;
+      if (lane == 0) base = atomicAdd(&S.compact_count, static_cast<unsigned>(__popc(m)));
+      base = __shfl_sync(FULL_MASK, base, 0);
+      if (sel) {
+        const unsigned pos = base + __popc(m & ((1u << lane) - 1u));
+        if (pos < static_cast<unsigned long long>(k)) out[row * out_stride + pos] = key;
+      }
+    }
+  }
+}
+
+// Writes output j of a row.  The index is checked against the row length so
+// that a selection that went wrong can never read outside x; such an entry is
+// written as (NaN, -1), which no valid result contains.
+__device__ __forceinline__ void emit_one(const unsigned long long key, int row, int64_t j, int64_t k, const float* x,
+                                         int64_t ld, int64_t n, float* out_vals, int64_t* out_idx) {
+  const uint32_t idx = cand_index(key);
+  if (static_cast<int64_t>(idx) < n) {
+    out_idx[row * k + j] = static_cast<int64_t>(idx);
+    out_vals[row * k + j] = x[row * ld + idx];
+  } else {
+    out_idx[row * k + j] = -1;
+    out_vals[row * k + j] = __int_as_float(0x7fc00000);
+  }
+}
+
+// One CTA per row: load k keys, pad to P with 0 (below every real key), sort
+// descending in shared memory, emit.
+__global__ void __launch_bounds__(SORT_THREADS) k_sort_small(const unsigned long long* keys, int64_t key_stride,
+                                                            int64_t k, int P, const int* rows, const float* x,
+                                                            int64_t ld, int64_t n, float* out_vals,
+                                                            int64_t* out_idx) {
+  extern __shared__ unsigned long long s[];
+  const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
+  const unsigned long long* kr = keys + row * key_stride;
+  for (int i = threadIdx.x; i < P; i += blockDim.x) s[i] = i < k ? kr[i] : 0ull;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < P; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned long long a = s[i], b = s[l];
+          const bool desc = (i & size) == 0;
+          if (desc ? (a < b) : (a > b)) {
+            s[i] = b;
+            s[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int j = threadIdx.x; j < k; j += blockDim.x) emit_one(s[j], row, j, k, x, ld, n, out_vals, out_idx);
+}
+
+// Multi-CTA bitonic sort (descending) of rows of P = 2^m keys.
+__global__ void __launch_bounds__(SORT_THREADS) k_pad(unsigned long long* keys, int64_t key_stride, int64_t k,
+                                                      int64_t P, const int* rows) {
+  const int row = launch_row(rows);
+  for (int64_t i = k + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < P;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    keys[row * key_stride + i] = 0ull;
+}
+
+// Stages size <= `upto` (all j < CHUNK) of one CHUNK-key chunk in shared memory,
+// starting at stage `from` (2 for a full local sort, or one merge stage).
+__global__ void __launch_bounds__(SORT_THREADS) k_bitonic_chunk(unsigned long long* keys, int64_t key_stride,
+                                                                int from, int64_t upto, const int* rows) {
+  extern __shared__ unsigned long long s[];
+  const int row = launch_row(rows);
+  unsigned long long* kr = keys + row * key_stride + static_cast<int64_t>(blockIdx.x) * CHUNK;
+  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * CHUNK;
+  for (int i = threadIdx.x; i < CHUNK; i += blockDim.x) s[i] = kr[i];
+  __syncthreads();
+  for (int64_t size = from; size <= upto; size <<= 1) {
+    int64_t j = size >> 1;
+    if (j >= CHUNK) j = CHUNK >> 1;
+    for (; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < CHUNK; i += blockDim.x) {
+        const int l = i ^ static_cast<int>(j);
+        if (l > i) {
+          const unsigned long long a = s[i], b = s[l];
+          const bool desc = ((g0 + i) & size) == 0;
+          if (desc ? (a < b) : (a > b)) {
+            s[i] = b;
+            s[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < CHUNK; i += blockDim.x) kr[i] = s[i];
+}
+
+__global__ void __launch_bounds__(SORT_THREADS) k_bitonic_global(unsigned long long* keys, int64_t key_stride,
+                                                                 int64_t P, int64_t size, int64_t j, const int* rows) {
+  const int row = launch_row(rows);
+  unsigned long long* kr = keys + row * key_stride;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < P;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t l = i ^ j;
+    if (l > i) {
+      const unsigned long long a = kr[i], b = kr[l];
+      const bool desc = (i & size) == 0;
+      if (desc ? (a < b) : (a > b)) {
+        kr[i] = b;
+        kr[l] = a;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(SORT_THREADS) k_emit(const unsigned long long* keys, int64_t key_stride, int64_t k,
+                                                       const int* rows, const float* x, int64_t ld, int64_t n,
+                                                       float* out_vals, int64_t* out_idx) {
+  const int row = launch_row(rows);
+  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < k;
+       j += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    emit_one(keys[row * key_stride + j], row, j, k, x, ld, n, out_vals, out_idx);
+}
+
+int64_t next_pow2(int64_t v) {
+  int64_t p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+unsigned blocks_for(int64_t len, int threads, int cap) {
+  int64_t b = (len + threads * 4 - 1) / (threads * 4);
+  if (b < 1) b = 1;
+  if (b > cap) b = cap;
+  return static_cast<unsigned>(b);
+}
+
+int g_sms = 0;
+int sms() {
+  if (!g_sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms <= 0) g_sms = 1;
+  }
+  return g_sms;
+}
+
+template <class Src>
+void run_passes(const Src& src, const SelectArgs& a, bool value_only, int first_pass, cudaStream_t stream) {
+  // Digits of the 64-bit key from the top: 11, 11, 10 | 11, 11, 10 bits.
+  static const int shifts[6] = {53, 42, 32, 21, 10, 0};
+  static const int widths[6] = {11, 11, 10, 11, 11, 10};
+  const int last = value_only ? 2 : 5;
+  const int final_shift = shifts[last];
+  const unsigned bx = blocks_for(a.len, SEL_THREADS, 4 * sms());
+  for (int p = first_pass; p <= last; ++p) {
+    ++launch_count();
+    k_radix_pass<Src><<<dim3(bx, a.nrows), SEL_THREADS, 0, stream>>>(src, a.st, a.rows, shifts[p], widths[p],
+                                                                     final_shift, value_only ? 1 : 0, p == 0);
+  }
+}
+
+}  // namespace
+
+void launch_select(const SelectArgs& a, uint64_t init_rank, bool value_only, int first_pass, cudaStream_t stream) {
+  if (init_rank > 0) {
+    ++launch_count();
+    k_sel_init<<<a.nrows, 256, 0, stream>>>(a.st, a.rows, init_rank);
+  }
+  switch (a.src) {
+    case KeySource::SampleKeys:
+      run_passes(SrcSample{static_cast<const uint32_t*>(a.base), a.stride, a.len}, a, value_only, first_pass, stream);
+      break;
+    case KeySource::Input:
+      run_passes(SrcInput{static_cast<const float*>(a.base), a.stride, a.len}, a, value_only, first_pass, stream);
+      break;
+    case KeySource::Buffer:
+      run_passes(SrcBuffer{static_cast<const unsigned long long*>(a.base), a.stride, a.len}, a, value_only,
+                 first_pass, stream);
+      break;
+  }
+}
+
+void launch_store_tau(int nrows, const int* rows, RowState* st, cudaStream_t stream) {
+  ++launch_count();
+  k_store_tau<<<nrows, 32, 0, stream>>>(st, rows);
+}
+
+void launch_tie_init(int nrows, const int* rows, RowState* st, int64_t k, cudaStream_t stream) {
+  ++launch_count();
+  k_tie_init<<<nrows, 256, 0, stream>>>(st, rows, static_cast<unsigned long long>(k));
+}
+
+void launch_compact(const SelectArgs& a, uint64_t* out, int64_t out_stride, int64_t k, cudaStream_t stream) {
+  const unsigned bx = blocks_for(a.len, SEL_THREADS, 4 * sms());
+  unsigned long long* o = reinterpret_cast<unsigned long long*>(out);
+  switch (a.src) {
+    case KeySource::SampleKeys:
+      ++launch_count();
+      k_compact<<<dim3(bx, a.nrows), SEL_THREADS, 0, stream>>>(
+          SrcSample{static_cast<const uint32_t*>(a.base), a.stride, a.len}, a.st, a.rows, o, out_stride, k);
+      break;
+    case KeySource::Input:
+      ++launch_count();
+      k_compact<<<dim3(bx, a.nrows), SEL_THREADS, 0, stream>>>(
+          SrcInput{static_cast<const float*>(a.base), a.stride, a.len}, a.st, a.rows, o, out_stride, k);
+      break;
+    case KeySource::Buffer:
+      ++launch_count();
+      k_compact<<<dim3(bx, a.nrows), SEL_THREADS, 0, stream>>>(
+          SrcBuffer{static_cast<const unsigned long long*>(a.base), a.stride, a.len}, a.st, a.rows, o, out_stride,
+          k);
+      break;
+  }
+}
+
+int64_t sort_stride(int64_t k) { return k > SMALL_SORT_MAX ? next_pow2(k) : k; }
+
+void launch_sort_emit(uint64_t* keys_u, int64_t key_stride, int64_t k, int nrows, const int* rows, const float* x,
+                      int64_t ld, int64_t n, float* out_vals, int64_t* out_idx, cudaStream_t stream) {
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(keys_u);
+  if (k <= SMALL_SORT_MAX) {
+    cudaFuncSetAttribute(k_sort_small, cudaFuncAttributeMaxDynamicSharedMemorySize, SMALL_SORT_MAX * 8);
+    const int P = static_cast<int>(next_pow2(k));
+    ++launch_count();
+    k_sort_small<<<nrows, SORT_THREADS, P * 8, stream>>>(keys, key_stride, k, P, rows, x, ld, n, out_vals, out_idx);
+    return;
+  }
+  const int64_t P = next_pow2(k);  // >= 2 * CHUNK here
+  cudaFuncSetAttribute(k_bitonic_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize, CHUNK * 8);
+  const unsigned padb = static_cast<unsigned>(std::min<int64_t>((P - k + SORT_THREADS - 1) / SORT_THREADS + 1, 1024));
+  ++launch_count();
+  k_pad<<<dim3(padb, nrows), SORT_THREADS, 0, stream>>>(keys, key_stride, k, P, rows);
+  const unsigned chunks = static_cast<unsigned>(P / CHUNK);
+  ++launch_count();
+  k_bitonic_chunk<<<dim3(chunks, nrows), SORT_THREADS, CHUNK * 8, stream>>>(keys, key_stride, 2, CHUNK, rows);
+  const unsigned gb = static_cast<unsigned>(std::min<int64_t>(P / 2 / SORT_THREADS + 1, 4096));
+  for (int64_t size = 2 * CHUNK; size <= P; size <<= 1) {
+    for (int64_t j = size >> 1; j >= CHUNK; j >>= 1) {
+      ++launch_count();
+      k_bitonic_global<<<dim3(gb, nrows), SORT_THREADS, 0, stream>>>(keys, key_stride, P, size, j, rows);
+    }
+    ++launch_count();
+    k_bitonic_chunk<<<dim3(chunks, nrows), SORT_THREADS, CHUNK * 8, stream>>>(keys, key_stride,
+                                                                             static_cast<int>(size), size, rows);
+  }
+  const unsigned eb = static_cast<unsigned>(std::min<int64_t>((k + SORT_THREADS - 1) / SORT_THREADS, 1024));
+  ++launch_count();
+  k_emit<<<dim3(eb, nrows), SORT_THREADS, 0, stream>>>(keys, key_stride, k, rows, x, ld, n, out_vals, out_idx);
+}
+
+}  // namespace profk

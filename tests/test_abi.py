@@ -1,0 +1,91 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every declared
+symbol, and its host-only entry points (parameters, options, argument checks)
+agree with the oracle.  No call here launches device work."""
+import ctypes as C
+import re
+from pathlib import Path
+
+import pytest
+
+from oracle import params as P
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "profk.h"
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(profk_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_method(pk):
+    names = declared_functions()
+    for must in ("profk_topk", "profk_topk_batched", "profk_params", "profk_workspace_size",
+                 "profk_set_option", "profk_get_option", "profk_strerror", "profk_sample",
+                 "profk_threshold", "profk_filter", "profk_refine", "profk_exact"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(pk):
+    lib = pk.lib()
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_params_match_oracle(pk, mode):
+    for N in (1 << 20, 1 << 22, 1 << 26, 1 << 28, 1 << 30, 50331648, 1 << 24, 3_000_000_000, 1 << 32):
+        for k in (1, 2, 32, 64, 1024, 4096, 32768, 131072, 1 << 19):
+            for eps in (1e-3, 1e-3 / 64, 0.05):
+                if k > N:
+                    continue
+                assert pk.params(N, k, eps, mode) == P.params(N, k, eps, mode), (N, k, eps, mode)
+
+
+def test_options_roundtrip_and_validation(pk):
+    assert pk.get_option(pk.OPT_MAX_ATTEMPTS) == 6
+    pk.set_option(pk.OPT_MAX_ATTEMPTS, 2)
+    assert pk.get_option(pk.OPT_MAX_ATTEMPTS) == 2
+    with pytest.raises(pk.ProfkError):
+        pk.set_option(99, 1)
+    with pytest.raises(pk.ProfkError):
+        pk.set_option(pk.OPT_PARAM_MODE, 5)
+    with pytest.raises(pk.ProfkError):
+        pk.set_option(pk.OPT_FORCE_S, -1)
+
+
+def test_strerror(pk):
+    lib = pk.lib()
+    for code in range(-5, 1):
+        assert lib.profk_strerror(code)
+    assert b"NaN" in lib.profk_strerror(-3)
+
+
+def test_invalid_arguments_are_rejected_before_any_device_work(pk):
+    lib = pk.lib()
+    st = pk.ProfkStats()
+    assert lib.profk_topk(None, 10, 1, 1e-3, 0, None, None, None, C.byref(st)) == -1
+    fake = C.c_void_p(256)  # never dereferenced: the arguments fail validation first
+    assert lib.profk_topk(fake, 10, 0, 1e-3, 0, fake, fake, None, None) == -1
+    assert lib.profk_topk(fake, 10, 11, 1e-3, 0, fake, fake, None, None) == -1
+    assert lib.profk_topk(fake, 10, 1, 0.0, 0, fake, fake, None, None) == -1
+    assert lib.profk_topk(fake, 10, 1, 1.0, 0, fake, fake, None, None) == -1
+    assert lib.profk_topk(fake, (1 << 32) + 1, 1, 1e-3, 0, fake, fake, None, None) == -4
+    assert lib.profk_topk(C.c_void_p(258), 10, 1, 1e-3, 0, fake, fake, None, None) == -4
+    assert lib.profk_topk_batched(fake, 0, 10, 10, 1, 1e-3, 0, fake, fake, None, None) == -1
+    assert lib.profk_topk_batched(fake, 2, 10, 9, 1, 1e-3, 0, fake, fake, None, None) == -1
+    assert lib.profk_topk_batched(fake, 2, 10, 10, 1, 1e-3, 0, fake, fake, None, None) == -4  # ld % 4
+    assert lib.profk_sample(fake, 10, 6, 0, 0, 0, fake, fake, None) == -1
+    assert lib.profk_threshold(fake, 10, 11, fake, None) == -1
+    assert lib.profk_refine(fake, 5, 6, fake, 10, fake, fake, None) == -1
+    assert lib.profk_exact(fake, 10, 11, fake, fake, None) == -1
+    S, t, M = C.c_int64(), C.c_int64(), C.c_int64()
+    assert lib.profk_params(10, 11, 1e-3, 0, C.byref(S), C.byref(t), C.byref(M)) == -1
+
+
+def test_workspace_is_O_M_plus_S(pk):
+    small = pk.workspace_size(1, 1 << 26, 1024)
+    big = pk.workspace_size(1, 1 << 30, 1024)
+    assert 0 < big < 16 << 20  # megabytes, not a fraction of the 4 GiB input
+    assert big < 16 * small
+    assert pk.workspace_size(1, 10, 11) == 0

@@ -1,0 +1,161 @@
+"""The whole Prof-K call (profk_topk / profk_topk_batched) against the oracle.
+
+Besides the output (bit-exact values, indices and order), the per-attempt
+statistics must equal the oracle procedure's: the same draw stream gives the
+same sample, the same threshold and the same exact counts."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_helpers import assert_same
+from oracle import profk as PK
+from oracle.topk import topk_sort
+
+pytestmark = pytest.mark.gpu
+
+
+def check_call(pk, x, k, eps, seed, force=None, tie_exit=True, max_attempts=6):
+    if force:
+        pk.set_option(pk.OPT_FORCE_S, force.get("S", 0))
+        pk.set_option(pk.OPT_FORCE_T, force.get("t", 0))
+        pk.set_option(pk.OPT_FORCE_M, force.get("M", 0))
+    pk.set_option(pk.OPT_TIE_EXIT, int(tie_exit))
+    pk.set_option(pk.OPT_MAX_ATTEMPTS, max_attempts)
+    vals, idx, st = pk.topk(x, k, eps, seed)
+    h = x.cpu().numpy()
+    ov, oi, ost = PK.profk(h, k, eps, seed, force=force, tie_exit=tie_exit, max_attempts=max_attempts)
+    assert_same(vals, idx, ov, oi, f"n={h.size} k={k} seed={seed} force={force}")
+    assert (st["S"], st["t"], st["M"]) == (ost.S, ost.t, ost.M)
+    assert st["path"] == ost.path, (st, ost)
+    assert st["attempts"] == ost.attempts
+    assert st["R_first"] == ost.R_first and st["R_gt_first"] == ost.R_gt_first
+    assert st["R_final"] == ost.R_final and st["R_gt_final"] == ost.R_gt_final
+    if ost.taus:
+        assert st["tau_first"] == ost.taus[0]
+    return st
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_uniform_2p22_k32(pk, cuda_device, seed):
+    x = workloads.uniform(1 << 22, seed, cuda_device)
+    for s in range(4):
+        st = check_call(pk, x, 32, 1e-3, 1000 + s)
+        assert st["path"] == pk.PATH_FILTER
+
+
+@pytest.mark.parametrize("gen,n,k", [("normal", 1 << 20, 64), ("pareto", 3_000_017, 100), ("levels16", 1 << 21, 16),
+                                     ("ulps_below_one", 1 << 22, 64), ("sorted_normal", 1 << 22, 1000),
+                                     ("uniform", (1 << 23) + 5, 1)])
+def test_distributions(pk, cuda_device, gen, n, k):
+    x = workloads.GENERATORS[gen](n, n % 1000, cuda_device)
+    for s in range(3):
+        check_call(pk, x, k, 1e-3, 7 + s)
+
+
+@pytest.mark.parametrize("force,tie_exit,attempts", [
+    ({"S": 4096, "t": 4096, "M": 100}, True, 6),   # tau = sample min: overflow every attempt -> fallback
+    ({"S": 4096, "t": 1, "M": 40}, True, 6),       # tau = sample max: recall failure, redraws
+    ({"S": 4096, "t": 3, "M": 5000}, True, 6),
+    ({"S": 2048, "t": 2, "M": 64}, True, 2),
+    ({"S": 4096, "t": 5, "M": 3000}, False, 6),
+    ({"S": 4096, "t": 5, "M": 3000}, True, 0),     # straight to the exact fallback
+])
+def test_forced_paths(pk, cuda_device, force, tie_exit, attempts):
+    x = workloads.normal((1 << 20) + 3, 4, cuda_device)
+    for s in range(3):
+        check_call(pk, x, 32, 1e-3, 50 + s, force=force, tie_exit=tie_exit, max_attempts=attempts)
+
+
+@pytest.mark.parametrize("tie_exit", [True, False])
+def test_tie_path(pk, cuda_device, tie_exit):
+    # 40 distinct values above a level holding most of the input: tau lands on the
+    # level, R >> M while R_gt < k.
+    n, k = (1 << 20) + 11, 100
+    x = torch.full((n,), 0.5, device=cuda_device)
+    top = torch.randperm(n, device=cuda_device)[:40]
+    x[top] = torch.rand(40, device=cuda_device) + 1.0
+    x[torch.randperm(n, device=cuda_device)[:1000]] = 0.25
+    st = check_call(pk, x, k, 1e-3, 5, force={"S": 4096}, tie_exit=tie_exit)
+    assert st["path"] == (pk.PATH_TIE if tie_exit else pk.PATH_FALLBACK)
+
+
+def test_exact_route_small_inputs(pk, cuda_device):
+    for n, k in [(1, 1), (10, 3), (1000, 1000), (1 << 16, 64), (200_000, 5000)]:
+        x = workloads.normal(n, n, cuda_device)
+        vals, idx, st = pk.topk(x, k, 1e-3, 1)
+        assert st["path"] == pk.PATH_EXACT and st["attempts"] == 0
+        assert_same(vals, idx, *topk_sort(x.cpu().numpy(), k), f"exact route n={n} k={k}")
+
+
+def test_nan_rejected(pk, cuda_device):
+    x = workloads.normal(1 << 20, 3, cuda_device)
+    x[12345] = float("nan")
+    with pytest.raises(pk.ProfkError) as e:
+        pk.topk(x, 64, 1e-3, 1)
+    assert e.value.code == -3
+    y = workloads.normal(1000, 3, cuda_device)
+    y[3] = float("nan")
+    with pytest.raises(pk.ProfkError) as e:
+        pk.topk(y, 10, 1e-3, 1)
+    assert e.value.code == -3
+
+
+def test_special_values(pk, cuda_device):
+    n = 1 << 20
+    x = workloads.normal(n, 8, cuda_device)
+    x[:1000] = 0.0
+    x[1000:2000] = -0.0
+    x[5] = float("inf")
+    x[77] = float("inf")
+    x[9] = float("-inf")
+    for k in (1, 2, 3, 64):
+        check_call(pk, x, k, 1e-3, 3)
+    y = torch.zeros(n, device=cuda_device)
+    y[::2] = -0.0
+    check_call(pk, y, 64, 1e-3, 3, force={"S": 4096})
+
+
+def test_reproducible(pk, cuda_device):
+    x = workloads.normal(1 << 22, 1, cuda_device)
+    a = pk.topk(x, 1000, 1e-3, 42)
+    b = pk.topk(x, 1000, 1e-3, 42)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and a[2]["R_first"] == b[2]["R_first"]
+
+
+def test_nondefault_stream(pk, cuda_device):
+    x = workloads.normal(1 << 21, 2, cuda_device)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        vals, idx, st = pk.topk(x, 500, 1e-3, 9)
+    s.synchronize()
+    assert_same(vals, idx, *topk_sort(x.cpu().numpy(), 500), "side stream")
+
+
+@pytest.mark.parametrize("rows,n,ld,k", [(4, 1 << 20, 1 << 20, 16), (3, 1_000_003, 1_000_008, 100),
+                                         (16, 1 << 18, 1 << 18, 1), (2, 5000, 5000, 5000)])
+def test_batched(pk, cuda_device, rows, n, ld, k):
+    base = workloads.normal_rows(rows, ld, rows + n, cuda_device)
+    x = base[:, :n]
+    vals, idx, sts = pk.topk_batched(x, k, 1e-3, 11)
+    h = x.cpu().numpy()
+    eps_row = 1e-3 / rows
+    for r in range(rows):
+        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, eps_row, 11, row=r)
+        assert_same(vals[r], idx[r], ov, oi, f"batched row {r}")
+        assert sts[r]["path"] == ost.path and sts[r]["R_first"] == ost.R_first
+
+
+def test_batched_rows_retry_alone(pk, cuda_device):
+    # Forced parameters that make roughly half the rows fail their first attempt.
+    rows, n, k = 8, 1 << 18, 40
+    x = workloads.normal_rows(rows, n, 99, cuda_device)
+    force = {"S": 2048, "t": 1, "M": 2000}
+    for o, v in ((pk.OPT_FORCE_S, 2048), (pk.OPT_FORCE_T, 1), (pk.OPT_FORCE_M, 2000)):
+        pk.set_option(o, v)
+    vals, idx, sts = pk.topk_batched(x, k, 1e-3, 5)
+    h = x.cpu().numpy()
+    for r in range(rows):
+        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 5, row=r, force=force)
+        assert_same(vals[r], idx[r], ov, oi, f"row {r}")
+        assert (sts[r]["attempts"], sts[r]["path"], sts[r]["R_first"]) == (ost.attempts, ost.path, ost.R_first)
