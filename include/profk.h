@@ -53,7 +53,8 @@ typedef enum profk_status {
   PROFK_ERR_CUDA = -2,           /* a CUDA call failed; stats->cuda_error has the code */
   PROFK_ERR_NAN = -3,            /* the input holds a NaN */
   PROFK_ERR_UNSUPPORTED = -4,    /* e.g. n > 2^32 or a misaligned input */
-  PROFK_ERR_DEVICE_TIMEOUT = -5  /* a bounded device-side wait gave up */
+  PROFK_ERR_DEVICE_TIMEOUT = -5, /* a bounded device-side wait gave up */
+  PROFK_ERR_SCRATCH = -6         /* profk_topk_noalloc: the problem needs more than its fixed scratch */
 } profk_status;
 
 /* How a row's result was produced. */
@@ -194,6 +195,35 @@ int profk_refine(const uint64_t* keys, int64_t R, int64_t k, const float* x, int
  * and sort.  Returns PROFK_ERR_NAN if x holds a NaN (synchronizes stream). */
 int profk_exact(const float* x, int64_t n, int64_t k, float* out_vals, int64_t* out_idx,
                 cudaStream_t stream);
+
+/* ---- calls that allocate nothing --------------------------------------- */
+
+/* Bytes of the fixed device scratch array behind profk_topk_noalloc.  Every
+ * GPU that loads the library holds this much device memory until exit. */
+#define PROFK_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* Exact top-k of one row, with the same arguments, result and statistics as
+ * profk_topk, but without allocating anything: no cudaMalloc/cudaMallocAsync,
+ * no pinned host buffer, no pool.  The paper has no counterpart to this entry
+ * point; it exists for callers that must not allocate on the call path (a
+ * latency-bounded serving loop, a plugin whose host owns all device memory
+ * through its own allocator, a process whose pool already holds nearly all
+ * of the GPU).  The workspace is a static device array of
+ * PROFK_NOALLOC_SCRATCH_BYTES reserved when the library is loaded.
+ *   Limits: a problem whose workspace (profk_workspace_size(1, n, k, eps))
+ *     exceeds the array returns PROFK_ERR_SCRATCH before any device work.
+ *   Sharing: every call on a device uses the same array and finds the
+ *     previous call's contents there (it clears what must start at zero);
+ *     calls whose GPU work overlaps on one device race and must be ordered
+ *     by the caller (one stream, or serialized).
+ *   Set-up: the first call on a device looks up the array's device address
+ *     with that device current and caches it; make that first call before any
+ *     stream capture.
+ *   Options honoured: PROFK_OPT_PARAM_MODE, PROFK_OPT_MAX_ATTEMPTS,
+ *     PROFK_OPT_TIE_EXIT.  stats->aux_bytes is 0 (nothing was allocated). */
+int profk_topk_noalloc(const float* x, int64_t n, int64_t k, double eps, uint64_t seed,
+                       float* out_vals, int64_t* out_idx, cudaStream_t stream,
+                       profk_stats* stats);
 
 #ifdef __cplusplus
 }

@@ -598,6 +598,7 @@ const char* profk_strerror(int code) {
     case PROFK_ERR_NAN: return "input contains NaN";
     case PROFK_ERR_UNSUPPORTED: return "unsupported input (n > 2^32 or misaligned pointer / stride)";
     case PROFK_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case PROFK_ERR_SCRATCH: return "problem needs more workspace than the fixed scratch of profk_topk_noalloc";
     default: return "unknown status";
   }
 }
