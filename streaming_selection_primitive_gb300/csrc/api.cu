@@ -114,6 +114,40 @@ __global__ void k_attempt_init(RowState* st, const int* rows) {
   S.error = 0;
 }
 
+// Start of an attempt for the listed rows: hash table back to "empty",
+// counters to zero, and the selection state ready for tau (rank t).
+__global__ void k_attempt_reset(unsigned long long* table, int log2H, const int* rows, RowState* st,
+                                unsigned long long t) {
+  const int row = launch_row(rows);
+  unsigned long long* tb = table + (static_cast<int64_t>(row) << log2H);
+  const int64_t H = 1ll << log2H;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < H;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    tb[i] = ~0ull;
+  if (blockIdx.x == 0) {
+    RowState& S = st[row];
+    for (int b = threadIdx.x; b < HIST_BINS; b += blockDim.x) S.hist[b] = 0;
+    if (threadIdx.x == 0) {
+      S.R_ge = 0;
+      S.R_gt = 0;
+      S.nan = 0;
+      S.distinct = 0;
+      S.error = 0;
+      S.sel_prefix = 0;
+      S.sel_rank = t;
+      S.sel_above = 0;
+      S.sel_bucket = 0;
+      S.sel_thresh = 0;
+      S.sel_nan = 0;
+      S.sel_bits = 0;
+      S.sel_done = 0;
+      S.done_blocks = 0;
+      S.compact_count = 0;
+      S.skip = 0;
+    }
+  }
+}
+
 // Hash tables of the listed rows back to "empty".
 __global__ void k_reset_tables(unsigned long long* table, int log2H, const int* rows) {
   const int row = launch_row(rows);
@@ -383,17 +417,15 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
       const int64_t H = 1ll << L.log2H;
       const unsigned rb = static_cast<unsigned>(std::min<int64_t>((H + 1023) / 1024, 256));
       ++launch_count();
-      k_reset_tables<<<dim3(rb, ng), 1024, 0, stream>>>(at<unsigned long long>(c.ws, L.off_table), L.log2H, gl);
-      ++launch_count();
-      k_attempt_init<<<ng, 1, 0, stream>>>(st, gl);
+      k_attempt_reset<<<dim3(rb, ng), 1024, 0, stream>>>(at<unsigned long long>(c.ws, L.off_table), L.log2H, gl, st,
+                                                        static_cast<unsigned long long>(P.t));
       SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, a, ng, gl, st,
                     at<unsigned long long>(c.ws, L.off_table), at<uint32_t>(c.ws, L.off_draws),
                     at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
                     at<uint32_t>(c.ws, L.off_skeys)};
       launch_sample(sa, stream);
       SelectArgs ta{KeySource::SampleKeys, at<uint32_t>(c.ws, L.off_skeys), P.S, P.S, ng, gl, st};
-      launch_select(ta, static_cast<uint64_t>(P.t), true, 0, stream);
-      launch_store_tau(ng, gl, st, stream);
+      launch_select(ta, 0, true, 0, stream);  // its last pass stores tau
       const bool time_it = timing && first_filter;
       if (time_it) {
         if (!t_events.a) {
@@ -405,6 +437,18 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
       FilterArgs fa{x, ld, n, P.M, ng, gl, st, at<unsigned long long>(c.ws, L.off_buf), filter_grid(cps)};
       launch_filter(fa, stream);
       if (time_it) PK_CHECK(cudaEventRecord(t_events.b, stream));
+      // Refinement, launched before the host has seen the counts: a row whose
+      // count fails the check is voided on the device and left untouched, so
+      // the host round trip of the check is off the critical path of the
+      // (likely) successful attempt.
+      {
+        launch_refine_init(ng, gl, st, k, P.M, stream);
+        SelectArgs ra{KeySource::Buffer, at<unsigned long long>(c.ws, L.off_buf), P.M, P.M, ng, gl, st};
+        uint64_t* sel = at<uint64_t>(c.ws, L.off_sel);
+        launch_select(ra, 0, false, 0, stream);
+        launch_compact(ra, sel, L.kstride, k, stream);
+        launch_sort_emit(sel, L.kstride, k, ng, gl, x, ld, n, out_vals, out_idx, stream, st);
+      }
       PK_CHECK(cudaGetLastError());
       // Run-time check: read the exact counts of every row.
       char* rep = static_cast<char*>(hbuf) + sizeof(int) * rows * 4;
@@ -415,7 +459,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         PK_CHECK(cudaEventElapsedTime(&filter_ms, t_events.a, t_events.b));
         first_filter = false;
       }
-      std::vector<int> ok, tie;
+      std::vector<int> tie;
       bool grow = false;
       for (int r : group) {
         const char* h = rep + REPORT_BYTES * r;
@@ -459,8 +503,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         s.R_gt_final = static_cast<int64_t>(Rt);
         s.tau_final = tau;
         if (static_cast<uint64_t>(k) <= Rg && Rg <= static_cast<uint64_t>(P.M)) {
-          s.path = PROFK_PATH_FILTER;
-          ok.push_back(r);
+          s.path = PROFK_PATH_FILTER;  // refined on the device already
         } else if (tie_exit && Rg > static_cast<uint64_t>(P.M) && Rt < static_cast<uint64_t>(k)) {
           s.path = PROFK_PATH_TIE;
           tie.push_back(r);
@@ -468,16 +511,6 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
           attempt[r] = a + 1;
           next.push_back(r);
         }
-      }
-      if (!ok.empty()) {
-        int* ol = nullptr;
-        PK_CHECK(upload_rows(L, c.ws, hbuf, 1, ok, stream, &ol));
-        SelectArgs ra{KeySource::Buffer, at<unsigned long long>(c.ws, L.off_buf), P.M, P.M,
-                      static_cast<int>(ok.size()), ol, st};
-        uint64_t* sel = at<uint64_t>(c.ws, L.off_sel);
-        launch_select(ra, static_cast<uint64_t>(k), false, 0, stream);
-        launch_compact(ra, sel, L.kstride, k, stream);
-        launch_sort_emit(sel, L.kstride, k, static_cast<int>(ok.size()), ol, x, ld, n, out_vals, out_idx, stream);
       }
       if (!tie.empty()) {
         int* tl = nullptr;
@@ -487,7 +520,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         uint64_t* sel = at<uint64_t>(c.ws, L.off_sel);
         launch_select(ia, 0, false, 3, stream);
         launch_compact(ia, sel, L.kstride, k, stream);
-        launch_sort_emit(sel, L.kstride, k, static_cast<int>(tie.size()), tl, x, ld, n, out_vals, out_idx, stream);
+        launch_sort_emit(sel, L.kstride, k, static_cast<int>(tie.size()), tl, x, ld, n, out_vals, out_idx, stream, st);
       }
       PK_CHECK(cudaGetLastError());
       if (grow) {

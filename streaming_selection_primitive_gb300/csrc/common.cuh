@@ -116,7 +116,7 @@ struct RowState {
   unsigned int done_blocks;       // last-block-done ticket
   unsigned int compact_count;     // output cursor of the compaction
   unsigned int error;             // nonzero: a device-side check failed
-  unsigned int pad;
+  unsigned int skip;              // 1: this row's refinement is void (its attempt failed the check)
   unsigned int hist[HIST_BINS];
 };
 

@@ -1,22 +1,25 @@
 // Step 3 of Prof-K, the filter pass ("Prof-K: Probabilistic One-Pass Filtering
 // for Efficient Top-k Selection", Section 3, stage 3, and Appendix C "The
 // Filter Kernel"): stream x once, count R = |{x_i >= tau}| exactly and append
-// the passers to a buffer of capacity M, one atomic reservation per block.
+// the passers to a buffer of capacity M.
 //
-// GB300 design.  The pass is a pure HBM read stream, so the kernel is built to
-// keep as many 16-byte loads in flight as the memory system wants and to do
-// almost nothing else on the common path:
-//  * persistent grid of resident CTAs striding over tiles of THREADS*4*U
-//    floats; each thread issues U independent 128-bit non-allocating loads;
-//  * fast path: one NaN-propagating max over the thread's 4U values and a
-//    single compare against tau (a NaN or a passer sends the block to the slow
-//    path, NaNs are then counted and reported);
-//  * slow path (any passer in the tile): per-element >= / > / NaN tests, a warp
-//    scan of the passer counts, one shared scan of the warp totals and ONE
-//    global atomicAdd per tile on the row's R counter, whose old value is the
-//    slot of the tile's first passer.  Stores are masked to M, the counter
-//    keeps counting past it, exactly as the pages' kernel does;
-//  * R_gt and the NaN count are per-thread registers reduced once per row.
+// GB300 design.  The pass is a pure HBM read stream, so the kernel keeps as
+// many 16-byte loads in flight as the memory system wants and does almost
+// nothing else on the common path, with no block-wide barrier anywhere:
+//  * persistent grid of resident CTAs; every warp strides on its own over
+//    warp tiles of 32 lanes x U float4 (4U values per lane), issuing U
+//    independent 128-bit non-allocating loads per lane;
+//  * fast path: a NaN-propagating max over the lane's 4U values, one compare
+//    against tau and one warp vote;
+//  * slow path (some lane holds a passer or a NaN): per-element >= / > / NaN
+//    tests into a 64-bit lane mask, a warp scan of the passer counts and ONE
+//    atomicAdd per warp tile on the row's counter, whose old value is the
+//    slot of the tile's first passer.  Stores are masked to M and the counter
+//    keeps counting, as in the pages' kernel.  Once a warp sees the counter
+//    pass M it counts the rest in a register (no more atomics, no stores), so
+//    tie-heavy inputs that overflow the buffer do not serialize on the counter;
+//  * R_gt, the NaN count and those late passers are per-lane registers,
+//    reduced once per row per warp.
 // A passer (v, i) is stored as the 64-bit key (ord(v) << 32) | ~i, the order
 // the refinement sorts by.
 #include "kernels.h"
@@ -42,8 +45,8 @@ __device__ __forceinline__ float comp(const float4& v, int c) {
   return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
 }
 
-template <int T>
-__device__ __forceinline__ void flush_row(RowState& S, unsigned long long& gt, unsigned long long& nan) {
+__device__ __forceinline__ void flush_row(RowState& S, unsigned long long& gt, unsigned long long& nan,
+                                          unsigned long long& late) {
   unsigned long long g = gt, q = nan;
   for (int o = 16; o; o >>= 1) {
     g += __shfl_down_sync(FULL_MASK, g, o);
@@ -52,106 +55,47 @@ __device__ __forceinline__ void flush_row(RowState& S, unsigned long long& gt, u
   if ((threadIdx.x & 31) == 0) {
     if (g) atomicAdd(&S.R_gt, g);
     if (q) atomicAdd(&S.nan, q);
+    if (late) atomicAdd(&S.R_ge, late);
   }
   gt = 0;
   nan = 0;
-}
-
-// Processes one tile whose values sit in v[] (U float4 per thread).  `valid`
-// marks real elements (all of them except in a row's last, partial tile).
-template <int T, int U>
-__device__ __forceinline__ void tile_slow(const float4 (&v)[U], uint64_t valid, bool hit, float tau, int64_t base,
-                                          RowState& S, unsigned long long* buf, int64_t M, unsigned long long& gt,
-                                          unsigned long long& nan, unsigned* s_warp, unsigned long long* s_gbase) {
-  constexpr int NW = T / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint64_t ge = 0;
-  if (hit) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int e = u * 4 + c;
-        const float f = comp(v[u], c);
-        const bool ok = (valid >> e) & 1ull;
-        ge |= static_cast<uint64_t>(ok && f >= tau) << e;
-        gt += (ok && f > tau);
-        nan += (ok && f != f);
-      }
-    }
-  }
-  const unsigned cnt = __popcll(ge);
-  unsigned incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const unsigned w = lane < NW ? s_warp[lane] : 0u;
-    unsigned wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned t = __shfl_up_sync(FULL_MASK, wi, o);
-      if (lane >= o) wi += t;
-    }
-    if (lane < NW) s_warp[lane] = wi - w;
-    const unsigned total = __shfl_sync(FULL_MASK, wi, 31);
-    if (lane == 0) *s_gbase = total ? atomicAdd(&S.R_ge, static_cast<unsigned long long>(total)) : 0ull;
-  }
-  __syncthreads();
-  if (cnt) {
-    unsigned long long pos = *s_gbase + s_warp[warp] + incl - cnt;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int e = u * 4 + c;
-        if ((ge >> e) & 1ull) {
-          if (pos < static_cast<unsigned long long>(M)) {
-            const int64_t idx = base + (static_cast<int64_t>(u) * T + threadIdx.x) * 4 + c;
-            buf[pos] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
-          }
-          ++pos;
-        }
-      }
-    }
-  }
+  late = 0;
 }
 
 template <int T, int U>
 __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
-  static_assert(4 * U <= 64, "at most 64 elements per thread");
-  constexpr int64_t TILE = static_cast<int64_t>(T) * 4 * U;
-  __shared__ unsigned s_warp[T / 32];
-  __shared__ unsigned long long s_gbase;
-  const int64_t tiles_per_row = (a.n + TILE - 1) / TILE;
+  static_assert(4 * U <= 64, "at most 64 elements per lane");
+  constexpr int64_t WT = 32 * 4 * U;  // elements per warp tile
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (T / 32);
+  const int64_t tiles_per_row = (a.n + WT - 1) / WT;
   const int64_t total = tiles_per_row * a.nrows;
   int cur = -1;
   int row = 0;
   float tau = 0.f;
+  bool over = false;  // this warp saw the row's counter pass M
   const float* xr = nullptr;
   unsigned long long* br = nullptr;
-  unsigned long long gt = 0, nan = 0;
-  for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+  unsigned long long gt = 0, nan = 0, late = 0;
+  for (int64_t tile = static_cast<int64_t>(blockIdx.x) * (T / 32) + (threadIdx.x >> 5); tile < total;
+       tile += nwarps) {
     const int ri = static_cast<int>(tile / tiles_per_row);
-    const int64_t base = (tile - static_cast<int64_t>(ri) * tiles_per_row) * TILE;
+    const int64_t base = (tile - static_cast<int64_t>(ri) * tiles_per_row) * WT;
     if (ri != cur) {
-      if (cur >= 0) flush_row<T>(a.st[row], gt, nan);
+      if (cur >= 0) flush_row(a.st[row], gt, nan, late);
       cur = ri;
       row = a.rows ? a.rows[ri] : ri;
       tau = key_to_float(a.st[row].tau_key);
       xr = a.x + static_cast<int64_t>(row) * a.ld;
       br = a.buf + static_cast<int64_t>(row) * a.M;
+      over = false;
     }
     float4 v[U];
     uint64_t valid = ~0ull;
-    if (base + TILE <= a.n) {
-      const float4* p = reinterpret_cast<const float4*>(xr + base) + threadIdx.x;
+    if (base + WT <= a.n) {
+      const float4* p = reinterpret_cast<const float4*>(xr + base) + lane;
 #pragma unroll
-      for (int u = 0; u < U; ++u) v[u] = ld_stream(p + u * T);
+      for (int u = 0; u < U; ++u) v[u] = ld_stream(p + u * 32);
     } else {
       valid = 0;
 #pragma unroll
@@ -159,7 +103,7 @@ __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
         float f[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int64_t i = base + (static_cast<int64_t>(u) * T + threadIdx.x) * 4 + c;
+          const int64_t i = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
           const bool ok = i < a.n;
           f[c] = ok ? xr[i] : -INFINITY;
           valid |= static_cast<uint64_t>(ok) << (u * 4 + c);
@@ -170,16 +114,72 @@ __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
     float m = max_nan(max_nan(v[0].x, v[0].y), max_nan(v[0].z, v[0].w));
 #pragma unroll
     for (int u = 1; u < U; ++u) m = max_nan(m, max_nan(max_nan(v[u].x, v[u].y), max_nan(v[u].z, v[u].w)));
-    // Masked lanes hold -inf; they can reach the slow path only when tau is
-    // -inf, and `valid` keeps them out of every count there.
+    // Masked lanes hold -inf; they reach the slow path only when tau is -inf,
+    // and `valid` keeps them out of every count there.
     const bool hit = !(m < tau);
-    if (__syncthreads_or(hit)) tile_slow<T, U>(v, valid, hit, tau, base, a.st[row], br, a.M, gt, nan, s_warp, &s_gbase);
+    if (!__any_sync(FULL_MASK, hit)) continue;
+    uint64_t ge = 0;
+    if (hit) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int e = u * 4 + c;
+          const float f = comp(v[u], c);
+          const bool ok = (valid >> e) & 1ull;
+          ge |= static_cast<uint64_t>(ok && f >= tau) << e;
+          gt += (ok && f > tau);
+          nan += (ok && f != f);
+        }
+      }
+    }
+    const unsigned cnt = __popcll(ge);
+    unsigned incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned tot = __shfl_sync(FULL_MASK, incl, 31);
+    if (tot == 0) continue;
+    if (over) {
+      if (lane == 0) late += tot;
+      continue;
+    }
+    unsigned long long gbase = 0;
+    if (lane == 0) gbase = atomicAdd(&a.st[row].R_ge, static_cast<unsigned long long>(tot));
+    gbase = __shfl_sync(FULL_MASK, gbase, 0);
+    if (gbase + tot > static_cast<unsigned long long>(a.M)) over = true;
+    if (cnt && gbase < static_cast<unsigned long long>(a.M)) {
+      unsigned long long pos = gbase + incl - cnt;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int e = u * 4 + c;
+          if ((ge >> e) & 1ull) {
+            if (pos < static_cast<unsigned long long>(a.M)) {
+              const int64_t idx = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
+              br[pos] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
+            }
+            ++pos;
+          }
+        }
+      }
+    }
   }
-  if (cur >= 0) flush_row<T>(a.st[row], gt, nan);
+  if (cur >= 0) flush_row(a.st[row], gt, nan, late);
 }
 
-constexpr int FT = 256;
-constexpr int FU = 16;
+// Launch shape: threads per CTA and 16-byte loads per lane per warp tile.
+#ifndef PROFK_FILTER_THREADS
+#define PROFK_FILTER_THREADS 256
+#endif
+#ifndef PROFK_FILTER_VEC
+#define PROFK_FILTER_VEC 8
+#endif
+constexpr int FT = PROFK_FILTER_THREADS;
+constexpr int FU = PROFK_FILTER_VEC;
 
 }  // namespace
 
@@ -191,10 +191,11 @@ int filter_default_grid(int sms) {
 }
 
 void launch_filter(const FilterArgs& a, cudaStream_t stream) {
-  const int64_t TILE = static_cast<int64_t>(FT) * 4 * FU;
-  const int64_t tiles = ((a.n + TILE - 1) / TILE) * a.nrows;
+  const int64_t WT = 32 * 4 * FU;
+  const int64_t warp_tiles = ((a.n + WT - 1) / WT) * a.nrows;
+  const int64_t ctas = (warp_tiles + FT / 32 - 1) / (FT / 32);
   int grid = a.grid;
-  if (tiles < grid) grid = static_cast<int>(tiles);
+  if (ctas < grid) grid = static_cast<int>(ctas);
   if (grid < 1) grid = 1;
   ++launch_count();
   k_filter<FT, FU><<<grid, FT, 0, stream>>>(a);

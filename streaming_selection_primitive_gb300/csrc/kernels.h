@@ -62,6 +62,9 @@ void launch_select(const SelectArgs& a, uint64_t init_rank, bool value_only, int
                    cudaStream_t stream);
 // Resolved value key of the tau selection into RowState::tau_key.
 void launch_store_tau(int nrows, const int* rows, RowState* st, cudaStream_t stream);
+// Refinement set-up straight after the filter: rows whose count fails
+// k <= R <= M are marked void on the device (their refinement writes nothing).
+void launch_refine_init(int nrows, const int* rows, RowState* st, int64_t k, int64_t M, cudaStream_t stream);
 // Tie path: set the state to "value ord(tau) resolved, rank k - R_gt left".
 void launch_tie_init(int nrows, const int* rows, RowState* st, int64_t k, cudaStream_t stream);
 
@@ -71,9 +74,10 @@ void launch_compact(const SelectArgs& a, uint64_t* out, int64_t out_stride, int6
 
 // Sorts each row's k keys descending (in place in `keys`, row stride
 // key_stride >= next_pow2(k)) and writes values (read from x) and indices.
+// Rows whose state says skip are left untouched when st is given.
 void launch_sort_emit(uint64_t* keys, int64_t key_stride, int64_t k, int nrows, const int* rows,
                       const float* x, int64_t ld, int64_t n, float* out_vals, int64_t* out_idx,
-                      cudaStream_t stream);
+                      cudaStream_t stream, const RowState* st = nullptr);
 int64_t sort_stride(int64_t k);  // key_stride the sort needs for k keys
 
 // Filter pass.

@@ -27,52 +27,46 @@ __device__ __forceinline__ uint64_t hash_slot(uint32_t u, int log2H) {
 }
 
 __global__ void __launch_bounds__(256) k_sample_draw(SampleArgs a, int64_t key_row0) {
+  // One draw per thread: the four lanes that share a Philox block each
+  // compute it (cheap arithmetic) and keep their own word, so every hash
+  // insertion proceeds in parallel.
   const int row = launch_row(a.rows);
-  const int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // Philox block
-  if (4 * q >= a.D) return;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= a.D) return;
   const uint64_t H = 1ull << a.log2H;
   unsigned long long* table = a.table + static_cast<int64_t>(row) * H;
-  uint32_t* draws = a.draws + static_cast<int64_t>(row) * a.D;
   const uint64_t k0 = a.seed, k1 = static_cast<uint64_t>(row + key_row0);
-  uint64_t w[4] = {static_cast<uint64_t>(q), static_cast<uint64_t>(a.attempt), 0ull, 0ull};
+  const uint64_t q = static_cast<uint64_t>(i >> 2);
+  const int e = static_cast<int>(i & 3);
+  uint64_t w[4] = {q, static_cast<uint64_t>(a.attempt), 0ull, 0ull};
   philox4x64_10(w, k0, k1);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int64_t i = 4 * q + e;
-    if (i >= a.D) break;
-    uint64_t u;
-    if (!lemire64(w[e], a.n, &u)) {
-      bool ok = false;
-      for (uint64_t j = 1; j <= 64 && !ok; ++j) {
-        uint64_t c[4] = {static_cast<uint64_t>(q), static_cast<uint64_t>(a.attempt), j, 0ull};
-        philox4x64_10(c, k0, k1);
-        ok = lemire64(c[e], a.n, &u);
-      }
-      if (!ok) {  // probability below (n / 2^64)^64: record, never hang
-        atomicOr(&a.st[row].error, 1u);
-        u = 0;
-      }
+  uint64_t u;
+  if (!lemire64(w[e], a.n, &u)) {
+    bool ok = false;
+    for (uint64_t j = 1; j <= 64 && !ok; ++j) {
+      uint64_t c[4] = {q, static_cast<uint64_t>(a.attempt), j, 0ull};
+      philox4x64_10(c, k0, k1);
+      ok = lemire64(c[e], a.n, &u);
     }
-    const uint32_t u32 = static_cast<uint32_t>(u);
-    draws[i] = u32;
-    const unsigned long long entry = (static_cast<unsigned long long>(u32) << 32) | static_cast<uint32_t>(i);
-    uint64_t slot = hash_slot(u32, a.log2H);
-    bool placed = false;
-    for (uint64_t probe = 0; probe < H; ++probe) {
-      const unsigned long long prev = atomicCAS(table + slot, EMPTY_SLOT, entry);
-      if (prev == EMPTY_SLOT) {
-        placed = true;
-        break;
-      }
-      if (static_cast<uint32_t>(prev >> 32) == u32) {
-        atomicMin(table + slot, entry);
-        placed = true;
-        break;
-      }
-      slot = (slot + 1) & (H - 1);
+    if (!ok) {  // probability below (n / 2^64)^64: record, never hang
+      atomicOr(&a.st[row].error, 1u);
+      u = 0;
     }
-    if (!placed) atomicOr(&a.st[row].error, 2u);
   }
+  const uint32_t u32 = static_cast<uint32_t>(u);
+  a.draws[static_cast<int64_t>(row) * a.D + i] = u32;
+  const unsigned long long entry = (static_cast<unsigned long long>(u32) << 32) | static_cast<uint32_t>(i);
+  uint64_t slot = hash_slot(u32, a.log2H);
+  for (uint64_t probe = 0; probe < H; ++probe) {
+    const unsigned long long prev = atomicCAS(table + slot, EMPTY_SLOT, entry);
+    if (prev == EMPTY_SLOT) return;
+    if (static_cast<uint32_t>(prev >> 32) == u32) {
+      atomicMin(table + slot, entry);
+      return;
+    }
+    slot = (slot + 1) & (H - 1);
+  }
+  atomicOr(&a.st[row].error, 2u);
 }
 
 __device__ __forceinline__ uint32_t first_position(const unsigned long long* table, int log2H, uint32_t u) {
@@ -158,7 +152,7 @@ __global__ void __launch_bounds__(MARK_THREADS) k_sample_compact(SampleArgs a) {
 }  // namespace
 
 void launch_sample_rows(const SampleArgs& a, int64_t key_row0, cudaStream_t stream) {
-  const int64_t blocks = ((a.D + 3) / 4 + 255) / 256;
+  const int64_t blocks = (a.D + 255) / 256;
   ++launch_count();
   k_sample_draw<<<dim3(static_cast<unsigned>(blocks), a.nrows), 256, 0, stream>>>(a, key_row0);
   const unsigned nb = static_cast<unsigned>((a.D + MARK_THREADS - 1) / MARK_THREADS);

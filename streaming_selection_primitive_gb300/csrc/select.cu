@@ -68,6 +68,31 @@ __global__ void k_sel_init(RowState* st, const int* rows, unsigned long long ran
     S.sel_done = 0;
     S.done_blocks = 0;
     S.compact_count = 0;
+    S.skip = 0;
+  }
+}
+
+// Refinement set-up, run right after the filter without waiting for the host:
+// a row whose count fails the check k <= R <= M is marked void (skip = 1), so
+// that every later refinement kernel leaves it and its outputs alone.
+__global__ void k_refine_init(RowState* st, const int* rows, unsigned long long k, unsigned long long M) {
+  const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
+  RowState& S = st[row];
+  for (int b = threadIdx.x; b < HIST_BINS; b += blockDim.x) S.hist[b] = 0;
+  if (threadIdx.x == 0) {
+    const unsigned long long R = S.R_ge;
+    const bool ok = k <= R && R <= M;
+    S.sel_prefix = 0;
+    S.sel_rank = k;
+    S.sel_above = 0;
+    S.sel_bucket = 0;
+    S.sel_thresh = ok ? 0ull : ~0ull;
+    S.sel_nan = 0;
+    S.sel_bits = 0;
+    S.sel_done = ok ? 0 : 1;
+    S.done_blocks = 0;
+    S.compact_count = 0;
+    S.skip = ok ? 0u : 1u;
   }
 }
 
@@ -86,6 +111,7 @@ __global__ void k_tie_init(RowState* st, const int* rows, unsigned long long k) 
     S.sel_done = 0;
     S.done_blocks = 0;
     S.compact_count = 0;
+    S.skip = 0;
   }
 }
 
@@ -184,6 +210,7 @@ __global__ void __launch_bounds__(SEL_THREADS) k_radix_pass(Src src, RowState* s
         if (shift == final_shift || (!value_only && c == rank - acc)) {
           S.sel_done = 1;
           S.sel_thresh = np << shift;
+          if (value_only) S.tau_key = static_cast<uint32_t>(np);  // the threshold of step 2
         }
         break;
       }
@@ -207,7 +234,7 @@ __global__ void __launch_bounds__(SEL_THREADS) k_compact(Src src, RowState* st, 
                                                         unsigned long long* out, int64_t out_stride, int64_t k) {
   const int row = launch_row(rows);
   RowState& S = st[row];
-  if (!S.sel_done) return;
+  if (!S.sel_done || S.skip) return;
   const unsigned long long thresh = S.sel_thresh;
   const int64_t len = src.length(S);
   const int lane = threadIdx.x & 31;
@@ -250,9 +277,10 @@ __device__ __forceinline__ void emit_one(const unsigned long long key, int row, 
 __global__ void __launch_bounds__(SORT_THREADS) k_sort_small(const unsigned long long* keys, int64_t key_stride,
                                                             int64_t k, int P, const int* rows, const float* x,
                                                             int64_t ld, int64_t n, float* out_vals,
-                                                            int64_t* out_idx) {
+                                                            int64_t* out_idx, const RowState* st) {
   extern __shared__ unsigned long long s[];
   const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
+  if (st && st[row].skip) return;
   const unsigned long long* kr = keys + row * key_stride;
   for (int i = threadIdx.x; i < P; i += blockDim.x) s[i] = i < k ? kr[i] : 0ull;
   __syncthreads();
@@ -335,8 +363,9 @@ __global__ void __launch_bounds__(SORT_THREADS) k_bitonic_global(unsigned long l
 
 __global__ void __launch_bounds__(SORT_THREADS) k_emit(const unsigned long long* keys, int64_t key_stride, int64_t k,
                                                        const int* rows, const float* x, int64_t ld, int64_t n,
-                                                       float* out_vals, int64_t* out_idx) {
+                                                       float* out_vals, int64_t* out_idx, const RowState* st) {
   const int row = launch_row(rows);
+  if (st && st[row].skip) return;
   for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < k;
        j += static_cast<int64_t>(gridDim.x) * blockDim.x)
     emit_one(keys[row * key_stride + j], row, j, k, x, ld, n, out_vals, out_idx);
@@ -407,6 +436,12 @@ void launch_store_tau(int nrows, const int* rows, RowState* st, cudaStream_t str
   k_store_tau<<<nrows, 32, 0, stream>>>(st, rows);
 }
 
+void launch_refine_init(int nrows, const int* rows, RowState* st, int64_t k, int64_t M, cudaStream_t stream) {
+  ++launch_count();
+  k_refine_init<<<nrows, 256, 0, stream>>>(st, rows, static_cast<unsigned long long>(k),
+                                           static_cast<unsigned long long>(M));
+}
+
 void launch_tie_init(int nrows, const int* rows, RowState* st, int64_t k, cudaStream_t stream) {
   ++launch_count();
   k_tie_init<<<nrows, 256, 0, stream>>>(st, rows, static_cast<unsigned long long>(k));
@@ -438,13 +473,15 @@ void launch_compact(const SelectArgs& a, uint64_t* out, int64_t out_stride, int6
 int64_t sort_stride(int64_t k) { return k > SMALL_SORT_MAX ? next_pow2(k) : k; }
 
 void launch_sort_emit(uint64_t* keys_u, int64_t key_stride, int64_t k, int nrows, const int* rows, const float* x,
-                      int64_t ld, int64_t n, float* out_vals, int64_t* out_idx, cudaStream_t stream) {
+                      int64_t ld, int64_t n, float* out_vals, int64_t* out_idx, cudaStream_t stream,
+                      const RowState* st) {
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(keys_u);
   if (k <= SMALL_SORT_MAX) {
     cudaFuncSetAttribute(k_sort_small, cudaFuncAttributeMaxDynamicSharedMemorySize, SMALL_SORT_MAX * 8);
     const int P = static_cast<int>(next_pow2(k));
     ++launch_count();
-    k_sort_small<<<nrows, SORT_THREADS, P * 8, stream>>>(keys, key_stride, k, P, rows, x, ld, n, out_vals, out_idx);
+    k_sort_small<<<nrows, SORT_THREADS, P * 8, stream>>>(keys, key_stride, k, P, rows, x, ld, n, out_vals, out_idx,
+                                                         st);
     return;
   }
   const int64_t P = next_pow2(k);  // >= 2 * CHUNK here
@@ -467,7 +504,7 @@ void launch_sort_emit(uint64_t* keys_u, int64_t key_stride, int64_t k, int nrows
   }
   const unsigned eb = static_cast<unsigned>(std::min<int64_t>((k + SORT_THREADS - 1) / SORT_THREADS, 1024));
   ++launch_count();
-  k_emit<<<dim3(eb, nrows), SORT_THREADS, 0, stream>>>(keys, key_stride, k, rows, x, ld, n, out_vals, out_idx);
+  k_emit<<<dim3(eb, nrows), SORT_THREADS, 0, stream>>>(keys, key_stride, k, rows, x, ld, n, out_vals, out_idx, st);
 }
 
 }  // namespace profk
