@@ -260,6 +260,13 @@ def main():
     achieved = 4.0 * n / (f_ms / 1e3) / 1e9
     traffic = traffic_from_profile(n)
     aux = pk.topk(x, k, EPS, 7, out=out)[2]["aux_bytes"]
+    # Stage breakdown from the library's own events, in separate untimed calls.
+    stage_acc = {}
+    for s in range(10):
+        pk.topk(x, k, EPS, 60_000 + s, out=out)
+        for name, ms in pk.last_stage_ms().items():
+            stage_acc.setdefault(name, []).append(ms)
+    stages = {name: round(statistics.mean(v), 4) for name, v in stage_acc.items()}
 
     # End to end through the C-ABI with host buffers.
     pk.set_option(pk.OPT_TIMING, 0)
@@ -328,6 +335,7 @@ def main():
                          "kernel": "k_filter", "bytes_per_launch": 4 * n, "mean_launch_ms": round(f_ms, 4)},
             "e2e": {"value": round(e2e_value, 3), "unit": "Gelem/s", "h2d_bytes_per_step": 4 * n,
                     "d2h_bytes_per_step": 12 * k, "ms_per_step": round(e2e_ms / args.e2e_steps, 3)},
+            "stages_ms": stages,
             "gpu_launches": launches,
             "retries": int(sum(a - 1 for a in attempts if a > 0)),
             "aux_bytes": aux,

@@ -151,6 +151,15 @@ typedef enum profk_option {
 int profk_set_option(int option, int64_t value);
 int64_t profk_get_option(int option);
 
+/* Stage times (ms) of the first filter attempt of this host thread's last
+ * profk_topk / profk_topk_batched call made with PROFK_OPT_TIMING on, from
+ * CUDA events on the call's stream: out[0] sampling, out[1] threshold
+ * selection, out[2] filter, out[3] refinement (enqueued before the check),
+ * out[4] read-back of the counts; out[5] is the host wall time of the whole
+ * call.  Writes min(count, 6) values (-1 where not measured) and returns that
+ * number, or PROFK_ERR_INVALID. */
+int profk_last_stage_ms(float* out, int count);
+
 /* Static description of a status code. */
 const char* profk_strerror(int code);
 

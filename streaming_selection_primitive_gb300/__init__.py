@@ -17,7 +17,8 @@ from ._abi import (OPT_FILTER_CTAS_PER_SM, OPT_FORCE_M, OPT_FORCE_S, OPT_FORCE_T
                    PATH_FALLBACK, PATH_FILTER, PATH_TIE, ProfkError, ProfkStats)
 
 __all__ = ["topk", "topk_batched", "params", "workspace_size", "set_option", "get_option", "reset_options",
-           "sample", "threshold", "filter_pass", "refine", "exact", "ProfkError", "ProfkStats", "lib"]
+           "sample", "threshold", "filter_pass", "refine", "exact", "last_stage_ms", "ProfkError", "ProfkStats",
+           "lib"]
 
 
 def lib():
@@ -63,6 +64,16 @@ def get_option(option: int) -> int:
 def reset_options() -> None:
     for o, v in _abi.OPT_DEFAULTS.items():
         set_option(o, v)
+
+
+STAGES = ("sample", "threshold", "filter", "refine", "readback", "call_wall")
+
+
+def last_stage_ms() -> dict:
+    """Stage times of this thread's last timed call (PROFK_OPT_TIMING on)."""
+    buf = (C.c_float * 6)()
+    m = lib().profk_last_stage_ms(buf, 6)
+    return {STAGES[i]: buf[i] for i in range(max(m, 0))}
 
 
 def topk(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=None):

@@ -69,6 +69,7 @@ _SIGS = {
     "profk_refine": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int64, C.c_void_p,
                                C.c_void_p, C.c_void_p]),
     "profk_exact": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "profk_last_stage_ms": (C.c_int, [C.POINTER(C.c_float), C.c_int]),
 }
 
 

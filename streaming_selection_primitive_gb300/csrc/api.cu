@@ -10,6 +10,7 @@
 // the Run-Time Check").  All arithmetic on the data happens in the kernels.
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <cstddef>
 #include <cstring>
 #include <map>
@@ -97,10 +98,13 @@ cudaError_t pinned(size_t bytes, void** out) {
   return cudaSuccess;
 }
 
+// Stage timing (PROFK_OPT_TIMING): events at the stage boundaries of the
+// first attempt, and the stage times of this thread's last timed call.
 struct Events {
-  cudaEvent_t a = nullptr, b = nullptr;
+  cudaEvent_t e[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
 };
 thread_local Events t_events;
+thread_local float t_stage_ms[6] = {-1.f, -1.f, -1.f, -1.f, -1.f, -1.f};
 
 // ---------------------------------------------------------------------------
 // Small kernels of the control flow.
@@ -376,6 +380,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   Call c;
   c.stream = stream;
   const int64_t launches0 = launch_count();
+  const auto wall0 = std::chrono::steady_clock::now();
   int64_t D = sampling ? draw_budget(n, P.S) : 0;
   Layout L = make_layout(rows, n, k, P.S, D, P.M, sampling);
   std::vector<int> pending, fallback, attempt(static_cast<size_t>(rows), 0);
@@ -416,6 +421,12 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
     {
       const int64_t H = 1ll << L.log2H;
       const unsigned rb = static_cast<unsigned>(std::min<int64_t>((H + 1023) / 1024, 256));
+      const bool time_it = timing && first_filter;
+      if (time_it) {
+        if (!t_events.e[0])
+          for (auto& ev : t_events.e) PK_CHECK(cudaEventCreate(&ev));
+        PK_CHECK(cudaEventRecord(t_events.e[0], stream));
+      }
       ++launch_count();
       k_attempt_reset<<<dim3(rb, ng), 1024, 0, stream>>>(at<unsigned long long>(c.ws, L.off_table), L.log2H, gl, st,
                                                         static_cast<unsigned long long>(P.t));
@@ -424,19 +435,13 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
                     at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
                     at<uint32_t>(c.ws, L.off_skeys)};
       launch_sample(sa, stream);
+      if (time_it) PK_CHECK(cudaEventRecord(t_events.e[1], stream));
       SelectArgs ta{KeySource::SampleKeys, at<uint32_t>(c.ws, L.off_skeys), P.S, P.S, ng, gl, st};
       launch_select(ta, 0, true, 0, stream);  // its last pass stores tau
-      const bool time_it = timing && first_filter;
-      if (time_it) {
-        if (!t_events.a) {
-          PK_CHECK(cudaEventCreate(&t_events.a));
-          PK_CHECK(cudaEventCreate(&t_events.b));
-        }
-        PK_CHECK(cudaEventRecord(t_events.a, stream));
-      }
+      if (time_it) PK_CHECK(cudaEventRecord(t_events.e[2], stream));
       FilterArgs fa{x, ld, n, P.M, ng, gl, st, at<unsigned long long>(c.ws, L.off_buf), filter_grid(cps)};
       launch_filter(fa, stream);
-      if (time_it) PK_CHECK(cudaEventRecord(t_events.b, stream));
+      if (time_it) PK_CHECK(cudaEventRecord(t_events.e[3], stream));
       // Refinement, launched before the host has seen the counts: a row whose
       // count fails the check is voided on the device and left untouched, so
       // the host round trip of the check is off the critical path of the
@@ -449,14 +454,17 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         launch_compact(ra, sel, L.kstride, k, stream);
         launch_sort_emit(sel, L.kstride, k, ng, gl, x, ld, n, out_vals, out_idx, stream, st);
       }
+      if (time_it) PK_CHECK(cudaEventRecord(t_events.e[4], stream));
       PK_CHECK(cudaGetLastError());
       // Run-time check: read the exact counts of every row.
       char* rep = static_cast<char*>(hbuf) + sizeof(int) * rows * 4;
       PK_CHECK(cudaMemcpy2DAsync(rep, REPORT_BYTES, st, sizeof(RowState), REPORT_BYTES, rows,
                                  cudaMemcpyDeviceToHost, stream));
+      if (time_it) PK_CHECK(cudaEventRecord(t_events.e[5], stream));
       PK_CHECK(cudaStreamSynchronize(stream));
       if (time_it) {
-        PK_CHECK(cudaEventElapsedTime(&filter_ms, t_events.a, t_events.b));
+        PK_CHECK(cudaEventElapsedTime(&filter_ms, t_events.e[2], t_events.e[3]));
+        for (int q = 0; q < 5; ++q) PK_CHECK(cudaEventElapsedTime(&t_stage_ms[q], t_events.e[q], t_events.e[q + 1]));
         first_filter = false;
       }
       std::vector<int> tie;
@@ -564,6 +572,8 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
 
 done:
   ws_free(c);
+  if (timing)
+    t_stage_ms[5] = std::chrono::duration<float, std::milli>(std::chrono::steady_clock::now() - wall0).count();
   if (stats) {
     for (int64_t r = 0; r < rows; ++r) {
       st_host[r].aux_bytes = c.ws_bytes;
@@ -634,6 +644,13 @@ const char* profk_strerror(int code) {
     case PROFK_ERR_SCRATCH: return "problem needs more workspace than the fixed scratch of profk_topk_noalloc";
     default: return "unknown status";
   }
+}
+
+int profk_last_stage_ms(float* out, int count) {
+  if (!out || count < 1) return PROFK_ERR_INVALID;
+  const int m = count < 6 ? count : 6;
+  for (int q = 0; q < m; ++q) out[q] = t_stage_ms[q];
+  return m;
 }
 
 int profk_sample(const float* x, int64_t n, int64_t S, uint64_t seed, int64_t row, int32_t attempt,

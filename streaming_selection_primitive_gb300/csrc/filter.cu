@@ -12,12 +12,14 @@
 //  * fast path: a NaN-propagating max over the lane's 4U values, one compare
 //    against tau and one warp vote;
 //  * slow path (some lane holds a passer or a NaN): per-element >= / > / NaN
-//    tests into a 64-bit lane mask, a warp scan of the passer counts and ONE
-//    atomicAdd per warp tile on the row's counter, whose old value is the
-//    slot of the tile's first passer.  Stores are masked to M and the counter
-//    keeps counting, as in the pages' kernel.  Once a warp sees the counter
-//    pass M it counts the rest in a register (no more atomics, no stores), so
-//    tie-heavy inputs that overflow the buffer do not serialize on the counter;
+//    tests into a 64-bit lane mask and a warp scan of the passer counts; the
+//    passers go to the warp's private staging area in shared memory (128
+//    keys).  A full stage is flushed with ONE atomicAdd on the row's counter,
+//    whose old value is the slot of the first flushed key, so dense inputs
+//    (large k) do not serialize on the counter.  Stores are masked to M and
+//    the counter keeps counting, as in the pages' kernel.  Once a warp sees
+//    the counter pass M it counts the rest in a register (no more atomics,
+//    no stores), so inputs that overflow the buffer cost no atomics either;
 //  * R_gt, the NaN count and those late passers are per-lane registers,
 //    reduced once per row per warp.
 // A passer (v, i) is stored as the 64-bit key (ord(v) << 32) | ~i, the order
@@ -62,10 +64,31 @@ __device__ __forceinline__ void flush_row(RowState& S, unsigned long long& gt, u
   late = 0;
 }
 
+constexpr int STAGE = 128;  // staged passer keys per warp
+
+// Moves a warp's staged keys into the buffer with one reservation.
+__device__ __forceinline__ void flush_stage(RowState& S, unsigned long long* stage, int& stage_n,
+                                            unsigned long long* br, int64_t M, bool& over) {
+  if (stage_n == 0) return;
+  const int lane = threadIdx.x & 31;
+  unsigned long long gbase = 0;
+  if (lane == 0) gbase = atomicAdd(&S.R_ge, static_cast<unsigned long long>(stage_n));
+  gbase = __shfl_sync(FULL_MASK, gbase, 0);
+  __syncwarp();
+  for (int j = lane; j < stage_n; j += 32)
+    if (gbase + j < static_cast<unsigned long long>(M)) br[gbase + j] = stage[j];
+  if (gbase + stage_n > static_cast<unsigned long long>(M)) over = true;
+  stage_n = 0;
+  __syncwarp();
+}
+
 template <int T, int U>
 __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
   static_assert(4 * U <= 64, "at most 64 elements per lane");
   constexpr int64_t WT = 32 * 4 * U;  // elements per warp tile
+  __shared__ unsigned long long s_stage[T / 32][STAGE];
+  unsigned long long* stage = s_stage[threadIdx.x >> 5];
+  int stage_n = 0;  // warp-uniform
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (T / 32);
   const int64_t tiles_per_row = (a.n + WT - 1) / WT;
@@ -82,7 +105,10 @@ __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
     const int ri = static_cast<int>(tile / tiles_per_row);
     const int64_t base = (tile - static_cast<int64_t>(ri) * tiles_per_row) * WT;
     if (ri != cur) {
-      if (cur >= 0) flush_row(a.st[row], gt, nan, late);
+      if (cur >= 0) {
+        flush_stage(a.st[row], stage, stage_n, br, a.M, over);
+        flush_row(a.st[row], gt, nan, late);
+      }
       cur = ri;
       row = a.rows ? a.rows[ri] : ri;
       tau = key_to_float(a.st[row].tau_key);
@@ -146,6 +172,33 @@ __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
       if (lane == 0) late += tot;
       continue;
     }
+    if (tot <= STAGE) {
+      if (stage_n + static_cast<int>(tot) > STAGE) {
+        flush_stage(a.st[row], stage, stage_n, br, a.M, over);
+        if (over) {
+          if (lane == 0) late += tot;
+          continue;
+        }
+      }
+      if (cnt) {
+        int pos = stage_n + static_cast<int>(incl - cnt);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int e = u * 4 + c;
+            if ((ge >> e) & 1ull) {
+              const int64_t idx = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
+              stage[pos++] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
+            }
+          }
+        }
+      }
+      stage_n += static_cast<int>(tot);
+      __syncwarp();
+      continue;
+    }
+    // More passers in this tile than a stage holds: reserve for the tile alone.
     unsigned long long gbase = 0;
     if (lane == 0) gbase = atomicAdd(&a.st[row].R_ge, static_cast<unsigned long long>(tot));
     gbase = __shfl_sync(FULL_MASK, gbase, 0);
@@ -168,7 +221,10 @@ __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
       }
     }
   }
-  if (cur >= 0) flush_row(a.st[row], gt, nan, late);
+  if (cur >= 0) {
+    flush_stage(a.st[row], stage, stage_n, br, a.M, over);
+    flush_row(a.st[row], gt, nan, late);
+  }
 }
 
 // Launch shape: threads per CTA and 16-byte loads per lane per warp tile.
