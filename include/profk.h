@@ -146,7 +146,8 @@ typedef enum profk_option {
   PROFK_OPT_FORCE_M = 5,       /* >0 overrides M [0] */
   PROFK_OPT_TIMING = 6,        /* record stats.filter_ms with CUDA events [0] */
   PROFK_OPT_FILTER_CTAS_PER_SM = 7, /* persistent filter grid = SMs x this; 0 = auto [0] */
-  PROFK_OPT__COUNT = 8
+  PROFK_OPT_PDL = 8,           /* launch kernels with programmatic dependent launch [1] */
+  PROFK_OPT__COUNT = 9
 } profk_option;
 int profk_set_option(int option, int64_t value);
 int64_t profk_get_option(int option);

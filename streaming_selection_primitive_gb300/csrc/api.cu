@@ -28,7 +28,7 @@ namespace {
 // ---------------------------------------------------------------------------
 // Options.
 std::atomic<int64_t> g_opt[PROFK_OPT__COUNT] = {
-    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}};
+    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}, {1}};
 
 // ---------------------------------------------------------------------------
 // Memoized parameters per (n, k, eps, mode).
@@ -109,6 +109,8 @@ thread_local float t_stage_ms[6] = {-1.f, -1.f, -1.f, -1.f, -1.f, -1.f};
 // ---------------------------------------------------------------------------
 // Small kernels of the control flow.
 __global__ void k_attempt_init(RowState* st, const int* rows) {
+  pdl_trigger();
+  pdl_wait();
   const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
   RowState& S = st[row];
   S.R_ge = 0;
@@ -122,6 +124,8 @@ __global__ void k_attempt_init(RowState* st, const int* rows) {
 // counters to zero, and the selection state ready for tau (rank t).
 __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int* rows, RowState* st,
                                 unsigned long long t) {
+  pdl_trigger();
+  pdl_wait();
   const int row = launch_row(rows);
   unsigned long long* tb = table + (static_cast<int64_t>(row) << log2H);
   const int64_t H = 1ll << log2H;
@@ -154,6 +158,8 @@ __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int*
 
 // Hash tables of the listed rows back to "empty".
 __global__ void k_reset_tables(unsigned long long* table, int log2H, const int* rows) {
+  pdl_trigger();
+  pdl_wait();
   const int row = launch_row(rows);
   unsigned long long* t = table + (static_cast<int64_t>(row) << log2H);
   const int64_t H = 1ll << log2H;
@@ -163,23 +169,33 @@ __global__ void k_reset_tables(unsigned long long* table, int log2H, const int* 
 }
 
 __global__ void k_set_tau(RowState* st, float tau) {
+  pdl_trigger();
+  pdl_wait();
   st->tau_key = ord_key(tau);
   st->R_ge = 0;
   st->R_gt = 0;
   st->nan = 0;
 }
 
-__global__ void k_set_count(RowState* st, unsigned long long R) { st->R_ge = R; }
+__global__ void k_set_count(RowState* st, unsigned long long R) {
+  pdl_trigger();
+  pdl_wait(); st->R_ge = R; }
 
 __global__ void k_vals_to_keys(const float* v, int64_t S, uint32_t* keys) {
+  pdl_trigger();
+  pdl_wait();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < S;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     keys[i] = ord_key(v[i]);
 }
 
-__global__ void k_tau_out(const RowState* st, float* out) { *out = key_to_float(st->tau_key); }
+__global__ void k_tau_out(const RowState* st, float* out) {
+  pdl_trigger();
+  pdl_wait(); *out = key_to_float(st->tau_key); }
 
 __global__ void k_sample_out(const uint32_t* sidx, int64_t S, const float* x, int64_t* out_sidx, float* out_vals) {
+  pdl_trigger();
+  pdl_wait();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < S;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint32_t u = sidx[i];
@@ -427,17 +443,18 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
           for (auto& ev : t_events.e) PK_CHECK(cudaEventCreate(&ev));
         PK_CHECK(cudaEventRecord(t_events.e[0], stream));
       }
-      ++launch_count();
-      k_attempt_reset<<<dim3(rb, ng), 1024, 0, stream>>>(at<unsigned long long>(c.ws, L.off_table), L.log2H, gl, st,
+      launch_kernel(k_attempt_reset, dim3(rb, ng), 1024, 0, stream, at<unsigned long long>(c.ws, L.off_table), L.log2H, gl, st,
                                                         static_cast<unsigned long long>(P.t));
+      // Sampling, with the first pass of the tau selection fused into its
+      // last kernel; the two remaining passes follow.
       SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, a, ng, gl, st,
                     at<unsigned long long>(c.ws, L.off_table), at<uint32_t>(c.ws, L.off_draws),
                     at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
-                    at<uint32_t>(c.ws, L.off_skeys)};
+                    at<uint32_t>(c.ws, L.off_skeys), true, static_cast<unsigned long long>(P.t)};
       launch_sample(sa, stream);
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[1], stream));
       SelectArgs ta{KeySource::SampleKeys, at<uint32_t>(c.ws, L.off_skeys), P.S, P.S, ng, gl, st};
-      launch_select(ta, 0, true, 0, stream);  // its last pass stores tau
+      launch_select(ta, 0, true, 1, stream);  // its last pass stores tau
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[2], stream));
       FilterArgs fa{x, ld, n, P.M, ng, gl, st, at<unsigned long long>(c.ws, L.off_buf), filter_grid(cps)};
       launch_filter(fa, stream);
@@ -446,7 +463,10 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
       // count fails the check is voided on the device and left untouched, so
       // the host round trip of the check is off the critical path of the
       // (likely) successful attempt.
-      {
+      if (k <= refine_one_max_k() && P.M <= refine_one_max_m()) {
+        RefineOneArgs oa{at<unsigned long long>(c.ws, L.off_buf), P.M, ng, gl, st, k, x, ld, n, out_vals, out_idx};
+        launch_refine_one(oa, stream);
+      } else {
         launch_refine_init(ng, gl, st, k, P.M, stream);
         SelectArgs ra{KeySource::Buffer, at<unsigned long long>(c.ws, L.off_buf), P.M, P.M, ng, gl, st};
         uint64_t* sel = at<uint64_t>(c.ws, L.off_sel);
@@ -587,6 +607,9 @@ done:
 }
 
 }  // namespace
+
+bool pdl_enabled() { return g_opt[PROFK_OPT_PDL].load(std::memory_order_relaxed) != 0; }
+
 }  // namespace profk
 
 using namespace profk;
@@ -668,8 +691,7 @@ int profk_sample(const float* x, int64_t n, int64_t S, uint64_t seed, int64_t ro
     {
       RowState* st = at<RowState>(c.ws, L.off_state);
       PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
-      ++launch_count();
-      k_reset_tables<<<dim3(256, 1), 1024, 0, stream>>>(at<unsigned long long>(c.ws, L.off_table), L.log2H, nullptr);
+      launch_kernel(k_reset_tables, dim3(256, 1), 1024, 0, stream, at<unsigned long long>(c.ws, L.off_table), L.log2H, nullptr);
       SampleArgs sa{x, n, static_cast<uint64_t>(n), S, D, L.log2H, seed, attempt, 1, nullptr, st,
                     at<unsigned long long>(c.ws, L.off_table), at<uint32_t>(c.ws, L.off_draws),
                     at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
@@ -688,8 +710,7 @@ int profk_sample(const float* x, int64_t n, int64_t S, uint64_t seed, int64_t ro
       }
       if (static_cast<int64_t>(distinct) >= S) {
         const unsigned b = static_cast<unsigned>(std::min<int64_t>((S + 255) / 256, 1024));
-        ++launch_count();
-        k_sample_out<<<b, 256, 0, stream>>>(at<uint32_t>(c.ws, L.off_sidx), S, x, out_sidx, out_vals);
+        launch_kernel(k_sample_out, b, 256, 0, stream, at<uint32_t>(c.ws, L.off_sidx), S, x, out_sidx, out_vals);
         PK_CHECK(cudaGetLastError());
         goto done;
       }
@@ -714,13 +735,11 @@ int profk_threshold(const float* vals, int64_t S, int64_t t, float* out_tau, cud
     uint32_t* keys = at<uint32_t>(c.ws, align_up(sizeof(RowState)));
     PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
     const unsigned b = static_cast<unsigned>(std::min<int64_t>((S + 255) / 256, 1024));
-    ++launch_count();
-    k_vals_to_keys<<<b, 256, 0, stream>>>(vals, S, keys);
+    launch_kernel(k_vals_to_keys, b, 256, 0, stream, vals, S, keys);
     SelectArgs ta{KeySource::SampleKeys, keys, S, S, 1, nullptr, st};
     launch_select(ta, static_cast<uint64_t>(t), true, 0, stream);
     launch_store_tau(1, nullptr, st, stream);
-    ++launch_count();
-    k_tau_out<<<1, 1, 0, stream>>>(st, out_tau);
+    launch_kernel(k_tau_out, 1, 1, 0, stream, st, out_tau);
     PK_CHECK(cudaGetLastError());
   }
 done:
@@ -738,8 +757,7 @@ int profk_filter(const float* x, int64_t n, float tau, int64_t M, uint64_t* out_
   {
     RowState* st = at<RowState>(c.ws, 0);
     PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
-    ++launch_count();
-    k_set_tau<<<1, 1, 0, stream>>>(st, tau);
+    launch_kernel(k_set_tau, 1, 1, 0, stream, st, tau);
     const int64_t cps = g_opt[PROFK_OPT_FILTER_CTAS_PER_SM].load();
     FilterArgs fa{x, n, n, M, 1, nullptr, st, reinterpret_cast<unsigned long long*>(out_keys), filter_grid(cps)};
     launch_filter(fa, stream);
@@ -762,12 +780,17 @@ int profk_refine(const uint64_t* keys, int64_t R, int64_t k, const float* x, int
     RowState* st = at<RowState>(c.ws, 0);
     unsigned long long* sel = at<unsigned long long>(c.ws, align_up(sizeof(RowState)));
     PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
-    ++launch_count();
-    k_set_count<<<1, 1, 0, stream>>>(st, static_cast<unsigned long long>(R));
-    SelectArgs ra{KeySource::Buffer, keys, R, R, 1, nullptr, st};
-    launch_select(ra, static_cast<uint64_t>(k), false, 0, stream);
-    launch_compact(ra, reinterpret_cast<uint64_t*>(sel), ks, k, stream);
-    launch_sort_emit(reinterpret_cast<uint64_t*>(sel), ks, k, 1, nullptr, x, 0, n, out_vals, out_idx, stream);
+    launch_kernel(k_set_count, 1, 1, 0, stream, st, static_cast<unsigned long long>(R));
+    if (k <= refine_one_max_k() && R <= refine_one_max_m()) {
+      RefineOneArgs oa{reinterpret_cast<const unsigned long long*>(keys), R, 1, nullptr, st, k, x, 0, n,
+                       out_vals, out_idx};
+      launch_refine_one(oa, stream);
+    } else {
+      SelectArgs ra{KeySource::Buffer, keys, R, R, 1, nullptr, st};
+      launch_select(ra, static_cast<uint64_t>(k), false, 0, stream);
+      launch_compact(ra, reinterpret_cast<uint64_t*>(sel), ks, k, stream);
+      launch_sort_emit(reinterpret_cast<uint64_t*>(sel), ks, k, 1, nullptr, x, 0, n, out_vals, out_idx, stream);
+    }
     PK_CHECK(cudaGetLastError());
   }
 done:

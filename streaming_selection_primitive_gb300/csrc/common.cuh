@@ -125,13 +125,19 @@ __device__ __forceinline__ int launch_row(const int* rows) {
   return rows ? rows[blockIdx.y] : static_cast<int>(blockIdx.y);
 }
 
-// Warp-aggregated shared-memory histogram increment.
+// Histogram increment by a whole warp (all 32 lanes call it).  Lanes with
+// nothing to count cost one vote; when every counting lane hits the same bin
+// (a heavily tied input) the warp adds once; otherwise each lane adds its own.
 __device__ __forceinline__ void hist_add(unsigned int* h, uint32_t bin, bool valid) {
   const unsigned act = __ballot_sync(FULL_MASK, valid);
-  if (valid) {
-    const unsigned peers = __match_any_sync(act, bin);
-    const int lane = threadIdx.x & 31;
-    if (lane == __ffs(peers) - 1) atomicAdd(h + bin, static_cast<unsigned>(__popc(peers)));
+  if (act == 0) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(act) - 1;
+  const uint32_t b0 = __shfl_sync(FULL_MASK, bin, leader);
+  if (__all_sync(FULL_MASK, !valid || bin == b0)) {
+    if (lane == leader) atomicAdd(h + b0, static_cast<unsigned>(__popc(act)));
+  } else if (valid) {
+    atomicAdd(h + bin, 1u);
   }
 }
 

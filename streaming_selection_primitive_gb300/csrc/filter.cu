@@ -84,6 +84,7 @@ __device__ __forceinline__ void flush_stage(RowState& S, unsigned long long* sta
 
 template <int T, int U>
 __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
+  pdl_wait();
   static_assert(4 * U <= 64, "at most 64 elements per lane");
   constexpr int64_t WT = 32 * 4 * U;  // elements per warp tile
   __shared__ unsigned long long s_stage[T / 32][STAGE];
@@ -253,8 +254,7 @@ void launch_filter(const FilterArgs& a, cudaStream_t stream) {
   int grid = a.grid;
   if (ctas < grid) grid = static_cast<int>(ctas);
   if (grid < 1) grid = 1;
-  ++launch_count();
-  k_filter<FT, FU><<<grid, FT, 0, stream>>>(a);
+  launch_kernel(k_filter<FT, FU>, grid, FT, 0, stream, a);
 }
 
 }  // namespace profk

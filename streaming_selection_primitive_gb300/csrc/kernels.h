@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -13,6 +14,35 @@ namespace profk {
 inline int64_t& launch_count() {
   thread_local int64_t count = 0;
   return count;
+}
+
+// Programmatic dependent launch.  Every kernel of the library starts with
+// pdl_wait() (griddepcontrol.wait: returns once the preceding kernel on the
+// stream has completed and its memory is visible; a no-op for an ordinary
+// launch).  Small kernels call pdl_trigger() first, so that the next kernel
+// can be launched while they run.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+bool pdl_enabled();  // PROFK_OPT_PDL
+
+// Launches a library kernel on `stream`, with the programmatic-serialization
+// attribute when PDL is enabled, and counts it.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 Args&&... args) {
+  ++launch_count();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Where a radix selection reads its keys from.
@@ -50,6 +80,12 @@ struct SampleArgs {
   uint32_t* blockcnt;         // rows x ceil(D / 1024)
   uint32_t* sidx;             // rows x S (out)
   uint32_t* skeys;            // rows x S (out)
+  // Optional: the first 11-bit pass of the tau selection (step 2, rank t)
+  // fused into the compaction; the selection state must have been reset
+  // (RowState::hist zero, done_blocks 0).  The two remaining passes are
+  // launch_select(..., first_pass = 1).
+  bool tau_pass1 = false;
+  unsigned long long t = 0;
 };
 void launch_sample(const SampleArgs& a, cudaStream_t stream);
 // Same, with Philox key word 1 = storage row + key_row0 (a single stored row
@@ -79,6 +115,27 @@ void launch_sort_emit(uint64_t* keys, int64_t key_stride, int64_t k, int nrows, 
                       const float* x, int64_t ld, int64_t n, float* out_vals, int64_t* out_idx,
                       cudaStream_t stream, const RowState* st = nullptr);
 int64_t sort_stride(int64_t k);  // key_stride the sort needs for k keys
+
+// Step 4 in one CTA per row for k <= refine_one_max_k() (select.cu): radix
+// selection over the candidate keys read from L2, early gather of the top
+// bucket, shared-memory sort and emission.  A row whose count fails
+// k <= R <= M is marked skip and left alone.
+struct RefineOneArgs {
+  const unsigned long long* buf;  // rows x M candidate keys
+  int64_t M;
+  int nrows;
+  const int* rows;
+  RowState* st;
+  int64_t k;
+  const float* x;
+  int64_t ld;
+  int64_t n;
+  float* out_vals;
+  int64_t* out_idx;
+};
+void launch_refine_one(const RefineOneArgs& a, cudaStream_t stream);
+int64_t refine_one_max_k();
+int64_t refine_one_max_m();
 
 // Filter pass.
 struct FilterArgs {

@@ -27,6 +27,8 @@ __device__ __forceinline__ uint64_t hash_slot(uint32_t u, int log2H) {
 }
 
 __global__ void __launch_bounds__(256) k_sample_draw(SampleArgs a, int64_t key_row0) {
+  pdl_trigger();
+  pdl_wait();
   // One draw per thread: the four lanes that share a Philox block each
   // compute it (cheap arithmetic) and keep their own word, so every hash
   // insertion proceeds in parallel.
@@ -82,6 +84,8 @@ __device__ __forceinline__ uint32_t first_position(const unsigned long long* tab
 }
 
 __global__ void __launch_bounds__(MARK_THREADS) k_sample_mark(SampleArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int row = launch_row(a.rows);
   const int64_t i = static_cast<int64_t>(blockIdx.x) * MARK_THREADS + threadIdx.x;
   const unsigned long long* table = a.table + (static_cast<int64_t>(row) << a.log2H);
@@ -94,7 +98,62 @@ __global__ void __launch_bounds__(MARK_THREADS) k_sample_mark(SampleArgs a) {
   if (threadIdx.x == 0) a.blockcnt[static_cast<int64_t>(row) * gridDim.x + blockIdx.x] = cnt;
 }
 
+// Last block of the compaction: the first radix pass of the tau selection
+// (step 2) over the row's S sample keys is complete in the 2048-bin histogram
+// of their top 11 bits; pick the bin that holds the t-th largest key and leave
+// the selection state at "11 bits resolved" for the two remaining passes.
+// Nothing is selected when fewer than S distinct draws were found (the host
+// then grows D and the attempt runs again).
+__device__ __noinline__ void tau_first_digit(const SampleArgs& a, int row) {
+  constexpr int NW = MARK_THREADS / 32;
+  __shared__ unsigned long long s_scan[NW];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  RowState& S = a.st[row];
+  const uint32_t* bc = a.blockcnt + static_cast<int64_t>(row) * gridDim.x;
+  unsigned long long total = 0;
+  for (unsigned b = lane; b < gridDim.x; b += 32) total += __ldcg(bc + b);
+  for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(FULL_MASK, total, o);
+  // Thread t owns bins 2047 - 2t and 2046 - 2t (descending order).
+  const int top = HIST_BINS - 1 - 2 * tid;
+  const unsigned c0 = __ldcg(S.hist + top), c1 = __ldcg(S.hist + top - 1);
+  const unsigned long long v = static_cast<unsigned long long>(c0) + c1;
+  unsigned long long incl = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(FULL_MASK, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s_scan[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long w = lane < NW ? s_scan[lane] : 0ull;
+    unsigned long long wi = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(FULL_MASK, wi, o);
+      if (lane >= o) wi += t;
+    }
+    if (lane < NW) s_scan[lane] = wi - w;
+  }
+  __syncthreads();
+  const unsigned long long excl = s_scan[warp] + incl - v;
+  const unsigned long long want = a.t;
+  if (total >= static_cast<unsigned long long>(a.S) && excl < want && want <= excl + v) {
+    const bool in0 = want <= excl + c0;
+    const unsigned d = in0 ? static_cast<unsigned>(top) : static_cast<unsigned>(top - 1);
+    S.sel_prefix = d;
+    S.sel_above = in0 ? excl : excl + c0;
+    S.sel_rank = want - (in0 ? excl : excl + c0);
+    S.sel_bucket = in0 ? c0 : c1;
+    S.sel_bits = HIST_BITS;
+  }
+  __syncthreads();
+  S.hist[top] = 0;
+  S.hist[top - 1] = 0;
+  if (tid == 0) S.done_blocks = 0;
+}
+
 __global__ void __launch_bounds__(MARK_THREADS) k_sample_compact(SampleArgs a) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int NW = MARK_THREADS / 32;
   __shared__ unsigned s_warp[NW];
   __shared__ unsigned long long s_base;
@@ -139,27 +198,48 @@ __global__ void __launch_bounds__(MARK_THREADS) k_sample_compact(SampleArgs a) {
     if (lane < NW) s_warp[lane] = incl - v;
   }
   __syncthreads();
+  bool has = false;
+  uint32_t key = 0;
   if (first) {
     const unsigned long long rank = s_base + s_warp[warp] + __popc(bal & ((1u << lane) - 1u));
     if (rank < static_cast<unsigned long long>(a.S)) {
       const int64_t o = static_cast<int64_t>(row) * a.S + static_cast<int64_t>(rank);
+      key = ord_key(a.x[static_cast<int64_t>(row) * a.ld + u]);
       a.sidx[o] = u;
-      a.skeys[o] = ord_key(a.x[static_cast<int64_t>(row) * a.ld + u]);
+      a.skeys[o] = key;
+      has = true;
     }
   }
+  if (!a.tau_pass1) return;
+  // First pass of step 2 fused: the keys' top 11 bits go to the row's
+  // histogram (block-local first, then one atomic per non-empty bin); the
+  // last block to finish picks the digit.
+  __shared__ unsigned s_h[HIST_BINS];
+  for (int b = threadIdx.x; b < HIST_BINS; b += MARK_THREADS) s_h[b] = 0;
+  __syncthreads();
+  hist_add(s_h, key >> (32 - HIST_BITS), has);
+  __syncthreads();
+  RowState& S = a.st[row];
+  for (int b = threadIdx.x; b < HIST_BINS; b += MARK_THREADS)
+    if (s_h[b]) atomicAdd(S.hist + b, s_h[b]);
+  __threadfence();
+  __syncthreads();
+  __shared__ int s_last;
+  if (threadIdx.x == 0) s_last = atomicAdd(&S.done_blocks, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  tau_first_digit(a, row);
 }
 
 }  // namespace
 
 void launch_sample_rows(const SampleArgs& a, int64_t key_row0, cudaStream_t stream) {
   const int64_t blocks = (a.D + 255) / 256;
-  ++launch_count();
-  k_sample_draw<<<dim3(static_cast<unsigned>(blocks), a.nrows), 256, 0, stream>>>(a, key_row0);
+  launch_kernel(k_sample_draw, dim3(static_cast<unsigned>(blocks), a.nrows), 256, 0, stream, a, key_row0);
   const unsigned nb = static_cast<unsigned>((a.D + MARK_THREADS - 1) / MARK_THREADS);
-  ++launch_count();
-  k_sample_mark<<<dim3(nb, a.nrows), MARK_THREADS, 0, stream>>>(a);
-  ++launch_count();
-  k_sample_compact<<<dim3(nb, a.nrows), MARK_THREADS, 0, stream>>>(a);
+  launch_kernel(k_sample_mark, dim3(nb, a.nrows), MARK_THREADS, 0, stream, a);
+  launch_kernel(k_sample_compact, dim3(nb, a.nrows), MARK_THREADS, 0, stream, a);
 }
 
 void launch_sample(const SampleArgs& a, cudaStream_t stream) { launch_sample_rows(a, 0, stream); }

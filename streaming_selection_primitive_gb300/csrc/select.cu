@@ -54,6 +54,8 @@ struct SrcBuffer {
 };
 
 __global__ void k_sel_init(RowState* st, const int* rows, unsigned long long rank) {
+  pdl_trigger();
+  pdl_wait();
   const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
   RowState& S = st[row];
   for (int b = threadIdx.x; b < HIST_BINS; b += blockDim.x) S.hist[b] = 0;
@@ -76,6 +78,8 @@ __global__ void k_sel_init(RowState* st, const int* rows, unsigned long long ran
 // a row whose count fails the check k <= R <= M is marked void (skip = 1), so
 // that every later refinement kernel leaves it and its outputs alone.
 __global__ void k_refine_init(RowState* st, const int* rows, unsigned long long k, unsigned long long M) {
+  pdl_trigger();
+  pdl_wait();
   const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
   RowState& S = st[row];
   for (int b = threadIdx.x; b < HIST_BINS; b += blockDim.x) S.hist[b] = 0;
@@ -97,6 +101,8 @@ __global__ void k_refine_init(RowState* st, const int* rows, unsigned long long 
 }
 
 __global__ void k_tie_init(RowState* st, const int* rows, unsigned long long k) {
+  pdl_trigger();
+  pdl_wait();
   const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
   RowState& S = st[row];
   for (int b = threadIdx.x; b < HIST_BINS; b += blockDim.x) S.hist[b] = 0;
@@ -116,6 +122,8 @@ __global__ void k_tie_init(RowState* st, const int* rows, unsigned long long k) 
 }
 
 __global__ void k_store_tau(RowState* st, const int* rows) {
+  pdl_trigger();
+  pdl_wait();
   const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
   if (threadIdx.x == 0) st[row].tau_key = static_cast<uint32_t>(st[row].sel_prefix);
 }
@@ -147,6 +155,8 @@ template <class Src>
 __global__ void __launch_bounds__(SEL_THREADS) k_radix_pass(Src src, RowState* st, const int* rows, int shift,
                                                            int width, int final_shift, int value_only,
                                                            int count_nan) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ unsigned h[HIST_BINS];
   __shared__ unsigned long long sw[32];
   __shared__ unsigned s_nan;
@@ -232,6 +242,8 @@ __global__ void __launch_bounds__(SEL_THREADS) k_radix_pass(Src src, RowState* s
 template <class Src>
 __global__ void __launch_bounds__(SEL_THREADS) k_compact(Src src, RowState* st, const int* rows,
                                                         unsigned long long* out, int64_t out_stride, int64_t k) {
+  pdl_trigger();
+  pdl_wait();
   const int row = launch_row(rows);
   RowState& S = st[row];
   if (!S.sel_done || S.skip) return;
@@ -278,6 +290,8 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort_small(const unsigned long
                                                             int64_t k, int P, const int* rows, const float* x,
                                                             int64_t ld, int64_t n, float* out_vals,
                                                             int64_t* out_idx, const RowState* st) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ unsigned long long s[];
   const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
   if (st && st[row].skip) return;
@@ -306,6 +320,8 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort_small(const unsigned long
 // Multi-CTA bitonic sort (descending) of rows of P = 2^m keys.
 __global__ void __launch_bounds__(SORT_THREADS) k_pad(unsigned long long* keys, int64_t key_stride, int64_t k,
                                                       int64_t P, const int* rows) {
+  pdl_trigger();
+  pdl_wait();
   const int row = launch_row(rows);
   for (int64_t i = k + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < P;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
@@ -316,6 +332,8 @@ __global__ void __launch_bounds__(SORT_THREADS) k_pad(unsigned long long* keys, 
 // starting at stage `from` (2 for a full local sort, or one merge stage).
 __global__ void __launch_bounds__(SORT_THREADS) k_bitonic_chunk(unsigned long long* keys, int64_t key_stride,
                                                                 int from, int64_t upto, const int* rows) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ unsigned long long s[];
   const int row = launch_row(rows);
   unsigned long long* kr = keys + row * key_stride + static_cast<int64_t>(blockIdx.x) * CHUNK;
@@ -345,6 +363,8 @@ __global__ void __launch_bounds__(SORT_THREADS) k_bitonic_chunk(unsigned long lo
 
 __global__ void __launch_bounds__(SORT_THREADS) k_bitonic_global(unsigned long long* keys, int64_t key_stride,
                                                                  int64_t P, int64_t size, int64_t j, const int* rows) {
+  pdl_trigger();
+  pdl_wait();
   const int row = launch_row(rows);
   unsigned long long* kr = keys + row * key_stride;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < P;
@@ -364,11 +384,167 @@ __global__ void __launch_bounds__(SORT_THREADS) k_bitonic_global(unsigned long l
 __global__ void __launch_bounds__(SORT_THREADS) k_emit(const unsigned long long* keys, int64_t key_stride, int64_t k,
                                                        const int* rows, const float* x, int64_t ld, int64_t n,
                                                        float* out_vals, int64_t* out_idx, const RowState* st) {
+  pdl_trigger();
+  pdl_wait();
   const int row = launch_row(rows);
   if (st && st[row].skip) return;
   for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < k;
        j += static_cast<int64_t>(gridDim.x) * blockDim.x)
     emit_one(keys[row * key_stride + j], row, j, k, x, ld, n, out_vals, out_idx);
+}
+
+// ---------------------------------------------------------------------------
+// Step 4 in one CTA per row.  The candidates (R <= M keys) are read from L2;
+// 11/11/10/11/11/10-bit MSD passes narrow the bucket that holds the k-th
+// largest key.  As soon as the keys above the bucket plus the bucket itself
+// fit the gather budget (at least 2k, at most ONE_OUT keys), all of them are
+// gathered into shared memory, sorted descending there, and the first k are
+// emitted.  The kernel is enqueued before the host has checked k <= R <= M;
+// a row that fails the check is marked skip and its outputs are not touched.
+constexpr int ONE_THREADS = 1024;
+constexpr int ONE_OUT = 16384;   // keys gathered into shared memory (128 KB)
+constexpr int ONE_MAX_K = 8192;
+constexpr int64_t ONE_MAX_M = 1 << 19;
+
+__global__ void __launch_bounds__(ONE_THREADS) k_refine_one(RefineOneArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ unsigned long long s_out[];  // ONE_OUT keys
+  __shared__ unsigned h[HIST_BINS];
+  __shared__ unsigned long long sw[32];
+  __shared__ int s_digit;
+  __shared__ unsigned long long s_above, s_count;
+  __shared__ unsigned s_cursor;
+  const int row = a.rows ? a.rows[blockIdx.x] : static_cast<int>(blockIdx.x);
+  RowState& S = a.st[row];
+  const int tid = threadIdx.x;
+  const unsigned long long R = S.R_ge;
+  const unsigned long long k = static_cast<unsigned long long>(a.k);
+  if (!(k <= R && R <= static_cast<unsigned long long>(a.M))) {
+    if (tid == 0) S.skip = 1;
+    return;  // block-uniform
+  }
+  if (tid == 0) {
+    S.skip = 0;
+    s_cursor = 0;
+  }
+  const unsigned long long* keys = a.buf + static_cast<int64_t>(row) * a.M;
+  const int64_t len = static_cast<int64_t>(R);
+  const unsigned long long budget = k * 2 < 2048 ? 2048 : (k * 2 > ONE_OUT ? ONE_OUT : k * 2);
+  unsigned long long prefix = 0, want = k, thresh = 0, total = k;
+  int bits = 0;
+  const int shifts[6] = {53, 42, 32, 21, 10, 0}, widths[6] = {11, 11, 10, 11, 11, 10};
+#pragma unroll 1
+  for (int p = 0; p < 6; ++p) {
+    const int shift = shifts[p], width = widths[p];
+    const int nb = 1 << width, hs = shift + width;
+    for (int b = tid; b < nb; b += ONE_THREADS) h[b] = 0;
+    if (tid == 0) {
+      s_digit = 0;
+      s_above = 0;
+      s_count = 0;
+    }
+    __syncthreads();
+    for (int64_t base = 0; base < len; base += 8 * ONE_THREADS) {
+      unsigned long long kk[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t i = base + static_cast<int64_t>(j) * ONE_THREADS + tid;
+        kk[j] = i < len ? __ldcg(keys + i) : 0ull;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t i = base + static_cast<int64_t>(j) * ONE_THREADS + tid;
+        const bool m = i < len && (bits == 0 || (kk[j] >> hs) == prefix);
+        hist_add(h, static_cast<uint32_t>(kk[j] >> shift) & (nb - 1), m);
+      }
+    }
+    __syncthreads();
+    // Bins counted down from the top: thread t owns nb / 1024 of them.
+    const int per = nb / ONE_THREADS;
+    const int top = nb - 1 - tid * per;
+    unsigned long long local = 0;
+    for (int q = 0; q < per; ++q) local += h[top - q];
+    const unsigned long long excl = block_excl_scan(local, sw);
+    if (excl < want && want <= excl + local) {
+      unsigned long long acc = excl;
+      for (int q = 0; q < per; ++q) {
+        const unsigned long long c = h[top - q];
+        if (want <= acc + c) {
+          s_digit = top - q;
+          s_above = acc;
+          s_count = c;
+          break;
+        }
+        acc += c;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << width) | static_cast<unsigned long long>(s_digit);
+    want -= s_above;
+    bits += width;
+    const unsigned long long above_all = k - want;  // keys above the bucket, all in the top-k
+    if (s_count == want || shift == 0) {  // the whole bucket is in the top-k: keys >= its bound are exactly k
+      thresh = prefix << shift;
+      total = k;
+      break;
+    }
+    if (above_all + s_count <= budget) {  // gather the whole bucket and finish in shared memory
+      thresh = prefix << shift;
+      total = above_all + s_count;
+      break;
+    }
+    __syncthreads();
+  }
+  // Gather every key >= thresh (exactly `total` of them).
+  for (int64_t base = 0; base < len; base += 8 * ONE_THREADS) {
+    unsigned long long kk[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t i = base + static_cast<int64_t>(j) * ONE_THREADS + tid;
+      kk[j] = i < len ? __ldcg(keys + i) : 0ull;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t i = base + static_cast<int64_t>(j) * ONE_THREADS + tid;
+      const bool sel = i < len && kk[j] >= thresh;
+      const unsigned m = __ballot_sync(FULL_MASK, sel);
+      if (m) {
+        unsigned pos0 = 0;
+        if ((tid & 31) == 0) pos0 = atomicAdd(&s_cursor, static_cast<unsigned>(__popc(m)));
+        pos0 = __shfl_sync(FULL_MASK, pos0, 0);
+        if (sel) {
+          const unsigned pos = pos0 + __popc(m & ((1u << (tid & 31)) - 1u));
+          if (pos < ONE_OUT) s_out[pos] = kk[j];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int cnt = static_cast<int>(total < ONE_OUT ? total : ONE_OUT);
+  int P = 1;
+  while (P < cnt) P <<= 1;
+  for (int i = tid; i < P; i += ONE_THREADS)
+    if (i >= cnt) s_out[i] = 0ull;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < P; i += ONE_THREADS) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned long long x0 = s_out[i], x1 = s_out[l];
+          const bool desc = (i & size) == 0;
+          if (desc ? (x0 < x1) : (x0 > x1)) {
+            s_out[i] = x1;
+            s_out[l] = x0;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int j = tid; j < static_cast<int>(a.k); j += ONE_THREADS)
+    emit_one(s_out[j], row, j, a.k, a.x, a.ld, a.n, a.out_vals, a.out_idx);
 }
 
 int64_t next_pow2(int64_t v) {
@@ -404,8 +580,7 @@ void run_passes(const Src& src, const SelectArgs& a, bool value_only, int first_
   const int final_shift = shifts[last];
   const unsigned bx = blocks_for(a.len, SEL_THREADS, 4 * sms());
   for (int p = first_pass; p <= last; ++p) {
-    ++launch_count();
-    k_radix_pass<Src><<<dim3(bx, a.nrows), SEL_THREADS, 0, stream>>>(src, a.st, a.rows, shifts[p], widths[p],
+    launch_kernel(k_radix_pass<Src>, dim3(bx, a.nrows), SEL_THREADS, 0, stream, src, a.st, a.rows, shifts[p], widths[p],
                                                                      final_shift, value_only ? 1 : 0, p == 0);
   }
 }
@@ -414,8 +589,7 @@ void run_passes(const Src& src, const SelectArgs& a, bool value_only, int first_
 
 void launch_select(const SelectArgs& a, uint64_t init_rank, bool value_only, int first_pass, cudaStream_t stream) {
   if (init_rank > 0) {
-    ++launch_count();
-    k_sel_init<<<a.nrows, 256, 0, stream>>>(a.st, a.rows, init_rank);
+    launch_kernel(k_sel_init, a.nrows, 256, 0, stream, a.st, a.rows, init_rank);
   }
   switch (a.src) {
     case KeySource::SampleKeys:
@@ -432,19 +606,16 @@ void launch_select(const SelectArgs& a, uint64_t init_rank, bool value_only, int
 }
 
 void launch_store_tau(int nrows, const int* rows, RowState* st, cudaStream_t stream) {
-  ++launch_count();
-  k_store_tau<<<nrows, 32, 0, stream>>>(st, rows);
+  launch_kernel(k_store_tau, nrows, 32, 0, stream, st, rows);
 }
 
 void launch_refine_init(int nrows, const int* rows, RowState* st, int64_t k, int64_t M, cudaStream_t stream) {
-  ++launch_count();
-  k_refine_init<<<nrows, 256, 0, stream>>>(st, rows, static_cast<unsigned long long>(k),
+  launch_kernel(k_refine_init, nrows, 256, 0, stream, st, rows, static_cast<unsigned long long>(k),
                                            static_cast<unsigned long long>(M));
 }
 
 void launch_tie_init(int nrows, const int* rows, RowState* st, int64_t k, cudaStream_t stream) {
-  ++launch_count();
-  k_tie_init<<<nrows, 256, 0, stream>>>(st, rows, static_cast<unsigned long long>(k));
+  launch_kernel(k_tie_init, nrows, 256, 0, stream, st, rows, static_cast<unsigned long long>(k));
 }
 
 void launch_compact(const SelectArgs& a, uint64_t* out, int64_t out_stride, int64_t k, cudaStream_t stream) {
@@ -452,23 +623,29 @@ void launch_compact(const SelectArgs& a, uint64_t* out, int64_t out_stride, int6
   unsigned long long* o = reinterpret_cast<unsigned long long*>(out);
   switch (a.src) {
     case KeySource::SampleKeys:
-      ++launch_count();
-      k_compact<<<dim3(bx, a.nrows), SEL_THREADS, 0, stream>>>(
+      launch_kernel(k_compact<SrcSample>, dim3(bx, a.nrows), SEL_THREADS, 0, stream,
           SrcSample{static_cast<const uint32_t*>(a.base), a.stride, a.len}, a.st, a.rows, o, out_stride, k);
       break;
     case KeySource::Input:
-      ++launch_count();
-      k_compact<<<dim3(bx, a.nrows), SEL_THREADS, 0, stream>>>(
+      launch_kernel(k_compact<SrcInput>, dim3(bx, a.nrows), SEL_THREADS, 0, stream,
           SrcInput{static_cast<const float*>(a.base), a.stride, a.len}, a.st, a.rows, o, out_stride, k);
       break;
     case KeySource::Buffer:
-      ++launch_count();
-      k_compact<<<dim3(bx, a.nrows), SEL_THREADS, 0, stream>>>(
+      launch_kernel(k_compact<SrcBuffer>, dim3(bx, a.nrows), SEL_THREADS, 0, stream,
           SrcBuffer{static_cast<const unsigned long long*>(a.base), a.stride, a.len}, a.st, a.rows, o, out_stride,
           k);
       break;
   }
 }
+
+void launch_refine_one(const RefineOneArgs& a, cudaStream_t stream) {
+  const size_t smem = sizeof(unsigned long long) * ONE_OUT;
+  cudaFuncSetAttribute(k_refine_one, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  launch_kernel(k_refine_one, a.nrows, ONE_THREADS, smem, stream, a);
+}
+
+int64_t refine_one_max_k() { return ONE_MAX_K; }
+int64_t refine_one_max_m() { return ONE_MAX_M; }
 
 int64_t sort_stride(int64_t k) { return k > SMALL_SORT_MAX ? next_pow2(k) : k; }
 
@@ -479,32 +656,26 @@ void launch_sort_emit(uint64_t* keys_u, int64_t key_stride, int64_t k, int nrows
   if (k <= SMALL_SORT_MAX) {
     cudaFuncSetAttribute(k_sort_small, cudaFuncAttributeMaxDynamicSharedMemorySize, SMALL_SORT_MAX * 8);
     const int P = static_cast<int>(next_pow2(k));
-    ++launch_count();
-    k_sort_small<<<nrows, SORT_THREADS, P * 8, stream>>>(keys, key_stride, k, P, rows, x, ld, n, out_vals, out_idx,
+    launch_kernel(k_sort_small, nrows, SORT_THREADS, P * 8, stream, keys, key_stride, k, P, rows, x, ld, n, out_vals, out_idx,
                                                          st);
     return;
   }
   const int64_t P = next_pow2(k);  // >= 2 * CHUNK here
   cudaFuncSetAttribute(k_bitonic_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize, CHUNK * 8);
   const unsigned padb = static_cast<unsigned>(std::min<int64_t>((P - k + SORT_THREADS - 1) / SORT_THREADS + 1, 1024));
-  ++launch_count();
-  k_pad<<<dim3(padb, nrows), SORT_THREADS, 0, stream>>>(keys, key_stride, k, P, rows);
+  launch_kernel(k_pad, dim3(padb, nrows), SORT_THREADS, 0, stream, keys, key_stride, k, P, rows);
   const unsigned chunks = static_cast<unsigned>(P / CHUNK);
-  ++launch_count();
-  k_bitonic_chunk<<<dim3(chunks, nrows), SORT_THREADS, CHUNK * 8, stream>>>(keys, key_stride, 2, CHUNK, rows);
+  launch_kernel(k_bitonic_chunk, dim3(chunks, nrows), SORT_THREADS, CHUNK * 8, stream, keys, key_stride, 2, CHUNK, rows);
   const unsigned gb = static_cast<unsigned>(std::min<int64_t>(P / 2 / SORT_THREADS + 1, 4096));
   for (int64_t size = 2 * CHUNK; size <= P; size <<= 1) {
     for (int64_t j = size >> 1; j >= CHUNK; j >>= 1) {
-      ++launch_count();
-      k_bitonic_global<<<dim3(gb, nrows), SORT_THREADS, 0, stream>>>(keys, key_stride, P, size, j, rows);
+      launch_kernel(k_bitonic_global, dim3(gb, nrows), SORT_THREADS, 0, stream, keys, key_stride, P, size, j, rows);
     }
-    ++launch_count();
-    k_bitonic_chunk<<<dim3(chunks, nrows), SORT_THREADS, CHUNK * 8, stream>>>(keys, key_stride,
+    launch_kernel(k_bitonic_chunk, dim3(chunks, nrows), SORT_THREADS, CHUNK * 8, stream, keys, key_stride,
                                                                              static_cast<int>(size), size, rows);
   }
   const unsigned eb = static_cast<unsigned>(std::min<int64_t>((k + SORT_THREADS - 1) / SORT_THREADS, 1024));
-  ++launch_count();
-  k_emit<<<dim3(eb, nrows), SORT_THREADS, 0, stream>>>(keys, key_stride, k, rows, x, ld, n, out_vals, out_idx, st);
+  launch_kernel(k_emit, dim3(eb, nrows), SORT_THREADS, 0, stream, keys, key_stride, k, rows, x, ld, n, out_vals, out_idx, st);
 }
 
 }  // namespace profk
