@@ -30,10 +30,15 @@ def _torch():
     return torch
 
 
-def _stream_handle(stream=None) -> int:
+def _stream_handle(stream=None, device=None) -> int:
+    """Raw cudaStream_t of `stream`, else of the current stream of `device`."""
+    if stream is not None:
+        return int(stream.cuda_stream)
     torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return int(s.cuda_stream)
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None and device is not None:
+        return int(raw(device.index if device.index is not None else torch.cuda.current_device()))
+    return int(torch.cuda.current_stream().cuda_stream)
 
 
 def _need_cuda_f32(x, name="x"):
@@ -90,7 +95,7 @@ def topk(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=None):
         vals, idx = out
     st = ProfkStats()
     code = lib().profk_topk(x.data_ptr(), n, int(k), float(eps), int(seed) & (2**64 - 1), vals.data_ptr(),
-                            idx.data_ptr(), _stream_handle(stream), C.byref(st))
+                            idx.data_ptr(), _stream_handle(stream, x.device), C.byref(st))
     _abi.check(code)
     return vals, idx, st.as_dict()
 
@@ -110,7 +115,7 @@ def topk_batched(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=N
     sts = (ProfkStats * rows)()
     code = lib().profk_topk_batched(x.data_ptr(), rows, n, x.stride(0), int(k), float(eps),
                                     int(seed) & (2**64 - 1), vals.data_ptr(), idx.data_ptr(),
-                                    _stream_handle(stream), sts)
+                                    _stream_handle(stream, x.device), sts)
     _abi.check(code)
     return vals, idx, [s.as_dict() for s in sts]
 

@@ -41,7 +41,12 @@ class ProfkStats(C.Structure):
     ]
 
     def as_dict(self) -> dict:
-        return {name: getattr(self, name) for name, _ in self._fields_}
+        return dict(zip(_STATS_NAMES, _STATS_FMT.unpack(bytes(self))))
+
+
+_STATS_NAMES = tuple(name for name, _ in ProfkStats._fields_)
+_STATS_FMT = __import__("struct").Struct("=7q2f4iQfi")
+assert _STATS_FMT.size == C.sizeof(ProfkStats)
 
 
 class ProfkError(RuntimeError):

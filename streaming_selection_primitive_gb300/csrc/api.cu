@@ -407,7 +407,9 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
 
   PK_CHECK(ws_alloc(c, L.total));
   st = at<RowState>(c.ws, L.off_state);
-  PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState) * rows, stream));
+  // The sampling path starts every attempt with k_attempt_reset, which
+  // initialises the state of its rows; the exact path needs zeroed state.
+  if (!sampling) PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState) * rows, stream));
   PK_CHECK(pinned(sizeof(int) * rows * 4 + REPORT_BYTES * rows, &hbuf));
 
   if (!sampling) {

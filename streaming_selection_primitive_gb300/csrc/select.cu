@@ -394,6 +394,85 @@ __global__ void __launch_bounds__(SORT_THREADS) k_emit(const unsigned long long*
 }
 
 // ---------------------------------------------------------------------------
+// Descending bitonic sort of 1024*E keys held in shared memory by a block of
+// 1024 threads.  Thread t of warp w holds keys w*32E + r*32 + lane
+// (r = 0..E-1) in registers: compare-exchange partners closer than 32E are
+// in the same warp (a shuffle for distance < 32, a register pair otherwise);
+// only the wider stages go through shared memory, with one barrier each.
+template <int E>
+__device__ __forceinline__ void block_sort_desc(unsigned long long* s) {
+  constexpr int T = 1024;
+  constexpr int P = T * E;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = warp * 32 * E;
+  unsigned long long v[E];
+#pragma unroll
+  for (int r = 0; r < E; ++r) v[r] = s[seg + r * 32 + lane];
+  for (int size = 2; size <= P; size <<= 1) {
+    int j = size >> 1;
+    if (j >= 32 * E) {
+#pragma unroll
+      for (int r = 0; r < E; ++r) s[seg + r * 32 + lane] = v[r];
+      __syncthreads();
+      for (; j >= 32 * E; j >>= 1) {
+        for (int i = threadIdx.x; i < P; i += T) {
+          const int l = i ^ j;
+          if (l > i) {
+            const unsigned long long a = s[i], b = s[l];
+            const bool desc = (i & size) == 0;
+            if (desc ? (a < b) : (a > b)) {
+              s[i] = b;
+              s[l] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int r = 0; r < E; ++r) v[r] = s[seg + r * 32 + lane];
+      __syncthreads();
+    }
+    // Partner in the same lane, register r ^ (jj / 32) (distances 32E/2 .. 32).
+#pragma unroll
+    for (int m = E / 2; m >= 1; m >>= 1) {
+      const int jj = 32 * m;
+      if (jj < size) {
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+          const int r2 = r ^ m;
+          if (r2 > r) {
+            const int i = seg + r * 32 + lane;
+            const bool desc = (i & size) == 0;
+            const unsigned long long a = v[r], b = v[r2];
+            if (desc ? (a < b) : (a > b)) {
+              v[r] = b;
+              v[r2] = a;
+            }
+          }
+        }
+      }
+    }
+    // Partner in lane ^ jj, same register (distances 16 .. 1).
+#pragma unroll
+    for (int jj = 16; jj >= 1; jj >>= 1) {
+      if (jj < size) {
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+          const int i = seg + r * 32 + lane;
+          const bool desc = (i & size) == 0;
+          const unsigned long long o = __shfl_xor_sync(FULL_MASK, v[r], jj);
+          const bool lower = (lane & jj) == 0;
+          v[r] = (desc == lower) ? (v[r] > o ? v[r] : o) : (v[r] < o ? v[r] : o);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < E; ++r) s[seg + r * 32 + lane] = v[r];
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
 // Step 4 in one CTA per row.  The candidates (R <= M keys) are read from L2;
 // 11/11/10/11/11/10-bit MSD passes narrow the bucket that holds the k-th
 // largest key.  As soon as the keys above the bucket plus the bucket itself
@@ -402,7 +481,7 @@ __global__ void __launch_bounds__(SORT_THREADS) k_emit(const unsigned long long*
 // emitted.  The kernel is enqueued before the host has checked k <= R <= M;
 // a row that fails the check is marked skip and its outputs are not touched.
 constexpr int ONE_THREADS = 1024;
-constexpr int ONE_OUT = 16384;   // keys gathered into shared memory (128 KB)
+constexpr int ONE_OUT = 8192;    // keys gathered into shared memory (64 KB)
 constexpr int ONE_MAX_K = 8192;
 constexpr int64_t ONE_MAX_M = 1 << 19;
 
@@ -522,26 +601,15 @@ __global__ void __launch_bounds__(ONE_THREADS) k_refine_one(RefineOneArgs a) {
   }
   __syncthreads();
   const int cnt = static_cast<int>(total < ONE_OUT ? total : ONE_OUT);
-  int P = 1;
+  int P = ONE_THREADS;
   while (P < cnt) P <<= 1;
-  for (int i = tid; i < P; i += ONE_THREADS)
-    if (i >= cnt) s_out[i] = 0ull;
+  for (int i = cnt + tid; i < P; i += ONE_THREADS) s_out[i] = 0ull;  // below every real key
   __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int j = size >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < P; i += ONE_THREADS) {
-        const int l = i ^ j;
-        if (l > i) {
-          const unsigned long long x0 = s_out[i], x1 = s_out[l];
-          const bool desc = (i & size) == 0;
-          if (desc ? (x0 < x1) : (x0 > x1)) {
-            s_out[i] = x1;
-            s_out[l] = x0;
-          }
-        }
-      }
-      __syncthreads();
-    }
+  switch (P / ONE_THREADS) {
+    case 1: block_sort_desc<1>(s_out); break;
+    case 2: block_sort_desc<2>(s_out); break;
+    case 4: block_sort_desc<4>(s_out); break;
+    default: block_sort_desc<8>(s_out); break;
   }
   for (int j = tid; j < static_cast<int>(a.k); j += ONE_THREADS)
     emit_one(s_out[j], row, j, a.k, a.x, a.ld, a.n, a.out_vals, a.out_idx);
