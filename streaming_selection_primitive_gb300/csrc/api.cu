@@ -213,7 +213,7 @@ struct Layout {
   int log2H = 0;
   bool sampling = false;
   size_t off_state = 0, off_lists = 0, off_table = 0, off_draws = 0, off_blockcnt = 0, off_sidx = 0, off_skeys = 0,
-         off_buf = 0, off_sel = 0, total = 0;
+         off_buf = 0, off_sel = 0, off_sort = 0, total = 0;
 };
 
 int64_t draw_budget(int64_t n, int64_t S) {
@@ -259,6 +259,8 @@ Layout make_layout(int64_t rows, int64_t n, int64_t k, int64_t S, int64_t D, int
   }
   L.off_sel = off;
   off = align_up(off + sizeof(unsigned long long) * rows * L.kstride);
+  L.off_sort = off;
+  if (k > small_sort_max()) off = align_up(off + radix_sort_scratch_bytes(k, L.kstride, rows));
   L.total = off;
   return L;
 }
@@ -326,7 +328,8 @@ void launch_exact(const Layout& L, void* ws, const float* x, int64_t ld, int nro
   SelectArgs a{KeySource::Input, x, ld, L.n, nrows, rows, st};
   launch_select(a, static_cast<uint64_t>(L.k), false, 0, stream);
   launch_compact(a, reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, stream);
-  launch_sort_emit(reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, nrows, rows, x, ld, L.n, out_vals, out_idx, stream);
+  launch_sort_emit(reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, nrows, rows, x, ld, L.n, out_vals, out_idx, stream,
+                   nullptr, at<char>(ws, L.off_sort), L.rows);
 }
 
 // SM count and the filter's persistent grid, cached per device.
@@ -474,7 +477,8 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         uint64_t* sel = at<uint64_t>(c.ws, L.off_sel);
         launch_select(ra, 0, false, 0, stream);
         launch_compact(ra, sel, L.kstride, k, stream);
-        launch_sort_emit(sel, L.kstride, k, ng, gl, x, ld, n, out_vals, out_idx, stream, st);
+        launch_sort_emit(sel, L.kstride, k, ng, gl, x, ld, n, out_vals, out_idx, stream, st, at<char>(c.ws, L.off_sort),
+                         L.rows);
       }
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[4], stream));
       PK_CHECK(cudaGetLastError());
@@ -550,7 +554,8 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         uint64_t* sel = at<uint64_t>(c.ws, L.off_sel);
         launch_select(ia, 0, false, 3, stream);
         launch_compact(ia, sel, L.kstride, k, stream);
-        launch_sort_emit(sel, L.kstride, k, static_cast<int>(tie.size()), tl, x, ld, n, out_vals, out_idx, stream, st);
+        launch_sort_emit(sel, L.kstride, k, static_cast<int>(tie.size()), tl, x, ld, n, out_vals, out_idx, stream, st,
+                         at<char>(c.ws, L.off_sort), L.rows);
       }
       PK_CHECK(cudaGetLastError());
       if (grow) {

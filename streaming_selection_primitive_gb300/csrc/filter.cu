@@ -138,9 +138,12 @@ __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
         v[u] = make_float4(f[0], f[1], f[2], f[3]);
       }
     }
-    float m = max_nan(max_nan(v[0].x, v[0].y), max_nan(v[0].z, v[0].w));
+    float mu[U];
 #pragma unroll
-    for (int u = 1; u < U; ++u) m = max_nan(m, max_nan(max_nan(v[u].x, v[u].y), max_nan(v[u].z, v[u].w)));
+    for (int u = 0; u < U; ++u) mu[u] = max_nan(max_nan(v[u].x, v[u].y), max_nan(v[u].z, v[u].w));
+    float m = mu[0];
+#pragma unroll
+    for (int u = 1; u < U; ++u) m = max_nan(m, mu[u]);
     // Masked lanes hold -inf; they reach the slow path only when tau is -inf,
     // and `valid` keeps them out of every count there.
     const bool hit = !(m < tau);
@@ -149,6 +152,7 @@ __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
     if (hit) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
+        if (mu[u] < tau) continue;  // no passer and no NaN among these four
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int e = u * 4 + c;

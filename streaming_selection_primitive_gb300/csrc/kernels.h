@@ -110,10 +110,19 @@ void launch_compact(const SelectArgs& a, uint64_t* out, int64_t out_stride, int6
 
 // Sorts each row's k keys descending (in place in `keys`, row stride
 // key_stride >= next_pow2(k)) and writes values (read from x) and indices.
-// Rows whose state says skip are left untouched when st is given.
+// Rows whose state says skip are left untouched when st is given.  For
+// k > 8192 the keys are radix-sorted when `scratch` (radix_sort_scratch_bytes
+// for all `total_rows` rows of the call) is given, else bitonic-sorted in
+// place (key_stride must then be next_pow2(k)).
 void launch_sort_emit(uint64_t* keys, int64_t key_stride, int64_t k, int nrows, const int* rows,
                       const float* x, int64_t ld, int64_t n, float* out_vals, int64_t* out_idx,
-                      cudaStream_t stream, const RowState* st = nullptr);
+                      cudaStream_t stream, const RowState* st = nullptr, void* scratch = nullptr,
+                      int64_t total_rows = 0);
+size_t radix_sort_scratch_bytes(int64_t k, int64_t key_stride, int64_t rows);
+cudaError_t launch_radix_sort_emit(uint64_t* keys, int64_t key_stride, int64_t k, int nrows, const int* rows,
+                                   void* scratch, int64_t total_rows, const float* x, int64_t ld, int64_t n,
+                                   float* out_vals, int64_t* out_idx, cudaStream_t stream, const RowState* st);
+int64_t small_sort_max();
 int64_t sort_stride(int64_t k);  // key_stride the sort needs for k keys
 
 // Step 4 in one CTA per row for k <= refine_one_max_k() (select.cu): radix

@@ -717,9 +717,16 @@ int64_t refine_one_max_m() { return ONE_MAX_M; }
 
 int64_t sort_stride(int64_t k) { return k > SMALL_SORT_MAX ? next_pow2(k) : k; }
 
+int64_t small_sort_max() { return SMALL_SORT_MAX; }
+
 void launch_sort_emit(uint64_t* keys_u, int64_t key_stride, int64_t k, int nrows, const int* rows, const float* x,
                       int64_t ld, int64_t n, float* out_vals, int64_t* out_idx, cudaStream_t stream,
-                      const RowState* st) {
+                      const RowState* st, void* scratch, int64_t total_rows) {
+  if (k > SMALL_SORT_MAX && scratch) {
+    launch_radix_sort_emit(keys_u, key_stride, k, nrows, rows, scratch, total_rows > 0 ? total_rows : nrows, x, ld,
+                           n, out_vals, out_idx, stream, st);
+    return;
+  }
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(keys_u);
   if (k <= SMALL_SORT_MAX) {
     cudaFuncSetAttribute(k_sort_small, cudaFuncAttributeMaxDynamicSharedMemorySize, SMALL_SORT_MAX * 8);
