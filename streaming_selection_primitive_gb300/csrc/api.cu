@@ -122,8 +122,10 @@ __global__ void k_attempt_init(RowState* st, const int* rows) {
 
 // Start of an attempt for the listed rows: hash table back to "empty",
 // counters to zero, and the selection state ready for tau (rank t).
+// The sort control blocks of the rows (sort_ctl, ctl_words 8-byte words per
+// row) are zeroed too when the attempt's refinement is the radix sort.
 __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int* rows, RowState* st,
-                                unsigned long long t) {
+                                unsigned long long t, unsigned long long* sort_ctl, int ctl_words) {
   pdl_trigger();
   pdl_wait();
   const int row = launch_row(rows);
@@ -134,6 +136,8 @@ __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int*
     tb[i] = ~0ull;
   if (blockIdx.x == 0) {
     RowState& S = st[row];
+    if (sort_ctl)
+      for (int i = threadIdx.x; i < ctl_words; i += blockDim.x) sort_ctl[static_cast<int64_t>(row) * ctl_words + i] = 0;
     for (int b = threadIdx.x; b < HIST_BINS; b += blockDim.x) S.hist[b] = 0;
     if (threadIdx.x == 0) {
       S.R_ge = 0;
@@ -212,6 +216,7 @@ struct Layout {
   int64_t rows = 0, n = 0, k = 0, S = 0, D = 0, M = 0, nbD = 0, kstride = 0;
   int log2H = 0;
   bool sampling = false;
+  bool radix_refine = false;  // step 4 on the filter buffer by the radix sort
   size_t off_state = 0, off_lists = 0, off_table = 0, off_draws = 0, off_blockcnt = 0, off_sidx = 0, off_skeys = 0,
          off_buf = 0, off_sel = 0, off_sort = 0, total = 0;
 };
@@ -260,7 +265,13 @@ Layout make_layout(int64_t rows, int64_t n, int64_t k, int64_t S, int64_t D, int
   L.off_sel = off;
   off = align_up(off + sizeof(unsigned long long) * rows * L.kstride);
   L.off_sort = off;
-  if (k > small_sort_max()) off = align_up(off + radix_sort_scratch_bytes(k, L.kstride, rows));
+  // Radix-sort scratch, for whichever of its two uses this call can have: the
+  // filter buffer (row stride M) and the k selected keys (row stride kstride).
+  L.radix_refine = sampling && !(k <= refine_one_max_k() && M <= refine_one_max_m());
+  size_t sort_bytes = 0;
+  if (k > small_sort_max()) sort_bytes = radix_sort_scratch_bytes(L.kstride, rows);
+  if (L.radix_refine) sort_bytes = std::max(sort_bytes, radix_sort_scratch_bytes(M, rows));
+  off = align_up(off + sort_bytes);
   L.total = off;
   return L;
 }
@@ -329,7 +340,7 @@ void launch_exact(const Layout& L, void* ws, const float* x, int64_t ld, int nro
   launch_select(a, static_cast<uint64_t>(L.k), false, 0, stream);
   launch_compact(a, reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, stream);
   launch_sort_emit(reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, nrows, rows, x, ld, L.n, out_vals, out_idx, stream,
-                   nullptr, at<char>(ws, L.off_sort), L.rows);
+                   st, at<char>(ws, L.off_sort), L.rows);
 }
 
 // SM count and the filter's persistent grid, cached per device.
@@ -403,7 +414,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   int64_t D = sampling ? draw_budget(n, P.S) : 0;
   Layout L = make_layout(rows, n, k, P.S, D, P.M, sampling);
   std::vector<int> pending, fallback, attempt(static_cast<size_t>(rows), 0);
-  bool exact_ran = false, first_filter = true;
+  bool exact_ran = false, tie_ran = false, first_filter = true;
   float filter_ms = -1.f;
   void* hbuf = nullptr;
   RowState* st = nullptr;
@@ -448,8 +459,12 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
           for (auto& ev : t_events.e) PK_CHECK(cudaEventCreate(&ev));
         PK_CHECK(cudaEventRecord(t_events.e[0], stream));
       }
-      launch_kernel(k_attempt_reset, dim3(rb, ng), 1024, 0, stream, at<unsigned long long>(c.ws, L.off_table), L.log2H, gl, st,
-                                                        static_cast<unsigned long long>(P.t));
+      unsigned long long* sort_ctl =
+          L.radix_refine ? static_cast<unsigned long long*>(radix_sort_ctl(at<char>(c.ws, L.off_sort), P.M, rows))
+                         : nullptr;
+      launch_kernel(k_attempt_reset, dim3(rb, ng), 1024, 0, stream, at<unsigned long long>(c.ws, L.off_table),
+                    L.log2H, gl, st, static_cast<unsigned long long>(P.t), sort_ctl,
+                    static_cast<int>(radix_sort_ctl_bytes() / 8));
       // Sampling, with the first pass of the tau selection fused into its
       // last kernel; the two remaining passes follow.
       SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, a, ng, gl, st,
@@ -468,17 +483,14 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
       // count fails the check is voided on the device and left untouched, so
       // the host round trip of the check is off the critical path of the
       // (likely) successful attempt.
-      if (k <= refine_one_max_k() && P.M <= refine_one_max_m()) {
+      if (!L.radix_refine) {
         RefineOneArgs oa{at<unsigned long long>(c.ws, L.off_buf), P.M, ng, gl, st, k, x, ld, n, out_vals, out_idx};
         launch_refine_one(oa, stream);
       } else {
-        launch_refine_init(ng, gl, st, k, P.M, stream);
-        SelectArgs ra{KeySource::Buffer, at<unsigned long long>(c.ws, L.off_buf), P.M, P.M, ng, gl, st};
-        uint64_t* sel = at<uint64_t>(c.ws, L.off_sel);
-        launch_select(ra, 0, false, 0, stream);
-        launch_compact(ra, sel, L.kstride, k, stream);
-        launch_sort_emit(sel, L.kstride, k, ng, gl, x, ld, n, out_vals, out_idx, stream, st, at<char>(c.ws, L.off_sort),
-                         L.rows);
+        // The whole buffer (R <= M keys) is sorted and its first k emitted.
+        RadixSortArgs ra{at<unsigned long long>(c.ws, L.off_buf), P.M, k, SortCount::FromState, ng, gl, rows,
+                         at<char>(c.ws, L.off_sort), true, x, ld, n, out_vals, out_idx, st};
+        PK_CHECK(launch_radix_sort(ra, stream));
       }
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[4], stream));
       PK_CHECK(cudaGetLastError());
@@ -510,7 +522,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
           goto done;
         }
         if (errf) {
-          c.status = PROFK_ERR_CUDA;
+          c.status = (errf & 8u) ? PROFK_ERR_DEVICE_TIMEOUT : PROFK_ERR_CUDA;
           goto done;
         }
         if (static_cast<int64_t>(distinct) < P.S) {
@@ -547,6 +559,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         }
       }
       if (!tie.empty()) {
+        tie_ran = true;
         int* tl = nullptr;
         PK_CHECK(upload_rows(L, c.ws, hbuf, 2, tie, stream, &tl));
         launch_tie_init(static_cast<int>(tie.size()), tl, st, k, stream);
@@ -581,17 +594,24 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
     PK_CHECK(cudaGetLastError());
     exact_ran = true;
   }
-  if (exact_ran) {
-    // The exact selection's first pass counted NaN keys of its rows.
+  if (exact_ran || tie_ran) {
+    // The exact selection's first pass counted NaN keys of its rows; a wait
+    // of the sort that ran out is recorded in the error bits.
     char* rep = static_cast<char*>(hbuf) + sizeof(int) * rows * 4;
     PK_CHECK(cudaMemcpy2DAsync(rep, REPORT_BYTES, st, sizeof(RowState), REPORT_BYTES, rows, cudaMemcpyDeviceToHost,
                                stream));
     PK_CHECK(cudaStreamSynchronize(stream));
     for (int64_t r = 0; r < rows; ++r) {
       unsigned long long q = 0;
+      unsigned errf = 0;
       std::memcpy(&q, rep + REPORT_BYTES * r + offsetof(RowState, sel_nan), 8);
-      if (q) {
+      std::memcpy(&errf, rep + REPORT_BYTES * r + offsetof(RowState, error), 4);
+      if (q && exact_ran) {
         c.status = PROFK_ERR_NAN;
+        goto done;
+      }
+      if (errf & 8u) {
+        c.status = PROFK_ERR_DEVICE_TIMEOUT;
         goto done;
       }
     }

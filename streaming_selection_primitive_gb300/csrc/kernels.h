@@ -98,9 +98,6 @@ void launch_select(const SelectArgs& a, uint64_t init_rank, bool value_only, int
                    cudaStream_t stream);
 // Resolved value key of the tau selection into RowState::tau_key.
 void launch_store_tau(int nrows, const int* rows, RowState* st, cudaStream_t stream);
-// Refinement set-up straight after the filter: rows whose count fails
-// k <= R <= M are marked void on the device (their refinement writes nothing).
-void launch_refine_init(int nrows, const int* rows, RowState* st, int64_t k, int64_t M, cudaStream_t stream);
 // Tie path: set the state to "value ord(tau) resolved, rank k - R_gt left".
 void launch_tie_init(int nrows, const int* rows, RowState* st, int64_t k, cudaStream_t stream);
 
@@ -112,16 +109,40 @@ void launch_compact(const SelectArgs& a, uint64_t* out, int64_t out_stride, int6
 // key_stride >= next_pow2(k)) and writes values (read from x) and indices.
 // Rows whose state says skip are left untouched when st is given.  For
 // k > 8192 the keys are radix-sorted when `scratch` (radix_sort_scratch_bytes
-// for all `total_rows` rows of the call) is given, else bitonic-sorted in
-// place (key_stride must then be next_pow2(k)).
+// of key_stride for all `total_rows` rows of the call) is given, else
+// bitonic-sorted in place (key_stride must then be next_pow2(k)).
 void launch_sort_emit(uint64_t* keys, int64_t key_stride, int64_t k, int nrows, const int* rows,
                       const float* x, int64_t ld, int64_t n, float* out_vals, int64_t* out_idx,
-                      cudaStream_t stream, const RowState* st = nullptr, void* scratch = nullptr,
+                      cudaStream_t stream, RowState* st = nullptr, void* scratch = nullptr,
                       int64_t total_rows = 0);
-size_t radix_sort_scratch_bytes(int64_t k, int64_t key_stride, int64_t rows);
-cudaError_t launch_radix_sort_emit(uint64_t* keys, int64_t key_stride, int64_t k, int nrows, const int* rows,
-                                   void* scratch, int64_t total_rows, const float* x, int64_t ld, int64_t n,
-                                   float* out_vals, int64_t* out_idx, cudaStream_t stream, const RowState* st);
+// Large-row sort and emission (sort.cu).  Which keys a row sorts:
+enum class SortCount {
+  All,          // k keys, every listed row
+  KUnlessSkip,  // k keys, rows whose RowState::skip is clear
+  FromState,    // RowState::R_ge keys, rows with k <= R_ge <= key_stride
+};
+struct RadixSortArgs {
+  unsigned long long* keys;  // rows x key_stride; permuted in place
+  int64_t key_stride;        // also the most keys a row may hold
+  int64_t k;                 // outputs per row: the k largest, descending
+  SortCount mode;
+  int nrows;
+  const int* rows;     // row list, or nullptr for 0..nrows-1
+  int64_t total_rows;  // rows the scratch is sized for (rows are indexed by number)
+  void* scratch;       // radix_sort_scratch_bytes(key_stride, total_rows)
+  bool ctl_zeroed;     // the control block (radix_sort_ctl) is already zero
+  const float* x;
+  int64_t ld;
+  int64_t n;
+  float* out_vals;
+  int64_t* out_idx;
+  RowState* st;  // skip / count source, and where a timed-out wait is reported
+};
+size_t radix_sort_scratch_bytes(int64_t key_stride, int64_t rows);
+void* radix_sort_ctl(void* scratch, int64_t key_stride, int64_t rows);  // per-row control blocks
+size_t radix_sort_ctl_bytes();                                          // one row's control block
+cudaError_t launch_radix_sort(const RadixSortArgs& a, cudaStream_t stream);
+int sms();  // SMs of the current device
 int64_t small_sort_max();
 int64_t sort_stride(int64_t k);  // key_stride the sort needs for k keys
 

@@ -74,32 +74,6 @@ __global__ void k_sel_init(RowState* st, const int* rows, unsigned long long ran
   }
 }
 
-// Refinement set-up, run right after the filter without waiting for the host:
-// a row whose count fails the check k <= R <= M is marked void (skip = 1), so
-// that every later refinement kernel leaves it and its outputs alone.
-__global__ void k_refine_init(RowState* st, const int* rows, unsigned long long k, unsigned long long M) {
-  pdl_trigger();
-  pdl_wait();
-  const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
-  RowState& S = st[row];
-  for (int b = threadIdx.x; b < HIST_BINS; b += blockDim.x) S.hist[b] = 0;
-  if (threadIdx.x == 0) {
-    const unsigned long long R = S.R_ge;
-    const bool ok = k <= R && R <= M;
-    S.sel_prefix = 0;
-    S.sel_rank = k;
-    S.sel_above = 0;
-    S.sel_bucket = 0;
-    S.sel_thresh = ok ? 0ull : ~0ull;
-    S.sel_nan = 0;
-    S.sel_bits = 0;
-    S.sel_done = ok ? 0 : 1;
-    S.done_blocks = 0;
-    S.compact_count = 0;
-    S.skip = ok ? 0u : 1u;
-  }
-}
-
 __global__ void k_tie_init(RowState* st, const int* rows, unsigned long long k) {
   pdl_trigger();
   pdl_wait();
@@ -628,16 +602,23 @@ unsigned blocks_for(int64_t len, int threads, int cap) {
   return static_cast<unsigned>(b);
 }
 
-int g_sms = 0;
+}  // namespace
+
 int sms() {
-  if (!g_sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sms <= 0) g_sms = 1;
+  static int count[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!count[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    count[dev] = v > 0 ? v : 1;
   }
-  return g_sms;
+  return count[dev];
 }
+
+namespace {
+
 
 template <class Src>
 void run_passes(const Src& src, const SelectArgs& a, bool value_only, int first_pass, cudaStream_t stream) {
@@ -675,11 +656,6 @@ void launch_select(const SelectArgs& a, uint64_t init_rank, bool value_only, int
 
 void launch_store_tau(int nrows, const int* rows, RowState* st, cudaStream_t stream) {
   launch_kernel(k_store_tau, nrows, 32, 0, stream, st, rows);
-}
-
-void launch_refine_init(int nrows, const int* rows, RowState* st, int64_t k, int64_t M, cudaStream_t stream) {
-  launch_kernel(k_refine_init, nrows, 256, 0, stream, st, rows, static_cast<unsigned long long>(k),
-                                           static_cast<unsigned long long>(M));
 }
 
 void launch_tie_init(int nrows, const int* rows, RowState* st, int64_t k, cudaStream_t stream) {
@@ -721,10 +697,12 @@ int64_t small_sort_max() { return SMALL_SORT_MAX; }
 
 void launch_sort_emit(uint64_t* keys_u, int64_t key_stride, int64_t k, int nrows, const int* rows, const float* x,
                       int64_t ld, int64_t n, float* out_vals, int64_t* out_idx, cudaStream_t stream,
-                      const RowState* st, void* scratch, int64_t total_rows) {
+                      RowState* st, void* scratch, int64_t total_rows) {
   if (k > SMALL_SORT_MAX && scratch) {
-    launch_radix_sort_emit(keys_u, key_stride, k, nrows, rows, scratch, total_rows > 0 ? total_rows : nrows, x, ld,
-                           n, out_vals, out_idx, stream, st);
+    RadixSortArgs ra{reinterpret_cast<unsigned long long*>(keys_u), key_stride, k,
+                     st ? SortCount::KUnlessSkip : SortCount::All, nrows, rows, total_rows > 0 ? total_rows : nrows,
+                     scratch, false, x, ld, n, out_vals, out_idx, st};
+    launch_radix_sort(ra, stream);
     return;
   }
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(keys_u);

@@ -1,278 +1,532 @@
-// Descending sort of the k selected 64-bit keys when k is too large for one
-// CTA (Prof-K step 4 and the exact path, "Prof-K: Probabilistic One-Pass
-// Filtering for Efficient Top-k Selection", Section 3, stage 4).
+// Descending sort and emission of a row's candidate keys when there are too
+// many for one CTA (Prof-K step 4 on the filter buffer, and the last step of
+// the exact and tie paths; "Prof-K: Probabilistic One-Pass Filtering for
+// Efficient Top-k Selection", Section 3, stage 4).
 //
-// Stable least-significant-digit radix sort, 8-bit digits, on the complement
-// of the key (ascending order of ~key = descending order of key):
-//  * one pre-pass histograms all eight digit positions at once; a digit
-//    position where every key has the same digit is skipped on the device
-//    (the sign and exponent bytes of a top-k usually are), and the
-//    ping-pong buffer of every remaining pass is fixed by the same kernel;
-//  * per pass, three kernels: per-tile digit counts, an exclusive scan of the
-//    counts in (digit, tile) order, and a stable scatter in which a tile of
-//    4096 keys is ranked in four rounds of 1024 keys (warp match for equal
-//    digits, shared per-warp digit counts scanned across warps).
-// No block waits on another block.
+// One persistent kernel per sort.  The keys of a row are cut into G
+// contiguous chunks, one 1024-thread CTA per chunk; all CTAs of the launch are
+// resident together (G x rows <= the SM count, one CTA per SM), so that they
+// can meet at grid barriers (bounded waits on a per-row arrival counter).
+//  1. Histograms of the eight byte positions of the keys, summed over the
+//     chunks; every CTA then derives the same plan from them: a position
+//     where every key has the same byte is skipped, and each byte value's
+//     global start is the exclusive scan of its position's histogram.
+//  2. Stable least-significant-digit radix passes (8-bit digits, on ~key, so
+//     that ascending ~key is descending key) over the VALUE bytes only (the
+//     upper 32 bits).  In a pass a CTA counts its chunk's digits and
+//     publishes the counts at once, ranks its keys stably in shared memory
+//     (a warp splits its keys by digit with nine ballots; per-warp counts are
+//     scanned across warps), finds the counts of all earlier chunks by a
+//     decoupled look-back over their published flags (32 chunks per step,
+//     stopping at the nearest chunk whose inclusive prefix is known), and
+//     writes the chunk out in digit order, so that the keys of one digit
+//     leave as a contiguous run.  A chunk of more than 8192 keys is ranked
+//     and written 8192 keys at a time.
+//  3. The keys are now in value order, equal values in arbitrary order.  If
+//     no run of equal values is longer than 32, every key finds its place
+//     inside its run by counting the run's larger keys (index order), and
+//     the first k positions are written as (value, index).  Otherwise (heavy
+//     ties) the full sort runs: passes over all eight positions, the last of
+//     which writes the output.
+// Output values are decoded from the key (it holds them exactly), except
+// zero, whose sign the key does not keep: it is read from x.  Every wait is
+// bounded; a wait that runs out sets an error bit in the row state.
 #include "kernels.h"
 
 namespace profk {
+
+// Per-row sort control, in the scratch; zero before each sort.
+struct SortCtl {
+  unsigned long long start[8][256];  // digit counts of every position, over all chunks
+  unsigned bar;                      // grid-barrier arrivals
+  unsigned long_run;                 // 1: some run of equal values is longer than 32
+  unsigned pad[30];
+};
+static_assert(sizeof(SortCtl) % 8 == 0, "SortCtl is zeroed in 8-byte words");
+
 namespace {
 
 constexpr int RS_THREADS = 1024;
-constexpr int RS_TILE = 4096;  // keys per tile (4 rounds of 1024)
-constexpr int RS_WARPS = RS_THREADS / 32;
+constexpr int RS_KMAX = 8;                                       // keys per thread in one piece
+constexpr int RS_SUB = RS_THREADS * RS_KMAX;                     // 8192 keys ranked at a time
+constexpr size_t RS_SMEM = sizeof(unsigned long long) * RS_SUB;  // staging of a piece (64 KB)
+constexpr int RUN_MAX = 32;                                      // longest run the fix-up orders
+// Look-back flag: status (2 bits) | pass sequence number (4 bits) | count (58 bits).
+constexpr unsigned long long FLAG_AGG = 1ull << 62;   // the chunk's own digit count
+constexpr unsigned long long FLAG_INCL = 2ull << 62;  // count of this and every earlier chunk
+constexpr int FLAG_SEQ_SHIFT = 58;
+constexpr unsigned long long FLAG_COUNT = (1ull << FLAG_SEQ_SHIFT) - 1;
+constexpr int WAIT_POLLS = 1 << 22;     // bound on one wait (a poll is an L2 round trip)
+constexpr unsigned ERR_SORT_WAIT = 8u;  // RowState::error bit of a wait that ran out
 
-__device__ __forceinline__ unsigned digit_of(unsigned long long key, int pass) {
-  return static_cast<unsigned>((~key) >> (8 * pass)) & 255u;
+__device__ __forceinline__ unsigned digit_of(unsigned long long key, int pos) {
+  return static_cast<unsigned>((~key) >> (8 * pos)) & 255u;
 }
 
-// Per-row sort control, in the workspace (zeroed by the host).
-struct SortCtl {
-  unsigned hist[8][256];
-  int src_of_pass[8];  // 0: keys -> tmp, 1: tmp -> keys, -1: pass skipped
-  int final_in_tmp;
-  int pad[7];
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ bool flag_ready(unsigned long long f, int seq) {
+  return (f >> 62) != 0 && ((f >> FLAG_SEQ_SHIFT) & 15ull) == static_cast<unsigned long long>(seq);
+}
+
+// Lanes of the warp whose digit equals this lane's (9-bit digits; 256 marks
+// a lane without a key): one ballot per bit.
+__device__ __forceinline__ unsigned same_digit_lanes(unsigned d) {
+  unsigned peers = FULL_MASK;
+#pragma unroll
+  for (int b = 0; b < 9; ++b) {
+    const bool bit = (d >> b) & 1u;
+    const unsigned m = __ballot_sync(FULL_MASK, bit);
+    peers &= bit ? m : ~m;
+  }
+  return peers;
+}
+
+// Keys a row sorts, or -1 when the row is left alone.
+__device__ __forceinline__ int64_t row_count(const RadixSortArgs& a, int row) {
+  if (a.mode == SortCount::FromState) {
+    const unsigned long long R = a.st[row].R_ge;
+    const bool ok = static_cast<unsigned long long>(a.k) <= R && R <= static_cast<unsigned long long>(a.key_stride);
+    return ok ? static_cast<int64_t>(R) : -1;
+  }
+  if (a.mode == SortCount::KUnlessSkip && a.st[row].skip) return -1;
+  return a.k;
+}
+
+// Writes output position pos of a row from its key.  The index is checked
+// against the row length, so that a sort that went wrong never reads outside
+// x: such an entry is (NaN, -1).
+__device__ __forceinline__ void emit_key(const RadixSortArgs& a, int row, int64_t pos, unsigned long long kk) {
+  const uint32_t idx = cand_index(kk);
+  const uint32_t vk = static_cast<uint32_t>(kk >> 32);
+  const int64_t o = static_cast<int64_t>(row) * a.k + pos;
+  if (static_cast<int64_t>(idx) < a.n) {
+    a.out_idx[o] = static_cast<int64_t>(idx);
+    a.out_vals[o] = vk == ord_key(0.0f) ? a.x[static_cast<int64_t>(row) * a.ld + idx] : key_to_float(vk);
+  } else {
+    a.out_idx[o] = -1;
+    a.out_vals[o] = __int_as_float(0x7fc00000);
+  }
+}
+
+struct Smem {
+  unsigned long long start[8][256];  // global start of each digit of each position
+  unsigned long long cur[256];       // where the chunk's next key of each digit goes
+  long long base[256];
+  unsigned hist[256], tot[256], texcl[256], wsum[8];
+  int trivial[8];
+  int err;
 };
 
-__global__ void __launch_bounds__(RS_THREADS) k_rs_hist(const unsigned long long* keys, int64_t key_stride,
-                                                       int64_t k, const int* rows, SortCtl* ctl,
-                                                       const RowState* st) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ unsigned h[8][256];
-  const int row = launch_row(rows);
-  if (st && st[row].skip) return;
-  for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS) (&h[0][0])[i] = 0;
-  __syncthreads();
-  const unsigned long long* kr = keys + row * key_stride;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * RS_THREADS + threadIdx.x; i < k;
-       i += static_cast<int64_t>(gridDim.x) * RS_THREADS) {
-    const unsigned long long key = kr[i];
-#pragma unroll
-    for (int p = 0; p < 8; ++p) atomicAdd(&h[p][digit_of(key, p)], 1u);
-  }
-  __syncthreads();
-  SortCtl& c = ctl[row];
-  for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS)
-    if ((&h[0][0])[i]) atomicAdd(&c.hist[0][0] + i, (&h[0][0])[i]);
-}
-
-// Which passes run, and from which buffer.
-__global__ void k_rs_plan(int64_t k, const int* rows, SortCtl* ctl, const RowState* st) {
-  pdl_trigger();
-  pdl_wait();
-  const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
-  if (st && st[row].skip) return;
-  SortCtl& c = ctl[row];
-  __shared__ int trivial[8];
-  if (threadIdx.x < 8) trivial[threadIdx.x] = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x)
-    if (static_cast<int64_t>((&c.hist[0][0])[i]) == k) trivial[i / 256] = 1;
+// Every CTA of the row arrives, then waits until all have (target arrivals).
+__device__ __forceinline__ void grid_sync(SortCtl& c, unsigned target, Smem& sm) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    int in_tmp = 0;
-    for (int p = 0; p < 8; ++p) {
-      if (trivial[p]) {
-        c.src_of_pass[p] = -1;
-      } else {
-        c.src_of_pass[p] = in_tmp;
-        in_tmp ^= 1;
+    __threadfence();
+    atomicAdd(&c.bar, 1u);
+    for (int poll = 0; ld_acquire(&c.bar) < target; ++poll) {
+      if (poll >= WAIT_POLLS) {
+        sm.err = 1;
+        break;
       }
     }
-    c.final_in_tmp = in_tmp;
-  }
-}
-
-// counts[row][digit * ntiles + tile]
-__global__ void __launch_bounds__(RS_THREADS) k_rs_count(const unsigned long long* keys, unsigned long long* tmp,
-                                                        int64_t key_stride, int64_t k, const int* rows,
-                                                        const SortCtl* ctl, unsigned* counts, int pass,
-                                                        const RowState* st) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ unsigned h[256];
-  const int row = launch_row(rows);
-  if (st && st[row].skip) return;
-  const int src = ctl[row].src_of_pass[pass];
-  if (src < 0) return;
-  const unsigned long long* in = (src ? tmp : keys) + row * key_stride;
-  const int ntiles = gridDim.x;
-  for (int i = threadIdx.x; i < 256; i += RS_THREADS) h[i] = 0;
-  __syncthreads();
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * RS_TILE;
-  for (int r = 0; r < RS_TILE / RS_THREADS; ++r) {
-    const int64_t i = t0 + r * RS_THREADS + threadIdx.x;
-    if (i < k) atomicAdd(&h[digit_of(in[i], pass)], 1u);
+    __threadfence();
   }
   __syncthreads();
-  unsigned* cr = counts + static_cast<int64_t>(row) * 256 * ntiles;
-  for (int d = threadIdx.x; d < 256; d += RS_THREADS) cr[static_cast<int64_t>(d) * ntiles + blockIdx.x] = h[d];
 }
 
-// Exclusive scan of one row's 256 * ntiles counts (one block per row).
-__global__ void __launch_bounds__(RS_THREADS) k_rs_scan(unsigned* counts, int ntiles, const int* rows,
-                                                       const SortCtl* ctl, int pass, const RowState* st) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ unsigned s_w[RS_WARPS];
-  __shared__ unsigned s_carry;
-  const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
-  if (st && st[row].skip) return;
-  if (ctl[row].src_of_pass[pass] < 0) return;
-  unsigned* cr = counts + static_cast<int64_t>(row) * 256 * ntiles;
-  const int64_t total = static_cast<int64_t>(256) * ntiles;
+// A piece of cnt keys at `base`: warp w holds positions [w span, (w + 1)
+// span), span = 32 kp; round r, lane l holds w span + 32 r + l, so (warp,
+// round, lane) order is input order.
+__device__ __forceinline__ bool in_piece(int r, int kp, int cnt) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) s_carry = 0;
+  return r < kp && warp * 32 * kp + r * 32 + lane < cnt;
+}
+
+__device__ __forceinline__ void load_piece(const unsigned long long* in, int64_t base, int cnt, int kp,
+                                           unsigned long long (&key)[RS_KMAX]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int r = 0; r < RS_KMAX; ++r)
+    key[r] = in_piece(r, kp, cnt) ? __ldcg(in + base + warp * 32 * kp + r * 32 + lane) : 0ull;
+}
+
+// One stable pass over byte position `pos` of the chunk [lo, hi) (chunk
+// number `chunk`, sequence number `seq` for the flags): in -> out, or to the
+// output when `emit`.
+__device__ __forceinline__ void radix_pass(const RadixSortArgs& a, int row, int64_t chunk, int64_t lo, int64_t hi,
+                                           int pos, int seq, bool emit, const unsigned long long* in,
+                                           unsigned long long* out, unsigned long long* fr, Smem& sm,
+                                           unsigned long long* s_keys) {
+  unsigned short(*cntw)[256] = reinterpret_cast<unsigned short(*)[256]>(s_keys);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const unsigned long long tag = static_cast<unsigned long long>(seq) << FLAG_SEQ_SHIFT;
+  if (threadIdx.x < 256) {
+    sm.hist[threadIdx.x] = 0;
+    sm.cur[threadIdx.x] = sm.start[pos][threadIdx.x];
+  }
   __syncthreads();
-  for (int64_t base = 0; base < total; base += RS_THREADS) {
-    const int64_t i = base + threadIdx.x;
-    const unsigned v = i < total ? cr[i] : 0u;
-    unsigned incl = v;
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
-      if (lane >= o) incl += t;
+  if (lo >= hi) return;  // an empty chunk: the last ones, on which no chunk waits
+  const int nsub = static_cast<int>((hi - lo + RS_SUB - 1) / RS_SUB);
+
+  // Count the chunk's digits and publish the counts (chunk 0's are already
+  // inclusive).  The first piece stays in registers for the ranking.
+  unsigned long long key[RS_KMAX];
+  int cnt = static_cast<int>(hi - lo < RS_SUB ? hi - lo : RS_SUB);
+  int kp = (cnt + RS_THREADS - 1) / RS_THREADS;
+  load_piece(in, lo, cnt, kp, key);
+#pragma unroll
+  for (int r = 0; r < RS_KMAX; ++r)
+    if (r < kp) hist_add(sm.hist, digit_of(key[r], pos), in_piece(r, kp, cnt));
+  for (int s = 1; s < nsub; ++s) {
+    const int64_t b = lo + static_cast<int64_t>(s) * RS_SUB;
+    const int sc = static_cast<int>(hi - b < RS_SUB ? hi - b : RS_SUB);
+    for (int i = threadIdx.x; i < ((sc + 31) & ~31); i += RS_THREADS) {
+      const bool v = i < sc;
+      hist_add(sm.hist, v ? digit_of(__ldcg(in + b + i), pos) : 0u, v);
     }
-    if (lane == 31) s_w[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      const unsigned w = s_w[lane];
-      unsigned wi = w;
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned t = __shfl_up_sync(FULL_MASK, wi, o);
-        if (lane >= o) wi += t;
+  }
+  __syncthreads();
+  if (threadIdx.x < 256)
+    st_relaxed(fr + chunk * 256 + threadIdx.x, (chunk == 0 ? FLAG_INCL : FLAG_AGG) | tag | sm.hist[threadIdx.x]);
+
+  for (int s = 0; s < nsub; ++s) {
+    const int64_t base = lo + static_cast<int64_t>(s) * RS_SUB;
+    if (s > 0) {
+      cnt = static_cast<int>(hi - base < RS_SUB ? hi - base : RS_SUB);
+      kp = (cnt + RS_THREADS - 1) / RS_THREADS;
+      load_piece(in, base, cnt, kp, key);
+    }
+    // Rank among the warp's keys of the same digit, in position order.
+    for (int d = lane; d < 256; d += 32) cntw[warp][d] = 0;
+    __syncwarp();
+    unsigned info[RS_KMAX];  // digit (9 bits) | rank among the warp's keys of that digit << 9
+#pragma unroll
+    for (int r = 0; r < RS_KMAX; ++r) {
+      info[r] = 256u;
+      if (r < kp) {
+        const bool valid = in_piece(r, kp, cnt);
+        const unsigned d = valid ? digit_of(key[r], pos) : 256u;
+        const unsigned peers = same_digit_lanes(d);
+        const unsigned prior = valid ? cntw[warp][d] : 0u;
+        __syncwarp();
+        if (valid && (peers & lt) == 0) cntw[warp][d] = static_cast<unsigned short>(prior + __popc(peers));
+        __syncwarp();
+        info[r] = d | ((prior + __popc(peers & lt)) << 9);
       }
-      s_w[lane] = wi - w;
     }
     __syncthreads();
-    const unsigned carry = s_carry;
-    if (i < total) cr[i] = carry + s_w[warp] + incl - v;
-    __syncthreads();
-    if (threadIdx.x == RS_THREADS - 1) s_carry = carry + s_w[warp] + incl;
-    __syncthreads();
-  }
-}
-
-// Stable scatter of one tile.
-__global__ void __launch_bounds__(RS_THREADS) k_rs_scatter(unsigned long long* keys, unsigned long long* tmp,
-                                                          int64_t key_stride, int64_t k, const int* rows,
-                                                          const SortCtl* ctl, const unsigned* counts, int pass,
-                                                          const RowState* st) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ unsigned short s_wc[RS_WARPS][256];  // per-warp digit counts of a round
-  __shared__ unsigned s_base[256];                // running tile offset per digit
-  const int row = launch_row(rows);
-  if (st && st[row].skip) return;
-  const int src = ctl[row].src_of_pass[pass];
-  if (src < 0) return;
-  const unsigned long long* in = (src ? tmp : keys) + row * key_stride;
-  unsigned long long* out = (src ? keys : tmp) + row * key_stride;
-  const int ntiles = gridDim.x;
-  const unsigned* cr = counts + static_cast<int64_t>(row) * 256 * ntiles;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int d = threadIdx.x; d < 256; d += RS_THREADS) s_base[d] = cr[static_cast<int64_t>(d) * ntiles + blockIdx.x];
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * RS_TILE;
-  for (int r = 0; r < RS_TILE / RS_THREADS; ++r) {
-    const int64_t i = t0 + r * RS_THREADS + threadIdx.x;  // tile order = input order
-    const bool valid = i < k;
-    const unsigned long long key = valid ? in[i] : 0ull;
-    const unsigned d = valid ? digit_of(key, pass) : 256u;  // 256: no digit
-    for (int j = threadIdx.x; j < RS_WARPS * 256; j += RS_THREADS) (&s_wc[0][0])[j] = 0;
-    __syncthreads();
-    const unsigned act = __ballot_sync(FULL_MASK, valid);
-    unsigned peers = 0, below = 0;
-    if (valid) {
-      peers = __match_any_sync(act, d);
-      below = __popc(peers & ((1u << lane) - 1u));
-      if (below == 0) s_wc[warp][d] = static_cast<unsigned short>(__popc(peers));
+    // Per digit, the exclusive scan of the 32 warp counts: four threads per
+    // digit, eight warps each, combined by shuffles among the four.
+    {
+      const int d = threadIdx.x >> 2, q = threadIdx.x & 3;
+      unsigned v[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[i] = cntw[8 * q + i][d];
+        sum += v[i];
+      }
+      unsigned incl = sum;
+      unsigned t = __shfl_up_sync(FULL_MASK, incl, 1, 4);
+      if (q >= 1) incl += t;
+      t = __shfl_up_sync(FULL_MASK, incl, 2, 4);
+      if (q >= 2) incl += t;
+      const unsigned total = __shfl_sync(FULL_MASK, incl, 3, 4);
+      unsigned run = incl - sum;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cntw[8 * q + i][d] = static_cast<unsigned short>(run);
+        run += v[i];
+      }
+      if (q == 0) sm.tot[d] = total;
     }
     __syncthreads();
-    // Per digit: exclusive scan of the warp counts over the warps, added to
-    // the running base; threads 0..255 own one digit each.
-    unsigned round_total = 0;
+    // Piece-local start of each digit (exclusive scan of tot over digits).
     if (threadIdx.x < 256) {
-      unsigned acc = 0;
-      for (int w = 0; w < RS_WARPS; ++w) {
-        const unsigned c = s_wc[w][threadIdx.x];
-        s_wc[w][threadIdx.x] = static_cast<unsigned short>(acc);
-        acc += c;
+      const unsigned v = sm.tot[threadIdx.x];
+      unsigned incl = v;
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += t;
       }
-      round_total = acc;
+      if (lane == 31) sm.wsum[warp] = incl;
+      sm.texcl[threadIdx.x] = incl - v;
     }
     __syncthreads();
-    if (valid) out[s_base[d] + s_wc[warp][d] + below] = key;
+    if (threadIdx.x < 256) {
+      unsigned add = 0;
+      for (int w = 0; w < warp; ++w) add += sm.wsum[w];
+      sm.texcl[threadIdx.x] += add;
+    }
     __syncthreads();
-    if (threadIdx.x < 256) s_base[threadIdx.x] += round_total;
+    // Piece-local positions; then the piece in digit order in shared memory
+    // (the counts are dead once every thread holds its positions).
+#pragma unroll
+    for (int r = 0; r < RS_KMAX; ++r) {
+      const unsigned d = info[r] & 511u;
+      info[r] = d < 256 ? sm.texcl[d] + cntw[warp][d] + (info[r] >> 9) : ~0u;
+    }
     __syncthreads();
+#pragma unroll
+    for (int r = 0; r < RS_KMAX; ++r)
+      if (info[r] != ~0u) s_keys[info[r]] = key[r];
+
+    if (s == 0 && chunk > 0) {
+      // Look-back: four threads per digit, each reading the flags of 8
+      // earlier chunks (32 per step for the four), nearest first; the loads
+      // are issued together and a flag not yet published is polled.
+      // Positions before the first chunk read as an empty inclusive prefix.
+      const int d = threadIdx.x >> 2, q = threadIdx.x & 3;
+      const unsigned gmask = 0xFu << (lane & ~3);
+      unsigned long long excl = 0;
+      bool timed_out = false;
+      for (int64_t j = chunk - 1; j >= 0; j -= 32) {
+        unsigned long long f[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int64_t tt = j - 8 * q - i;
+          f[i] = tt >= 0 ? ld_relaxed(fr + tt * 256 + d) : (FLAG_INCL | tag);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          for (int poll = 0; !flag_ready(f[i], seq); ++poll) {
+            if (poll >= WAIT_POLLS) {
+              timed_out = true;
+              f[i] = FLAG_INCL | tag;  // give up here: adds nothing, ends the walk
+              break;
+            }
+            f[i] = ld_relaxed(fr + (j - 8 * q - i) * 256 + d);
+          }
+        }
+        unsigned long long part = 0;
+        bool found = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (!found) {
+            part += f[i] & FLAG_COUNT;
+            found = (f[i] >> 62) == 2;
+          }
+        }
+        // The nearest thread (lowest q) that met an inclusive prefix ends
+        // the walk; its part and the nearer ones are added.
+        const unsigned fb = (__ballot_sync(gmask, found) >> (lane & ~3)) & 0xFu;
+        const int stop = fb ? __ffs(fb) - 1 : 4;
+        unsigned long long mine = q <= stop ? part : 0ull;
+        mine += __shfl_xor_sync(gmask, mine, 1, 4);
+        mine += __shfl_xor_sync(gmask, mine, 2, 4);
+        excl += mine;
+        if (fb) break;
+      }
+      if (timed_out) sm.err = 1;
+      if (q == 0) {
+        st_relaxed(fr + chunk * 256 + d, FLAG_INCL | tag | ((excl + sm.hist[d]) & FLAG_COUNT));
+        sm.cur[d] += excl;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < 256)
+      sm.base[threadIdx.x] = static_cast<long long>(sm.cur[threadIdx.x]) - static_cast<long long>(sm.texcl[threadIdx.x]);
+    __syncthreads();
+
+    // Position i of the digit-ordered piece goes to base[digit] + i.
+    for (int i = threadIdx.x; i < cnt; i += RS_THREADS) {
+      const unsigned long long kk = s_keys[i];
+      const int64_t p = sm.base[digit_of(kk, pos)] + i;
+      if (!emit) {
+        out[p] = kk;
+      } else if (p < a.k) {
+        emit_key(a, row, p, kk);
+      }
+    }
+    __syncthreads();  // the next piece reuses shared memory
+    if (threadIdx.x < 256) sm.cur[threadIdx.x] += sm.tot[threadIdx.x];
   }
 }
 
-__global__ void __launch_bounds__(RS_THREADS) k_rs_emit(const unsigned long long* keys,
-                                                       const unsigned long long* tmp, int64_t key_stride, int64_t k,
-                                                       const int* rows, const SortCtl* ctl, const float* x,
-                                                       int64_t ld, int64_t n, float* out_vals, int64_t* out_idx,
-                                                       const RowState* st) {
+__global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, SortCtl* ctl, unsigned long long* tmp,
+                                                          unsigned long long* flags, int64_t flag_stride) {
   pdl_trigger();
   pdl_wait();
-  const int row = launch_row(rows);
-  if (st && st[row].skip) return;
-  const unsigned long long* sorted = (ctl[row].final_in_tmp ? tmp : keys) + row * key_stride;
-  for (int64_t j = static_cast<int64_t>(blockIdx.x) * RS_THREADS + threadIdx.x; j < k;
-       j += static_cast<int64_t>(gridDim.x) * RS_THREADS) {
-    const uint32_t idx = cand_index(sorted[j]);
-    const int64_t o = static_cast<int64_t>(row) * k + j;
-    if (static_cast<int64_t>(idx) < n) {
-      out_idx[o] = static_cast<int64_t>(idx);
-      out_vals[o] = x[static_cast<int64_t>(row) * ld + idx];
-    } else {
-      out_idx[o] = -1;
-      out_vals[o] = __int_as_float(0x7fc00000);
+  extern __shared__ unsigned long long s_keys[];  // 64 KB: a piece, its per-warp counts, or histograms
+  __shared__ Smem sm;
+  const int row = launch_row(a.rows);
+  const int64_t len = row_count(a, row);
+  if (len < 0) return;  // every CTA of the row leaves: no barrier is met
+  SortCtl& c = ctl[row];
+  unsigned long long* fr = flags + row * flag_stride;
+  const int64_t G = gridDim.x, chunk = blockIdx.x;
+  const int64_t C = (((len + G - 1) / G) + 31) & ~int64_t(31);
+  const int64_t lo = chunk * C < len ? chunk * C : len;
+  const int64_t hi = lo + C < len ? lo + C : len;
+  unsigned target = 0;
+  if (threadIdx.x == 0) sm.err = 0;
+
+  // 1. Histograms of all positions (and this chunk's flags zeroed).
+  {
+    unsigned(*h)[256] = reinterpret_cast<unsigned(*)[256]>(s_keys);
+    for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS) (&h[0][0])[i] = 0;
+    if (threadIdx.x < 256) fr[chunk * 256 + threadIdx.x] = 0;
+    __syncthreads();
+    for (int64_t i = lo + threadIdx.x; i < lo + ((hi - lo + 31) & ~int64_t(31)); i += RS_THREADS) {
+      const bool valid = i < hi;
+      const unsigned long long key = valid ? __ldcg(a.keys + row * a.key_stride + i) : 0ull;
+#pragma unroll
+      for (int p = 0; p < 8; ++p) hist_add(h[p], digit_of(key, p), valid);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS)
+      if ((&h[0][0])[i]) atomicAdd(&c.start[0][0] + i, static_cast<unsigned long long>((&h[0][0])[i]));
+  }
+  grid_sync(c, target += G, sm);
+  // The plan, the same in every CTA.
+  if (threadIdx.x < 8) sm.trivial[threadIdx.x] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS) {
+    const unsigned long long v = __ldcg(&c.start[0][0] + i);
+    (&sm.start[0][0])[i] = v;
+    if (static_cast<int64_t>(v) == len) sm.trivial[i >> 8] = 1;
+  }
+  __syncthreads();
+  {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < 8) {  // exclusive scan of position `warp`, 8 digits per lane
+      unsigned long long v[8], s = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[j] = sm.start[warp][lane * 8 + j];
+        s += v[j];
+      }
+      unsigned long long incl = s;
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += t;
+      }
+      unsigned long long run = incl - s;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sm.start[warp][lane * 8 + j] = run;
+        run += v[j];
+      }
     }
   }
+  __syncthreads();
+
+  // 2. Value positions.
+  int seq = 0, cur = 0;
+  for (int p = 4; p < 8; ++p) {
+    if (sm.trivial[p]) continue;
+    radix_pass(a, row, chunk, lo, hi, p, seq, false, (cur ? tmp : a.keys) + row * a.key_stride,
+               (cur ? a.keys : tmp) + row * a.key_stride, fr, sm, s_keys);
+    ++seq;
+    cur ^= 1;
+    grid_sync(c, target += G, sm);
+  }
+
+  // 3. Runs of equal values: a run longer than RUN_MAX has equal values
+  // RUN_MAX positions apart.
+  const unsigned long long* srt = (cur ? tmp : a.keys) + row * a.key_stride;
+  for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS)
+    if (i + RUN_MAX < len && (__ldcg(srt + i) >> 32) == (__ldcg(srt + i + RUN_MAX) >> 32)) c.long_run = 1u;
+  grid_sync(c, target += G, sm);
+  if (!__ldcg(&c.long_run)) {
+    // A key's place inside its run of equal values is the run's start plus
+    // the number of the run's larger keys (keys are distinct).
+    for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS) {
+      const unsigned long long kk = __ldcg(srt + i);
+      const uint32_t v = static_cast<uint32_t>(kk >> 32);
+      int64_t s = i, e = i + 1;
+      while (s > 0 && static_cast<uint32_t>(__ldcg(srt + s - 1) >> 32) == v) --s;
+      while (e < len && static_cast<uint32_t>(__ldcg(srt + e) >> 32) == v) ++e;
+      int64_t p = s;
+      for (int64_t j = s; j < e; ++j) p += __ldcg(srt + j) > kk;
+      if (p < a.k) emit_key(a, row, p, kk);
+    }
+  } else {
+    // Heavy ties: the full sort, from the value order reached so far.
+    int lastp = -1;
+    for (int p = 0; p < 8; ++p)
+      if (!sm.trivial[p]) lastp = p;
+    for (int p = 0; p < 8; ++p) {
+      if (sm.trivial[p]) continue;
+      radix_pass(a, row, chunk, lo, hi, p, seq, p == lastp, (cur ? tmp : a.keys) + row * a.key_stride,
+                 (cur ? a.keys : tmp) + row * a.key_stride, fr, sm, s_keys);
+      ++seq;
+      cur ^= 1;
+      if (p != lastp) grid_sync(c, target += G, sm);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && sm.err && a.st) atomicOr(&a.st[row].error, ERR_SORT_WAIT);
+}
+
+struct Scratch {
+  unsigned long long* tmp;
+  unsigned long long* flags;
+  int64_t flag_stride;
+  SortCtl* ctl;
+};
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// Chunks per row: no chunk shorter than 32 keys, and all CTAs of the launch
+// (chunks x rows) resident at once, one per SM.
+int64_t chunks_per_row(int64_t key_stride, int64_t nrows) {
+  int64_t g = sms() / (nrows > 0 ? nrows : 1);
+  const int64_t by_len = (key_stride + 31) / 32;
+  if (g > by_len) g = by_len;
+  return g < 1 ? 1 : g;
+}
+
+Scratch carve(void* scratch, int64_t key_stride, int64_t rows) {
+  Scratch s;
+  char* p = static_cast<char*>(scratch);
+  s.tmp = reinterpret_cast<unsigned long long*>(p);
+  p += align256(sizeof(unsigned long long) * key_stride * rows);
+  s.flag_stride = chunks_per_row(key_stride, 1) * 256;
+  s.flags = reinterpret_cast<unsigned long long*>(p);
+  p += align256(sizeof(unsigned long long) * s.flag_stride * rows);
+  s.ctl = reinterpret_cast<SortCtl*>(p);
+  return s;
 }
 
 }  // namespace
 
-size_t radix_sort_scratch_bytes(int64_t k, int64_t key_stride, int64_t rows) {
-  const int64_t ntiles = (k + RS_TILE - 1) / RS_TILE;
-  const size_t tmp = sizeof(unsigned long long) * key_stride * rows;
-  const size_t counts = sizeof(unsigned) * 256 * ntiles * rows;
-  const size_t ctl = sizeof(SortCtl) * rows;
-  return ((tmp + 255) & ~size_t(255)) + ((counts + 255) & ~size_t(255)) + ((ctl + 255) & ~size_t(255));
+size_t radix_sort_scratch_bytes(int64_t key_stride, int64_t rows) {
+  return align256(sizeof(unsigned long long) * key_stride * rows) +
+         align256(sizeof(unsigned long long) * chunks_per_row(key_stride, 1) * 256 * rows) +
+         align256(sizeof(SortCtl) * rows);
 }
 
-cudaError_t launch_radix_sort_emit(uint64_t* keys_u, int64_t key_stride, int64_t k, int nrows, const int* rows,
-                                   void* scratch, int64_t total_rows, const float* x, int64_t ld, int64_t n,
-                                   float* out_vals, int64_t* out_idx, cudaStream_t stream, const RowState* st) {
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(keys_u);
-  const int64_t ntiles = (k + RS_TILE - 1) / RS_TILE;
-  char* p = static_cast<char*>(scratch);
-  // Scratch regions are indexed by row number, so they are sized for all
-  // `total_rows` rows of the call (a row list may hold any of them).
-  const size_t tmp_bytes = sizeof(unsigned long long) * key_stride * total_rows;
-  unsigned long long* tmp = reinterpret_cast<unsigned long long*>(p);
-  p += (tmp_bytes + 255) & ~size_t(255);
-  unsigned* counts = reinterpret_cast<unsigned*>(p);
-  p += (sizeof(unsigned) * 256 * ntiles * total_rows + 255) & ~size_t(255);
-  SortCtl* ctl = reinterpret_cast<SortCtl*>(p);
-  cudaError_t e = cudaMemsetAsync(ctl, 0, sizeof(SortCtl) * total_rows, stream);
-  if (e != cudaSuccess) return e;
-  const unsigned hb = static_cast<unsigned>(ntiles < 256 ? ntiles : 256);
-  launch_kernel(k_rs_hist, dim3(hb, nrows), RS_THREADS, 0, stream, keys, key_stride, k, rows, ctl, st);
-  launch_kernel(k_rs_plan, dim3(nrows), 256, 0, stream, k, rows, ctl, st);
-  for (int pass = 0; pass < 8; ++pass) {
-    launch_kernel(k_rs_count, dim3(static_cast<unsigned>(ntiles), nrows), RS_THREADS, 0, stream, keys, tmp,
-                  key_stride, k, rows, ctl, counts, pass, st);
-    launch_kernel(k_rs_scan, dim3(nrows), RS_THREADS, 0, stream, counts, static_cast<int>(ntiles), rows, ctl, pass,
-                  st);
-    launch_kernel(k_rs_scatter, dim3(static_cast<unsigned>(ntiles), nrows), RS_THREADS, 0, stream, keys, tmp,
-                  key_stride, k, rows, ctl, counts, pass, st);
+void* radix_sort_ctl(void* scratch, int64_t key_stride, int64_t rows) { return carve(scratch, key_stride, rows).ctl; }
+
+size_t radix_sort_ctl_bytes() { return sizeof(SortCtl); }
+
+cudaError_t launch_radix_sort(const RadixSortArgs& a, cudaStream_t stream) {
+  const Scratch s = carve(a.scratch, a.key_stride, a.total_rows);
+  if (!a.ctl_zeroed) {
+    const cudaError_t e = cudaMemsetAsync(s.ctl, 0, sizeof(SortCtl) * a.total_rows, stream);
+    if (e != cudaSuccess) return e;
   }
-  const unsigned eb = static_cast<unsigned>((k + RS_THREADS - 1) / RS_THREADS < 1024 ? (k + RS_THREADS - 1) / RS_THREADS
-                                                                                    : 1024);
-  return launch_kernel(k_rs_emit, dim3(eb, nrows), RS_THREADS, 0, stream, keys, tmp, key_stride, k, rows, ctl, x, ld,
-                       n, out_vals, out_idx, st);
+  const unsigned G = static_cast<unsigned>(chunks_per_row(a.key_stride, a.nrows));
+  cudaFuncSetAttribute(k_rs_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(RS_SMEM));
+  launch_kernel(k_rs_sort, dim3(G, static_cast<unsigned>(a.nrows)), RS_THREADS, RS_SMEM, stream, a, s.ctl, s.tmp,
+                s.flags, s.flag_stride);
+  return cudaGetLastError();
 }
 
 }  // namespace profk

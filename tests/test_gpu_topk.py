@@ -133,7 +133,8 @@ def test_nondefault_stream(pk, cuda_device):
 
 
 @pytest.mark.parametrize("rows,n,ld,k", [(4, 1 << 20, 1 << 20, 16), (3, 1_000_003, 1_000_008, 100),
-                                         (16, 1 << 18, 1 << 18, 1), (2, 5000, 5000, 5000)])
+                                         (16, 1 << 18, 1 << 18, 1), (2, 5000, 5000, 5000),
+                                         (3, 1 << 22, 1 << 22, 10_000)])
 def test_batched(pk, cuda_device, rows, n, ld, k):
     base = workloads.normal_rows(rows, ld, rows + n, cuda_device)
     x = base[:, :n]
@@ -157,5 +158,37 @@ def test_batched_rows_retry_alone(pk, cuda_device):
     h = x.cpu().numpy()
     for r in range(rows):
         ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 5, row=r, force=force)
+        assert_same(vals[r], idx[r], ov, oi, f"row {r}")
+        assert (sts[r]["attempts"], sts[r]["path"], sts[r]["R_first"]) == (ost.attempts, ost.path, ost.R_first)
+
+
+@pytest.mark.parametrize("gen,n,k", [("normal", 1 << 24, 8193), ("normal", 1 << 24, 1 << 18),
+                                     ("uniform", (1 << 24) + 3, 20_000), ("pareto", 1 << 24, 100_000),
+                                     ("sorted_normal", 1 << 23, 1 << 16), ("levels16", 1 << 23, 50_000)])
+def test_large_k(pk, cuda_device, gen, n, k):
+    """k beyond one CTA's sort: the filter buffer is radix-sorted (levels16
+    takes the tie path, whose k selected keys are radix-sorted)."""
+    x = workloads.GENERATORS[gen](n, 17, cuda_device)
+    for s in range(2):
+        check_call(pk, x, k, 1e-3, 90 + s)
+
+
+def test_large_k_fallback(pk, cuda_device):
+    x = workloads.normal(1 << 22, 5, cuda_device)
+    st = check_call(pk, x, 20_000, 1e-3, 3, force={"S": 32768, "t": 1}, max_attempts=2)
+    assert st["path"] == pk.PATH_FALLBACK
+
+
+def test_batched_large_k_rows_retry_alone(pk, cuda_device):
+    # About half the rows fail each attempt, so the radix sort runs on row lists.
+    rows, n, k = 4, 1 << 20, 9000
+    x = workloads.normal_rows(rows, n, 77, cuda_device)
+    force = {"S": 8192, "t": 71, "M": 11000}
+    for o, v in ((pk.OPT_FORCE_S, 8192), (pk.OPT_FORCE_T, 71), (pk.OPT_FORCE_M, 11000)):
+        pk.set_option(o, v)
+    vals, idx, sts = pk.topk_batched(x, k, 1e-3, 6)
+    h = x.cpu().numpy()
+    for r in range(rows):
+        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 6, row=r, force=force)
         assert_same(vals[r], idx[r], ov, oi, f"row {r}")
         assert (sts[r]["attempts"], sts[r]["path"], sts[r]["R_first"]) == (ost.attempts, ost.path, ost.R_first)
