@@ -122,8 +122,8 @@ __global__ void k_attempt_init(RowState* st, const int* rows) {
 
 // Start of an attempt for the listed rows: hash table back to "empty",
 // counters to zero, and the selection state ready for tau (rank t).
-// The sort control blocks of the rows (sort_ctl, ctl_words 8-byte words per
-// row) are zeroed too when the attempt's refinement is the radix sort.
+// The refinement's control block of each row (ref_ctl, ctl_words 8-byte
+// words per row) is zeroed too.
 __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int* rows, RowState* st,
                                 unsigned long long t, unsigned long long* sort_ctl, int ctl_words) {
   pdl_trigger();
@@ -218,7 +218,7 @@ struct Layout {
   bool sampling = false;
   bool radix_refine = false;  // step 4 on the filter buffer by the radix sort
   size_t off_state = 0, off_lists = 0, off_table = 0, off_draws = 0, off_blockcnt = 0, off_sidx = 0, off_skeys = 0,
-         off_buf = 0, off_sel = 0, off_sort = 0, total = 0;
+         off_buf = 0, off_sel = 0, off_sort = 0, off_refine = 0, total = 0;
 };
 
 int64_t draw_budget(int64_t n, int64_t S) {
@@ -267,11 +267,13 @@ Layout make_layout(int64_t rows, int64_t n, int64_t k, int64_t S, int64_t D, int
   L.off_sort = off;
   // Radix-sort scratch, for whichever of its two uses this call can have: the
   // filter buffer (row stride M) and the k selected keys (row stride kstride).
-  L.radix_refine = sampling && !(k <= refine_one_max_k() && M <= refine_one_max_m());
+  L.radix_refine = sampling && !(k <= refine_grid_max_k() && M <= refine_grid_max_m());
   size_t sort_bytes = 0;
   if (k > small_sort_max()) sort_bytes = radix_sort_scratch_bytes(L.kstride, rows);
   if (L.radix_refine) sort_bytes = std::max(sort_bytes, radix_sort_scratch_bytes(M, rows));
   off = align_up(off + sort_bytes);
+  L.off_refine = off;
+  if (sampling && !L.radix_refine) off = align_up(off + refine_grid_scratch_bytes(rows));
   L.total = off;
   return L;
 }
@@ -459,12 +461,13 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
           for (auto& ev : t_events.e) PK_CHECK(cudaEventCreate(&ev));
         PK_CHECK(cudaEventRecord(t_events.e[0], stream));
       }
-      unsigned long long* sort_ctl =
+      // The refinement's control blocks start every attempt at zero.
+      unsigned long long* ref_ctl =
           L.radix_refine ? static_cast<unsigned long long*>(radix_sort_ctl(at<char>(c.ws, L.off_sort), P.M, rows))
-                         : nullptr;
+                         : static_cast<unsigned long long*>(refine_grid_ctl(at<char>(c.ws, L.off_refine)));
+      const int ref_words = static_cast<int>((L.radix_refine ? radix_sort_ctl_bytes() : refine_grid_ctl_bytes()) / 8);
       launch_kernel(k_attempt_reset, dim3(rb, ng), 1024, 0, stream, at<unsigned long long>(c.ws, L.off_table),
-                    L.log2H, gl, st, static_cast<unsigned long long>(P.t), sort_ctl,
-                    static_cast<int>(radix_sort_ctl_bytes() / 8));
+                    L.log2H, gl, st, static_cast<unsigned long long>(P.t), ref_ctl, ref_words);
       // Sampling, with the first pass of the tau selection fused into its
       // last kernel; the two remaining passes follow.
       SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, a, ng, gl, st,
@@ -484,8 +487,8 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
       // the host round trip of the check is off the critical path of the
       // (likely) successful attempt.
       if (!L.radix_refine) {
-        RefineOneArgs oa{at<unsigned long long>(c.ws, L.off_buf), P.M, ng, gl, st, k, x, ld, n, out_vals, out_idx};
-        launch_refine_one(oa, stream);
+        RefineGridArgs ga{at<unsigned long long>(c.ws, L.off_buf), P.M, ng, gl, st, k, x, ld, n, out_vals, out_idx};
+        PK_CHECK(launch_refine_grid(ga, at<char>(c.ws, L.off_refine), rows, stream));
       } else {
         // The whole buffer (R <= M keys) is sorted and its first k emitted.
         RadixSortArgs ra{at<unsigned long long>(c.ws, L.off_buf), P.M, k, SortCount::FromState, ng, gl, rows,

@@ -167,6 +167,19 @@ void launch_refine_one(const RefineOneArgs& a, cudaStream_t stream);
 int64_t refine_one_max_k();
 int64_t refine_one_max_m();
 
+// Step 4 on the filter path for k <= refine_grid_max_k() and M <=
+// refine_grid_max_m() (refine.cu): the same result as launch_refine_one, by
+// one CTA per SM with grid barriers.  `scratch` holds
+// refine_grid_scratch_bytes(total_rows); its control blocks (refine_grid_ctl,
+// refine_grid_ctl_bytes each, indexed by row) must be zero at launch.
+using RefineGridArgs = RefineOneArgs;
+size_t refine_grid_scratch_bytes(int64_t rows);
+void* refine_grid_ctl(void* scratch);
+size_t refine_grid_ctl_bytes();
+int64_t refine_grid_max_k();
+int64_t refine_grid_max_m();
+cudaError_t launch_refine_grid(const RefineGridArgs& a, void* scratch, int64_t total_rows, cudaStream_t stream);
+
 // Filter pass.
 struct FilterArgs {
   const float* x;

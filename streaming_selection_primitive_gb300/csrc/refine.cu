@@ -1,0 +1,288 @@
+// Prof-K step 4 for k <= 8192 ("Prof-K: Probabilistic One-Pass Filtering for
+// Efficient Top-k Selection", Section 3, stage 4): the exact top-k of the
+// filter's candidate buffer, sorted, written as (value, index).
+//
+// One persistent kernel, one 1024-thread CTA per SM and contiguous chunk of
+// the candidates; all CTAs of the launch are resident together (chunks x rows
+// <= the SM count), so that they can meet at grid barriers (bounded waits on
+// a per-row arrival counter).  11/11/10/11/11/10-bit MSD passes over the
+// 64-bit keys narrow the bucket that holds the k-th largest key: each CTA
+// histograms its chunk's keys inside the current bucket, the histograms meet
+// in global atomics, and after the barrier every CTA reads the same totals
+// and takes the same decision.  As soon as the keys above the bucket plus
+// the bucket fit the gather budget (at least 2k, at most 8192 keys), every
+// CTA appends its keys at or above the bucket's bound to a gather list, and
+// after one more barrier the first CTA sorts the list in shared memory and
+// writes the first k.  Values are decoded from the keys (they hold them
+// exactly), except zero, whose sign the key does not keep: it is read from x.
+//
+// The kernel is enqueued before the host has checked k <= R <= M; a row that
+// fails the check is marked skip and its outputs are not touched.
+#include "kernels.h"
+#include "blocksort.cuh"
+
+namespace profk {
+
+// Per-row control block, zeroed at the start of every attempt.
+struct RefineCtl {
+  unsigned hist[6][HIST_BINS];  // pass histograms, summed over the chunks
+  unsigned bar;                 // grid-barrier arrivals
+  unsigned cursor;              // gather-list length
+  unsigned pad[62];
+};
+static_assert(sizeof(RefineCtl) % 8 == 0, "RefineCtl is zeroed in 8-byte words");
+
+namespace {
+
+constexpr int RG_THREADS = 1024;
+constexpr int RG_KPT = 4;                         // keys per thread held across the passes
+constexpr int RG_PIECE = RG_THREADS * RG_KPT;     // 4096
+constexpr int RG_OUT = 8192;                      // gather capacity (64 KB of shared memory)
+constexpr int RG_MAX_K = 8192;
+constexpr int64_t RG_MAX_M = int64_t(1) << 19;
+constexpr int WAIT_POLLS = 1 << 22;  // bound on one barrier wait (a poll is an L2 round trip)
+constexpr unsigned ERR_WAIT = 8u;    // RowState::error bit of a wait that ran out
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Every CTA of the row arrives, then waits until all have (target arrivals).
+__device__ __forceinline__ void grid_sync(unsigned* bar, unsigned target, int* err) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    for (int poll = 0; ld_acquire(bar) < target; ++poll) {
+      if (poll >= WAIT_POLLS) {
+        *err = 1;
+        break;
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+// Block-wide exclusive scan of one u64 per thread (thread order).
+__device__ __forceinline__ unsigned long long excl_scan(unsigned long long v, unsigned long long* sw) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long incl = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(FULL_MASK, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sw[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long w = sw[lane];
+    unsigned long long wi = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(FULL_MASK, wi, o);
+      if (lane >= o) wi += t;
+    }
+    sw[lane] = wi - w;
+  }
+  __syncthreads();
+  const unsigned long long r = sw[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a, RefineCtl* ctl,
+                                                              unsigned long long* gather) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ unsigned long long s_out[];  // RG_OUT keys: the first CTA's final sort
+  __shared__ unsigned h[HIST_BINS];
+  __shared__ unsigned long long sw[32];
+  __shared__ int s_digit, s_err;
+  __shared__ unsigned long long s_above, s_count;
+  const int row = launch_row(a.rows);
+  RowState& S = a.st[row];
+  RefineCtl& c = ctl[row];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const unsigned long long R = S.R_ge;
+  const unsigned long long k = static_cast<unsigned long long>(a.k);
+  if (!(k <= R && R <= static_cast<unsigned long long>(a.M))) {
+    if (blockIdx.x == 0 && tid == 0) S.skip = 1;
+    return;  // every CTA of the row leaves: no barrier is met
+  }
+  if (tid == 0) {
+    s_err = 0;
+    if (blockIdx.x == 0) S.skip = 0;
+  }
+  const int64_t len = static_cast<int64_t>(R);
+  const int64_t G = gridDim.x;
+  const int64_t C = (((len + G - 1) / G) + 31) & ~int64_t(31);
+  const int64_t lo = blockIdx.x * C < len ? blockIdx.x * C : len;
+  const int64_t hi = lo + C < len ? lo + C : len;
+  const unsigned long long* keys = a.buf + static_cast<int64_t>(row) * a.M;
+  const bool held = hi - lo <= RG_PIECE;  // the chunk stays in registers across the passes
+  unsigned long long kk[RG_KPT];
+  if (held) {
+#pragma unroll
+    for (int r = 0; r < RG_KPT; ++r) {
+      const int64_t i = lo + r * RG_THREADS + tid;
+      kk[r] = i < hi ? __ldcg(keys + i) : 0ull;
+    }
+  }
+  const unsigned long long budget = k * 2 < 2048 ? 2048 : (k * 2 > RG_OUT ? RG_OUT : k * 2);
+  unsigned long long prefix = 0, want = k, thresh = 0, total = k;
+  int bits = 0;
+  unsigned target = 0;
+#pragma unroll 1
+  for (int p = 0; p < 6; ++p) {
+    // Digits from the top: 11, 11, 10 | 11, 11, 10 bits (shifts 53, 42, 32, 21, 10, 0).
+    const int width = p % 3 == 2 ? 10 : 11;
+    const int shift = (p < 3 ? 53 : 21) - 11 * (p % 3) + (p % 3 == 2 ? 1 : 0);
+    const int nb = 1 << width, hs = shift + width;
+    for (int b = tid; b < nb; b += RG_THREADS) h[b] = 0;
+    __syncthreads();
+    for (int64_t base = lo; base < hi; base += RG_PIECE) {
+#pragma unroll
+      for (int r = 0; r < RG_KPT; ++r) {
+        const int64_t i = base + r * RG_THREADS + tid;
+        const unsigned long long key = held ? kk[r] : (i < hi ? __ldcg(keys + i) : 0ull);
+        const bool m = i < hi && (bits == 0 || (key >> hs) == prefix);
+        hist_add(h, static_cast<uint32_t>(key >> shift) & (nb - 1), m);
+      }
+    }
+    __syncthreads();
+    for (int b = tid; b < nb; b += RG_THREADS)
+      if (h[b]) atomicAdd(&c.hist[p][b], h[b]);
+    grid_sync(&c.bar, target += static_cast<unsigned>(G), &s_err);
+    // Every CTA finds the same digit: the bins counted down from the top,
+    // thread t owning nb / 1024 of them.
+    if (tid == 0) {
+      s_digit = 0;
+      s_above = 0;
+      s_count = 0;
+    }
+    const int per = nb / RG_THREADS;
+    const int top = nb - 1 - tid * per;
+    unsigned hv[2] = {0u, 0u};
+    unsigned long long local = 0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      if (q < per) {
+        hv[q] = __ldcg(&c.hist[p][top - q]);
+        local += hv[q];
+      }
+    }
+    const unsigned long long excl = excl_scan(local, sw);
+    if (excl < want && want <= excl + local) {
+      unsigned long long acc = excl;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (q < per && want <= acc + hv[q]) {
+          s_digit = top - q;
+          s_above = acc;
+          s_count = hv[q];
+          break;
+        }
+        acc += hv[q];
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << width) | static_cast<unsigned long long>(s_digit);
+    want -= s_above;
+    bits += width;
+    const unsigned long long above_all = k - want;  // keys above the bucket, all in the top-k
+    if (s_count == want || shift == 0) {  // the whole bucket is in the top-k: keys >= its bound are exactly k
+      thresh = prefix << shift;
+      total = k;
+      break;
+    }
+    if (above_all + s_count <= budget) {  // gather the whole bucket and finish in shared memory
+      thresh = prefix << shift;
+      total = above_all + s_count;
+      break;
+    }
+    __syncthreads();
+  }
+  // Gather every key >= thresh (exactly `total` of them, at most RG_OUT).
+  unsigned long long* gr = gather + static_cast<int64_t>(row) * RG_OUT;
+  for (int64_t base = lo; base < hi; base += RG_PIECE) {
+#pragma unroll
+    for (int r = 0; r < RG_KPT; ++r) {
+      const int64_t i = base + r * RG_THREADS + tid;
+      const unsigned long long key = held ? kk[r] : (i < hi ? __ldcg(keys + i) : 0ull);
+      const bool sel = i < hi && key >= thresh;
+      const unsigned m = __ballot_sync(FULL_MASK, sel);
+      if (m) {
+        unsigned pos0 = 0;
+        if (lane == 0) pos0 = atomicAdd(&c.cursor, static_cast<unsigned>(__popc(m)));
+        pos0 = __shfl_sync(FULL_MASK, pos0, 0);
+        if (sel) {
+          const unsigned pos = pos0 + __popc(m & ((1u << lane) - 1u));
+          if (pos < RG_OUT) gr[pos] = key;
+        }
+      }
+    }
+  }
+  grid_sync(&c.bar, target += static_cast<unsigned>(G), &s_err);
+  if (s_err && tid == 0) atomicOr(&S.error, ERR_WAIT);
+  if (blockIdx.x != 0) return;
+  const int cnt = static_cast<int>(total < RG_OUT ? total : RG_OUT);
+  int P = RG_THREADS;
+  while (P < cnt) P <<= 1;
+  for (int i = tid; i < P; i += RG_THREADS) s_out[i] = i < cnt ? __ldcg(gr + i) : 0ull;  // 0: below every real key
+  __syncthreads();
+  switch (P / RG_THREADS) {
+    case 1: block_sort_desc<1>(s_out); break;
+    case 2: block_sort_desc<2>(s_out); break;
+    case 4: block_sort_desc<4>(s_out); break;
+    default: block_sort_desc<8>(s_out); break;
+  }
+  for (int j = tid; j < static_cast<int>(a.k); j += RG_THREADS) {
+    const unsigned long long key = s_out[j];
+    const uint32_t idx = cand_index(key);
+    const uint32_t vk = static_cast<uint32_t>(key >> 32);
+    const int64_t o = static_cast<int64_t>(row) * a.k + j;
+    // The index is checked against the row length, so that a selection that
+    // went wrong never reads outside x: such an entry is (NaN, -1).
+    if (static_cast<int64_t>(idx) < a.n) {
+      a.out_idx[o] = static_cast<int64_t>(idx);
+      a.out_vals[o] = vk == ord_key(0.0f) ? a.x[static_cast<int64_t>(row) * a.ld + idx] : key_to_float(vk);
+    } else {
+      a.out_idx[o] = -1;
+      a.out_vals[o] = __int_as_float(0x7fc00000);
+    }
+  }
+}
+
+}  // namespace
+
+size_t refine_grid_scratch_bytes(int64_t rows) {
+  return ((sizeof(RefineCtl) * rows + 255) & ~size_t(255)) + sizeof(unsigned long long) * RG_OUT * rows;
+}
+
+void* refine_grid_ctl(void* scratch) { return scratch; }
+
+size_t refine_grid_ctl_bytes() { return sizeof(RefineCtl); }
+
+int64_t refine_grid_max_k() { return RG_MAX_K; }
+
+int64_t refine_grid_max_m() { return RG_MAX_M; }
+
+cudaError_t launch_refine_grid(const RefineGridArgs& a, void* scratch, int64_t total_rows, cudaStream_t stream) {
+  RefineCtl* ctl = static_cast<RefineCtl*>(scratch);
+  unsigned long long* gather = reinterpret_cast<unsigned long long*>(
+      static_cast<char*>(scratch) + ((sizeof(RefineCtl) * total_rows + 255) & ~size_t(255)));
+  // Chunks per row: all CTAs (chunks x rows) resident at once, one per SM,
+  // and no chunk shorter than 256 keys.
+  int64_t G = sms() / (a.nrows > 0 ? a.nrows : 1);
+  const int64_t by_len = (a.M + 255) / 256;
+  if (G > by_len) G = by_len;
+  if (G < 1) G = 1;
+  cudaFuncSetAttribute(k_refine_grid, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(sizeof(unsigned long long) * RG_OUT));
+  launch_kernel(k_refine_grid, dim3(static_cast<unsigned>(G), static_cast<unsigned>(a.nrows)), RG_THREADS,
+                sizeof(unsigned long long) * RG_OUT, stream, a, ctl, gather);
+  return cudaGetLastError();
+}
+
+}  // namespace profk
