@@ -27,7 +27,9 @@
 //     inside its run by counting the run's larger keys (index order), and
 //     the first k positions are written as (value, index).  Otherwise (heavy
 //     ties) the full sort runs: passes over all eight positions, the last of
-//     which writes the output.
+//     which writes the output.  When the histograms already prove a run longer
+//     than 32 (fewer than len / 32 distinct values are possible), steps 2-3
+//     are skipped and the full sort runs at once.
 // Output values are decoded from the key (it holds them exactly), except
 // zero, whose sign the key does not keep: it is read from x.  Every wait is
 // bounded; a wait that runs out sets an error bit in the row state.
@@ -129,6 +131,7 @@ struct Smem {
   long long base[256];
   unsigned hist[256], tot[256], texcl[256], wsum[8];
   int trivial[8];
+  unsigned distinct[8];  // byte values present at each position
   int err;
 };
 
@@ -406,11 +409,15 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp < 8) {  // exclusive scan of position `warp`, 8 digits per lane
       unsigned long long v[8], s = 0;
+      unsigned present = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         v[j] = sm.start[warp][lane * 8 + j];
         s += v[j];
+        present += v[j] != 0;
       }
+      for (int o = 16; o >= 1; o >>= 1) present += __shfl_xor_sync(FULL_MASK, present, o);
+      if (lane == 0) sm.distinct[warp] = present;
       unsigned long long incl = s;
       for (int o = 1; o < 32; o <<= 1) {
         const unsigned long long t = __shfl_up_sync(FULL_MASK, incl, o);
@@ -426,38 +433,47 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
   }
   __syncthreads();
 
-  // 2. Value positions.
+  // When the value bytes allow fewer than len / RUN_MAX distinct values,
+  // some value repeats more than RUN_MAX times: the full sort is certain to
+  // be needed and the value passes would be wasted.
+  unsigned long long distinct_max = 1;
+  for (int p = 4; p < 8; ++p) distinct_max *= sm.distinct[p];
+  bool full = len > RUN_MAX * static_cast<int64_t>(distinct_max);
   int seq = 0, cur = 0;
-  for (int p = 4; p < 8; ++p) {
-    if (sm.trivial[p]) continue;
-    radix_pass(a, row, chunk, lo, hi, p, seq, false, (cur ? tmp : a.keys) + row * a.key_stride,
-               (cur ? a.keys : tmp) + row * a.key_stride, fr, sm, s_keys);
-    ++seq;
-    cur ^= 1;
-    grid_sync(c, target += G, sm);
-  }
-
-  // 3. Runs of equal values: a run longer than RUN_MAX has equal values
-  // RUN_MAX positions apart.
-  const unsigned long long* srt = (cur ? tmp : a.keys) + row * a.key_stride;
-  for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS)
-    if (i + RUN_MAX < len && (__ldcg(srt + i) >> 32) == (__ldcg(srt + i + RUN_MAX) >> 32)) c.long_run = 1u;
-  grid_sync(c, target += G, sm);
-  if (!__ldcg(&c.long_run)) {
-    // A key's place inside its run of equal values is the run's start plus
-    // the number of the run's larger keys (keys are distinct).
-    for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS) {
-      const unsigned long long kk = __ldcg(srt + i);
-      const uint32_t v = static_cast<uint32_t>(kk >> 32);
-      int64_t s = i, e = i + 1;
-      while (s > 0 && static_cast<uint32_t>(__ldcg(srt + s - 1) >> 32) == v) --s;
-      while (e < len && static_cast<uint32_t>(__ldcg(srt + e) >> 32) == v) ++e;
-      int64_t p = s;
-      for (int64_t j = s; j < e; ++j) p += __ldcg(srt + j) > kk;
-      if (p < a.k) emit_key(a, row, p, kk);
+  if (!full) {
+    // 2. Value positions.
+    for (int p = 4; p < 8; ++p) {
+      if (sm.trivial[p]) continue;
+      radix_pass(a, row, chunk, lo, hi, p, seq, false, (cur ? tmp : a.keys) + row * a.key_stride,
+                 (cur ? a.keys : tmp) + row * a.key_stride, fr, sm, s_keys);
+      ++seq;
+      cur ^= 1;
+      grid_sync(c, target += G, sm);
     }
-  } else {
-    // Heavy ties: the full sort, from the value order reached so far.
+    // 3. Runs of equal values: a run longer than RUN_MAX has equal values
+    // RUN_MAX positions apart.
+    const unsigned long long* srt = (cur ? tmp : a.keys) + row * a.key_stride;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS)
+      if (i + RUN_MAX < len && (__ldcg(srt + i) >> 32) == (__ldcg(srt + i + RUN_MAX) >> 32)) c.long_run = 1u;
+    grid_sync(c, target += G, sm);
+    full = __ldcg(&c.long_run) != 0;
+    if (!full) {
+      // A key's place inside its run of equal values is the run's start plus
+      // the number of the run's larger keys (keys are distinct).
+      for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS) {
+        const unsigned long long kk = __ldcg(srt + i);
+        const uint32_t v = static_cast<uint32_t>(kk >> 32);
+        int64_t s = i, e = i + 1;
+        while (s > 0 && static_cast<uint32_t>(__ldcg(srt + s - 1) >> 32) == v) --s;
+        while (e < len && static_cast<uint32_t>(__ldcg(srt + e) >> 32) == v) ++e;
+        int64_t p = s;
+        for (int64_t j = s; j < e; ++j) p += __ldcg(srt + j) > kk;
+        if (p < a.k) emit_key(a, row, p, kk);
+      }
+    }
+  }
+  if (full) {
+    // Heavy ties: the full sort (from whatever order the keys are in).
     int lastp = -1;
     for (int p = 0; p < 8; ++p)
       if (!sm.trivial[p]) lastp = p;
