@@ -122,10 +122,11 @@ __global__ void k_attempt_init(RowState* st, const int* rows) {
 
 // Start of an attempt for the listed rows: hash table back to "empty",
 // counters to zero, and the selection state ready for tau (rank t).
-// The refinement's control block of each row (ref_ctl, ctl_words 8-byte
-// words per row) is zeroed too.
+// The control blocks of each row's sampling (sample_ctl, sample_words 8-byte
+// words per row) and refinement (sort_ctl, ctl_words) are zeroed too.
 __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int* rows, RowState* st,
-                                unsigned long long t, unsigned long long* sort_ctl, int ctl_words) {
+                                unsigned long long t, unsigned long long* sort_ctl, int ctl_words,
+                                unsigned long long* sample_ctl, int sample_words) {
   pdl_trigger();
   pdl_wait();
   const int row = launch_row(rows);
@@ -138,6 +139,8 @@ __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int*
     RowState& S = st[row];
     if (sort_ctl)
       for (int i = threadIdx.x; i < ctl_words; i += blockDim.x) sort_ctl[static_cast<int64_t>(row) * ctl_words + i] = 0;
+    for (int i = threadIdx.x; i < sample_words; i += blockDim.x)
+      sample_ctl[static_cast<int64_t>(row) * sample_words + i] = 0;
     for (int b = threadIdx.x; b < HIST_BINS; b += blockDim.x) S.hist[b] = 0;
     if (threadIdx.x == 0) {
       S.R_ge = 0;
@@ -218,7 +221,7 @@ struct Layout {
   bool sampling = false;
   bool radix_refine = false;  // step 4 on the filter buffer by the radix sort
   size_t off_state = 0, off_lists = 0, off_table = 0, off_draws = 0, off_blockcnt = 0, off_sidx = 0, off_skeys = 0,
-         off_buf = 0, off_sel = 0, off_sort = 0, off_refine = 0, total = 0;
+         off_buf = 0, off_sel = 0, off_sort = 0, off_refine = 0, off_sctl = 0, total = 0;
 };
 
 int64_t draw_budget(int64_t n, int64_t S) {
@@ -261,6 +264,8 @@ Layout make_layout(int64_t rows, int64_t n, int64_t k, int64_t S, int64_t D, int
     off = align_up(off + sizeof(uint32_t) * rows * S);
     L.off_buf = off;
     off = align_up(off + sizeof(unsigned long long) * rows * M);
+    L.off_sctl = off;
+    off = align_up(off + sample_tau_ctl_bytes() * rows);
   }
   L.off_sel = off;
   off = align_up(off + sizeof(unsigned long long) * rows * L.kstride);
@@ -467,17 +472,16 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
                          : static_cast<unsigned long long*>(refine_grid_ctl(at<char>(c.ws, L.off_refine)));
       const int ref_words = static_cast<int>((L.radix_refine ? radix_sort_ctl_bytes() : refine_grid_ctl_bytes()) / 8);
       launch_kernel(k_attempt_reset, dim3(rb, ng), 1024, 0, stream, at<unsigned long long>(c.ws, L.off_table),
-                    L.log2H, gl, st, static_cast<unsigned long long>(P.t), ref_ctl, ref_words);
-      // Sampling, with the first pass of the tau selection fused into its
-      // last kernel; the two remaining passes follow.
+                    L.log2H, gl, st, static_cast<unsigned long long>(P.t), ref_ctl, ref_words,
+                    at<unsigned long long>(c.ws, L.off_sctl), static_cast<int>(sample_tau_ctl_bytes() / 8));
+      // Sampling and tau in one kernel (its stage time is reported as the
+      // sampling's; the threshold stage is then empty).
       SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, a, ng, gl, st,
                     at<unsigned long long>(c.ws, L.off_table), at<uint32_t>(c.ws, L.off_draws),
                     at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
-                    at<uint32_t>(c.ws, L.off_skeys), true, static_cast<unsigned long long>(P.t)};
-      launch_sample(sa, stream);
+                    at<uint32_t>(c.ws, L.off_skeys), false, static_cast<unsigned long long>(P.t)};
+      PK_CHECK(launch_sample_tau(sa, at<char>(c.ws, L.off_sctl), stream));
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[1], stream));
-      SelectArgs ta{KeySource::SampleKeys, at<uint32_t>(c.ws, L.off_skeys), P.S, P.S, ng, gl, st};
-      launch_select(ta, 0, true, 1, stream);  // its last pass stores tau
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[2], stream));
       FilterArgs fa{x, ld, n, P.M, ng, gl, st, at<unsigned long long>(c.ws, L.off_buf), filter_grid(cps)};
       launch_filter(fa, stream);

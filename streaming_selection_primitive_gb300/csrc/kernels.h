@@ -91,6 +91,13 @@ void launch_sample(const SampleArgs& a, cudaStream_t stream);
 // Same, with Philox key word 1 = storage row + key_row0 (a single stored row
 // can then reproduce any row's stream).
 void launch_sample_rows(const SampleArgs& a, int64_t key_row0, cudaStream_t stream);
+// Steps 1 and 2 of the main path in one persistent kernel: the sample (sidx,
+// skeys, RowState::distinct) and tau (RowState::tau_key, rank a.t) of each
+// listed row.  `ctl` holds rows x sample_tau_ctl_bytes(), indexed by row and
+// zero at launch; the hash tables must be empty.  a.draws and a.blockcnt
+// are not used.
+size_t sample_tau_ctl_bytes();
+cudaError_t launch_sample_tau(const SampleArgs& a, void* ctl, cudaStream_t stream);
 
 // Radix selection of the rank-th largest key per row.  init_rank > 0 resets the
 // state of each row first; otherwise the state is taken as it is (tie path).
