@@ -49,9 +49,19 @@ def measured_peaks():
 
 
 def filter_source_hash() -> str:
+    """Hash of the source the filter kernel is compiled from: filter.cu,
+    common.cuh, and the parts of kernels.h it uses (the PDL helpers, the launch
+    helper and FilterArgs)."""
+    csrc = ROOT / "streaming_selection_primitive_gb300" / "csrc"
     h = hashlib.sha256()
-    for name in ("filter.cu", "common.cuh", "kernels.h"):
-        h.update((ROOT / "streaming_selection_primitive_gb300" / "csrc" / name).read_bytes())
+    for name in ("filter.cu", "common.cuh"):
+        h.update((csrc / name).read_bytes())
+    k = (csrc / "kernels.h").read_text()
+    start = k.index("__device__ __forceinline__ void pdl_wait()")
+    end = k.index("\n}\n", k.index("inline cudaError_t launch_kernel")) + 3
+    h.update(k[start:end].encode())
+    m = re.search(r"struct FilterArgs \{.*?\};", k, flags=re.S)
+    h.update(m.group(0).encode())
     return h.hexdigest()[:16]
 
 

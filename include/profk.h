@@ -121,7 +121,7 @@ int profk_topk_batched(const float* x, int64_t rows, int64_t n, int64_t ld, int6
 /* Parameters (S, t, M) for one row of length n at budget eps.
  *   mode PROFK_PARAMS_DEFAULT: S from the older version's Theorem 5,
  *     S* = (z log2(k) / 2)^(2/3) (k(n-k))^(1/3) with z = 2 Phi^{-1}(1-eps/2),
- *     rounded and clamped to [32768, 131072] (its Algorithm 1, lines 1-4);
+ *     rounded and clamped to [32768, 131072] (its Algorithm 1, the sample-size step);
  *     t and M from the corrected Algorithm 1 (Eq 10 or 11, then Eq 12) with
  *     z = Phi^{-1}(1-eps/2); then 1 <= t <= S and k <= M <= n.
  *   mode PROFK_PARAMS_OLD: the older Algorithm 1 literally (Eq 6 t,

@@ -21,7 +21,7 @@ Older version (same title, mirrored page):
 
 Default rule used by the library (a reading, because the two versions conflict):
 S from the older version's Theorem 5 with its clamp, rounding and log2 (its
-Algorithm 1, lines 1-4), and t, M from the corrected Algorithm 1 (lines 5-15)
+Algorithm 1, its sample-size step), and t, M from the corrected Algorithm 1 (its t and M steps)
 with z = Phi^{-1}(1 - eps/2), then 1 <= t <= S and k <= M <= N.  The older
 t-rule sets t = 1 exactly where recall failure is likely (its own text derives
 the bound in the wrong direction), so it is kept only as a named function and
@@ -101,7 +101,7 @@ def params_exact(N: int, k: int, S: int, eps: float, eps_a: float | None = None,
 
 
 def threshold_rank_fast(N: int, k: int, S: int, eps: float) -> int:
-    """Algorithm 1 lines 5-14: Eq 10 (Cornish-Fisher) or Eq 11 (Poisson)."""
+    """Corrected Algorithm 1, the t step: Eq 10 (Cornish-Fisher) or Eq 11 (Poisson)."""
     z = norm_ppf(1.0 - eps / 2)
     mu = (k - 1) * S / N
     if mu >= 15:
@@ -118,14 +118,14 @@ def threshold_rank_fast(N: int, k: int, S: int, eps: float) -> int:
 
 
 def buffer_capacity_fast(N: int, S: int, t: int, eps: float) -> int:
-    """Algorithm 1 line 15: Eq 12, Wilson-Hilferty quantile of Gamma(t,1)."""
+    """Corrected Algorithm 1, the M step: Eq 12, Wilson-Hilferty quantile of Gamma(t,1)."""
     z = norm_ppf(1.0 - eps / 2)
     h = 1.0 / (9.0 * t)
     return math.ceil((N + 1) / (S + 1) * t * (1.0 - h + z * math.sqrt(h)) ** 3)
 
 
 def params_fast(N: int, k: int, S: int, eps: float):
-    """Algorithm 1 lines 5-15 for a given S, then 1 <= t <= S and k <= M <= N."""
+    """Corrected Algorithm 1 (t and M steps) for a given S, then 1 <= t <= S and k <= M <= N."""
     t = min(max(threshold_rank_fast(N, k, S, eps), 1), S)
     M = min(max(buffer_capacity_fast(N, S, t, eps), k), N)
     return t, M
@@ -194,7 +194,7 @@ S_MAX_OLD = 131072
 
 def sample_size_old(N: int, k: int, eps: float, s_min: int = S_MIN_OLD,
                     s_max: int = S_MAX_OLD, cost_ratio: float = 1.0) -> int:
-    """Older Algorithm 1 lines 1-4: z = 2 Phi^{-1}(1-eps/2), S* with log2, round, clamp."""
+    """Older Algorithm 1, the sample-size step: z = 2 Phi^{-1}(1-eps/2), S* with log2, round, clamp."""
     z = 2.0 * norm_ppf(1.0 - eps / 2)
     s = s_thm5(N, k, z, cost_ratio) if k > 1 else 0.0
     return int(min(s_max, max(s_min, math.floor(s + 0.5))))
@@ -202,7 +202,7 @@ def sample_size_old(N: int, k: int, eps: float, s_min: int = S_MIN_OLD,
 
 def params_old(N: int, k: int, eps: float, s_min: int = S_MIN_OLD, s_max: int = S_MAX_OLD,
                cost_ratio: float = 1.0):
-    """Older Algorithm 1, literally (lines 1-9)."""
+    """Older Algorithm 1, literally (all of its steps)."""
     z = 2.0 * norm_ppf(1.0 - eps / 2)
     alpha = k / N
     S = sample_size_old(N, k, eps, s_min, s_max, cost_ratio)

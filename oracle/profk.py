@@ -97,7 +97,7 @@ def tie_path(x: np.ndarray, tau, k: int):
 def profk(x: np.ndarray, k: int, eps: float, seed: int, row: int = 0, *, max_attempts: int = 6,
           mode: int = P.MODE_DEFAULT, tie_exit: bool = True, force=None):
     """One row of Prof-K.  ``force`` may override (S, t, M) as a dict; a forced
-    S recomputes t and M from it (Algorithm 1 lines 5-15) unless those are
+    S recomputes t and M from it (the corrected Algorithm 1, t and M steps) unless those are
     forced as well.  Any override routes through sampling."""
     x = np.asarray(x, dtype=np.float32)
     if np.isnan(x).any():

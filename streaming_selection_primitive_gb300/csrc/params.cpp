@@ -2,10 +2,10 @@
 //
 // Sources ("Prof-K: Probabilistic One-Pass Filtering for Efficient Top-k
 // Selection"; two versions of the page exist and are cited separately):
-//  * older version, Theorem 5 (Eq 14) and its Algorithm 1, lines 1-4:
+//  * older version, Theorem 5 (Eq 14) and its Algorithm 1, the sample-size step:
 //      z = 2 Phi^{-1}(1 - eps/2),  S* = (z log2(k) / 2)^(2/3) (k (n-k))^(1/3),
 //      S = clamp(round(S*), 32768, 131072);
-//  * corrected version, Algorithm 1 lines 5-15 (Appendix B, Eq 9-12), with
+//  * corrected version, Algorithm 1, the t and M steps (Appendix B, Eq 9-12), with
 //    z = Phi^{-1}(1 - eps/2) by Acklam's rational approximation:
 //      mu = (k-1) S / n;
 //      mu >= 15: t = ceil(mu + z sigma + (z^2 - 1)/6) + 1,

@@ -58,7 +58,7 @@ def test_acklam_within_stated_bound():
 
 def test_z_values():
     assert P.norm_ppf(1 - 5e-4) == pytest.approx(3.2905267, abs=1e-6)
-    assert 2 * P.norm_ppf(1 - 5e-4) == pytest.approx(6.58, abs=0.005)  # older Algorithm 1, line 1
+    assert 2 * P.norm_ppf(1 - 5e-4) == pytest.approx(6.58, abs=0.005)  # older Algorithm 1, its z
 
 
 def test_wilson_hilferty_at_t1_overestimates_by_about_3_percent():
