@@ -11,15 +11,16 @@
 // in global atomics, and after the barrier every CTA reads the same totals
 // and takes the same decision.  As soon as the keys above the bucket plus
 // the bucket fit the gather budget (at least 2k, at most 8192 keys), every
-// CTA appends its keys at or above the bucket's bound to a gather list, and
-// after one more barrier the first CTA sorts the list in shared memory and
-// writes the first k.  Values are decoded from the keys (they hold them
-// exactly), except zero, whose sign the key does not keep: it is read from x.
+// CTA appends its keys at or above the bucket's bound to a gather list.
+// After one more barrier every CTA reads the list, and each key's output
+// position is the number of listed keys above it, counted by one warp per key
+// over all warps of the launch; the first k are written.  Values are decoded
+// from the keys (they hold them exactly), except zero, whose sign the key
+// does not keep: it is read from x.
 //
 // The kernel is enqueued before the host has checked k <= R <= M; a row that
 // fails the check is marked skip and its outputs are not touched.
 #include "kernels.h"
-#include "blocksort.cuh"
 
 namespace profk {
 
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
                                                               unsigned long long* gather) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ unsigned long long s_out[];  // RG_OUT keys: the first CTA's final sort
+  extern __shared__ unsigned long long s_out[];  // RG_OUT keys: the gather list
   __shared__ unsigned h[HIST_BINS];
   __shared__ unsigned long long sw[32];
   __shared__ int s_digit, s_err;
@@ -225,31 +226,31 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
   }
   grid_sync(&c.bar, target += static_cast<unsigned>(G), &s_err);
   if (s_err && tid == 0) atomicOr(&S.error, ERR_WAIT);
-  if (blockIdx.x != 0) return;
+  // Every CTA reads the gather list; a key's output position is the number
+  // of listed keys above it (keys are distinct), counted by one warp per key,
+  // the keys spread over all warps of the launch.
   const int cnt = static_cast<int>(total < RG_OUT ? total : RG_OUT);
-  int P = RG_THREADS;
-  while (P < cnt) P <<= 1;
-  for (int i = tid; i < P; i += RG_THREADS) s_out[i] = i < cnt ? __ldcg(gr + i) : 0ull;  // 0: below every real key
+  for (int i = tid; i < cnt; i += RG_THREADS) s_out[i] = __ldcg(gr + i);
   __syncthreads();
-  switch (P / RG_THREADS) {
-    case 1: block_sort_desc<1>(s_out); break;
-    case 2: block_sort_desc<2>(s_out); break;
-    case 4: block_sort_desc<4>(s_out); break;
-    default: block_sort_desc<8>(s_out); break;
-  }
-  for (int j = tid; j < static_cast<int>(a.k); j += RG_THREADS) {
-    const unsigned long long key = s_out[j];
-    const uint32_t idx = cand_index(key);
-    const uint32_t vk = static_cast<uint32_t>(key >> 32);
-    const int64_t o = static_cast<int64_t>(row) * a.k + j;
-    // The index is checked against the row length, so that a selection that
-    // went wrong never reads outside x: such an entry is (NaN, -1).
-    if (static_cast<int64_t>(idx) < a.n) {
-      a.out_idx[o] = static_cast<int64_t>(idx);
-      a.out_vals[o] = vk == ord_key(0.0f) ? a.x[static_cast<int64_t>(row) * a.ld + idx] : key_to_float(vk);
-    } else {
-      a.out_idx[o] = -1;
-      a.out_vals[o] = __int_as_float(0x7fc00000);
+  const int warp = tid >> 5;
+  for (int e = blockIdx.x * (RG_THREADS / 32) + warp; e < cnt; e += G * (RG_THREADS / 32)) {
+    const unsigned long long key = s_out[e];
+    unsigned above = 0;
+    for (int j = lane; j < cnt; j += 32) above += s_out[j] > key;
+    for (int o = 16; o >= 1; o >>= 1) above += __shfl_xor_sync(FULL_MASK, above, o);
+    if (lane == 0 && above < k) {
+      const uint32_t idx = cand_index(key);
+      const uint32_t vk = static_cast<uint32_t>(key >> 32);
+      const int64_t o = static_cast<int64_t>(row) * a.k + above;
+      // The index is checked against the row length, so that a selection
+      // that went wrong never reads outside x: such an entry is (NaN, -1).
+      if (static_cast<int64_t>(idx) < a.n) {
+        a.out_idx[o] = static_cast<int64_t>(idx);
+        a.out_vals[o] = vk == ord_key(0.0f) ? a.x[static_cast<int64_t>(row) * a.ld + idx] : key_to_float(vk);
+      } else {
+        a.out_idx[o] = -1;
+        a.out_vals[o] = __int_as_float(0x7fc00000);
+      }
     }
   }
 }
