@@ -81,15 +81,16 @@ __device__ __forceinline__ unsigned long long table_try_home(unsigned long long*
   return atomicCAS(table + hash_slot(u, log2H), EMPTY_SLOT, table_entry(u, i));
 }
 
-__device__ __forceinline__ void table_finish(const SampleArgs& a, int row, unsigned long long* table, uint32_t u,
-                                             int64_t i, unsigned long long prev) {
+// Returns the slot that holds u (values never move once placed).
+__device__ __forceinline__ uint64_t table_finish(const SampleArgs& a, int row, unsigned long long* table, uint32_t u,
+                                                 int64_t i, unsigned long long prev) {
   const uint64_t H = 1ull << a.log2H;
   const unsigned long long entry = table_entry(u, i);
   uint64_t slot = hash_slot(u, a.log2H);
-  if (prev == EMPTY_SLOT) return;
+  if (prev == EMPTY_SLOT) return slot;
   if (static_cast<uint32_t>(prev >> 32) == u) {
     atomicMin(table + slot, entry);
-    return;
+    return slot;
   }
   slot = (slot + 1) & (H - 1);
   for (uint64_t seen = 1; seen < H;) {
@@ -103,21 +104,22 @@ __device__ __forceinline__ void table_finish(const SampleArgs& a, int row, unsig
       const uint64_t sq = (slot + q) & (H - 1);
       if (v[q] == EMPTY_SLOT) {
         prev = atomicCAS(table + sq, EMPTY_SLOT, entry);
-        if (prev == EMPTY_SLOT) return;
+        if (prev == EMPTY_SLOT) return sq;
         if (static_cast<uint32_t>(prev >> 32) == u) {
           atomicMin(table + sq, entry);
-          return;
+          return sq;
         }
         adv = q + 1;  // taken by another value: continue after it
       } else if (static_cast<uint32_t>(v[q] >> 32) == u) {
         atomicMin(table + sq, entry);
-        return;
+        return sq;
       }
     }
     slot = (slot + adv) & (H - 1);
     seen += adv;
   }
   atomicOr(&a.st[row].error, 2u);
+  return 0;
 }
 
 __device__ __forceinline__ void table_insert(const SampleArgs& a, int row, unsigned long long* table, uint32_t u,
@@ -440,6 +442,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   uint32_t uh[ST_HELD] = {0u, 0u};
   float vh[ST_HELD] = {0.f, 0.f};
   unsigned long long ph[ST_HELD] = {EMPTY_SLOT, EMPTY_SLOT};
+  uint64_t sh[ST_HELD] = {0, 0};  // the slot that holds each held draw's value
 #pragma unroll
   for (int j = 0; j < ST_HELD; ++j) {
     const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
 #pragma unroll
   for (int j = 0; j < ST_HELD; ++j) {
     const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
-    if (j < rounds && i < hi) table_finish(a, row, table, uh[j], i, ph[j]);
+    if (j < rounds && i < hi) sh[j] = table_finish(a, row, table, uh[j], i, ph[j]);
   }
   for (int j = ST_HELD; j < rounds; ++j) {
     const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
@@ -471,7 +474,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   for (int j = 0; j < ST_HELD; ++j) {
     if (j < rounds) {
       const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
-      first_h[j] = i < hi && first_position(table, a.log2H, uh[j]) == static_cast<uint32_t>(i);
+      // The table is complete: the slot's draw is the smallest draw of u.
+      first_h[j] = i < hi && static_cast<uint32_t>(__ldcg(table + sh[j])) == static_cast<uint32_t>(i);
       cnt += __syncthreads_count(first_h[j]);
     }
   }
