@@ -50,19 +50,19 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
-// Every CTA of the row arrives, then waits until all have (target arrivals).
+// Every CTA of the row arrives (a release: the CTA's writes, ordered before
+// it by the block barrier, become visible with it), then waits until all
+// have (target arrivals; acquire loads of the arrival count).
 __device__ __forceinline__ void grid_sync(unsigned* bar, unsigned target, int* err) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(bar, 1u);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
     for (int poll = 0; ld_acquire(bar) < target; ++poll) {
       if (poll >= WAIT_POLLS) {
         *err = 1;
         break;
       }
     }
-    __threadfence();
   }
   __syncthreads();
 }

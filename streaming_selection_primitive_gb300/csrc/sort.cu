@@ -23,13 +23,15 @@
 //     leave as a contiguous run.  A chunk of more than 8192 keys is ranked
 //     and written 8192 keys at a time.
 //  3. The keys are now in value order, equal values in arbitrary order.  If
-//     no run of equal values is longer than 32, every key finds its place
-//     inside its run by counting the run's larger keys (index order), and
-//     the first k positions are written as (value, index).  Otherwise (heavy
-//     ties) the full sort runs: passes over all eight positions, the last of
-//     which writes the output.  When the histograms already prove a run longer
-//     than 32 (fewer than len / 32 distinct values are possible), steps 2-3
-//     are skipped and the full sort runs at once.
+//     no run of equal values is longer than 256, each run is put in index
+//     order: a warp places every key of a run at the run's start plus the
+//     number of the run's larger keys; the first k positions are written as
+//     (value, index).
+//     Otherwise (heavy ties) the full sort runs: passes over all eight
+//     positions, the last of which writes the output.  When the histograms
+//     already prove a run longer than 256 (fewer than len / 256 distinct
+//     values are possible), steps 2-3 are skipped and the full sort runs at
+//     once.
 // Output values are decoded from the key (it holds them exactly), except
 // zero, whose sign the key does not keep: it is read from x.  Every wait is
 // bounded; a wait that runs out sets an error bit in the row state.
@@ -52,7 +54,7 @@ constexpr int RS_THREADS = 1024;
 constexpr int RS_KMAX = 8;                                       // keys per thread in one piece
 constexpr int RS_SUB = RS_THREADS * RS_KMAX;                     // 8192 keys ranked at a time
 constexpr size_t RS_SMEM = sizeof(unsigned long long) * RS_SUB;  // staging of a piece (64 KB)
-constexpr int RUN_MAX = 32;                                      // longest run the fix-up orders
+constexpr int RUN_MAX = 256;   // runs up to this long are ordered by a warp
 // Look-back flag: status (2 bits) | pass sequence number (4 bits) | count (58 bits).
 constexpr unsigned long long FLAG_AGG = 1ull << 62;   // the chunk's own digit count
 constexpr unsigned long long FLAG_INCL = 2ull << 62;  // count of this and every earlier chunk
@@ -132,22 +134,23 @@ struct Smem {
   unsigned hist[256], tot[256], texcl[256], wsum[8];
   int trivial[8];
   unsigned distinct[8];  // byte values present at each position
+  unsigned nruns;  // runs of 2 .. RUN_MAX keys starting in this chunk
   int err;
 };
 
-// Every CTA of the row arrives, then waits until all have (target arrivals).
+// Every CTA of the row arrives (a release: the CTA's writes, ordered before
+// it by the block barrier, become visible with it), then waits until all
+// have (target arrivals; acquire loads of the arrival count).
 __device__ __forceinline__ void grid_sync(SortCtl& c, unsigned target, Smem& sm) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&c.bar, 1u);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&c.bar) : "memory");
     for (int poll = 0; ld_acquire(&c.bar) < target; ++poll) {
       if (poll >= WAIT_POLLS) {
         sm.err = 1;
         break;
       }
     }
-    __threadfence();
   }
   __syncthreads();
 }
@@ -438,7 +441,11 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
   // be needed and the value passes would be wasted.
   unsigned long long distinct_max = 1;
   for (int p = 4; p < 8; ++p) distinct_max *= sm.distinct[p];
-  bool full = len > RUN_MAX * static_cast<int64_t>(distinct_max);
+  // (Step 3 keeps the chunk, RUN_MAX keys on each side of it and the list of
+  // its runs, at most C / 2, in the staging area: 8 (C + 2 RUN_MAX) + 2 C
+  // bytes; longer chunks take the full sort too.)
+  bool full = len > RUN_MAX * static_cast<int64_t>(distinct_max) ||
+              10 * C + 16 * RUN_MAX > static_cast<int64_t>(RS_SMEM);
   int seq = 0, cur = 0;
   if (!full) {
     // 2. Value positions.
@@ -458,17 +465,52 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
     grid_sync(c, target += G, sm);
     full = __ldcg(&c.long_run) != 0;
     if (!full) {
-      // A key's place inside its run of equal values is the run's start plus
-      // the number of the run's larger keys (keys are distinct).
+      // The chunk and RUN_MAX keys on each side go to shared memory.  A key
+      // alone with its value is in place, and the first key of a pair places
+      // both; a longer run is listed by its first key, and a warp finds its
+      // end and places each of its keys at the run's start plus the number of
+      // the run's larger keys (keys are distinct).
+      const int64_t wlo = lo > RUN_MAX ? lo - RUN_MAX : 0;
+      const int64_t whi = hi + RUN_MAX < len ? hi + RUN_MAX : len;
+      for (int64_t j = wlo + threadIdx.x; j < whi; j += RS_THREADS) s_keys[j - wlo] = __ldcg(srt + j);
+      unsigned* runs = reinterpret_cast<unsigned*>(s_keys + (whi - wlo));  // run starts, relative to lo
+      if (threadIdx.x == 0) sm.nruns = 0;
+      __syncthreads();
+      auto val = [&](int64_t j) { return static_cast<uint32_t>(s_keys[j - wlo] >> 32); };
       for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS) {
-        const unsigned long long kk = __ldcg(srt + i);
+        const unsigned long long kk = s_keys[i - wlo];
         const uint32_t v = static_cast<uint32_t>(kk >> 32);
-        int64_t s = i, e = i + 1;
-        while (s > 0 && static_cast<uint32_t>(__ldcg(srt + s - 1) >> 32) == v) --s;
-        while (e < len && static_cast<uint32_t>(__ldcg(srt + e) >> 32) == v) ++e;
-        int64_t p = s;
-        for (int64_t j = s; j < e; ++j) p += __ldcg(srt + j) > kk;
-        if (p < a.k) emit_key(a, row, p, kk);
+        if (i > 0 && val(i - 1) == v) continue;  // not the first of its run
+        if (i + 1 == len || val(i + 1) != v) {
+          if (i < a.k) emit_key(a, row, i, kk);
+        } else if (i + 2 == len || val(i + 2) != v) {  // a pair: the larger key first
+          const unsigned long long k2 = s_keys[i + 1 - wlo];
+          if (i < a.k) emit_key(a, row, i, kk > k2 ? kk : k2);
+          if (i + 1 < a.k) emit_key(a, row, i + 1, kk > k2 ? k2 : kk);
+        } else {
+          runs[atomicAdd(&sm.nruns, 1u)] = static_cast<unsigned>(i - lo);
+        }
+      }
+      __syncthreads();
+      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      for (unsigned t = warp; t < sm.nruns; t += RS_THREADS / 32) {
+        const int64_t st = lo + runs[t];
+        const uint32_t v = val(st);
+        int64_t L = 0;  // run length (at most RUN_MAX, so within the staged keys)
+        for (int64_t b = st;; b += 32) {
+          const int64_t j = b + lane;
+          const unsigned same = __ballot_sync(FULL_MASK, j < whi && val(j) == v);
+          if (same != FULL_MASK) {
+            L = b - st + __ffs(~same) - 1;
+            break;
+          }
+        }
+        for (int64_t q = lane; q < L; q += 32) {
+          const unsigned long long kk = s_keys[st + q - wlo];
+          int64_t p = st;
+          for (int64_t j = 0; j < L; ++j) p += s_keys[st + j - wlo] > kk;
+          if (p < a.k) emit_key(a, row, p, kk);
+        }
       }
     }
   }
