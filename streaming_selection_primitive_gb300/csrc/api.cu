@@ -221,7 +221,7 @@ struct Layout {
   bool sampling = false;
   bool radix_refine = false;  // step 4 on the filter buffer by the radix sort
   size_t off_state = 0, off_lists = 0, off_table = 0, off_draws = 0, off_blockcnt = 0, off_sidx = 0, off_skeys = 0,
-         off_buf = 0, off_sel = 0, off_sort = 0, off_refine = 0, off_sctl = 0, total = 0;
+         off_buf = 0, off_sel = 0, off_sort = 0, off_refine = 0, off_sctl = 0, off_tie = 0, total = 0;
 };
 
 int64_t draw_budget(int64_t n, int64_t S) {
@@ -279,6 +279,10 @@ Layout make_layout(int64_t rows, int64_t n, int64_t k, int64_t S, int64_t D, int
   off = align_up(off + sort_bytes);
   L.off_refine = off;
   if (sampling && !L.radix_refine) off = align_up(off + refine_grid_scratch_bytes(rows));
+  L.off_tie = off;  // tie exit: control blocks, block counts and their prefixes
+  if (sampling)
+    off = align_up(off + align_up(tie_ctl_bytes() * rows) + align_up(sizeof(unsigned) * tie_blocks(n) * rows) +
+                   sizeof(unsigned long long) * tie_blocks(n) * rows);
   L.total = off;
   return L;
 }
@@ -474,14 +478,24 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
       launch_kernel(k_attempt_reset, dim3(rb, ng), 1024, 0, stream, at<unsigned long long>(c.ws, L.off_table),
                     L.log2H, gl, st, static_cast<unsigned long long>(P.t), ref_ctl, ref_words,
                     at<unsigned long long>(c.ws, L.off_sctl), static_cast<int>(sample_tau_ctl_bytes() / 8));
-      // Sampling and tau in one kernel (its stage time is reported as the
-      // sampling's; the threshold stage is then empty).
+      // Sampling and tau: one persistent kernel (its stage time is reported as
+      // the sampling's, the threshold stage then being empty), or, when many
+      // rows share the SMs, the step-by-step kernels with the first radix pass
+      // of tau fused into the sampler's last one.
       SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, a, ng, gl, st,
                     at<unsigned long long>(c.ws, L.off_table), at<uint32_t>(c.ws, L.off_draws),
                     at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
                     at<uint32_t>(c.ws, L.off_skeys), false, static_cast<unsigned long long>(P.t)};
-      PK_CHECK(launch_sample_tau(sa, at<char>(c.ws, L.off_sctl), stream));
-      if (time_it) PK_CHECK(cudaEventRecord(t_events.e[1], stream));
+      if (sample_tau_fits(L.D, ng)) {
+        PK_CHECK(launch_sample_tau(sa, at<char>(c.ws, L.off_sctl), stream));
+        if (time_it) PK_CHECK(cudaEventRecord(t_events.e[1], stream));
+      } else {
+        sa.tau_pass1 = true;
+        launch_sample(sa, stream);
+        if (time_it) PK_CHECK(cudaEventRecord(t_events.e[1], stream));
+        SelectArgs ta{KeySource::SampleKeys, at<uint32_t>(c.ws, L.off_skeys), P.S, P.S, ng, gl, st};
+        launch_select(ta, 0, true, 1, stream);  // its last pass stores tau
+      }
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[2], stream));
       FilterArgs fa{x, ld, n, P.M, ng, gl, st, at<unsigned long long>(c.ws, L.off_buf), filter_grid(cps)};
       launch_filter(fa, stream);
@@ -569,11 +583,15 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         tie_ran = true;
         int* tl = nullptr;
         PK_CHECK(upload_rows(L, c.ws, hbuf, 2, tie, stream, &tl));
-        launch_tie_init(static_cast<int>(tie.size()), tl, st, k, stream);
-        SelectArgs ia{KeySource::Input, x, ld, n, static_cast<int>(tie.size()), tl, st};
         uint64_t* sel = at<uint64_t>(c.ws, L.off_sel);
-        launch_select(ia, 0, false, 3, stream);
-        launch_compact(ia, sel, L.kstride, k, stream);
+        char* tw = at<char>(c.ws, L.off_tie);
+        const int64_t nb = tie_blocks(n);
+        TieArgs ta{x, ld, n, static_cast<int>(tie.size()), tl, st, reinterpret_cast<unsigned long long*>(sel),
+                   L.kstride, k, reinterpret_cast<unsigned*>(tw + align_up(tie_ctl_bytes() * rows)),
+                   reinterpret_cast<unsigned long long*>(tw + align_up(tie_ctl_bytes() * rows) +
+                                                         align_up(sizeof(unsigned) * nb * rows)),
+                   nb, reinterpret_cast<TieCtl*>(tw), rows};
+        PK_CHECK(launch_tie_take(ta, filter_grid(cps), stream));
         launch_sort_emit(sel, L.kstride, k, static_cast<int>(tie.size()), tl, x, ld, n, out_vals, out_idx, stream, st,
                          at<char>(c.ws, L.off_sort), L.rows);
       }

@@ -98,6 +98,10 @@ void launch_sample_rows(const SampleArgs& a, int64_t key_row0, cudaStream_t stre
 // are not used.
 size_t sample_tau_ctl_bytes();
 cudaError_t launch_sample_tau(const SampleArgs& a, void* ctl, cudaStream_t stream);
+// Whether each CTA of launch_sample_tau keeps all of its draws in registers
+// (true unless many rows share the SMs); otherwise the step-by-step kernels
+// (launch_sample with tau_pass1, then launch_select) are faster.
+bool sample_tau_fits(int64_t D, int nrows);
 
 // Radix selection of the rank-th largest key per row.  init_rank > 0 resets the
 // state of each row first; otherwise the state is taken as it is (tie path).
@@ -107,6 +111,30 @@ void launch_select(const SelectArgs& a, uint64_t init_rank, bool value_only, int
 void launch_store_tau(int nrows, const int* rows, RowState* st, cudaStream_t stream);
 // Tie path: set the state to "value ord(tau) resolved, rank k - R_gt left".
 void launch_tie_init(int nrows, const int* rows, RowState* st, int64_t k, cudaStream_t stream);
+
+// Tie exit (tie.cu): the k outputs of each listed row (R > M, R_gt < k) into
+// `sel` (every x > tau, then the k - R_gt lowest-index copies of tau), ready
+// for launch_sort_emit; also clears RowState::skip of those rows.
+struct TieCtl;
+struct TieArgs {
+  const float* x;
+  int64_t ld;
+  int64_t n;
+  int nrows;
+  const int* rows;
+  RowState* st;
+  unsigned long long* sel;  // rows x kstride output keys
+  int64_t kstride;
+  int64_t k;
+  unsigned* block_eq;             // rows x nblocks: copies of tau per block of 2^18 elements
+  unsigned long long* block_pre;  // rows x nblocks: their exclusive prefix
+  int64_t nblocks;                // tie_blocks(n)
+  TieCtl* ctl;                    // rows x tie_ctl_bytes()
+  int64_t total_rows;             // rows the arrays are sized for
+};
+int64_t tie_blocks(int64_t n);
+size_t tie_ctl_bytes();
+cudaError_t launch_tie_take(const TieArgs& a, int filter_grid, cudaStream_t stream);
 
 // Writes the k keys >= the selected threshold into out (row stride out_stride).
 void launch_compact(const SelectArgs& a, uint64_t* out, int64_t out_stride, int64_t k,

@@ -683,14 +683,26 @@ void launch_sample(const SampleArgs& a, cudaStream_t stream) { launch_sample_row
 
 size_t sample_tau_ctl_bytes() { return sizeof(SampleCtl); }
 
-cudaError_t launch_sample_tau(const SampleArgs& a, void* ctl, cudaStream_t stream) {
-  // Chunks per row: all CTAs (chunks x rows) resident at once, one per SM,
-  // at most 256 (the control block's count slots), no chunk shorter than 512.
-  int64_t G = sms() / (a.nrows > 0 ? a.nrows : 1);
-  const int64_t by_len = (a.D + ST_THREADS - 1) / ST_THREADS;
+namespace {
+// Chunks per row: all CTAs (chunks x rows) resident at once, one per SM, at
+// most 256 (the control block's count slots), no chunk shorter than 512.
+int64_t sample_tau_chunks(int64_t D, int nrows) {
+  int64_t G = sms() / (nrows > 0 ? nrows : 1);
+  const int64_t by_len = (D + ST_THREADS - 1) / ST_THREADS;
   if (G > by_len) G = by_len;
   if (G > 256) G = 256;
-  if (G < 1) G = 1;
+  return G < 1 ? 1 : G;
+}
+}  // namespace
+
+bool sample_tau_fits(int64_t D, int nrows) {
+  const int64_t G = sample_tau_chunks(D, nrows);
+  const int64_t Dc = (((D + G - 1) / G) + 31) & ~int64_t(31);
+  return Dc <= static_cast<int64_t>(ST_HELD) * ST_THREADS;
+}
+
+cudaError_t launch_sample_tau(const SampleArgs& a, void* ctl, cudaStream_t stream) {
+  const int64_t G = sample_tau_chunks(a.D, a.nrows);
   launch_kernel(k_sample_tau, dim3(static_cast<unsigned>(G), static_cast<unsigned>(a.nrows)), ST_THREADS, 0, stream,
                 a, static_cast<SampleCtl*>(ctl));
   return cudaGetLastError();
