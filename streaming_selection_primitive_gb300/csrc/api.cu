@@ -130,36 +130,37 @@ __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int*
   pdl_trigger();
   pdl_wait();
   const int row = launch_row(rows);
-  unsigned long long* tb = table + (static_cast<int64_t>(row) << log2H);
-  const int64_t H = 1ll << log2H;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < H;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    tb[i] = ~0ull;
-  if (blockIdx.x == 0) {
-    RowState& S = st[row];
-    if (sort_ctl)
-      for (int i = threadIdx.x; i < ctl_words; i += blockDim.x) sort_ctl[static_cast<int64_t>(row) * ctl_words + i] = 0;
-    for (int i = threadIdx.x; i < sample_words; i += blockDim.x)
-      sample_ctl[static_cast<int64_t>(row) * sample_words + i] = 0;
-    for (int b = threadIdx.x; b < HIST_BINS; b += blockDim.x) S.hist[b] = 0;
-    if (threadIdx.x == 0) {
-      S.R_ge = 0;
-      S.R_gt = 0;
-      S.nan = 0;
-      S.distinct = 0;
-      S.error = 0;
-      S.sel_prefix = 0;
-      S.sel_rank = t;
-      S.sel_above = 0;
-      S.sel_bucket = 0;
-      S.sel_thresh = 0;
-      S.sel_nan = 0;
-      S.sel_bits = 0;
-      S.sel_done = 0;
-      S.done_blocks = 0;
-      S.compact_count = 0;
-      S.skip = 0;
-    }
+  // 16-byte stores, grid-strided over the row's CTAs: the hash table to
+  // "empty", the control blocks (an even number of words each) to zero.
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t gstride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  ulonglong2* tb = reinterpret_cast<ulonglong2*>(table + (static_cast<int64_t>(row) << log2H));
+  for (int64_t i = gtid; i < (int64_t(1) << log2H) / 2; i += gstride) tb[i] = make_ulonglong2(~0ull, ~0ull);
+  if (sort_ctl) {
+    ulonglong2* sc = reinterpret_cast<ulonglong2*>(sort_ctl + static_cast<int64_t>(row) * ctl_words);
+    for (int64_t i = gtid; i < ctl_words / 2; i += gstride) sc[i] = make_ulonglong2(0ull, 0ull);
+  }
+  ulonglong2* pc = reinterpret_cast<ulonglong2*>(sample_ctl + static_cast<int64_t>(row) * sample_words);
+  for (int64_t i = gtid; i < sample_words / 2; i += gstride) pc[i] = make_ulonglong2(0ull, 0ull);
+  RowState& S = st[row];
+  for (int64_t b = gtid; b < HIST_BINS; b += gstride) S.hist[b] = 0;
+  if (gtid == 0) {
+    S.R_ge = 0;
+    S.R_gt = 0;
+    S.nan = 0;
+    S.distinct = 0;
+    S.error = 0;
+    S.sel_prefix = 0;
+    S.sel_rank = t;
+    S.sel_above = 0;
+    S.sel_bucket = 0;
+    S.sel_thresh = 0;
+    S.sel_nan = 0;
+    S.sel_bits = 0;
+    S.sel_done = 0;
+    S.done_blocks = 0;
+    S.compact_count = 0;
+    S.skip = 0;
   }
 }
 
@@ -463,7 +464,8 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
     PK_CHECK(upload_rows(L, c.ws, hbuf, 0, group, stream, &gl));
     {
       const int64_t H = 1ll << L.log2H;
-      const unsigned rb = static_cast<unsigned>(std::min<int64_t>((H + 1023) / 1024, 256));
+      // Reset CTAs per row: about eight 16-byte stores per thread of 256.
+      const unsigned rb = static_cast<unsigned>(std::min<int64_t>(std::max<int64_t>(H / 2 / (256 * 8), 1), 64));
       const bool time_it = timing && first_filter;
       if (time_it) {
         if (!t_events.e[0])
@@ -475,7 +477,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
           L.radix_refine ? static_cast<unsigned long long*>(radix_sort_ctl(at<char>(c.ws, L.off_sort), P.M, rows))
                          : static_cast<unsigned long long*>(refine_grid_ctl(at<char>(c.ws, L.off_refine)));
       const int ref_words = static_cast<int>((L.radix_refine ? radix_sort_ctl_bytes() : refine_grid_ctl_bytes()) / 8);
-      launch_kernel(k_attempt_reset, dim3(rb, ng), 1024, 0, stream, at<unsigned long long>(c.ws, L.off_table),
+      launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, at<unsigned long long>(c.ws, L.off_table),
                     L.log2H, gl, st, static_cast<unsigned long long>(P.t), ref_ctl, ref_words,
                     at<unsigned long long>(c.ws, L.off_sctl), static_cast<int>(sample_tau_ctl_bytes() / 8));
       // Sampling and tau: one persistent kernel (its stage time is reported as

@@ -31,7 +31,7 @@ struct RefineCtl {
   unsigned cursor;              // gather-list length
   unsigned pad[62];
 };
-static_assert(sizeof(RefineCtl) % 8 == 0, "RefineCtl is zeroed in 8-byte words");
+static_assert(sizeof(RefineCtl) % 16 == 0, "RefineCtl is zeroed with 16-byte stores");
 
 namespace {
 

@@ -344,7 +344,7 @@ struct SampleCtl {
   unsigned bar;                       // grid-barrier arrivals
   unsigned pad[62];
 };
-static_assert(sizeof(SampleCtl) % 8 == 0, "SampleCtl is zeroed in 8-byte words");
+static_assert(sizeof(SampleCtl) % 16 == 0, "SampleCtl is zeroed with 16-byte stores");
 
 namespace {
 

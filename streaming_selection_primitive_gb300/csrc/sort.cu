@@ -46,7 +46,7 @@ struct SortCtl {
   unsigned long_run;                 // 1: some run of equal values is longer than 32
   unsigned pad[30];
 };
-static_assert(sizeof(SortCtl) % 8 == 0, "SortCtl is zeroed in 8-byte words");
+static_assert(sizeof(SortCtl) % 16 == 0, "SortCtl is zeroed with 16-byte stores");
 
 namespace {
 
