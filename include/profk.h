@@ -54,7 +54,7 @@ typedef enum profk_status {
   PROFK_ERR_NAN = -3,            /* the input holds a NaN */
   PROFK_ERR_UNSUPPORTED = -4,    /* e.g. n > 2^32 or a misaligned input */
   PROFK_ERR_DEVICE_TIMEOUT = -5, /* a bounded device-side wait gave up */
-  PROFK_ERR_SCRATCH = -6         /* profk_topk_noalloc: the problem needs more than its fixed scratch */
+  PROFK_ERR_SCRATCH = -6         /* the problem needs more than the fixed scratch or the caller's workspace */
 } profk_status;
 
 /* How a row's result was produced. */
@@ -135,6 +135,17 @@ int profk_params(int64_t n, int64_t k, double eps, int mode,
 /* Device bytes one call of profk_topk_batched(rows, n, k, eps) allocates at
  * most (profk_topk is rows = 1).  0 on invalid arguments. */
 size_t profk_workspace_size(int64_t rows, int64_t n, int64_t k, double eps);
+
+/* Caller-owned workspace for this host thread's later profk_topk and
+ * profk_topk_batched calls (the step entry points below keep allocating).
+ * dev_ptr: device memory of `bytes` bytes on the device of those calls,
+ * 256-byte aligned; the library uses it instead of its memory pool and never
+ * frees it.  A call that needs more than `bytes` (profk_workspace_size gives
+ * the need) returns PROFK_ERR_SCRATCH without producing output.  The buffer
+ * is used in stream order, so calls on different streams must not have it in
+ * flight at the same time.  dev_ptr = NULL or bytes = 0 returns to the pool.
+ * Returns PROFK_OK, or PROFK_ERR_INVALID for a misaligned pointer. */
+int profk_set_workspace(void* dev_ptr, size_t bytes);
 
 /* Process-wide options (defaults in brackets). */
 typedef enum profk_option {

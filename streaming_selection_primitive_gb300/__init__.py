@@ -58,6 +58,25 @@ def workspace_size(rows: int, n: int, k: int, eps: float = 1e-3) -> int:
     return int(lib().profk_workspace_size(int(rows), int(n), int(k), float(eps)))
 
 
+_user_workspace = None  # keeps the caller's buffer alive while it is registered
+
+
+def set_workspace(buf=None):
+    """Use the CUDA tensor `buf` (any dtype, contiguous, 256-byte aligned) as the
+    workspace of this thread's topk / topk_batched calls; None returns to the
+    library's memory pool.  A call that needs more than buf's bytes raises
+    ProfkError (PROFK_ERR_SCRATCH)."""
+    global _user_workspace
+    if buf is None:
+        _abi.check(lib().profk_set_workspace(None, 0))
+        _user_workspace = None
+        return
+    if not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("the workspace must be a contiguous CUDA tensor")
+    _abi.check(lib().profk_set_workspace(buf.data_ptr(), buf.numel() * buf.element_size()))
+    _user_workspace = buf
+
+
 def set_option(option: int, value: int) -> None:
     _abi.check(lib().profk_set_option(int(option), int(value)))
 

@@ -65,6 +65,7 @@ _SIGS = {
     "profk_params": (C.c_int, [C.c_int64, C.c_int64, C.c_double, C.c_int,
                                C.POINTER(C.c_int64), C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
     "profk_workspace_size": (C.c_size_t, [C.c_int64, C.c_int64, C.c_int64, C.c_double]),
+    "profk_set_workspace": (C.c_int, [C.c_void_p, C.c_size_t]),
     "profk_set_option": (C.c_int, [C.c_int, C.c_int64]),
     "profk_get_option": (C.c_int64, [C.c_int]),
     "profk_strerror": (C.c_char_p, [C.c_int]),

@@ -300,21 +300,41 @@ struct Call {
   cudaStream_t stream;
   void* ws = nullptr;
   size_t ws_bytes = 0;
+  bool ws_user = false;  // the caller's workspace (profk_set_workspace): never freed
   cudaError_t err = cudaSuccess;
   int status = PROFK_OK;
 };
 
-#define PK_CHECK(expr)                      \
-  do {                                      \
-    cudaError_t e_ = (expr);                \
-    if (e_ != cudaSuccess) {                \
-      c.err = e_;                           \
-      c.status = PROFK_ERR_CUDA;            \
-      goto done;                            \
-    }                                       \
+// A failed CUDA call ends the call with PROFK_ERR_CUDA, unless a more specific
+// status was already set.
+#define PK_CHECK(expr)                                  \
+  do {                                                  \
+    cudaError_t e_ = (expr);                            \
+    if (e_ != cudaSuccess) {                            \
+      c.err = e_;                                       \
+      if (c.status == PROFK_OK) c.status = PROFK_ERR_CUDA; \
+      goto done;                                        \
+    }                                                   \
   } while (0)
 
-cudaError_t ws_alloc(Call& c, size_t bytes) {
+// Caller-owned workspace of this host thread (profk_set_workspace).
+thread_local void* t_user_ws = nullptr;
+thread_local size_t t_user_ws_bytes = 0;
+
+// The workspace of a call: the caller's, when one is set and `allow_user`
+// (the whole-call entry points), else a stream-ordered pool allocation.
+cudaError_t ws_alloc(Call& c, size_t bytes, bool allow_user = false) {
+  if (allow_user && t_user_ws) {
+    if (bytes > t_user_ws_bytes) {
+      c.status = PROFK_ERR_SCRATCH;
+      return cudaErrorMemoryAllocation;
+    }
+    c.ws = t_user_ws;
+    c.ws_bytes = bytes;
+    c.ws_user = true;
+    return cudaSuccess;
+  }
+  c.ws_user = false;
   cudaMemPool_t pool;
   cudaError_t e = pool_for_current_device(&pool);
   if (e != cudaSuccess) return e;
@@ -324,7 +344,7 @@ cudaError_t ws_alloc(Call& c, size_t bytes) {
 }
 
 void ws_free(Call& c) {
-  if (c.ws) cudaFreeAsync(c.ws, c.stream);
+  if (c.ws && !c.ws_user) cudaFreeAsync(c.ws, c.stream);
   c.ws = nullptr;
 }
 
@@ -431,7 +451,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   void* hbuf = nullptr;
   RowState* st = nullptr;
 
-  PK_CHECK(ws_alloc(c, L.total));
+  PK_CHECK(ws_alloc(c, L.total, true));
   st = at<RowState>(c.ws, L.off_state);
   // The sampling path starts every attempt with k_attempt_reset, which
   // initialises the state of its rows; the exact path needs zeroed state.
@@ -605,7 +625,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         ws_free(c);
         D *= 2;
         L = make_layout(rows, n, k, P.S, D, P.M, true);
-        PK_CHECK(ws_alloc(c, L.total));
+        PK_CHECK(ws_alloc(c, L.total, true));
         st = at<RowState>(c.ws, L.off_state);
         PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState) * rows, stream));
       }
@@ -690,6 +710,13 @@ int profk_params(int64_t n, int64_t k, double eps, int mode, int64_t* S, int64_t
   return PROFK_OK;
 }
 
+int profk_set_workspace(void* dev_ptr, size_t bytes) {
+  if (dev_ptr && (reinterpret_cast<uintptr_t>(dev_ptr) & 255u)) return PROFK_ERR_INVALID;
+  t_user_ws = bytes ? dev_ptr : nullptr;
+  t_user_ws_bytes = dev_ptr ? bytes : 0;
+  return PROFK_OK;
+}
+
 size_t profk_workspace_size(int64_t rows, int64_t n, int64_t k, double eps) {
   if (rows < 1 || n < 1 || k < 1 || k > n || !(eps > 0.0 && eps < 1.0)) return 0;
   const Params P = cached_params(n, k, eps / static_cast<double>(rows), static_cast<int>(g_opt[0].load()));
@@ -718,7 +745,7 @@ const char* profk_strerror(int code) {
     case PROFK_ERR_NAN: return "input contains NaN";
     case PROFK_ERR_UNSUPPORTED: return "unsupported input (n > 2^32 or misaligned pointer / stride)";
     case PROFK_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
-    case PROFK_ERR_SCRATCH: return "problem needs more workspace than the fixed scratch of profk_topk_noalloc";
+    case PROFK_ERR_SCRATCH: return "problem needs more workspace than the fixed scratch or the caller's workspace";
     default: return "unknown status";
   }
 }

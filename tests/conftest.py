@@ -40,3 +40,4 @@ def pk(profk_lib):
     profk_lib.reset_options()
     yield profk_lib
     profk_lib.reset_options()
+    profk_lib.set_workspace(None)

@@ -22,7 +22,7 @@ def test_header_declares_the_method(pk):
     names = declared_functions()
     for must in ("profk_topk", "profk_topk_batched", "profk_params", "profk_workspace_size",
                  "profk_set_option", "profk_get_option", "profk_strerror", "profk_sample",
-                 "profk_threshold", "profk_filter", "profk_refine", "profk_exact"):
+                 "profk_threshold", "profk_filter", "profk_refine", "profk_exact", "profk_set_workspace"):
         assert must in names
 
 
@@ -89,3 +89,10 @@ def test_workspace_is_O_M_plus_S(pk):
     assert 0 < big < 16 << 20  # megabytes, not a fraction of the 4 GiB input
     assert big < 16 * small
     assert pk.workspace_size(1, 10, 11) == 0
+
+
+def test_set_workspace_validation(pk):
+    lib = pk.lib()
+    assert lib.profk_set_workspace(C.c_void_p(256 + 8), 1 << 20) == -1  # not 256-byte aligned
+    assert lib.profk_set_workspace(None, 0) == 0
+    assert lib.profk_set_workspace(C.c_void_p(1 << 20), 0) == 0  # zero bytes: back to the pool

@@ -192,3 +192,43 @@ def test_batched_large_k_rows_retry_alone(pk, cuda_device):
         ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 6, row=r, force=force)
         assert_same(vals[r], idx[r], ov, oi, f"row {r}")
         assert (sts[r]["attempts"], sts[r]["path"], sts[r]["R_first"]) == (ost.attempts, ost.path, ost.R_first)
+
+
+def test_caller_workspace(pk, cuda_device):
+    x = workloads.normal((1 << 22) + 8, 12, cuda_device)
+    k = 1000
+    ref = pk.topk(x, k, 1e-3, 3)
+    need = pk.workspace_size(1, x.numel(), k)
+    buf = torch.empty(need, dtype=torch.uint8, device=cuda_device)
+    pk.set_workspace(buf)
+    got = pk.topk(x, k, 1e-3, 3)
+    assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+    assert got[2]["R_first"] == ref[2]["R_first"] and got[2]["path"] == ref[2]["path"]
+    # Batched rows through the same buffer when it is big enough, else refused.
+    xb = workloads.normal_rows(3, 1 << 20, 4, cuda_device)
+    if pk.workspace_size(3, 1 << 20, 64) <= need:
+        vb, ib, _ = pk.topk_batched(xb, 64, 1e-3, 2)
+        for r in range(3):
+            assert_same(vb[r], ib[r], *topk_sort(xb[r].cpu().numpy(), 64), f"row {r}")
+    small = torch.empty(need // 2 & ~255, dtype=torch.uint8, device=cuda_device)
+    pk.set_workspace(small)
+    with pytest.raises(pk.ProfkError) as e:
+        pk.topk(x, k, 1e-3, 3)
+    assert e.value.code == -6
+    pk.set_workspace(None)
+    again = pk.topk(x, k, 1e-3, 3)
+    assert torch.equal(again[1], ref[1])
+
+
+@pytest.mark.parametrize("rows,n,k", [(1024, 1 << 16, 16), (256, 1 << 20, 32), (512, (1 << 18) + 4, 100)])
+def test_batched_many_rows(pk, cuda_device, rows, n, k):
+    """Many rows sharing the SMs (one CTA per row in the persistent kernels,
+    the step-by-step sampler; exact routing for the 2^16 rows)."""
+    x = workloads.normal_rows(rows, n, rows + k, cuda_device)
+    vals, idx, sts = pk.topk_batched(x, k, 1e-3, 21)
+    rng = np.random.default_rng(rows)
+    for r in sorted(set(rng.integers(0, rows, 8).tolist()) | {0, rows - 1}):
+        h = x[r].cpu().numpy()
+        assert_same(vals[r], idx[r], *topk_sort(h, k), f"row {r}")
+    paths = {s["path"] for s in sts}
+    assert paths == ({pk.PATH_EXACT} if n == 1 << 16 else {pk.PATH_FILTER}) or pk.PATH_FALLBACK not in paths
