@@ -295,6 +295,53 @@ T* at(void* base, size_t off) {
 
 // Per-row counters read back after each filter pass (the head of RowState).
 constexpr size_t REPORT_BYTES = offsetof(RowState, hist);
+static_assert(REPORT_BYTES % 4 == 0, "the report is copied in 4-byte words");
+
+// The check's report written straight into pinned host memory: the heads of
+// the first `rows` row states, then (after a system-scope fence) the call's
+// sequence number in *flag, which the host waits for.  One CTA; used for up
+// to REPORT_ROWS_MAPPED rows.
+constexpr int64_t REPORT_ROWS_MAPPED = 64;
+
+__global__ void __launch_bounds__(256) k_report(const RowState* st, int rows, unsigned* rep,
+                                                unsigned long long* flag, unsigned long long seq) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int W = static_cast<int>(REPORT_BYTES / 4);
+  for (int i = threadIdx.x; i < rows * W; i += blockDim.x) {
+    const unsigned* src = reinterpret_cast<const unsigned*>(st + i / W);
+    *reinterpret_cast<volatile unsigned*>(rep + i) = __ldcg(src + i % W);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence_system();
+    *reinterpret_cast<volatile unsigned long long*>(flag) = seq;
+  }
+}
+
+thread_local unsigned long long t_report_seq = 0;
+
+// Waits for the report of sequence number `seq`.  A stream that fails or
+// finishes without it (or a wait of more than 10 s) ends the wait with the
+// stream synchronized, so that its error, if any, is returned.
+cudaError_t wait_report(const volatile unsigned long long* flag, unsigned long long seq, cudaStream_t stream) {
+  const auto t0 = std::chrono::steady_clock::now();
+  for (uint64_t spin = 0;; ++spin) {
+    if (*flag == seq) {
+      std::atomic_thread_fence(std::memory_order_acquire);
+      return cudaSuccess;
+    }
+    if ((spin & 1023) == 1023) {
+      const cudaError_t q = cudaStreamQuery(stream);
+      const bool late = std::chrono::steady_clock::now() - t0 > std::chrono::seconds(10);
+      if ((q != cudaErrorNotReady && *flag != seq) || late) {
+        const cudaError_t e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return e;
+        return *flag == seq ? cudaSuccess : cudaErrorUnknown;
+      }
+    }
+  }
+}
 
 struct Call {
   cudaStream_t stream;
@@ -456,7 +503,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   // The sampling path starts every attempt with k_attempt_reset, which
   // initialises the state of its rows; the exact path needs zeroed state.
   if (!sampling) PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState) * rows, stream));
-  PK_CHECK(pinned(sizeof(int) * rows * 4 + REPORT_BYTES * rows, &hbuf));
+  PK_CHECK(pinned(sizeof(int) * rows * 4 + REPORT_BYTES * rows + 512, &hbuf));
 
   if (!sampling) {
     for (int64_t r = 0; r < rows; ++r) st_host[r].path = PROFK_PATH_EXACT;
@@ -537,12 +584,26 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
       }
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[4], stream));
       PK_CHECK(cudaGetLastError());
-      // Run-time check: read the exact counts of every row.
+      // Run-time check: read the exact counts of every row (written into
+      // pinned memory by a kernel and waited for, or copied and synchronized
+      // for many rows).
       char* rep = static_cast<char*>(hbuf) + sizeof(int) * rows * 4;
-      PK_CHECK(cudaMemcpy2DAsync(rep, REPORT_BYTES, st, sizeof(RowState), REPORT_BYTES, rows,
-                                 cudaMemcpyDeviceToHost, stream));
-      if (time_it) PK_CHECK(cudaEventRecord(t_events.e[5], stream));
-      PK_CHECK(cudaStreamSynchronize(stream));
+      if (rows <= REPORT_ROWS_MAPPED) {
+        unsigned long long* flag =
+            reinterpret_cast<unsigned long long*>(align_up(reinterpret_cast<uintptr_t>(rep + REPORT_BYTES * rows)));
+        const unsigned long long seq = ++t_report_seq;
+        launch_kernel(k_report, 1, 256, 0, stream, st, static_cast<int>(rows), reinterpret_cast<unsigned*>(rep), flag,
+                      seq);
+        if (time_it) PK_CHECK(cudaEventRecord(t_events.e[5], stream));
+        PK_CHECK(cudaGetLastError());
+        PK_CHECK(wait_report(flag, seq, stream));
+        if (time_it) PK_CHECK(cudaEventSynchronize(t_events.e[5]));
+      } else {
+        PK_CHECK(cudaMemcpy2DAsync(rep, REPORT_BYTES, st, sizeof(RowState), REPORT_BYTES, rows,
+                                   cudaMemcpyDeviceToHost, stream));
+        if (time_it) PK_CHECK(cudaEventRecord(t_events.e[5], stream));
+        PK_CHECK(cudaStreamSynchronize(stream));
+      }
       if (time_it) {
         PK_CHECK(cudaEventElapsedTime(&filter_ms, t_events.e[2], t_events.e[3]));
         for (int q = 0; q < 5; ++q) PK_CHECK(cudaEventElapsedTime(&t_stage_ms[q], t_events.e[q], t_events.e[q + 1]));
