@@ -126,9 +126,15 @@ int profk_topk_batched(const float* x, int64_t rows, int64_t n, int64_t ld, int6
  *     z = Phi^{-1}(1-eps/2); then 1 <= t <= S and k <= M <= n.
  *   mode PROFK_PARAMS_OLD: the older Algorithm 1 literally (Eq 6 t,
  *     Corollary 4 M, and t = 1 when (k/n) S < -ln(eps/2)).
+ *   mode PROFK_PARAMS_EXACT: S as in the default mode; t and M the exact
+ *     optimum of Theorem 4 (corrected version) for that S, with the budget
+ *     split eps/2 + eps/2: t - 1 is the (1 - eps/2)-quantile of the
+ *     hypergeometric count of the top k - 1 in the sample, M the smallest M
+ *     with Pr(at most t - 1 of the top M are sampled) <= eps/2.
  * Pure host arithmetic (fp64), no device work. */
 #define PROFK_PARAMS_DEFAULT 0
 #define PROFK_PARAMS_OLD 1
+#define PROFK_PARAMS_EXACT 2
 int profk_params(int64_t n, int64_t k, double eps, int mode,
                  int64_t* S, int64_t* t, int64_t* M);
 
@@ -149,7 +155,7 @@ int profk_set_workspace(void* dev_ptr, size_t bytes);
 
 /* Process-wide options (defaults in brackets). */
 typedef enum profk_option {
-  PROFK_OPT_PARAM_MODE = 0,    /* PROFK_PARAMS_DEFAULT [0] or PROFK_PARAMS_OLD */
+  PROFK_OPT_PARAM_MODE = 0,    /* PROFK_PARAMS_DEFAULT [0], PROFK_PARAMS_OLD or PROFK_PARAMS_EXACT */
   PROFK_OPT_MAX_ATTEMPTS = 1,  /* filter attempts before the exact fallback [6]; 0 = fallback at once */
   PROFK_OPT_TIE_EXIT = 2,      /* take PROFK_PATH_TIE when R > M and R_gt < k [1] */
   PROFK_OPT_FORCE_S = 3,       /* >0 overrides S (and disables the exact-path routing) [0] */

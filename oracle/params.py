@@ -25,7 +25,8 @@ Algorithm 1, its sample-size step), and t, M from the corrected Algorithm 1 (its
 with z = Phi^{-1}(1 - eps/2), then 1 <= t <= S and k <= M <= N.  The older
 t-rule sets t = 1 exactly where recall failure is likely (its own text derives
 the bound in the wrong direction), so it is kept only as a named function and
-an optional mode.
+an optional mode.  A third mode keeps that S and takes the exact optimal t and
+M of the corrected Theorem 4 (``params_exact``, pinned to Table 3).
 """
 from __future__ import annotations
 
@@ -219,6 +220,7 @@ def params_old(N: int, k: int, eps: float, s_min: int = S_MIN_OLD, s_max: int = 
 
 MODE_DEFAULT = 0
 MODE_OLD = 1
+MODE_EXACT = 2
 
 
 def params(N: int, k: int, eps: float, mode: int = MODE_DEFAULT):
@@ -228,6 +230,9 @@ def params(N: int, k: int, eps: float, mode: int = MODE_DEFAULT):
         S = min(S, N)
         return S, min(max(t, 1), S), min(max(M, k), N)
     S = min(sample_size_old(N, k, eps), N)
+    if mode == MODE_EXACT:  # Theorem 4 at that S
+        t, M = params_exact(N, k, S, eps)
+        return S, min(max(t, 1), S), min(max(M, k), N)
     t, M = params_fast(N, k, S, eps)
     return S, t, M
 

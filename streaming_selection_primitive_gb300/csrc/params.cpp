@@ -92,6 +92,78 @@ int64_t buffer_capacity_fast(int64_t n, int64_t S, int64_t t, double eps) {
 
 static int64_t clamp64(int64_t v, int64_t lo, int64_t hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
+// ---- Exact optimal (t*, M*) for a given S: Theorem 4 of the corrected
+// version (Section 4), with the failure budget split eps/2 + eps/2.
+// X ~ Hypergeometric(N, K, S) counts the distinguished items among S drawn
+// without replacement from N, K of them distinguished.  The first pmf term
+// comes from log-binomials in extended precision, the next ones from the
+// ratio Pr(X = j+1) / Pr(X = j) = (K-j)(S-j) / ((j+1)(N-K-S+j+1)).
+namespace {
+
+long double log_choose(long double a, long double b) {
+  return std::lgamma(a + 1.0L) - std::lgamma(b + 1.0L) - std::lgamma(a - b + 1.0L);
+}
+
+// Walks the pmf upwards from the bottom of the support.
+struct HyperWalk {
+  int64_t N, K, S, j, hi;
+  double lp;  // log Pr(X = j)
+  HyperWalk(int64_t n, int64_t kk, int64_t s) : N(n), K(kk), S(s) {
+    j = s - (n - kk) > 0 ? s - (n - kk) : 0;
+    hi = kk < s ? kk : s;
+    lp = static_cast<double>(log_choose(static_cast<long double>(K), static_cast<long double>(j)) +
+                             log_choose(static_cast<long double>(N - K), static_cast<long double>(S - j)) -
+                             log_choose(static_cast<long double>(N), static_cast<long double>(S)));
+  }
+  double pmf() const { return std::exp(lp); }
+  void next() {
+    lp += std::log(static_cast<double>(K - j)) + std::log(static_cast<double>(S - j)) -
+          std::log(static_cast<double>(j + 1)) - std::log(static_cast<double>(N - K - S + j + 1));
+    ++j;
+  }
+};
+
+// Pr(X <= x).
+double hyper_cdf(int64_t N, int64_t K, int64_t S, int64_t x) {
+  HyperWalk w(N, K, S);
+  if (x < w.j) return 0.0;
+  if (x >= w.hi) return 1.0;
+  double c = 0.0;
+  for (;; w.next()) {
+    c += w.pmf();
+    if (w.j == x) break;
+  }
+  return c < 1.0 ? c : 1.0;
+}
+
+// min { x : Pr(X <= x) >= p }.
+int64_t hyper_quantile(int64_t N, int64_t K, int64_t S, double p) {
+  HyperWalk w(N, K, S);
+  double c = 0.0;
+  for (;; w.next()) {
+    c += w.pmf();
+    if (c >= p || w.j >= w.hi) return w.j;
+  }
+}
+
+}  // namespace
+
+void exact_params(int64_t n, int64_t k, int64_t S, double eps, int64_t* t, int64_t* M) {
+  // t*: the smallest t with Pr(fewer than t of the top k - 1 are sampled) ...
+  // i.e. t - 1 = the (1 - eps/2)-quantile of X_{k-1}; M*: the smallest M
+  // with Pr(X_M <= t - 1) <= eps/2 (nonincreasing in M, zero at M = n).
+  *t = hyper_quantile(n, k - 1, S, 1.0 - eps / 2.0) + 1;
+  int64_t lo = k, hi = n;
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (hyper_cdf(n, mid, S, *t - 1) <= eps / 2.0)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  *M = lo;
+}
+
 Params compute_params(int64_t n, int64_t k, double eps, int mode) {
   Params p{};
   if (mode == 1) {
@@ -113,6 +185,14 @@ Params compute_params(int64_t n, int64_t k, double eps, int mode) {
   }
   int64_t S = sample_size_thm5(n, k, eps);
   if (S > n) S = n;
+  if (mode == 2) {
+    int64_t t = 1, M = n;
+    exact_params(n, k, S, eps, &t, &M);
+    p.S = S;
+    p.t = clamp64(t, 1, S);
+    p.M = clamp64(M, k, n);
+    return p;
+  }
   const int64_t t = clamp64(threshold_rank_fast(n, k, S, eps), 1, S);
   const int64_t M = clamp64(buffer_capacity_fast(n, S, t, eps), k, n);
   p.S = S;

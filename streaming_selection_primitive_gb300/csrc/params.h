@@ -13,7 +13,10 @@ double inv_norm_cdf(double p);
 int64_t sample_size_thm5(int64_t n, int64_t k, double eps);
 int64_t threshold_rank_fast(int64_t n, int64_t k, int64_t S, double eps);
 int64_t buffer_capacity_fast(int64_t n, int64_t S, int64_t t, double eps);
-// mode 0: default rule, mode 1: the older version's Algorithm 1 literally.
+// Theorem 4 (corrected version): exact optimal t and M for a given S.
+void exact_params(int64_t n, int64_t k, int64_t S, double eps, int64_t* t, int64_t* M);
+// mode 0: default rule, mode 1: the older version's Algorithm 1 literally,
+// mode 2: S as in mode 0 with the exact t and M of Theorem 4.
 Params compute_params(int64_t n, int64_t k, double eps, int mode);
 // Sampling pays off only when S <= n/8 and k <= n/64; otherwise the exact path runs.
 bool uses_filter(int64_t n, int64_t k, int64_t S);

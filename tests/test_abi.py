@@ -32,10 +32,15 @@ def test_library_exports_every_declared_symbol(pk):
     assert not missing, missing
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_params_match_oracle(pk, mode):
-    for N in (1 << 20, 1 << 22, 1 << 26, 1 << 28, 1 << 30, 50331648, 1 << 24, 3_000_000_000, 1 << 32):
-        for k in (1, 2, 32, 64, 1024, 4096, 32768, 131072, 1 << 19):
+    # The oracle's exact search (mode 2) is slow, so it gets a smaller grid.
+    Ns = (1 << 20, 1 << 22, 1 << 26, 1 << 28, 1 << 30, 50331648, 1 << 24, 3_000_000_000, 1 << 32)
+    ks = (1, 2, 32, 64, 1024, 4096, 32768, 131072, 1 << 19)
+    if mode == 2:
+        Ns, ks = (1 << 20, 1 << 26, 1 << 30, 3_000_000_000), (1, 32, 1024, 131072)
+    for N in Ns:
+        for k in ks:
             for eps in (1e-3, 1e-3 / 64, 0.05):
                 if k > N:
                     continue
@@ -50,6 +55,7 @@ def test_options_roundtrip_and_validation(pk):
         pk.set_option(99, 1)
     with pytest.raises(pk.ProfkError):
         pk.set_option(pk.OPT_PARAM_MODE, 5)
+    pk.set_option(pk.OPT_PARAM_MODE, 2)  # the exact Theorem 4 mode
     with pytest.raises(pk.ProfkError):
         pk.set_option(pk.OPT_FORCE_S, -1)
 

@@ -232,3 +232,16 @@ def test_batched_many_rows(pk, cuda_device, rows, n, k):
         assert_same(vals[r], idx[r], *topk_sort(h, k), f"row {r}")
     paths = {s["path"] for s in sts}
     assert paths == ({pk.PATH_EXACT} if n == 1 << 16 else {pk.PATH_FILTER}) or pk.PATH_FALLBACK not in paths
+
+
+def test_exact_parameter_mode(pk, cuda_device):
+    """Theorem 4's exact t and M (PROFK_PARAMS_EXACT) through the whole call."""
+    x = workloads.normal((1 << 22) + 12, 9, cuda_device)
+    pk.set_option(pk.OPT_PARAM_MODE, pk.PARAMS_EXACT)
+    h = x.cpu().numpy()
+    for k in (32, 1000):
+        vals, idx, st = pk.topk(x, k, 1e-3, 4)
+        ov, oi, ost = PK.profk(h, k, 1e-3, 4, mode=2)
+        assert_same(vals, idx, ov, oi, f"exact-parameter mode k={k}")
+        assert (st["S"], st["t"], st["M"]) == (ost.S, ost.t, ost.M)
+        assert st["R_first"] == ost.R_first and st["attempts"] == ost.attempts
