@@ -118,6 +118,29 @@ int profk_topk_batched(const float* x, int64_t rows, int64_t n, int64_t ld, int6
                        double eps, uint64_t seed, float* out_vals, int64_t* out_idx,
                        cudaStream_t stream, profk_stats* stats);
 
+/* Asynchronous form of profk_topk / profk_topk_batched.  The call enqueues
+ * the first attempt (sampling, filter, the refinement and a kernel that
+ * writes the run-time check's counts into pinned host memory) on `stream`
+ * and returns at once with *call set; profk_wait(call, stats) then completes
+ * it: it waits for those counts (not for the stream), and if every row
+ * passed the check the outputs are final and stream-ordered; otherwise (a
+ * redraw, the tie exit, the fallback, a NaN) it runs the whole call again
+ * synchronously, with the same result and statistics as profk_topk.  Calls
+ * with non-default options (forced parameters, timing, no attempts), those
+ * routed to the exact path, and those made while a caller workspace is set
+ * run synchronously at submission instead.  Each call owns its workspace, so
+ * several may be in flight; every call must be passed to profk_wait exactly
+ * once, which also frees it.  Submission returns PROFK_ERR_INVALID /
+ * PROFK_ERR_UNSUPPORTED as profk_topk does (with *call NULL) and PROFK_OK
+ * otherwise; the call's own status is profk_wait's return value. */
+typedef struct profk_call profk_call;
+int profk_topk_async(const float* x, int64_t n, int64_t k, double eps, uint64_t seed,
+                     float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_call** call);
+int profk_topk_batched_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
+                             double eps, uint64_t seed, float* out_vals, int64_t* out_idx,
+                             cudaStream_t stream, profk_call** call);
+int profk_wait(profk_call* call, profk_stats* stats /* array[rows] or NULL */);
+
 /* Parameters (S, t, M) for one row of length n at budget eps.
  *   mode PROFK_PARAMS_DEFAULT: S from the older version's Theorem 5,
  *     S* = (z log2(k) / 2)^(2/3) (k(n-k))^(1/3) with z = 2 Phi^{-1}(1-eps/2),

@@ -139,6 +139,67 @@ def topk_batched(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=N
     return vals, idx, [s.as_dict() for s in sts]
 
 
+class Pending:
+    """An asynchronous call (topk_async / topk_batched_async).  wait() completes
+    it exactly once and returns (values, indices, stats); it keeps the input and
+    the outputs alive until then."""
+
+    def __init__(self, handle, x, vals, idx, rows, batched):
+        self._h, self._x, self.vals, self.idx, self.rows, self.batched = handle, x, vals, idx, rows, batched
+
+    def wait(self):
+        if self._h is None:
+            raise RuntimeError("this call was already waited for")
+        sts = (ProfkStats * self.rows)()
+        code = lib().profk_wait(self._h, sts)
+        self._h, self._x = None, None
+        _abi.check(code)
+        if self.batched:
+            return self.vals, self.idx, [s.as_dict() for s in sts]
+        return self.vals, self.idx, sts[0].as_dict()
+
+    def __del__(self):
+        if getattr(self, "_h", None) is not None:
+            lib().profk_wait(self._h, None)
+
+
+def topk_async(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=None) -> Pending:
+    """Asynchronous topk: enqueues the call and returns a Pending; see Pending.wait."""
+    torch = _torch()
+    _need_cuda_f32(x)
+    if x.dim() != 1 or not x.is_contiguous():
+        raise ValueError("x must be 1-D and contiguous")
+    if out is None:
+        vals = torch.empty(k, dtype=torch.float32, device=x.device)
+        idx = torch.empty(k, dtype=torch.int64, device=x.device)
+    else:
+        vals, idx = out
+    h = C.c_void_p()
+    _abi.check(lib().profk_topk_async(x.data_ptr(), x.numel(), int(k), float(eps), int(seed) & (2**64 - 1),
+                                      vals.data_ptr(), idx.data_ptr(), _stream_handle(stream, x.device),
+                                      C.byref(h)))
+    return Pending(h, x, vals, idx, 1, False)
+
+
+def topk_batched_async(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=None) -> Pending:
+    """Asynchronous topk_batched: enqueues the call and returns a Pending."""
+    torch = _torch()
+    _need_cuda_f32(x)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    rows, n = x.shape
+    if out is None:
+        vals = torch.empty((rows, k), dtype=torch.float32, device=x.device)
+        idx = torch.empty((rows, k), dtype=torch.int64, device=x.device)
+    else:
+        vals, idx = out
+    h = C.c_void_p()
+    _abi.check(lib().profk_topk_batched_async(x.data_ptr(), rows, n, x.stride(0), int(k), float(eps),
+                                              int(seed) & (2**64 - 1), vals.data_ptr(), idx.data_ptr(),
+                                              _stream_handle(stream, x.device), C.byref(h)))
+    return Pending(h, x, vals, idx, rows, True)
+
+
 def sample(x, S: int, seed: int, row: int = 0, attempt: int = 0, stream=None):
     """Step 1 alone: the sample's indices (int64, draw order) and values."""
     torch = _torch()

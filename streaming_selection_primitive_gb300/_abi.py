@@ -66,6 +66,12 @@ _SIGS = {
                                C.POINTER(C.c_int64), C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
     "profk_workspace_size": (C.c_size_t, [C.c_int64, C.c_int64, C.c_int64, C.c_double]),
     "profk_set_workspace": (C.c_int, [C.c_void_p, C.c_size_t]),
+    "profk_topk_async": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_double, C.c_uint64, C.c_void_p,
+                                   C.c_void_p, C.c_void_p, C.POINTER(C.c_void_p)]),
+    "profk_topk_batched_async": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_int64, C.c_double,
+                                           C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p,
+                                           C.POINTER(C.c_void_p)]),
+    "profk_wait": (C.c_int, [C.c_void_p, C.c_void_p]),
     "profk_set_option": (C.c_int, [C.c_int, C.c_int64]),
     "profk_get_option": (C.c_int64, [C.c_int]),
     "profk_strerror": (C.c_char_p, [C.c_int]),

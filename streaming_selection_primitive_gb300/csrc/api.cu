@@ -454,6 +454,79 @@ void fill_stats_params(profk_stats* s, const Params& P) {
 }
 
 
+// One attempt of the listed rows (gl, ng of them; all rows when gl is null):
+// reset, sampling and tau, filter, and the refinement, which is enqueued
+// before the host has seen the counts (a row whose count fails the check is
+// voided on the device and left untouched, so the host round trip of the
+// check is off the critical path of the likely successful attempt).  ev:
+// stage events e[1..4] (e[0] is the caller's), or nullptr.
+cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, int ng, const int* gl, int64_t rows,
+                            const float* x, int64_t ld, int64_t n, int64_t k, uint64_t seed, int64_t cps,
+                            float* out_vals, int64_t* out_idx, cudaStream_t stream, cudaEvent_t* ev) {
+  RowState* st = at<RowState>(ws, L.off_state);
+  const int64_t H = 1ll << L.log2H;
+  // Reset CTAs per row: about eight 16-byte stores per thread of 256.
+  const unsigned rb = static_cast<unsigned>(std::min<int64_t>(std::max<int64_t>(H / 2 / (256 * 8), 1), 64));
+  // The refinement's control blocks start every attempt at zero.
+  unsigned long long* ref_ctl =
+      L.radix_refine ? static_cast<unsigned long long*>(radix_sort_ctl(at<char>(ws, L.off_sort), P.M, rows))
+                     : static_cast<unsigned long long*>(refine_grid_ctl(at<char>(ws, L.off_refine)));
+  const int ref_words = static_cast<int>((L.radix_refine ? radix_sort_ctl_bytes() : refine_grid_ctl_bytes()) / 8);
+  launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, at<unsigned long long>(ws, L.off_table), L.log2H, gl,
+                st, static_cast<unsigned long long>(P.t), ref_ctl, ref_words, at<unsigned long long>(ws, L.off_sctl),
+                static_cast<int>(sample_tau_ctl_bytes() / 8));
+  // Sampling and tau: one persistent kernel (its stage time is reported as
+  // the sampling's, the threshold stage then being empty), or, when many rows
+  // share the SMs, the step-by-step kernels with the first radix pass of tau
+  // fused into the sampler's last one.
+  SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, a, ng, gl, st,
+                at<unsigned long long>(ws, L.off_table), at<uint32_t>(ws, L.off_draws),
+                at<uint32_t>(ws, L.off_blockcnt), at<uint32_t>(ws, L.off_sidx), at<uint32_t>(ws, L.off_skeys), false,
+                static_cast<unsigned long long>(P.t)};
+  cudaError_t e = cudaSuccess;
+  if (sample_tau_fits(L.D, ng)) {
+    e = launch_sample_tau(sa, at<char>(ws, L.off_sctl), stream);
+    if (e != cudaSuccess) return e;
+    if (ev) cudaEventRecord(ev[1], stream);
+  } else {
+    sa.tau_pass1 = true;
+    launch_sample(sa, stream);
+    if (ev) cudaEventRecord(ev[1], stream);
+    SelectArgs ta{KeySource::SampleKeys, at<uint32_t>(ws, L.off_skeys), P.S, P.S, ng, gl, st};
+    launch_select(ta, 0, true, 1, stream);  // its last pass stores tau
+  }
+  if (ev) cudaEventRecord(ev[2], stream);
+  FilterArgs fa{x, ld, n, P.M, ng, gl, st, at<unsigned long long>(ws, L.off_buf), filter_grid(cps)};
+  launch_filter(fa, stream);
+  if (ev) cudaEventRecord(ev[3], stream);
+  if (!L.radix_refine) {
+    RefineGridArgs ga{at<unsigned long long>(ws, L.off_buf), P.M, ng, gl, st, k, x, ld, n, out_vals, out_idx};
+    e = launch_refine_grid(ga, at<char>(ws, L.off_refine), rows, stream);
+  } else {
+    // The whole buffer (R <= M keys) is sorted and its first k emitted.
+    RadixSortArgs ra{at<unsigned long long>(ws, L.off_buf), P.M, k, SortCount::FromState, ng, gl, rows,
+                     at<char>(ws, L.off_sort), true, x, ld, n, out_vals, out_idx, st};
+    e = launch_radix_sort(ra, stream);
+  }
+  if (e != cudaSuccess) return e;
+  if (ev) cudaEventRecord(ev[4], stream);
+  return cudaGetLastError();
+}
+
+// The check's report of the first `rows` row states into `rep` (pinned):
+// written by k_report followed by the sequence number in *flag (up to
+// REPORT_ROWS_MAPPED rows), else copied (the caller then synchronizes).
+cudaError_t enqueue_report(const RowState* st, int64_t rows, char* rep, unsigned long long* flag,
+                           unsigned long long seq, cudaStream_t stream) {
+  if (rows <= REPORT_ROWS_MAPPED) {
+    launch_kernel(k_report, 1, 256, 0, stream, st, static_cast<int>(rows), reinterpret_cast<unsigned*>(rep), flag,
+                  seq);
+    return cudaGetLastError();
+  }
+  return cudaMemcpy2DAsync(rep, REPORT_BYTES, st, sizeof(RowState), REPORT_BYTES, rows, cudaMemcpyDeviceToHost,
+                           stream);
+}
+
 int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,
              float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_stats* stats) {
   if (!x || !out_vals || !out_idx) return PROFK_ERR_INVALID;
@@ -530,79 +603,32 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
     int* gl = nullptr;
     PK_CHECK(upload_rows(L, c.ws, hbuf, 0, group, stream, &gl));
     {
-      const int64_t H = 1ll << L.log2H;
-      // Reset CTAs per row: about eight 16-byte stores per thread of 256.
-      const unsigned rb = static_cast<unsigned>(std::min<int64_t>(std::max<int64_t>(H / 2 / (256 * 8), 1), 64));
       const bool time_it = timing && first_filter;
       if (time_it) {
         if (!t_events.e[0])
           for (auto& ev : t_events.e) PK_CHECK(cudaEventCreate(&ev));
         PK_CHECK(cudaEventRecord(t_events.e[0], stream));
       }
-      // The refinement's control blocks start every attempt at zero.
-      unsigned long long* ref_ctl =
-          L.radix_refine ? static_cast<unsigned long long*>(radix_sort_ctl(at<char>(c.ws, L.off_sort), P.M, rows))
-                         : static_cast<unsigned long long*>(refine_grid_ctl(at<char>(c.ws, L.off_refine)));
-      const int ref_words = static_cast<int>((L.radix_refine ? radix_sort_ctl_bytes() : refine_grid_ctl_bytes()) / 8);
-      launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, at<unsigned long long>(c.ws, L.off_table),
-                    L.log2H, gl, st, static_cast<unsigned long long>(P.t), ref_ctl, ref_words,
-                    at<unsigned long long>(c.ws, L.off_sctl), static_cast<int>(sample_tau_ctl_bytes() / 8));
-      // Sampling and tau: one persistent kernel (its stage time is reported as
-      // the sampling's, the threshold stage then being empty), or, when many
-      // rows share the SMs, the step-by-step kernels with the first radix pass
-      // of tau fused into the sampler's last one.
-      SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, a, ng, gl, st,
-                    at<unsigned long long>(c.ws, L.off_table), at<uint32_t>(c.ws, L.off_draws),
-                    at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
-                    at<uint32_t>(c.ws, L.off_skeys), false, static_cast<unsigned long long>(P.t)};
-      if (sample_tau_fits(L.D, ng)) {
-        PK_CHECK(launch_sample_tau(sa, at<char>(c.ws, L.off_sctl), stream));
-        if (time_it) PK_CHECK(cudaEventRecord(t_events.e[1], stream));
-      } else {
-        sa.tau_pass1 = true;
-        launch_sample(sa, stream);
-        if (time_it) PK_CHECK(cudaEventRecord(t_events.e[1], stream));
-        SelectArgs ta{KeySource::SampleKeys, at<uint32_t>(c.ws, L.off_skeys), P.S, P.S, ng, gl, st};
-        launch_select(ta, 0, true, 1, stream);  // its last pass stores tau
-      }
-      if (time_it) PK_CHECK(cudaEventRecord(t_events.e[2], stream));
-      FilterArgs fa{x, ld, n, P.M, ng, gl, st, at<unsigned long long>(c.ws, L.off_buf), filter_grid(cps)};
-      launch_filter(fa, stream);
-      if (time_it) PK_CHECK(cudaEventRecord(t_events.e[3], stream));
-      // Refinement, launched before the host has seen the counts: a row whose
-      // count fails the check is voided on the device and left untouched, so
-      // the host round trip of the check is off the critical path of the
-      // (likely) successful attempt.
-      if (!L.radix_refine) {
-        RefineGridArgs ga{at<unsigned long long>(c.ws, L.off_buf), P.M, ng, gl, st, k, x, ld, n, out_vals, out_idx};
-        PK_CHECK(launch_refine_grid(ga, at<char>(c.ws, L.off_refine), rows, stream));
-      } else {
-        // The whole buffer (R <= M keys) is sorted and its first k emitted.
-        RadixSortArgs ra{at<unsigned long long>(c.ws, L.off_buf), P.M, k, SortCount::FromState, ng, gl, rows,
-                         at<char>(c.ws, L.off_sort), true, x, ld, n, out_vals, out_idx, st};
-        PK_CHECK(launch_radix_sort(ra, stream));
-      }
+      PK_CHECK(enqueue_attempt(L, c.ws, P, a, ng, gl, rows, x, ld, n, k, seed, cps, out_vals, out_idx, stream,
+                               time_it ? t_events.e : nullptr));
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[4], stream));
       PK_CHECK(cudaGetLastError());
       // Run-time check: read the exact counts of every row (written into
       // pinned memory by a kernel and waited for, or copied and synchronized
       // for many rows).
       char* rep = static_cast<char*>(hbuf) + sizeof(int) * rows * 4;
-      if (rows <= REPORT_ROWS_MAPPED) {
+      {
         unsigned long long* flag =
             reinterpret_cast<unsigned long long*>(align_up(reinterpret_cast<uintptr_t>(rep + REPORT_BYTES * rows)));
         const unsigned long long seq = ++t_report_seq;
-        launch_kernel(k_report, 1, 256, 0, stream, st, static_cast<int>(rows), reinterpret_cast<unsigned*>(rep), flag,
-                      seq);
+        PK_CHECK(enqueue_report(st, rows, rep, flag, seq, stream));
         if (time_it) PK_CHECK(cudaEventRecord(t_events.e[5], stream));
-        PK_CHECK(cudaGetLastError());
-        PK_CHECK(wait_report(flag, seq, stream));
-        if (time_it) PK_CHECK(cudaEventSynchronize(t_events.e[5]));
-      } else {
-        PK_CHECK(cudaMemcpy2DAsync(rep, REPORT_BYTES, st, sizeof(RowState), REPORT_BYTES, rows,
-                                   cudaMemcpyDeviceToHost, stream));
-        if (time_it) PK_CHECK(cudaEventRecord(t_events.e[5], stream));
-        PK_CHECK(cudaStreamSynchronize(stream));
+        if (rows <= REPORT_ROWS_MAPPED) {
+          PK_CHECK(wait_report(flag, seq, stream));
+          if (time_it) PK_CHECK(cudaEventSynchronize(t_events.e[5]));
+        } else {
+          PK_CHECK(cudaStreamSynchronize(stream));
+        }
       }
       if (time_it) {
         PK_CHECK(cudaEventElapsedTime(&filter_ms, t_events.e[2], t_events.e[3]));
@@ -749,11 +775,216 @@ bool pdl_enabled() { return g_opt[PROFK_OPT_PDL].load(std::memory_order_relaxed)
 
 using namespace profk;
 
+// An asynchronous call (profk_topk_async / profk_topk_batched_async): its
+// first attempt is enqueued and the check's report is waited for later, in
+// profk_wait.  A call that the check does not clear is run again, whole and
+// synchronously, at that point (the same seed gives the same attempt, so the
+// outputs and statistics are those of the synchronous call).
+struct profk_call {
+  const float* x = nullptr;
+  int64_t rows = 0, n = 0, ld = 0, k = 0;
+  double eps = 0.0;
+  uint64_t seed = 0;
+  float* out_vals = nullptr;
+  int64_t* out_idx = nullptr;
+  cudaStream_t stream = nullptr;
+  bool complete = false;  // already run synchronously at submission
+  int status = PROFK_OK;
+  std::vector<profk_stats> stats;
+  Params P{};
+  size_t ws_bytes = 0;
+  void* ws = nullptr;
+  char* host = nullptr;  // pinned: the report, then the flag
+  size_t host_bytes = 0;
+  unsigned long long* flag = nullptr;
+  unsigned long long seq = 0;
+  cudaEvent_t copied = nullptr;  // the report copy of more than REPORT_ROWS_MAPPED rows
+  int64_t launches = 0;
+};
+
+namespace {
+
+// Process-wide sequence numbers of asynchronous reports (never reused, so a
+// recycled pinned block cannot show a stale match).
+std::atomic<unsigned long long> g_async_seq{0};
+
+// Pinned report blocks, recycled per host thread.
+struct PinnedBlock {
+  char* p;
+  size_t bytes;
+};
+thread_local std::vector<PinnedBlock> t_free_blocks;
+
+cudaError_t take_block(size_t bytes, char** out, size_t* got) {
+  for (size_t i = 0; i < t_free_blocks.size(); ++i) {
+    if (t_free_blocks[i].bytes >= bytes) {
+      *out = t_free_blocks[i].p;
+      *got = t_free_blocks[i].bytes;
+      t_free_blocks.erase(t_free_blocks.begin() + static_cast<std::ptrdiff_t>(i));
+      return cudaSuccess;
+    }
+  }
+  const size_t cap = std::max<size_t>(bytes, 4096);
+  void* p = nullptr;
+  const cudaError_t e = cudaHostAlloc(&p, cap, cudaHostAllocDefault);
+  if (e != cudaSuccess) return e;
+  *out = static_cast<char*>(p);
+  *got = cap;
+  return cudaSuccess;
+}
+
+void give_block(char* p, size_t bytes) {
+  if (p) t_free_blocks.push_back({p, bytes});
+}
+
+int submit_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,
+                 float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_call** out) {
+  if (!out) return PROFK_ERR_INVALID;
+  *out = nullptr;
+  if (!x || !out_vals || !out_idx) return PROFK_ERR_INVALID;
+  if (rows < 1 || n < 1 || k < 1 || k > n || ld < n || !(eps > 0.0 && eps < 1.0)) return PROFK_ERR_INVALID;
+  if (rows > (1 << 20)) return PROFK_ERR_INVALID;
+  if (n > (1ll << 32)) return PROFK_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) != 0 || (rows > 1 && (ld & 3) != 0)) return PROFK_ERR_UNSUPPORTED;
+  profk_call* call = new profk_call;
+  call->x = x;
+  call->rows = rows;
+  call->n = n;
+  call->ld = ld;
+  call->k = k;
+  call->eps = eps;
+  call->seed = seed;
+  call->out_vals = out_vals;
+  call->out_idx = out_idx;
+  call->stream = stream;
+  call->stats.resize(static_cast<size_t>(rows));
+  *out = call;
+
+  const int mode = static_cast<int>(g_opt[PROFK_OPT_PARAM_MODE].load());
+  const bool plain = g_opt[PROFK_OPT_FORCE_S].load() == 0 && g_opt[PROFK_OPT_FORCE_T].load() == 0 &&
+                     g_opt[PROFK_OPT_FORCE_M].load() == 0 && g_opt[PROFK_OPT_TIMING].load() == 0 &&
+                     g_opt[PROFK_OPT_MAX_ATTEMPTS].load() > 0 && t_user_ws == nullptr;
+  const Params P = cached_params(n, k, eps / static_cast<double>(rows), mode);
+  if (!plain || !uses_filter(n, k, P.S)) {
+    // Options, routes and caller workspaces outside the asynchronous form:
+    // the call runs now; profk_wait returns its result.
+    call->status = run_topk(x, rows, n, ld, k, eps, seed, out_vals, out_idx, stream, call->stats.data());
+    call->complete = true;
+    return PROFK_OK;
+  }
+  call->P = P;
+  const int64_t launches0 = launch_count();
+  const Layout L = make_layout(rows, n, k, P.S, draw_budget(n, P.S), P.M, true);
+  Call c;
+  c.stream = stream;
+  cudaError_t e = ws_alloc(c, L.total, false);
+  if (e == cudaSuccess) {
+    call->ws = c.ws;
+    call->ws_bytes = L.total;
+    e = take_block(REPORT_BYTES * rows + 512, &call->host, &call->host_bytes);
+  }
+  if (e == cudaSuccess)
+    e = enqueue_attempt(L, call->ws, P, 0, static_cast<int>(rows), nullptr, rows, x, ld, n, k, seed,
+                        g_opt[PROFK_OPT_FILTER_CTAS_PER_SM].load(), out_vals, out_idx, stream, nullptr);
+  if (e == cudaSuccess) {
+    call->flag = reinterpret_cast<unsigned long long*>(
+        align_up(reinterpret_cast<uintptr_t>(call->host + REPORT_BYTES * rows)));
+    call->seq = ++g_async_seq;
+    e = enqueue_report(at<RowState>(call->ws, L.off_state), rows, call->host, call->flag, call->seq, stream);
+  }
+  if (e == cudaSuccess && rows > REPORT_ROWS_MAPPED) {
+    e = cudaEventCreateWithFlags(&call->copied, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(call->copied, stream);
+  }
+  call->launches = launch_count() - launches0;
+  if (e != cudaSuccess) {
+    // Nothing usable was enqueued: the call completes with the error.
+    if (call->ws) cudaFreeAsync(call->ws, stream);
+    call->ws = nullptr;
+    give_block(call->host, call->host_bytes);
+    call->host = nullptr;
+    for (auto& s : call->stats) s.cuda_error = static_cast<int32_t>(e);
+    call->status = PROFK_ERR_CUDA;
+    call->complete = true;
+  }
+  return PROFK_OK;
+}
+
+int finish_async(profk_call* call, profk_stats* stats) {
+  int status = call->status;
+  if (!call->complete) {
+    cudaError_t e = call->rows <= REPORT_ROWS_MAPPED ? wait_report(call->flag, call->seq, call->stream)
+                                                     : cudaEventSynchronize(call->copied);
+    bool clear = e == cudaSuccess;
+    const unsigned long long k = static_cast<unsigned long long>(call->k);
+    for (int64_t r = 0; clear && r < call->rows; ++r) {
+      const char* h = call->host + REPORT_BYTES * r;
+      unsigned long long Rg = 0, Rt = 0, nanc = 0;
+      unsigned distinct = 0, tau_key = 0, errf = 0;
+      std::memcpy(&Rg, h + offsetof(RowState, R_ge), 8);
+      std::memcpy(&Rt, h + offsetof(RowState, R_gt), 8);
+      std::memcpy(&nanc, h + offsetof(RowState, nan), 8);
+      std::memcpy(&distinct, h + offsetof(RowState, distinct), 4);
+      std::memcpy(&tau_key, h + offsetof(RowState, tau_key), 4);
+      std::memcpy(&errf, h + offsetof(RowState, error), 4);
+      clear = nanc == 0 && errf == 0 && static_cast<int64_t>(distinct) >= call->P.S && k <= Rg &&
+              Rg <= static_cast<unsigned long long>(call->P.M);
+      if (clear) {
+        profk_stats& s = call->stats[static_cast<size_t>(r)];
+        fill_stats_params(&s, call->P);
+        const float tau = key_to_float(tau_key);
+        s.R_first = s.R_final = static_cast<int64_t>(Rg);
+        s.R_gt_first = s.R_gt_final = static_cast<int64_t>(Rt);
+        s.tau_first = s.tau_final = tau;
+        s.attempts = 1;
+        s.path = PROFK_PATH_FILTER;
+        s.aux_bytes = call->ws_bytes;
+        s.launches = static_cast<int32_t>(call->launches);
+      }
+    }
+    cudaFreeAsync(call->ws, call->stream);
+    call->ws = nullptr;
+    if (call->copied) cudaEventDestroy(call->copied);
+    give_block(call->host, call->host_bytes);
+    call->host = nullptr;
+    if (clear) {
+      status = PROFK_OK;
+    } else {
+      // Not cleared (a redraw, the tie exit, the fallback, NaN, an error):
+      // the whole call again, synchronously.
+      status = run_topk(call->x, call->rows, call->n, call->ld, call->k, call->eps, call->seed, call->out_vals,
+                        call->out_idx, call->stream, call->stats.data());
+    }
+  }
+  if (stats)
+    for (int64_t r = 0; r < call->rows; ++r) stats[r] = call->stats[static_cast<size_t>(r)];
+  delete call;
+  return status;
+}
+
+}  // namespace
+
 extern "C" {
 
 int profk_topk(const float* x, int64_t n, int64_t k, double eps, uint64_t seed, float* out_vals, int64_t* out_idx,
                cudaStream_t stream, profk_stats* stats) {
   return run_topk(x, 1, n, n, k, eps, seed, out_vals, out_idx, stream, stats);
+}
+
+int profk_topk_async(const float* x, int64_t n, int64_t k, double eps, uint64_t seed, float* out_vals,
+                     int64_t* out_idx, cudaStream_t stream, profk_call** call) {
+  return submit_async(x, 1, n, n, k, eps, seed, out_vals, out_idx, stream, call);
+}
+
+int profk_topk_batched_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps,
+                             uint64_t seed, float* out_vals, int64_t* out_idx, cudaStream_t stream,
+                             profk_call** call) {
+  return submit_async(x, rows, n, ld, k, eps, seed, out_vals, out_idx, stream, call);
+}
+
+int profk_wait(profk_call* call, profk_stats* stats) {
+  if (!call) return PROFK_ERR_INVALID;
+  return finish_async(call, stats);
 }
 
 int profk_topk_batched(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,

@@ -22,7 +22,8 @@ def test_header_declares_the_method(pk):
     names = declared_functions()
     for must in ("profk_topk", "profk_topk_batched", "profk_params", "profk_workspace_size",
                  "profk_set_option", "profk_get_option", "profk_strerror", "profk_sample",
-                 "profk_threshold", "profk_filter", "profk_refine", "profk_exact", "profk_set_workspace"):
+                 "profk_threshold", "profk_filter", "profk_refine", "profk_exact", "profk_set_workspace",
+                 "profk_topk_async", "profk_topk_batched_async", "profk_wait"):
         assert must in names
 
 
@@ -102,3 +103,14 @@ def test_set_workspace_validation(pk):
     assert lib.profk_set_workspace(C.c_void_p(256 + 8), 1 << 20) == -1  # not 256-byte aligned
     assert lib.profk_set_workspace(None, 0) == 0
     assert lib.profk_set_workspace(C.c_void_p(1 << 20), 0) == 0  # zero bytes: back to the pool
+
+
+def test_async_argument_checks(pk):
+    lib = pk.lib()
+    h = C.c_void_p(7)
+    fake = C.c_void_p(256)
+    assert lib.profk_topk_async(None, 10, 1, 1e-3, 0, fake, fake, None, C.byref(h)) == -1
+    assert not h.value  # no call was created
+    assert lib.profk_topk_async(fake, 10, 1, 1e-3, 0, fake, fake, None, None) == -1
+    assert lib.profk_topk_batched_async(fake, 2, 10, 10, 1, 1e-3, 0, fake, fake, None, C.byref(h)) == -4
+    assert lib.profk_wait(None, None) == -1

@@ -245,3 +245,47 @@ def test_exact_parameter_mode(pk, cuda_device):
         assert_same(vals, idx, ov, oi, f"exact-parameter mode k={k}")
         assert (st["S"], st["t"], st["M"]) == (ost.S, ost.t, ost.M)
         assert st["R_first"] == ost.R_first and st["attempts"] == ost.attempts
+
+
+STAT_KEYS = ("S", "t", "M", "R_first", "R_gt_first", "tau_first", "R_final", "attempts", "path")
+
+
+def test_async_matches_sync(pk, cuda_device):
+    x = workloads.normal((1 << 22) + 4, 21, cuda_device)
+    calls = ((1, 32), (2, 1000), (3, 5000), (4, 20000))
+    ref = [pk.topk(x, k, 1e-3, s) for s, k in calls]
+    pend = [pk.topk_async(x, k, 1e-3, s) for s, k in calls]  # all in flight at once
+    for p, r in zip(pend, ref):
+        v, i, st = p.wait()
+        assert torch.equal(v, r[0]) and torch.equal(i, r[1])
+        assert all(st[key] == r[2][key] for key in STAT_KEYS), (st, r[2])
+
+
+def test_async_rerun_when_not_cleared(pk, cuda_device):
+    # 16 levels: tau lands on a level, R > M, the check does not clear the
+    # first attempt and the call runs again (tie exit).
+    x = workloads.levels16(1 << 20, 3, cuda_device)
+    h = x.cpu().numpy()
+    for k in (100, 5000):
+        v, i, st = pk.topk_async(x, k, 1e-3, 5).wait()
+        ov, oi, ost = PK.profk(h, k, 1e-3, 5)
+        assert_same(v, i, ov, oi, f"async tie k={k}")
+        assert st["path"] == ost.path and st["attempts"] == ost.attempts
+
+
+def test_async_nan(pk, cuda_device):
+    x = workloads.normal(1 << 20, 3, cuda_device)
+    x[777] = float("nan")
+    p = pk.topk_async(x, 64, 1e-3, 1)
+    with pytest.raises(pk.ProfkError) as e:
+        p.wait()
+    assert e.value.code == -3
+
+
+@pytest.mark.parametrize("rows,n,k", [(3, 1 << 20, 50), (80, 1 << 18, 20)])
+def test_async_batched(pk, cuda_device, rows, n, k):
+    x = workloads.normal_rows(rows, n, 8, cuda_device)
+    ref = pk.topk_batched(x, k, 1e-3, 2)
+    v, i, sts = pk.topk_batched_async(x, k, 1e-3, 2).wait()
+    assert torch.equal(v, ref[0]) and torch.equal(i, ref[1])
+    assert [s["R_first"] for s in sts] == [s["R_first"] for s in ref[2]]
