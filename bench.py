@@ -14,6 +14,11 @@ Prints ONE JSON line (rank 0).  Keys beyond the base contract:
                 copies x host->device from pinned memory, runs the call and
                 copies the k results back
   sweep         the other k and distributions at 2^30 (fewer steps each)
+  synchronous   the same calls through profk_topk (one host round trip per call)
+
+The timed steps go through the asynchronous form (profk_topk_async, all K calls
+in flight, each completed by profk_wait): one step is still one whole exact
+top-k call, check included.
 
 --impl reference times the CPU oracle itself (the reference arm).
 """
@@ -237,6 +242,7 @@ def main():
     out = (torch.empty(k, dtype=torch.float32, device=dev), torch.empty(k, dtype=torch.int64, device=dev))
     for w in range(args.warmup):
         pk.topk(x, k, EPS, 10_000 + w, out=out)
+        pk.topk_async(x, k, EPS, 20_000 + w, out=out).wait()
     barrier()
     filter_ms, attempts, launches, paths, Rs = [], [], 0, [], []
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -244,11 +250,14 @@ def main():
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         gpu_id = str(dev.index)
+    # The job: K calls on the resident input through the asynchronous form
+    # (profk_topk_async), all in flight, each completed with profk_wait.
     with ClockSampler(gpu_id) as clk:
         barrier()
         ev0.record(stream)
-        for s in range(args.steps):
-            _, _, st = pk.topk(x, k, EPS, 1000 + s, out=out)
+        pending = [pk.topk_async(x, k, EPS, 1000 + s, out=out) for s in range(args.steps)]
+        for p in pending:
+            _, _, st = p.wait()
             attempts.append(st["attempts"])
             launches += st["launches"]
             paths.append(st["path"])
@@ -266,6 +275,22 @@ def main():
     peak, peak_kind = measured_peaks()
     traffic = traffic_from_profile(n)
     aux = pk.topk(x, k, EPS, 7, out=out)[2]["aux_bytes"]
+    # The same calls through the synchronous form (profk_topk: each call
+    # returns after its check, so the host round trip sits between calls).
+    barrier()
+    ev0.record(stream)
+    for s in range(args.steps):
+        pk.topk(x, k, EPS, 30_000 + s, out=out)
+    ev1.record(stream)
+    barrier()
+    sync_ms = ev0.elapsed_time(ev1)
+    if ws > 1:
+        t = torch.tensor([sync_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        sync_ms = float(t.item())
+    synchronous = {"api": "profk_topk", "value": round(n * args.steps * ws / (sync_ms / 1e3) / 1e9, 3),
+                   "unit": "Gelem/s", "ms_per_step": round(sync_ms / args.steps, 4),
+                   "hbm_frac_of_8TBs": round(4 * n / (sync_ms / args.steps / 1e3) / 8e12, 4)}
     # Stage breakdown and the filter's own launch time, from CUDA events the
     # library records around each stage on the call's stream (PROFK_OPT_TIMING),
     # in separate calls after the timed loop so the events cost it nothing.
@@ -318,8 +343,8 @@ def main():
                 a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 reps = 5
                 a0.record(stream)
-                for s in range(reps):
-                    _, _, st = pk.topk(xs, kk, EPS, 50_000 + s, out=o2)
+                for p in [pk.topk_async(xs, kk, EPS, 50_000 + s, out=o2) for s in range(reps)]:
+                    p.wait()
                 a1.record(stream)
                 torch.cuda.synchronize()
                 ms = a0.elapsed_time(a1) / reps
@@ -339,7 +364,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": f"normal_2^30_k{k}", "n": n, "k": k, "eps": EPS, "input": "float32 N(0,1)",
-                       "l2": "input 4 GiB > L2 129 MB: no flush between steps", "parallelism": f"replicas x{ws}"},
+                       "l2": "input 4 GiB > L2 129 MB: no flush between steps", "parallelism": f"replicas x{ws}",
+                       "api": f"profk_topk_async, {args.steps} calls in flight, each completed by profk_wait"},
             "hbm_gbs_end_to_end": round(4 * n / (ms_step / 1e3) / 1e9, 1),
             "hbm_frac_of_8TBs": round(4 * n / (ms_step / 1e3) / 8e12, 4),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -348,6 +374,7 @@ def main():
             "e2e": {"value": round(e2e_value, 3), "unit": "Gelem/s", "h2d_bytes_per_step": 4 * n,
                     "d2h_bytes_per_step": 12 * k, "ms_per_step": round(e2e_ms / args.e2e_steps, 3)},
             "stages_ms": stages,
+            "synchronous": synchronous,
             "gpu_launches": launches,
             "retries": int(sum(a - 1 for a in attempts if a > 0)),
             "aux_bytes": aux,
