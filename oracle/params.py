@@ -237,11 +237,17 @@ def params(N: int, k: int, eps: float, mode: int = MODE_DEFAULT):
     return S, t, M
 
 
-def uses_filter(N: int, k: int, S: int) -> bool:
-    """Route: sample-and-filter only when S <= N/8 and k <= N/64.
+def uses_filter(N: int, k: int, S: int, rows: int = 1) -> bool:
+    """Route: sample-and-filter only when S <= N/8 and k <= N/64, and, in calls
+    of 128 or more rows with k <= 2048, only when S < N/32.
 
     Otherwise sampling buys nothing (the corrected paper's Appendix B keeps the
     floor sample size once k/N exceeds about 2^-10, and a sample that is a
     sizable share of the input is itself a full pass); the exact path runs.
+    The rows clause is a choice of this implementation, not of the pages:
+    with many short rows, drawing 1/32 of every row by random access costs
+    more than an exact selection of each row by one CTA.
     """
-    return 8 * S <= N and 64 * k <= N
+    if 8 * S > N or 64 * k > N:
+        return False
+    return not (rows >= 128 and 32 * S >= N and k <= 2048)

@@ -95,10 +95,11 @@ def tie_path(x: np.ndarray, tau, k: int):
 
 
 def profk(x: np.ndarray, k: int, eps: float, seed: int, row: int = 0, *, max_attempts: int = 6,
-          mode: int = P.MODE_DEFAULT, tie_exit: bool = True, force=None):
+          mode: int = P.MODE_DEFAULT, tie_exit: bool = True, force=None, rows: int = 1):
     """One row of Prof-K.  ``force`` may override (S, t, M) as a dict; a forced
     S recomputes t and M from it (the corrected Algorithm 1, t and M steps) unless those are
-    forced as well.  Any override routes through sampling."""
+    forced as well.  Any override routes through sampling.  ``rows`` is the
+    number of rows of the call the row belongs to (it enters the route)."""
     x = np.asarray(x, dtype=np.float32)
     if np.isnan(x).any():
         raise ValueError("NaN in input")
@@ -111,7 +112,7 @@ def profk(x: np.ndarray, k: int, eps: float, seed: int, row: int = 0, *, max_att
             t, M = P.params_fast(N, k, S, eps)
         t, M = force.get("t", t), force.get("M", M)
     st.S, st.t, st.M = S, t, M
-    if not P.uses_filter(N, k, S) and not force:
+    if not P.uses_filter(N, k, S, rows) and not force:
         st.path = PATH_EXACT
         v, i = topk_sort(x, k)
         return v, i, st

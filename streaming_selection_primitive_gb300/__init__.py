@@ -119,8 +119,9 @@ def topk(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=None):
     return vals, idx, st.as_dict()
 
 
-def topk_batched(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=None):
-    """Exact top-k of each row of a 2-D float32 CUDA tensor (row stride x.stride(0))."""
+def topk_batched(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=None, stats: bool = True):
+    """Exact top-k of each row of a 2-D float32 CUDA tensor (row stride x.stride(0)).
+    Returns (values, indices, per-row stats dicts, or None when stats=False)."""
     torch = _torch()
     _need_cuda_f32(x)
     if x.dim() != 2 or x.stride(1) != 1:
@@ -131,12 +132,12 @@ def topk_batched(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=N
         idx = torch.empty((rows, k), dtype=torch.int64, device=x.device)
     else:
         vals, idx = out
-    sts = (ProfkStats * rows)()
+    sts = (ProfkStats * rows)() if stats else None
     code = lib().profk_topk_batched(x.data_ptr(), rows, n, x.stride(0), int(k), float(eps),
                                     int(seed) & (2**64 - 1), vals.data_ptr(), idx.data_ptr(),
                                     _stream_handle(stream, x.device), sts)
     _abi.check(code)
-    return vals, idx, [s.as_dict() for s in sts]
+    return vals, idx, ([s.as_dict() for s in sts] if stats else None)
 
 
 class Pending:

@@ -414,6 +414,11 @@ cudaError_t upload_rows(const Layout& L, void* ws, void* hbuf, int slot, const s
 void launch_exact(const Layout& L, void* ws, const float* x, int64_t ld, int nrows, const int* rows,
                   float* out_vals, int64_t* out_idx, cudaStream_t stream) {
   RowState* st = at<RowState>(ws, L.off_state);
+  const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (L.rows == 1 || (ld & 3) == 0);
+  if (aligned && rows_exact_suits(nrows, L.n, L.k)) {
+    launch_rows_exact(RowsExactArgs{x, ld, L.n, L.k, nrows, rows, st, out_vals, out_idx}, stream);
+    return;
+  }
   unsigned long long* sel = at<unsigned long long>(ws, L.off_sel);
   SelectArgs a{KeySource::Input, x, ld, L.n, nrows, rows, st};
   launch_select(a, static_cast<uint64_t>(L.k), false, 0, stream);
@@ -484,7 +489,7 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
                 at<uint32_t>(ws, L.off_blockcnt), at<uint32_t>(ws, L.off_sidx), at<uint32_t>(ws, L.off_skeys), false,
                 static_cast<unsigned long long>(P.t)};
   cudaError_t e = cudaSuccess;
-  if (sample_tau_fits(L.D, ng)) {
+  if (sample_tau_fits(L.D, ng, static_cast<uint64_t>(n))) {
     e = launch_sample_tau(sa, at<char>(ws, L.off_sctl), stream);
     if (e != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[1], stream);
@@ -555,7 +560,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   if (fM > 0) P.M = std::min<int64_t>(std::max<int64_t>(fM, k), n);
   if (forced && 2 * P.S > n) return PROFK_ERR_INVALID;
 
-  const bool sampling = forced ? true : uses_filter(n, k, P.S);
+  const bool sampling = forced ? true : uses_filter(n, k, P.S, rows);
   std::vector<profk_stats> st_host(static_cast<size_t>(rows));
   for (auto& s : st_host) fill_stats_params(&s, P);
 
@@ -865,7 +870,7 @@ int submit_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
                      g_opt[PROFK_OPT_FORCE_M].load() == 0 && g_opt[PROFK_OPT_TIMING].load() == 0 &&
                      g_opt[PROFK_OPT_MAX_ATTEMPTS].load() > 0 && t_user_ws == nullptr;
   const Params P = cached_params(n, k, eps / static_cast<double>(rows), mode);
-  if (!plain || !uses_filter(n, k, P.S)) {
+  if (!plain || !uses_filter(n, k, P.S, rows)) {
     // Options, routes and caller workspaces outside the asynchronous form:
     // the call runs now; profk_wait returns its result.
     call->status = run_topk(x, rows, n, ld, k, eps, seed, out_vals, out_idx, stream, call->stats.data());
@@ -1012,7 +1017,7 @@ int profk_set_workspace(void* dev_ptr, size_t bytes) {
 size_t profk_workspace_size(int64_t rows, int64_t n, int64_t k, double eps) {
   if (rows < 1 || n < 1 || k < 1 || k > n || !(eps > 0.0 && eps < 1.0)) return 0;
   const Params P = cached_params(n, k, eps / static_cast<double>(rows), static_cast<int>(g_opt[0].load()));
-  const bool sampling = uses_filter(n, k, P.S);
+  const bool sampling = uses_filter(n, k, P.S, rows);
   return make_layout(rows, n, k, P.S, sampling ? draw_budget(n, P.S) : 0, P.M, sampling).total;
 }
 
@@ -1068,8 +1073,15 @@ int profk_sample(const float* x, int64_t n, int64_t S, uint64_t seed, int64_t ro
       SampleArgs sa{x, n, static_cast<uint64_t>(n), S, D, L.log2H, seed, attempt, 1, nullptr, st,
                     at<unsigned long long>(c.ws, L.off_table), at<uint32_t>(c.ws, L.off_draws),
                     at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
-                    at<uint32_t>(c.ws, L.off_skeys)};
-      launch_sample_rows(sa, row, stream);
+                    at<uint32_t>(c.ws, L.off_skeys), false, 1ull, row};
+      // The main path's kernel where it takes the problem (it also finds a
+      // tau, of rank 1 here, which is not used), else the step-by-step one.
+      if (sample_tau_fits(D, 1, static_cast<uint64_t>(n))) {
+        PK_CHECK(cudaMemsetAsync(at<char>(c.ws, L.off_sctl), 0, sample_tau_ctl_bytes(), stream));
+        PK_CHECK(launch_sample_tau(sa, at<char>(c.ws, L.off_sctl), stream));
+      } else {
+        launch_sample_rows(sa, row, stream);
+      }
       PK_CHECK(cudaGetLastError());
       PK_CHECK(pinned(REPORT_BYTES, &hbuf));
       PK_CHECK(cudaMemcpyAsync(hbuf, st, REPORT_BYTES, cudaMemcpyDeviceToHost, stream));

@@ -86,6 +86,8 @@ struct SampleArgs {
   // launch_select(..., first_pass = 1).
   bool tau_pass1 = false;
   unsigned long long t = 0;
+  // launch_sample_tau: Philox key word 1 = storage row + key_row0.
+  int64_t key_row0 = 0;
 };
 void launch_sample(const SampleArgs& a, cudaStream_t stream);
 // Same, with Philox key word 1 = storage row + key_row0 (a single stored row
@@ -98,10 +100,30 @@ void launch_sample_rows(const SampleArgs& a, int64_t key_row0, cudaStream_t stre
 // are not used.
 size_t sample_tau_ctl_bytes();
 cudaError_t launch_sample_tau(const SampleArgs& a, void* ctl, cudaStream_t stream);
-// Whether each CTA of launch_sample_tau keeps all of its draws in registers
-// (true unless many rows share the SMs); otherwise the step-by-step kernels
-// (launch_sample with tau_pass1, then launch_select) are faster.
-bool sample_tau_fits(int64_t D, int nrows);
+// Whether launch_sample_tau takes these rows: each CTA's chunk of draws held
+// in registers (up to 1024 draws) or in shared memory (up to 49152, rows
+// shorter than 2^32); otherwise the step-by-step kernels (launch_sample with
+// tau_pass1, then launch_select).
+bool sample_tau_fits(int64_t D, int nrows, uint64_t n);
+
+// Exact top-k of short rows, one CTA per row (rows.cu): outputs of each listed
+// row (or rows 0 .. nrows-1) sorted, RowState::sel_nan set to the row's NaN
+// count.  Needs k <= rows_exact_max_k(), n < 2^32 and 16-byte aligned rows.
+struct RowsExactArgs {
+  const float* x;
+  int64_t ld;
+  int64_t n;
+  int64_t k;
+  int nrows;
+  const int* rows;
+  RowState* st;
+  float* out_vals;
+  int64_t* out_idx;
+};
+int64_t rows_exact_max_k();
+// Whether the one-CTA-per-row selection is expected to beat the multi-CTA one.
+bool rows_exact_suits(int64_t nrows, int64_t n, int64_t k);
+void launch_rows_exact(const RowsExactArgs& a, cudaStream_t stream);
 
 // Radix selection of the rank-th largest key per row.  init_rank > 0 resets the
 // state of each row first; otherwise the state is taken as it is (tie path).

@@ -201,6 +201,12 @@ Params compute_params(int64_t n, int64_t k, double eps, int mode) {
   return p;
 }
 
-bool uses_filter(int64_t n, int64_t k, int64_t S) { return 8 * S <= n && 64 * k <= n; }
+bool uses_filter(int64_t n, int64_t k, int64_t S, int64_t rows) {
+  if (8 * S > n || 64 * k > n) return false;
+  // Many short rows: a sample of 1/32 of each row or more, drawn by random
+  // access, costs more than selecting each row exactly inside one CTA.
+  if (rows >= 128 && 32 * S >= n && k <= 2048) return false;
+  return true;
+}
 
 }  // namespace profk

@@ -18,7 +18,8 @@ void exact_params(int64_t n, int64_t k, int64_t S, double eps, int64_t* t, int64
 // mode 0: default rule, mode 1: the older version's Algorithm 1 literally,
 // mode 2: S as in mode 0 with the exact t and M of Theorem 4.
 Params compute_params(int64_t n, int64_t k, double eps, int mode);
-// Sampling pays off only when S <= n/8 and k <= n/64; otherwise the exact path runs.
-bool uses_filter(int64_t n, int64_t k, int64_t S);
+// Sampling pays off only when S <= n/8 and k <= n/64, and, for calls of 128
+// or more rows with k <= 2048, only when S < n/32; otherwise the exact path runs.
+bool uses_filter(int64_t n, int64_t k, int64_t S, int64_t rows = 1);
 
 }  // namespace profk

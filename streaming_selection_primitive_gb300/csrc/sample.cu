@@ -332,6 +332,10 @@ constexpr int ST_WAIT_POLLS = 1 << 22;          // bound on one wait (a poll is 
 constexpr unsigned ST_ERR_WAIT = 8u;            // RowState::error bit of a wait that ran out
 constexpr unsigned long long CNT_READY = 1ull << 63;
 constexpr int TAU_GATHER = ST_THREADS;  // a tau bucket this small is finished by one CTA
+constexpr int ST_QB = 2;                // wide form: quads per thread in flight
+constexpr int ST_WIDE_ROUNDS = 24;      // wide form: at most this many rounds of 512 quads
+constexpr int64_t ST_WIDE_MAX = static_cast<int64_t>(ST_WIDE_ROUNDS) * 4 * ST_THREADS;  // draws per chunk
+constexpr uint32_t NOT_FIRST = 0xffffffffu;  // a repeated draw (values are below n < 2^32)
 
 }  // namespace
 
@@ -409,6 +413,24 @@ __device__ __forceinline__ unsigned long long st_excl_scan(unsigned long long v,
   return r;
 }
 
+// Draws 4q .. 4q + 3 of a row's stream, all four words of one Philox block
+// (the same values as draw_value; a word that Lemire rejects takes the
+// replacement path, out of line since it is rare).
+__device__ __noinline__ uint32_t draw_value_slow(const SampleArgs& a, int row, uint64_t key_row, int64_t i) {
+  return draw_value(a, row, key_row, i);
+}
+
+__device__ __forceinline__ void draw_quad(const SampleArgs& a, int row, uint64_t key_row, int64_t q,
+                                          uint32_t (&u)[4]) {
+  uint64_t w[4] = {static_cast<uint64_t>(q), static_cast<uint64_t>(a.attempt), 0ull, 0ull};
+  philox4x64_10(w, a.seed, key_row);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    uint64_t v;
+    u[e] = lemire64(w[e], a.n, &v) ? static_cast<uint32_t>(v) : draw_value_slow(a, row, key_row, 4 * q + e);
+  }
+}
+
 __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, SampleCtl* ctl) {
   pdl_trigger();
   pdl_wait();
@@ -419,71 +441,153 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   __shared__ unsigned long long s_above, s_count, s_base;
   __shared__ uint32_t s_list[TAU_GATHER];
   __shared__ uint32_t s_tau;
+  __shared__ unsigned s_wcnt[ST_WIDE_ROUNDS * (ST_THREADS / 32)];
+  extern __shared__ uint4 st_dyn[];
   const int row = launch_row(a.rows);
   RowState& S = a.st[row];
   SampleCtl& c = ctl[row];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) s_err = 0;
   const int64_t G = gridDim.x, chunk = blockIdx.x;
   const int64_t Dc = (((a.D + G - 1) / G) + 31) & ~int64_t(31);
   const int64_t lo = chunk * Dc < a.D ? chunk * Dc : a.D;
   const int64_t hi = lo + Dc < a.D ? lo + Dc : a.D;
-  const int rounds = static_cast<int>((hi - lo + ST_THREADS - 1) / ST_THREADS);
   unsigned long long* table = a.table + (static_cast<int64_t>(row) << a.log2H);
+  const float* xr = a.x + static_cast<int64_t>(row) * a.ld;
+  const int64_t orow = static_cast<int64_t>(row) * a.S;
+  const uint64_t key_row = static_cast<uint64_t>(row + a.key_row0);
   unsigned target = 0;
+  // Held form: at most ST_HELD draws per thread, kept in registers.  Wide
+  // form (launched with dynamic shared memory): the chunk's draws in quads,
+  // thread t taking quads t, t + 512, ...; per quad one 16-byte shared-memory
+  // entry that holds in turn the four draws' table slots, their values (or
+  // NOT_FIRST), then the members' keys, and four membership bits.
+  const bool wide = hi - lo > static_cast<int64_t>(ST_HELD) * ST_THREADS;
+  const int nq = static_cast<int>((hi - lo + 3) / 4);
+  const int nm = (nq + ST_THREADS - 1) / ST_THREADS;  // rounds of quads
+  uint4* W4 = st_dyn;
+  unsigned* mbits = reinterpret_cast<unsigned*>(st_dyn + Dc / 4);
 
   // a. Draw and insert.
-  // Rounds j < ST_HELD keep their draws (and later keys) in registers; the
-  // loops over them are unrolled so that the arrays stay there.
-  // Their values are gathered at once (used only if the draw is a member),
-  // so that the gather's latency overlaps the insertions.
-  // Both rounds' loads and home-slot swaps are issued before any result is
-  // waited for.
   uint32_t uh[ST_HELD] = {0u, 0u};
   float vh[ST_HELD] = {0.f, 0.f};
-  unsigned long long ph[ST_HELD] = {EMPTY_SLOT, EMPTY_SLOT};
   uint64_t sh[ST_HELD] = {0, 0};  // the slot that holds each held draw's value
+  if (!wide) {
+    // Both draws' value loads and home-slot swaps are issued before any
+    // result is waited for (the values are used only if the draw is a
+    // member, so the gather's latency overlaps the insertions).
+    unsigned long long ph[ST_HELD] = {EMPTY_SLOT, EMPTY_SLOT};
 #pragma unroll
-  for (int j = 0; j < ST_HELD; ++j) {
-    const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
-    if (j < rounds && i < hi) uh[j] = draw_value(a, row, static_cast<uint64_t>(row), i);
-  }
-#pragma unroll
-  for (int j = 0; j < ST_HELD; ++j) {
-    const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
-    if (j < rounds && i < hi) {
-      vh[j] = a.x[static_cast<int64_t>(row) * a.ld + uh[j]];
-      ph[j] = table_try_home(table, a.log2H, uh[j], i);
+    for (int j = 0; j < ST_HELD; ++j) {
+      const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
+      if (i < hi) uh[j] = draw_value(a, row, key_row, i);
     }
-  }
 #pragma unroll
-  for (int j = 0; j < ST_HELD; ++j) {
-    const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
-    if (j < rounds && i < hi) sh[j] = table_finish(a, row, table, uh[j], i, ph[j]);
-  }
-  for (int j = ST_HELD; j < rounds; ++j) {
-    const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
-    if (i < hi) table_insert(a, row, table, draw_value(a, row, static_cast<uint64_t>(row), i), i);
+    for (int j = 0; j < ST_HELD; ++j) {
+      const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
+      if (i < hi) {
+        vh[j] = xr[uh[j]];
+        ph[j] = table_try_home(table, a.log2H, uh[j], i);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < ST_HELD; ++j) {
+      const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
+      if (i < hi) sh[j] = table_finish(a, row, table, uh[j], i, ph[j]);
+    }
+  } else {
+    for (int w = tid; w < Dc / 32; w += ST_THREADS) mbits[w] = 0u;
+    // ST_QB rounds at a time: 4 x ST_QB swaps in flight per thread.
+    for (int m0 = 0; m0 < nm; m0 += ST_QB) {
+      uint32_t u[ST_QB][4];
+      unsigned long long p[ST_QB][4];
+#pragma unroll
+      for (int b = 0; b < ST_QB; ++b) {
+        const int q = tid + (m0 + b) * ST_THREADS;
+        if (q < nq) draw_quad(a, row, key_row, lo / 4 + q, u[b]);
+      }
+#pragma unroll
+      for (int b = 0; b < ST_QB; ++b) {
+        const int q = tid + (m0 + b) * ST_THREADS;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int64_t i = lo + 4 * static_cast<int64_t>(q) + e;
+          if (q < nq && i < hi) p[b][e] = table_try_home(table, a.log2H, u[b][e], i);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < ST_QB; ++b) {
+        const int q = tid + (m0 + b) * ST_THREADS;
+        if (q < nq) {
+          uint32_t s[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int64_t i = lo + 4 * static_cast<int64_t>(q) + e;
+            if (i < hi) s[e] = static_cast<uint32_t>(table_finish(a, row, table, u[b][e], i, p[b][e]));
+          }
+          W4[q] = make_uint4(s[0], s[1], s[2], s[3]);
+        }
+      }
+    }
   }
   st_grid_sync(&c.bar, target += static_cast<unsigned>(G), &s_err);
 
-  // b. First occurrences, their count and their place in draw order.
+  // b. First occurrences (the table is complete: a slot's draw is the
+  // smallest draw of its value), their count and their place in draw order.
   bool first_h[ST_HELD] = {false, false};
   unsigned long long cnt = 0;
+  if (!wide) {
 #pragma unroll
-  for (int j = 0; j < ST_HELD; ++j) {
-    if (j < rounds) {
+    for (int j = 0; j < ST_HELD; ++j) {
       const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
-      // The table is complete: the slot's draw is the smallest draw of u.
       first_h[j] = i < hi && static_cast<uint32_t>(__ldcg(table + sh[j])) == static_cast<uint32_t>(i);
       cnt += __syncthreads_count(first_h[j]);
     }
-  }
-  for (int j = ST_HELD; j < rounds; ++j) {
-    const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
-    const bool f = i < hi && first_position(table, a.log2H, draw_value(a, row, static_cast<uint64_t>(row), i)) ==
-                                 static_cast<uint32_t>(i);
-    cnt += __syncthreads_count(f);
+  } else {
+    // Per quad: the four slots' entries (loaded ST_QB quads at a time); the
+    // entry carries the value, so the quad's entry becomes the values of its
+    // first occurrences.  Per (round, warp): the count of first occurrences.
+    for (int m0 = 0; m0 < nm; m0 += ST_QB) {
+      unsigned long long ent[ST_QB][4];
+#pragma unroll
+      for (int b = 0; b < ST_QB; ++b) {
+        const int q = tid + (m0 + b) * ST_THREADS;
+        if (q < nq) {
+          const uint4 s = W4[q];
+          const uint32_t sl[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            ent[b][e] = lo + 4 * static_cast<int64_t>(q) + e < hi ? __ldcg(table + sl[e]) : 0ull;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < ST_QB; ++b) {
+        if (m0 + b >= nm) break;  // uniform across the block
+        const int q = tid + (m0 + b) * ST_THREADS;
+        uint32_t o[4] = {NOT_FIRST, NOT_FIRST, NOT_FIRST, NOT_FIRST};
+        unsigned f = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int64_t i = lo + 4 * static_cast<int64_t>(q) + e;
+          if (q < nq && i < hi && static_cast<uint32_t>(ent[b][e]) == static_cast<uint32_t>(i)) {
+            o[e] = static_cast<uint32_t>(ent[b][e] >> 32);
+            ++f;
+          }
+        }
+        if (q < nq) W4[q] = make_uint4(o[0], o[1], o[2], o[3]);
+        const unsigned wsum = __reduce_add_sync(FULL_MASK, f);
+        if (lane == 0) s_wcnt[(m0 + b) * (ST_THREADS / 32) + warp] = wsum;
+      }
+    }
+    __syncthreads();
+    // Exclusive prefix over (round, warp) in draw order; the total is the
+    // chunk's count.
+    const int E = nm * (ST_THREADS / 32);
+    const unsigned v = tid < E ? s_wcnt[tid] : 0u;
+    unsigned long long tot;
+    const unsigned long long ex = st_excl_scan(v, sw, &tot);
+    if (tid < E) s_wcnt[tid] = static_cast<unsigned>(ex);
+    cnt = tot;
   }
   if (tid == 0) st_st_relaxed(&c.count[chunk], CNT_READY | cnt);
   {
@@ -501,7 +605,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
       before = v & ~CNT_READY;
     }
     for (int o = 16; o >= 1; o >>= 1) before += __shfl_xor_sync(FULL_MASK, before, o);
-    if ((tid & 31) == 0) sw[tid >> 5] = before;
+    if (lane == 0) sw[warp] = before;
     __syncthreads();
     if (tid == 0) {
       unsigned long long b = 0;
@@ -511,47 +615,110 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     }
     __syncthreads();
   }
-  // Sample members: keys kept for the held rounds; all are stored.
+  // Sample members (first occurrences of rank < S): indices and keys stored;
+  // the keys also kept (registers, or the quad's shared-memory entry).
   uint32_t kh[ST_HELD] = {0u, 0u};
   bool mh[ST_HELD] = {false, false};
-  unsigned long long run = s_base;
+  const unsigned long long Su = static_cast<unsigned long long>(a.S);
+  if (!wide) {
+    unsigned long long run = s_base;
 #pragma unroll
-  for (int j = 0; j < ST_HELD; ++j) {
-    if (j < rounds) {
+    for (int j = 0; j < ST_HELD; ++j) {
       unsigned long long tot;
       const unsigned long long rank = run + st_excl_scan(first_h[j] ? 1ull : 0ull, sw, &tot);
       run += tot;
-      if (first_h[j] && rank < static_cast<unsigned long long>(a.S)) {
-        const int64_t o = static_cast<int64_t>(row) * a.S + static_cast<int64_t>(rank);
+      if (first_h[j] && rank < Su) {
+        const int64_t o = orow + static_cast<int64_t>(rank);
         kh[j] = ord_key(vh[j]);
         mh[j] = true;
         a.sidx[o] = uh[j];
         a.skeys[o] = kh[j];
       }
     }
-  }
-  for (int j = ST_HELD; j < rounds; ++j) {
-    const int64_t i = lo + static_cast<int64_t>(j) * ST_THREADS + tid;
-    uint32_t u = 0;
-    bool f = false;
-    if (i < hi) {
-      u = draw_value(a, row, static_cast<uint64_t>(row), i);
-      f = first_position(table, a.log2H, u) == static_cast<uint32_t>(i);
+  } else {
+    // A quad's first rank: the chunk's base, the (round, warp) prefix and the
+    // first occurrences of the warp's earlier lanes; values gathered ST_QB
+    // quads at a time.
+    for (int m0 = 0; m0 < nm; m0 += ST_QB) {
+      uint32_t uq[ST_QB][4];
+      float v[ST_QB][4];
+      unsigned long long r0[ST_QB];
+      unsigned fl[ST_QB];
+#pragma unroll
+      for (int b = 0; b < ST_QB; ++b) {
+        fl[b] = 0u;
+        r0[b] = 0ull;
+        if (m0 + b >= nm) break;  // uniform across the block
+        const int q = tid + (m0 + b) * ST_THREADS;
+        const uint4 e4 = q < nq ? W4[q] : make_uint4(NOT_FIRST, NOT_FIRST, NOT_FIRST, NOT_FIRST);
+        uq[b][0] = e4.x;
+        uq[b][1] = e4.y;
+        uq[b][2] = e4.z;
+        uq[b][3] = e4.w;
+        unsigned f = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f |= (uq[b][e] != NOT_FIRST ? 1u : 0u) << e;
+        const unsigned cq = __popc(f);
+        unsigned incl = cq;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
+          if (lane >= o) incl += t;
+        }
+        r0[b] = s_base + s_wcnt[(m0 + b) * (ST_THREADS / 32) + warp] + (incl - cq);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool mem = ((f >> e) & 1u) && r0[b] + __popc(f & ((1u << e) - 1u)) < Su;
+          if (mem) {
+            fl[b] |= 1u << e;
+            v[b][e] = xr[uq[b][e]];
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < ST_QB; ++b) {
+        if (fl[b] == 0u) continue;
+        const int q = tid + (m0 + b) * ST_THREADS;
+        unsigned long long r = r0[b];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if ((fl[b] >> e) & 1u) {
+            const uint32_t key = ord_key(v[b][e]);
+            a.sidx[orow + static_cast<int64_t>(r)] = uq[b][e];
+            a.skeys[orow + static_cast<int64_t>(r)] = key;
+            uq[b][e] = key;
+            ++r;
+          }
+        }
+        W4[q] = make_uint4(uq[b][0], uq[b][1], uq[b][2], uq[b][3]);
+        atomicOr(&mbits[q >> 3], fl[b] << ((q & 7) * 4));
+      }
     }
-    unsigned long long tot;
-    const unsigned long long rank = run + st_excl_scan(f ? 1ull : 0ull, sw, &tot);
-    run += tot;
-    if (f && rank < static_cast<unsigned long long>(a.S)) {
-      const int64_t o = static_cast<int64_t>(row) * a.S + static_cast<int64_t>(rank);
-      a.sidx[o] = u;
-      a.skeys[o] = ord_key(a.x[static_cast<int64_t>(row) * a.ld + u]);
-    }
   }
-  // The chunk's members are the sample ranks [m0, m1).
-  const int64_t m0 = s_base < static_cast<unsigned long long>(a.S) ? static_cast<int64_t>(s_base) : a.S;
-  const int64_t m1 = s_base + cnt < static_cast<unsigned long long>(a.S) ? static_cast<int64_t>(s_base + cnt) : a.S;
-  const bool held = rounds <= ST_HELD;
   __syncthreads();
+
+  // Every member key of this CTA through fn(key, is_member) on every thread,
+  // the same number of times (fn may be warp-collective).
+  auto each_key = [&](auto&& fn) {
+    if (!wide) {
+#pragma unroll
+      for (int j = 0; j < ST_HELD; ++j) fn(kh[j], mh[j]);
+    } else {
+      for (int m = 0; m < nm; ++m) {
+        const int q = tid + m * ST_THREADS;
+        uint4 k4 = make_uint4(0u, 0u, 0u, 0u);
+        unsigned f = 0u;
+        if (q < nq) {
+          k4 = W4[q];
+          f = (mbits[q >> 3] >> ((q & 7) * 4)) & 15u;
+        }
+        fn(k4.x, (f & 1u) != 0u);
+        fn(k4.y, (f & 2u) != 0u);
+        fn(k4.z, (f & 4u) != 0u);
+        fn(k4.w, (f & 8u) != 0u);
+      }
+    }
+  };
 
   // c. tau: the t-th largest sample key.
   unsigned long long prefix = 0, want = a.t;
@@ -563,21 +730,10 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     const unsigned nb = 1u << width;
     for (unsigned b = tid; b < nb; b += ST_THREADS) h[b] = 0;
     __syncthreads();
-    if (held) {
-#pragma unroll
-      for (int j = 0; j < ST_HELD; ++j) {
-        const bool m = mh[j] && (bits == 0 || (static_cast<unsigned long long>(kh[j]) >> (shift + width)) == prefix);
-        hist_add(h, (kh[j] >> shift) & (nb - 1), m);
-      }
-    } else {
-      for (int64_t r0 = m0; r0 < m0 + (((m1 - m0) + 31) & ~int64_t(31)); r0 += ST_THREADS) {
-        const int64_t r = r0 + tid;
-        const bool v = r < m1;
-        const uint32_t key = v ? __ldcg(a.skeys + static_cast<int64_t>(row) * a.S + r) : 0u;
-        const bool m = v && (bits == 0 || (static_cast<unsigned long long>(key) >> (shift + width)) == prefix);
-        hist_add(h, (key >> shift) & (nb - 1), m);
-      }
-    }
+    each_key([&](uint32_t key, bool mem) {
+      const bool m = mem && (bits == 0 || (static_cast<unsigned long long>(key) >> (shift + width)) == prefix);
+      hist_add(h, (key >> shift) & (nb - 1), m);
+    });
     __syncthreads();
     for (unsigned b = tid; b < nb; b += ST_THREADS)
       if (h[b]) atomicAdd(&c.hist[p][b], h[b]);
@@ -622,19 +778,12 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     __syncthreads();
     if (p < 2 && bucket_n <= TAU_GATHER) {
       // The bucket's sample keys go to one list; the first CTA ranks them.
-      auto put = [&](uint32_t key) {
-        if ((static_cast<unsigned long long>(key) >> (32 - bits)) == prefix) {
+      each_key([&](uint32_t key, bool mem) {
+        if (mem && (static_cast<unsigned long long>(key) >> (32 - bits)) == prefix) {
           const unsigned pos = atomicAdd(&c.bucket_n, 1u);
           if (pos < TAU_GATHER) c.bucket[pos] = key;
         }
-      };
-      if (held) {
-#pragma unroll
-        for (int j = 0; j < ST_HELD; ++j)
-          if (mh[j]) put(kh[j]);
-      } else {
-        for (int64_t r = m0 + tid; r < m1; r += ST_THREADS) put(__ldcg(a.skeys + static_cast<int64_t>(row) * a.S + r));
-      }
+      });
       st_grid_sync(&c.bar, target += static_cast<unsigned>(G), &s_err);
       if (chunk == 0) {
         const int nl = static_cast<int>(bucket_n);
@@ -693,18 +842,35 @@ int64_t sample_tau_chunks(int64_t D, int nrows) {
   if (G > 256) G = 256;
   return G < 1 ? 1 : G;
 }
+
+// Dynamic shared memory of the wide form: a 16-byte entry per quad and four
+// membership bits per quad.
+size_t sample_tau_wide_smem(int64_t Dc) { return static_cast<size_t>(Dc) * 4 + static_cast<size_t>(Dc) / 8; }
+
+int64_t sample_tau_chunk_len(int64_t D, int nrows) {
+  const int64_t G = sample_tau_chunks(D, nrows);
+  return (((D + G - 1) / G) + 31) & ~int64_t(31);
+}
 }  // namespace
 
-bool sample_tau_fits(int64_t D, int nrows) {
-  const int64_t G = sample_tau_chunks(D, nrows);
-  const int64_t Dc = (((D + G - 1) / G) + 31) & ~int64_t(31);
-  return Dc <= static_cast<int64_t>(ST_HELD) * ST_THREADS;
+bool sample_tau_fits(int64_t D, int nrows, uint64_t n) {
+  const int64_t Dc = sample_tau_chunk_len(D, nrows);
+  if (Dc <= static_cast<int64_t>(ST_HELD) * ST_THREADS) return true;
+  return Dc <= ST_WIDE_MAX && n < (1ull << 32);
 }
 
 cudaError_t launch_sample_tau(const SampleArgs& a, void* ctl, cudaStream_t stream) {
   const int64_t G = sample_tau_chunks(a.D, a.nrows);
-  launch_kernel(k_sample_tau, dim3(static_cast<unsigned>(G), static_cast<unsigned>(a.nrows)), ST_THREADS, 0, stream,
-                a, static_cast<SampleCtl*>(ctl));
+  const int64_t Dc = sample_tau_chunk_len(a.D, a.nrows);
+  size_t smem = 0;
+  if (Dc > static_cast<int64_t>(ST_HELD) * ST_THREADS) {
+    if (Dc > ST_WIDE_MAX || a.n >= (1ull << 32)) return cudaErrorInvalidValue;
+    smem = sample_tau_wide_smem(Dc);
+    cudaFuncSetAttribute(k_sample_tau, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(sample_tau_wide_smem(ST_WIDE_MAX)));
+  }
+  launch_kernel(k_sample_tau, dim3(static_cast<unsigned>(G), static_cast<unsigned>(a.nrows)), ST_THREADS, smem,
+                stream, a, static_cast<SampleCtl*>(ctl));
   return cudaGetLastError();
 }
 

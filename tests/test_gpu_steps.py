@@ -17,7 +17,9 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("n,S,seed,row,attempt", [
     (1 << 22, 32768, 1, 0, 0), (1 << 22, 32768, 2, 5, 3), (1000003, 4099, 77, 1, 0), (64, 32, 9, 0, 0),
-    (1 << 30, 105985, 3, 0, 0), (3 * (1 << 20) + 17, 131072, 4, 2, 1)])
+    (1 << 30, 105985, 3, 0, 0), (3 * (1 << 20) + 17, 131072, 4, 2, 1),
+    # more than 1024 draws per CTA (the draws held in shared memory), many repeats
+    (1 << 24, 400_000, 5, 3, 2), (1 << 20, 1 << 19, 6, 0, 0), ((1 << 21) + 5, 300_001, 7, 1, 4)])
 def test_sample_matches_oracle(pk, cuda_device, n, S, seed, row, attempt):
     x = workloads.uniform(n, seed, cuda_device)
     sidx, svals = pk.sample(x, S, seed, row, attempt)
@@ -102,7 +104,9 @@ def test_refine_matches_oracle(pk, cuda_device, n, k):
 
 
 @pytest.mark.parametrize("n,k", [(1, 1), (5, 5), (1000, 1), (1000, 1000), (65537, 9000), (1 << 20, 17),
-                                 ((1 << 20) + 3, 1 << 15)])
+                                 ((1 << 20) + 3, 1 << 15),
+                                 # one CTA per row: placed by counting (k <= 512) or sorted, ragged tails
+                                 (1 << 16, 512), ((1 << 17) + 2, 513), (65537, 2048), (200_003, 100)])
 @pytest.mark.parametrize("kind", ["normal", "levels16", "specials"])
 def test_exact_matches_oracle(pk, cuda_device, n, k, kind):
     if kind == "specials":

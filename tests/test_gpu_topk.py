@@ -9,6 +9,7 @@ import torch
 
 import workloads
 from gpu_helpers import assert_same
+from oracle import params as PP
 from oracle import profk as PK
 from oracle.topk import topk_sort
 
@@ -134,7 +135,11 @@ def test_nondefault_stream(pk, cuda_device):
 
 @pytest.mark.parametrize("rows,n,ld,k", [(4, 1 << 20, 1 << 20, 16), (3, 1_000_003, 1_000_008, 100),
                                          (16, 1 << 18, 1 << 18, 1), (2, 5000, 5000, 5000),
-                                         (3, 1 << 22, 1 << 22, 10_000)])
+                                         (3, 1 << 22, 1 << 22, 10_000),
+                                         # several chunks of more than 1024 draws per row
+                                         (24, 1 << 20, 1 << 20, 64), (40, 1 << 19, (1 << 19) + 4, 5),
+                                         # exact routing, one CTA per row (several rows per CTA for 700)
+                                         (64, 1 << 16, (1 << 16) + 4, 1000), (700, 20_000, 20_004, 64)])
 def test_batched(pk, cuda_device, rows, n, ld, k):
     base = workloads.normal_rows(rows, ld, rows + n, cuda_device)
     x = base[:, :n]
@@ -142,9 +147,12 @@ def test_batched(pk, cuda_device, rows, n, ld, k):
     h = x.cpu().numpy()
     eps_row = 1e-3 / rows
     for r in range(rows):
-        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, eps_row, 11, row=r)
+        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, eps_row, 11, row=r, rows=rows)
         assert_same(vals[r], idx[r], ov, oi, f"batched row {r}")
         assert sts[r]["path"] == ost.path and sts[r]["R_first"] == ost.R_first
+        assert sts[r]["R_gt_first"] == ost.R_gt_first
+        if ost.taus:
+            assert sts[r]["tau_first"] == ost.taus[0]
 
 
 def test_batched_rows_retry_alone(pk, cuda_device):
@@ -157,7 +165,7 @@ def test_batched_rows_retry_alone(pk, cuda_device):
     vals, idx, sts = pk.topk_batched(x, k, 1e-3, 5)
     h = x.cpu().numpy()
     for r in range(rows):
-        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 5, row=r, force=force)
+        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 5, row=r, force=force, rows=rows)
         assert_same(vals[r], idx[r], ov, oi, f"row {r}")
         assert (sts[r]["attempts"], sts[r]["path"], sts[r]["R_first"]) == (ost.attempts, ost.path, ost.R_first)
 
@@ -179,6 +187,42 @@ def test_large_k_fallback(pk, cuda_device):
     assert st["path"] == pk.PATH_FALLBACK
 
 
+def test_batched_wide_sampler_rows_retry_alone(pk, cuda_device):
+    # 32 rows share the SMs, so each row's CTAs hold thousands of draws; about
+    # half the rows overflow each attempt and redraw alone.
+    rows, n, k = 32, 1 << 20, 1
+    x = workloads.normal_rows(rows, n, 41, cuda_device)
+    force = {"S": 32768, "t": 1, "M": 22}
+    for o, v in ((pk.OPT_FORCE_S, 32768), (pk.OPT_FORCE_T, 1), (pk.OPT_FORCE_M, 22)):
+        pk.set_option(o, v)
+    vals, idx, sts = pk.topk_batched(x, k, 1e-3, 8)
+    h = x.cpu().numpy()
+    retried = 0
+    for r in range(rows):
+        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 8, row=r, force=force, rows=rows)
+        assert_same(vals[r], idx[r], ov, oi, f"row {r}")
+        assert (sts[r]["attempts"], sts[r]["path"], sts[r]["R_first"], sts[r]["tau_first"]) == \
+            (ost.attempts, ost.path, ost.R_first, ost.taus[0])
+        retried += sts[r]["attempts"] > 1
+    assert retried > 0
+
+
+def test_batched_fallback_rows(pk, cuda_device):
+    # tau = the sample minimum overflows the buffer on every attempt: all rows
+    # take the exact fallback (one CTA per row at this size), some rows tied.
+    rows, n, k = 40, 1 << 17, 100
+    x = workloads.normal_rows(rows, n, 63, cuda_device)
+    x[3] = torch.round(x[3] * 4) / 4
+    force = {"S": 4096, "t": 4096, "M": 100}
+    for o, v in ((pk.OPT_FORCE_S, 4096), (pk.OPT_FORCE_T, 4096), (pk.OPT_FORCE_M, 100), (pk.OPT_MAX_ATTEMPTS, 2)):
+        pk.set_option(o, v)
+    vals, idx, sts = pk.topk_batched(x, k, 1e-3, 2)
+    h = x.cpu().numpy()
+    for r in range(rows):
+        assert_same(vals[r], idx[r], *topk_sort(h[r], k), f"row {r}")
+        assert sts[r]["path"] == pk.PATH_FALLBACK and sts[r]["attempts"] == 2
+
+
 def test_batched_large_k_rows_retry_alone(pk, cuda_device):
     # About half the rows fail each attempt, so the radix sort runs on row lists.
     rows, n, k = 4, 1 << 20, 9000
@@ -189,7 +233,7 @@ def test_batched_large_k_rows_retry_alone(pk, cuda_device):
     vals, idx, sts = pk.topk_batched(x, k, 1e-3, 6)
     h = x.cpu().numpy()
     for r in range(rows):
-        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 6, row=r, force=force)
+        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 6, row=r, force=force, rows=rows)
         assert_same(vals[r], idx[r], ov, oi, f"row {r}")
         assert (sts[r]["attempts"], sts[r]["path"], sts[r]["R_first"]) == (ost.attempts, ost.path, ost.R_first)
 
@@ -220,10 +264,12 @@ def test_caller_workspace(pk, cuda_device):
     assert torch.equal(again[1], ref[1])
 
 
-@pytest.mark.parametrize("rows,n,k", [(1024, 1 << 16, 16), (256, 1 << 20, 32), (512, (1 << 18) + 4, 100)])
+@pytest.mark.parametrize("rows,n,k", [(1024, 1 << 16, 16), (256, 1 << 20, 32), (512, (1 << 18) + 4, 100),
+                                      (128, 1 << 21, 32), (160, (1 << 20) + 8, 2049)])
 def test_batched_many_rows(pk, cuda_device, rows, n, k):
-    """Many rows sharing the SMs (one CTA per row in the persistent kernels,
-    the step-by-step sampler; exact routing for the 2^16 rows)."""
+    """Many rows sharing the SMs: exact routing (one CTA per row) for rows
+    whose sample would be 1/32 of the row or more, else the filter path with
+    one sampler CTA per row."""
     x = workloads.normal_rows(rows, n, rows + k, cuda_device)
     vals, idx, sts = pk.topk_batched(x, k, 1e-3, 21)
     rng = np.random.default_rng(rows)
@@ -231,7 +277,8 @@ def test_batched_many_rows(pk, cuda_device, rows, n, k):
         h = x[r].cpu().numpy()
         assert_same(vals[r], idx[r], *topk_sort(h, k), f"row {r}")
     paths = {s["path"] for s in sts}
-    assert paths == ({pk.PATH_EXACT} if n == 1 << 16 else {pk.PATH_FILTER}) or pk.PATH_FALLBACK not in paths
+    S = sts[0]["S"]
+    assert paths == ({pk.PATH_FILTER} if PP.uses_filter(n, k, S, rows) else {pk.PATH_EXACT})
 
 
 def test_exact_parameter_mode(pk, cuda_device):

@@ -153,3 +153,15 @@ def test_default_rule_invariants():
             assert 32768 <= S <= 131072 and 1 <= t <= S and k <= M <= N
             if P.uses_filter(N, k, S):
                 assert P.prob_fail(N, k, S, t, M) <= 1e-3
+
+
+def test_route():
+    # The pages' clauses: a sample of more than 1/8 of the row, or k above
+    # 1/64 of it, takes the exact path.
+    assert P.uses_filter(2**20, 64, 32768) and P.uses_filter(2**18, 64, 32768)
+    assert not P.uses_filter(2**18 - 1, 64, 32768) and not P.uses_filter(2**20, 2**14 + 1, 32768)
+    # Calls of 128 or more rows with k <= 2048: only samples below 1/32 of a row.
+    assert P.uses_filter(2**20, 64, 32768, rows=127) and not P.uses_filter(2**20, 64, 32768, rows=128)
+    assert P.uses_filter(2**20 + 4, 2048, 32768, rows=1024) and not P.uses_filter(2**20, 2048, 32768, rows=1024)
+    assert P.uses_filter(2**20, 2049, 32768, rows=1024)
+    assert P.uses_filter(2**24, 32, 32768, rows=64) and P.uses_filter(2**24, 32, 32768, rows=4096)
