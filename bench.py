@@ -353,6 +353,28 @@ def main():
             if gen != "normal":
                 del xs
                 torch.cuda.empty_cache()
+        # The corrected paper's own sample-size rule (Proposition 7 with the
+        # GB300 cost ratio) on the same normal input, beside the default rule.
+        pk.set_option(pk.OPT_PARAM_MODE, pk.PARAMS_CORRECTED)
+        try:
+            for kk in (32, 1024, 1 << 19):
+                o2 = (torch.empty(kk, dtype=torch.float32, device=dev), torch.empty(kk, dtype=torch.int64, device=dev))
+                for w in range(2):
+                    pk.topk(x, kk, EPS, 40_000 + w, out=o2)
+                torch.cuda.synchronize()
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 5
+                a0.record(stream)
+                for p in [pk.topk_async(x, kk, EPS, 50_000 + s, out=o2) for s in range(reps)]:
+                    p.wait()
+                a1.record(stream)
+                torch.cuda.synchronize()
+                ms = a0.elapsed_time(a1) / reps
+                sweep[f"normal_k{kk}_corrected_rule"] = {
+                    "S": pk.params(n, kk, EPS, pk.PARAMS_CORRECTED)[0], "ms": round(ms, 4),
+                    "gelem_s": round(n / ms / 1e6, 2), "hbm_frac_of_8TBs": round(4 * n / (ms / 1e3) / 8e12, 3)}
+        finally:
+            pk.set_option(pk.OPT_PARAM_MODE, pk.PARAMS_DEFAULT)
 
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu and args.gpus == 1:

@@ -154,10 +154,21 @@ int profk_wait(profk_call* call, profk_stats* stats /* array[rows] or NULL */);
  *     split eps/2 + eps/2: t - 1 is the (1 - eps/2)-quantile of the
  *     hypergeometric count of the top k - 1 in the sample, M the smallest M
  *     with Pr(at most t - 1 of the top M are sampled) <= eps/2.
+ *   mode PROFK_PARAMS_CORRECTED: the corrected Algorithm 1 throughout: S
+ *     from its sample-size steps (Proposition 7, Appendix E.1),
+ *     S = clip(floor(max(S1, S2)), 2^14, 2^18) with
+ *     S1 = (z/r)^(2/3) (k n)^(1/3), S2 = ((z^2 + 1/2) n / r)^(1/2),
+ *     z = Phi^{-1}(1-eps/2); S = 2^14 when r is infinite or k/n > 2^-10;
+ *     then S <= n/128.  The cost ratio r(k) has the paper's form
+ *     1/r = a log2(k) + b for k > 2^7 (infinite below), with a = 0.0033 and
+ *     b = 0.41 fitted on a GB300 by the paper's procedure
+ *     (streaming_selection_primitive_gb300/calibrate.py).  t and M as in
+ *     the default mode.
  * Pure host arithmetic (fp64), no device work. */
 #define PROFK_PARAMS_DEFAULT 0
 #define PROFK_PARAMS_OLD 1
 #define PROFK_PARAMS_EXACT 2
+#define PROFK_PARAMS_CORRECTED 3
 int profk_params(int64_t n, int64_t k, double eps, int mode,
                  int64_t* S, int64_t* t, int64_t* M);
 
@@ -178,7 +189,7 @@ int profk_set_workspace(void* dev_ptr, size_t bytes);
 
 /* Process-wide options (defaults in brackets). */
 typedef enum profk_option {
-  PROFK_OPT_PARAM_MODE = 0,    /* PROFK_PARAMS_DEFAULT [0], PROFK_PARAMS_OLD or PROFK_PARAMS_EXACT */
+  PROFK_OPT_PARAM_MODE = 0,    /* PROFK_PARAMS_DEFAULT [0], _OLD, _EXACT or _CORRECTED */
   PROFK_OPT_MAX_ATTEMPTS = 1,  /* filter attempts before the exact fallback [6]; 0 = fallback at once */
   PROFK_OPT_TIE_EXIT = 2,      /* take PROFK_PATH_TIE when R > M and R_gt < k [1] */
   PROFK_OPT_FORCE_S = 3,       /* >0 overrides S (and disables the exact-path routing) [0] */

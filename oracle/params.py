@@ -26,7 +26,10 @@ with z = Phi^{-1}(1 - eps/2), then 1 <= t <= S and k <= M <= N.  The older
 t-rule sets t = 1 exactly where recall failure is likely (its own text derives
 the bound in the wrong direction), so it is kept only as a named function and
 an optional mode.  A third mode keeps that S and takes the exact optimal t and
-M of the corrected Theorem 4 (``params_exact``, pinned to Table 3).
+M of the corrected Theorem 4 (``params_exact``, pinned to Table 3).  A fourth
+follows the corrected Algorithm 1 throughout, its sample size included
+(Proposition 7 with a cost ratio r(k) calibrated on a GB300; the paper's own
+RTX 3060 calibration reproduces Table 3's S column).
 """
 from __future__ import annotations
 
@@ -150,6 +153,55 @@ def sample_size_prop7(N: int, k: int, eps: float, r: float):
     return S1, S2
 
 
+# Bounds of the corrected rule: the fixed-cost floor S_min = 2^14 (Appendix E.1,
+# "the fixed-cost floor"), S_max = 2^18 (Table 3 tops out there at N = 2^31).
+S_MIN_CORRECTED = 1 << 14
+S_MAX_CORRECTED = 1 << 18
+
+
+def inv_r_rtx3060(k: int):
+    """The paper's calibration of 1/r(k) on its RTX 3060 (Appendix E.1):
+    0.59 log2 k - 4.3 for k > 2^7; None (r = infinity) below."""
+    return 0.59 * math.log2(k) - 4.3 if k > (1 << 7) else None
+
+
+# The same fit on a GB300 (this library's kernels, an S sweep over n = 2^22..2^30,
+# k = 2^5..2^19): the buffer cost per element barely grows with k there, the
+# refinement being latency-bound, so the line is nearly flat.
+GB300_INV_R_SLOPE = 0.0033
+GB300_INV_R_INTERCEPT = 0.41
+
+
+def inv_r_gb300(k: int):
+    """1/r(k) calibrated on a GB300 in the paper's form: a + b log2 k for k > 2^7."""
+    return GB300_INV_R_SLOPE * math.log2(k) + GB300_INV_R_INTERCEPT if k > (1 << 7) else None
+
+
+def sample_size_corrected(N: int, k: int, eps: float, inv_r=inv_r_gb300, s_min: int = S_MIN_CORRECTED,
+                          s_max: int = S_MAX_CORRECTED) -> int:
+    """Corrected Algorithm 1, its sample-size steps (lines 1-4) with Proposition 7:
+    z = Phi^{-1}(1 - eps/2), kappa = z^2 + 1/2, S = clip(floor(max(S1, S2)), S_min, S_max),
+    S_min when r = infinity or k/N > 2^-10; then at most N/128.
+
+    The cap N/128 is a reading: Table 3 uses S = 8,192 = N/128 for every k at
+    N = 2^20, below the floor, and no other row reaches N/128.
+    """
+    ir = inv_r(k)
+    if ir is None or ir <= 0.0 or k > N / 1024.0:
+        S = s_min
+    else:
+        S1, S2 = sample_size_prop7(N, k, eps, 1.0 / ir)
+        S = min(max(math.floor(max(S1, S2)), s_min), s_max)
+    return max(1, min(S, N // 128))
+
+
+def params_corrected(N: int, k: int, eps: float, inv_r=inv_r_gb300):
+    """Corrected Algorithm 1 in full: the sample-size steps, then its t and M steps."""
+    S = sample_size_corrected(N, k, eps, inv_r)
+    t, M = params_fast(N, k, S, eps)
+    return S, t, M
+
+
 # ---------------------------------------------------------------------------
 # Older version: closed forms.
 
@@ -221,6 +273,7 @@ def params_old(N: int, k: int, eps: float, s_min: int = S_MIN_OLD, s_max: int = 
 MODE_DEFAULT = 0
 MODE_OLD = 1
 MODE_EXACT = 2
+MODE_CORRECTED = 3
 
 
 def params(N: int, k: int, eps: float, mode: int = MODE_DEFAULT):
@@ -229,6 +282,8 @@ def params(N: int, k: int, eps: float, mode: int = MODE_DEFAULT):
         S, t, M = params_old(N, k, eps)
         S = min(S, N)
         return S, min(max(t, 1), S), min(max(M, k), N)
+    if mode == MODE_CORRECTED:  # the corrected Algorithm 1 throughout, GB300 calibration
+        return params_corrected(N, k, eps)
     S = min(sample_size_old(N, k, eps), N)
     if mode == MODE_EXACT:  # Theorem 4 at that S
         t, M = params_exact(N, k, S, eps)

@@ -14,7 +14,7 @@ PROFK_ERR_UNSUPPORTED = -4
 PROFK_ERR_DEVICE_TIMEOUT = -5
 
 PATH_FILTER, PATH_TIE, PATH_FALLBACK, PATH_EXACT = 0, 1, 2, 3
-PARAMS_DEFAULT, PARAMS_OLD, PARAMS_EXACT = 0, 1, 2
+PARAMS_DEFAULT, PARAMS_OLD, PARAMS_EXACT, PARAMS_CORRECTED = 0, 1, 2, 3
 
 OPT_PARAM_MODE = 0
 OPT_MAX_ATTEMPTS = 1

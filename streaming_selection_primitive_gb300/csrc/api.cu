@@ -998,7 +998,7 @@ int profk_topk_batched(const float* x, int64_t rows, int64_t n, int64_t ld, int6
 }
 
 int profk_params(int64_t n, int64_t k, double eps, int mode, int64_t* S, int64_t* t, int64_t* M) {
-  if (n < 1 || k < 1 || k > n || !(eps > 0.0 && eps < 1.0) || mode < 0 || mode > 2 || !S || !t || !M)
+  if (n < 1 || k < 1 || k > n || !(eps > 0.0 && eps < 1.0) || mode < 0 || mode > 3 || !S || !t || !M)
     return PROFK_ERR_INVALID;
   const Params p = cached_params(n, k, eps, mode);
   *S = p.S;
@@ -1023,7 +1023,7 @@ size_t profk_workspace_size(int64_t rows, int64_t n, int64_t k, double eps) {
 
 int profk_set_option(int option, int64_t value) {
   if (option < 0 || option >= PROFK_OPT__COUNT) return PROFK_ERR_INVALID;
-  if (option == PROFK_OPT_PARAM_MODE && (value < 0 || value > 2)) return PROFK_ERR_INVALID;
+  if (option == PROFK_OPT_PARAM_MODE && (value < 0 || value > 3)) return PROFK_ERR_INVALID;
   if (value < 0) return PROFK_ERR_INVALID;
   g_opt[option].store(value);
   return PROFK_OK;

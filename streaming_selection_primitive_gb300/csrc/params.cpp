@@ -14,6 +14,14 @@
 //      M = ceil((n+1)/(S+1) t (1 - h + z sqrt(h))^3), h = 1/(9t)  (Eq 12)
 //  * older version, Algorithm 1 literally (Eq 6 t, Corollary 4 M, and t = 1
 //    when (k/n) S < -ln(eps/2)) as the optional mode.
+//  * corrected version, Algorithm 1 throughout (mode 3): its sample-size steps
+//    with Proposition 7, kappa = z^2 + 1/2,
+//      S1 = (z r(k)^-1)^(2/3) (k n)^(1/3),  S2 = (kappa n / r(k))^(1/2),
+//      S = clip(floor(max(S1, S2)), 2^14, 2^18), 2^14 when r = infinity or
+//      k/n > 2^-10, then at most n/128 (Table 3 uses n/128 at n = 2^20);
+//    the cost ratio in the paper's form 1/r(k) = a log2 k + b for k > 2^7
+//    (r = infinity below), with a and b fitted on a GB300 from an S sweep
+//    of whole calls (Appendix E.1's procedure).
 // The default mixes the two because the older t-rule sets t = 1 exactly where
 // recall failure is likely; the corrected version replaces it.
 #include <cmath>
@@ -164,8 +172,40 @@ void exact_params(int64_t n, int64_t k, int64_t S, double eps, int64_t* t, int64
   *M = lo;
 }
 
+// 1/r(k) of the corrected rule, fitted on a GB300: the buffer selection's cost
+// per element barely grows with k on this GPU (its refinement is bound by
+// latency, not by the number of keys), so the line is nearly flat.
+constexpr double kInvRSlope = 0.0033, kInvRIntercept = 0.41;
+
+int64_t sample_size_corrected(int64_t n, int64_t k, double eps) {
+  const int64_t s_min = int64_t(1) << 14, s_max = int64_t(1) << 18;
+  const double nn = static_cast<double>(n), kk = static_cast<double>(k);
+  int64_t S = s_min;
+  if (k > (1 << 7) && kk <= nn / 1024.0) {
+    const double inv_r = kInvRSlope * std::log2(kk) + kInvRIntercept;
+    if (inv_r > 0.0) {
+      const double z = inv_norm_cdf(1.0 - eps / 2.0);
+      const double kappa = z * z + 0.5;
+      const double S1 = std::pow(z * inv_r, 2.0 / 3.0) * std::cbrt(kk * nn);
+      const double S2 = std::sqrt(kappa * nn * inv_r);
+      const double s = std::floor(std::max(S1, S2));
+      S = s < static_cast<double>(s_min) ? s_min : (s > static_cast<double>(s_max) ? s_max : static_cast<int64_t>(s));
+    }
+  }
+  if (S > n / 128) S = n / 128;
+  return S < 1 ? 1 : S;
+}
+
 Params compute_params(int64_t n, int64_t k, double eps, int mode) {
   Params p{};
+  if (mode == 3) {
+    const int64_t S = sample_size_corrected(n, k, eps);
+    const int64_t t = clamp64(threshold_rank_fast(n, k, S, eps), 1, S);
+    p.S = S;
+    p.t = t;
+    p.M = clamp64(buffer_capacity_fast(n, S, t, eps), k, n);
+    return p;
+  }
   if (mode == 1) {
     const double z = 2.0 * inv_norm_cdf(1.0 - eps / 2.0);
     const double N = static_cast<double>(n), K = static_cast<double>(k);

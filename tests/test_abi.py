@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol(pk):
     assert not missing, missing
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_params_match_oracle(pk, mode):
     # The oracle's exact search (mode 2) is slow, so it gets a smaller grid.
     Ns = (1 << 20, 1 << 22, 1 << 26, 1 << 28, 1 << 30, 50331648, 1 << 24, 3_000_000_000, 1 << 32)

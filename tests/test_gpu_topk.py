@@ -294,6 +294,20 @@ def test_exact_parameter_mode(pk, cuda_device):
         assert st["R_first"] == ost.R_first and st["attempts"] == ost.attempts
 
 
+@pytest.mark.parametrize("n,k", [((1 << 22) + 12, 32), ((1 << 22) + 12, 1000), (1 << 24, 4096)])
+def test_corrected_parameter_mode(pk, cuda_device, n, k):
+    """The corrected Algorithm 1 throughout (PROFK_PARAMS_CORRECTED: its own
+    sample size, from Proposition 7 with the GB300 cost ratio)."""
+    x = workloads.normal(n, 10, cuda_device)
+    pk.set_option(pk.OPT_PARAM_MODE, pk.PARAMS_CORRECTED)
+    h = x.cpu().numpy()
+    vals, idx, st = pk.topk(x, k, 1e-3, 5)
+    ov, oi, ost = PK.profk(h, k, 1e-3, 5, mode=PP.MODE_CORRECTED)
+    assert_same(vals, idx, ov, oi, f"corrected-parameter mode n={n} k={k}")
+    assert (st["S"], st["t"], st["M"]) == (ost.S, ost.t, ost.M) == PP.params(n, k, 1e-3, PP.MODE_CORRECTED)
+    assert st["R_first"] == ost.R_first and st["attempts"] == ost.attempts and st["path"] == ost.path
+
+
 STAT_KEYS = ("S", "t", "M", "R_first", "R_gt_first", "tau_first", "R_final", "attempts", "path")
 
 

@@ -3,7 +3,8 @@
 Sources: the corrected page's Table 3 (golden file), its stated error bound of
 Acklam's approximation, its Appendix B remarks (k = 1 gives t = 1; the
 Wilson-Hilferty quantile overestimates ln(1/eps_B) by about 3% at t = 1),
-Proposition 7's bracket, the older page's z ~ 6.58 and S* ~ 4,600 example, and
+Proposition 7's bracket and Table 3's S column (the corrected Algorithm 1
+with the paper's RTX 3060 cost ratio), the older page's z ~ 6.58 and S* ~ 4,600 example, and
 the algebra of its Corollary 4.  scipy is an independent library check.
 """
 import itertools
@@ -165,3 +166,44 @@ def test_route():
     assert P.uses_filter(2**20 + 4, 2048, 32768, rows=1024) and not P.uses_filter(2**20, 2048, 32768, rows=1024)
     assert P.uses_filter(2**20, 2049, 32768, rows=1024)
     assert P.uses_filter(2**24, 32, 32768, rows=64) and P.uses_filter(2**24, 32, 32768, rows=4096)
+
+@pytest.mark.parametrize("r", ROWS, ids=lambda r: f"N2^{int(math.log2(r['N']))}-k2^{int(math.log2(r['k']))}")
+def test_table3_sample_size_column(r):
+    # Table 3's S column is the corrected Algorithm 1's sample size with the
+    # paper's RTX 3060 cost ratio (Appendix E.1: 1/r = 0.59 log2 k - 4.3 above
+    # k = 2^7).  Rows set by the floor 2^14, the cap 2^18 or N/128 (N = 2^20)
+    # match exactly; rows set by S1 or S2 within 5 %, the printed two-digit
+    # coefficients of r(k) being rounded (their largest effect, at k = 2^8
+    # where 1/r = 0.42 is a small difference of two large terms, is 4.7 %).
+    N, k = r["N"], r["k"]
+    S = P.sample_size_corrected(N, k, 1e-3, P.inv_r_rtx3060)
+    if r["S"] in (8192, 16384, 262144):
+        assert S == r["S"]
+    else:
+        assert abs(S / r["S"] - 1) < 0.05, (S, r["S"])
+
+
+def test_corrected_rule_regimes():
+    # Proposition 7's two regimes: sqrt(N) scaling (S2) for small k, (kN)^(1/3) (S1) above
+    # k ~ z sqrt(r N); S_min below the cut-off of r and for k/N > 2^-10.
+    inv = lambda k: 0.5
+    N = 1 << 40
+    s_small = P.sample_size_corrected(N, 256, 1e-3, inv, s_min=1, s_max=1 << 40)
+    z = P.norm_ppf(1 - 5e-4)
+    assert s_small == math.floor(math.sqrt((z * z + 0.5) * N * 0.5))
+    k = 1 << 30
+    s_big = P.sample_size_corrected(1 << 50, k, 1e-3, inv, s_min=1, s_max=1 << 50)
+    assert s_big == math.floor((z * 0.5) ** (2 / 3) * (k * (1 << 50)) ** (1 / 3))
+    assert P.sample_size_corrected(1 << 30, 100, 1e-3, P.inv_r_rtx3060) == P.S_MIN_CORRECTED
+    assert P.sample_size_corrected(1 << 20, 2048, 1e-3, P.inv_r_gb300) == 8192  # N/128 cap
+    assert P.sample_size_corrected(1 << 24, 1 << 15, 1e-3, P.inv_r_gb300) == P.S_MIN_CORRECTED  # k/N > 2^-10
+
+
+def test_corrected_mode_budget():
+    for N in (2**22, 2**26, 2**30, 50331648):
+        for k in (32, 1024, 4096, 2**19):
+            if 64 * k > N:
+                continue
+            S, t, M = P.params(N, k, 1e-3, P.MODE_CORRECTED)
+            assert 1 <= t <= S and k <= M <= N
+            assert P.prob_fail(N, k, S, t, M) <= 1e-3
