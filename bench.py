@@ -375,6 +375,32 @@ def main():
                     "gelem_s": round(n / ms / 1e6, 2), "hbm_frac_of_8TBs": round(4 * n / (ms / 1e3) / 8e12, 3)}
         finally:
             pk.set_option(pk.OPT_PARAM_MODE, pk.PARAMS_DEFAULT)
+        # The corrected paper's Table 4 sizes (single rows beyond 2^31, standard
+        # normal): latency and auxiliary memory of synchronous calls.  Rows above
+        # 2^32 elements are split into segments and merged.
+        table4 = {}
+        for big_n, kks in ((1 << 31, (1 << 10, 1 << 14, 1 << 18, 1 << 22)), (3_000_000_000, (1 << 10, 1 << 18)),
+                           (4_300_000_000, (1 << 10, 1 << 18, 1 << 22))):
+            xb = workloads.normal(big_n, 31 + rank, dev)
+            for kk in kks:
+                o2 = (torch.empty(kk, dtype=torch.float32, device=dev), torch.empty(kk, dtype=torch.int64, device=dev))
+                for w in range(2):
+                    pk.topk(xb, kk, EPS, 40_000 + w, out=o2)
+                torch.cuda.synchronize()
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 5
+                a0.record(stream)
+                for s in range(reps):
+                    _, _, st = pk.topk(xb, kk, EPS, 50_000 + s, out=o2)
+                a1.record(stream)
+                torch.cuda.synchronize()
+                ms = a0.elapsed_time(a1) / reps
+                table4[f"n{big_n}_k{kk}"] = {"ms": round(ms, 4), "gelem_s": round(big_n / ms / 1e6, 2),
+                                             "hbm_frac_of_8TBs": round(4 * big_n / (ms / 1e3) / 8e12, 3),
+                                             "aux_mb": round(st["aux_bytes"] / 1e6, 2), "path": st["path"]}
+            del xb
+            torch.cuda.empty_cache()
+        sweep["table4"] = table4
 
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu and args.gpus == 1:

@@ -22,7 +22,7 @@
  * Pointers.  x, out_vals, out_idx and every array documented as "device" are
  *   device pointers owned by the caller; x is only read.  stats is a host
  *   pointer and may be NULL.
- * Indices.  int64, relative to the row (0 .. n-1).  n must be <= 2^32.
+ * Indices.  int64, relative to the row (0 .. n-1).  n < 2^40.
  * Streams.  All device work is ordered on `stream` (0 = legacy default).
  *   profk_topk / profk_topk_batched synchronize `stream` once per filter
  *   attempt to read the exact count R (the pages' run-time check); outputs
@@ -52,7 +52,7 @@ typedef enum profk_status {
   PROFK_ERR_INVALID = -1,        /* an argument is out of range or NULL */
   PROFK_ERR_CUDA = -2,           /* a CUDA call failed; stats->cuda_error has the code */
   PROFK_ERR_NAN = -3,            /* the input holds a NaN */
-  PROFK_ERR_UNSUPPORTED = -4,    /* e.g. n > 2^32 or a misaligned input */
+  PROFK_ERR_UNSUPPORTED = -4,    /* e.g. n >= 2^40 or a misaligned input */
   PROFK_ERR_DEVICE_TIMEOUT = -5, /* a bounded device-side wait gave up */
   PROFK_ERR_SCRATCH = -6         /* the problem needs more than the fixed scratch or the caller's workspace */
 } profk_status;
@@ -90,7 +90,19 @@ typedef struct profk_stats {
 /* Exact top-k of one row x[0..n) (problem statement: paper Section 3).
  *   x         device, n floats, 16-byte aligned for the vectorised filter
  *             (other alignments return PROFK_ERR_UNSUPPORTED)
- *   n         1 <= n <= 2^32
+ *   n         1 <= n < 2^40.  A row longer than 2^32 elements (the paper's
+ *             Table 4 goes to 4.3e9) is split into P = ceil(n / 2^32)
+ *             contiguous segments of equal length rounded up to a multiple
+ *             of 4, the last one possibly shorter; each segment's exact
+ *             top-min(k, length) is selected as a row of the batched call
+ *             with the budget eps / P, and the P sorted lists are merged by
+ *             value and global index.  The result is the row's exact top-k;
+ *             the call then runs synchronously, and its stats describe the
+ *             segments together: S, t, M and tau of the first segment, the
+ *             counts R summed over segments (-1 if any is -1), attempts and
+ *             path the largest over segments, aux_bytes the workspace of the
+ *             largest segment call plus the merge's 12 bytes per candidate.
+ *             PROFK_OPT_MAX_SEGMENT lowers the 2^32 split point (for tests).
  *   k         1 <= k <= n
  *   eps       failure budget of one attempt, 0 < eps < 1, split eps/2 + eps/2
  *             between recall failure and overflow (Theorem 4's default split)
@@ -198,7 +210,9 @@ typedef enum profk_option {
   PROFK_OPT_TIMING = 6,        /* record stats.filter_ms with CUDA events [0] */
   PROFK_OPT_FILTER_CTAS_PER_SM = 7, /* persistent filter grid = SMs x this; 0 = auto [0] */
   PROFK_OPT_PDL = 8,           /* launch kernels with programmatic dependent launch [1] */
-  PROFK_OPT__COUNT = 9
+  PROFK_OPT_MAX_SEGMENT = 9,   /* rows longer than this are split into segments (see profk_topk);
+                                  a multiple of 4, >= 2^16; 0 = 2^32 [0] */
+  PROFK_OPT__COUNT = 10
 } profk_option;
 int profk_set_option(int option, int64_t value);
 int64_t profk_get_option(int option);

@@ -25,7 +25,8 @@ OPT_FORCE_M = 5
 OPT_TIMING = 6
 OPT_FILTER_CTAS_PER_SM = 7
 OPT_PDL = 8
-OPT_DEFAULTS = {0: 0, 1: 6, 2: 1, 3: 0, 4: 0, 5: 0, 6: 0, 7: 0, 8: 1}
+OPT_MAX_SEGMENT = 9
+OPT_DEFAULTS = {0: 0, 1: 6, 2: 1, 3: 0, 4: 0, 5: 0, 6: 0, 7: 0, 8: 1, 9: 0}
 
 
 class ProfkStats(C.Structure):

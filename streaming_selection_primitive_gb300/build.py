@@ -22,7 +22,7 @@ LIB = LIBDIR / "libprofk.so"
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", str(INCLUDE)] + ARCH
-SOURCES = ["sample.cu", "select.cu", "sort.cu", "refine.cu", "tie.cu", "rows.cu", "filter.cu", "api.cu", "params.cpp", "noalloc.cu"]
+SOURCES = ["sample.cu", "select.cu", "sort.cu", "refine.cu", "tie.cu", "rows.cu", "filter.cu", "segments.cu", "api.cu", "params.cpp", "noalloc.cu"]
 
 
 def _nvcc() -> str:

@@ -28,7 +28,35 @@ namespace {
 // ---------------------------------------------------------------------------
 // Options.
 std::atomic<int64_t> g_opt[PROFK_OPT__COUNT] = {
-    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}, {1}};
+    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}, {1}, {0}};
+
+// Longest row handled as one (PROFK_OPT_MAX_SEGMENT; 0 = 2^32, the reach of a
+// candidate key's 32-bit index field).  Longer rows are split into segments.
+int64_t max_segment() {
+  const int64_t v = g_opt[PROFK_OPT_MAX_SEGMENT].load();
+  return v > 0 ? v : (int64_t(1) << 32);
+}
+
+// Rows up to 2^40 elements, split into at most this many segments.
+constexpr int64_t MAX_ROW = int64_t(1) << 40;
+constexpr int64_t MAX_SEGMENTS = 4096;
+
+// A row of n > max_segment() elements as P segments: the first main_rows of
+// seg_len elements (a multiple of 4, so every segment stays 16-byte aligned),
+// then, unless all are equal (main_rows == P), a shorter last one of tail_len.
+struct SegmentPlan {
+  int64_t P = 1, seg_len = 0, tail_len = 0, main_rows = 0;
+};
+
+SegmentPlan plan_segments(int64_t n, int64_t max_seg) {
+  SegmentPlan p;
+  p.P = (n + max_seg - 1) / max_seg;
+  const int64_t per = (n + p.P - 1) / p.P;
+  p.seg_len = (per + 3) & ~int64_t(3);
+  p.tail_len = n - (p.P - 1) * p.seg_len;
+  p.main_rows = p.tail_len == p.seg_len ? p.P : p.P - 1;
+  return p;
+}
 
 // ---------------------------------------------------------------------------
 // Memoized parameters per (n, k, eps, mode).
@@ -533,12 +561,108 @@ cudaError_t enqueue_report(const RowState* st, int64_t rows, char* rep, unsigned
 }
 
 int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,
+             float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_stats* stats);
+
+// Rows longer than max_segment(): each row is split into segments (see
+// plan_segments), the segments' exact top-k lists are selected by the batched
+// path (budget eps / (rows P) per segment), and merged into the row's top k
+// by k_merge_segments.  Rows are handled one after the other.
+int run_long_rows(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,
+                  float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_stats* stats) {
+  const SegmentPlan sp = plan_segments(n, max_segment());
+  if (sp.P > MAX_SEGMENTS || sp.tail_len < 1) return PROFK_ERR_UNSUPPORTED;
+  const int64_t k_main = std::min(k, sp.seg_len);
+  const bool has_tail = sp.main_rows < sp.P;
+  const int64_t k_tail = has_tail ? std::min(k, sp.tail_len) : 0;
+  const int64_t cand = sp.main_rows * k_main + k_tail;
+  const size_t val_bytes = align_up(sizeof(float) * cand);
+  const size_t temp = val_bytes + align_up(sizeof(int64_t) * cand);
+  const double eps_seg = eps / static_cast<double>(rows) / static_cast<double>(sp.P);
+  const int64_t launches0 = launch_count();
+  std::vector<profk_stats> sub(static_cast<size_t>(sp.P));
+  int status = PROFK_OK;
+  if (stats)
+    for (int64_t r = 0; r < rows; ++r) fill_stats_params(&stats[r], Params{0, 0, 0});
+  // The candidate lists: from the caller's workspace (its last `temp` bytes,
+  // the segment calls using the rest) or from the library's pool.
+  void* const user_ws = t_user_ws;
+  const size_t user_bytes = t_user_ws_bytes;
+  char* tbuf = nullptr;
+  cudaMemPool_t pool = nullptr;
+  cudaError_t ce = cudaSuccess;
+  if (user_ws) {
+    if (user_bytes < temp) return PROFK_ERR_SCRATCH;
+    tbuf = static_cast<char*>(user_ws) + ((user_bytes - temp) & ~static_cast<size_t>(255));
+    t_user_ws_bytes = (user_bytes - temp) & ~static_cast<size_t>(255);
+  } else {
+    ce = pool_for_current_device(&pool);
+    if (ce == cudaSuccess) ce = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&tbuf), temp, pool, stream);
+    if (ce != cudaSuccess) {
+      if (stats)
+        for (int64_t r = 0; r < rows; ++r) {
+          std::memset(&stats[r], 0, sizeof(profk_stats));
+          stats[r].cuda_error = static_cast<int32_t>(ce);
+        }
+      return PROFK_ERR_CUDA;
+    }
+  }
+  float* tv = reinterpret_cast<float*>(tbuf);
+  int64_t* ti = reinterpret_cast<int64_t*>(tbuf + val_bytes);
+  uint64_t aux = 0;
+  for (int64_t r = 0; r < rows && status == PROFK_OK; ++r) {
+    const float* xr = x + r * ld;
+    status = run_topk(xr, sp.main_rows, sp.seg_len, sp.seg_len, k_main, eps_seg * static_cast<double>(sp.main_rows),
+                      seed, tv, ti, stream, sub.data());
+    if (status == PROFK_OK && has_tail)
+      status = run_topk(xr + sp.main_rows * sp.seg_len, 1, sp.tail_len, sp.tail_len, k_tail, eps_seg, seed,
+                        tv + sp.main_rows * k_main, ti + sp.main_rows * k_main, stream, &sub[sp.P - 1]);
+    if (status == PROFK_OK) {
+      launch_merge_segments(MergeSegmentsArgs{tv, ti, static_cast<int>(sp.P), k_main, has_tail ? k_tail : k_main,
+                                              sp.seg_len, k, out_vals + r * k, out_idx + r * k},
+                            stream);
+      ce = cudaGetLastError();
+      if (ce != cudaSuccess) status = PROFK_ERR_CUDA;
+    }
+    if (stats) {
+      profk_stats& o = stats[r];
+      o = sub[0];
+      o.attempts = 0;
+      o.path = 0;
+      o.draw_doublings = 0;
+      o.cuda_error = static_cast<int32_t>(ce);
+      int64_t* const sums[4] = {&o.R_first, &o.R_gt_first, &o.R_final, &o.R_gt_final};
+      for (auto* p : sums) *p = 0;
+      for (const profk_stats& q : sub) {
+        const int64_t vals[4] = {q.R_first, q.R_gt_first, q.R_final, q.R_gt_final};
+        for (int j = 0; j < 4; ++j) *sums[j] = (*sums[j] < 0 || vals[j] < 0) ? -1 : *sums[j] + vals[j];
+        o.attempts = std::max(o.attempts, q.attempts);
+        o.path = std::max(o.path, q.path);
+        o.draw_doublings += q.draw_doublings;
+        if (!o.cuda_error) o.cuda_error = q.cuda_error;
+        aux = std::max<uint64_t>(aux, q.aux_bytes);
+      }
+    }
+  }
+  if (user_ws)
+    t_user_ws_bytes = user_bytes;
+  else
+    cudaFreeAsync(tbuf, stream);
+  if (stats)
+    for (int64_t r = 0; r < rows; ++r) {
+      stats[r].aux_bytes = aux + temp;
+      stats[r].launches = static_cast<int32_t>(launch_count() - launches0);
+    }
+  return status;
+}
+
+int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,
              float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_stats* stats) {
   if (!x || !out_vals || !out_idx) return PROFK_ERR_INVALID;
   if (rows < 1 || n < 1 || k < 1 || k > n || ld < n || !(eps > 0.0 && eps < 1.0)) return PROFK_ERR_INVALID;
   if (rows > (1 << 20)) return PROFK_ERR_INVALID;
-  if (n > (1ll << 32)) return PROFK_ERR_UNSUPPORTED;
+  if (n >= MAX_ROW) return PROFK_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(x) & 15) != 0 || (rows > 1 && (ld & 3) != 0)) return PROFK_ERR_UNSUPPORTED;
+  if (n > max_segment()) return run_long_rows(x, rows, n, ld, k, eps, seed, out_vals, out_idx, stream, stats);
 
   const int mode = static_cast<int>(g_opt[PROFK_OPT_PARAM_MODE].load());
   const int max_attempts = static_cast<int>(std::max<int64_t>(0, g_opt[PROFK_OPT_MAX_ATTEMPTS].load()));
@@ -849,7 +973,7 @@ int submit_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
   if (!x || !out_vals || !out_idx) return PROFK_ERR_INVALID;
   if (rows < 1 || n < 1 || k < 1 || k > n || ld < n || !(eps > 0.0 && eps < 1.0)) return PROFK_ERR_INVALID;
   if (rows > (1 << 20)) return PROFK_ERR_INVALID;
-  if (n > (1ll << 32)) return PROFK_ERR_UNSUPPORTED;
+  if (n >= MAX_ROW) return PROFK_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(x) & 15) != 0 || (rows > 1 && (ld & 3) != 0)) return PROFK_ERR_UNSUPPORTED;
   profk_call* call = new profk_call;
   call->x = x;
@@ -868,7 +992,7 @@ int submit_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
   const int mode = static_cast<int>(g_opt[PROFK_OPT_PARAM_MODE].load());
   const bool plain = g_opt[PROFK_OPT_FORCE_S].load() == 0 && g_opt[PROFK_OPT_FORCE_T].load() == 0 &&
                      g_opt[PROFK_OPT_FORCE_M].load() == 0 && g_opt[PROFK_OPT_TIMING].load() == 0 &&
-                     g_opt[PROFK_OPT_MAX_ATTEMPTS].load() > 0 && t_user_ws == nullptr;
+                     g_opt[PROFK_OPT_MAX_ATTEMPTS].load() > 0 && t_user_ws == nullptr && n <= max_segment();
   const Params P = cached_params(n, k, eps / static_cast<double>(rows), mode);
   if (!plain || !uses_filter(n, k, P.S, rows)) {
     // Options, routes and caller workspaces outside the asynchronous form:
@@ -1014,16 +1138,37 @@ int profk_set_workspace(void* dev_ptr, size_t bytes) {
   return PROFK_OK;
 }
 
-size_t profk_workspace_size(int64_t rows, int64_t n, int64_t k, double eps) {
-  if (rows < 1 || n < 1 || k < 1 || k > n || !(eps > 0.0 && eps < 1.0)) return 0;
+namespace profk {
+namespace {
+size_t layout_bytes(int64_t rows, int64_t n, int64_t k, double eps) {
   const Params P = cached_params(n, k, eps / static_cast<double>(rows), static_cast<int>(g_opt[0].load()));
   const bool sampling = uses_filter(n, k, P.S, rows);
   return make_layout(rows, n, k, P.S, sampling ? draw_budget(n, P.S) : 0, P.M, sampling).total;
+}
+}  // namespace
+}  // namespace profk
+
+size_t profk_workspace_size(int64_t rows, int64_t n, int64_t k, double eps) {
+  if (rows < 1 || n < 1 || k < 1 || k > n || !(eps > 0.0 && eps < 1.0) || n >= MAX_ROW) return 0;
+  if (n <= max_segment()) return layout_bytes(rows, n, k, eps);
+  // A long row: the larger of its segment calls plus the merge's candidate lists.
+  const SegmentPlan sp = plan_segments(n, max_segment());
+  if (sp.P > MAX_SEGMENTS || sp.tail_len < 1) return 0;
+  const int64_t k_main = std::min(k, sp.seg_len);
+  const bool has_tail = sp.main_rows < sp.P;
+  const int64_t k_tail = has_tail ? std::min(k, sp.tail_len) : 0;
+  const int64_t cand = sp.main_rows * k_main + k_tail;
+  const double eps_seg = eps / static_cast<double>(rows) / static_cast<double>(sp.P);
+  size_t need = layout_bytes(sp.main_rows, sp.seg_len, k_main, eps_seg * static_cast<double>(sp.main_rows));
+  if (has_tail) need = std::max(need, layout_bytes(1, sp.tail_len, k_tail, eps_seg));
+  return align_up(need) + align_up(sizeof(float) * cand) + align_up(sizeof(int64_t) * cand);
 }
 
 int profk_set_option(int option, int64_t value) {
   if (option < 0 || option >= PROFK_OPT__COUNT) return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_PARAM_MODE && (value < 0 || value > 3)) return PROFK_ERR_INVALID;
+  if (option == PROFK_OPT_MAX_SEGMENT && value != 0 && (value < (1 << 16) || value > (int64_t(1) << 32) || (value & 3)))
+    return PROFK_ERR_INVALID;
   if (value < 0) return PROFK_ERR_INVALID;
   g_opt[option].store(value);
   return PROFK_OK;

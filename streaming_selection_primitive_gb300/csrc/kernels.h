@@ -252,4 +252,19 @@ struct FilterArgs {
 void launch_filter(const FilterArgs& a, cudaStream_t stream);
 int filter_default_grid(int sms);
 
+// Merge of the per-segment top-k lists of a row split into segments
+// (segments.cu).  List s (s < lists - 1) holds list_len entries at
+// vals/idx + s * list_len, the last list last_len <= list_len entries after
+// them; each is sorted in the library order with indices relative to its
+// segment, which starts at s * seg_len in the row.  Writes the row's top k.
+struct MergeSegmentsArgs {
+  const float* vals;
+  const int64_t* idx;
+  int lists;
+  int64_t list_len, last_len, seg_len, k;
+  float* out_vals;
+  int64_t* out_idx;
+};
+void launch_merge_segments(const MergeSegmentsArgs& a, cudaStream_t stream);
+
 }  // namespace profk

@@ -77,7 +77,7 @@ def test_invalid_arguments_are_rejected_before_any_device_work(pk):
     assert lib.profk_topk(fake, 10, 11, 1e-3, 0, fake, fake, None, None) == -1
     assert lib.profk_topk(fake, 10, 1, 0.0, 0, fake, fake, None, None) == -1
     assert lib.profk_topk(fake, 10, 1, 1.0, 0, fake, fake, None, None) == -1
-    assert lib.profk_topk(fake, (1 << 32) + 1, 1, 1e-3, 0, fake, fake, None, None) == -4
+    assert lib.profk_topk(fake, 1 << 40, 1, 1e-3, 0, fake, fake, None, None) == -4
     assert lib.profk_topk(C.c_void_p(258), 10, 1, 1e-3, 0, fake, fake, None, None) == -4
     assert lib.profk_topk_batched(fake, 0, 10, 10, 1, 1e-3, 0, fake, fake, None, None) == -1
     assert lib.profk_topk_batched(fake, 2, 10, 9, 1, 1e-3, 0, fake, fake, None, None) == -1
@@ -114,3 +114,22 @@ def test_async_argument_checks(pk):
     assert lib.profk_topk_async(fake, 10, 1, 1e-3, 0, fake, fake, None, None) == -1
     assert lib.profk_topk_batched_async(fake, 2, 10, 10, 1, 1e-3, 0, fake, fake, None, C.byref(h)) == -4
     assert lib.profk_wait(None, None) == -1
+
+
+def test_long_row_workspace_size(pk):
+    # A row beyond the split point needs the larger of its segment calls plus
+    # 12 bytes per merged candidate.  The plan: P = ceil(n / 2^32) segments of
+    # ceil(n / P) rounded up to a multiple of 4, the last one possibly shorter;
+    # equal segments go through one batched call, a shorter last one alone.
+    round256 = lambda v: (v + 255) // 256 * 256
+    k = 1 << 18
+    n = 4_300_000_000  # two equal segments: one batched call of two rows
+    seg = n // 2
+    cand = 2 * k
+    assert pk.workspace_size(1, n, k, 1e-3) == (round256(pk.workspace_size(2, seg, k, 1e-3))
+                                                 + round256(4 * cand) + round256(8 * cand))
+    n = 4_300_000_004  # ceil(n / 2) = 2,150,000,002 -> 2,150,000,004; the tail has 2,150,000,000
+    seg, tail = 2_150_000_004, 2_150_000_000
+    need = max(pk.workspace_size(1, seg, k, 1e-3 / 2), pk.workspace_size(1, tail, k, 1e-3 / 2))
+    assert pk.workspace_size(1, n, k, 1e-3) == round256(need) + round256(4 * cand) + round256(8 * cand)
+    assert pk.workspace_size(1, 1 << 40, 1, 1e-3) == 0
