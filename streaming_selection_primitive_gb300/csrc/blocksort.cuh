@@ -83,4 +83,101 @@ __device__ __forceinline__ void block_sort_desc(unsigned long long* s) {
   __syncthreads();
 }
 
+// Descending sort of 32 E keys (E = 1, 2, 4 or 8) by one warp, E in each
+// lane's registers: key r * 32 + lane is v[r].  The bitonic network's
+// partners closer than 32 are other lanes (shuffles), the rest other registers.
+template <int E>
+__device__ __forceinline__ void warp_sort_desc(unsigned long long (&v)[E]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32 * E; size <<= 1) {
+#pragma unroll
+    for (int m = E / 2; m >= 1; m >>= 1) {
+      if (32 * m < size) {
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+          const int r2 = r ^ m;
+          if (r2 > r) {
+            const bool desc = ((r * 32 + lane) & size) == 0;
+            const unsigned long long a = v[r], b = v[r2];
+            if (desc ? (a < b) : (a > b)) {
+              v[r] = b;
+              v[r2] = a;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int jj = 16; jj >= 1; jj >>= 1) {
+      if (jj < size) {
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+          const bool desc = ((r * 32 + lane) & size) == 0;
+          const unsigned long long o = __shfl_xor_sync(FULL_MASK, v[r], jj);
+          const bool lower = (lane & jj) == 0;
+          v[r] = (desc == lower) ? (v[r] > o ? v[r] : o) : (v[r] < o ? v[r] : o);
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void warp_sort256_desc(unsigned long long (&v)[8]) { warp_sort_desc<8>(v); }
+
+// Descending sort of P keys s[0..P) (P a multiple of 256, at most 256 x the
+// warps of the block) by a block of 1024 threads: every warp sorts one run of
+// 256 in registers, then runs are merged pairwise (merge path: each thread
+// finds where its P / 1024 outputs start by a binary search, then merges
+// them), alternating between s and t (P keys each).  Keys must be distinct.
+// Returns the buffer that holds the result; ends with a block barrier.
+__device__ __forceinline__ unsigned long long* block_merge_sort_desc(unsigned long long* s, unsigned long long* t,
+                                                                     int P) {
+  constexpr int T = 1024;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp * 256 < P) {
+    unsigned long long v[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) v[r] = s[warp * 256 + r * 32 + lane];
+    warp_sort256_desc(v);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) s[warp * 256 + r * 32 + lane] = v[r];
+  }
+  __syncthreads();
+  // Outputs per thread and round: a power of two, so that no thread's run of
+  // outputs crosses the boundary of a merged pair (pairs are 512 or more long).
+  int per = 1;
+  while (per * T < P) per <<= 1;
+  for (int w = 256; w < P; w <<= 1) {
+    const int p0 = threadIdx.x * per;
+    if (p0 < P) {
+      const int base = p0 / (2 * w) * (2 * w);  // this pair's first position
+      const int na = w < P - base ? w : P - base;
+      const int nb = P - base - na < w ? P - base - na : w;
+      const unsigned long long* A = s + base;
+      const unsigned long long* B = A + na;
+      const int off = p0 - base;
+      int lo = off > nb ? off - nb : 0, hi = off < na ? off : na;
+      while (lo < hi) {  // how many of the first `off` outputs come from A
+        const int mid = (lo + hi) >> 1;
+        if (A[mid] > B[off - mid - 1])
+          lo = mid + 1;
+        else
+          hi = mid;
+      }
+      int i = lo, j = off - lo;
+      const int end = p0 + per < base + na + nb ? p0 + per : base + na + nb;
+      for (int p = p0; p < end; ++p) {
+        const bool takeA = j >= nb || (i < na && A[i] > B[j]);
+        t[p] = takeA ? A[i++] : B[j++];
+      }
+    }
+    __syncthreads();
+    unsigned long long* x = s;
+    s = t;
+    t = x;
+  }
+  return s;
+}
+
 }  // namespace profk

@@ -32,9 +32,26 @@
 //     already prove a run longer than 256 (fewer than len / 256 distinct
 //     values are possible), steps 2-3 are skipped and the full sort runs at
 //     once.
+//  B. For rows of at least 8192 keys, a bucket stage runs between steps 1
+//     and 2 instead of the passes: the keys are counted into at most 2^14
+//     buckets in key order, each digit of the highest varying byte split by
+//     the bits below it into as many as its step-1 count calls for (about
+//     len / 7500 keys a bucket), scattered once into bucket order, and then
+//     sorted: when no bucket holds more than 256 keys, each bucket by one warp
+//     in registers; otherwise range by
+//     range: a range is a run of whole buckets of at most 8191 keys, sorted
+//     completely (value and index) by one CTA in shared memory (runs of 256
+//     keys sorted in registers by each warp, then merged pairwise), so ties
+//     need no further work; ranges that start at or beyond position k are not
+//     sorted.  Three grid barriers in all.  When some bucket holds more than
+//     4096 keys (a few values repeated very often), every CTA sees it in the
+//     same histogram and the row takes steps 2-3 instead.
 // Output values are decoded from the key (it holds them exactly), except
 // zero, whose sign the key does not keep: it is read from x.  Every wait is
 // bounded; a wait that runs out sets an error bit in the row state.
+#include <type_traits>
+
+#include "blocksort.cuh"
 #include "kernels.h"
 
 namespace profk {
@@ -55,6 +72,14 @@ constexpr int RS_KMAX = 8;                                       // keys per thr
 constexpr int RS_SUB = RS_THREADS * RS_KMAX;                     // 8192 keys ranked at a time
 constexpr size_t RS_SMEM = sizeof(unsigned long long) * RS_SUB;  // staging of a piece (64 KB)
 constexpr int RUN_MAX = 256;   // runs up to this long are ordered by a warp
+constexpr int BK_BITS = 14;
+constexpr int BK = 1 << BK_BITS;           // buckets of the bucket stage
+constexpr unsigned BK_CAP = 4096;          // largest bucket the stage takes
+constexpr int64_t BK_MIN_LEN = RS_SUB;     // rows of fewer keys take the passes
+constexpr int64_t RANGE_MAX = RS_SUB;      // keys one CTA sorts in shared memory at once
+// Dynamic shared memory: the staging area (a piece, a range) and, for the
+// bucket stage, the buckets' starts and the merge buffer of a range.
+constexpr size_t RS_SMEM_LAUNCH = 2 * RS_SMEM + sizeof(unsigned) * BK;
 // Look-back flag: status (2 bits) | pass sequence number (4 bits) | count (58 bits).
 constexpr unsigned long long FLAG_AGG = 1ull << 62;   // the chunk's own digit count
 constexpr unsigned long long FLAG_INCL = 2ull << 62;  // count of this and every earlier chunk
@@ -136,6 +161,12 @@ struct Smem {
   unsigned distinct[8];  // byte values present at each position
   unsigned nruns;  // runs of 2 .. RUN_MAX keys starting in this chunk
   int err;
+  unsigned boff[256];         // bucket stage: first bucket of each digit of the top position
+  unsigned char bbits[256];   // and the bits that split the digit into buckets
+  unsigned nbuckets;
+  unsigned bwsum[32];         // bucket stage: per-warp sums of the starts' scan
+  unsigned bmax[32];          // and per-warp largest buckets
+  long long rlo, rhi;         // the range a CTA sorts next
 };
 
 // Every CTA of the row arrives (a release: the CTA's writes, ordered before
@@ -364,11 +395,257 @@ __device__ __forceinline__ void radix_pass(const RadixSortArgs& a, int row, int6
   }
 }
 
+// First position of the bucket starts st[0..BK) (nondecreasing) at or after
+// pos: the start of the first bucket beginning there, or len.
+__device__ __forceinline__ int64_t bucket_at(const unsigned* st, int64_t pos, int64_t len) {
+  int lo = 0, hi = BK;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (static_cast<int64_t>(st[mid]) >= pos)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  return lo < BK ? static_cast<int64_t>(st[lo]) : len;
+}
+
+// The bucket stage (B in the header).  Returns true when it sorted and
+// emitted the row, false (in every CTA alike, after one grid barrier) when a
+// bucket is too large; the row's keys are then untouched.
+__device__ bool bucket_stage(const RadixSortArgs& a, int row, int64_t len, int64_t lo, int64_t hi, SortCtl& c,
+                             unsigned& target, unsigned* bkr, unsigned long long* tmp_row, Smem& sm,
+                             unsigned long long* s_keys) {
+  const unsigned long long* keys = a.keys + row * a.key_stride;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned G = gridDim.x;
+  // Buckets in key order, sized from the data: the bytes above ps, the
+  // highest position with more than one digit, are the same in every key;
+  // each digit d of position ps gets 2^b(d) buckets, split by the b(d) bits
+  // below it, with b(d) the least for which its c(d) keys average at most
+  // ceil(len / 7500) per bucket (2^b(d) < 2 c(d) / that + 1, so fewer than
+  // 15,256 in all).
+  int ps = -1;
+  for (int p = 7; p >= 0 && ps < 0; --p)
+    if (!sm.trivial[p]) ps = p;
+  if (ps < 0) ps = 0;  // a single key
+  if (warp == 0) {
+    const int64_t target = (len + 7499) / 7500;  // >= len / 7500, so the buckets number < 15,000 + 256
+    unsigned nb[8], tot = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int d = lane * 8 + j;
+      const int64_t c = static_cast<int64_t>((d < 255 ? sm.start[ps][d + 1] : static_cast<unsigned long long>(len)) -
+                                             sm.start[ps][d]);
+      int b = 0;
+      while (b < BK_BITS && b < 8 * ps && (static_cast<int64_t>(1) << b) * target < c) ++b;
+      sm.bbits[d] = static_cast<unsigned char>(b);
+      nb[j] = 1u << b;
+      tot += nb[j];
+    }
+    unsigned incl = tot;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += t;
+    }
+    unsigned run = incl - tot;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sm.boff[lane * 8 + j] = run;
+      run += nb[j];
+    }
+    if (lane == 31) sm.nbuckets = incl;
+  }
+  __syncthreads();
+  if (sm.nbuckets > static_cast<unsigned>(BK)) return false;  // (not reached, see above)
+  const int pb = 8 * ps;
+  auto bucket_of = [&](unsigned long long kk) {
+    const unsigned long long nk = ~kk;
+    const unsigned d = static_cast<unsigned>(nk >> pb) & 255u;
+    const int b = sm.bbits[d];
+    return sm.boff[d] + (b ? static_cast<unsigned>(nk >> (pb - b)) & ((1u << b) - 1u) : 0u);
+  };
+  unsigned* h = reinterpret_cast<unsigned*>(s_keys);            // the chunk's counts, then its cursors
+  unsigned* st = reinterpret_cast<unsigned*>(s_keys + RS_SUB);  // every bucket's start in the row
+  // The chunk's keys: in shared memory when step 1 kept them there.
+  const unsigned long long* cst = s_keys + 2 * RS_SUB;
+  const bool staged = hi - lo <= RS_SUB;
+  auto key_at = [&](int64_t i) { return staged ? cst[i - lo] : __ldcg(keys + i); };
+  for (int i = threadIdx.x; i < BK; i += RS_THREADS) h[i] = 0;
+  __syncthreads();
+  for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS) atomicAdd(&h[bucket_of(key_at(i))], 1u);
+  __syncthreads();
+  for (int i = threadIdx.x; i < BK; i += RS_THREADS)
+    if (h[i]) atomicAdd(&bkr[i], h[i]);
+  grid_sync(c, target += G, sm);
+
+  // Starts: the exclusive scan of the row's counts.  The counts come into
+  // shared memory with coalesced loads; each thread then scans 16 consecutive
+  // ones (four 16-byte reads).
+  constexpr int PER = BK / RS_THREADS;
+  {
+    unsigned cv[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) cv[j] = __ldcg(bkr + j * RS_THREADS + threadIdx.x);
+#pragma unroll
+    for (int j = 0; j < PER; ++j) st[j * RS_THREADS + threadIdx.x] = cv[j];
+  }
+  __syncthreads();
+  unsigned v[PER], sum = 0, mx = 0;
+  {
+    const uint4* s4 = reinterpret_cast<const uint4*>(st + threadIdx.x * PER);
+#pragma unroll
+    for (int q = 0; q < PER / 4; ++q) {
+      const uint4 u = s4[q];
+      v[4 * q] = u.x;
+      v[4 * q + 1] = u.y;
+      v[4 * q + 2] = u.z;
+      v[4 * q + 3] = u.w;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    sum += v[j];
+    mx = v[j] > mx ? v[j] : mx;
+  }
+  unsigned incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
+    if (lane >= o) incl += t;
+    mx = max(mx, __shfl_xor_sync(FULL_MASK, mx, o));
+  }
+  if (lane == 31) sm.bwsum[warp] = incl;
+  if (lane == 0) sm.bmax[warp] = mx;
+  __syncthreads();
+  unsigned run = incl - sum;
+  for (int w = 0; w < warp; ++w) run += sm.bwsum[w];
+  {
+    uint4* s4 = reinterpret_cast<uint4*>(st + threadIdx.x * PER);
+#pragma unroll
+    for (int q = 0; q < PER / 4; ++q) {
+      uint4 u;
+      u.x = run;
+      run += v[4 * q];
+      u.y = run;
+      run += v[4 * q + 1];
+      u.z = run;
+      run += v[4 * q + 2];
+      u.w = run;
+      run += v[4 * q + 3];
+      s4[q] = u;
+    }
+  }
+  unsigned maxb = 0;
+  for (int w = 0; w < RS_THREADS / 32; ++w) maxb = sm.bmax[w] > maxb ? sm.bmax[w] : maxb;
+  __syncthreads();
+  if (maxb > BK_CAP) return false;
+
+  // Scatter: the chunk reserves its slots of each bucket at once (the
+  // reservations of a thread are issued together); its keys then take
+  // consecutive slots (in any order: each bucket is sorted whole).
+  unsigned* gcur = bkr + BK;
+  {
+    unsigned res[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = j * RS_THREADS + threadIdx.x;
+      res[j] = h[i] ? atomicAdd(&gcur[i], h[i]) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = j * RS_THREADS + threadIdx.x;
+      if (h[i]) h[i] = st[i] + res[j];
+    }
+  }
+  __syncthreads();
+  for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS) {
+    const unsigned long long kk = key_at(i);
+    tmp_row[atomicAdd(&h[bucket_of(kk)], 1u)] = kk;
+  }
+  grid_sync(c, target += G, sm);
+
+  if (maxb <= 256) {
+    // Small buckets: each is sorted by one warp in registers (the smallest
+    // network of 32, 64, 128 or 256 keys that holds it), bucket b by the
+    // grid's warp b mod (32 G); buckets that start at or beyond k are skipped.
+    const unsigned nbk = sm.nbuckets;
+    for (unsigned b = blockIdx.x * (RS_THREADS / 32) + warp; b < nbk; b += G * (RS_THREADS / 32)) {
+      const int64_t bs = st[b], be = b + 1 < nbk ? static_cast<int64_t>(st[b + 1]) : len;
+      if (bs >= be || bs >= a.k) continue;
+      const int sz = static_cast<int>(be - bs);
+      auto sort_emit = [&](auto tagE) {
+        constexpr int E = decltype(tagE)::value;
+        unsigned long long kv[E];
+#pragma unroll
+        for (int r = 0; r < E; ++r) kv[r] = r * 32 + lane < sz ? __ldcg(tmp_row + bs + r * 32 + lane) : 0ull;
+        warp_sort_desc<E>(kv);
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+          const int q = r * 32 + lane;
+          if (q < sz && bs + q < a.k) emit_key(a, row, bs + q, kv[r]);
+        }
+      };
+      if (sz <= 32)
+        sort_emit(std::integral_constant<int, 1>{});
+      else if (sz <= 64)
+        sort_emit(std::integral_constant<int, 2>{});
+      else if (sz <= 128)
+        sort_emit(std::integral_constant<int, 4>{});
+      else
+        sort_emit(std::integral_constant<int, 8>{});
+    }
+    return true;
+  }
+
+  // Ranges: positions [r T, (r + 1) T) widened to whole buckets (fewer than
+  // T + maxb <= RANGE_MAX keys), taken by the CTAs in turn.
+  const int64_t room = RANGE_MAX - 1 - static_cast<int64_t>(maxb);
+  const int64_t m = (len + static_cast<int64_t>(G) * room - 1) / (static_cast<int64_t>(G) * room);
+  const int64_t T = (len + static_cast<int64_t>(G) * m - 1) / (static_cast<int64_t>(G) * m);
+  const int64_t nr = (len + T - 1) / T;
+  for (int64_t r = blockIdx.x; r < nr; r += G) {
+    if (threadIdx.x == 0) {
+      const int64_t plo = r * T, phi = plo + T < len ? plo + T : len;
+      sm.rlo = bucket_at(st, plo, len);
+      sm.rhi = bucket_at(st, phi, len);
+    }
+    __syncthreads();
+    const int64_t rs = sm.rlo, re = sm.rhi;
+    __syncthreads();
+    if (rs >= re || rs >= a.k) continue;
+    const int L = static_cast<int>(re - rs);
+    const int P = (L + 255) & ~255;  // zero keys pad the last run and sort last
+    unsigned long long* mbuf = s_keys + 2 * RS_SUB;
+    {
+      unsigned long long kv[RS_KMAX];  // P <= RS_SUB: at most RS_KMAX per thread, loaded together
+#pragma unroll
+      for (int r = 0; r < RS_KMAX; ++r) {
+        const int i = r * RS_THREADS + threadIdx.x;
+        kv[r] = i < L ? __ldcg(tmp_row + rs + i) : 0ull;
+      }
+#pragma unroll
+      for (int r = 0; r < RS_KMAX; ++r) {
+        const int i = r * RS_THREADS + threadIdx.x;
+        if (i < P) s_keys[i] = kv[r];
+      }
+    }
+    __syncthreads();
+    const unsigned long long* srt = block_merge_sort_desc(s_keys, mbuf, P);
+    for (int i = threadIdx.x; i < L; i += RS_THREADS)
+      if (rs + i < a.k) emit_key(a, row, rs + i, srt[i]);
+    __syncthreads();
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, SortCtl* ctl, unsigned long long* tmp,
-                                                          unsigned long long* flags, int64_t flag_stride) {
+                                                          unsigned long long* flags, int64_t flag_stride,
+                                                          unsigned* bk) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ unsigned long long s_keys[];  // 64 KB: a piece, its per-warp counts, or histograms
+  // 64 KB: a piece, its per-warp counts, or histograms; then 64 KB of bucket
+  // starts and a 64 KB merge buffer (the bucket stage).
+  extern __shared__ unsigned long long s_keys[];
   __shared__ Smem sm;
   const int row = launch_row(a.rows);
   const int64_t len = row_count(a, row);
@@ -382,17 +659,37 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
   unsigned target = 0;
   if (threadIdx.x == 0) sm.err = 0;
 
-  // 1. Histograms of all positions (and this chunk's flags zeroed).
+  unsigned* bkr = bk + static_cast<int64_t>(row) * 2 * BK;  // bucket counts, then cursors
+
+  // 1. Histograms of all positions (and this chunk's flags and share of the
+  // bucket counters zeroed).
   {
     unsigned(*h)[256] = reinterpret_cast<unsigned(*)[256]>(s_keys);
     for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS) (&h[0][0])[i] = 0;
     if (threadIdx.x < 256) fr[chunk * 256 + threadIdx.x] = 0;
+    for (int64_t i = chunk * RS_THREADS + threadIdx.x; i < 2 * BK; i += G * RS_THREADS) bkr[i] = 0;
     __syncthreads();
-    for (int64_t i = lo + threadIdx.x; i < lo + ((hi - lo + 31) & ~int64_t(31)); i += RS_THREADS) {
-      const bool valid = i < hi;
-      const unsigned long long key = valid ? __ldcg(a.keys + row * a.key_stride + i) : 0ull;
+    // Pieces of RS_SUB keys, RS_KMAX loads per thread issued together; a
+    // chunk of at most RS_SUB keys is also kept in shared memory (the merge
+    // buffer's place) for the bucket stage.
+    unsigned long long* cst = s_keys + 2 * RS_SUB;
+    for (int64_t b0 = lo; b0 < hi; b0 += RS_SUB) {
+      const int cnt = static_cast<int>(hi - b0 < RS_SUB ? hi - b0 : RS_SUB);
+      unsigned long long kv[RS_KMAX];
 #pragma unroll
-      for (int p = 0; p < 8; ++p) hist_add(h[p], digit_of(key, p), valid);
+      for (int r = 0; r < RS_KMAX; ++r) {
+        const int j = r * RS_THREADS + threadIdx.x;
+        kv[r] = j < cnt ? __ldcg(a.keys + row * a.key_stride + b0 + j) : 0ull;
+      }
+#pragma unroll
+      for (int r = 0; r < RS_KMAX; ++r) {
+        const int j = r * RS_THREADS + threadIdx.x;
+        if (r * RS_THREADS >= cnt) break;  // uniform across the block
+        const bool valid = j < cnt;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) hist_add(h[p], digit_of(kv[r], p), valid);
+        if (valid && hi - lo <= RS_SUB) cst[j] = kv[r];
+      }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS)
@@ -435,6 +732,13 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
     }
   }
   __syncthreads();
+
+  if (len >= BK_MIN_LEN && len < (int64_t(1) << 31) &&
+      bucket_stage(a, row, len, lo, hi, c, target, bkr, tmp + row * a.key_stride, sm, s_keys)) {
+    __syncthreads();
+    if (threadIdx.x == 0 && sm.err && a.st) atomicOr(&a.st[row].error, ERR_SORT_WAIT);
+    return;
+  }
 
   // When the value bytes allow fewer than len / RUN_MAX distinct values,
   // some value repeats more than RUN_MAX times: the full sort is certain to
@@ -537,6 +841,7 @@ struct Scratch {
   unsigned long long* flags;
   int64_t flag_stride;
   SortCtl* ctl;
+  unsigned* bk;  // per row: the bucket stage's counts and cursors (2 BK)
 };
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -559,6 +864,8 @@ Scratch carve(void* scratch, int64_t key_stride, int64_t rows) {
   s.flags = reinterpret_cast<unsigned long long*>(p);
   p += align256(sizeof(unsigned long long) * s.flag_stride * rows);
   s.ctl = reinterpret_cast<SortCtl*>(p);
+  p += align256(sizeof(SortCtl) * rows);
+  s.bk = reinterpret_cast<unsigned*>(p);
   return s;
 }
 
@@ -567,7 +874,7 @@ Scratch carve(void* scratch, int64_t key_stride, int64_t rows) {
 size_t radix_sort_scratch_bytes(int64_t key_stride, int64_t rows) {
   return align256(sizeof(unsigned long long) * key_stride * rows) +
          align256(sizeof(unsigned long long) * chunks_per_row(key_stride, 1) * 256 * rows) +
-         align256(sizeof(SortCtl) * rows);
+         align256(sizeof(SortCtl) * rows) + align256(sizeof(unsigned) * 2 * BK * rows);
 }
 
 void* radix_sort_ctl(void* scratch, int64_t key_stride, int64_t rows) { return carve(scratch, key_stride, rows).ctl; }
@@ -581,9 +888,9 @@ cudaError_t launch_radix_sort(const RadixSortArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   const unsigned G = static_cast<unsigned>(chunks_per_row(a.key_stride, a.nrows));
-  cudaFuncSetAttribute(k_rs_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(RS_SMEM));
-  launch_kernel(k_rs_sort, dim3(G, static_cast<unsigned>(a.nrows)), RS_THREADS, RS_SMEM, stream, a, s.ctl, s.tmp,
-                s.flags, s.flag_stride);
+  cudaFuncSetAttribute(k_rs_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(RS_SMEM_LAUNCH));
+  launch_kernel(k_rs_sort, dim3(G, static_cast<unsigned>(a.nrows)), RS_THREADS, RS_SMEM_LAUNCH, stream, a, s.ctl,
+                s.tmp, s.flags, s.flag_stride, s.bk);
   return cudaGetLastError();
 }
 
