@@ -61,7 +61,9 @@ struct SortCtl {
   unsigned long long start[8][256];  // digit counts of every position, over all chunks
   unsigned bar;                      // grid-barrier arrivals
   unsigned long_run;                 // 1: some run of equal values is longer than 32
-  unsigned pad[30];
+  unsigned long long kmax;           // the largest key
+  unsigned long long nkmax;          // the largest ~key (the smallest key, complemented)
+  unsigned pad[26];
 };
 static_assert(sizeof(SortCtl) % 16 == 0, "SortCtl is zeroed with 16-byte stores");
 
@@ -161,8 +163,11 @@ struct Smem {
   unsigned distinct[8];  // byte values present at each position
   unsigned nruns;  // runs of 2 .. RUN_MAX keys starting in this chunk
   int err;
-  unsigned boff[256];         // bucket stage: first bucket of each digit of the top position
-  unsigned char bbits[256];   // and the bits that split the digit into buckets
+  unsigned long long blo[256];  // bucket stage, per digit of the top position: the lowest bits below it,
+  unsigned boff[256];           // the digit's first bucket,
+  unsigned char bbits[256];     // log2 of its buckets
+  unsigned char bsh[256];       // and the shift of (low bits - blo) that gives the bucket
+  unsigned long long kmax, nkmax;
   unsigned nbuckets;
   unsigned bwsum[32];         // bucket stage: per-warp sums of the starts' scan
   unsigned bmax[32];          // and per-warp largest buckets
@@ -420,25 +425,38 @@ __device__ bool bucket_stage(const RadixSortArgs& a, int row, int64_t len, int64
   const unsigned G = gridDim.x;
   // Buckets in key order, sized from the data: the bytes above ps, the
   // highest position with more than one digit, are the same in every key;
-  // each digit d of position ps gets 2^b(d) buckets, split by the b(d) bits
-  // below it, with b(d) the least for which its c(d) keys average at most
+  // each digit d of position ps gets 2^b(d) buckets, equal parts of the range
+  // of the bits below it that its keys can take, with b(d) the least for
+  // which its c(d) keys average at most
   // ceil(len / 7500) per bucket (2^b(d) < 2 c(d) / that + 1, so fewer than
   // 15,256 in all).
   int ps = -1;
   for (int p = 7; p >= 0 && ps < 0; --p)
     if (!sm.trivial[p]) ps = p;
   if (ps < 0) ps = 0;  // a single key
+  const int pb = 8 * ps;
+  const unsigned long long lowmask = (1ull << pb) - 1ull;  // pb <= 56
   if (warp == 0) {
     const int64_t target = (len + 7499) / 7500;  // >= len / 7500, so the buckets number < 15,000 + 256
+    // The first and last digits hold keys only from the largest (smallest)
+    // key on: their buckets split that part of the digit, not all of it.
+    const unsigned long long nkmin = ~sm.kmax, nkmaxv = sm.nkmax;
+    const unsigned dfirst = static_cast<unsigned>(nkmin >> pb) & 255u, dlast = static_cast<unsigned>(nkmaxv >> pb) & 255u;
     unsigned nb[8], tot = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int d = lane * 8 + j;
       const int64_t c = static_cast<int64_t>((d < 255 ? sm.start[ps][d + 1] : static_cast<unsigned long long>(len)) -
                                              sm.start[ps][d]);
+      const unsigned long long blo = d == static_cast<int>(dfirst) ? (nkmin & lowmask) : 0ull;
+      const unsigned long long bhi = d == static_cast<int>(dlast) ? (nkmaxv & lowmask) : lowmask;
+      const unsigned long long span = bhi >= blo ? bhi - blo : 0ull;
+      const int wbits = span ? 64 - __clzll(span) : 0;  // (low - blo) < 2^wbits
       int b = 0;
-      while (b < BK_BITS && b < 8 * ps && (static_cast<int64_t>(1) << b) * target < c) ++b;
+      while (b < BK_BITS && b < wbits && (static_cast<int64_t>(1) << b) * target < c) ++b;
       sm.bbits[d] = static_cast<unsigned char>(b);
+      sm.bsh[d] = static_cast<unsigned char>(wbits - b);
+      sm.blo[d] = blo;
       nb[j] = 1u << b;
       tot += nb[j];
     }
@@ -457,12 +475,10 @@ __device__ bool bucket_stage(const RadixSortArgs& a, int row, int64_t len, int64
   }
   __syncthreads();
   if (sm.nbuckets > static_cast<unsigned>(BK)) return false;  // (not reached, see above)
-  const int pb = 8 * ps;
   auto bucket_of = [&](unsigned long long kk) {
     const unsigned long long nk = ~kk;
     const unsigned d = static_cast<unsigned>(nk >> pb) & 255u;
-    const int b = sm.bbits[d];
-    return sm.boff[d] + (b ? static_cast<unsigned>(nk >> (pb - b)) & ((1u << b) - 1u) : 0u);
+    return sm.boff[d] + (sm.bbits[d] ? static_cast<unsigned>(((nk & lowmask) - sm.blo[d]) >> sm.bsh[d]) : 0u);
   };
   unsigned* h = reinterpret_cast<unsigned*>(s_keys);            // the chunk's counts, then its cursors
   unsigned* st = reinterpret_cast<unsigned*>(s_keys + RS_SUB);  // every bucket's start in the row
@@ -668,7 +684,9 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
     for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS) (&h[0][0])[i] = 0;
     if (threadIdx.x < 256) fr[chunk * 256 + threadIdx.x] = 0;
     for (int64_t i = chunk * RS_THREADS + threadIdx.x; i < 2 * BK; i += G * RS_THREADS) bkr[i] = 0;
+    if (threadIdx.x == 0) sm.kmax = sm.nkmax = 0;
     __syncthreads();
+    unsigned long long kmx = 0, nkmx = 0;
     // Pieces of RS_SUB keys, RS_KMAX loads per thread issued together; a
     // chunk of at most RS_SUB keys is also kept in shared memory (the merge
     // buffer's place) for the bucket stage.
@@ -688,16 +706,38 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
         const bool valid = j < cnt;
 #pragma unroll
         for (int p = 0; p < 8; ++p) hist_add(h[p], digit_of(kv[r], p), valid);
-        if (valid && hi - lo <= RS_SUB) cst[j] = kv[r];
+        if (valid) {
+          kmx = kv[r] > kmx ? kv[r] : kmx;
+          nkmx = ~kv[r] > nkmx ? ~kv[r] : nkmx;
+          if (hi - lo <= RS_SUB) cst[j] = kv[r];
+        }
       }
     }
+    // The chunk's largest key and largest ~key, then the row's (one atomic each).
+    for (int o = 16; o >= 1; o >>= 1) {
+      const unsigned long long t1 = __shfl_xor_sync(FULL_MASK, kmx, o), t2 = __shfl_xor_sync(FULL_MASK, nkmx, o);
+      kmx = t1 > kmx ? t1 : kmx;
+      nkmx = t2 > nkmx ? t2 : nkmx;
+    }
+    if ((threadIdx.x & 31) == 0 && kmx) {
+      atomicMax(&sm.kmax, kmx);
+      atomicMax(&sm.nkmax, nkmx);
+    }
     __syncthreads();
+    if (threadIdx.x == 0 && sm.kmax) {
+      atomicMax(&c.kmax, sm.kmax);
+      atomicMax(&c.nkmax, sm.nkmax);
+    }
     for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS)
       if ((&h[0][0])[i]) atomicAdd(&c.start[0][0] + i, static_cast<unsigned long long>((&h[0][0])[i]));
   }
   grid_sync(c, target += G, sm);
   // The plan, the same in every CTA.
   if (threadIdx.x < 8) sm.trivial[threadIdx.x] = 0;
+  if (threadIdx.x == 0) {
+    sm.kmax = __ldcg(&c.kmax);
+    sm.nkmax = __ldcg(&c.nkmax);
+  }
   __syncthreads();
   for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS) {
     const unsigned long long v = __ldcg(&c.start[0][0] + i);
