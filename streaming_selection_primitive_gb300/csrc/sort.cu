@@ -657,7 +657,11 @@ __device__ bool bucket_stage(const RadixSortArgs& a, int row, int64_t len, int64
 __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, SortCtl* ctl, unsigned long long* tmp,
                                                           unsigned long long* flags, int64_t flag_stride,
                                                           unsigned* bk) {
-  pdl_trigger();
+  // No early trigger: the next kernels of the stream launch when this one has
+  // finished.  Triggered at the start, they took SMs as this kernel's CTAs
+  // left them, and with calls in flight back to back that cost about 80 us
+  // per call at k = 2^17 .. 2^19 (measured); the kernel after a sort is the
+  // small report, so nothing is lost by waiting.
   pdl_wait();
   // 64 KB: a piece, its per-warp counts, or histograms; then 64 KB of bucket
   // starts and a 64 KB merge buffer (the bucket stage).
