@@ -63,7 +63,8 @@ typedef enum profk_path {
   PROFK_PATH_TIE = 1,       /* R > M but R_gt < k: tau is the k-th largest value; the
                                library emits x > tau plus the lowest-index copies of tau */
   PROFK_PATH_FALLBACK = 2,  /* every attempt failed: exact selection over the row */
-  PROFK_PATH_EXACT = 3      /* no sampling (S > n/8 or k > n/64): exact selection */
+  PROFK_PATH_EXACT = 3      /* no sampling (S > n/8, or t = S or M = n: k too close
+                               to n for the budget): exact selection */
 } profk_path;
 
 /* Per-row report.  Counts of attempts that did not run are -1. */

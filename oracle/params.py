@@ -292,17 +292,22 @@ def params(N: int, k: int, eps: float, mode: int = MODE_DEFAULT):
     return S, t, M
 
 
-def uses_filter(N: int, k: int, S: int, rows: int = 1) -> bool:
-    """Route: sample-and-filter only when S <= N/8 and k <= N/64, and, in calls
-    of 128 or more rows with k <= 2048, only when S < N/32.
+def uses_filter(N: int, k: int, S: int, t: int, M: int, rows: int = 1) -> bool:
+    """Route: sample-and-filter when the sample is at most N/8 and the
+    parameters can meet the budget (t < S and M < N: at t = S or M = N the
+    rules were clamped, which happens as k approaches N), and, in calls of
+    128 or more rows with k <= 2048, only when S < N/32.  Otherwise the exact
+    path runs.
 
-    Otherwise sampling buys nothing (the corrected paper's Appendix B keeps the
-    floor sample size once k/N exceeds about 2^-10, and a sample that is a
-    sizable share of the input is itself a full pass); the exact path runs.
+    A sample that is a sizable share of the input is itself a full pass.  The
+    corrected paper keeps the method, at the floor sample size, for dense k
+    (Appendix B: "the floor is again the best choice" once k/N exceeds about
+    2^-10), and so does this rule: no cut on k/N (an earlier cut at k > N/64
+    measured 4-6 times slower on GB300 than sampling for k/N = 1/32 .. 1/8).
     The rows clause is a choice of this implementation, not of the pages:
     with many short rows, drawing 1/32 of every row by random access costs
     more than an exact selection of each row by one CTA.
     """
-    if 8 * S > N or 64 * k > N:
+    if 8 * S > N or t >= S or M >= N:
         return False
     return not (rows >= 128 and 32 * S >= N and k <= 2048)

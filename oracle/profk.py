@@ -112,7 +112,7 @@ def profk(x: np.ndarray, k: int, eps: float, seed: int, row: int = 0, *, max_att
             t, M = P.params_fast(N, k, S, eps)
         t, M = force.get("t", t), force.get("M", M)
     st.S, st.t, st.M = S, t, M
-    if not P.uses_filter(N, k, S, rows) and not force:
+    if not P.uses_filter(N, k, S, t, M, rows) and not force:
         st.path = PATH_EXACT
         v, i = topk_sort(x, k)
         return v, i, st

@@ -684,7 +684,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   if (fM > 0) P.M = std::min<int64_t>(std::max<int64_t>(fM, k), n);
   if (forced && 2 * P.S > n) return PROFK_ERR_INVALID;
 
-  const bool sampling = forced ? true : uses_filter(n, k, P.S, rows);
+  const bool sampling = forced ? true : uses_filter(P, n, k, rows);
   std::vector<profk_stats> st_host(static_cast<size_t>(rows));
   for (auto& s : st_host) fill_stats_params(&s, P);
 
@@ -994,7 +994,7 @@ int submit_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
                      g_opt[PROFK_OPT_FORCE_M].load() == 0 && g_opt[PROFK_OPT_TIMING].load() == 0 &&
                      g_opt[PROFK_OPT_MAX_ATTEMPTS].load() > 0 && t_user_ws == nullptr && n <= max_segment();
   const Params P = cached_params(n, k, eps / static_cast<double>(rows), mode);
-  if (!plain || !uses_filter(n, k, P.S, rows)) {
+  if (!plain || !uses_filter(P, n, k, rows)) {
     // Options, routes and caller workspaces outside the asynchronous form:
     // the call runs now; profk_wait returns its result.
     call->status = run_topk(x, rows, n, ld, k, eps, seed, out_vals, out_idx, stream, call->stats.data());
@@ -1142,7 +1142,7 @@ namespace profk {
 namespace {
 size_t layout_bytes(int64_t rows, int64_t n, int64_t k, double eps) {
   const Params P = cached_params(n, k, eps / static_cast<double>(rows), static_cast<int>(g_opt[0].load()));
-  const bool sampling = uses_filter(n, k, P.S, rows);
+  const bool sampling = uses_filter(P, n, k, rows);
   return make_layout(rows, n, k, P.S, sampling ? draw_budget(n, P.S) : 0, P.M, sampling).total;
 }
 }  // namespace

@@ -117,7 +117,7 @@ extern "C" int profk_topk_noalloc(const float* x, int64_t n, int64_t k, double e
   const int64_t max_attempts = profk_get_option(PROFK_OPT_MAX_ATTEMPTS);
   const bool tie_exit = profk_get_option(PROFK_OPT_TIE_EXIT) != 0;
   const Params P = compute_params(n, k, eps, mode);
-  const bool sampling = uses_filter(n, k, P.S);
+  const bool sampling = uses_filter(P, n, k);
   int64_t D = sampling ? draws_for(n, P.S) : 0;
   ScratchLayout L = plan(P.S, D, P.M, k, sampling);
   if (L.total > PROFK_NOALLOC_SCRATCH_BYTES) return PROFK_ERR_SCRATCH;

@@ -21,8 +21,8 @@ void exact_params(int64_t n, int64_t k, int64_t S, double eps, int64_t* t, int64
 // mode 2: S as in mode 0 with the exact t and M of Theorem 4,
 // mode 3: the corrected Algorithm 1 throughout (its own sample size).
 Params compute_params(int64_t n, int64_t k, double eps, int mode);
-// Sampling pays off only when S <= n/8 and k <= n/64, and, for calls of 128
-// or more rows with k <= 2048, only when S < n/32; otherwise the exact path runs.
-bool uses_filter(int64_t n, int64_t k, int64_t S, int64_t rows = 1);
+// Sample-and-filter when S <= n/8, t < S and M < n, and, for calls of 128 or
+// more rows with k <= 2048, only when S < n/32; otherwise the exact path runs.
+bool uses_filter(const Params& P, int64_t n, int64_t k, int64_t rows = 1);
 
 }  // namespace profk

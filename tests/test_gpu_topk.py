@@ -89,6 +89,18 @@ def test_exact_route_small_inputs(pk, cuda_device):
         assert_same(vals, idx, *topk_sort(x.cpu().numpy(), k), f"exact route n={n} k={k}")
 
 
+@pytest.mark.parametrize("n,k", [((1 << 22) + 8, 1 << 17), (1 << 22, 1 << 20), (1 << 21, (1 << 21) - 3),
+                                 (1_000_003, 400_000)])
+def test_dense_k(pk, cuda_device, n, k):
+    """k a large share of the row: the filter path while its parameters can
+    meet the budget (here k/n = 1/32, 1/4 and 0.4), the exact path when k
+    nearly equals n; every statistic as the oracle procedure predicts."""
+    x = workloads.normal(n, 17, cuda_device)
+    st = check_call(pk, x, k, 1e-3, 8)
+    S, t, M = PP.params(n, k, 1e-3)
+    assert st["path"] == (pk.PATH_FILTER if PP.uses_filter(n, k, S, t, M) else pk.PATH_EXACT)
+
+
 def test_nan_rejected(pk, cuda_device):
     x = workloads.normal(1 << 20, 3, cuda_device)
     x[12345] = float("nan")
@@ -277,8 +289,8 @@ def test_batched_many_rows(pk, cuda_device, rows, n, k):
         h = x[r].cpu().numpy()
         assert_same(vals[r], idx[r], *topk_sort(h, k), f"row {r}")
     paths = {s["path"] for s in sts}
-    S = sts[0]["S"]
-    assert paths == ({pk.PATH_FILTER} if PP.uses_filter(n, k, S, rows) else {pk.PATH_EXACT})
+    S, t, M = sts[0]["S"], sts[0]["t"], sts[0]["M"]
+    assert paths == ({pk.PATH_FILTER} if PP.uses_filter(n, k, S, t, M, rows) else {pk.PATH_EXACT})
 
 
 def test_exact_parameter_mode(pk, cuda_device):

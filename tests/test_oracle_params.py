@@ -147,25 +147,37 @@ def test_older_rule_literal_and_its_budget():
 
 def test_default_rule_invariants():
     for N in (2**20, 2**22, 2**26, 2**30, 50331648, 2**32):
-        for k in (1, 2, 32, 1024, 4096, 2**19):
-            if k * 64 > N:
+        for k in (1, 2, 32, 1024, 4096, 2**19, N // 64, N // 16, N // 4):
+            if k > N:
                 continue
             S, t, M = P.params(N, k, 1e-3)
             assert 32768 <= S <= 131072 and 1 <= t <= S and k <= M <= N
-            if P.uses_filter(N, k, S):
+            if P.uses_filter(N, k, S, t, M) and N <= 2**26:
+                # every configuration the filter path takes meets the budget
+                # (exact Propositions 2-3; kept to N <= 2^26 for the CPU's time)
                 assert P.prob_fail(N, k, S, t, M) <= 1e-3
 
 
+def route(N, k, rows=1, eps=1e-3):
+    S, t, M = P.params(N, k, eps / rows)
+    return P.uses_filter(N, k, S, t, M, rows)
+
+
 def test_route():
-    # The pages' clauses: a sample of more than 1/8 of the row, or k above
-    # 1/64 of it, takes the exact path.
-    assert P.uses_filter(2**20, 64, 32768) and P.uses_filter(2**18, 64, 32768)
-    assert not P.uses_filter(2**18 - 1, 64, 32768) and not P.uses_filter(2**20, 2**14 + 1, 32768)
+    # A sample of more than 1/8 of the row takes the exact path.
+    assert route(2**20, 64) and route(2**18, 64)
+    assert not route(2**18 - 4, 64)
+    # Dense k stays on the filter path (no cut on k / N) ...
+    assert route(2**20, 2**14 + 1) and route(2**24, 2**21) and route(2**26, 2**24)
+    # ... until the rules clamp t to S or M to N, as k approaches N.
+    assert not route(2**20, 2**20 - 5) and not route(2**20, 2**20)
+    S, t, M = P.params(2**20, 2**20 - 5, 1e-3)
+    assert t == S or M == 2**20
     # Calls of 128 or more rows with k <= 2048: only samples below 1/32 of a row.
-    assert P.uses_filter(2**20, 64, 32768, rows=127) and not P.uses_filter(2**20, 64, 32768, rows=128)
-    assert P.uses_filter(2**20 + 4, 2048, 32768, rows=1024) and not P.uses_filter(2**20, 2048, 32768, rows=1024)
-    assert P.uses_filter(2**20, 2049, 32768, rows=1024)
-    assert P.uses_filter(2**24, 32, 32768, rows=64) and P.uses_filter(2**24, 32, 32768, rows=4096)
+    assert route(2**20, 64, rows=127) and not route(2**20, 64, rows=128)
+    assert route(2**20 + 4, 2048, rows=1024) and not route(2**20, 2048, rows=1024)
+    assert route(2**20, 2049, rows=1024)
+    assert route(2**24, 32, rows=64) and route(2**24, 32, rows=4096)
 
 @pytest.mark.parametrize("r", ROWS, ids=lambda r: f"N2^{int(math.log2(r['N']))}-k2^{int(math.log2(r['k']))}")
 def test_table3_sample_size_column(r):
