@@ -137,8 +137,9 @@ int profk_topk_batched(const float* x, int64_t rows, int64_t n, int64_t ld, int6
  * and returns at once with *call set; profk_wait(call, stats) then completes
  * it: it waits for those counts (not for the stream), and if every row
  * passed the check the outputs are final and stream-ordered; otherwise (a
- * redraw, the tie exit, the fallback, a NaN) it runs the whole call again
- * synchronously, with the same result and statistics as profk_topk.  Calls
+ * redraw, the tie exit, the fallback, a NaN) it continues synchronously from
+ * that first attempt, in the call's workspace, with the same result and
+ * statistics as profk_topk.  Calls
  * with non-default options (forced parameters, timing, no attempts), those
  * routed to the exact path, and those made while a caller workspace is set
  * run synchronously at submission instead.  Each call owns its workspace, so

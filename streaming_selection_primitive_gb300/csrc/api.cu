@@ -560,8 +560,22 @@ cudaError_t enqueue_report(const RowState* st, int64_t rows, char* rep, unsigned
                            stream);
 }
 
+// The state an asynchronous call hands to the synchronous loop when its first
+// attempt did not clear the check: the workspace that attempt used (its layout
+// is run_topk's for the same arguments), its parameters and its report (the
+// heads of every row's state).  The loop continues from there instead of
+// repeating the attempt.
+struct Resume {
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  const char* report = nullptr;
+  Params P{};
+  int64_t launches = 0;  // kernels the first attempt launched
+};
+
 int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,
-             float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_stats* stats);
+             float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_stats* stats,
+             const Resume* resume = nullptr);
 
 // Rows longer than max_segment(): each row is split into segments (see
 // plan_segments), the segments' exact top-k lists are selected by the batched
@@ -656,7 +670,7 @@ int run_long_rows(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k
 }
 
 int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,
-             float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_stats* stats) {
+             float* out_vals, int64_t* out_idx, cudaStream_t stream, profk_stats* stats, const Resume* resume) {
   if (!x || !out_vals || !out_idx) return PROFK_ERR_INVALID;
   if (rows < 1 || n < 1 || k < 1 || k > n || ld < n || !(eps > 0.0 && eps < 1.0)) return PROFK_ERR_INVALID;
   if (rows > (1 << 20)) return PROFK_ERR_INVALID;
@@ -683,8 +697,9 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   if (ft > 0) P.t = std::min<int64_t>(ft, P.S);
   if (fM > 0) P.M = std::min<int64_t>(std::max<int64_t>(fM, k), n);
   if (forced && 2 * P.S > n) return PROFK_ERR_INVALID;
+  if (resume) P = resume->P;
 
-  const bool sampling = forced ? true : uses_filter(P, n, k, rows);
+  const bool sampling = resume || forced ? true : uses_filter(P, n, k, rows);
   std::vector<profk_stats> st_host(static_cast<size_t>(rows));
   for (auto& s : st_host) fill_stats_params(&s, P);
 
@@ -695,12 +710,18 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   int64_t D = sampling ? draw_budget(n, P.S) : 0;
   Layout L = make_layout(rows, n, k, P.S, D, P.M, sampling);
   std::vector<int> pending, fallback, attempt(static_cast<size_t>(rows), 0);
-  bool exact_ran = false, tie_ran = false, first_filter = true;
+  bool exact_ran = false, tie_ran = false, first_filter = true, resume_used = false;
   float filter_ms = -1.f;
   void* hbuf = nullptr;
   RowState* st = nullptr;
 
-  PK_CHECK(ws_alloc(c, L.total, true));
+  if (resume) {  // the first attempt's workspace, freed at the end like our own
+    c.ws = resume->ws;
+    c.ws_bytes = resume->ws_bytes;
+    c.ws_user = false;
+  } else {
+    PK_CHECK(ws_alloc(c, L.total, true));
+  }
   st = at<RowState>(c.ws, L.off_state);
   // The sampling path starts every attempt with k_attempt_reset, which
   // initialises the state of its rows; the exact path needs zeroed state.
@@ -730,14 +751,21 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
     }
     const int ng = static_cast<int>(group.size());
     int* gl = nullptr;
-    PK_CHECK(upload_rows(L, c.ws, hbuf, 0, group, stream, &gl));
+    // The first attempt of all rows already ran (asynchronous call): take its report.
+    const bool resumed = resume && !resume_used && a == 0 && static_cast<int64_t>(ng) == rows;
+    if (!resumed) PK_CHECK(upload_rows(L, c.ws, hbuf, 0, group, stream, &gl));
     {
-      const bool time_it = timing && first_filter;
+      const bool time_it = timing && first_filter && !resumed;
       if (time_it) {
         if (!t_events.e[0])
           for (auto& ev : t_events.e) PK_CHECK(cudaEventCreate(&ev));
         PK_CHECK(cudaEventRecord(t_events.e[0], stream));
       }
+      char* rep = static_cast<char*>(hbuf) + sizeof(int) * rows * 4;
+      if (resumed) {
+        std::memcpy(rep, resume->report, REPORT_BYTES * rows);
+        resume_used = true;
+      } else {
       PK_CHECK(enqueue_attempt(L, c.ws, P, a, ng, gl, rows, x, ld, n, k, seed, cps, out_vals, out_idx, stream,
                                time_it ? t_events.e : nullptr));
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[4], stream));
@@ -745,7 +773,6 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
       // Run-time check: read the exact counts of every row (written into
       // pinned memory by a kernel and waited for, or copied and synchronized
       // for many rows).
-      char* rep = static_cast<char*>(hbuf) + sizeof(int) * rows * 4;
       {
         unsigned long long* flag =
             reinterpret_cast<unsigned long long*>(align_up(reinterpret_cast<uintptr_t>(rep + REPORT_BYTES * rows)));
@@ -758,6 +785,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         } else {
           PK_CHECK(cudaStreamSynchronize(stream));
         }
+      }
       }
       if (time_it) {
         PK_CHECK(cudaEventElapsedTime(&filter_ms, t_events.e[2], t_events.e[3]));
@@ -889,7 +917,7 @@ done:
       st_host[r].aux_bytes = c.ws_bytes;
       st_host[r].filter_ms = filter_ms;
       st_host[r].cuda_error = static_cast<int32_t>(c.err);
-      st_host[r].launches = static_cast<int32_t>(launch_count() - launches0);
+      st_host[r].launches = static_cast<int32_t>(launch_count() - launches0 + (resume ? resume->launches : 0));
       stats[r] = st_host[r];
     }
   }
@@ -1071,19 +1099,32 @@ int finish_async(profk_call* call, profk_stats* stats) {
         s.launches = static_cast<int32_t>(call->launches);
       }
     }
-    cudaFreeAsync(call->ws, call->stream);
-    call->ws = nullptr;
     if (call->copied) cudaEventDestroy(call->copied);
-    give_block(call->host, call->host_bytes);
-    call->host = nullptr;
     if (clear) {
+      cudaFreeAsync(call->ws, call->stream);
       status = PROFK_OK;
+    } else if (e == cudaSuccess) {
+      // Not cleared (a redraw, the tie exit, the fallback, NaN, a device
+      // error): the synchronous loop continues from this first attempt, in
+      // its workspace (which it frees), with the same result and statistics
+      // as profk_topk.
+      Resume rs;
+      rs.ws = call->ws;
+      rs.ws_bytes = call->ws_bytes;
+      rs.report = call->host;
+      rs.P = call->P;
+      rs.launches = call->launches;
+      status = run_topk(call->x, call->rows, call->n, call->ld, call->k, call->eps, call->seed, call->out_vals,
+                        call->out_idx, call->stream, call->stats.data(), &rs);
     } else {
-      // Not cleared (a redraw, the tie exit, the fallback, NaN, an error):
-      // the whole call again, synchronously.
+      // The report never came: the whole call again, synchronously.
+      cudaFreeAsync(call->ws, call->stream);
       status = run_topk(call->x, call->rows, call->n, call->ld, call->k, call->eps, call->seed, call->out_vals,
                         call->out_idx, call->stream, call->stats.data());
     }
+    call->ws = nullptr;
+    give_block(call->host, call->host_bytes);
+    call->host = nullptr;
   }
   if (stats)
     for (int64_t r = 0; r < call->rows; ++r) stats[r] = call->stats[static_cast<size_t>(r)];

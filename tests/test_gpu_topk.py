@@ -346,6 +346,38 @@ def test_async_rerun_when_not_cleared(pk, cuda_device):
         assert st["path"] == ost.path and st["attempts"] == ost.attempts
 
 
+def test_async_resumes_redraws(pk, cuda_device):
+    # eps = 0.5: many first attempts fail the check; the asynchronous call
+    # continues from its first attempt (redraw, then the filter again) and
+    # must end exactly as the synchronous call: result and every statistic.
+    x = workloads.normal((1 << 20) + 4, 23, cuda_device)
+    redraws = 0
+    for seed in range(12):
+        ref = pk.topk(x, 300, 0.5, seed)
+        v, i, st = pk.topk_async(x, 300, 0.5, seed).wait()
+        assert torch.equal(v, ref[0]) and torch.equal(i, ref[1])
+        assert all(st[key] == ref[2][key] for key in STAT_KEYS + ("R_gt_final",)), (seed, st, ref[2])
+        redraws += st["attempts"] > 1
+    assert redraws > 0  # the resumed path was taken
+
+
+def test_async_batched_mixed_rows(pk, cuda_device):
+    # Rows that clear the check in the first attempt and tie rows that take
+    # the tie exit after it, in one asynchronous call.
+    n = 1 << 19
+    x = torch.empty((4, n), dtype=torch.float32, device=cuda_device)
+    x[0] = workloads.normal(n, 1, cuda_device)
+    x[1] = workloads.levels16(n, 2, cuda_device)
+    x[2] = workloads.normal(n, 3, cuda_device)
+    x[3] = workloads.levels16(n, 4, cuda_device)
+    ref = pk.topk_batched(x, 700, 1e-3, 9)
+    v, i, sts = pk.topk_batched_async(x, 700, 1e-3, 9).wait()
+    assert torch.equal(v, ref[0]) and torch.equal(i, ref[1])
+    for a, b in zip(sts, ref[2]):
+        assert all(a[key] == b[key] for key in STAT_KEYS), (a, b)
+    assert {s["path"] for s in sts} == {pk.PATH_FILTER, pk.PATH_TIE}
+
+
 def test_async_nan(pk, cuda_device):
     x = workloads.normal(1 << 20, 3, cuda_device)
     x[777] = float("nan")
