@@ -308,10 +308,9 @@ Layout make_layout(int64_t rows, int64_t n, int64_t k, int64_t S, int64_t D, int
   off = align_up(off + sort_bytes);
   L.off_refine = off;
   if (sampling && !L.radix_refine) off = align_up(off + refine_grid_scratch_bytes(rows));
-  L.off_tie = off;  // tie exit: control blocks, block counts and their prefixes
-  if (sampling)
-    off = align_up(off + align_up(tie_ctl_bytes() * rows) + align_up(sizeof(unsigned) * tie_blocks(n) * rows) +
-                   sizeof(unsigned long long) * tie_blocks(n) * rows);
+  L.off_tie = off;  // tie exit and exact path: control blocks, block counts and their prefixes
+  off = align_up(off + align_up(tie_ctl_bytes() * rows) + align_up(sizeof(unsigned) * tie_blocks(n) * rows) +
+                 sizeof(unsigned long long) * tie_blocks(n) * rows);
   L.total = off;
   return L;
 }
@@ -438,7 +437,28 @@ cudaError_t upload_rows(const Layout& L, void* ws, void* hbuf, int slot, const s
   return cudaMemcpyAsync(d, hs, sizeof(int) * rows.size(), cudaMemcpyHostToDevice, stream);
 }
 
-// Exact selection over whole rows (fallback / exact path).
+__global__ void k_exact_to_tie(RowState* st, const int* rows) {
+  pdl_trigger();
+  pdl_wait();
+  const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
+  if (threadIdx.x == 0) st[row].R_gt = st[row].sel_above;  // |{x > v_k}|, below k
+}
+
+int filter_grid(int64_t ctas_per_sm);
+
+// Rows from which the exact path goes through the value selection and the
+// tie step (measured: 430 vs 668 us at n = 2^26; below 2^25 the selection of
+// the 64-bit keys, which stops as soon as its bucket is exactly the rest of
+// the top k, is faster: 51 vs 78 us at 2^18, 154 vs 212 us at 2^24).
+constexpr int64_t EXACT_TIE_MIN_N = int64_t(1) << 25;
+
+// Exact selection over whole rows (fallback / exact path).  Many short rows:
+// one CTA per row.  Long rows: the k-th largest VALUE v_k by three radix
+// passes over the row's value keys (11, 11 and 10 bits), which also count
+// the x > v_k; then the tie step takes every x > v_k and the lowest-index
+// copies of v_k (one streaming pass and a re-read up to the last copy taken),
+// and the k keys are sorted: five reads of the row in all.  Other rows: the
+// radix selection of the 64-bit (value, index) keys, a compaction and the sort.
 void launch_exact(const Layout& L, void* ws, const float* x, int64_t ld, int nrows, const int* rows,
                   float* out_vals, int64_t* out_idx, cudaStream_t stream) {
   RowState* st = at<RowState>(ws, L.off_state);
@@ -449,8 +469,21 @@ void launch_exact(const Layout& L, void* ws, const float* x, int64_t ld, int nro
   }
   unsigned long long* sel = at<unsigned long long>(ws, L.off_sel);
   SelectArgs a{KeySource::Input, x, ld, L.n, nrows, rows, st};
-  launch_select(a, static_cast<uint64_t>(L.k), false, 0, stream);
-  launch_compact(a, reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, stream);
+  if (aligned && L.n >= EXACT_TIE_MIN_N) {
+    launch_select(a, static_cast<uint64_t>(L.k), true, 0, stream);  // value only; leaves tau_key = v_k
+    launch_kernel(k_exact_to_tie, nrows, 32, 0, stream, st, rows);
+    char* tw = at<char>(ws, L.off_tie);
+    const int64_t nb = tie_blocks(L.n);
+    TieArgs ta{x, ld, L.n, nrows, rows, st, sel, L.kstride, L.k,
+               reinterpret_cast<unsigned*>(tw + align_up(tie_ctl_bytes() * L.rows)),
+               reinterpret_cast<unsigned long long*>(tw + align_up(tie_ctl_bytes() * L.rows) +
+                                                     align_up(sizeof(unsigned) * nb * L.rows)),
+               nb, reinterpret_cast<TieCtl*>(tw), L.rows};
+    launch_tie_take(ta, filter_grid(0), stream);
+  } else {
+    launch_select(a, static_cast<uint64_t>(L.k), false, 0, stream);
+    launch_compact(a, reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, stream);
+  }
   launch_sort_emit(reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, nrows, rows, x, ld, L.n, out_vals, out_idx, stream,
                    st, at<char>(ws, L.off_sort), L.rows);
 }

@@ -127,3 +127,14 @@ def test_exact_rejects_nan(pk, cuda_device):
     with pytest.raises(pk.ProfkError) as e:
         pk.exact(x, 10)
     assert e.value.code == -3
+
+
+def test_exact_unaligned_input(pk, cuda_device):
+    """profk_exact on a row that does not start on a 16-byte boundary: the
+    selection reads it element by element and the result is the same."""
+    base = workloads.normal((1 << 20) + 8, 41, cuda_device)
+    x = base[1:(1 << 20) + 1]  # 4 bytes past an aligned start
+    assert x.data_ptr() % 16 == 4
+    for k in (10, 5000):
+        vals, idx = pk.exact(x, k)
+        assert_same(vals, idx, *topk_sort(x.cpu().numpy(), k), f"unaligned exact k={k}")
