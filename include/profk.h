@@ -214,8 +214,19 @@ typedef enum profk_option {
   PROFK_OPT_PDL = 8,           /* launch kernels with programmatic dependent launch [1] */
   PROFK_OPT_MAX_SEGMENT = 9,   /* rows longer than this are split into segments (see profk_topk);
                                   a multiple of 4, >= 2^16; 0 = 2^32 [0] */
-  PROFK_OPT__COUNT = 10
+  PROFK_OPT_SAMPLER = 10,      /* kernels of steps 1-2 (sample and tau): PROFK_SAMPLER_AUTO [0],
+                                  _GRID or _STEPS (GRID falls back to the automatic choice
+                                  where it cannot take the problem) */
+  PROFK_OPT__COUNT = 11
 } profk_option;
+/* Forms of the sampling kernels (PROFK_OPT_SAMPLER); both give the same
+ * sample and tau.  GRID: one persistent kernel whose CTAs (all resident) meet
+ * at grid barriers; taken when each CTA's share of the draws fits its
+ * registers or shared memory.  STEPS: barrier-free kernels, one per step,
+ * then a radix selection of tau; taken otherwise. */
+#define PROFK_SAMPLER_AUTO 0
+#define PROFK_SAMPLER_GRID 1
+#define PROFK_SAMPLER_STEPS 2
 int profk_set_option(int option, int64_t value);
 int64_t profk_get_option(int option);
 

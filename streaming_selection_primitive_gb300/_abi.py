@@ -26,7 +26,9 @@ OPT_TIMING = 6
 OPT_FILTER_CTAS_PER_SM = 7
 OPT_PDL = 8
 OPT_MAX_SEGMENT = 9
-OPT_DEFAULTS = {0: 0, 1: 6, 2: 1, 3: 0, 4: 0, 5: 0, 6: 0, 7: 0, 8: 1, 9: 0}
+OPT_SAMPLER = 10
+SAMPLER_AUTO, SAMPLER_GRID, SAMPLER_STEPS = 0, 1, 2
+OPT_DEFAULTS = {0: 0, 1: 6, 2: 1, 3: 0, 4: 0, 5: 0, 6: 0, 7: 0, 8: 1, 9: 0, 10: 0}
 
 
 class ProfkStats(C.Structure):

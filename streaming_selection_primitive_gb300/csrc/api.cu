@@ -28,7 +28,7 @@ namespace {
 // ---------------------------------------------------------------------------
 // Options.
 std::atomic<int64_t> g_opt[PROFK_OPT__COUNT] = {
-    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}, {1}, {0}};
+    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}, {1}, {0}, {PROFK_SAMPLER_AUTO}};
 
 // Longest row handled as one (PROFK_OPT_MAX_SEGMENT; 0 = 2^32, the reach of a
 // candidate key's 32-bit index field).  Longer rows are split into segments.
@@ -520,6 +520,16 @@ void fill_stats_params(profk_stats* s, const Params& P) {
 }
 
 
+// Kernels of steps 1-2 for ng rows of D draws each: the step-by-step ones
+// when PROFK_OPT_SAMPLER asks for them, else the persistent grid kernel
+// where its CTAs' shares of the draws fit, else the step-by-step ones.
+enum class Sampler { Grid, Steps };
+
+Sampler choose_sampler(int64_t D, int64_t ng, uint64_t n) {
+  if (g_opt[PROFK_OPT_SAMPLER].load() == PROFK_SAMPLER_STEPS) return Sampler::Steps;
+  return sample_tau_fits(D, static_cast<int>(ng), n) ? Sampler::Grid : Sampler::Steps;
+}
+
 // One attempt of the listed rows (gl, ng of them; all rows when gl is null):
 // reset, sampling and tau, filter, and the refinement, which is enqueued
 // before the host has seen the counts (a row whose count fails the check is
@@ -530,7 +540,9 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
                             const float* x, int64_t ld, int64_t n, int64_t k, uint64_t seed, int64_t cps,
                             float* out_vals, int64_t* out_idx, cudaStream_t stream, cudaEvent_t* ev) {
   RowState* st = at<RowState>(ws, L.off_state);
-  const int64_t H = 1ll << L.log2H;
+  const Sampler form = choose_sampler(L.D, ng, static_cast<uint64_t>(n));
+  const int log2H = L.log2H;
+  const int64_t H = 1ll << log2H;
   // Reset CTAs per row: about eight 16-byte stores per thread of 256.
   const unsigned rb = static_cast<unsigned>(std::min<int64_t>(std::max<int64_t>(H / 2 / (256 * 8), 1), 64));
   // The refinement's control blocks start every attempt at zero.
@@ -538,7 +550,7 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
       L.radix_refine ? static_cast<unsigned long long*>(radix_sort_ctl(at<char>(ws, L.off_sort), P.M, rows))
                      : static_cast<unsigned long long*>(refine_grid_ctl(at<char>(ws, L.off_refine)));
   const int ref_words = static_cast<int>((L.radix_refine ? radix_sort_ctl_bytes() : refine_grid_ctl_bytes()) / 8);
-  launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, at<unsigned long long>(ws, L.off_table), L.log2H, gl,
+  launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, at<unsigned long long>(ws, L.off_table), log2H, gl,
                 st, static_cast<unsigned long long>(P.t), ref_ctl, ref_words, at<unsigned long long>(ws, L.off_sctl),
                 static_cast<int>(sample_tau_ctl_bytes() / 8));
   // Sampling and tau: one persistent kernel (its stage time is reported as
@@ -550,7 +562,7 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
                 at<uint32_t>(ws, L.off_blockcnt), at<uint32_t>(ws, L.off_sidx), at<uint32_t>(ws, L.off_skeys), false,
                 static_cast<unsigned long long>(P.t)};
   cudaError_t e = cudaSuccess;
-  if (sample_tau_fits(L.D, ng, static_cast<uint64_t>(n))) {
+  if (form == Sampler::Grid) {
     e = launch_sample_tau(sa, at<char>(ws, L.off_sctl), stream);
     if (e != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[1], stream);
@@ -1241,6 +1253,8 @@ size_t profk_workspace_size(int64_t rows, int64_t n, int64_t k, double eps) {
 int profk_set_option(int option, int64_t value) {
   if (option < 0 || option >= PROFK_OPT__COUNT) return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_PARAM_MODE && (value < 0 || value > 3)) return PROFK_ERR_INVALID;
+  if (option == PROFK_OPT_SAMPLER && (value < PROFK_SAMPLER_AUTO || value > PROFK_SAMPLER_STEPS))
+    return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_MAX_SEGMENT && value != 0 && (value < (1 << 16) || value > (int64_t(1) << 32) || (value & 3)))
     return PROFK_ERR_INVALID;
   if (value < 0) return PROFK_ERR_INVALID;
@@ -1293,9 +1307,10 @@ int profk_sample(const float* x, int64_t n, int64_t S, uint64_t seed, int64_t ro
                     at<unsigned long long>(c.ws, L.off_table), at<uint32_t>(c.ws, L.off_draws),
                     at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
                     at<uint32_t>(c.ws, L.off_skeys), false, 1ull, row};
-      // The main path's kernel where it takes the problem (it also finds a
-      // tau, of rank 1 here, which is not used), else the step-by-step one.
-      if (sample_tau_fits(D, 1, static_cast<uint64_t>(n))) {
+      // The main path's kernel for one row (it also finds a tau, of rank 1
+      // here, which is not used), else the step-by-step one.
+      const Sampler form = choose_sampler(D, 1, static_cast<uint64_t>(n));
+      if (form == Sampler::Grid) {
         PK_CHECK(cudaMemsetAsync(at<char>(c.ws, L.off_sctl), 0, sample_tau_ctl_bytes(), stream));
         PK_CHECK(launch_sample_tau(sa, at<char>(c.ws, L.off_sctl), stream));
       } else {

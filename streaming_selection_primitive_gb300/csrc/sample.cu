@@ -645,9 +645,12 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
       unsigned long long r0[ST_QB];
       unsigned fl[ST_QB];
 #pragma unroll
-      for (int b = 0; b < ST_QB; ++b) {
+      for (int b = 0; b < ST_QB; ++b) {  // every round of the group, also those past nm
         fl[b] = 0u;
         r0[b] = 0ull;
+      }
+#pragma unroll
+      for (int b = 0; b < ST_QB; ++b) {
         if (m0 + b >= nm) break;  // uniform across the block
         const int q = tid + (m0 + b) * ST_THREADS;
         const uint4 e4 = q < nq ? W4[q] : make_uint4(NOT_FIRST, NOT_FIRST, NOT_FIRST, NOT_FIRST);
@@ -677,7 +680,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
       }
 #pragma unroll
       for (int b = 0; b < ST_QB; ++b) {
-        if (fl[b] == 0u) continue;
+        if (m0 + b >= nm || fl[b] == 0u) continue;
         const int q = tid + (m0 + b) * ST_THREADS;
         unsigned long long r = r0[b];
 #pragma unroll

@@ -20,7 +20,10 @@ pytestmark = pytest.mark.gpu
     (1 << 30, 105985, 3, 0, 0), (3 * (1 << 20) + 17, 131072, 4, 2, 1),
     # more than 1024 draws per CTA (the draws held in shared memory), many repeats
     (1 << 24, 400_000, 5, 3, 2), (1 << 20, 1 << 19, 6, 0, 0), ((1 << 21) + 5, 300_001, 7, 1, 4)])
-def test_sample_matches_oracle(pk, cuda_device, n, S, seed, row, attempt):
+@pytest.mark.parametrize("form", ["auto", "steps"])
+def test_sample_matches_oracle(pk, cuda_device, n, S, seed, row, attempt, form):
+    """Both kernel forms draw the same sample."""
+    pk.set_option(pk.OPT_SAMPLER, {"auto": pk.SAMPLER_AUTO, "steps": pk.SAMPLER_STEPS}[form])
     x = workloads.uniform(n, seed, cuda_device)
     sidx, svals = pk.sample(x, S, seed, row, attempt)
     ref = PX.sample_indices(n, S, seed, row, attempt)

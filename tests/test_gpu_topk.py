@@ -167,6 +167,32 @@ def test_batched(pk, cuda_device, rows, n, ld, k):
             assert sts[r]["tau_first"] == ost.taus[0]
 
 
+SAMPLER_FORMS = ("grid", "steps")
+
+
+def sampler_option(pk, form):
+    return {"grid": pk.SAMPLER_GRID, "steps": pk.SAMPLER_STEPS}[form]
+
+
+@pytest.mark.parametrize("form", SAMPLER_FORMS)
+@pytest.mark.parametrize("rows,n,k", [(5, 1 << 20, 64), (12, (1 << 18) + 3, 700), (3, 3 * (1 << 20) + 8, 20_000),
+                                      (2, 1 << 24, 32)])
+def test_batched_sampler_forms(pk, cuda_device, form, rows, n, k):
+    """Both forms of the sampling kernels (the persistent grid kernel, the
+    step-by-step kernels) give every row the oracle's sample: the same tau and
+    counts.  The third shape draws about 137,000 times per row."""
+    pk.set_option(pk.OPT_SAMPLER, sampler_option(pk, form))
+    ld = (n + 3) // 4 * 4  # row stride a multiple of 4 elements
+    x = workloads.normal_rows(rows, ld, 3 * rows + k, cuda_device)[:, :n]
+    vals, idx, sts = pk.topk_batched(x, k, 1e-3, 21)
+    h = x.cpu().numpy()
+    for r in range(rows):
+        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 21, row=r, rows=rows)
+        assert_same(vals[r], idx[r], ov, oi, f"{form} row {r}")
+        assert (sts[r]["path"], sts[r]["R_first"], sts[r]["R_gt_first"]) == (ost.path, ost.R_first, ost.R_gt_first)
+        assert sts[r]["tau_first"] == ost.taus[0]
+
+
 def test_batched_rows_retry_alone(pk, cuda_device):
     # Forced parameters that make roughly half the rows fail their first attempt.
     rows, n, k = 8, 1 << 18, 40
@@ -199,10 +225,13 @@ def test_large_k_fallback(pk, cuda_device):
     assert st["path"] == pk.PATH_FALLBACK
 
 
-def test_batched_wide_sampler_rows_retry_alone(pk, cuda_device):
+@pytest.mark.parametrize("form", ("auto",) + SAMPLER_FORMS)
+def test_batched_wide_sampler_rows_retry_alone(pk, cuda_device, form):
     # 32 rows share the SMs, so each row's CTAs hold thousands of draws; about
-    # half the rows overflow each attempt and redraw alone.
+    # half the rows overflow each attempt and redraw alone (a row list).
     rows, n, k = 32, 1 << 20, 1
+    if form != "auto":
+        pk.set_option(pk.OPT_SAMPLER, sampler_option(pk, form))
     x = workloads.normal_rows(rows, n, 41, cuda_device)
     force = {"S": 32768, "t": 1, "M": 22}
     for o, v in ((pk.OPT_FORCE_S, 32768), (pk.OPT_FORCE_T, 1), (pk.OPT_FORCE_M, 22)):
