@@ -163,6 +163,25 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """The largest of every rank's x (a job takes its slowest rank's time);
+    a collective of the ranks' process group (nccl on the GPUs, gloo on CPU)."""
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gelems(n: int, steps: int, ws: int, ms: float) -> float:
+    """Whole-job throughput: every rank's steps x n elements (each rank selects
+    from its own row: weak scaling) over the slowest rank's time."""
+    return n * steps * ws / (ms / 1e3) / 1e9
+
+
 def run_reference(args):
     ws, rank, local = dist_env()
     if rank != 0:
@@ -265,14 +284,10 @@ def main():
             Rs.append(st["R_first"])
         ev1.record(stream)
         barrier()
-    total_ms = ev0.elapsed_time(ev1)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
     clocks = clk.summary()
     ms_step = total_ms / args.steps
-    value = n * args.steps * ws / (total_ms / 1e3) / 1e9
+    value = job_gelems(n, args.steps, ws, total_ms)
     peak, peak_kind = measured_peaks()
     traffic = traffic_from_profile(n)
     aux = pk.topk(x, k, EPS, 7, out=out)[2]["aux_bytes"]
@@ -284,12 +299,8 @@ def main():
         pk.topk(x, k, EPS, 30_000 + s, out=out)
     ev1.record(stream)
     barrier()
-    sync_ms = ev0.elapsed_time(ev1)
-    if ws > 1:
-        t = torch.tensor([sync_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        sync_ms = float(t.item())
-    synchronous = {"api": "profk_topk", "value": round(n * args.steps * ws / (sync_ms / 1e3) / 1e9, 3),
+    sync_ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
+    synchronous = {"api": "profk_topk", "value": round(job_gelems(n, args.steps, ws, sync_ms), 3),
                    "unit": "Gelem/s", "ms_per_step": round(sync_ms / args.steps, 4),
                    "hbm_frac_of_8TBs": round(4 * n / (sync_ms / args.steps / 1e3) / 8e12, 4)}
     # Stage breakdown and the filter's own launch time, from CUDA events the
@@ -344,8 +355,8 @@ def main():
     e2e_run(args.e2e_steps, 30_000)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_value = n * args.e2e_steps * ws / (e2e_ms / 1e3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    e2e_value = job_gelems(n, args.e2e_steps, ws, e2e_ms)
     del xh, xds
 
     sweep = {}
