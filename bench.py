@@ -86,9 +86,12 @@ def traffic_from_profile(n: int):
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms while active."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms while
+    active; the summary keeps the samples taken inside the timed region
+    (mark() at its start and end), or, for a region shorter than the sampling
+    interval, the two samples nearest to it."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -96,6 +99,7 @@ class ClockSampler:
         self.gpu = gpu_id
         self.proc = None
         self.path = None
+        self.marks = []
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -103,13 +107,17 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
         time.sleep(0.3)
         return self
 
+    def mark(self):
+        self.marks.append(time.time())
+
     def __exit__(self, *exc):
+        time.sleep(0.05)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -120,23 +128,32 @@ class ClockSampler:
     def summary(self):
         if not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        sm, smax, reasons = [], [], set()
+        from datetime import datetime
+
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                ts = datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), [nm for nm, v in zip(names, f[6:10])
+                                                              if v.lower() == "active"]))
             except ValueError:
                 continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (float("-inf"), float("inf"))
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        where = "inside the timed region"
+        if not inside and rows:
+            mid = 0.5 * (t0 + t1) if len(self.marks) >= 2 else rows[len(rows) // 2][0]
+            inside = sorted(rows, key=lambda r: abs(r[0] - mid))[:2]
+            where = "nearest to the timed region (shorter than the 20 ms sampling interval)"
+        reasons = sorted({nm for r in inside for nm in r[3]})
+        return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "reasons": reasons, "samples": len(inside), "samples_from": where}
 
 
 def cpu_baseline(x_host_prefix, k, budget_s=12.0):
@@ -221,7 +238,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="profk", choices=["profk", "reference"])
     ap.add_argument("--n", type=int, default=N_DEFAULT)
@@ -274,6 +291,7 @@ def main():
     # (profk_topk_async), all in flight, each completed with profk_wait.
     with ClockSampler(gpu_id) as clk:
         barrier()
+        clk.mark()
         ev0.record(stream)
         pending = [pk.topk_async(x, k, EPS, 1000 + s, out=out) for s in range(args.steps)]
         for p in pending:
@@ -284,6 +302,7 @@ def main():
             Rs.append(st["R_first"])
         ev1.record(stream)
         barrier()
+        clk.mark()
     total_ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
     clocks = clk.summary()
     ms_step = total_ms / args.steps
