@@ -154,7 +154,8 @@ __global__ void k_attempt_init(RowState* st, const int* rows) {
 // words per row) and refinement (sort_ctl, ctl_words) are zeroed too.
 __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int* rows, RowState* st,
                                 unsigned long long t, unsigned long long* sort_ctl, int ctl_words,
-                                unsigned long long* sample_ctl, int sample_words) {
+                                unsigned long long* sample_ctl, int sample_words, unsigned* block_eq,
+                                int64_t nblocks) {
   pdl_trigger();
   pdl_wait();
   const int row = launch_row(rows);
@@ -172,6 +173,10 @@ __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int*
   for (int64_t i = gtid; i < sample_words / 2; i += gstride) pc[i] = make_ulonglong2(0ull, 0ull);
   RowState& S = st[row];
   for (int64_t b = gtid; b < HIST_BINS; b += gstride) S.hist[b] = 0;
+  if (block_eq) {
+    unsigned* be = block_eq + static_cast<int64_t>(row) * nblocks;
+    for (int64_t b = gtid; b < nblocks; b += gstride) be[b] = 0u;
+  }
   if (gtid == 0) {
     S.R_ge = 0;
     S.R_gt = 0;
@@ -189,6 +194,8 @@ __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int*
     S.done_blocks = 0;
     S.compact_count = 0;
     S.skip = 0;
+    S.tie_gt = 0;
+    S.tau_copies = 0;
   }
 }
 
@@ -480,10 +487,12 @@ void launch_exact(const Layout& L, void* ws, const float* x, int64_t ld, int nro
                                                      align_up(sizeof(unsigned) * nb * L.rows)),
                nb, reinterpret_cast<TieCtl*>(tw), L.rows};
     launch_tie_take(ta, filter_grid(0), stream);
-  } else {
-    launch_select(a, static_cast<uint64_t>(L.k), false, 0, stream);
-    launch_compact(a, reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, stream);
+    launch_sort_emit(reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, nrows, rows, x, ld, L.n, out_vals, out_idx,
+                     stream, st, at<char>(ws, L.off_sort), L.rows, true);
+    return;
   }
+  launch_select(a, static_cast<uint64_t>(L.k), false, 0, stream);
+  launch_compact(a, reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, stream);
   launch_sort_emit(reinterpret_cast<uint64_t*>(sel), L.kstride, L.k, nrows, rows, x, ld, L.n, out_vals, out_idx, stream,
                    st, at<char>(ws, L.off_sort), L.rows);
 }
@@ -538,7 +547,8 @@ Sampler choose_sampler(int64_t D, int64_t ng, uint64_t n) {
 // stage events e[1..4] (e[0] is the caller's), or nullptr.
 cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, int ng, const int* gl, int64_t rows,
                             const float* x, int64_t ld, int64_t n, int64_t k, uint64_t seed, int64_t cps,
-                            float* out_vals, int64_t* out_idx, cudaStream_t stream, cudaEvent_t* ev) {
+                            float* out_vals, int64_t* out_idx, cudaStream_t stream, cudaEvent_t* ev,
+                            bool tie_book) {
   RowState* st = at<RowState>(ws, L.off_state);
   const Sampler form = choose_sampler(L.D, ng, static_cast<uint64_t>(n));
   const int log2H = L.log2H;
@@ -550,9 +560,16 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
       L.radix_refine ? static_cast<unsigned long long*>(radix_sort_ctl(at<char>(ws, L.off_sort), P.M, rows))
                      : static_cast<unsigned long long*>(refine_grid_ctl(at<char>(ws, L.off_refine)));
   const int ref_words = static_cast<int>((L.radix_refine ? radix_sort_ctl_bytes() : refine_grid_ctl_bytes()) / 8);
+  // tie_book (the call's tie exit is on): the filter keeps the tie step's
+  // per-block counts of tau and the x > tau that its full buffer drops (in
+  // the selection keys), which the tie exit then uses instead of a pass.
+  const int64_t nb = tie_blocks(n);
+  unsigned* block_eq = tie_book ? reinterpret_cast<unsigned*>(at<char>(ws, L.off_tie) +
+                                                              align_up(tie_ctl_bytes() * rows))
+                                : nullptr;
   launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, at<unsigned long long>(ws, L.off_table), log2H, gl,
                 st, static_cast<unsigned long long>(P.t), ref_ctl, ref_words, at<unsigned long long>(ws, L.off_sctl),
-                static_cast<int>(sample_tau_ctl_bytes() / 8));
+                static_cast<int>(sample_tau_ctl_bytes() / 8), block_eq, nb);
   // Sampling and tau: one persistent kernel (its stage time is reported as
   // the sampling's, the threshold stage then being empty), or, when many rows
   // share the SMs, the step-by-step kernels with the first radix pass of tau
@@ -574,7 +591,8 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
     launch_select(ta, 0, true, 1, stream);  // its last pass stores tau
   }
   if (ev) cudaEventRecord(ev[2], stream);
-  FilterArgs fa{x, ld, n, P.M, ng, gl, st, at<unsigned long long>(ws, L.off_buf), filter_grid(cps)};
+  FilterArgs fa{x, ld, n, P.M, ng, gl, st, at<unsigned long long>(ws, L.off_buf), filter_grid(cps), block_eq, nb,
+                tie_book ? at<unsigned long long>(ws, L.off_sel) : nullptr, L.kstride, k};
   launch_filter(fa, stream);
   if (ev) cudaEventRecord(ev[3], stream);
   if (!L.radix_refine) {
@@ -616,6 +634,7 @@ struct Resume {
   const char* report = nullptr;
   Params P{};
   int64_t launches = 0;  // kernels the first attempt launched
+  bool tie_exit = true;  // PROFK_OPT_TIE_EXIT when the first attempt was enqueued
 };
 
 int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,
@@ -725,7 +744,8 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
 
   const int mode = static_cast<int>(g_opt[PROFK_OPT_PARAM_MODE].load());
   const int max_attempts = static_cast<int>(std::max<int64_t>(0, g_opt[PROFK_OPT_MAX_ATTEMPTS].load()));
-  const bool tie_exit = g_opt[PROFK_OPT_TIE_EXIT].load() != 0;
+  // The first attempt's tie bookkeeping decides for a resumed call.
+  const bool tie_exit = resume ? resume->tie_exit : g_opt[PROFK_OPT_TIE_EXIT].load() != 0;
   const int64_t fS = g_opt[PROFK_OPT_FORCE_S].load(), ft = g_opt[PROFK_OPT_FORCE_T].load(),
                 fM = g_opt[PROFK_OPT_FORCE_M].load();
   const bool timing = g_opt[PROFK_OPT_TIMING].load() != 0;
@@ -812,7 +832,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         resume_used = true;
       } else {
       PK_CHECK(enqueue_attempt(L, c.ws, P, a, ng, gl, rows, x, ld, n, k, seed, cps, out_vals, out_idx, stream,
-                               time_it ? t_events.e : nullptr));
+                               time_it ? t_events.e : nullptr, tie_exit));
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[4], stream));
       PK_CHECK(cudaGetLastError());
       // Run-time check: read the exact counts of every row (written into
@@ -837,12 +857,13 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         for (int q = 0; q < 5; ++q) PK_CHECK(cudaEventElapsedTime(&t_stage_ms[q], t_events.e[q], t_events.e[q + 1]));
         first_filter = false;
       }
-      std::vector<int> tie;
+      std::vector<int> tie, tie_count;  // tie exit rows with the filter's bookkeeping, and without
       bool grow = false;
       for (int r : group) {
         const char* h = rep + REPORT_BYTES * r;
         unsigned long long Rg = 0, Rt = 0, nanc = 0;
-        unsigned distinct = 0, tau_key = 0, errf = 0;
+        unsigned distinct = 0, tau_key = 0, errf = 0, copies = 0;
+        std::memcpy(&copies, h + offsetof(RowState, tau_copies), 4);
         std::memcpy(&Rg, h + offsetof(RowState, R_ge), 8);
         std::memcpy(&Rt, h + offsetof(RowState, R_gt), 8);
         std::memcpy(&nanc, h + offsetof(RowState, nan), 8);
@@ -884,27 +905,36 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
           s.path = PROFK_PATH_FILTER;  // refined on the device already
         } else if (tie_exit && Rg > static_cast<uint64_t>(P.M) && Rt < static_cast<uint64_t>(k)) {
           s.path = PROFK_PATH_TIE;
-          tie.push_back(r);
+          // The filter kept the tie step's counts for the rows whose sample
+          // held tau more than once; the others need the counting pass.
+          (copies >= 2 ? tie : tie_count).push_back(r);
         } else {
           attempt[r] = a + 1;
           next.push_back(r);
         }
       }
-      if (!tie.empty()) {
+      // The rows with the filter's bookkeeping first: the counting pass of
+      // the others starts by clearing every row's block counts.
+      for (int pass = 0; pass < 2; ++pass) {
+        const std::vector<int>& tr = pass == 0 ? tie : tie_count;
+        if (tr.empty()) continue;
         tie_ran = true;
         int* tl = nullptr;
-        PK_CHECK(upload_rows(L, c.ws, hbuf, 2, tie, stream, &tl));
+        PK_CHECK(upload_rows(L, c.ws, hbuf, pass == 0 ? 2 : 1, tr, stream, &tl));
         uint64_t* sel = at<uint64_t>(c.ws, L.off_sel);
         char* tw = at<char>(c.ws, L.off_tie);
         const int64_t nb = tie_blocks(n);
-        TieArgs ta{x, ld, n, static_cast<int>(tie.size()), tl, st, reinterpret_cast<unsigned long long*>(sel),
+        TieArgs ta{x, ld, n, static_cast<int>(tr.size()), tl, st, reinterpret_cast<unsigned long long*>(sel),
                    L.kstride, k, reinterpret_cast<unsigned*>(tw + align_up(tie_ctl_bytes() * rows)),
                    reinterpret_cast<unsigned long long*>(tw + align_up(tie_ctl_bytes() * rows) +
                                                          align_up(sizeof(unsigned) * nb * rows)),
                    nb, reinterpret_cast<TieCtl*>(tw), rows};
-        PK_CHECK(launch_tie_take(ta, filter_grid(cps), stream));
-        launch_sort_emit(sel, L.kstride, k, static_cast<int>(tie.size()), tl, x, ld, n, out_vals, out_idx, stream, st,
-                         at<char>(c.ws, L.off_sort), L.rows);
+        if (pass == 0)
+          PK_CHECK(launch_tie_after_filter(ta, at<unsigned long long>(c.ws, L.off_buf), P.M, stream));
+        else
+          PK_CHECK(launch_tie_take(ta, filter_grid(cps), stream));
+        launch_sort_emit(sel, L.kstride, k, static_cast<int>(tr.size()), tl, x, ld, n, out_vals, out_idx, stream, st,
+                         at<char>(c.ws, L.off_sort), L.rows, true);
       }
       PK_CHECK(cudaGetLastError());
       if (grow) {
@@ -1002,6 +1032,7 @@ struct profk_call {
   unsigned long long seq = 0;
   cudaEvent_t copied = nullptr;  // the report copy of more than REPORT_ROWS_MAPPED rows
   int64_t launches = 0;
+  bool tie_exit = true;  // PROFK_OPT_TIE_EXIT at submission
 };
 
 namespace {
@@ -1085,9 +1116,11 @@ int submit_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
     call->ws_bytes = L.total;
     e = take_block(REPORT_BYTES * rows + 512, &call->host, &call->host_bytes);
   }
+  call->tie_exit = g_opt[PROFK_OPT_TIE_EXIT].load() != 0;
   if (e == cudaSuccess)
     e = enqueue_attempt(L, call->ws, P, 0, static_cast<int>(rows), nullptr, rows, x, ld, n, k, seed,
-                        g_opt[PROFK_OPT_FILTER_CTAS_PER_SM].load(), out_vals, out_idx, stream, nullptr);
+                        g_opt[PROFK_OPT_FILTER_CTAS_PER_SM].load(), out_vals, out_idx, stream, nullptr,
+                        call->tie_exit);
   if (e == cudaSuccess) {
     call->flag = reinterpret_cast<unsigned long long*>(
         align_up(reinterpret_cast<uintptr_t>(call->host + REPORT_BYTES * rows)));
@@ -1159,6 +1192,7 @@ int finish_async(profk_call* call, profk_stats* stats) {
       rs.report = call->host;
       rs.P = call->P;
       rs.launches = call->launches;
+      rs.tie_exit = call->tie_exit;
       status = run_topk(call->x, call->rows, call->n, call->ld, call->k, call->eps, call->seed, call->out_vals,
                         call->out_idx, call->stream, call->stats.data(), &rs);
     } else {

@@ -117,6 +117,8 @@ struct RowState {
   unsigned int compact_count;     // output cursor of the compaction
   unsigned int error;             // nonzero: a device-side check failed
   unsigned int skip;              // 1: this row's refinement is void (its attempt failed the check)
+  unsigned int tie_gt;            // x > tau appended to the tie list by the filter
+  unsigned int tau_copies;        // copies of tau among the sample keys (2 or more: a tied top)
   unsigned int hist[HIST_BINS];
 };
 

@@ -18,12 +18,24 @@
 //    whose old value is the slot of the first flushed key, so dense inputs
 //    (large k) do not serialize on the counter.  Stores are masked to M and
 //    the counter keeps counting, as in the pages' kernel.  Once a warp sees
-//    the counter pass M it counts the rest in a register (no more atomics,
-//    no stores), so inputs that overflow the buffer cost no atomics either;
+//    the counter pass M it only counts the rest, per lane (no mask, scan,
+//    atomic or store), so inputs that overflow the buffer, such as heavily
+//    tied ones whose check takes the tie exit, stream at full rate;
+//  * NaNs are counted only on a lane whose maximum is NaN;
 //  * R_gt, the NaN count and those late passers are per-lane registers,
 //    reduced once per row per warp.
 // A passer (v, i) is stored as the 64-bit key (ord(v) << 32) | ~i, the order
 // the refinement sorts by.
+//
+// Two loops over the tiles.  The plain one is all of the above.  With the
+// tie exit's bookkeeping requested, the rows whose sample held tau more than
+// once (a heavily tied top, the case in which the check may take the tie
+// exit) go to a second loop.  That loop also counts the copies of tau per
+// block of 2^TIE_BLOCK_LOG2 elements and appends to the row's tie list every
+// x > tau that the full buffer drops.  The tie exit then needs no second
+// pass over those rows.  Each loop skips the other's rows whole; keeping the
+// bookkeeping out of the plain loop keeps its registers, and its speed, those
+// of a kernel without it.
 #include "kernels.h"
 
 namespace profk {
@@ -49,15 +61,16 @@ __device__ __forceinline__ float comp(const float4& v, int c) {
 
 __device__ __forceinline__ void flush_row(RowState& S, unsigned long long& gt, unsigned long long& nan,
                                           unsigned long long& late) {
-  unsigned long long g = gt, q = nan;
+  unsigned long long g = gt, q = nan, l = late;
   for (int o = 16; o; o >>= 1) {
     g += __shfl_down_sync(FULL_MASK, g, o);
     q += __shfl_down_sync(FULL_MASK, q, o);
+    l += __shfl_down_sync(FULL_MASK, l, o);
   }
   if ((threadIdx.x & 31) == 0) {
     if (g) atomicAdd(&S.R_gt, g);
     if (q) atomicAdd(&S.nan, q);
-    if (late) atomicAdd(&S.R_ge, late);
+    if (l) atomicAdd(&S.R_ge, l);
   }
   gt = 0;
   nan = 0;
@@ -66,9 +79,63 @@ __device__ __forceinline__ void flush_row(RowState& S, unsigned long long& gt, u
 
 constexpr int STAGE = 128;  // staged passer keys per warp
 
-// Moves a warp's staged keys into the buffer with one reservation.
+// Tie list of a row (the x > tau that the full buffer drops): one key per
+// lane whose `take` is set, appended at the row's cursor with one atomic per
+// warp.  All 32 lanes call it.
+__device__ __forceinline__ void tie_append_one(RowState& S, unsigned long long* tl, int64_t k, bool take,
+                                               unsigned long long key) {
+  const unsigned m = __ballot_sync(FULL_MASK, take);
+  if (m == 0) return;
+  const int lane = threadIdx.x & 31, lead = __ffs(m) - 1;
+  unsigned b0 = 0;
+  if (lane == lead) b0 = atomicAdd(&S.tie_gt, static_cast<unsigned>(__popc(m)));
+  b0 = __shfl_sync(FULL_MASK, b0, lead);
+  if (take) {
+    const unsigned pos = b0 + __popc(m & ((1u << lane) - 1u));
+    if (pos < static_cast<unsigned long long>(k)) tl[pos] = key;
+  }
+}
+
+// The same for the elements of a warp tile that bit e of each lane's mask m
+// selects (element e is component e % 4 of the lane's float4 v[e / 4]).
+template <int U>
+__device__ __forceinline__ void tie_append_tile(RowState& S, unsigned long long* tl, int64_t k, uint64_t m,
+                                                const float4 (&v)[U], int64_t base) {
+  if (!__any_sync(FULL_MASK, m != 0)) return;
+  const int lane = threadIdx.x & 31;
+  const unsigned c = static_cast<unsigned>(__popcll(m));
+  unsigned incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
+    if (lane >= o) incl += t;
+  }
+  unsigned b0 = 0;
+  if (lane == 31) b0 = atomicAdd(&S.tie_gt, incl);
+  b0 = __shfl_sync(FULL_MASK, b0, 31);
+  unsigned long long pos = b0 + incl - c;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if ((m >> (u * 4 + q)) & 1ull) {
+        if (pos < static_cast<unsigned long long>(k)) {
+          const int64_t idx = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + q;
+          tl[pos] = cand_key(comp(v[u], q), static_cast<uint32_t>(idx));
+        }
+        ++pos;
+      }
+    }
+  }
+}
+
+// Moves a warp's staged keys into the buffer with one reservation; with the
+// tie bookkeeping (TIE), the keys above tau (key tkey) that fall beyond M go
+// to the tie list tl.
+template <bool TIE>
 __device__ __forceinline__ void flush_stage(RowState& S, unsigned long long* stage, int& stage_n,
-                                            unsigned long long* br, int64_t M, bool& over) {
+                                            unsigned long long* br, int64_t M, bool& over, unsigned long long* tl,
+                                            int64_t k, uint32_t tkey) {
   if (stage_n == 0) return;
   const int lane = threadIdx.x & 31;
   unsigned long long gbase = 0;
@@ -77,44 +144,75 @@ __device__ __forceinline__ void flush_stage(RowState& S, unsigned long long* sta
   __syncwarp();
   for (int j = lane; j < stage_n; j += 32)
     if (gbase + j < static_cast<unsigned long long>(M)) br[gbase + j] = stage[j];
-  if (gbase + stage_n > static_cast<unsigned long long>(M)) over = true;
+  if (gbase + stage_n > static_cast<unsigned long long>(M)) {
+    over = true;
+    if constexpr (TIE) {
+      for (int j0 = 0; j0 < stage_n; j0 += 32) {
+        const int j = j0 + lane;
+        const unsigned long long key = j < stage_n ? stage[j] : 0ull;
+        tie_append_one(S, tl, k, j < stage_n && gbase + j >= static_cast<unsigned long long>(M) &&
+                                     static_cast<uint32_t>(key >> 32) > tkey,
+                       key);
+      }
+    }
+  }
   stage_n = 0;
   __syncwarp();
 }
 
-template <int T, int U>
-__global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
-  pdl_wait();
+// The pass over the rows this loop takes: with the tie bookkeeping on
+// (a.block_eq), the rows whose sample holds tau more than once (a heavily
+// tied top, RowState::tau_copies >= 2) go to the TIE loop and the others to
+// the plain one; with it off the plain loop takes every row.  A row of the
+// other loop is skipped whole.
+template <int T, int U, bool TIE>
+__device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long long* stage) {
   static_assert(4 * U <= 64, "at most 64 elements per lane");
   constexpr int64_t WT = 32 * 4 * U;  // elements per warp tile
-  __shared__ unsigned long long s_stage[T / 32][STAGE];
-  unsigned long long* stage = s_stage[threadIdx.x >> 5];
   int stage_n = 0;  // warp-uniform
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (T / 32);
   const int64_t tiles_per_row = (a.n + WT - 1) / WT;
   const int64_t total = tiles_per_row * a.nrows;
   int cur = -1;
+  bool active = false;  // the row `row` is this loop's and has state to flush
   int row = 0;
   float tau = 0.f;
   bool over = false;  // this warp saw the row's counter pass M
   const float* xr = nullptr;
   unsigned long long* br = nullptr;
+  unsigned long long* tl = nullptr;  // the row's tie list (with the tie bookkeeping)
+  unsigned* beq = nullptr;           // the row's per-block counts of tau
+  uint32_t tkey = 0;
   unsigned long long gt = 0, nan = 0, late = 0;
   for (int64_t tile = static_cast<int64_t>(blockIdx.x) * (T / 32) + (threadIdx.x >> 5); tile < total;
        tile += nwarps) {
     const int ri = static_cast<int>(tile / tiles_per_row);
     const int64_t base = (tile - static_cast<int64_t>(ri) * tiles_per_row) * WT;
     if (ri != cur) {
-      if (cur >= 0) {
-        flush_stage(a.st[row], stage, stage_n, br, a.M, over);
+      if (active) {
+        flush_stage<TIE>(a.st[row], stage, stage_n, br, a.M, over, tl, a.k, tkey);
         flush_row(a.st[row], gt, nan, late);
+        active = false;
       }
       cur = ri;
-      row = a.rows ? a.rows[ri] : ri;
-      tau = key_to_float(a.st[row].tau_key);
+      const int nrow = a.rows ? a.rows[ri] : ri;
+      if (a.block_eq && (a.st[nrow].tau_copies >= 2) != TIE) {
+        // The other loop's row: on to this warp's first tile past it.
+        const int64_t next = static_cast<int64_t>(ri + 1) * tiles_per_row;
+        tile += (next - tile + nwarps - 1) / nwarps * nwarps - nwarps;
+        continue;
+      }
+      row = nrow;
+      active = true;
+      tkey = a.st[row].tau_key;
+      tau = key_to_float(tkey);
       xr = a.x + static_cast<int64_t>(row) * a.ld;
       br = a.buf + static_cast<int64_t>(row) * a.M;
+      if constexpr (TIE) {
+        tl = a.tie_keys + static_cast<int64_t>(row) * a.tie_stride;
+        beq = a.block_eq + static_cast<int64_t>(row) * a.nblocks;
+      }
       over = false;
     }
     float4 v[U];
@@ -148,7 +246,18 @@ __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
     // and `valid` keeps them out of every count there.
     const bool hit = !(m < tau);
     if (!__any_sync(FULL_MASK, hit)) continue;
-    uint64_t ge = 0;
+    if (hit && m != m) {  // a NaN among the lane's values (the max propagates it)
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float f = comp(v[u], c);
+          nan += (((valid >> (u * 4 + c)) & 1ull) && f != f);
+        }
+    }
+    // Per lane: the elements >= tau and those > tau (the rest of ge are
+    // copies of tau).
+    uint64_t ge = 0, gtm = 0;
     if (hit) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -159,77 +268,100 @@ __global__ void __launch_bounds__(T) k_filter(FilterArgs a) {
           const float f = comp(v[u], c);
           const bool ok = (valid >> e) & 1ull;
           ge |= static_cast<uint64_t>(ok && f >= tau) << e;
-          gt += (ok && f > tau);
-          nan += (ok && f != f);
+          gtm |= static_cast<uint64_t>(ok && f > tau) << e;
         }
       }
     }
-    const unsigned cnt = __popcll(ge);
-    unsigned incl = cnt;
+    gt += static_cast<unsigned long long>(__popcll(gtm));
+    if constexpr (TIE) {
+      const unsigned eq = static_cast<unsigned>(__popcll(ge) - __popcll(gtm));
+      if (__any_sync(FULL_MASK, eq != 0)) {
+        unsigned w = eq;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const unsigned tot = __shfl_sync(FULL_MASK, incl, 31);
-    if (tot == 0) continue;
-    if (over) {
-      if (lane == 0) late += tot;
-      continue;
-    }
-    if (tot <= STAGE) {
-      if (stage_n + static_cast<int>(tot) > STAGE) {
-        flush_stage(a.st[row], stage, stage_n, br, a.M, over);
-        if (over) {
-          if (lane == 0) late += tot;
-          continue;
-        }
+        for (int o = 16; o >= 1; o >>= 1) w += __shfl_xor_sync(FULL_MASK, w, o);
+        if (lane == 0 && w) atomicAdd(beq + (base >> TIE_BLOCK_LOG2), w);
       }
-      if (cnt) {
-        int pos = stage_n + static_cast<int>(incl - cnt);
+    }
+    // With the tie bookkeeping: this tile's x > tau that the buffer does not
+    // keep, appended to the row's tie list at the end of the tile.
+    uint64_t dropm = 0;
+    if (over) {
+      // The row's buffer is full: only the counts are left (per lane).
+      late += static_cast<unsigned long long>(__popcll(ge));
+      dropm = gtm;
+    } else {
+      const unsigned cnt = __popcll(ge);
+      unsigned incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const unsigned tot = __shfl_sync(FULL_MASK, incl, 31);
+      if (tot != 0 && tot <= STAGE) {
+        if (stage_n + static_cast<int>(tot) > STAGE)
+          flush_stage<TIE>(a.st[row], stage, stage_n, br, a.M, over, tl, a.k, tkey);
+        if (over) {  // the flush filled the buffer: this tile's passers are only counted
+          if (lane == 0) late += tot;
+          dropm = gtm;
+        } else {
+          if (cnt) {
+            int pos = stage_n + static_cast<int>(incl - cnt);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const int e = u * 4 + c;
+                if ((ge >> e) & 1ull) {
+                  const int64_t idx = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
+                  stage[pos++] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
+                }
+              }
+            }
+          }
+          stage_n += static_cast<int>(tot);
+          __syncwarp();
+        }
+      } else if (tot > STAGE) {
+        // More passers in this tile than a stage holds: reserve for the tile alone.
+        unsigned long long gbase = 0;
+        if (lane == 0) gbase = atomicAdd(&a.st[row].R_ge, static_cast<unsigned long long>(tot));
+        gbase = __shfl_sync(FULL_MASK, gbase, 0);
+        if (gbase + tot > static_cast<unsigned long long>(a.M)) over = true;
+        unsigned long long pos = gbase + incl - cnt;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int e = u * 4 + c;
             if ((ge >> e) & 1ull) {
-              const int64_t idx = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
-              stage[pos++] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
+              if (pos < static_cast<unsigned long long>(a.M)) {
+                const int64_t idx = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
+                br[pos] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
+              } else if constexpr (TIE) {
+                dropm |= gtm & (1ull << e);
+              }
+              ++pos;
             }
           }
         }
       }
-      stage_n += static_cast<int>(tot);
-      __syncwarp();
-      continue;
     }
-    // More passers in this tile than a stage holds: reserve for the tile alone.
-    unsigned long long gbase = 0;
-    if (lane == 0) gbase = atomicAdd(&a.st[row].R_ge, static_cast<unsigned long long>(tot));
-    gbase = __shfl_sync(FULL_MASK, gbase, 0);
-    if (gbase + tot > static_cast<unsigned long long>(a.M)) over = true;
-    if (cnt && gbase < static_cast<unsigned long long>(a.M)) {
-      unsigned long long pos = gbase + incl - cnt;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int e = u * 4 + c;
-          if ((ge >> e) & 1ull) {
-            if (pos < static_cast<unsigned long long>(a.M)) {
-              const int64_t idx = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
-              br[pos] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
-            }
-            ++pos;
-          }
-        }
-      }
-    }
+    if constexpr (TIE) tie_append_tile<U>(a.st[row], tl, a.k, dropm, v, base);
   }
-  if (cur >= 0) {
-    flush_stage(a.st[row], stage, stage_n, br, a.M, over);
+  if (active) {
+    flush_stage<TIE>(a.st[row], stage, stage_n, br, a.M, over, tl, a.k, tkey);
     flush_row(a.st[row], gt, nan, late);
   }
+}
+
+template <int T, int U>
+__global__ void __launch_bounds__(T, 3) k_filter(FilterArgs a) {
+  pdl_wait();
+  __shared__ unsigned long long s_stage[T / 32][STAGE];
+  unsigned long long* stage = s_stage[threadIdx.x >> 5];
+  filter_rows<T, U, false>(a, stage);
+  if (a.block_eq) filter_rows<T, U, true>(a, stage);
 }
 
 // Launch shape: threads per CTA and 16-byte loads per lane per warp tile.

@@ -138,6 +138,9 @@ void launch_tie_init(int nrows, const int* rows, RowState* st, int64_t k, cudaSt
 // `sel` (every x > tau, then the k - R_gt lowest-index copies of tau), ready
 // for launch_sort_emit; also clears RowState::skip of those rows.
 struct TieCtl;
+// Counting blocks of the tie step: 2^TIE_BLOCK_LOG2 elements.
+constexpr int TIE_BLOCK_LOG2 = 18;
+
 struct TieArgs {
   const float* x;
   int64_t ld;
@@ -156,7 +159,16 @@ struct TieArgs {
 };
 int64_t tie_blocks(int64_t n);
 size_t tie_ctl_bytes();
+// The tie step after a selection of tau = v_k that left RowState::R_gt = the
+// count of x > v_k (the exact path): one counting pass over the rows, then
+// the cut and the take.
 cudaError_t launch_tie_take(const TieArgs& a, int filter_grid, cudaStream_t stream);
+// The tie exit after a filter pass run with its tie bookkeeping (block_eq
+// and the appended x > tau already filled): the buffer's x > tau join the
+// appended ones, then the cut and the take.  buf: the filter's buffer, M its
+// capacity per row.
+cudaError_t launch_tie_after_filter(const TieArgs& a, const unsigned long long* buf, int64_t M,
+                                    cudaStream_t stream);
 
 // Writes the k keys >= the selected threshold into out (row stride out_stride).
 void launch_compact(const SelectArgs& a, uint64_t* out, int64_t out_stride, int64_t k,
@@ -168,10 +180,13 @@ void launch_compact(const SelectArgs& a, uint64_t* out, int64_t out_stride, int6
 // k > 8192 the keys are radix-sorted when `scratch` (radix_sort_scratch_bytes
 // of key_stride for all `total_rows` rows of the call) is given, else
 // bitonic-sorted in place (key_stride must then be next_pow2(k)).
+// gt_first (with st, k <= 8192): each row's keys [R_gt, k) are copies of one
+// value in ascending index order, below the keys [0, R_gt) (the tie step's
+// layout), and only the latter are sorted.
 void launch_sort_emit(uint64_t* keys, int64_t key_stride, int64_t k, int nrows, const int* rows,
                       const float* x, int64_t ld, int64_t n, float* out_vals, int64_t* out_idx,
                       cudaStream_t stream, RowState* st = nullptr, void* scratch = nullptr,
-                      int64_t total_rows = 0);
+                      int64_t total_rows = 0, bool gt_first = false);
 // Large-row sort and emission (sort.cu).  Which keys a row sorts:
 enum class SortCount {
   All,          // k keys, every listed row
@@ -248,6 +263,17 @@ struct FilterArgs {
   RowState* st;
   unsigned long long* buf;  // rows x M
   int grid;                 // persistent CTAs
+  // Bookkeeping for the tie exit (off when block_eq is null): the copies of
+  // tau per block of 2^TIE_BLOCK_LOG2 elements (rows x nblocks, zero at
+  // launch), and every x > tau that the full buffer drops, appended to the
+  // row's tie list (row stride tie_stride) from RowState::tie_gt on (stores
+  // beyond k are dropped; the count goes on).  The x > tau of the buffer and
+  // those appended are then all of them.
+  unsigned* block_eq = nullptr;
+  int64_t nblocks = 0;
+  unsigned long long* tie_keys = nullptr;
+  int64_t tie_stride = 0;
+  int64_t k = 0;
 };
 void launch_filter(const FilterArgs& a, cudaStream_t stream);
 int filter_default_grid(int sms);

@@ -441,6 +441,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   __shared__ unsigned long long s_above, s_count, s_base;
   __shared__ uint32_t s_list[TAU_GATHER];
   __shared__ uint32_t s_tau;
+  __shared__ unsigned s_copies;
   __shared__ unsigned s_wcnt[ST_WIDE_ROUNDS * (ST_THREADS / 32)];
   extern __shared__ uint4 st_dyn[];
   const int row = launch_row(a.rows);
@@ -723,8 +724,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     }
   };
 
-  // c. tau: the t-th largest sample key.
-  unsigned long long prefix = 0, want = a.t;
+  // c. tau: the t-th largest sample key (and its copies among them).
+  unsigned long long prefix = 0, want = a.t, copies = 0;
   int bits = 0;
 #pragma unroll 1
   for (int p = 0; p < 3; ++p) {
@@ -778,6 +779,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     want -= s_above;
     bits += width;
     const unsigned long long bucket_n = s_count;
+    copies = bucket_n;  // after the last pass: the keys equal to tau
     __syncthreads();
     if (p < 2 && bucket_n <= TAU_GATHER) {
       // The bucket's sample keys go to one list; the first CTA ranks them.
@@ -791,7 +793,10 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
       if (chunk == 0) {
         const int nl = static_cast<int>(bucket_n);
         if (tid < nl) s_list[tid] = __ldcg(&c.bucket[tid]);
-        if (tid == 0) s_tau = 0;
+        if (tid == 0) {
+          s_tau = 0;
+          s_copies = 0;
+        }
         __syncthreads();
         if (tid < nl) {
           // The want-th largest: fewer than want keys above it, want or
@@ -802,10 +807,14 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
             gt += s_list[j] > e;
             eq += s_list[j] == e;
           }
-          if (gt < want && want <= gt + eq) s_tau = e;
+          if (gt < want && want <= gt + eq) {
+            s_tau = e;
+            s_copies = eq;
+          }
         }
         __syncthreads();
         prefix = s_tau;
+        copies = s_copies;
       }
       break;
     }
@@ -813,6 +822,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   if (tid == 0) {
     if (chunk == 0) {
       S.tau_key = static_cast<uint32_t>(prefix);
+      S.tau_copies = static_cast<unsigned>(copies < 0xffffffffull ? copies : 0xffffffffull);
       S.sel_prefix = prefix;
       S.sel_bits = 32;
       S.sel_done = 1;

@@ -229,7 +229,10 @@ __global__ void __launch_bounds__(SEL_THREADS) k_radix_pass(Src src, RowState* s
         if (shift == final_shift || (!value_only && c == rank - acc)) {
           S.sel_done = 1;
           S.sel_thresh = np << shift;
-          if (value_only) S.tau_key = static_cast<uint32_t>(np);  // the threshold of step 2
+          if (value_only) {  // the threshold of step 2, and how many keys hold it
+            S.tau_key = static_cast<uint32_t>(np);
+            S.tau_copies = static_cast<unsigned>(c < 0xffffffffull ? c : 0xffffffffull);
+          }
         }
         break;
       }
@@ -293,34 +296,37 @@ __device__ __forceinline__ void emit_one(const unsigned long long key, int row, 
   }
 }
 
-// One CTA per row: load k keys, pad to P with 0 (below every real key), sort
-// descending in shared memory, emit.
+// One CTA per row: load k keys, pad to P (>= 1024) with 0 (below every real
+// key), sort descending in shared memory (registers and shuffles for the
+// closer compare-exchange partners), emit.  gt_first: keys [R_gt, k) of the
+// row are copies of one value in ascending index order, below every key of
+// [0, R_gt) (the tie step's layout), so only a prefix that covers the first
+// R_gt keys is sorted (none when R_gt <= 1): its other keys are the largest
+// of the ordered copies, and every key after it is smaller.
 __global__ void __launch_bounds__(SORT_THREADS) k_sort_small(const unsigned long long* keys, int64_t key_stride,
                                                             int64_t k, int P, const int* rows, const float* x,
                                                             int64_t ld, int64_t n, float* out_vals,
-                                                            int64_t* out_idx, const RowState* st) {
+                                                            int64_t* out_idx, const RowState* st, bool gt_first) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ unsigned long long s[];
   const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
   if (st && st[row].skip) return;
   const unsigned long long* kr = keys + row * key_stride;
+  const int64_t count = gt_first && st ? static_cast<int64_t>(st[row].R_gt < static_cast<unsigned long long>(k)
+                                                                   ? st[row].R_gt
+                                                                   : static_cast<unsigned long long>(k))
+                                       : k;
+  int Ps = SORT_THREADS;  // the sorted prefix: a power of two >= 1024, <= P
+  while (Ps < count) Ps <<= 1;
   for (int i = threadIdx.x; i < P; i += blockDim.x) s[i] = i < k ? kr[i] : 0ull;
   __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int j = size >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < P; i += blockDim.x) {
-        const int l = i ^ j;
-        if (l > i) {
-          const unsigned long long a = s[i], b = s[l];
-          const bool desc = (i & size) == 0;
-          if (desc ? (a < b) : (a > b)) {
-            s[i] = b;
-            s[l] = a;
-          }
-        }
-      }
-      __syncthreads();
+  if (count > 1) {
+    switch (Ps / SORT_THREADS) {
+      case 1: block_sort_desc<1>(s); break;
+      case 2: block_sort_desc<2>(s); break;
+      case 4: block_sort_desc<4>(s); break;
+      default: block_sort_desc<8>(s); break;
     }
   }
   for (int j = threadIdx.x; j < k; j += blockDim.x) emit_one(s[j], row, j, k, x, ld, n, out_vals, out_idx);
@@ -658,7 +664,7 @@ int64_t small_sort_max() { return SMALL_SORT_MAX; }
 
 void launch_sort_emit(uint64_t* keys_u, int64_t key_stride, int64_t k, int nrows, const int* rows, const float* x,
                       int64_t ld, int64_t n, float* out_vals, int64_t* out_idx, cudaStream_t stream,
-                      RowState* st, void* scratch, int64_t total_rows) {
+                      RowState* st, void* scratch, int64_t total_rows, bool gt_first) {
   if (k > SMALL_SORT_MAX && scratch) {
     RadixSortArgs ra{reinterpret_cast<unsigned long long*>(keys_u), key_stride, k,
                      st ? SortCount::KUnlessSkip : SortCount::All, nrows, rows, total_rows > 0 ? total_rows : nrows,
@@ -669,9 +675,9 @@ void launch_sort_emit(uint64_t* keys_u, int64_t key_stride, int64_t k, int nrows
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(keys_u);
   if (k <= SMALL_SORT_MAX) {
     cudaFuncSetAttribute(k_sort_small, cudaFuncAttributeMaxDynamicSharedMemorySize, SMALL_SORT_MAX * 8);
-    const int P = static_cast<int>(next_pow2(k));
+    const int P = static_cast<int>(std::max<int64_t>(next_pow2(k), SORT_THREADS));
     launch_kernel(k_sort_small, nrows, SORT_THREADS, P * 8, stream, keys, key_stride, k, P, rows, x, ld, n, out_vals, out_idx,
-                                                         st);
+                  st, gt_first && st != nullptr);
     return;
   }
   const int64_t P = next_pow2(k);  // >= 2 * CHUNK here

@@ -15,6 +15,12 @@
 //     tau in index order (segments of 16K elements, one block-wide scan
 //     each), the first `need` of the row written after the x > tau keys.
 // Only the input up to the cut is read a second time.
+//
+// After a filter pass that ran with its tie bookkeeping, step 1 is not a
+// pass over the input: the filter has counted the copies of tau per block
+// and appended every x > tau that its full buffer dropped, so
+//  1'. `k_tie_gather` adds the buffer's own x > tau to those, and the cut
+//      checks that they are R_gt in all.
 #include "kernels.h"
 
 namespace profk {
@@ -31,7 +37,6 @@ namespace {
 constexpr int TC_THREADS = 256;
 constexpr int TC_U = 8;                        // float4 per lane per warp tile
 constexpr int64_t TC_WT = 32 * 4 * TC_U;       // elements per warp tile
-constexpr int TIE_BLOCK_LOG2 = 18;             // counting block: 2^18 elements
 constexpr int TT_THREADS = 256;
 constexpr int TT_F4 = 16;                      // float4 per thread per segment
 constexpr int64_t TT_SEG = TT_THREADS * TT_F4 * 4;  // 16K elements
@@ -118,8 +123,44 @@ __global__ void __launch_bounds__(TC_THREADS) k_tie_count(TieArgs a) {
   }
 }
 
-// One CTA per row: exclusive prefix of the block counts, and the cut.
-__global__ void __launch_bounds__(1024) k_tie_cut(TieArgs a) {
+// The buffer's keys above tau (its first min(R_ge, M) entries), appended to
+// the row's tie list after those the filter appended: CTAs (blockIdx.x) take
+// strided runs of the buffer of row blockIdx.y, one atomic per warp and run.
+constexpr int TG_THREADS = 256;
+
+__global__ void __launch_bounds__(TG_THREADS) k_tie_gather(TieArgs a, const unsigned long long* buf, int64_t M) {
+  pdl_trigger();
+  pdl_wait();
+  const int row = launch_row(a.rows);
+  RowState& S = a.st[row];
+  const uint32_t tkey = S.tau_key;
+  const int64_t len = S.R_ge < static_cast<unsigned long long>(M) ? static_cast<int64_t>(S.R_ge) : M;
+  const unsigned long long* br = buf + static_cast<int64_t>(row) * M;
+  unsigned long long* out = a.sel + static_cast<int64_t>(row) * a.kstride;
+  const int lane = threadIdx.x & 31;
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * TG_THREADS; i0 < len;
+       i0 += static_cast<int64_t>(gridDim.x) * TG_THREADS) {  // uniform across the warp
+    const int64_t i = i0 + threadIdx.x;
+    const unsigned long long key = i < len ? br[i] : 0ull;
+    const bool take = i < len && static_cast<uint32_t>(key >> 32) > tkey;
+    const unsigned m = __ballot_sync(FULL_MASK, take);
+    if (m == 0) continue;
+    const int lead = __ffs(m) - 1;
+    unsigned b0 = 0;
+    if (lane == lead) b0 = atomicAdd(&S.tie_gt, static_cast<unsigned>(__popc(m)));
+    b0 = __shfl_sync(FULL_MASK, b0, lead);
+    if (take) {
+      const unsigned pos = b0 + __popc(m & ((1u << lane) - 1u));
+      if (pos < static_cast<unsigned long long>(a.k)) out[pos] = key;
+    }
+  }
+}
+
+// One CTA per row: exclusive prefix of the block counts, and the cut.  With
+// check_gt, the tie list must hold exactly the R_gt keys above tau (the
+// filter's appended ones and the buffer's); a row where it does not is
+// marked with a device error (never expected: a broken invariant).
+__global__ void __launch_bounds__(1024) k_tie_cut(TieArgs a, bool check_gt) {
   pdl_trigger();
   pdl_wait();
   __shared__ unsigned long long sw[33];
@@ -165,6 +206,7 @@ __global__ void __launch_bounds__(1024) k_tie_cut(TieArgs a) {
     a.ctl[row].cut = s_cut;
     a.ctl[row].need = need;
     S.skip = 0;  // the refinement enqueued before the check voided this row
+    if (check_gt && static_cast<unsigned long long>(atomicAdd(&S.tie_gt, 0u)) != S.R_gt) atomicOr(&S.error, 32u);
   }
 }
 
@@ -251,7 +293,20 @@ cudaError_t launch_tie_take(const TieArgs& a, int filter_grid, cudaStream_t stre
   if (ctas > filter_grid) ctas = filter_grid;
   if (ctas < 1) ctas = 1;
   launch_kernel(k_tie_count, dim3(static_cast<unsigned>(ctas)), TC_THREADS, 0, stream, a);
-  launch_kernel(k_tie_cut, dim3(static_cast<unsigned>(a.nrows)), 1024, 0, stream, a);
+  launch_kernel(k_tie_cut, dim3(static_cast<unsigned>(a.nrows)), 1024, 0, stream, a, false);
+  launch_kernel(k_tie_take, dim3(static_cast<unsigned>(a.nblocks), static_cast<unsigned>(a.nrows)), TT_THREADS, 0,
+                stream, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tie_after_filter(const TieArgs& a, const unsigned long long* buf, int64_t M,
+                                    cudaStream_t stream) {
+  int64_t runs = (M + 8 * TG_THREADS - 1) / (8 * TG_THREADS);  // about eight keys per thread
+  if (runs > 64) runs = 64;
+  if (runs < 1) runs = 1;
+  launch_kernel(k_tie_gather, dim3(static_cast<unsigned>(runs), static_cast<unsigned>(a.nrows)), TG_THREADS, 0,
+                stream, a, buf, M);
+  launch_kernel(k_tie_cut, dim3(static_cast<unsigned>(a.nrows)), 1024, 0, stream, a, true);
   launch_kernel(k_tie_take, dim3(static_cast<unsigned>(a.nblocks), static_cast<unsigned>(a.nrows)), TT_THREADS, 0,
                 stream, a);
   return cudaGetLastError();
