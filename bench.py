@@ -180,6 +180,21 @@ def dist_env():
     return ws, rank, local
 
 
+INPUTS = {
+    "normal": "float32 N(0,1)",
+    "uniform": "float32 Uniform[0,1) (2^24 levels)",
+    "pareto": "float32 Pareto alpha = 1.5, x_m = 1",
+    "ulps_below_one": "float32: 99.9 % in the 256 values just below 1.0, else Uniform[0,1)",
+    "levels16": "float32: 16 equally likely levels i / 16",
+    "sorted_normal": "float32 N(0,1) sorted ascending",
+}
+
+
+def workload_name(gen: str, n: int, k: int) -> str:
+    size = f"2^{n.bit_length() - 1}" if n & (n - 1) == 0 else str(n)
+    return f"{gen}_{size}_k{k}"
+
+
 def max_over_ranks(x: float, ws: int, device) -> float:
     """The largest of every rank's x (a job takes its slowest rank's time);
     a collective of the ranks' process group (nccl on the GPUs, gloo on CPU)."""
@@ -224,7 +239,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "Gelem/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"normal_2^30_k{args.k}", "n": args.n, "k": args.k, "eps": EPS,
+        "config": {"workload": workload_name("normal", args.n, args.k), "n": args.n, "k": args.k, "eps": EPS,
                    "sample_elems": n_sample},
         "cpu_baseline": {"value": value, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
                          "sample": f"each step: oracle.topk_sort (full sort, one thread) on a {n_sample}-element "
@@ -243,6 +258,8 @@ def main():
     ap.add_argument("--impl", default="profk", choices=["profk", "reference"])
     ap.add_argument("--n", type=int, default=N_DEFAULT)
     ap.add_argument("--k", type=int, default=K_DEFAULT)
+    ap.add_argument("--gen", default="normal",
+                    help="input generator of the timed steps (workloads.GENERATORS; default normal)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -267,8 +284,10 @@ def main():
     pk.lib()
     pk.reset_options()
     n, k = args.n, args.k
+    if args.gen not in workloads.GENERATORS:
+        raise SystemExit(f"--gen: one of {sorted(workloads.GENERATORS)}")
 
-    x = workloads.normal(n, 1 + rank, dev)
+    x = workloads.GENERATORS[args.gen](n, 1 + rank, dev)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -308,7 +327,7 @@ def main():
     ms_step = total_ms / args.steps
     value = job_gelems(n, args.steps, ws, total_ms)
     peak, peak_kind = measured_peaks()
-    traffic = traffic_from_profile(n)
+    traffic = traffic_from_profile(n) if args.gen == "normal" else None  # the capture is of the normal input
     aux = pk.topk(x, k, EPS, 7, out=out)[2]["aux_bytes"]
     # The same calls through the synchronous form (profk_topk: each call
     # returns after its check, so the host round trip sits between calls).
@@ -458,7 +477,8 @@ def main():
             "metric": METRIC, "value": round(value, 3), "unit": "Gelem/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": f"normal_2^30_k{k}", "n": n, "k": k, "eps": EPS, "input": "float32 N(0,1)",
+            "config": {"workload": workload_name(args.gen, n, k), "n": n, "k": k, "eps": EPS,
+                       "input": INPUTS.get(args.gen, args.gen),
                        "l2": "input 4 GiB > L2 129 MB: no flush between steps", "parallelism": f"replicas x{ws}",
                        "api": f"profk_topk_async, {args.steps} calls in flight, each completed by profk_wait"},
             "hbm_gbs_end_to_end": round(4 * n / (ms_step / 1e3) / 1e9, 1),
