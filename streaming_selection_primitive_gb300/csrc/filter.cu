@@ -255,10 +255,23 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
           nan += (((valid >> (u * 4 + c)) & 1ull) && f != f);
         }
     }
+    // Copies of tau in this tile (per lane), added to the block's counter.
+    auto count_ties = [&](unsigned eq) {
+      if constexpr (TIE) {
+        if (__any_sync(FULL_MASK, eq != 0)) {
+          unsigned w = eq;
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) w += __shfl_xor_sync(FULL_MASK, w, o);
+          if (lane == 0 && w) atomicAdd(beq + (base >> TIE_BLOCK_LOG2), w);
+        }
+      }
+    };
     // Per lane: the elements >= tau and those > tau (the rest of ge are
-    // copies of tau).
-    uint64_t ge = 0, gtm = 0;
-    if (hit) {
+    // copies of tau); ok: element e of the lane is in the row.
+    auto masks = [&](uint64_t& ge, uint64_t& gtm) {
+      ge = 0;
+      gtm = 0;
+      if (!hit) return;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (mu[u] < tau) continue;  // no passer and no NaN among these four
@@ -271,25 +284,47 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
           gtm |= static_cast<uint64_t>(ok && f > tau) << e;
         }
       }
-    }
-    gt += static_cast<unsigned long long>(__popcll(gtm));
-    if constexpr (TIE) {
-      const unsigned eq = static_cast<unsigned>(__popcll(ge) - __popcll(gtm));
-      if (__any_sync(FULL_MASK, eq != 0)) {
-        unsigned w = eq;
+    };
+    if (over) {
+      // The row's buffer is full: only the counts are left (per lane), and
+      // with the bookkeeping the x > tau (those rarely exist when the tie exit
+      // applies).  A full tile is counted without masks or branches.
+      unsigned cge = 0, cgt = 0;
+      if (base + WT <= a.n) {
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) w += __shfl_xor_sync(FULL_MASK, w, o);
-        if (lane == 0 && w) atomicAdd(beq + (base >> TIE_BLOCK_LOG2), w);
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float f = comp(v[u], c);
+            cge += f >= tau;
+            cgt += f > tau;
+          }
+      } else {
+        uint64_t ge, gtm;
+        masks(ge, gtm);
+        cge = static_cast<unsigned>(__popcll(ge));
+        cgt = static_cast<unsigned>(__popcll(gtm));
       }
+      late += cge;
+      gt += cgt;
+      count_ties(cge - cgt);
+      if constexpr (TIE) {
+        if (__any_sync(FULL_MASK, cgt != 0)) {
+          uint64_t ge, gtm;
+          masks(ge, gtm);
+          tie_append_tile<U>(a.st[row], tl, a.k, gtm, v, base);
+        }
+      }
+      continue;
     }
+    uint64_t ge, gtm;
+    masks(ge, gtm);
+    gt += static_cast<unsigned long long>(__popcll(gtm));
+    count_ties(static_cast<unsigned>(__popcll(ge) - __popcll(gtm)));
     // With the tie bookkeeping: this tile's x > tau that the buffer does not
     // keep, appended to the row's tie list at the end of the tile.
     uint64_t dropm = 0;
-    if (over) {
-      // The row's buffer is full: only the counts are left (per lane).
-      late += static_cast<unsigned long long>(__popcll(ge));
-      dropm = gtm;
-    } else {
+    {
       const unsigned cnt = __popcll(ge);
       unsigned incl = cnt;
 #pragma unroll
