@@ -138,8 +138,9 @@ void launch_tie_init(int nrows, const int* rows, RowState* st, int64_t k, cudaSt
 // `sel` (every x > tau, then the k - R_gt lowest-index copies of tau), ready
 // for launch_sort_emit; also clears RowState::skip of those rows.
 struct TieCtl;
-// Counting blocks of the tie step: 2^TIE_BLOCK_LOG2 elements.
-constexpr int TIE_BLOCK_LOG2 = 18;
+// Counting blocks of the tie step: 2^TIE_BLOCK_LOG2 elements (one segment of
+// the take, so that the blocks up to the cut are taken in parallel).
+constexpr int TIE_BLOCK_LOG2 = 14;
 
 struct TieArgs {
   const float* x;

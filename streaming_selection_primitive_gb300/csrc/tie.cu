@@ -10,10 +10,11 @@
 //     output keys (fewer than k of them), and the copies of tau are counted
 //     per block of 2^18 elements (one atomic per warp tile that has any);
 //  2. `k_tie_cut`, one CTA per row: the exclusive prefix of the block counts
-//     and the block in which the running count of tau reaches `need`;
-//  3. `k_tie_take`, one CTA per block up to that one: the block's copies of
-//     tau in index order (segments of 16K elements, one block-wide scan
-//     each), the first `need` of the row written after the x > tau keys.
+//     and the block in which the running count of tau reaches `need` (the
+//     scan stops there);
+//  3. `k_tie_take`, CTAs striding over the blocks up to that one: a block's
+//     copies of tau in index order (one block-wide scan of its 16K
+//     elements), the first `need` of the row written after the x > tau keys.
 // Only the input up to the cut is read a second time.
 //
 // After a filter pass that ran with its tie bookkeeping, step 1 is not a
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(1024) k_tie_cut(TieArgs a, bool check_gt) {
     }
     carry += sw[32];
     __syncthreads();
+    if (carry >= need) break;  // the cut is known; later blocks are not taken
   }
   if (threadIdx.x == 0) {
     a.ctl[row].cut = s_cut;
@@ -210,16 +212,10 @@ __global__ void __launch_bounds__(1024) k_tie_cut(TieArgs a, bool check_gt) {
   }
 }
 
-// One CTA per block (blockIdx.x) of a row (blockIdx.y): its copies of tau in
-// index order, those of rank < need written after the row's x > tau keys.
-__global__ void __launch_bounds__(TT_THREADS) k_tie_take(TieArgs a) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ unsigned long long sw[TT_THREADS / 32 + 1];
-  const int row = launch_row(a.rows);
+// Block blk of a row: its copies of tau in index order, those of rank < need
+// written after the row's x > tau keys (all threads of the CTA call it).
+__device__ __forceinline__ void tie_take_block(const TieArgs& a, int row, int64_t blk, unsigned long long* sw) {
   const TieCtl& c = a.ctl[row];
-  const int64_t blk = blockIdx.x;
-  if (blk > c.cut) return;
   RowState& S = a.st[row];
   const float tau = key_to_float(S.tau_key);
   const unsigned long long need = c.need, gt = S.R_gt;
@@ -276,7 +272,26 @@ __global__ void __launch_bounds__(TT_THREADS) k_tie_take(TieArgs a) {
   }
 }
 
+// CTAs striding over the blocks (blockIdx.x, ...) of a row (blockIdx.y) up
+// to the cut: a block's copies of tau in index order, those of rank < need
+// written after the row's x > tau keys.
+__global__ void __launch_bounds__(TT_THREADS) k_tie_take(TieArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ unsigned long long sw[TT_THREADS / 32 + 1];
+  const int row = launch_row(a.rows);
+  const TieCtl& c = a.ctl[row];
+  const int64_t cut = c.cut;
+  for (int64_t blk = blockIdx.x; blk <= cut; blk += gridDim.x) tie_take_block(a, row, blk, sw);
+}
+
 }  // namespace
+
+// CTAs of the take per row: the blocks, at most two per SM (they stride).
+unsigned take_ctas(int64_t nblocks) {
+  const int64_t cap = 2 * static_cast<int64_t>(sms());
+  return static_cast<unsigned>(nblocks < cap ? (nblocks > 0 ? nblocks : 1) : cap);
+}
 
 int64_t tie_blocks(int64_t n) { return (n + (int64_t(1) << TIE_BLOCK_LOG2) - 1) >> TIE_BLOCK_LOG2; }
 
@@ -294,8 +309,7 @@ cudaError_t launch_tie_take(const TieArgs& a, int filter_grid, cudaStream_t stre
   if (ctas < 1) ctas = 1;
   launch_kernel(k_tie_count, dim3(static_cast<unsigned>(ctas)), TC_THREADS, 0, stream, a);
   launch_kernel(k_tie_cut, dim3(static_cast<unsigned>(a.nrows)), 1024, 0, stream, a, false);
-  launch_kernel(k_tie_take, dim3(static_cast<unsigned>(a.nblocks), static_cast<unsigned>(a.nrows)), TT_THREADS, 0,
-                stream, a);
+  launch_kernel(k_tie_take, dim3(take_ctas(a.nblocks), static_cast<unsigned>(a.nrows)), TT_THREADS, 0, stream, a);
   return cudaGetLastError();
 }
 
@@ -307,8 +321,7 @@ cudaError_t launch_tie_after_filter(const TieArgs& a, const unsigned long long* 
   launch_kernel(k_tie_gather, dim3(static_cast<unsigned>(runs), static_cast<unsigned>(a.nrows)), TG_THREADS, 0,
                 stream, a, buf, M);
   launch_kernel(k_tie_cut, dim3(static_cast<unsigned>(a.nrows)), 1024, 0, stream, a, true);
-  launch_kernel(k_tie_take, dim3(static_cast<unsigned>(a.nblocks), static_cast<unsigned>(a.nrows)), TT_THREADS, 0,
-                stream, a);
+  launch_kernel(k_tie_take, dim3(take_ctas(a.nblocks), static_cast<unsigned>(a.nrows)), TT_THREADS, 0, stream, a);
   return cudaGetLastError();
 }
 
