@@ -152,7 +152,7 @@ struct TieArgs {
   unsigned long long* sel;  // rows x kstride output keys
   int64_t kstride;
   int64_t k;
-  unsigned* block_eq;             // rows x nblocks: copies of tau per block of 2^18 elements
+  unsigned* block_eq;             // rows x nblocks: copies of tau per block of 2^TIE_BLOCK_LOG2 elements
   unsigned long long* block_pre;  // rows x nblocks: their exclusive prefix
   int64_t nblocks;                // tie_blocks(n)
   TieCtl* ctl;                    // rows x tie_ctl_bytes()

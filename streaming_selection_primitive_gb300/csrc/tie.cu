@@ -8,7 +8,7 @@
 //  1. `k_tie_count`, one streaming pass like the filter's (persistent grid,
 //     warp tiles of 128-bit loads): every x > tau is appended to the row's
 //     output keys (fewer than k of them), and the copies of tau are counted
-//     per block of 2^18 elements (one atomic per warp tile that has any);
+//     per block of 2^TIE_BLOCK_LOG2 elements (one atomic per warp tile that has any);
 //  2. `k_tie_cut`, one CTA per row: the exclusive prefix of the block counts
 //     and the block in which the running count of tau reaches `need` (the
 //     scan stops there);
