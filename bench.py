@@ -261,6 +261,8 @@ def main():
     ap.add_argument("--gen", default="normal",
                     help="input generator of the timed steps (workloads.GENERATORS; default normal)")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-protocol", action="store_true",
+                    help="skip the per-call latency over several input tensors")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     args = ap.parse_args()
@@ -397,6 +399,30 @@ def main():
     e2e_value = job_gelems(n, args.e2e_steps, ws, e2e_ms)
     del xh, xds
 
+    # Per-call latency as the pages measure it: several input tensors (data
+    # seeds), each with 20 synchronous calls of their own algorithm seeds,
+    # every call bracketed by CUDA events on the launch stream.
+    protocol = None
+    if not args.no_protocol:
+        per_call = []
+        inputs = 5
+        for d in range(inputs):
+            xs = x if d == 0 else workloads.GENERATORS[args.gen](n, 101 + d + 10 * rank, dev)
+            pk.topk(xs, k, EPS, 60_000 + d, out=out)  # warm for this tensor
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+            for s, (a0, a1) in enumerate(evs):
+                a0.record(stream)
+                pk.topk(xs, k, EPS, 61_000 + 100 * d + s, out=out)
+                a1.record(stream)
+            torch.cuda.synchronize()
+            per_call += [a0.elapsed_time(a1) for a0, a1 in evs]
+            if d > 0:
+                del xs
+        per_call.sort()
+        q = lambda f: per_call[min(len(per_call) - 1, int(f * len(per_call)))]
+        protocol = {"api": "profk_topk", "inputs": inputs, "calls_each": 20, "mean_ms": round(statistics.mean(per_call), 4),
+                    "p50_ms": round(q(0.50), 4), "p99_ms": round(q(0.99), 4), "max_ms": round(per_call[-1], 4)}
+
     sweep = {}
     if not args.no_sweep:
         for gen in ("uniform", "normal", "pareto"):
@@ -496,6 +522,7 @@ def main():
             "R_first_mean": round(float(np.mean(Rs)), 1),
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "protocol": protocol,
             "sweep": sweep,
         }
         print(json.dumps(line), flush=True)
