@@ -79,6 +79,12 @@ __device__ __forceinline__ void flush_row(RowState& S, unsigned long long& gt, u
 
 constexpr int STAGE = 128;  // staged passer keys per warp
 
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Tie list of a row (the x > tau that the full buffer drops): one key per
 // lane whose `take` is set, appended at the row's cursor with one atomic per
 // warp.  All 32 lanes call it.
@@ -215,6 +221,13 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
       }
       over = false;
     }
+    // The bookkeeping loop's rows are heavily tied, and other warps fill the
+    // buffer long before this warp's own stage would tell it so: the row's
+    // counter is read with the tile (its latency hidden by the tile's loads).
+    unsigned long long rge = 0;
+    if constexpr (TIE) {
+      if (!over && lane == 0) rge = ld_relaxed_u64(&a.st[row].R_ge);
+    }
     float4 v[U];
     uint64_t valid = ~0ull;
     if (base + WT <= a.n) {
@@ -285,6 +298,9 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
         }
       }
     };
+    if constexpr (TIE) {
+      if (!over && __shfl_sync(FULL_MASK, rge, 0) >= static_cast<unsigned long long>(a.M)) over = true;
+    }
     if (over) {
       // The row's buffer is full: only the counts are left (per lane), and
       // with the bookkeeping the x > tau (those rarely exist when the tie exit
