@@ -50,7 +50,9 @@ extern "C" {
 typedef enum profk_status {
   PROFK_OK = 0,
   PROFK_ERR_INVALID = -1,        /* an argument is out of range or NULL */
-  PROFK_ERR_CUDA = -2,           /* a CUDA call failed; stats->cuda_error has the code */
+  PROFK_ERR_CUDA = -2,           /* a CUDA call failed (stats->cuda_error has the code), or a
+                                    device-side consistency check of the library's own state failed
+                                    (cuda_error 0; never expected) */
   PROFK_ERR_NAN = -3,            /* the input holds a NaN */
   PROFK_ERR_UNSUPPORTED = -4,    /* e.g. n >= 2^40 or a misaligned input */
   PROFK_ERR_DEVICE_TIMEOUT = -5, /* a bounded device-side wait gave up */

@@ -962,7 +962,8 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   }
   if (exact_ran || tie_ran) {
     // The exact selection's first pass counted NaN keys of its rows; a wait
-    // of the sort that ran out is recorded in the error bits.
+    // of the sort that ran out, or a tie list that does not hold exactly the
+    // R_gt keys above tau, is recorded in the error bits.
     char* rep = static_cast<char*>(hbuf) + sizeof(int) * rows * 4;
     PK_CHECK(cudaMemcpy2DAsync(rep, REPORT_BYTES, st, sizeof(RowState), REPORT_BYTES, rows, cudaMemcpyDeviceToHost,
                                stream));
@@ -976,8 +977,8 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         c.status = PROFK_ERR_NAN;
         goto done;
       }
-      if (errf & 8u) {
-        c.status = PROFK_ERR_DEVICE_TIMEOUT;
+      if (errf) {
+        c.status = (errf & 8u) ? PROFK_ERR_DEVICE_TIMEOUT : PROFK_ERR_CUDA;
         goto done;
       }
     }
