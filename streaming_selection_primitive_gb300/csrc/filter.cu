@@ -360,6 +360,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
             int pos = stage_n + static_cast<int>(incl - cnt);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
+              if (((ge >> (u * 4)) & 15ull) == 0) continue;  // sparse passers: skip empty groups
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 const int e = u * 4 + c;
