@@ -315,8 +315,8 @@ cudaError_t launch_tie_take(const TieArgs& a, int filter_grid, cudaStream_t stre
 
 cudaError_t launch_tie_after_filter(const TieArgs& a, const unsigned long long* buf, int64_t M,
                                     cudaStream_t stream) {
-  int64_t runs = (M + 8 * TG_THREADS - 1) / (8 * TG_THREADS);  // about eight keys per thread
-  if (runs > 64) runs = 64;
+  int64_t runs = (M + TG_THREADS - 1) / TG_THREADS;  // one key per thread: one round of atomics
+  if (runs > 1024) runs = 1024;
   if (runs < 1) runs = 1;
   launch_kernel(k_tie_gather, dim3(static_cast<unsigned>(runs), static_cast<unsigned>(a.nrows)), TG_THREADS, 0,
                 stream, a, buf, M);
