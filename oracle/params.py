@@ -143,8 +143,11 @@ def mean_rank(N: int, S: int, t: int) -> float:
 def sample_size_prop7(N: int, k: int, eps: float, r: float):
     """Proposition 7 candidates (S1, S2) for cost ratio r; kappa = z^2 + 1/2.
 
-    parity unpinned against the pages' Table 3 S column (that column also
-    depends on an unstated cap); the tests pin only Proposition 7's bracket.
+    Pinned by Proposition 7's bracket (the cost's minimiser lies between
+    max(S1, S2) and 2^(2/3) times it) and, through sample_size_corrected, by
+    the corrected page's Table 3 S column: exact on the rows the floor, the cap
+    or n/128 set, within 5 % on those S1 or S2 set (the printed two-digit
+    coefficients of r(k) are rounded).
     """
     z = norm_ppf(1.0 - eps / 2)
     kappa = z * z + 0.5
