@@ -130,3 +130,28 @@ def test_batched_rows_mix_the_forms(pk, cuda_device):
             (ost.path, ost.attempts, ost.R_first, ost.R_gt_first)
         paths.add(sts[r]["path"])
     assert pk.PATH_TIE in paths and pk.PATH_FILTER in paths
+
+
+def test_batched_rows_take_both_tie_forms_in_one_attempt(pk, cuda_device):
+    """Twelve tied rows with a tiny forced sample: in the same attempt some rows
+    hold tau once in their sample (the counting pass) and others more often
+    (the bookkeeping), so both tie flows run in one call, one after the other
+    on their own row lists."""
+    rows, n, k = 12, 1 << 20, 200
+    force = {"S": 256, "t": 1, "M": 400}
+    x = torch.stack([tied_top(n, 6000, 30, 500 + r, "cpu") for r in range(rows)]).to(cuda_device)
+    for o, v in ((pk.OPT_FORCE_S, 256), (pk.OPT_FORCE_T, 1), (pk.OPT_FORCE_M, 400)):
+        pk.set_option(o, v)
+    vals, idx, sts = pk.topk_batched(x, k, 1e-3, 17)
+    h = x.cpu().numpy()
+    forms_by_attempt = {}
+    for r in range(rows):
+        hr = np.ascontiguousarray(h[r])
+        ov, oi, ost = PK.profk(hr, k, 1e-3 / rows, 17, row=r, force=force, rows=rows)
+        assert_same(vals[r], idx[r], ov, oi, f"row {r}")
+        assert (sts[r]["path"], sts[r]["attempts"], sts[r]["R_final"], sts[r]["R_gt_final"]) == \
+            (ost.path, ost.attempts, ost.R_final, ost.R_gt_final)
+        if ost.path == PK.PATH_TIE:
+            copies = sample_copies_of_tau(hr, 256, 1, 17, ost.attempts - 1, row=r)
+            forms_by_attempt.setdefault(ost.attempts, set()).add(copies >= 2)
+    assert any(f == {False, True} for f in forms_by_attempt.values()), forms_by_attempt
