@@ -468,9 +468,10 @@ constexpr int64_t EXACT_TIE_MIN_N = int64_t(1) << 25;
 // one CTA per row.  Long rows: the k-th largest VALUE v_k by three radix
 // passes over the row's value keys (11, 11 and 10 bits), which also count
 // the x > v_k; then the tie step takes every x > v_k and the lowest-index
-// copies of v_k (one streaming pass and a re-read up to the last copy taken),
-// and the k keys are sorted: five reads of the row in all.  Other rows: the
-// radix selection of the 64-bit (value, index) keys, a compaction and the sort.
+// copies of v_k (one streaming pass, then a re-read of the blocks that hold
+// copies up to the last one taken), and the k keys are sorted: four reads of
+// the row and those blocks.  Other rows: the radix selection of the 64-bit
+// (value, index) keys, a compaction and the sort.
 void launch_exact(const Layout& L, void* ws, const float* x, int64_t ld, int nrows, const int* rows,
                   float* out_vals, int64_t* out_idx, cudaStream_t stream) {
   RowState* st = at<RowState>(ws, L.off_state);

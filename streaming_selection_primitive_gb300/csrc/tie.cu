@@ -15,7 +15,7 @@
 //  3. `k_tie_take`, CTAs striding over the blocks up to that one: a block's
 //     copies of tau in index order (one block-wide scan of its 16K
 //     elements), the first `need` of the row written after the x > tau keys.
-// Only the input up to the cut is read a second time.
+// Only the blocks up to the cut that hold copies of tau are read a second time.
 //
 // After a filter pass that ran with its tie bookkeeping, step 1 is not a
 // pass over the input: the filter has counted the copies of tau per block
@@ -215,6 +215,9 @@ __global__ void __launch_bounds__(1024) k_tie_cut(TieArgs a, bool check_gt) {
 // Block blk of a row: its copies of tau in index order, those of rank < need
 // written after the row's x > tau keys (all threads of the CTA call it).
 __device__ __forceinline__ void tie_take_block(const TieArgs& a, int row, int64_t blk, unsigned long long* sw) {
+  // A block without copies of tau has nothing to take: only the blocks that
+  // hold copies are read (for distinct values, one block however far the cut).
+  if (a.block_eq[static_cast<int64_t>(row) * a.nblocks + blk] == 0) return;
   const TieCtl& c = a.ctl[row];
   RowState& S = a.st[row];
   const float tau = key_to_float(S.tau_key);
