@@ -431,6 +431,9 @@ __device__ __forceinline__ void draw_quad(const SampleArgs& a, int row, uint64_t
   }
 }
 
+// WIDE: the launch's chunks are longer than the registers hold (the host
+// knows from the chunk length); each form is its own, smaller, kernel.
+template <bool WIDE>
 __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, SampleCtl* ctl) {
   pdl_trigger();
   pdl_wait();
@@ -463,7 +466,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   // thread t taking quads t, t + 512, ...; per quad one 16-byte shared-memory
   // entry that holds in turn the four draws' table slots, their values (or
   // NOT_FIRST), then the members' keys, and four membership bits.
-  const bool wide = hi - lo > static_cast<int64_t>(ST_HELD) * ST_THREADS;
+  const bool wide = WIDE;  // the held form needs every chunk within ST_HELD x ST_THREADS
   const int nq = static_cast<int>((hi - lo + 3) / 4);
   const int nm = (nq + ST_THREADS - 1) / ST_THREADS;  // rounds of quads
   uint4* W4 = st_dyn;
@@ -875,15 +878,16 @@ bool sample_tau_fits(int64_t D, int nrows, uint64_t n) {
 cudaError_t launch_sample_tau(const SampleArgs& a, void* ctl, cudaStream_t stream) {
   const int64_t G = sample_tau_chunks(a.D, a.nrows);
   const int64_t Dc = sample_tau_chunk_len(a.D, a.nrows);
-  size_t smem = 0;
   if (Dc > static_cast<int64_t>(ST_HELD) * ST_THREADS) {
     if (Dc > ST_WIDE_MAX || a.n >= (1ull << 32)) return cudaErrorInvalidValue;
-    smem = sample_tau_wide_smem(Dc);
-    cudaFuncSetAttribute(k_sample_tau, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(k_sample_tau<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(sample_tau_wide_smem(ST_WIDE_MAX)));
+    launch_kernel(k_sample_tau<true>, dim3(static_cast<unsigned>(G), static_cast<unsigned>(a.nrows)), ST_THREADS,
+                  sample_tau_wide_smem(Dc), stream, a, static_cast<SampleCtl*>(ctl));
+  } else {
+    launch_kernel(k_sample_tau<false>, dim3(static_cast<unsigned>(G), static_cast<unsigned>(a.nrows)), ST_THREADS, 0,
+                  stream, a, static_cast<SampleCtl*>(ctl));
   }
-  launch_kernel(k_sample_tau, dim3(static_cast<unsigned>(G), static_cast<unsigned>(a.nrows)), ST_THREADS, smem,
-                stream, a, static_cast<SampleCtl*>(ctl));
   return cudaGetLastError();
 }
 
