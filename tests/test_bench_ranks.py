@@ -66,3 +66,12 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
     args = argparse.Namespace(gpus=2, steps=3, warmup=3, n=1 << 30, k=1024)
     assert bench.run_reference(args) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_workload_names_and_l2_note():
+    assert bench.workload_name("normal", 1 << 30, 1024) == "normal_2^30_k1024"
+    assert bench.workload_name("levels16", 1 << 28, 4096) == "levels16_2^28_k4096"
+    assert bench.workload_name("sae", 50_331_648, 131_072) == "sae_50331648_k131072"
+    assert bench.l2_note(1 << 30).startswith("input 4295 MB > L2")
+    assert "hot-cache" in bench.l2_note(1 << 22)
+    assert set(bench.INPUTS) >= {"normal", "uniform", "pareto", "ulps_below_one", "levels16", "sae"}
