@@ -75,3 +75,21 @@ def test_workload_names_and_l2_note():
     assert bench.l2_note(1 << 30).startswith("input 4295 MB > L2")
     assert "hot-cache" in bench.l2_note(1 << 22)
     assert set(bench.INPUTS) >= {"normal", "uniform", "pareto", "ulps_below_one", "levels16", "sae"}
+
+
+def test_reference_arm_prints_its_line():
+    """The reference arm (the oracle on the host cores) prints one JSON line
+    with the contract's keys, without a GPU."""
+    import json
+    import subprocess
+    import sys
+
+    out = subprocess.run([sys.executable, str(bench.ROOT / "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=600, check=True).stdout
+    lines = [ln for ln in out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "Gelem/s"
+    assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
