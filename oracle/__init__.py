@@ -19,7 +19,9 @@ params     parameter rules: the corrected paper's Algorithm 1 (fast t, M), its
            (Lemma 2, Eq 6, Corollary 4, Theorem 5, its Algorithm 1).
 profk      the Prof-K pipeline itself (sample, threshold, filter, check, refine,
            redraw, fallback) written step by step, for stage parity and the
-           Monte-Carlo checks of Lemma 1 / Propositions 2-3.
+           Monte-Carlo checks of Lemma 1 / Propositions 2-3.  Whether a call
+           runs the method or an exact selection is passed in (``route``): a
+           library's routing rule is its own, not the pages'.
 
 Pins (what ties each function to something other than itself) live in
 ``tests/test_oracle_*.py``; every function whose header says "parity unpinned"

@@ -30,6 +30,41 @@ M of the corrected Theorem 4 (``params_exact``, pinned to Table 3).  A fourth
 follows the corrected Algorithm 1 throughout, its sample size included
 (Proposition 7 with a cost ratio r(k) calibrated on a GB300; the paper's own
 RTX 3060 calibration reproduces Table 3's S column).
+
+What pins each function (tests/test_oracle_params.py unless named):
+  norm_ppf                    scipy's ndtri within Acklam's stated 1.15e-9
+  prob_recall_failure,
+  prob_overflow, prob_fail    enumeration of every S-subset of a tiny [N]
+                              (tests/test_oracle_theory.py); Table 3's failure
+                              probabilities
+  params_exact                Table 3's t* and M* columns (21 rows)
+  threshold_rank_fast,
+  params_fast                 Table 3's t and M columns; k = 1 gives t = 1
+  buffer_capacity_fast        Table 3's M column; scipy's exact Gamma quantile
+                              (3 % high at t = 1, Appendix B, closing with t)
+  sample_size_prop7           Proposition 7's bracket around the numerical
+                              minimiser of the Eq 13 cost
+  sample_size_corrected,
+  inv_r_rtx3060               Table 3's S column with the paper's r(k)
+  params_corrected            its two steps
+  inv_r_gb300                 a measured calibration (its fit is tested in
+                              tests/test_calibrate_fit.py); parity unpinned
+                              by the pages, which fix only the form
+  lemma1_nhg_moments,
+  mean_rank                   enumeration (Eq 1-2; Lemma 6)
+  lemma2_normal               converges to Lemma 1's moments like 1/S at
+                              fixed S/N (Eq 3-4 as a limit)
+  t_eq6                       the smallest t meeting Eq 5's normal tail bound
+  m_cor4                      Eq 8 and Eq 11 (M = c k) algebra
+  s_thm5                      the numerical minimiser of Eq 13 with
+                              Corollary 4's M at f = 1 (Theorem 5)
+  s_star_scaling              the page's "S* ~ 4,600 at N = 1e9, k = 100"
+  sample_size_old             that minimiser rounded and clamped to
+                              [32768, 131072] (older Algorithm 1)
+  params_old                  Eq 6 / Eq 8 / Eq 11 at a point above the t = 1
+                              cut, and both sides of the cut at -ln(eps/2)
+  params                      composition of the above (the library's modes
+                              equal it: tests/test_abi.py)
 """
 from __future__ import annotations
 
@@ -258,14 +293,16 @@ def sample_size_old(N: int, k: int, eps: float, s_min: int = S_MIN_OLD,
 
 def params_old(N: int, k: int, eps: float, s_min: int = S_MIN_OLD, s_max: int = S_MAX_OLD,
                cost_ratio: float = 1.0):
-    """Older Algorithm 1, literally (all of its steps)."""
-    z = 2.0 * norm_ppf(1.0 - eps / 2)
-    alpha = k / N
+    """Older Algorithm 1, literally (all of its steps), through the named
+    closed forms: z = z_A + z_B with z_A = z_B = Phi^{-1}(1 - eps/2); S from
+    Theorem 5 (sample_size_old); t = max(1, Eq 6 with z_A); M = the ceiling of
+    Corollary 4 with z; and t = 1 when alpha S < -ln(eps/2)."""
+    z_half = norm_ppf(1.0 - eps / 2)
+    z = 2.0 * z_half
     S = sample_size_old(N, k, eps, s_min, s_max, cost_ratio)
-    f = 1.0 - S / N
-    t = max(1, math.ceil(S * alpha + z / 2.0 * math.sqrt(S * alpha * (1.0 - alpha) * f)))
-    M = math.ceil(k + z * math.sqrt(k * (N - k) / S * f))
-    if alpha * S < -math.log(eps / 2):
+    t = max(1, t_eq6(N, k, S, z_half))
+    M = math.ceil(m_cor4(N, k, S, z))
+    if (k / N) * S < -math.log(eps / 2):
         t = 1
     return S, t, M
 
@@ -294,23 +331,3 @@ def params(N: int, k: int, eps: float, mode: int = MODE_DEFAULT):
     t, M = params_fast(N, k, S, eps)
     return S, t, M
 
-
-def uses_filter(N: int, k: int, S: int, t: int, M: int, rows: int = 1) -> bool:
-    """Route: sample-and-filter when the sample is at most N/8 and the
-    parameters can meet the budget (t < S and M < N: at t = S or M = N the
-    rules were clamped, which happens as k approaches N), and, in calls of
-    128 or more rows with k <= 2048, only when S < N/32.  Otherwise the exact
-    path runs.
-
-    A sample that is a sizable share of the input is itself a full pass.  The
-    corrected paper keeps the method, at the floor sample size, for dense k
-    (Appendix B: "the floor is again the best choice" once k/N exceeds about
-    2^-10), and so does this rule: no cut on k/N (an earlier cut at k > N/64
-    measured 4-6 times slower on GB300 than sampling for k/N = 1/32 .. 1/8).
-    The rows clause is a choice of this implementation, not of the pages:
-    with many short rows, drawing 1/32 of every row by random access costs
-    more than an exact selection of each row by one CTA.
-    """
-    if 8 * S > N or t >= S or M >= N:
-        return False
-    return not (rows >= 128 and 32 * S >= N and k <= 2048)

@@ -20,6 +20,12 @@ It can be switched off (``tie_exit=False``) to follow the pages literally.
 
 Everything is per row; batched inputs run the procedure row by row with
 eps / rows per row (union bound, corrected paper Appendix E.2).
+
+Which calls run the method at all is not the oracle's decision: the caller
+passes ``route``.  ROUTE_FILTER runs the four stages above; ROUTE_EXACT
+returns the exact top-k without sampling (the result is the same either way;
+only the statistics differ).  The rule a library uses to pick the route is an
+implementation choice and lives with that library's tests.
 """
 from __future__ import annotations
 
@@ -35,6 +41,9 @@ PATH_FILTER = 0
 PATH_TIE = 1
 PATH_FALLBACK = 2
 PATH_EXACT = 3
+
+ROUTE_FILTER = "filter"
+ROUTE_EXACT = "exact"
 
 
 @dataclass
@@ -94,12 +103,15 @@ def tie_path(x: np.ndarray, tau, k: int):
     return refine(x[sel], sel, k)
 
 
-def profk(x: np.ndarray, k: int, eps: float, seed: int, row: int = 0, *, max_attempts: int = 6,
-          mode: int = P.MODE_DEFAULT, tie_exit: bool = True, force=None, rows: int = 1):
-    """One row of Prof-K.  ``force`` may override (S, t, M) as a dict; a forced
-    S recomputes t and M from it (the corrected Algorithm 1, t and M steps) unless those are
-    forced as well.  Any override routes through sampling.  ``rows`` is the
-    number of rows of the call the row belongs to (it enters the route)."""
+def profk(x: np.ndarray, k: int, eps: float, seed: int, row: int = 0, *, route: str = ROUTE_FILTER,
+          max_attempts: int = 6, mode: int = P.MODE_DEFAULT, tie_exit: bool = True, force=None):
+    """One row of Prof-K.  ``route`` (ROUTE_FILTER or ROUTE_EXACT) says whether
+    the method runs or the exact selection does (see the module docstring).
+    ``force`` may override (S, t, M) as a dict; a forced S recomputes t and M
+    from it (the corrected Algorithm 1, t and M steps) unless those are forced
+    as well."""
+    if route not in (ROUTE_FILTER, ROUTE_EXACT):
+        raise ValueError(f"route must be {ROUTE_FILTER!r} or {ROUTE_EXACT!r}")
     x = np.asarray(x, dtype=np.float32)
     if np.isnan(x).any():
         raise ValueError("NaN in input")
@@ -112,7 +124,7 @@ def profk(x: np.ndarray, k: int, eps: float, seed: int, row: int = 0, *, max_att
             t, M = P.params_fast(N, k, S, eps)
         t, M = force.get("t", t), force.get("M", M)
     st.S, st.t, st.M = S, t, M
-    if not P.uses_filter(N, k, S, t, M, rows) and not force:
+    if route == ROUTE_EXACT:
         st.path = PATH_EXACT
         v, i = topk_sort(x, k)
         return v, i, st

@@ -65,3 +65,24 @@ def test_batched_64_rows(pk, cuda_device):
         rv, ri = topk_partition(np.ascontiguousarray(h[r]), 32)
         assert_same(vals[r], idx[r], rv, ri, f"row {r}")
     assert all(s["path"] == pk.PATH_FILTER for s in sts) or any(s["attempts"] > 1 for s in sts)
+
+
+@pytest.mark.parametrize("k", [32, 1024, 1 << 19])
+def test_bench_protocol_async_2p30(pk, cuda_device, k):
+    """The call the benchmark times, in its launch configuration: 20
+    profk_topk_async calls in flight on the 2^30 standard-normal input (the
+    bench's input seed), each with its own output buffers, completed by
+    profk_wait in order; every call's values (bits), indices and order equal
+    the oracle's."""
+    x = workloads.normal(1 << 30, 1, cuda_device)
+    rv, ri = topk_partition(x.cpu().numpy(), k)
+    calls = 20
+    outs = [(torch.empty(k, dtype=torch.float32, device=cuda_device),
+             torch.empty(k, dtype=torch.int64, device=cuda_device)) for _ in range(calls)]
+    pending = [pk.topk_async(x, k, 1e-3, 1000 + s, out=outs[s]) for s in range(calls)]
+    for s, p in enumerate(pending):
+        v, i, st = p.wait()
+        assert_same(v, i, rv, ri, f"async call {s} k={k} stats={st}")
+        assert st["path"] in (pk.PATH_FILTER, pk.PATH_TIE) or st["attempts"] > 1
+    del x
+    torch.cuda.empty_cache()

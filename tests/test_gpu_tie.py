@@ -17,6 +17,7 @@ import torch
 from gpu_helpers import assert_same
 from oracle import philox as PX
 from oracle import profk as PK
+from routing import oracle_profk
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +49,7 @@ def run(pk, x, k, seed, force=None, eps=1e-3):
         pk.set_option(pk.OPT_FORCE_M, force.get("M", 0))
     vals, idx, st = pk.topk(x, k, eps, seed)
     h = x.cpu().numpy()
-    ov, oi, ost = PK.profk(h, k, eps, seed, force=force)
+    ov, oi, ost = oracle_profk(h, k, eps, seed, force=force)
     assert_same(vals, idx, ov, oi, f"k={k} seed={seed} force={force} stats={st}")
     assert (st["path"], st["attempts"], st["R_first"], st["R_gt_first"], st["R_final"], st["R_gt_final"]) == \
         (ost.path, ost.attempts, ost.R_first, ost.R_gt_first, ost.R_final, ost.R_gt_final)
@@ -124,7 +125,7 @@ def test_batched_rows_mix_the_forms(pk, cuda_device):
     h = x.cpu().numpy()
     paths = set()
     for r in range(rows):
-        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 9, row=r, rows=rows)
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 9, row=r, rows=rows)
         assert_same(vals[r], idx[r], ov, oi, f"row {r}")
         assert (sts[r]["path"], sts[r]["attempts"], sts[r]["R_first"], sts[r]["R_gt_first"]) == \
             (ost.path, ost.attempts, ost.R_first, ost.R_gt_first)
@@ -147,7 +148,7 @@ def test_batched_rows_take_both_tie_forms_in_one_attempt(pk, cuda_device):
     forms_by_attempt = {}
     for r in range(rows):
         hr = np.ascontiguousarray(h[r])
-        ov, oi, ost = PK.profk(hr, k, 1e-3 / rows, 17, row=r, force=force, rows=rows)
+        ov, oi, ost = oracle_profk(hr, k, 1e-3 / rows, 17, row=r, force=force, rows=rows)
         assert_same(vals[r], idx[r], ov, oi, f"row {r}")
         assert (sts[r]["path"], sts[r]["attempts"], sts[r]["R_final"], sts[r]["R_gt_final"]) == \
             (ost.path, ost.attempts, ost.R_final, ost.R_gt_final)

@@ -11,6 +11,7 @@ import workloads
 from gpu_helpers import assert_same
 from oracle import params as PP
 from oracle import profk as PK
+from routing import oracle_profk, uses_filter
 from oracle.topk import topk_sort
 
 pytestmark = pytest.mark.gpu
@@ -25,7 +26,7 @@ def check_call(pk, x, k, eps, seed, force=None, tie_exit=True, max_attempts=6):
     pk.set_option(pk.OPT_MAX_ATTEMPTS, max_attempts)
     vals, idx, st = pk.topk(x, k, eps, seed)
     h = x.cpu().numpy()
-    ov, oi, ost = PK.profk(h, k, eps, seed, force=force, tie_exit=tie_exit, max_attempts=max_attempts)
+    ov, oi, ost = oracle_profk(h, k, eps, seed, force=force, tie_exit=tie_exit, max_attempts=max_attempts)
     assert_same(vals, idx, ov, oi, f"n={h.size} k={k} seed={seed} force={force}")
     assert (st["S"], st["t"], st["M"]) == (ost.S, ost.t, ost.M)
     assert st["path"] == ost.path, (st, ost)
@@ -98,7 +99,7 @@ def test_dense_k(pk, cuda_device, n, k):
     x = workloads.normal(n, 17, cuda_device)
     st = check_call(pk, x, k, 1e-3, 8)
     S, t, M = PP.params(n, k, 1e-3)
-    assert st["path"] == (pk.PATH_FILTER if PP.uses_filter(n, k, S, t, M) else pk.PATH_EXACT)
+    assert st["path"] == (pk.PATH_FILTER if uses_filter(n, k, S, t, M) else pk.PATH_EXACT)
 
 
 def test_nan_rejected(pk, cuda_device):
@@ -159,7 +160,7 @@ def test_batched(pk, cuda_device, rows, n, ld, k):
     h = x.cpu().numpy()
     eps_row = 1e-3 / rows
     for r in range(rows):
-        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, eps_row, 11, row=r, rows=rows)
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, eps_row, 11, row=r, rows=rows)
         assert_same(vals[r], idx[r], ov, oi, f"batched row {r}")
         assert sts[r]["path"] == ost.path and sts[r]["R_first"] == ost.R_first
         assert sts[r]["R_gt_first"] == ost.R_gt_first
@@ -187,7 +188,7 @@ def test_batched_sampler_forms(pk, cuda_device, form, rows, n, k):
     vals, idx, sts = pk.topk_batched(x, k, 1e-3, 21)
     h = x.cpu().numpy()
     for r in range(rows):
-        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 21, row=r, rows=rows)
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 21, row=r, rows=rows)
         assert_same(vals[r], idx[r], ov, oi, f"{form} row {r}")
         assert (sts[r]["path"], sts[r]["R_first"], sts[r]["R_gt_first"]) == (ost.path, ost.R_first, ost.R_gt_first)
         assert sts[r]["tau_first"] == ost.taus[0]
@@ -203,7 +204,7 @@ def test_batched_rows_retry_alone(pk, cuda_device):
     vals, idx, sts = pk.topk_batched(x, k, 1e-3, 5)
     h = x.cpu().numpy()
     for r in range(rows):
-        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 5, row=r, force=force, rows=rows)
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 5, row=r, force=force, rows=rows)
         assert_same(vals[r], idx[r], ov, oi, f"row {r}")
         assert (sts[r]["attempts"], sts[r]["path"], sts[r]["R_first"]) == (ost.attempts, ost.path, ost.R_first)
 
@@ -240,7 +241,7 @@ def test_batched_wide_sampler_rows_retry_alone(pk, cuda_device, form):
     h = x.cpu().numpy()
     retried = 0
     for r in range(rows):
-        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 8, row=r, force=force, rows=rows)
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 8, row=r, force=force, rows=rows)
         assert_same(vals[r], idx[r], ov, oi, f"row {r}")
         assert (sts[r]["attempts"], sts[r]["path"], sts[r]["R_first"], sts[r]["tau_first"]) == \
             (ost.attempts, ost.path, ost.R_first, ost.taus[0])
@@ -274,7 +275,7 @@ def test_batched_large_k_rows_retry_alone(pk, cuda_device):
     vals, idx, sts = pk.topk_batched(x, k, 1e-3, 6)
     h = x.cpu().numpy()
     for r in range(rows):
-        ov, oi, ost = PK.profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 6, row=r, force=force, rows=rows)
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 6, row=r, force=force, rows=rows)
         assert_same(vals[r], idx[r], ov, oi, f"row {r}")
         assert (sts[r]["attempts"], sts[r]["path"], sts[r]["R_first"]) == (ost.attempts, ost.path, ost.R_first)
 
@@ -319,7 +320,7 @@ def test_batched_many_rows(pk, cuda_device, rows, n, k):
         assert_same(vals[r], idx[r], *topk_sort(h, k), f"row {r}")
     paths = {s["path"] for s in sts}
     S, t, M = sts[0]["S"], sts[0]["t"], sts[0]["M"]
-    assert paths == ({pk.PATH_FILTER} if PP.uses_filter(n, k, S, t, M, rows) else {pk.PATH_EXACT})
+    assert paths == ({pk.PATH_FILTER} if uses_filter(n, k, S, t, M, rows) else {pk.PATH_EXACT})
 
 
 def test_exact_parameter_mode(pk, cuda_device):
@@ -329,7 +330,7 @@ def test_exact_parameter_mode(pk, cuda_device):
     h = x.cpu().numpy()
     for k in (32, 1000):
         vals, idx, st = pk.topk(x, k, 1e-3, 4)
-        ov, oi, ost = PK.profk(h, k, 1e-3, 4, mode=2)
+        ov, oi, ost = oracle_profk(h, k, 1e-3, 4, mode=2)
         assert_same(vals, idx, ov, oi, f"exact-parameter mode k={k}")
         assert (st["S"], st["t"], st["M"]) == (ost.S, ost.t, ost.M)
         assert st["R_first"] == ost.R_first and st["attempts"] == ost.attempts
@@ -343,7 +344,7 @@ def test_corrected_parameter_mode(pk, cuda_device, n, k):
     pk.set_option(pk.OPT_PARAM_MODE, pk.PARAMS_CORRECTED)
     h = x.cpu().numpy()
     vals, idx, st = pk.topk(x, k, 1e-3, 5)
-    ov, oi, ost = PK.profk(h, k, 1e-3, 5, mode=PP.MODE_CORRECTED)
+    ov, oi, ost = oracle_profk(h, k, 1e-3, 5, mode=PP.MODE_CORRECTED)
     assert_same(vals, idx, ov, oi, f"corrected-parameter mode n={n} k={k}")
     assert (st["S"], st["t"], st["M"]) == (ost.S, ost.t, ost.M) == PP.params(n, k, 1e-3, PP.MODE_CORRECTED)
     assert st["R_first"] == ost.R_first and st["attempts"] == ost.attempts and st["path"] == ost.path
@@ -352,14 +353,20 @@ def test_corrected_parameter_mode(pk, cuda_device, n, k):
 STAT_KEYS = ("S", "t", "M", "R_first", "R_gt_first", "tau_first", "R_final", "attempts", "path")
 
 
-def test_async_matches_sync(pk, cuda_device):
+def test_async_matches_oracle_and_sync(pk, cuda_device):
+    """Asynchronous calls in flight together: each equals the oracle procedure
+    (result, path and counts) and the synchronous call's statistics."""
     x = workloads.normal((1 << 22) + 4, 21, cuda_device)
+    h = x.cpu().numpy()
     calls = ((1, 32), (2, 1000), (3, 5000), (4, 20000))
     ref = [pk.topk(x, k, 1e-3, s) for s, k in calls]
     pend = [pk.topk_async(x, k, 1e-3, s) for s, k in calls]  # all in flight at once
-    for p, r in zip(pend, ref):
+    for p, r, (s, k) in zip(pend, ref, calls):
         v, i, st = p.wait()
-        assert torch.equal(v, r[0]) and torch.equal(i, r[1])
+        ov, oi, ost = oracle_profk(h, k, 1e-3, s)
+        assert_same(v, i, ov, oi, f"async k={k} seed={s}")
+        assert (st["S"], st["t"], st["M"], st["path"], st["attempts"]) == (ost.S, ost.t, ost.M, ost.path, ost.attempts)
+        assert (st["R_first"], st["R_gt_first"], st["tau_first"]) == (ost.R_first, ost.R_gt_first, ost.taus[0])
         assert all(st[key] == r[2][key] for key in STAT_KEYS), (st, r[2])
 
 
@@ -370,7 +377,7 @@ def test_async_rerun_when_not_cleared(pk, cuda_device):
     h = x.cpu().numpy()
     for k in (100, 5000):
         v, i, st = pk.topk_async(x, k, 1e-3, 5).wait()
-        ov, oi, ost = PK.profk(h, k, 1e-3, 5)
+        ov, oi, ost = oracle_profk(h, k, 1e-3, 5)
         assert_same(v, i, ov, oi, f"async tie k={k}")
         assert st["path"] == ost.path and st["attempts"] == ost.attempts
 
@@ -380,10 +387,14 @@ def test_async_resumes_redraws(pk, cuda_device):
     # continues from its first attempt (redraw, then the filter again) and
     # must end exactly as the synchronous call: result and every statistic.
     x = workloads.normal((1 << 20) + 4, 23, cuda_device)
+    h = x.cpu().numpy()
     redraws = 0
     for seed in range(12):
         ref = pk.topk(x, 300, 0.5, seed)
         v, i, st = pk.topk_async(x, 300, 0.5, seed).wait()
+        ov, oi, ost = oracle_profk(h, 300, 0.5, seed)
+        assert_same(v, i, ov, oi, f"resumed async seed={seed}")
+        assert (st["attempts"], st["path"], st["R_final"]) == (ost.attempts, ost.path, ost.R_final)
         assert torch.equal(v, ref[0]) and torch.equal(i, ref[1])
         assert all(st[key] == ref[2][key] for key in STAT_KEYS + ("R_gt_final",)), (seed, st, ref[2])
         redraws += st["attempts"] > 1

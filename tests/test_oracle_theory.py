@@ -91,8 +91,10 @@ def test_paths_are_reached():
     v, i, st = PK.profk(x, 10, 1e-3, 1, force={"S": 256, "t": 5, "M": 100}, tie_exit=False)
     assert st.path == PK.PATH_FALLBACK and st.attempts == 6
     y = np.random.default_rng(2).standard_normal(1 << 16).astype(np.float32)
-    v, i, st = PK.profk(y, 64, 1e-3, 3)
-    assert st.path == PK.PATH_EXACT  # S = 32768 > n / 8
+    v, i, st = PK.profk(y, 64, 1e-3, 3, route=PK.ROUTE_EXACT)
+    assert st.path == PK.PATH_EXACT and st.attempts == 0 and same_result(v, i, *topk_sort(y, 64))
+    v, i, st = PK.profk(y, 64, 1e-3, 3)  # the method itself, even with S = n / 2
+    assert st.path == PK.PATH_FILTER and same_result(v, i, *topk_sort(y, 64))
     v, i, st = PK.profk(y, 16, 1e-3, 3, force={"S": 2048, "t": 4, "M": 500})
     assert st.path == PK.PATH_FILTER and k_le(16, st.R_first, 500)
 
