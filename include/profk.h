@@ -292,16 +292,34 @@ int profk_exact(const float* x, int64_t n, int64_t k, float* out_vals, int64_t* 
  * GPU that loads the library holds this much device memory until exit. */
 #define PROFK_NOALLOC_SCRATCH_BYTES (32u << 20)
 
-/* Exact top-k of one row, with the same arguments, result and statistics as
+/* Exact top-k of one row, with the arguments and the exact result of
  * profk_topk, but without allocating anything: no cudaMalloc/cudaMallocAsync,
  * no pinned host buffer, no pool.  The paper has no counterpart to this entry
  * point; it exists for callers that must not allocate on the call path (a
  * latency-bounded serving loop, a plugin whose host owns all device memory
  * through its own allocator, a process whose pool already holds nearly all
  * of the GPU).  The workspace is a static device array of
- * PROFK_NOALLOC_SCRATCH_BYTES reserved when the library is loaded.
- *   Limits: a problem whose workspace (profk_workspace_size(1, n, k, eps))
- *     exceeds the array returns PROFK_ERR_SCRATCH before any device work.
+ * PROFK_NOALLOC_SCRATCH_BYTES reserved when the library is loaded.  The call
+ * runs the step-by-step kernels (sampler, radix selections, sorts without
+ * scratch), not the persistent ones of profk_topk, and synchronizes `stream`
+ * once per attempt and once at the end.
+ *   Limits: n <= 2^32 (longer rows return PROFK_ERR_UNSUPPORTED) and x
+ *     16-byte aligned (else PROFK_ERR_UNSUPPORTED).  The array must hold, at
+ *     the parameters (S, t, M) that profk_params gives, each part rounded up
+ *     to 256 bytes: the row state (8.3 KB); on the sampling route a hash table
+ *     of 8 x (the power of two >= 2D) bytes with D = S + 2r + 8 sqrt(r) + 256
+ *     draws (r = S^2 / 2n, rounded up to a multiple of 4), 4D bytes of draws,
+ *     4 ceil(D / 1024) bytes of counts, 8S bytes of sample and 8M bytes of
+ *     candidate buffer; and 8 K bytes of selected keys, K = k for k <= 8192,
+ *     else the power of two >= k.  A problem that needs more returns
+ *     PROFK_ERR_SCRATCH before any device work.  If D draws hold fewer than S
+ *     distinct indices (practically never), D doubles and the need is checked
+ *     again, so such a call can return PROFK_ERR_SCRATCH after device work.
+ *   Errors: as profk_topk, including PROFK_ERR_CUDA / PROFK_ERR_DEVICE_TIMEOUT
+ *     when a device-side check of any step fails.
+ *   Statistics: S, t, M, the counts, tau, attempts and path as profk_topk;
+ *     aux_bytes is 0 (nothing was allocated); launches counts this call's
+ *     kernels, which differ from profk_topk's.
  *   Sharing: every call on a device uses the same array and finds the
  *     previous call's contents there (it clears what must start at zero);
  *     calls whose GPU work overlaps on one device race and must be ordered
@@ -310,7 +328,7 @@ int profk_exact(const float* x, int64_t n, int64_t k, float* out_vals, int64_t* 
  *     with that device current and caches it; make that first call before any
  *     stream capture.
  *   Options honoured: PROFK_OPT_PARAM_MODE, PROFK_OPT_MAX_ATTEMPTS,
- *     PROFK_OPT_TIE_EXIT.  stats->aux_bytes is 0 (nothing was allocated). */
+ *     PROFK_OPT_TIE_EXIT. */
 int profk_topk_noalloc(const float* x, int64_t n, int64_t k, double eps, uint64_t seed,
                        float* out_vals, int64_t* out_idx, cudaStream_t stream,
                        profk_stats* stats);

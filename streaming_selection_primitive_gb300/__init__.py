@@ -17,7 +17,7 @@ from ._abi import (OPT_FILTER_CTAS_PER_SM, OPT_FORCE_M, OPT_FORCE_S, OPT_FORCE_T
                    PARAMS_DEFAULT, PARAMS_EXACT, SAMPLER_AUTO, SAMPLER_GRID, SAMPLER_STEPS,
                    PARAMS_OLD, PATH_EXACT, PATH_FALLBACK, PATH_FILTER, PATH_TIE, ProfkError, ProfkStats)
 
-__all__ = ["topk", "topk_batched", "params", "workspace_size", "set_option", "get_option", "reset_options",
+__all__ = ["topk", "topk_batched", "topk_noalloc", "params", "workspace_size", "set_option", "get_option", "reset_options",
            "sample", "threshold", "filter_pass", "refine", "exact", "last_stage_ms", "ProfkError", "ProfkStats",
            "lib"]
 
@@ -116,6 +116,27 @@ def topk(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=None):
     st = ProfkStats()
     code = lib().profk_topk(x.data_ptr(), n, int(k), float(eps), int(seed) & (2**64 - 1), vals.data_ptr(),
                             idx.data_ptr(), _stream_handle(stream, x.device), C.byref(st))
+    _abi.check(code)
+    return vals, idx, st.as_dict()
+
+
+def topk_noalloc(x, k: int, eps: float = 1e-3, seed: int = 0, out=None, stream=None):
+    """topk through profk_topk_noalloc: the call itself allocates no device or
+    pinned memory (the library's fixed scratch array serves it; calls that
+    overlap on one device race on that array).  Pass ``out`` = (values, indices)
+    to keep this wrapper from allocating the outputs too."""
+    torch = _torch()
+    _need_cuda_f32(x)
+    if x.dim() != 1 or not x.is_contiguous():
+        raise ValueError("x must be 1-D and contiguous")
+    if out is None:
+        vals = torch.empty(k, dtype=torch.float32, device=x.device)
+        idx = torch.empty(k, dtype=torch.int64, device=x.device)
+    else:
+        vals, idx = out
+    st = ProfkStats()
+    code = lib().profk_topk_noalloc(x.data_ptr(), x.numel(), int(k), float(eps), int(seed) & (2**64 - 1),
+                                    vals.data_ptr(), idx.data_ptr(), _stream_handle(stream, x.device), C.byref(st))
     _abi.check(code)
     return vals, idx, st.as_dict()
 

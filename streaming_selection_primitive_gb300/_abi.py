@@ -12,6 +12,7 @@ PROFK_ERR_CUDA = -2
 PROFK_ERR_NAN = -3
 PROFK_ERR_UNSUPPORTED = -4
 PROFK_ERR_DEVICE_TIMEOUT = -5
+PROFK_ERR_SCRATCH = -6
 
 PATH_FILTER, PATH_TIE, PATH_FALLBACK, PATH_EXACT = 0, 1, 2, 3
 PARAMS_DEFAULT, PARAMS_OLD, PARAMS_EXACT, PARAMS_CORRECTED = 0, 1, 2, 3
@@ -86,6 +87,8 @@ _SIGS = {
                                C.c_void_p, C.c_void_p]),
     "profk_exact": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
     "profk_last_stage_ms": (C.c_int, [C.POINTER(C.c_float), C.c_int]),
+    "profk_topk_noalloc": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_double, C.c_uint64,
+                                     C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(ProfkStats)]),
 }
 
 

@@ -129,133 +129,152 @@ extern "C" int profk_topk_noalloc(const float* x, int64_t n, int64_t k, double e
   s.M = P.M;
   s.R_first = s.R_gt_first = s.R_final = s.R_gt_final = -1;
   s.filter_ms = -1.f;
+  s.path = sampling ? PROFK_PATH_FALLBACK : PROFK_PATH_EXACT;
   const int64_t launches0 = launch_count();
   int status = PROFK_OK;
   cudaError_t err = cudaSuccess;
   void* base = nullptr;
   RowState* st = nullptr;
   alignas(16) unsigned char rep[offsetof(RowState, hist)];
-  bool exact = !sampling;
+  bool ended = false;  // a terminal path (refinement, tie exit, exact selection) was enqueued
   int sms = 1;
 
-#define NA_CHECK(expr)          \
-  do {                          \
-    err = (expr);               \
-    if (err != cudaSuccess) {   \
-      status = PROFK_ERR_CUDA;  \
-      goto done;                \
-    }                           \
-  } while (0)
+  // The row state's head (counts, error bits) back on the host, the stream synchronized.
+  auto read_report = [&]() -> bool {
+    err = cudaMemcpyAsync(rep, st, sizeof(rep), cudaMemcpyDeviceToHost, stream);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess) status = PROFK_ERR_CUDA;
+    return err == cudaSuccess;
+  };
+  auto word = [&](size_t off) {
+    unsigned v = 0;
+    std::memcpy(&v, rep + off, 4);
+    return v;
+  };
+  auto dword = [&](size_t off) {
+    unsigned long long v = 0;
+    std::memcpy(&v, rep + off, 8);
+    return v;
+  };
+  // A device-side check that failed (a bounded wait that ran out: bit 8) ends the call.
+  auto error_status = [](unsigned errf) { return (errf & 8u) ? PROFK_ERR_DEVICE_TIMEOUT : PROFK_ERR_CUDA; };
 
-  NA_CHECK(scratch_address(&base));
-  st = in<RowState>(base, 0);
-  {
+  err = scratch_address(&base);
+  if (err == cudaSuccess) {
     int dev = 0;
-    NA_CHECK(cudaGetDevice(&dev));
-    NA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   }
-  if (sampling) {
-    int64_t a = 0;
-    while (a < max_attempts) {
-      NA_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
-      NA_CHECK(cudaMemsetAsync(in<void>(base, L.off_table), 0xff,
-                               sizeof(unsigned long long) * (static_cast<size_t>(1) << L.log2H), stream));
-      SampleArgs sa{x, n, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, static_cast<int>(a), 1, nullptr, st,
-                    in<unsigned long long>(base, L.off_table), in<uint32_t>(base, L.off_draws),
-                    in<uint32_t>(base, L.off_blockcnt), in<uint32_t>(base, L.off_sidx),
-                    in<uint32_t>(base, L.off_skeys)};
-      launch_sample(sa, stream);
-      SelectArgs ta{KeySource::SampleKeys, in<uint32_t>(base, L.off_skeys), P.S, P.S, 1, nullptr, st};
-      launch_select(ta, static_cast<uint64_t>(P.t), true, 0, stream);
-      launch_store_tau(1, nullptr, st, stream);
-      FilterArgs fa{x, n, n, P.M, 1, nullptr, st, in<unsigned long long>(base, L.off_buf),
-                    filter_default_grid(sms)};
-      launch_filter(fa, stream);
-      NA_CHECK(cudaGetLastError());
-      NA_CHECK(cudaMemcpyAsync(rep, st, sizeof(rep), cudaMemcpyDeviceToHost, stream));
-      NA_CHECK(cudaStreamSynchronize(stream));
-      unsigned long long Rg = 0, Rt = 0, nanc = 0;
-      unsigned distinct = 0, tau_key = 0, errf = 0;
-      std::memcpy(&Rg, rep + offsetof(RowState, R_ge), 8);
-      std::memcpy(&Rt, rep + offsetof(RowState, R_gt), 8);
-      std::memcpy(&nanc, rep + offsetof(RowState, nan), 8);
-      std::memcpy(&distinct, rep + offsetof(RowState, distinct), 4);
-      std::memcpy(&tau_key, rep + offsetof(RowState, tau_key), 4);
-      std::memcpy(&errf, rep + offsetof(RowState, error), 4);
-      if (nanc > 0) {
-        status = PROFK_ERR_NAN;
-        goto done;
-      }
-      if (errf) {
+  if (err != cudaSuccess) status = PROFK_ERR_CUDA;
+  st = in<RowState>(base, 0);
+
+  // Steps 1-4 per attempt; redraws with attempt + 1, up to max_attempts.
+  for (int64_t a = 0; status == PROFK_OK && sampling && !ended && a < max_attempts;) {
+    err = cudaMemsetAsync(st, 0, sizeof(RowState), stream);
+    if (err == cudaSuccess)
+      err = cudaMemsetAsync(in<void>(base, L.off_table), 0xff,
+                            sizeof(unsigned long long) * (static_cast<size_t>(1) << L.log2H), stream);
+    if (err != cudaSuccess) {
+      status = PROFK_ERR_CUDA;
+      break;
+    }
+    SampleArgs sa{x, n, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, static_cast<int>(a), 1, nullptr, st,
+                  in<unsigned long long>(base, L.off_table), in<uint32_t>(base, L.off_draws),
+                  in<uint32_t>(base, L.off_blockcnt), in<uint32_t>(base, L.off_sidx), in<uint32_t>(base, L.off_skeys)};
+    launch_sample(sa, stream);
+    SelectArgs ta{KeySource::SampleKeys, in<uint32_t>(base, L.off_skeys), P.S, P.S, 1, nullptr, st};
+    launch_select(ta, static_cast<uint64_t>(P.t), true, 0, stream);
+    launch_store_tau(1, nullptr, st, stream);
+    FilterArgs fa{x, n, n, P.M, 1, nullptr, st, in<unsigned long long>(base, L.off_buf), filter_default_grid(sms)};
+    launch_filter(fa, stream);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) {
+      status = PROFK_ERR_CUDA;
+      break;
+    }
+    if (!read_report()) break;
+    const unsigned long long Rg = dword(offsetof(RowState, R_ge)), Rt = dword(offsetof(RowState, R_gt));
+    const unsigned errf = word(offsetof(RowState, error));
+    if (dword(offsetof(RowState, nan)) > 0) {
+      status = PROFK_ERR_NAN;
+      break;
+    }
+    if (errf) {
+      status = error_status(errf);
+      break;
+    }
+    if (static_cast<int64_t>(word(offsetof(RowState, distinct))) < P.S) {  // more draws, same attempt
+      if (s.draw_doublings >= 24) {  // cannot happen for S <= n/2
         status = PROFK_ERR_CUDA;
-        goto done;
+        break;
       }
-      if (static_cast<int64_t>(distinct) < P.S) {  // more draws, same attempt
-        if (++s.draw_doublings > 24) {
-          status = PROFK_ERR_CUDA;
-          goto done;
-        }
-        D *= 2;
-        L = plan(P.S, D, P.M, k, true);
-        if (L.total > PROFK_NOALLOC_SCRATCH_BYTES) {
-          status = PROFK_ERR_SCRATCH;
-          goto done;
-        }
-        continue;
-      }
-      s.attempts = static_cast<int32_t>(a + 1);
-      const float tau = key_to_float(tau_key);
-      if (a == 0) {
-        s.R_first = static_cast<int64_t>(Rg);
-        s.R_gt_first = static_cast<int64_t>(Rt);
-        s.tau_first = tau;
-      }
-      s.R_final = static_cast<int64_t>(Rg);
-      s.R_gt_final = static_cast<int64_t>(Rt);
-      s.tau_final = tau;
-      uint64_t* sel = in<uint64_t>(base, L.off_sel);
-      if (static_cast<uint64_t>(k) <= Rg && Rg <= static_cast<uint64_t>(P.M)) {
-        s.path = PROFK_PATH_FILTER;
-        SelectArgs ra{KeySource::Buffer, in<unsigned long long>(base, L.off_buf), P.M, P.M, 1, nullptr, st};
-        launch_select(ra, static_cast<uint64_t>(k), false, 0, stream);
-        launch_compact(ra, sel, L.kstride, k, stream);
-        launch_sort_emit(sel, L.kstride, k, 1, nullptr, x, n, n, out_vals, out_idx, stream);
-        NA_CHECK(cudaGetLastError());
-        goto done;
-      }
-      if (tie_exit && Rg > static_cast<uint64_t>(P.M) && Rt < static_cast<uint64_t>(k)) {
-        s.path = PROFK_PATH_TIE;
-        launch_tie_init(1, nullptr, st, k, stream);
-        SelectArgs ia{KeySource::Input, x, n, n, 1, nullptr, st};
-        launch_select(ia, 0, false, 3, stream);
-        launch_compact(ia, sel, L.kstride, k, stream);
-        launch_sort_emit(sel, L.kstride, k, 1, nullptr, x, n, n, out_vals, out_idx, stream);
-        NA_CHECK(cudaGetLastError());
-        goto done;
-      }
+      s.draw_doublings += 1;
+      D *= 2;
+      L = plan(P.S, D, P.M, k, true);
+      if (L.total > PROFK_NOALLOC_SCRATCH_BYTES) status = PROFK_ERR_SCRATCH;
+      continue;
+    }
+    s.attempts = static_cast<int32_t>(a + 1);
+    const float tau = key_to_float(word(offsetof(RowState, tau_key)));
+    if (a == 0) {
+      s.R_first = static_cast<int64_t>(Rg);
+      s.R_gt_first = static_cast<int64_t>(Rt);
+      s.tau_first = tau;
+    }
+    s.R_final = static_cast<int64_t>(Rg);
+    s.R_gt_final = static_cast<int64_t>(Rt);
+    s.tau_final = tau;
+    uint64_t* sel = in<uint64_t>(base, L.off_sel);
+    if (static_cast<uint64_t>(k) <= Rg && Rg <= static_cast<uint64_t>(P.M)) {
+      // Refinement: exact top-k of the R buffered keys.
+      s.path = PROFK_PATH_FILTER;
+      SelectArgs ra{KeySource::Buffer, in<unsigned long long>(base, L.off_buf), P.M, P.M, 1, nullptr, st};
+      launch_select(ra, static_cast<uint64_t>(k), false, 0, stream);
+      launch_compact(ra, sel, L.kstride, k, stream);
+      launch_sort_emit(sel, L.kstride, k, 1, nullptr, x, n, n, out_vals, out_idx, stream);
+      ended = true;
+    } else if (tie_exit && Rg > static_cast<uint64_t>(P.M) && Rt < static_cast<uint64_t>(k)) {
+      // Tie exit: tau is the k-th largest value; x > tau and the lowest-index copies of tau.
+      s.path = PROFK_PATH_TIE;
+      launch_tie_init(1, nullptr, st, k, stream);
+      SelectArgs ia{KeySource::Input, x, n, n, 1, nullptr, st};
+      launch_select(ia, 0, false, 3, stream);
+      launch_compact(ia, sel, L.kstride, k, stream);
+      launch_sort_emit(sel, L.kstride, k, 1, nullptr, x, n, n, out_vals, out_idx, stream);
+      ended = true;
+    } else {
       ++a;
     }
-    s.path = PROFK_PATH_FALLBACK;
-    exact = true;
-  } else {
-    s.path = PROFK_PATH_EXACT;
   }
-  if (exact) {
-    NA_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
-    uint64_t* sel = in<uint64_t>(base, L.off_sel);
-    SelectArgs ea{KeySource::Input, x, n, n, 1, nullptr, st};
-    launch_select(ea, static_cast<uint64_t>(k), false, 0, stream);
-    launch_compact(ea, sel, L.kstride, k, stream);
-    launch_sort_emit(sel, L.kstride, k, 1, nullptr, x, n, n, out_vals, out_idx, stream);
-    NA_CHECK(cudaGetLastError());
-    NA_CHECK(cudaMemcpyAsync(rep, st, sizeof(rep), cudaMemcpyDeviceToHost, stream));
-    NA_CHECK(cudaStreamSynchronize(stream));
-    unsigned long long q = 0;
-    std::memcpy(&q, rep + offsetof(RowState, sel_nan), 8);
-    if (q) status = PROFK_ERR_NAN;
+  if (status == PROFK_OK && !ended) {
+    // The exact selection over the row: the exact route, or the fallback after
+    // every attempt failed the check.
+    err = cudaMemsetAsync(st, 0, sizeof(RowState), stream);
+    if (err != cudaSuccess) status = PROFK_ERR_CUDA;
+    if (status == PROFK_OK) {
+      uint64_t* sel = in<uint64_t>(base, L.off_sel);
+      SelectArgs ea{KeySource::Input, x, n, n, 1, nullptr, st};
+      launch_select(ea, static_cast<uint64_t>(k), false, 0, stream);
+      launch_compact(ea, sel, L.kstride, k, stream);
+      launch_sort_emit(sel, L.kstride, k, 1, nullptr, x, n, n, out_vals, out_idx, stream);
+      ended = true;
+    }
   }
-#undef NA_CHECK
-done:
+  if (status == PROFK_OK && ended) {
+    // The terminal path's own device checks: a NaN found by the exact
+    // selection's first pass, or any error bit (a selection that found no
+    // digit, a bounded wait that ran out) fails the call as profk_topk does.
+    err = cudaGetLastError();
+    if (err != cudaSuccess) {
+      status = PROFK_ERR_CUDA;
+    } else if (read_report()) {
+      const unsigned errf = word(offsetof(RowState, error));
+      if (s.path >= PROFK_PATH_FALLBACK && dword(offsetof(RowState, sel_nan)) > 0)
+        status = PROFK_ERR_NAN;
+      else if (errf)
+        status = error_status(errf);
+    }
+  }
   if (stats) {
     s.aux_bytes = 0;  // nothing was allocated; the call used L.total bytes of the fixed scratch
     s.cuda_error = static_cast<int32_t>(err);

@@ -70,9 +70,10 @@ def test_options_roundtrip_and_validation(pk):
 
 def test_strerror(pk):
     lib = pk.lib()
-    for code in range(-5, 1):
-        assert lib.profk_strerror(code)
+    for code in range(-6, 1):
+        assert lib.profk_strerror(code) and lib.profk_strerror(code) != b"unknown status"
     assert b"NaN" in lib.profk_strerror(-3)
+    assert b"scratch" in lib.profk_strerror(-6)
 
 
 def test_invalid_arguments_are_rejected_before_any_device_work(pk):
@@ -140,3 +141,22 @@ def test_long_row_workspace_size(pk):
     need = max(pk.workspace_size(1, seg, k, 1e-3 / 2), pk.workspace_size(1, tail, k, 1e-3 / 2))
     assert pk.workspace_size(1, n, k, 1e-3) == round256(need) + round256(4 * cand) + round256(8 * cand)
     assert pk.workspace_size(1, 1 << 40, 1, 1e-3) == 0
+
+
+def test_noalloc_argument_and_size_checks(pk):
+    # The entry point that allocates nothing refuses, before any device work:
+    # bad arguments, rows beyond 2^32 elements or misaligned, and problems whose
+    # workspace does not fit its fixed scratch (k = n = 2^23 takes the exact
+    # route and needs 8 x 2^23 bytes of selection keys, beyond 32 MiB).
+    from streaming_selection_primitive_gb300 import _abi
+    lib = pk.lib()
+    fake = C.c_void_p(256)
+    st = pk.ProfkStats()
+    assert lib.profk_topk_noalloc(None, 10, 1, 1e-3, 0, fake, fake, None, C.byref(st)) == _abi.PROFK_ERR_INVALID
+    assert lib.profk_topk_noalloc(fake, 10, 11, 1e-3, 0, fake, fake, None, None) == _abi.PROFK_ERR_INVALID
+    assert lib.profk_topk_noalloc(fake, (1 << 32) + 4, 1, 1e-3, 0, fake, fake, None, None) == \
+        _abi.PROFK_ERR_UNSUPPORTED
+    assert lib.profk_topk_noalloc(C.c_void_p(260), 100, 1, 1e-3, 0, fake, fake, None, None) == \
+        _abi.PROFK_ERR_UNSUPPORTED
+    assert lib.profk_topk_noalloc(fake, 1 << 23, 1 << 23, 1e-3, 0, fake, fake, None, None) == \
+        _abi.PROFK_ERR_SCRATCH
