@@ -219,8 +219,20 @@ typedef enum profk_option {
   PROFK_OPT_SAMPLER = 10,      /* kernels of steps 1-2 (sample and tau): PROFK_SAMPLER_AUTO [0],
                                   _GRID or _STEPS (GRID falls back to the automatic choice
                                   where it cannot take the problem) */
-  PROFK_OPT__COUNT = 11
+  PROFK_OPT_WAIT_TEST = 11,    /* test of the path taken when a bounded device wait runs out [0]:
+                                  PROFK_WAIT_TEST_SAMPLER, _REFINE or _SORT makes the first grid barrier
+                                  of that persistent kernel (the sampler's grid form, the grid
+                                  refinement for k <= 8192, the buffer sort above) wait for one CTA
+                                  more than the launch has, with a bound of 4096 polls instead of
+                                  2^22.  Every CTA of the row then gives up, writes nothing more, and
+                                  the call returns PROFK_ERR_DEVICE_TIMEOUT with its outputs untouched;
+                                  the next call is unaffected */
+  PROFK_OPT__COUNT = 12
 } profk_option;
+#define PROFK_WAIT_TEST_OFF 0
+#define PROFK_WAIT_TEST_SAMPLER 1
+#define PROFK_WAIT_TEST_REFINE 2
+#define PROFK_WAIT_TEST_SORT 3
 /* Forms of the sampling kernels (PROFK_OPT_SAMPLER); both give the same
  * sample and tau.  GRID: one persistent kernel whose CTAs (all resident) meet
  * at grid barriers; taken when each CTA's share of the draws fits its

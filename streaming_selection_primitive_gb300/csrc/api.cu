@@ -28,7 +28,19 @@ namespace {
 // ---------------------------------------------------------------------------
 // Options.
 std::atomic<int64_t> g_opt[PROFK_OPT__COUNT] = {
-    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}, {1}, {0}, {PROFK_SAMPLER_AUTO}};
+    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}, {1}, {0}, {PROFK_SAMPLER_AUTO}, {PROFK_WAIT_TEST_OFF}};
+
+// PROFK_OPT_WAIT_TEST: the wait setting of the persistent kernel it names
+// (one arrival more than the launch has at its first grid barrier, and a
+// short bound), the default setting for every other kernel.
+WaitCfg wait_cfg_for(int64_t kernel) {
+  const int64_t t = g_opt[PROFK_OPT_WAIT_TEST].load();
+  if (t == PROFK_WAIT_TEST_OFF || t != kernel) return WaitCfg{};
+  WaitCfg w;
+  w.skew = 1u;
+  w.polls = 1 << 12;
+  return w;
+}
 
 // Longest row handled as one (PROFK_OPT_MAX_SEGMENT; 0 = 2^32, the reach of a
 // candidate key's 32-bit index field).  Longer rows are split into segments.
@@ -584,6 +596,7 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
                 at<unsigned long long>(ws, L.off_table), at<uint32_t>(ws, L.off_draws),
                 at<uint32_t>(ws, L.off_blockcnt), at<uint32_t>(ws, L.off_sidx), at<uint32_t>(ws, L.off_skeys), false,
                 static_cast<unsigned long long>(P.t)};
+  sa.wait = wait_cfg_for(PROFK_WAIT_TEST_SAMPLER);
   cudaError_t e = cudaSuccess;
   if (form == Sampler::Grid) {
     e = launch_sample_tau(sa, at<char>(ws, L.off_sctl), stream);
@@ -603,11 +616,13 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
   if (ev) cudaEventRecord(ev[3], stream);
   if (!L.radix_refine) {
     RefineGridArgs ga{at<unsigned long long>(ws, L.off_buf), P.M, ng, gl, st, k, x, ld, n, out_vals, out_idx};
+    ga.wait = wait_cfg_for(PROFK_WAIT_TEST_REFINE);
     e = launch_refine_grid(ga, at<char>(ws, L.off_refine), rows, stream);
   } else {
     // The whole buffer (R <= M keys) is sorted and its first k emitted.
     RadixSortArgs ra{at<unsigned long long>(ws, L.off_buf), P.M, k, SortCount::FromState, ng, gl, rows,
                      at<char>(ws, L.off_sort), true, x, ld, n, out_vals, out_idx, st};
+    ra.wait = wait_cfg_for(PROFK_WAIT_TEST_SORT);
     e = launch_radix_sort(ra, stream);
   }
   if (e != cudaSuccess) return e;
@@ -1295,6 +1310,8 @@ int profk_set_option(int option, int64_t value) {
   if (option < 0 || option >= PROFK_OPT__COUNT) return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_PARAM_MODE && (value < 0 || value > 3)) return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_SAMPLER && (value < PROFK_SAMPLER_AUTO || value > PROFK_SAMPLER_STEPS))
+    return PROFK_ERR_INVALID;
+  if (option == PROFK_OPT_WAIT_TEST && (value < PROFK_WAIT_TEST_OFF || value > PROFK_WAIT_TEST_SORT))
     return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_MAX_SEGMENT && value != 0 && (value < (1 << 16) || value > (int64_t(1) << 32) || (value & 3)))
     return PROFK_ERR_INVALID;

@@ -122,6 +122,61 @@ struct RowState {
   unsigned int hist[HIST_BINS];
 };
 
+// ---------------------------------------------------------------------------
+// Bounded waits of the persistent kernels (grid barriers and look-backs).
+// A wait gives up after a bounded number of polls, or as soon as another CTA
+// of the same row has given up (the row's abort word, in the kernel's control
+// block, zero at launch).  A CTA that gives up sets the abort word, reports
+// ERR_WAIT in RowState::error and leaves the kernel without writing any more
+// data; the kernels after it skip a row whose error word is set, so the
+// host sees PROFK_ERR_DEVICE_TIMEOUT and the outputs are left alone.
+constexpr int WAIT_POLLS = 1 << 22;   // default bound on one wait (a poll is an L2 round trip: seconds in all)
+constexpr int WAIT_ABORT_EVERY = 32;  // polls between two reads of the abort word
+constexpr unsigned ERR_WAIT = 8u;     // RowState::error bit of a wait that gave up
+
+// Test setting of a kernel's waits: `skew` extra arrivals awaited at its
+// first grid barrier (which then can never be met) and a shorter bound
+// `polls` (0: WAIT_POLLS).  Both zero on every ordinary call.
+struct WaitCfg {
+  unsigned skew = 0;
+  int polls = 0;
+};
+
+__device__ __forceinline__ int wait_limit(const WaitCfg& w) { return w.polls > 0 ? w.polls : WAIT_POLLS; }
+
+__device__ __forceinline__ unsigned wait_ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ bool wait_aborted(const unsigned* abort_word) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(abort_word) : "memory");
+  return v != 0u;
+}
+
+__device__ __forceinline__ void wait_give_up(unsigned* abort_word) { atomicExch(abort_word, 1u); }
+
+// Whether poll number `poll` of a wait should end it: the bound was reached
+// (the wait gives up, setting the abort word) or, every WAIT_ABORT_EVERY
+// polls, another CTA of the row has given up.
+__device__ __forceinline__ bool wait_should_stop(int poll, int limit, unsigned* abort_word) {
+  if (poll >= limit) {
+    wait_give_up(abort_word);
+    return true;
+  }
+  return poll % WAIT_ABORT_EVERY == WAIT_ABORT_EVERY - 1 && wait_aborted(abort_word);
+}
+
+// One thread waits (acquire loads) until *count reaches target.  Returns
+// false if the wait ended without it.
+__device__ __forceinline__ bool wait_count(const unsigned* count, unsigned target, unsigned* abort_word, int limit) {
+  for (int poll = 0; wait_ld_acquire(count) < target; ++poll)
+    if (wait_should_stop(poll, limit, abort_word)) return false;
+  return true;
+}
+
 // Row of a launch: identity unless a row list is given.
 __device__ __forceinline__ int launch_row(const int* rows) {
   return rows ? rows[blockIdx.y] : static_cast<int>(blockIdx.y);

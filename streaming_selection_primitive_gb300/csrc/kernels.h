@@ -88,6 +88,7 @@ struct SampleArgs {
   unsigned long long t = 0;
   // launch_sample_tau: Philox key word 1 = storage row + key_row0.
   int64_t key_row0 = 0;
+  WaitCfg wait{};  // launch_sample_tau: test setting of its waits
 };
 void launch_sample(const SampleArgs& a, cudaStream_t stream);
 // Same, with Philox key word 1 = storage row + key_row0 (a single stored row
@@ -210,6 +211,7 @@ struct RadixSortArgs {
   float* out_vals;
   int64_t* out_idx;
   RowState* st;  // skip / count source, and where a timed-out wait is reported
+  WaitCfg wait{};  // test setting of its waits
 };
 size_t radix_sort_scratch_bytes(int64_t key_stride, int64_t rows);
 void* radix_sort_ctl(void* scratch, int64_t key_stride, int64_t rows);  // per-row control blocks
@@ -235,6 +237,7 @@ struct RefineOneArgs {
   int64_t n;
   float* out_vals;
   int64_t* out_idx;
+  WaitCfg wait{};  // launch_refine_grid: test setting of its waits
 };
 void launch_refine_one(const RefineOneArgs& a, cudaStream_t stream);
 int64_t refine_one_max_k();

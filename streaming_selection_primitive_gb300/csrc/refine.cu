@@ -29,7 +29,8 @@ struct RefineCtl {
   unsigned hist[6][HIST_BINS];  // pass histograms, summed over the chunks
   unsigned bar;                 // grid-barrier arrivals
   unsigned cursor;              // gather-list length
-  unsigned pad[62];
+  unsigned abort;               // set by a CTA whose wait gave up
+  unsigned pad[61];
 };
 static_assert(sizeof(RefineCtl) % 16 == 0, "RefineCtl is zeroed with 16-byte stores");
 
@@ -41,28 +42,16 @@ constexpr int RG_PIECE = RG_THREADS * RG_KPT;     // 4096
 constexpr int RG_OUT = 8192;                      // gather capacity (64 KB of shared memory)
 constexpr int RG_MAX_K = 8192;
 constexpr int64_t RG_MAX_M = int64_t(1) << 19;
-constexpr int WAIT_POLLS = 1 << 22;  // bound on one barrier wait (a poll is an L2 round trip)
-constexpr unsigned ERR_WAIT = 8u;    // RowState::error bit of a wait that ran out
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // Every CTA of the row arrives (a release: the CTA's writes, ordered before
 // it by the block barrier, become visible with it), then waits until all
-// have (target arrivals; acquire loads of the arrival count).
-__device__ __forceinline__ void grid_sync(unsigned* bar, unsigned target, int* err) {
+// have (target arrivals; acquire loads of the arrival count).  A wait that
+// ends without them (bounded, see wait_count) sets *err, which every thread
+// reads afterwards.
+__device__ __forceinline__ void grid_sync(RefineCtl& c, unsigned target, int* err, int limit) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
-    for (int poll = 0; ld_acquire(bar) < target; ++poll) {
-      if (poll >= WAIT_POLLS) {
-        *err = 1;
-        break;
-      }
-    }
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&c.bar) : "memory");
+    if (!wait_count(&c.bar, target, &c.abort, limit)) *err = 1;
   }
   __syncthreads();
 }
@@ -107,10 +96,16 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
   const int tid = threadIdx.x, lane = tid & 31;
   const unsigned long long R = S.R_ge;
   const unsigned long long k = static_cast<unsigned long long>(a.k);
-  if (!(k <= R && R <= static_cast<unsigned long long>(a.M))) {
+  // A row that fails the check, or whose earlier steps reported an error,
+  // is left alone (its outputs are not touched).  One thread decides for
+  // the block.
+  if (tid == 0) s_digit = !(k <= R && R <= static_cast<unsigned long long>(a.M)) || __ldcg(&S.error) != 0u;
+  __syncthreads();
+  if (s_digit) {
     if (blockIdx.x == 0 && tid == 0) S.skip = 1;
     return;  // every CTA of the row leaves: no barrier is met
   }
+  const int limit = wait_limit(a.wait);
   if (tid == 0) {
     s_err = 0;
     if (blockIdx.x == 0) S.skip = 0;
@@ -154,7 +149,8 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
     __syncthreads();
     for (int b = tid; b < nb; b += RG_THREADS)
       if (h[b]) atomicAdd(&c.hist[p][b], h[b]);
-    grid_sync(&c.bar, target += static_cast<unsigned>(G), &s_err);
+    grid_sync(c, (target += static_cast<unsigned>(G)) + (p == 0 ? a.wait.skew : 0u), &s_err, limit);
+    if (s_err) break;  // block-uniform (read after a block barrier)
     // Every CTA finds the same digit: the bins counted down from the top,
     // thread t owning nb / 1024 of them.
     if (tid == 0) {
@@ -204,6 +200,12 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
     }
     __syncthreads();
   }
+  // After a wait that gave up, the CTA reports it and leaves without writing
+  // anything else.
+  if (s_err) {
+    if (tid == 0) atomicOr(&S.error, ERR_WAIT);
+    return;
+  }
   // Gather every key >= thresh (exactly `total` of them, at most RG_OUT).
   unsigned long long* gr = gather + static_cast<int64_t>(row) * RG_OUT;
   for (int64_t base = lo; base < hi; base += RG_PIECE) {
@@ -224,8 +226,11 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
       }
     }
   }
-  grid_sync(&c.bar, target += static_cast<unsigned>(G), &s_err);
-  if (s_err && tid == 0) atomicOr(&S.error, ERR_WAIT);
+  grid_sync(c, target += static_cast<unsigned>(G), &s_err, limit);
+  if (s_err) {
+    if (tid == 0) atomicOr(&S.error, ERR_WAIT);
+    return;
+  }
   // Every CTA reads the gather list; a key's output position is the number
   // of listed keys above it (keys are distinct), counted by one warp per key,
   // the keys spread over all warps of the launch.

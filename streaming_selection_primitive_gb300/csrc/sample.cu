@@ -328,8 +328,6 @@ __global__ void __launch_bounds__(MARK_THREADS) k_sample_compact(SampleArgs a) {
 
 constexpr int ST_THREADS = 512;
 constexpr int ST_HELD = 2;                      // rounds of draws whose keys stay in registers
-constexpr int ST_WAIT_POLLS = 1 << 22;          // bound on one wait (a poll is an L2 round trip)
-constexpr unsigned ST_ERR_WAIT = 8u;            // RowState::error bit of a wait that ran out
 constexpr unsigned long long CNT_READY = 1ull << 63;
 constexpr int TAU_GATHER = ST_THREADS;  // a tau bucket this small is finished by one CTA
 constexpr int ST_QB = 2;                // wide form: quads per thread in flight
@@ -346,17 +344,12 @@ struct SampleCtl {
   uint32_t bucket[TAU_GATHER];        // the sample keys of tau's final bucket
   unsigned bucket_n;
   unsigned bar;                       // grid-barrier arrivals
-  unsigned pad[62];
+  unsigned abort;                     // set by a CTA whose wait gave up
+  unsigned pad[61];
 };
 static_assert(sizeof(SampleCtl) % 16 == 0, "SampleCtl is zeroed with 16-byte stores");
 
 namespace {
-
-__device__ __forceinline__ unsigned st_ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
 __device__ __forceinline__ unsigned long long st_ld_relaxed(const unsigned long long* p) {
   unsigned long long v;
@@ -370,20 +363,24 @@ __device__ __forceinline__ void st_st_relaxed(unsigned long long* p, unsigned lo
 
 // Every CTA of the row arrives (a release: the CTA's writes, ordered before
 // it by the block barrier, become visible with it), then waits until all
-// have (acquire loads of the arrival count).
-__device__ __forceinline__ void st_grid_sync(unsigned* bar, unsigned target, int* err) {
+// have (acquire loads of the arrival count).  A wait that ends without them
+// (bounded, see wait_count) sets *err, which every thread reads afterwards.
+__device__ __forceinline__ void st_grid_sync(SampleCtl& c, unsigned target, int* err, int limit) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
-    for (int poll = 0; st_ld_acquire(bar) < target; ++poll) {
-      if (poll >= ST_WAIT_POLLS) {
-        *err = 1;
-        break;
-      }
-    }
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&c.bar) : "memory");
+    if (!wait_count(&c.bar, target, &c.abort, limit)) *err = 1;
   }
   __syncthreads();
 }
+
+// After a wait that gave up, the CTA reports it and leaves without writing
+// anything else (s_err is block-uniform here: read after a block barrier).
+#define ST_LEAVE_IF_GAVE_UP()                 \
+  if (s_err) {                                \
+    if (tid == 0) atomicOr(&S.error, ERR_WAIT); \
+    return;                                   \
+  }
 
 // Block-wide sum and exclusive scan (thread order) of one value per thread.
 __device__ __forceinline__ unsigned long long st_excl_scan(unsigned long long v, unsigned long long* sw,
@@ -452,6 +449,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   SampleCtl& c = ctl[row];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) s_err = 0;
+  const int limit = wait_limit(a.wait);
   const int64_t G = gridDim.x, chunk = blockIdx.x;
   const int64_t Dc = (((a.D + G - 1) / G) + 31) & ~int64_t(31);
   const int64_t lo = chunk * Dc < a.D ? chunk * Dc : a.D;
@@ -534,7 +532,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
       }
     }
   }
-  st_grid_sync(&c.bar, target += static_cast<unsigned>(G), &s_err);
+  st_grid_sync(c, (target += static_cast<unsigned>(G)) + a.wait.skew, &s_err, limit);
+  ST_LEAVE_IF_GAVE_UP();
 
   // b. First occurrences (the table is complete: a slot's draw is the
   // smallest draw of its value), their count and their place in draw order.
@@ -599,7 +598,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     if (tid < chunk) {
       unsigned long long v = st_ld_relaxed(&c.count[tid]);
       for (int poll = 0; !(v & CNT_READY); ++poll) {
-        if (poll >= ST_WAIT_POLLS) {
+        if (wait_should_stop(poll, limit, &c.abort)) {
           s_err = 1;
           v = CNT_READY;
           break;
@@ -611,6 +610,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     for (int o = 16; o >= 1; o >>= 1) before += __shfl_xor_sync(FULL_MASK, before, o);
     if (lane == 0) sw[warp] = before;
     __syncthreads();
+    ST_LEAVE_IF_GAVE_UP();
     if (tid == 0) {
       unsigned long long b = 0;
       for (int w = 0; w < ST_THREADS / 32; ++w) b += sw[w];
@@ -744,7 +744,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     __syncthreads();
     for (unsigned b = tid; b < nb; b += ST_THREADS)
       if (h[b]) atomicAdd(&c.hist[p][b], h[b]);
-    st_grid_sync(&c.bar, target += static_cast<unsigned>(G), &s_err);
+    st_grid_sync(c, target += static_cast<unsigned>(G), &s_err, limit);
+    ST_LEAVE_IF_GAVE_UP();
     // Bins counted down from the top: thread t owns nb / 512 of them.
     if (tid == 0) {
       s_digit = 0;
@@ -792,7 +793,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
           if (pos < TAU_GATHER) c.bucket[pos] = key;
         }
       });
-      st_grid_sync(&c.bar, target += static_cast<unsigned>(G), &s_err);
+      st_grid_sync(c, target += static_cast<unsigned>(G), &s_err, limit);
+      ST_LEAVE_IF_GAVE_UP();
       if (chunk == 0) {
         const int nl = static_cast<int>(bucket_n);
         if (tid < nl) s_list[tid] = __ldcg(&c.bucket[tid]);
@@ -830,9 +832,9 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
       S.sel_bits = 32;
       S.sel_done = 1;
     }
-    if (s_err) atomicOr(&S.error, ST_ERR_WAIT);
   }
 }
+#undef ST_LEAVE_IF_GAVE_UP
 
 }  // namespace
 

@@ -63,7 +63,8 @@ struct SortCtl {
   unsigned long_run;                 // 1: some run of equal values is longer than 32
   unsigned long long kmax;           // the largest key
   unsigned long long nkmax;          // the largest ~key (the smallest key, complemented)
-  unsigned pad[26];
+  unsigned abort;                    // set by a CTA whose wait gave up
+  unsigned pad[25];
 };
 static_assert(sizeof(SortCtl) % 16 == 0, "SortCtl is zeroed with 16-byte stores");
 
@@ -87,8 +88,6 @@ constexpr unsigned long long FLAG_AGG = 1ull << 62;   // the chunk's own digit c
 constexpr unsigned long long FLAG_INCL = 2ull << 62;  // count of this and every earlier chunk
 constexpr int FLAG_SEQ_SHIFT = 58;
 constexpr unsigned long long FLAG_COUNT = (1ull << FLAG_SEQ_SHIFT) - 1;
-constexpr int WAIT_POLLS = 1 << 22;     // bound on one wait (a poll is an L2 round trip)
-constexpr unsigned ERR_SORT_WAIT = 8u;  // RowState::error bit of a wait that ran out
 
 __device__ __forceinline__ unsigned digit_of(unsigned long long key, int pos) {
   return static_cast<unsigned>((~key) >> (8 * pos)) & 255u;
@@ -97,12 +96,6 @@ __device__ __forceinline__ unsigned digit_of(unsigned long long key, int pos) {
 __device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -130,8 +123,11 @@ __device__ __forceinline__ unsigned same_digit_lanes(unsigned d) {
 // Keys a row sorts, or -1 when the row is left alone.
 __device__ __forceinline__ int64_t row_count(const RadixSortArgs& a, int row) {
   if (a.mode == SortCount::FromState) {
+    // The refinement of the filter buffer: rows that fail the check, or whose
+    // earlier steps reported an error, are left alone.
     const unsigned long long R = a.st[row].R_ge;
-    const bool ok = static_cast<unsigned long long>(a.k) <= R && R <= static_cast<unsigned long long>(a.key_stride);
+    const bool ok = static_cast<unsigned long long>(a.k) <= R && R <= static_cast<unsigned long long>(a.key_stride) &&
+                    __ldcg(&a.st[row].error) == 0u;
     return ok ? static_cast<int64_t>(R) : -1;
   }
   if (a.mode == SortCount::KUnlessSkip && a.st[row].skip) return -1;
@@ -163,6 +159,8 @@ struct Smem {
   unsigned distinct[8];  // byte values present at each position
   unsigned nruns;  // runs of 2 .. RUN_MAX keys starting in this chunk
   int err;
+  int limit;          // bound on one wait
+  long long row_len;  // keys of the row, or -1: the row is skipped
   unsigned long long blo[256];  // bucket stage, per digit of the top position: the lowest bits below it,
   unsigned boff[256];           // the digit's first bucket,
   unsigned char bbits[256];     // log2 of its buckets
@@ -177,16 +175,13 @@ struct Smem {
 // Every CTA of the row arrives (a release: the CTA's writes, ordered before
 // it by the block barrier, become visible with it), then waits until all
 // have (target arrivals; acquire loads of the arrival count).
+// A wait that ends without them (bounded, see wait_count) sets sm.err, which
+// every thread reads afterwards.
 __device__ __forceinline__ void grid_sync(SortCtl& c, unsigned target, Smem& sm) {
   __syncthreads();
   if (threadIdx.x == 0) {
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&c.bar) : "memory");
-    for (int poll = 0; ld_acquire(&c.bar) < target; ++poll) {
-      if (poll >= WAIT_POLLS) {
-        sm.err = 1;
-        break;
-      }
-    }
+    if (!wait_count(&c.bar, target, &c.abort, sm.limit)) sm.err = 1;
   }
   __syncthreads();
 }
@@ -213,7 +208,7 @@ __device__ __forceinline__ void load_piece(const unsigned long long* in, int64_t
 __device__ __forceinline__ void radix_pass(const RadixSortArgs& a, int row, int64_t chunk, int64_t lo, int64_t hi,
                                            int pos, int seq, bool emit, const unsigned long long* in,
                                            unsigned long long* out, unsigned long long* fr, Smem& sm,
-                                           unsigned long long* s_keys) {
+                                           unsigned long long* s_keys, SortCtl& c) {
   unsigned short(*cntw)[256] = reinterpret_cast<unsigned short(*)[256]>(s_keys);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const unsigned lt = (1u << lane) - 1u;
@@ -347,7 +342,7 @@ __device__ __forceinline__ void radix_pass(const RadixSortArgs& a, int row, int6
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           for (int poll = 0; !flag_ready(f[i], seq); ++poll) {
-            if (poll >= WAIT_POLLS) {
+            if (wait_should_stop(poll, sm.limit, &c.abort)) {
               timed_out = true;
               f[i] = FLAG_INCL | tag;  // give up here: adds nothing, ends the walk
               break;
@@ -374,13 +369,17 @@ __device__ __forceinline__ void radix_pass(const RadixSortArgs& a, int row, int6
         excl += mine;
         if (fb) break;
       }
-      if (timed_out) sm.err = 1;
-      if (q == 0) {
+      // A group whose walk gave up publishes nothing: later chunks then walk
+      // past this chunk's own count, and this CTA leaves below.
+      const bool gave_up = ((__ballot_sync(gmask, timed_out) >> (lane & ~3)) & 0xFu) != 0u;
+      if (gave_up) sm.err = 1;
+      if (q == 0 && !gave_up) {
         st_relaxed(fr + chunk * 256 + d, FLAG_INCL | tag | ((excl + sm.hist[d]) & FLAG_COUNT));
         sm.cur[d] += excl;
       }
     }
     __syncthreads();
+    if (sm.err) return;  // block-uniform: read after the block barrier
     if (threadIdx.x < 256)
       sm.base[threadIdx.x] = static_cast<long long>(sm.cur[threadIdx.x]) - static_cast<long long>(sm.texcl[threadIdx.x]);
     __syncthreads();
@@ -493,6 +492,7 @@ __device__ bool bucket_stage(const RadixSortArgs& a, int row, int64_t len, int64
   for (int i = threadIdx.x; i < BK; i += RS_THREADS)
     if (h[i]) atomicAdd(&bkr[i], h[i]);
   grid_sync(c, target += G, sm);
+  if (sm.err) return true;  // the wait gave up: the caller reports it and leaves
 
   // Starts: the exclusive scan of the row's counts.  The counts come into
   // shared memory with coalesced loads; each thread then scans 16 consecutive
@@ -579,6 +579,7 @@ __device__ bool bucket_stage(const RadixSortArgs& a, int row, int64_t len, int64
     tmp_row[atomicAdd(&h[bucket_of(kk)], 1u)] = kk;
   }
   grid_sync(c, target += G, sm);
+  if (sm.err) return true;
 
   if (maxb <= 256) {
     // Small buckets: each is sorted by one warp in registers (the smallest
@@ -668,7 +669,13 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
   extern __shared__ unsigned long long s_keys[];
   __shared__ Smem sm;
   const int row = launch_row(a.rows);
-  const int64_t len = row_count(a, row);
+  if (threadIdx.x == 0) {
+    sm.row_len = row_count(a, row);  // one thread decides for the block
+    sm.err = 0;
+    sm.limit = wait_limit(a.wait);
+  }
+  __syncthreads();
+  const int64_t len = sm.row_len;
   if (len < 0) return;  // every CTA of the row leaves: no barrier is met
   SortCtl& c = ctl[row];
   unsigned long long* fr = flags + row * flag_stride;
@@ -677,7 +684,13 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
   const int64_t lo = chunk * C < len ? chunk * C : len;
   const int64_t hi = lo + C < len ? lo + C : len;
   unsigned target = 0;
-  if (threadIdx.x == 0) sm.err = 0;
+// After a wait that gave up, the CTA reports it and leaves without writing
+// anything else (sm.err is block-uniform where this is used).
+#define RS_LEAVE_IF_GAVE_UP()                                           \
+  if (sm.err) {                                                         \
+    if (threadIdx.x == 0 && a.st) atomicOr(&a.st[row].error, ERR_WAIT); \
+    return;                                                             \
+  }
 
   unsigned* bkr = bk + static_cast<int64_t>(row) * 2 * BK;  // bucket counts, then cursors
 
@@ -735,7 +748,8 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
     for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS)
       if ((&h[0][0])[i]) atomicAdd(&c.start[0][0] + i, static_cast<unsigned long long>((&h[0][0])[i]));
   }
-  grid_sync(c, target += G, sm);
+  grid_sync(c, (target += G) + a.wait.skew, sm);
+  RS_LEAVE_IF_GAVE_UP();
   // The plan, the same in every CTA.
   if (threadIdx.x < 8) sm.trivial[threadIdx.x] = 0;
   if (threadIdx.x == 0) {
@@ -780,7 +794,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
   if (len >= BK_MIN_LEN && len < (int64_t(1) << 31) &&
       bucket_stage(a, row, len, lo, hi, c, target, bkr, tmp + row * a.key_stride, sm, s_keys)) {
     __syncthreads();
-    if (threadIdx.x == 0 && sm.err && a.st) atomicOr(&a.st[row].error, ERR_SORT_WAIT);
+    RS_LEAVE_IF_GAVE_UP();
     return;
   }
 
@@ -800,10 +814,12 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
     for (int p = 4; p < 8; ++p) {
       if (sm.trivial[p]) continue;
       radix_pass(a, row, chunk, lo, hi, p, seq, false, (cur ? tmp : a.keys) + row * a.key_stride,
-                 (cur ? a.keys : tmp) + row * a.key_stride, fr, sm, s_keys);
+                 (cur ? a.keys : tmp) + row * a.key_stride, fr, sm, s_keys, c);
+      RS_LEAVE_IF_GAVE_UP();
       ++seq;
       cur ^= 1;
       grid_sync(c, target += G, sm);
+      RS_LEAVE_IF_GAVE_UP();
     }
     // 3. Runs of equal values: a run longer than RUN_MAX has equal values
     // RUN_MAX positions apart.
@@ -811,6 +827,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
     for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS)
       if (i + RUN_MAX < len && (__ldcg(srt + i) >> 32) == (__ldcg(srt + i + RUN_MAX) >> 32)) c.long_run = 1u;
     grid_sync(c, target += G, sm);
+    RS_LEAVE_IF_GAVE_UP();
     full = __ldcg(&c.long_run) != 0;
     if (!full) {
       // The chunk and RUN_MAX keys on each side go to shared memory.  A key
@@ -870,14 +887,17 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
     for (int p = 0; p < 8; ++p) {
       if (sm.trivial[p]) continue;
       radix_pass(a, row, chunk, lo, hi, p, seq, p == lastp, (cur ? tmp : a.keys) + row * a.key_stride,
-                 (cur ? a.keys : tmp) + row * a.key_stride, fr, sm, s_keys);
+                 (cur ? a.keys : tmp) + row * a.key_stride, fr, sm, s_keys, c);
+      RS_LEAVE_IF_GAVE_UP();
       ++seq;
       cur ^= 1;
-      if (p != lastp) grid_sync(c, target += G, sm);
+      if (p != lastp) {
+        grid_sync(c, target += G, sm);
+        RS_LEAVE_IF_GAVE_UP();
+      }
     }
   }
-  __syncthreads();
-  if (threadIdx.x == 0 && sm.err && a.st) atomicOr(&a.st[row].error, ERR_SORT_WAIT);
+#undef RS_LEAVE_IF_GAVE_UP
 }
 
 struct Scratch {

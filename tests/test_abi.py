@@ -160,3 +160,15 @@ def test_noalloc_argument_and_size_checks(pk):
         _abi.PROFK_ERR_UNSUPPORTED
     assert lib.profk_topk_noalloc(fake, 1 << 23, 1 << 23, 1e-3, 0, fake, fake, None, None) == \
         _abi.PROFK_ERR_SCRATCH
+
+
+def test_wait_test_option(pk):
+    # The test setting of the bounded device waits: off by default, one of the
+    # three persistent kernels, nothing else.
+    assert pk.get_option(pk.OPT_WAIT_TEST) == pk.WAIT_TEST_OFF
+    for v in (pk.WAIT_TEST_SAMPLER, pk.WAIT_TEST_REFINE, pk.WAIT_TEST_SORT, pk.WAIT_TEST_OFF):
+        pk.set_option(pk.OPT_WAIT_TEST, v)
+        assert pk.get_option(pk.OPT_WAIT_TEST) == v
+    for bad in (4, -1):
+        with pytest.raises(pk.ProfkError):
+            pk.set_option(pk.OPT_WAIT_TEST, bad)
