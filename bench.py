@@ -72,17 +72,16 @@ def filter_source_hash() -> str:
 
 
 def traffic_from_profile(n: int):
-    """DRAM bytes per filter launch from the committed ncu summary, scaled to n;
-    None when absent or when the filter source changed since the capture."""
-    p = ROOT / "profiles" / "filter_normal_2p28.md"
+    """DRAM bytes per filter launch from the committed ncu figures
+    (profiles/filter_normal_2p28.json), scaled to n; None when absent or when
+    the filter source changed since the capture."""
+    p = ROOT / "profiles" / "filter_normal_2p28.json"
     if not p.exists():
         return None
-    text = p.read_text()
-    m_hash = re.search(r"filter_source_hash:\s*([0-9a-f]+)", text)
-    m_b = re.search(r"dram_bytes_per_element:\s*([0-9.]+)", text)
-    if not m_hash or not m_b or m_hash.group(1) != filter_source_hash():
+    d = json.loads(p.read_text())
+    if d.get("filter_source_hash") != filter_source_hash():
         return None
-    return float(m_b.group(1)) * n
+    return float(d["dram_bytes_per_element"]) * n
 
 
 class ClockSampler:
@@ -156,21 +155,38 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside), "samples_from": where}
 
 
-def cpu_baseline(x_host_prefix, k, budget_s=12.0):
-    """The oracle (full sort) on a bounded prefix of the same input."""
-    from oracle.topk import topk_sort
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
-    elems, t0, reps = 0, time.perf_counter(), 0
-    while True:
-        topk_sort(x_host_prefix, k)
-        reps += 1
-        elems += x_host_prefix.size
-        if time.perf_counter() - t0 >= budget_s or reps >= 50:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": elems / dt / 1e9, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
-            "sample": f"oracle.topk_sort (numpy lexsort, one thread) on the first {x_host_prefix.size} elements "
-                      f"of the same normal input, k={k}, {reps} calls in {dt:.1f} s"}
+
+def cpu_baseline(x_host, k, reps=3):
+    """The oracle on the whole input, on the host cores: its threaded form
+    (topk_chunked, one thread per core, four chunks per thread) gives the
+    value; its single-thread O(n) form (topk_partition) is timed once beside it."""
+    from oracle.topk import topk_chunked, topk_partition
+
+    cores = host_cores()
+    n = x_host.size
+    multi = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        topk_chunked(x_host, k, cores, 4 * cores)
+        multi.append(time.perf_counter() - t0)
+    t0 = time.perf_counter()
+    topk_partition(x_host, k)
+    single = time.perf_counter() - t0
+    t = statistics.median(multi)
+    return {"value": round(n / t / 1e9, 4), "unit": "Gelem/s", "cores": cores, "kind": "oracle",
+            "ms_per_call": round(1e3 * t, 1),
+            "sample": f"the whole {n}-element input of the timed steps, copied to the host; "
+                      f"oracle.topk.topk_chunked (numpy selection per chunk on {cores} threads, then the "
+                      f"exact merge), median of {reps} calls, k={k}",
+            "single_thread": {"value": round(n / single / 1e9, 4), "unit": "Gelem/s", "cores": 1,
+                              "ms_per_call": round(1e3 * single, 1),
+                              "sample": "oracle.topk.topk_partition (numpy, one thread), one call on the same input"}}
 
 
 def dist_env():
@@ -222,24 +238,175 @@ def job_gelems(n: int, steps: int, ws: int, ms: float) -> float:
     return n * steps * ws / (ms / 1e3) / 1e9
 
 
-def run_reference(args):
-    ws, rank, local = dist_env()
-    if rank != 0:
-        return 0
-    import numpy as np
+L2_FLUSH_BYTES = 256 << 20  # written between timed calls whose input fits the 129 MB L2
+
+
+def time_sync_calls(call, reps, stream, flush=None):
+    """Per-call latency of synchronous calls: CUDA events on the launch stream
+    around each call.  With `flush` (a device buffer larger than L2) the
+    buffer is overwritten before each call, outside the events, so that the
+    call starts from a cold L2.  Returns (mean ms, every call's stats)."""
+    import torch
+
+    times, sts = [], []
+    for s in range(reps):
+        if flush is not None:
+            flush.fill_(s & 0x7F)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st = call(s)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+        sts += st if isinstance(st, list) else [st]
+    return statistics.mean(times), sts
+
+
+def time_async_calls(submit, reps, stream):
+    """Calls in flight together (the asynchronous form, the timed steps'
+    form), each completed by profk_wait: (ms per call, every call's stats)."""
+    import torch
+
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    pend = [submit(s) for s in range(reps)]
+    sts = []
+    for p in pend:
+        st = p.wait()[2]
+        sts += st if isinstance(st, list) else [st]
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps, sts
+
+
+def config_entry(n_elems, ms, sts, peak, **extra):
+    """One configuration's figures: ms per call, Gelem/s, the input bytes per
+    second as a fraction of 8 TB/s and of the measured copy peak, retries
+    (attempts beyond the first, over every call and row), workspace, paths."""
+    gbs = 4 * n_elems / (ms / 1e3) / 1e9
+    return {"ms": round(ms, 4), "gelem_s": round(n_elems / ms / 1e6, 2), "hbm_gbs": round(gbs, 1),
+            "hbm_frac_of_8TBs": round(gbs / 8000, 3), "hbm_frac_of_measured": round(gbs / peak, 3),
+            "retries": int(sum(max(st["attempts"] - 1, 0) for st in sts)),
+            "aux_bytes": int(max(st["aux_bytes"] for st in sts)),
+            "paths": sorted({int(st["path"]) for st in sts}), **extra}
+
+
+def binom_upper(n, p, q=0.99):
+    """Smallest F with P(Binomial(n, p) <= F) >= q (log-space pmf recurrence)."""
+    import math
+
+    logp = n * math.log1p(-p)
+    cdf, f = 0.0, 0
+    while True:
+        cdf += math.exp(logp)
+        if cdf >= q or f >= n:
+            return f
+        logp += math.log((n - f) / (f + 1)) + math.log(p) - math.log1p(-p)
+        f += 1
+
+
+def baseline_configs(pk, dev, stream, rank, peak):
+    """Every configuration of the project's specification beyond the headline
+    2^30 row (those are in `sweep`), each with its own figures."""
     import torch
 
     import workloads
-    from oracle.topk import topk_sort
 
-    n_sample = 1 << 22
+    out = {}
+
+    def buf(k, rows=1):
+        shape = (k,) if rows == 1 else (rows, k)
+        return (torch.empty(shape, dtype=torch.float32, device=dev), torch.empty(shape, dtype=torch.int64, device=dev))
+
+    # 1. 2^22 uniform, k = 32: the 16 MB input fits L2, so the per-call figure
+    # flushes L2 before every call; the calls in flight are a hot-cache figure.
+    x = workloads.uniform(1 << 22, 1 + rank, dev)
+    o = buf(32)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for w in range(3):
+        pk.topk(x, 32, EPS, 69_000 + w, out=o)
+    ms, sts = time_sync_calls(lambda s: pk.topk(x, 32, EPS, 70_000 + s, out=o)[2], 30, stream, flush)
+    out["uniform_2^22_k32_l2_flushed"] = config_entry(x.numel(), ms, sts, peak,
+                                                      form="profk_topk, L2 flushed before each call")
+    ms, sts = time_async_calls(lambda s: pk.topk_async(x, 32, EPS, 71_000 + s, out=o), 30, stream)
+    out["uniform_2^22_k32_hot"] = config_entry(x.numel(), ms, sts, peak, form="30 async calls in flight, hot L2")
+    del x, flush
+
+    # 2. 2^26 normal, k in {32, 1024, 32768}; the retry rate over 10^4 seeds at 2^20, k = 64.
+    x = workloads.normal(1 << 26, 1 + rank, dev)
+    for kk in (32, 1024, 32768):
+        o = buf(kk)
+        for w in range(2):
+            pk.topk(x, kk, EPS, 72_000 + w, out=o)
+        ms, sts = time_async_calls(lambda s: pk.topk_async(x, kk, EPS, 73_000 + s, out=o), 20, stream)
+        out[f"normal_2^26_k{kk}"] = config_entry(x.numel(), ms, sts, peak, form="20 async calls in flight")
+    del x
+    x = workloads.normal(1 << 20, 1 + rank, dev)
+    o = buf(64)
+    seeds, fails, t0 = 10_000, 0, time.perf_counter()
+    for b0 in range(0, seeds, 250):
+        pend = [pk.topk_async(x, 64, EPS, 100_000 + b0 + s, out=o) for s in range(250)]
+        fails += sum(p.wait()[2]["attempts"] > 1 for p in pend)
+    out["retry_rate_normal_2^20_k64"] = {
+        "calls": seeds, "first_attempt_failures": int(fails), "rate": fails / seeds, "eps": EPS,
+        "binomial_99_upper_at_eps": binom_upper(seeds, EPS), "seconds": round(time.perf_counter() - t0, 2),
+        "seeds": "algorithm seeds 100000 .. 109999 on one input"}
+    del x
+
+    # 4. The 2^28 tie-stress variants, k = 4096.
+    for gen in ("ulps_below_one", "levels16", "sorted_normal"):
+        x = workloads.GENERATORS[gen](1 << 28, 4 + rank, dev)
+        o = buf(4096)
+        for w in range(2):
+            pk.topk(x, 4096, EPS, 74_000 + w, out=o)
+        ms, sts = time_async_calls(lambda s: pk.topk_async(x, 4096, EPS, 75_000 + s, out=o), 10, stream)
+        out[f"{gen}_2^28_k4096"] = config_entry(x.numel(), ms, sts, peak, form="10 async calls in flight")
+        del x
+        torch.cuda.empty_cache()
+
+    # 5. The SAE-shaped selection and 64 batched rows of 2^24.
+    x = workloads.sae_preacts(5 + rank, dev)
+    o = buf(131_072)
+    for w in range(2):
+        pk.topk(x, 131_072, EPS, 76_000 + w, out=o)
+    ms, sts = time_async_calls(lambda s: pk.topk_async(x, 131_072, EPS, 77_000 + s, out=o), 10, stream)
+    out["sae_50331648_k131072"] = config_entry(x.numel(), ms, sts, peak, form="10 async calls in flight")
+    del x
+    x = workloads.normal_rows(64, 1 << 24, 6 + rank, dev)
+    o = buf(32, rows=64)
+    for w in range(2):
+        pk.topk_batched(x, 32, EPS, 78_000 + w, out=o)
+    ms, sts = time_async_calls(lambda s: pk.topk_batched_async(x, 32, EPS, 79_000 + s, out=o), 10, stream)
+    out["batched_64x2^24_k32"] = config_entry(x.numel(), ms, sts, peak, form="10 async calls in flight")
+    del x
+    torch.cuda.empty_cache()
+    return out
+
+
+REF_SAMPLE_ELEMS = 1 << 26
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle itself, as it stands, on the host
+    cores.  Each step selects the top k of a 2^26-element sample of the same
+    workload (standard normal, from the CPU generator) with the oracle's
+    threaded form on every core; the config says so."""
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    import workloads
+    from oracle.topk import topk_chunked
+
+    n_sample = min(REF_SAMPLE_ELEMS, args.n)
+    cores = host_cores()
     x = workloads.normal(n_sample, 1, "cpu").numpy()
     for _ in range(args.warmup):
-        topk_sort(x, args.k)
+        topk_chunked(x, args.k, cores, 4 * cores)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        topk_sort(x, args.k)
+        topk_chunked(x, args.k, cores, 4 * cores)
         times.append(time.perf_counter() - t0)
     tot = sum(times)
     value = n_sample * args.steps / tot / 1e9
@@ -247,11 +414,14 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "Gelem/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": workload_name("normal", args.n, args.k), "n": args.n, "k": args.k, "eps": EPS,
-                   "sample_elems": n_sample},
-        "cpu_baseline": {"value": value, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
-                         "sample": f"each step: oracle.topk_sort (full sort, one thread) on a {n_sample}-element "
-                                   f"prefix-sized sample of the normal workload, k={args.k}"},
+        "config": {"workload": workload_name("normal", args.n, args.k), "n": n_sample, "k": args.k, "eps": EPS,
+                   "sample_of": f"each step selects from {n_sample} elements of the {args.n}-element workload's "
+                                f"distribution (the oracle would take about {args.n // n_sample} times as long "
+                                f"per call on the whole input)"},
+        "cpu_baseline": {"value": value, "unit": "Gelem/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: oracle.topk.topk_chunked (numpy selection per chunk on {cores} "
+                                   f"threads, then the exact merge) on a {n_sample}-element standard-normal "
+                                   f"sample, k={args.k}"},
         "e2e": {"value": value, "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -510,9 +680,13 @@ def main():
             torch.cuda.empty_cache()
         sweep["table4"] = table4
 
+    configs = None
+    if not args.no_sweep and args.gen == "normal" and n == N_DEFAULT:
+        configs = baseline_configs(pk, dev, stream, rank, peak)
+
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu and args.gpus == 1:
-        cpu = cpu_baseline(x[: 1 << 24].cpu().numpy(), k)
+        cpu = cpu_baseline(x.cpu().numpy(), k)
 
     if rank == 0:
         line = {
@@ -540,6 +714,7 @@ def main():
             "cpu_baseline": cpu,
             "protocol": protocol,
             "sweep": sweep,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -93,3 +93,15 @@ def test_reference_arm_prints_its_line():
     assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3 and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["n"] == bench.REF_SAMPLE_ELEMS and d["config"]["workload"] == "normal_2^30_k1024"
+    assert d["cpu_baseline"]["cores"] == bench.host_cores()
+
+
+def test_config_entry_and_binomial_bound():
+    sts = [{"attempts": 1, "aux_bytes": 10, "path": 0}, {"attempts": 3, "aux_bytes": 30, "path": 1}]
+    e = bench.config_entry(1 << 30, 0.5, sts, 6800.0)
+    assert e["retries"] == 2 and e["aux_bytes"] == 30 and e["paths"] == [0, 1]
+    assert e["hbm_gbs"] == pytest.approx(4 * 2**30 / 0.5e-3 / 1e9, abs=0.1)
+    assert e["hbm_frac_of_8TBs"] == pytest.approx(e["hbm_gbs"] / 8000, abs=1e-3)
+    # P(Binomial(10^4, 10^-3) <= 18) >= 0.99 > P(... <= 17): the bound the retry run is read against.
+    assert bench.binom_upper(10_000, 1e-3) == 18

@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 import workloads
-from oracle.topk import same_result, topk_partition, topk_rows, topk_sort
+from oracle.topk import same_result, topk_chunked, topk_partition, topk_rows, topk_sort
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
@@ -39,6 +39,8 @@ def test_sort_and_partition_match_brute_force(seed):
         pv, pi = topk_partition(x, k)
         assert same_result(sv, si, bv, bi)
         assert same_result(pv, pi, bv, bi)
+        for chunks in (1, 3, 7):
+            assert same_result(*topk_chunked(x, k, workers=2, chunks=chunks), bv, bi)
 
 
 def test_zero_signs_are_equal_and_bits_are_kept():
@@ -61,6 +63,16 @@ def test_partition_matches_sort_on_medium_inputs():
         x = workloads.GENERATORS[gen](50_000, seed, "cpu").numpy()
         for k in (1, 17, 4096, 50_000):
             assert same_result(*topk_sort(x, k), *topk_partition(x, k)), (gen, k)
+
+
+def test_chunked_matches_sort_on_medium_inputs():
+    # Ties straddling chunk boundaries (16 levels, the 256 ulps below 1.0), k
+    # larger than a chunk, and more chunks than threads.
+    for seed, gen in enumerate(["levels16", "ulps_below_one", "normal", "sorted_normal"]):
+        x = workloads.GENERATORS[gen](50_001, seed, "cpu").numpy()
+        for k in (1, 17, 4096, 20_000, 50_001):
+            for workers, chunks in ((4, None), (3, 16)):
+                assert same_result(*topk_sort(x, k), *topk_chunked(x, k, workers, chunks)), (gen, k, chunks)
 
 
 def test_closed_form_ulps_below_one():
