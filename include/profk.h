@@ -54,7 +54,7 @@ typedef enum profk_status {
                                     device-side consistency check of the library's own state failed
                                     (cuda_error 0; never expected) */
   PROFK_ERR_NAN = -3,            /* the input holds a NaN */
-  PROFK_ERR_UNSUPPORTED = -4,    /* e.g. n >= 2^40 or a misaligned input */
+  PROFK_ERR_UNSUPPORTED = -4,    /* e.g. n >= 2^40, or x not 4-byte aligned */
   PROFK_ERR_DEVICE_TIMEOUT = -5, /* a bounded device-side wait gave up */
   PROFK_ERR_SCRATCH = -6         /* the problem needs more than the fixed scratch or the caller's workspace */
 } profk_status;
@@ -91,8 +91,12 @@ typedef struct profk_stats {
 /* ---- the method -------------------------------------------------------- */
 
 /* Exact top-k of one row x[0..n) (problem statement: paper Section 3).
- *   x         device, n floats, 16-byte aligned for the vectorised filter
- *             (other alignments return PROFK_ERR_UNSUPPORTED)
+ *   x         device, n floats, 4-byte aligned (else PROFK_ERR_UNSUPPORTED).
+ *             The filter reads 16-byte blocks; a row that does not start on
+ *             a 16-byte boundary (a tensor slice such as x + 1) takes its
+ *             first and last elements with element loads, and its tie exit
+ *             (if any) by radix selection over the row instead of the
+ *             vectorised tie step.  The result is the same.
  *   n         1 <= n < 2^40.  A row longer than 2^32 elements (the paper's
  *             Table 4 goes to 4.3e9) is split into P = ceil(n / 2^32)
  *             contiguous segments of equal length rounded up to a multiple
@@ -124,7 +128,8 @@ int profk_topk(const float* x, int64_t n, int64_t k, double eps, uint64_t seed,
  * Each row gets the budget eps / rows, so one attempt of the whole call fails
  * with probability <= eps (union bound, Appendix E.2).  Rows that fail the
  * check are redrawn alone.
- *   ld        row stride in elements, ld >= n, ld % 4 == 0
+ *   ld        row stride in elements, ld >= n (any value: rows off the
+ *             16-byte grid are handled as profk_topk describes)
  *   out_vals  device, rows*k floats, row-major (row r at r*k)
  *   out_idx   device, rows*k int64, row-relative indices
  *   stats     host array of `rows` entries, or NULL
@@ -275,7 +280,7 @@ int profk_threshold(const float* vals, int64_t S, int64_t t, float* out_tau,
                     cudaStream_t stream);
 
 /* Step 3, filter (Section 3, stage 3; Appendix C): one pass over x[0..n)
- * (device, 16-byte aligned) counting out_counts[0] = R = |{x_i >= tau}|,
+ * (device, 4-byte aligned) counting out_counts[0] = R = |{x_i >= tau}|,
  * out_counts[1] = |{x_i > tau}|, out_counts[2] = |{x_i is NaN}| (device
  * uint64[3]), and storing min(R, M) passers into out_keys[0..M) (device) in
  * an unspecified order.  A passer (v, i) is stored as the 64-bit key
@@ -316,7 +321,7 @@ int profk_exact(const float* x, int64_t n, int64_t k, float* out_vals, int64_t* 
  * scratch), not the persistent ones of profk_topk, and synchronizes `stream`
  * once per attempt and once at the end.
  *   Limits: n <= 2^32 (longer rows return PROFK_ERR_UNSUPPORTED) and x
- *     16-byte aligned (else PROFK_ERR_UNSUPPORTED).  The array must hold, at
+ *     4-byte aligned (else PROFK_ERR_UNSUPPORTED).  The array must hold, at
  *     the parameters (S, t, M) that profk_params gives, each part rounded up
  *     to 256 bytes: the row state (8.3 KB); on the sampling route a hash table
  *     of 8 x (the power of two >= 2D) bytes with D = S + 2r + 8 sqrt(r) + 256

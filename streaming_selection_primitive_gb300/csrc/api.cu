@@ -470,6 +470,11 @@ __global__ void k_exact_to_tie(RowState* st, const int* rows) {
 
 int filter_grid(int64_t ctas_per_sm);
 
+// Whether every row starts on a 16-byte boundary.
+bool rows_aligned(const float* x, int64_t rows, int64_t ld) {
+  return (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (rows == 1 || (ld & 3) == 0);
+}
+
 // Rows from which the exact path goes through the value selection and the
 // tie step (measured: 430 vs 668 us at n = 2^26; below 2^25 the selection of
 // the 64-bit keys, which stops as soon as its bucket is exactly the rest of
@@ -760,13 +765,16 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   if (rows < 1 || n < 1 || k < 1 || k > n || ld < n || !(eps > 0.0 && eps < 1.0)) return PROFK_ERR_INVALID;
   if (rows > (1 << 20)) return PROFK_ERR_INVALID;
   if (n >= MAX_ROW) return PROFK_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(x) & 15) != 0 || (rows > 1 && (ld & 3) != 0)) return PROFK_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(x) & 3) != 0) return PROFK_ERR_UNSUPPORTED;  // not a float pointer
   if (n > max_segment()) return run_long_rows(x, rows, n, ld, k, eps, seed, out_vals, out_idx, stream, stats);
 
   const int mode = static_cast<int>(g_opt[PROFK_OPT_PARAM_MODE].load());
   const int max_attempts = static_cast<int>(std::max<int64_t>(0, g_opt[PROFK_OPT_MAX_ATTEMPTS].load()));
   // The first attempt's tie bookkeeping decides for a resumed call.
   const bool tie_exit = resume ? resume->tie_exit : g_opt[PROFK_OPT_TIE_EXIT].load() != 0;
+  // Rows that all start on a 16-byte boundary take the vectorised tie step
+  // (and the filter's bookkeeping for it); others the selection-based one.
+  const bool aligned_rows = rows_aligned(x, rows, ld);
   const int64_t fS = g_opt[PROFK_OPT_FORCE_S].load(), ft = g_opt[PROFK_OPT_FORCE_T].load(),
                 fM = g_opt[PROFK_OPT_FORCE_M].load();
   const bool timing = g_opt[PROFK_OPT_TIMING].load() != 0;
@@ -853,7 +861,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         resume_used = true;
       } else {
       PK_CHECK(enqueue_attempt(L, c.ws, P, a, ng, gl, rows, x, ld, n, k, seed, cps, out_vals, out_idx, stream,
-                               time_it ? t_events.e : nullptr, tie_exit));
+                               time_it ? t_events.e : nullptr, tie_exit && aligned_rows));
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[4], stream));
       PK_CHECK(cudaGetLastError());
       // Run-time check: read the exact counts of every row (written into
@@ -927,8 +935,9 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         } else if (tie_exit && Rg > static_cast<uint64_t>(P.M) && Rt < static_cast<uint64_t>(k)) {
           s.path = PROFK_PATH_TIE;
           // The filter kept the tie step's counts for the rows whose sample
-          // held tau more than once; the others need the counting pass.
-          (copies >= 2 ? tie : tie_count).push_back(r);
+          // held tau more than once (aligned rows); the others need the
+          // counting pass (or, unaligned, the selection-based step).
+          (copies >= 2 && aligned_rows ? tie : tie_count).push_back(r);
         } else {
           attempt[r] = a + 1;
           next.push_back(r);
@@ -950,6 +959,20 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
                    reinterpret_cast<unsigned long long*>(tw + align_up(tie_ctl_bytes() * rows) +
                                                          align_up(sizeof(unsigned) * nb * rows)),
                    nb, reinterpret_cast<TieCtl*>(tw), rows};
+        if (!aligned_rows) {
+          // Rows off the 16-byte grid: the selection passes over the rows'
+          // (value, index) keys below the resolved value ord(tau) (element
+          // loads), the k selected keys compacted, then sorted.  The rows'
+          // state is marked skip by the refinement, so the sort takes the
+          // listed rows whole.
+          launch_tie_init(static_cast<int>(tr.size()), tl, st, k, stream);
+          SelectArgs ia{KeySource::Input, x, ld, n, static_cast<int>(tr.size()), tl, st};
+          launch_select(ia, 0, false, 3, stream);
+          launch_compact(ia, sel, L.kstride, k, stream);
+          launch_sort_emit(sel, L.kstride, k, static_cast<int>(tr.size()), tl, x, ld, n, out_vals, out_idx, stream,
+                           nullptr, at<char>(c.ws, L.off_sort), L.rows);
+          continue;
+        }
         if (pass == 0)
           PK_CHECK(launch_tie_after_filter(ta, at<unsigned long long>(c.ws, L.off_buf), P.M, stream));
         else
@@ -1100,7 +1123,7 @@ int submit_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
   if (rows < 1 || n < 1 || k < 1 || k > n || ld < n || !(eps > 0.0 && eps < 1.0)) return PROFK_ERR_INVALID;
   if (rows > (1 << 20)) return PROFK_ERR_INVALID;
   if (n >= MAX_ROW) return PROFK_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(x) & 15) != 0 || (rows > 1 && (ld & 3) != 0)) return PROFK_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(x) & 3) != 0) return PROFK_ERR_UNSUPPORTED;  // not a float pointer
   profk_call* call = new profk_call;
   call->x = x;
   call->rows = rows;
@@ -1142,7 +1165,7 @@ int submit_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
   if (e == cudaSuccess)
     e = enqueue_attempt(L, call->ws, P, 0, static_cast<int>(rows), nullptr, rows, x, ld, n, k, seed,
                         g_opt[PROFK_OPT_FILTER_CTAS_PER_SM].load(), out_vals, out_idx, stream, nullptr,
-                        call->tie_exit);
+                        call->tie_exit && rows_aligned(x, rows, ld));
   if (e == cudaSuccess) {
     call->flag = reinterpret_cast<unsigned long long*>(
         align_up(reinterpret_cast<uintptr_t>(call->host + REPORT_BYTES * rows)));
@@ -1331,7 +1354,7 @@ const char* profk_strerror(int code) {
     case PROFK_ERR_INVALID: return "invalid argument";
     case PROFK_ERR_CUDA: return "CUDA error";
     case PROFK_ERR_NAN: return "input contains NaN";
-    case PROFK_ERR_UNSUPPORTED: return "unsupported input (n > 2^32 or misaligned pointer / stride)";
+    case PROFK_ERR_UNSUPPORTED: return "unsupported input (a row longer than the library takes, or x not 4-byte aligned)";
     case PROFK_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case PROFK_ERR_SCRATCH: return "problem needs more workspace than the fixed scratch or the caller's workspace";
     default: return "unknown status";
@@ -1427,7 +1450,7 @@ done:
 int profk_filter(const float* x, int64_t n, float tau, int64_t M, uint64_t* out_keys, uint64_t* out_counts,
                  cudaStream_t stream) {
   if (!x || !out_counts || n < 1 || M < 0 || (M > 0 && !out_keys) || n > (1ll << 32)) return PROFK_ERR_INVALID;
-  if ((reinterpret_cast<uintptr_t>(x) & 15) != 0) return PROFK_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(x) & 3) != 0) return PROFK_ERR_UNSUPPORTED;
   Call c;
   c.stream = stream;
   PK_CHECK(ws_alloc(c, align_up(sizeof(RowState))));

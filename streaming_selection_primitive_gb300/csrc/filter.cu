@@ -171,21 +171,27 @@ __device__ __forceinline__ void flush_stage(RowState& S, unsigned long long* sta
 // tied top, RowState::tau_copies >= 2) go to the TIE loop and the others to
 // the plain one; with it off the plain loop takes every row.  A row of the
 // other loop is skipped whole.
-template <int T, int U, bool TIE>
+template <int T, int U, bool TIE, bool UNAL>
 __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long long* stage) {
+  static_assert(!(TIE && UNAL), "the tie bookkeeping counts per aligned block");
   static_assert(4 * U <= 64, "at most 64 elements per lane");
   constexpr int64_t WT = 32 * 4 * U;  // elements per warp tile
   int stage_n = 0;  // warp-uniform
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (T / 32);
-  const int64_t tiles_per_row = (a.n + WT - 1) / WT;
+  // A row's warp tiles cover positions 0 .. n + head of the row counted from
+  // the 16-byte boundary at or before it (head: the 0-3 elements between;
+  // always 0 when every row is aligned); element e of the row is position
+  // e + head.
+  const int64_t tiles_per_row = (a.n + (UNAL ? 3 : 0) + WT - 1) / WT;
   const int64_t total = tiles_per_row * a.nrows;
   int cur = -1;
   bool active = false;  // the row `row` is this loop's and has state to flush
   int row = 0;
   float tau = 0.f;
   bool over = false;  // this warp saw the row's counter pass M
-  const float* xr = nullptr;
+  const float* xr = nullptr;  // the row's position 0 (head elements before the row)
+  int64_t head = 0;
   unsigned long long* br = nullptr;
   unsigned long long* tl = nullptr;  // the row's tie list (with the tie bookkeeping)
   unsigned* beq = nullptr;           // the row's per-block counts of tau
@@ -214,6 +220,10 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
       tkey = a.st[row].tau_key;
       tau = key_to_float(tkey);
       xr = a.x + static_cast<int64_t>(row) * a.ld;
+      if constexpr (UNAL) {
+        head = static_cast<int64_t>((reinterpret_cast<uintptr_t>(xr) >> 2) & 3u);
+        xr -= head;  // never read below the row: positions < head are masked
+      }
       br = a.buf + static_cast<int64_t>(row) * a.M;
       if constexpr (TIE) {
         tl = a.tie_keys + static_cast<int64_t>(row) * a.tie_stride;
@@ -230,7 +240,11 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
     }
     float4 v[U];
     uint64_t valid = ~0ull;
-    if (base + WT <= a.n) {
+    // A full tile holds only the row's elements; the row's element index of
+    // the tile's position 0 is ebase.
+    auto full_tile = [&]() { return UNAL ? base >= head && base + WT <= a.n + head : base + WT <= a.n; };
+    const int64_t ebase = UNAL ? base - head : base;
+    if (full_tile()) {
       const float4* p = reinterpret_cast<const float4*>(xr + base) + lane;
 #pragma unroll
       for (int u = 0; u < U; ++u) v[u] = ld_stream(p + u * 32);
@@ -242,7 +256,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int64_t i = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
-          const bool ok = i < a.n;
+          const bool ok = UNAL ? i >= head && i < a.n + head : i < a.n;
           f[c] = ok ? xr[i] : -INFINITY;
           valid |= static_cast<uint64_t>(ok) << (u * 4 + c);
         }
@@ -275,7 +289,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
           unsigned w = eq;
 #pragma unroll
           for (int o = 16; o >= 1; o >>= 1) w += __shfl_xor_sync(FULL_MASK, w, o);
-          if (lane == 0 && w) atomicAdd(beq + (base >> TIE_BLOCK_LOG2), w);
+          if (lane == 0 && w) atomicAdd(beq + (ebase >> TIE_BLOCK_LOG2), w);  // aligned rows: ebase = base
         }
       }
     };
@@ -306,7 +320,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
       // with the bookkeeping the x > tau (those rarely exist when the tie exit
       // applies).  A full tile is counted without masks or branches.
       unsigned cge = 0, cgt = 0;
-      if (base + WT <= a.n) {
+      if (full_tile()) {
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
@@ -328,7 +342,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
         if (__any_sync(FULL_MASK, cgt != 0)) {
           uint64_t ge, gtm;
           masks(ge, gtm);
-          tie_append_tile<U>(a.st[row], tl, a.k, gtm, v, base);
+          tie_append_tile<U>(a.st[row], tl, a.k, gtm, v, ebase);
         }
       }
       continue;
@@ -365,7 +379,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
               for (int c = 0; c < 4; ++c) {
                 const int e = u * 4 + c;
                 if ((ge >> e) & 1ull) {
-                  const int64_t idx = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
+                  const int64_t idx = ebase + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
                   stage[pos++] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
                 }
               }
@@ -388,7 +402,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
             const int e = u * 4 + c;
             if ((ge >> e) & 1ull) {
               if (pos < static_cast<unsigned long long>(a.M)) {
-                const int64_t idx = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
+                const int64_t idx = ebase + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
                 br[pos] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
               } else if constexpr (TIE) {
                 dropm |= gtm & (1ull << e);
@@ -399,7 +413,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
         }
       }
     }
-    if constexpr (TIE) tie_append_tile<U>(a.st[row], tl, a.k, dropm, v, base);
+    if constexpr (TIE) tie_append_tile<U>(a.st[row], tl, a.k, dropm, v, ebase);
   }
   if (active) {
     flush_stage<TIE>(a.st[row], stage, stage_n, br, a.M, over, tl, a.k, tkey);
@@ -407,13 +421,17 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
   }
 }
 
-template <int T, int U>
+// UNAL: some row is off the 16-byte grid (its own instantiation, so that the
+// aligned kernel's code is that of a kernel without the head).
+template <int T, int U, bool UNAL>
 __global__ void __launch_bounds__(T, 3) k_filter(FilterArgs a) {
   pdl_wait();
   __shared__ unsigned long long s_stage[T / 32][STAGE];
   unsigned long long* stage = s_stage[threadIdx.x >> 5];
-  filter_rows<T, U, false>(a, stage);
-  if (a.block_eq) filter_rows<T, U, true>(a, stage);
+  filter_rows<T, U, false, UNAL>(a, stage);
+  if constexpr (!UNAL) {
+    if (a.block_eq) filter_rows<T, U, true, false>(a, stage);
+  }
 }
 
 // Launch shape: threads per CTA and 16-byte loads per lane per warp tile.
@@ -430,19 +448,25 @@ constexpr int FU = PROFK_FILTER_VEC;
 
 int filter_default_grid(int sms) {
   int per = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_filter<FT, FU>, FT, 0);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_filter<FT, FU, false>, FT, 0);
   if (per < 1) per = 1;
   return sms * per;
 }
 
-void launch_filter(const FilterArgs& a, cudaStream_t stream) {
+void launch_filter(const FilterArgs& args, cudaStream_t stream) {
+  FilterArgs a = args;
+  const bool unaligned = (reinterpret_cast<uintptr_t>(a.x) & 15u) != 0 || (a.nrows > 1 && (a.ld & 3) != 0);
+  if (unaligned) a.block_eq = nullptr;  // the tie bookkeeping counts per aligned block
   const int64_t WT = 32 * 4 * FU;
-  const int64_t warp_tiles = ((a.n + WT - 1) / WT) * a.nrows;
+  const int64_t warp_tiles = ((a.n + (unaligned ? 3 : 0) + WT - 1) / WT) * a.nrows;
   const int64_t ctas = (warp_tiles + FT / 32 - 1) / (FT / 32);
   int grid = a.grid;
   if (ctas < grid) grid = static_cast<int>(ctas);
   if (grid < 1) grid = 1;
-  launch_kernel(k_filter<FT, FU>, grid, FT, 0, stream, a);
+  if (unaligned)
+    launch_kernel(k_filter<FT, FU, true>, grid, FT, 0, stream, a);
+  else
+    launch_kernel(k_filter<FT, FU, false>, grid, FT, 0, stream, a);
 }
 
 }  // namespace profk

@@ -279,6 +279,13 @@ struct FilterArgs {
   int64_t tie_stride = 0;
   int64_t k = 0;
 };
+// The filter pass over the listed rows.  x must be 4-byte aligned.  When some
+// row does not start on a 16-byte boundary (x 4-byte aligned only, or a row
+// stride that is not a multiple of 4), a kernel instantiation of its own
+// starts each row's warp tiles at the boundary at or before the row, and the
+// row's first and last tiles take the masked path (element loads of the
+// row's own elements only); the tie bookkeeping, which counts per aligned
+// block, is then dropped.
 void launch_filter(const FilterArgs& a, cudaStream_t stream);
 int filter_default_grid(int sms);
 

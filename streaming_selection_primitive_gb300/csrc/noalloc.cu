@@ -111,7 +111,7 @@ extern "C" int profk_topk_noalloc(const float* x, int64_t n, int64_t k, double e
   if (!x || !out_vals || !out_idx) return PROFK_ERR_INVALID;
   if (n < 1 || k < 1 || k > n || !(eps > 0.0 && eps < 1.0)) return PROFK_ERR_INVALID;
   if (n > (1ll << 32)) return PROFK_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(x) & 15) != 0) return PROFK_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(x) & 3) != 0) return PROFK_ERR_UNSUPPORTED;  // not a float pointer
 
   const int mode = static_cast<int>(profk_get_option(PROFK_OPT_PARAM_MODE));
   const int64_t max_attempts = profk_get_option(PROFK_OPT_MAX_ATTEMPTS);

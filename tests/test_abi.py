@@ -89,7 +89,8 @@ def test_invalid_arguments_are_rejected_before_any_device_work(pk):
     assert lib.profk_topk(C.c_void_p(258), 10, 1, 1e-3, 0, fake, fake, None, None) == -4
     assert lib.profk_topk_batched(fake, 0, 10, 10, 1, 1e-3, 0, fake, fake, None, None) == -1
     assert lib.profk_topk_batched(fake, 2, 10, 9, 1, 1e-3, 0, fake, fake, None, None) == -1
-    assert lib.profk_topk_batched(fake, 2, 10, 10, 1, 1e-3, 0, fake, fake, None, None) == -4  # ld % 4
+    # x must be a float pointer (4-byte aligned); any row stride ld >= n is taken.
+    assert lib.profk_topk_batched(C.c_void_p(258), 2, 10, 10, 1, 1e-3, 0, fake, fake, None, None) == -4
     assert lib.profk_sample(fake, 10, 6, 0, 0, 0, fake, fake, None) == -1
     assert lib.profk_threshold(fake, 10, 11, fake, None) == -1
     assert lib.profk_refine(fake, 5, 6, fake, 10, fake, fake, None) == -1
@@ -120,7 +121,7 @@ def test_async_argument_checks(pk):
     assert lib.profk_topk_async(None, 10, 1, 1e-3, 0, fake, fake, None, C.byref(h)) == -1
     assert not h.value  # no call was created
     assert lib.profk_topk_async(fake, 10, 1, 1e-3, 0, fake, fake, None, None) == -1
-    assert lib.profk_topk_batched_async(fake, 2, 10, 10, 1, 1e-3, 0, fake, fake, None, C.byref(h)) == -4
+    assert lib.profk_topk_batched_async(C.c_void_p(258), 2, 10, 10, 1, 1e-3, 0, fake, fake, None, C.byref(h)) == -4
     assert lib.profk_wait(None, None) == -1
 
 
@@ -145,7 +146,7 @@ def test_long_row_workspace_size(pk):
 
 def test_noalloc_argument_and_size_checks(pk):
     # The entry point that allocates nothing refuses, before any device work:
-    # bad arguments, rows beyond 2^32 elements or misaligned, and problems whose
+    # bad arguments, rows beyond 2^32 elements or not float-aligned, and problems whose
     # workspace does not fit its fixed scratch (k = n = 2^23 takes the exact
     # route and needs 8 x 2^23 bytes of selection keys, beyond 32 MiB).
     from streaming_selection_primitive_gb300 import _abi
@@ -156,7 +157,7 @@ def test_noalloc_argument_and_size_checks(pk):
     assert lib.profk_topk_noalloc(fake, 10, 11, 1e-3, 0, fake, fake, None, None) == _abi.PROFK_ERR_INVALID
     assert lib.profk_topk_noalloc(fake, (1 << 32) + 4, 1, 1e-3, 0, fake, fake, None, None) == \
         _abi.PROFK_ERR_UNSUPPORTED
-    assert lib.profk_topk_noalloc(C.c_void_p(260), 100, 1, 1e-3, 0, fake, fake, None, None) == \
+    assert lib.profk_topk_noalloc(C.c_void_p(258), 100, 1, 1e-3, 0, fake, fake, None, None) == \
         _abi.PROFK_ERR_UNSUPPORTED
     assert lib.profk_topk_noalloc(fake, 1 << 23, 1 << 23, 1e-3, 0, fake, fake, None, None) == \
         _abi.PROFK_ERR_SCRATCH

@@ -1,0 +1,115 @@
+"""Rows that do not start on a 16-byte boundary, against the oracle.
+
+The problem statement takes any vector x (corrected paper, Section 3); a tensor
+slice such as x[1:] starts 4, 8 or 12 bytes past a 16-byte boundary, and a
+row stride that is not a multiple of 4 puts the rows of a batch at every such
+offset.  The filter then reads the row's first and last elements one by one,
+and the tie exit takes its selection-based form.  Every path is checked at
+offsets 1, 2 and 3: the result (values as bits, indices, order) and the
+per-attempt statistics must equal the oracle procedure's.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_helpers import assert_same
+from oracle import profk as PK
+from routing import oracle_profk
+
+pytestmark = pytest.mark.gpu
+
+OFFSETS = (1, 2, 3)
+
+
+def sliced(gen, n, off, seed, device):
+    base = workloads.GENERATORS[gen](n + 8, seed, device)
+    x = base[off:off + n]
+    assert x.data_ptr() % 16 == 4 * off
+    return x
+
+
+def check(pk, x, k, seed, eps=1e-3, **kw):
+    v, i, st = pk.topk(x, k, eps, seed)
+    ov, oi, ost = oracle_profk(x.cpu().numpy(), k, eps, seed, **kw)
+    assert_same(v, i, ov, oi, f"offset {x.data_ptr() % 16 // 4} n={x.numel()} k={k}")
+    assert (st["path"], st["attempts"], st["R_first"], st["R_gt_first"]) == \
+        (ost.path, ost.attempts, ost.R_first, ost.R_gt_first), (st, ost)
+    return st
+
+
+@pytest.mark.parametrize("off", OFFSETS)
+@pytest.mark.parametrize("gen,n,k", [("normal", (1 << 20) + 5, 64), ("uniform", 1 << 22, 1),
+                                     ("normal", 1 << 24, 1000), ("pareto", (1 << 22) + 3, 20_000)])
+def test_filter_path_unaligned(pk, cuda_device, off, gen, n, k):
+    x = sliced(gen, n, off, 11, cuda_device)
+    st = check(pk, x, k, 5)
+    assert st["path"] in (PK.PATH_FILTER, PK.PATH_FALLBACK) or st["attempts"] > 1
+
+
+@pytest.mark.parametrize("off", OFFSETS)
+def test_tie_exit_unaligned(pk, cuda_device, off):
+    # 16 levels: tau lands on the k-th value with R >> M; the selection-based
+    # tie step replaces the vectorised one, with the same result.
+    x = sliced("levels16", 1 << 22, off, 3, cuda_device)
+    for k in (100, 9000):
+        st = check(pk, x, k, 7)
+        assert st["path"] == PK.PATH_TIE
+
+
+@pytest.mark.parametrize("off", OFFSETS)
+def test_exact_and_fallback_unaligned(pk, cuda_device, off):
+    check(pk, sliced("normal", 1 << 16, off, 4, cuda_device), 77, 1)  # exact route (S > n/8)
+    pk.set_option(pk.OPT_MAX_ATTEMPTS, 0)
+    st = check(pk, sliced("normal", 1 << 22, off, 5, cuda_device), 500, 2, max_attempts=0)
+    assert st["path"] == PK.PATH_FALLBACK
+
+
+@pytest.mark.parametrize("rows,n,ld", [(5, 1 << 20, (1 << 20) + 1), (6, 300_001, 300_003), (3, 1 << 22, (1 << 22) + 2)])
+def test_batched_rows_at_every_offset(pk, cuda_device, rows, n, ld):
+    base = workloads.normal(rows * ld + 8, rows, cuda_device)
+    x = base[1:1 + rows * ld].view(rows, ld)[:, :n]
+    assert len({(x[r].data_ptr() % 16) for r in range(rows)}) > 1
+    k = 50
+    vals, idx, sts = pk.topk_batched(x, k, 1e-3, 13)
+    h = x.cpu().numpy()
+    for r in range(rows):
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 13, row=r, rows=rows)
+        assert_same(vals[r], idx[r], ov, oi, f"row {r} at offset {x[r].data_ptr() % 16 // 4}")
+        assert (sts[r]["path"], sts[r]["R_first"]) == (ost.path, ost.R_first)
+
+
+def test_batched_tie_rows_unaligned(pk, cuda_device):
+    rows, n, ld = 4, 1 << 19, (1 << 19) + 3
+    base = workloads.levels16(rows * ld + 8, 9, cuda_device)
+    x = base[2:2 + rows * ld].view(rows, ld)[:, :n]
+    vals, idx, sts = pk.topk_batched(x, 700, 1e-3, 4)
+    h = x.cpu().numpy()
+    for r in range(rows):
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), 700, 1e-3 / rows, 4, row=r, rows=rows)
+        assert_same(vals[r], idx[r], ov, oi, f"tie row {r}")
+        assert sts[r]["path"] == ost.path == PK.PATH_TIE
+
+
+@pytest.mark.parametrize("off", OFFSETS)
+def test_async_and_noalloc_unaligned(pk, cuda_device, off):
+    x = sliced("normal", (1 << 22) + 1, off, 6, cuda_device)
+    h = x.cpu().numpy()
+    ov, oi, ost = oracle_profk(h, 1000, 1e-3, 8)
+    v, i, st = pk.topk_async(x, 1000, 1e-3, 8).wait()
+    assert_same(v, i, ov, oi, f"async offset {off}")
+    v, i, st = pk.topk_noalloc(x, 1000, 1e-3, 8)
+    assert_same(v, i, ov, oi, f"noalloc offset {off}")
+    assert st["R_first"] == ost.R_first
+
+
+@pytest.mark.parametrize("off", OFFSETS)
+def test_filter_step_unaligned(pk, cuda_device, off):
+    x = sliced("normal", (1 << 20) + 7, off, 7, cuda_device)
+    tau = 2.5
+    keys, counts = pk.filter_pass(x, tau, 20_000)
+    h = x.cpu().numpy()
+    R, R_gt = PK.filter_counts(h, np.float32(tau))
+    assert counts.tolist() == [R, R_gt, 0]
+    got = np.sort((~(keys[:R].cpu().numpy().view(np.uint64) & np.uint64(0xFFFFFFFF))).astype(np.uint32))
+    assert np.array_equal(got, np.flatnonzero(h >= np.float32(tau)).astype(np.uint32))
