@@ -80,7 +80,7 @@ typedef struct profk_stats {
   float tau_final;
   int32_t attempts;          /* filter passes run for this row (0 on the exact path) */
   int32_t path;              /* a profk_path */
-  int32_t draw_doublings;    /* times the draw budget had to grow (see profk_sample) */
+  int32_t draw_doublings;    /* always 0: the sample has no repeats to redraw (see profk_sample) */
   int32_t cuda_error;        /* cudaError_t of the failing call, else 0 */
   uint64_t aux_bytes;        /* device workspace of the whole call, bytes */
   float filter_ms;           /* device time of the first filter pass over all rows when
@@ -239,10 +239,11 @@ typedef enum profk_option {
 #define PROFK_WAIT_TEST_REFINE 2
 #define PROFK_WAIT_TEST_SORT 3
 /* Forms of the sampling kernels (PROFK_OPT_SAMPLER); both give the same
- * sample and tau.  GRID: one persistent kernel whose CTAs (all resident) meet
- * at grid barriers; taken when each CTA's share of the draws fits its
- * registers or shared memory.  STEPS: barrier-free kernels, one per step,
- * then a radix selection of tau; taken otherwise. */
+ * sample and tau.  GRID: one persistent kernel (all CTAs resident), each CTA
+ * taking up to 1024 sample positions; tau from per-CTA candidate lists that
+ * one CTA waits for (t <= 128) or from passes whose CTAs meet at grid
+ * barriers (larger t).  STEPS: one thread per sample position, then a radix
+ * selection of tau; taken when the rows' shares of the SMs are too small. */
 #define PROFK_SAMPLER_AUTO 0
 #define PROFK_SAMPLER_GRID 1
 #define PROFK_SAMPLER_STEPS 2
@@ -263,14 +264,21 @@ const char* profk_strerror(int code);
 
 /* ---- the individual steps (for testing and composition) ---------------- */
 
-/* Step 1, sampling (paper Section 3, stage 1).  The sample is the first S
- * distinct values of the draw stream u_0, u_1, ... in order of first
- * appearance, where draw i is
- *   w = Philox4x64-10(counter = (i / 4, attempt, j, 0), key = (seed, row))[i % 4]
- * accepted by Lemire's method for the range n (128-bit product m = w * n,
- * reject while (m mod 2^64) < (2^64 - n) mod n, retrying with j = 1, 2, ...),
- * u_i = m >> 64.  Writes out_sidx[0..S) (device int64) and
- * out_vals[0..S) = x[out_sidx] (device float).  Requires 1 <= S <= n/2. */
+/* Step 1, sampling (paper Section 3, stage 1: a uniform sample of S indices
+ * without replacement).  The sample is pi(0), ..., pi(S-1) for a keyed
+ * pseudo-random permutation pi of [0, n):
+ *   round keys K_0 .. K_11: the words of Philox4x64-10 blocks with counters
+ *     (q, attempt, 0, 0), q = 0, 1, 2, under the key (seed, row), in order;
+ *   E: a twelve-round Feistel network on [0, 2^b), b = max(2, ceil(log2 n)):
+ *     round i splits the state into its high part L and its low w bits R
+ *     (w = floor(b/2) in round 0, then the widths alternate) and maps it to
+ *     (R << (b - w)) | (L xor (mix(R xor K_i) mod 2^(b - w))), mix being the
+ *     SplitMix64 output function (z ^= z >> 30; z *= 0xBF58476D1CE4E5B9;
+ *     z ^= z >> 27; z *= 0x94D049BB133111EB; z ^= z >> 31, mod 2^64);
+ *   pi(j): E applied to j, then again while the value is >= n.
+ * The S indices are distinct by construction.  Writes out_sidx[0..S)
+ * (device int64, in that order) and out_vals[0..S) = x[out_sidx] (device
+ * float).  Requires 1 <= S <= n <= 2^32. */
 int profk_sample(const float* x, int64_t n, int64_t S, uint64_t seed, int64_t row,
                  int32_t attempt, int64_t* out_sidx, float* out_vals, cudaStream_t stream);
 

@@ -11,8 +11,11 @@ Modules
 -------
 topk       exact top-k by full sort (the definition), an O(N) restatement of the
            same definition for large inputs, and order-key helpers.
-philox     Philox4x64-10 counter-based generator (Salmon et al., SC'11),
-           Lemire's bounded integers, and the "first S distinct draws" sampler.
+philox     Philox4x64-10 counter-based generator (Salmon et al., SC'11) and the
+           sampler: the first S values of a keyed Feistel permutation of [0, n)
+           cycle-walked into range (numpy definition).
+csample    the same sampler in plain C (sampler.c, built with gcc on first use)
+           for the Monte-Carlo checks, held equal to the numpy definition.
 hypergeom  hypergeometric pmf / cdf / quantile in fp64.
 params     parameter rules: the corrected paper's Algorithm 1 (fast t, M), its
            Theorem 4 (exact t*, M*), and the older version's closed forms

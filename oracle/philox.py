@@ -6,24 +6,44 @@ Prof-K's first stage draws S indices uniformly *without replacement* from
 pages do not say how the subset is drawn.  The reading taken here, shared with
 the CUDA library only as a written definition (no code is shared):
 
-Draw stream.  For a call with user seed ``seed``, batch row ``row`` and
-attempt ``attempt`` (0 for the first pass, +1 per redraw), draw number i
-(i = 0, 1, 2, ...) is produced as follows.  Rejection round j starts at 0.
+Permutation.  For a call with user seed ``seed``, batch row ``row`` and
+attempt ``attempt`` (0 for the first pass, +1 per redraw), a keyed
+pseudo-random permutation pi of [0, n) is built in two steps.
 
-  1. w = Philox4x64-10(counter=(i // 4, attempt, j, 0), key=(seed, row))[i % 4]
-  2. Lemire's bounded integer: m = w * n as a 128-bit product; let lo be its
-     low 64 bits.  If lo < (2^64 - n) mod n the word is rejected: j += 1 and
-     go to 1.  Otherwise the draw is u_i = m >> 64, uniform on [0, n).
+  1. Round keys K_0 .. K_11: the twelve words of the Philox4x64-10 blocks
+     with counters (q, attempt, 0, 0), q = 0, 1, 2, under the key (seed, row),
+     in order.
+  2. A Feistel network E on [0, 2^b), b = max(2, ceil(log2 n)), of twelve
+     rounds.  The state x is split into a high part L and a low part R of
+     width w (w = floor(b/2) in round 0); round i maps it to
+         x' = (R << (b - w)) | (L xor (f_i(R) mod 2^(b - w)))
+     and the next round splits at w' = b - w.  Every round is invertible, so
+     E permutes [0, 2^b).  The round function is f_i(R) = mix(R xor K_i),
+     mix being the SplitMix64 output function (Steele, Lea and Flood, "Fast
+     splittable pseudorandom number generators", OOPSLA 2014):
+         z ^= z >> 30; z *= 0xBF58476D1CE4E5B9; z ^= z >> 27;
+         z *= 0x94D049BB133111EB; z ^= z >> 31     (mod 2^64).
+  3. Cycle-walking into [0, n): pi(j) = the first of E(j), E(E(j)), ... that
+     is below n.  Because E is a permutation and j < n, the walk returns to
+     [0, n), and pi is a permutation of [0, n) (Black and Rogaway, "Ciphers
+     with arbitrary finite domains", CT-RSA 2002).  Since 2^b < 2n, a walk
+     takes fewer than two steps on average.
 
-Sample.  The sample is the first S *distinct* values of u_0, u_1, ..., in order
-of first appearance.  Rejecting repeats while drawing i.i.d. uniform indices
-yields every ordered S-tuple of distinct indices with probability
-1 / (n (n-1) ... (n-S+1)), so the set is a uniform S-subset, as the analysis
-requires.
+Sample.  The sample is pi(0), pi(1), ..., pi(S-1): S distinct indices by
+construction, in that order.  With enough rounds of a well-mixing round
+function the set is a uniform S-subset to the precision the analysis needs;
+twelve rounds are where the subset law passes a chi-square test even on
+domains of 3 to 8 elements (four rounds of the same kind fail there), and the
+tests also check the positions of the indices and Lemma 1 by Monte Carlo.
 
 Philox4x64-10 is the generator of Salmon, Moraes, Dror and Shaw, "Parallel
 random numbers: as easy as 1, 2, 3" (SC'11): ten rounds of two 64x64->128
 multiplications, with the key bumped by two Weyl constants between rounds.
+
+This module writes the definition out in numpy (slow, vectorised); the same
+definition in plain C (oracle/sampler.c, through oracle.csample) serves the
+Monte-Carlo tests, which need about 10^9 round-function calls, and the tests
+require the two to agree element by element.
 """
 from __future__ import annotations
 
@@ -88,76 +108,72 @@ def philox4x64(c0, c1, c2, c3, k0, k1, rounds: int = 10):
     return c0, c1, c2, c3
 
 
-def lemire_accept(w: int, n: int, bits: int = 64):
-    """Lemire's multiply-shift bounded integer for one word of ``bits`` bits.
-
-    Returns the value in [0, n) or None when the word is rejected.  ``bits`` is
-    a parameter only so that tests can check the method exhaustively on small
-    words; the sampler uses 64.
-    """
-    full = 1 << bits
-    m = w * n
-    lo = m & (full - 1)
-    if lo < (full - n) % n:
-        return None
-    return m >> bits
+FEISTEL_ROUNDS = 12
+MIX_M1 = 0xBF58476D1CE4E5B9  # SplitMix64 output function (Steele, Lea, Flood, OOPSLA 2014)
+MIX_M2 = 0x94D049BB133111EB
 
 
-def draw_values(n: int, seed: int, row: int, attempt: int, start: int, stop: int) -> np.ndarray:
-    """Draws u_start .. u_{stop-1} of the stream defined in the module docstring."""
-    if not (1 <= n <= (1 << 32)):
-        raise ValueError("n must be in [1, 2^32]")
-    if stop <= start:
-        return np.empty(0, dtype=np.int64)
-    b0, b1 = start >> 2, ((stop - 1) >> 2) + 1
-    blocks = np.arange(b0, b1, dtype=np.uint64)
-    w = np.stack(philox4x64(blocks, attempt, 0, 0, seed, row), axis=1).reshape(-1)
-    w = w[start - 4 * b0: stop - 4 * b0]
-    hi, lo = mulhilo64(w, np.uint64(n))
-    thr = np.uint64(((1 << 64) - n) % n)
-    out = hi.astype(np.int64)
-    for p in np.flatnonzero(lo < thr):
-        i = start + int(p)
-        j = 1
-        while True:
-            word = philox4x64_scalar((i >> 2, attempt, j, 0), (seed, row))[i & 3]
-            v = lemire_accept(word, n)
-            if v is not None:
-                out[p] = v
-                break
-            j += 1
-    return out
+def domain_bits(n: int) -> int:
+    """b = max(2, ceil(log2 n)): the Feistel network permutes [0, 2^b), 2^b >= n."""
+    return max(2, (int(n) - 1).bit_length())
 
 
-def draw_values_many(n: int, seeds, row: int, attempt: int, stop: int) -> np.ndarray:
-    """Draws u_0 .. u_{stop-1} for many seeds at once (int64[len(seeds), stop])."""
-    seeds = np.asarray(seeds, dtype=np.uint64).reshape(-1, 1)
-    nb = (stop + 3) >> 2
-    blocks = np.arange(nb, dtype=np.uint64).reshape(1, -1)
-    w = np.stack(philox4x64(blocks, attempt, 0, 0, seeds, row), axis=2).reshape(seeds.shape[0], -1)[:, :stop]
-    hi, lo = mulhilo64(w, np.uint64(n))
-    thr = np.uint64(((1 << 64) - n) % n)
-    out = hi.astype(np.int64)
-    for r, p in zip(*np.nonzero(lo < thr)):
-        i, j = int(p), 1
-        while True:
-            word = philox4x64_scalar((i >> 2, attempt, j, 0), (int(seeds[r, 0]), row))[i & 3]
-            v = lemire_accept(word, n)
-            if v is not None:
-                out[r, p] = v
-                break
-            j += 1
-    return out
+def round_keys(seed: int, row: int, attempt: int) -> list:
+    """K_0 .. K_11: the words of Philox4x64-10 blocks (q, attempt, 0, 0), q = 0, 1, 2."""
+    keys = []
+    for q in range((FEISTEL_ROUNDS + 3) // 4):
+        keys += philox4x64_scalar((q, attempt, 0, 0), (seed, row))
+    return keys[:FEISTEL_ROUNDS]
+
+
+def mix64(z):
+    """The SplitMix64 output function on uint64 arrays (products mod 2^64)."""
+    z = np.asarray(z, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(MIX_M1)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(MIX_M2)
+        return z ^ (z >> np.uint64(31))
+
+
+def feistel(x, bits: int, keys) -> np.ndarray:
+    """E(x) for every x of a uint64 array: the rounds of the module docstring."""
+    x = np.asarray(x, dtype=np.uint64).copy()
+    w = bits // 2
+    for k in keys:
+        wl = bits - w
+        right = x & np.uint64((1 << w) - 1)
+        left = x >> np.uint64(w)
+        f = mix64(right ^ np.uint64(k))
+        x = (right << np.uint64(wl)) | (left ^ (f & np.uint64((1 << wl) - 1)))
+        w = wl
+    return x
+
+
+def permute(j, n: int, seed: int, row: int = 0, attempt: int = 0) -> np.ndarray:
+    """pi(j) for every j (all < n): E applied until the value falls below n."""
+    j = np.asarray(j, dtype=np.uint64)
+    if j.size and int(j.max()) >= n:
+        raise ValueError("need j < n")
+    b = domain_bits(n)
+    keys = round_keys(seed, row, attempt)
+    out = feistel(j, b, keys)
+    walking = np.flatnonzero(out >= np.uint64(n))
+    while walking.size:
+        out[walking] = feistel(out[walking], b, keys)
+        walking = walking[out[walking] >= np.uint64(n)]
+    return out.astype(np.int64)
+
+
+def sample_indices_numpy(n: int, S: int, seed: int, row: int = 0, attempt: int = 0) -> np.ndarray:
+    """The sample pi(0), ..., pi(S-1) (int64[S]), by the numpy definition."""
+    if not (1 <= S <= n):
+        raise ValueError("need 1 <= S <= n")
+    return permute(np.arange(S, dtype=np.uint64), n, seed, row, attempt)
 
 
 def sample_indices(n: int, S: int, seed: int, row: int = 0, attempt: int = 0) -> np.ndarray:
-    """The first S distinct draws, in order of first appearance (int64[S])."""
-    if not (1 <= S <= n):
-        raise ValueError("need 1 <= S <= n")
-    D = S + 64
-    while True:
-        u = draw_values(n, seed, row, attempt, 0, D)
-        _, first = np.unique(u, return_index=True)
-        if first.size >= S:
-            return u[np.sort(first)[:S]]
-        D *= 2
+    """The sample pi(0), ..., pi(S-1) (int64[S]), by the C form of the same
+    definition (oracle/sampler.c), which the tests hold equal to the numpy one."""
+    from . import csample
+
+    return csample.sample_indices(n, S, seed, row, attempt)

@@ -157,21 +157,17 @@ def first_attempt_ranks(xs, N: int, S: int, t: int, seeds, row: int = 0):
     depends only on (N, S, seed), so one draw serves every input.  Returns
     int64 arrays of shape (len(xs), len(seeds)) for R and R_gt.
     """
+    from . import csample
+
     seeds = list(seeds)
     R = np.zeros((len(xs), len(seeds)), dtype=np.int64)
     Rg = np.zeros_like(R)
-    D = S + 64 + 4 * S * S // N
     chunk = 64
     for c0 in range(0, len(seeds), chunk):
         cs = seeds[c0:c0 + chunk]
-        u = philox.draw_values_many(N, cs, row, 0, D)
-        for j, sd in enumerate(cs):
-            _, first = np.unique(u[j], return_index=True)
-            if first.size >= S:
-                sidx = u[j][np.sort(first)[:S]]
-            else:
-                sidx = philox.sample_indices(N, S, sd, row, 0)
+        sidx = csample.sample_many(N, S, cs, row, 0)
+        for j in range(len(cs)):
             for q, x in enumerate(xs):
-                tau = threshold(x[sidx], t)
+                tau = threshold(x[sidx[j]], t)
                 R[q, c0 + j], Rg[q, c0 + j] = filter_counts(x, tau)
     return R, Rg

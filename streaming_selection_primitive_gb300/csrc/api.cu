@@ -160,23 +160,20 @@ __global__ void k_attempt_init(RowState* st, const int* rows) {
   S.error = 0;
 }
 
-// Start of an attempt for the listed rows: hash table back to "empty",
-// counters to zero, and the selection state ready for tau (rank t).
-// The control blocks of each row's sampling (sample_ctl, sample_words 8-byte
-// words per row) and refinement (sort_ctl, ctl_words) are zeroed too.
-__global__ void k_attempt_reset(unsigned long long* table, int log2H, const int* rows, RowState* st,
-                                unsigned long long t, unsigned long long* sort_ctl, int ctl_words,
-                                unsigned long long* sample_ctl, int sample_words, unsigned* block_eq,
+// Start of an attempt for the listed rows: counters to zero and the
+// selection state ready for tau (rank t).  The control blocks of each row's
+// sampling (sample_ctl, sample_words 8-byte words per row) and refinement
+// (sort_ctl, ctl_words) are zeroed too.
+__global__ void k_attempt_reset(const int* rows, RowState* st, unsigned long long t, unsigned long long* sort_ctl,
+                                int ctl_words, unsigned long long* sample_ctl, int sample_words, unsigned* block_eq,
                                 int64_t nblocks) {
   pdl_trigger();
   pdl_wait();
   const int row = launch_row(rows);
-  // 16-byte stores, grid-strided over the row's CTAs: the hash table to
-  // "empty", the control blocks (an even number of words each) to zero.
+  // 16-byte stores, grid-strided over the row's CTAs: the control blocks (an
+  // even number of words each) to zero.
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t gstride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  ulonglong2* tb = reinterpret_cast<ulonglong2*>(table + (static_cast<int64_t>(row) << log2H));
-  for (int64_t i = gtid; i < (int64_t(1) << log2H) / 2; i += gstride) tb[i] = make_ulonglong2(~0ull, ~0ull);
   if (sort_ctl) {
     ulonglong2* sc = reinterpret_cast<ulonglong2*>(sort_ctl + static_cast<int64_t>(row) * ctl_words);
     for (int64_t i = gtid; i < ctl_words / 2; i += gstride) sc[i] = make_ulonglong2(0ull, 0ull);
@@ -209,18 +206,6 @@ __global__ void k_attempt_reset(unsigned long long* table, int log2H, const int*
     S.tie_gt = 0;
     S.tau_copies = 0;
   }
-}
-
-// Hash tables of the listed rows back to "empty".
-__global__ void k_reset_tables(unsigned long long* table, int log2H, const int* rows) {
-  pdl_trigger();
-  pdl_wait();
-  const int row = launch_row(rows);
-  unsigned long long* t = table + (static_cast<int64_t>(row) << log2H);
-  const int64_t H = 1ll << log2H;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < H;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    t[i] = ~0ull;
 }
 
 __global__ void k_set_tau(RowState* st, float tau) {
@@ -264,30 +249,19 @@ __global__ void k_sample_out(const uint32_t* sidx, int64_t S, const float* x, in
 size_t align_up(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-  int64_t rows = 0, n = 0, k = 0, S = 0, D = 0, M = 0, nbD = 0, kstride = 0;
-  int log2H = 0;
+  int64_t rows = 0, n = 0, k = 0, S = 0, M = 0, kstride = 0;
   bool sampling = false;
   bool radix_refine = false;  // step 4 on the filter buffer by the radix sort
-  size_t off_state = 0, off_lists = 0, off_table = 0, off_draws = 0, off_blockcnt = 0, off_sidx = 0, off_skeys = 0,
-         off_buf = 0, off_sel = 0, off_sort = 0, off_refine = 0, off_sctl = 0, off_tie = 0, total = 0;
+  size_t off_state = 0, off_lists = 0, off_sidx = 0, off_skeys = 0, off_buf = 0, off_sel = 0, off_sort = 0,
+         off_refine = 0, off_sctl = 0, off_tie = 0, total = 0;
 };
 
-int64_t draw_budget(int64_t n, int64_t S) {
-  // Expected repeats among the first ~S draws are about S^2 / (2n); ask for
-  // twice that plus 8 standard deviations and a margin, so that growing D
-  // is practically never needed (the result does not depend on D).
-  const double rep = static_cast<double>(S) * static_cast<double>(S) / (2.0 * static_cast<double>(n));
-  int64_t D = S + static_cast<int64_t>(2.0 * rep + 8.0 * std::sqrt(rep) + 256.0);
-  return (D + 3) & ~3ll;
-}
-
-Layout make_layout(int64_t rows, int64_t n, int64_t k, int64_t S, int64_t D, int64_t M, bool sampling) {
+Layout make_layout(int64_t rows, int64_t n, int64_t k, int64_t S, int64_t M, bool sampling) {
   Layout L;
   L.rows = rows;
   L.n = n;
   L.k = k;
   L.S = S;
-  L.D = D;
   L.M = M;
   L.sampling = sampling;
   L.kstride = sort_stride(k);
@@ -297,20 +271,6 @@ Layout make_layout(int64_t rows, int64_t n, int64_t k, int64_t S, int64_t D, int
   L.off_lists = off;
   off = align_up(off + sizeof(int) * rows * 4);
   if (sampling) {
-    L.log2H = 1;
-    while ((1ll << L.log2H) < 2 * D) ++L.log2H;
-    // Twice as sparse where all rows' tables together stay within 32 MB: the
-    // draws of a single row then meet fewer occupied home slots (measured:
-    // 2^30, 106K draws, 37 -> 32 us), while many rows keep the denser tables,
-    // whose total stays in L2 (64 rows of 2^24: 158 us dense, 181 sparse).
-    if ((rows << (L.log2H + 1)) * static_cast<int64_t>(sizeof(unsigned long long)) <= (int64_t(32) << 20)) ++L.log2H;
-    L.nbD = (D + 1023) / 1024;
-    L.off_table = off;
-    off = align_up(off + sizeof(unsigned long long) * (static_cast<size_t>(rows) << L.log2H));
-    L.off_draws = off;
-    off = align_up(off + sizeof(uint32_t) * rows * D);
-    L.off_blockcnt = off;
-    off = align_up(off + sizeof(uint32_t) * rows * L.nbD);
     L.off_sidx = off;
     off = align_up(off + sizeof(uint32_t) * rows * S);
     L.off_skeys = off;
@@ -318,7 +278,7 @@ Layout make_layout(int64_t rows, int64_t n, int64_t k, int64_t S, int64_t D, int
     L.off_buf = off;
     off = align_up(off + sizeof(unsigned long long) * rows * M);
     L.off_sctl = off;
-    off = align_up(off + sample_tau_ctl_bytes() * rows);
+    off = align_up(off + sample_tau_scratch_bytes(rows));
   }
   L.off_sel = off;
   off = align_up(off + sizeof(unsigned long long) * rows * L.kstride);
@@ -552,14 +512,15 @@ void fill_stats_params(profk_stats* s, const Params& P) {
 }
 
 
-// Kernels of steps 1-2 for ng rows of D draws each: the step-by-step ones
-// when PROFK_OPT_SAMPLER asks for them, else the persistent grid kernel
-// where its CTAs' shares of the draws fit, else the step-by-step ones.
+// Kernels of steps 1-2 for ng rows of S sample positions each: the
+// step-by-step ones when PROFK_OPT_SAMPLER asks for them, else the
+// persistent grid kernel where its CTAs' shares of the sample fit their
+// registers, else the step-by-step ones.
 enum class Sampler { Grid, Steps };
 
-Sampler choose_sampler(int64_t D, int64_t ng, uint64_t n) {
+Sampler choose_sampler(int64_t S, int64_t ng) {
   if (g_opt[PROFK_OPT_SAMPLER].load() == PROFK_SAMPLER_STEPS) return Sampler::Steps;
-  return sample_tau_fits(D, static_cast<int>(ng), n) ? Sampler::Grid : Sampler::Steps;
+  return sample_tau_fits(S, static_cast<int>(ng)) ? Sampler::Grid : Sampler::Steps;
 }
 
 // One attempt of the listed rows (gl, ng of them; all rows when gl is null):
@@ -573,11 +534,9 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
                             float* out_vals, int64_t* out_idx, cudaStream_t stream, cudaEvent_t* ev,
                             bool tie_book) {
   RowState* st = at<RowState>(ws, L.off_state);
-  const Sampler form = choose_sampler(L.D, ng, static_cast<uint64_t>(n));
-  const int log2H = L.log2H;
-  const int64_t H = 1ll << log2H;
-  // Reset CTAs per row: about eight 16-byte stores per thread of 256.
-  const unsigned rb = static_cast<unsigned>(std::min<int64_t>(std::max<int64_t>(H / 2 / (256 * 8), 1), 64));
+  const Sampler form = choose_sampler(P.S, ng);
+  // Reset CTAs per row: a few 16-byte stores per thread of 256.
+  constexpr unsigned rb = 8;
   // The refinement's control blocks start every attempt at zero.
   unsigned long long* ref_ctl =
       L.radix_refine ? static_cast<unsigned long long*>(radix_sort_ctl(at<char>(ws, L.off_sort), P.M, rows))
@@ -590,21 +549,19 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
   unsigned* block_eq = tie_book ? reinterpret_cast<unsigned*>(at<char>(ws, L.off_tie) +
                                                               align_up(tie_ctl_bytes() * rows))
                                 : nullptr;
-  launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, at<unsigned long long>(ws, L.off_table), log2H, gl,
-                st, static_cast<unsigned long long>(P.t), ref_ctl, ref_words, at<unsigned long long>(ws, L.off_sctl),
-                static_cast<int>(sample_tau_ctl_bytes() / 8), block_eq, nb);
+  launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, gl, st, static_cast<unsigned long long>(P.t), ref_ctl,
+                ref_words, at<unsigned long long>(ws, L.off_sctl), static_cast<int>(sample_tau_ctl_bytes() / 8),
+                block_eq, nb);
   // Sampling and tau: one persistent kernel (its stage time is reported as
   // the sampling's, the threshold stage then being empty), or, when many rows
   // share the SMs, the step-by-step kernels with the first radix pass of tau
   // fused into the sampler's last one.
-  SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, a, ng, gl, st,
-                at<unsigned long long>(ws, L.off_table), at<uint32_t>(ws, L.off_draws),
-                at<uint32_t>(ws, L.off_blockcnt), at<uint32_t>(ws, L.off_sidx), at<uint32_t>(ws, L.off_skeys), false,
-                static_cast<unsigned long long>(P.t)};
+  SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, seed, a, ng, gl, st, at<uint32_t>(ws, L.off_sidx),
+                at<uint32_t>(ws, L.off_skeys), false, static_cast<unsigned long long>(P.t)};
   sa.wait = wait_cfg_for(PROFK_WAIT_TEST_SAMPLER);
   cudaError_t e = cudaSuccess;
   if (form == Sampler::Grid) {
-    e = launch_sample_tau(sa, at<char>(ws, L.off_sctl), stream);
+    e = launch_sample_tau(sa, at<char>(ws, L.off_sctl), rows, stream);
     if (e != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[1], stream);
   } else {
@@ -801,8 +758,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   c.stream = stream;
   const int64_t launches0 = launch_count();
   const auto wall0 = std::chrono::steady_clock::now();
-  int64_t D = sampling ? draw_budget(n, P.S) : 0;
-  Layout L = make_layout(rows, n, k, P.S, D, P.M, sampling);
+  const Layout L = make_layout(rows, n, k, P.S, P.M, sampling);
   std::vector<int> pending, fallback, attempt(static_cast<size_t>(rows), 0);
   bool exact_ran = false, tie_ran = false, first_filter = true, resume_used = false;
   float filter_ms = -1.f;
@@ -887,7 +843,6 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         first_filter = false;
       }
       std::vector<int> tie, tie_count;  // tie exit rows with the filter's bookkeeping, and without
-      bool grow = false;
       for (int r : group) {
         const char* h = rep + REPORT_BYTES * r;
         unsigned long long Rg = 0, Rt = 0, nanc = 0;
@@ -907,17 +862,9 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
           c.status = (errf & 8u) ? PROFK_ERR_DEVICE_TIMEOUT : PROFK_ERR_CUDA;
           goto done;
         }
-        if (static_cast<int64_t>(distinct) < P.S) {
-          // Fewer than S distinct values among the D draws: the same attempt
-          // runs again with more draws (same stream, so the same sample).
-          if (st_host[r].draw_doublings >= 24) {  // cannot happen for S <= n/2
-            c.status = PROFK_ERR_CUDA;
-            goto done;
-          }
-          st_host[r].draw_doublings += 1;
-          grow = true;
-          next.push_back(r);
-          continue;
+        if (static_cast<int64_t>(distinct) != P.S) {  // the sampler always reports S (a consistency check)
+          c.status = PROFK_ERR_CUDA;
+          goto done;
         }
         profk_stats& s = st_host[r];
         s.attempts = a + 1;
@@ -981,17 +928,6 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
                          at<char>(c.ws, L.off_sort), L.rows, true);
       }
       PK_CHECK(cudaGetLastError());
-      if (grow) {
-        // Grow the draw budget.  Everything enqueued so far uses the old
-        // workspace, whose release is stream-ordered behind it; per-row state
-        // is rebuilt by the next attempt's initialisation.
-        ws_free(c);
-        D *= 2;
-        L = make_layout(rows, n, k, P.S, D, P.M, true);
-        PK_CHECK(ws_alloc(c, L.total, true));
-        st = at<RowState>(c.ws, L.off_state);
-        PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState) * rows, stream));
-      }
     }
     pending = next;
   }
@@ -1152,7 +1088,7 @@ int submit_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
   }
   call->P = P;
   const int64_t launches0 = launch_count();
-  const Layout L = make_layout(rows, n, k, P.S, draw_budget(n, P.S), P.M, true);
+  const Layout L = make_layout(rows, n, k, P.S, P.M, true);
   Call c;
   c.stream = stream;
   cudaError_t e = ws_alloc(c, L.total, false);
@@ -1308,7 +1244,7 @@ namespace {
 size_t layout_bytes(int64_t rows, int64_t n, int64_t k, double eps) {
   const Params P = cached_params(n, k, eps / static_cast<double>(rows), static_cast<int>(g_opt[0].load()));
   const bool sampling = uses_filter(P, n, k, rows);
-  return make_layout(rows, n, k, P.S, sampling ? draw_budget(n, P.S) : 0, P.M, sampling).total;
+  return make_layout(rows, n, k, P.S, P.M, sampling).total;
 }
 }  // namespace
 }  // namespace profk
@@ -1370,55 +1306,40 @@ int profk_last_stage_ms(float* out, int count) {
 
 int profk_sample(const float* x, int64_t n, int64_t S, uint64_t seed, int64_t row, int32_t attempt,
                  int64_t* out_sidx, float* out_vals, cudaStream_t stream) {
-  if (!x || !out_sidx || !out_vals || n < 2 || S < 1 || 2 * S > n || n > (1ll << 32) || row < 0 || attempt < 0)
+  if (!x || !out_sidx || !out_vals || n < 1 || S < 1 || S > n || n > (1ll << 32) || row < 0 || attempt < 0)
     return PROFK_ERR_INVALID;
   Call c;
   c.stream = stream;
-  int64_t D = draw_budget(n, S);
-  Layout L;
+  const Layout L = make_layout(1, n, 1, S, 1, true);
   void* hbuf = nullptr;
-  for (int iter = 0; iter < 40; ++iter) {
-    L = make_layout(1, n, 1, S, D, 1, true);
-    PK_CHECK(ws_alloc(c, L.total));
-    {
-      RowState* st = at<RowState>(c.ws, L.off_state);
-      PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
-      launch_kernel(k_reset_tables, dim3(256, 1), 1024, 0, stream, at<unsigned long long>(c.ws, L.off_table), L.log2H, nullptr);
-      SampleArgs sa{x, n, static_cast<uint64_t>(n), S, D, L.log2H, seed, attempt, 1, nullptr, st,
-                    at<unsigned long long>(c.ws, L.off_table), at<uint32_t>(c.ws, L.off_draws),
-                    at<uint32_t>(c.ws, L.off_blockcnt), at<uint32_t>(c.ws, L.off_sidx),
-                    at<uint32_t>(c.ws, L.off_skeys), false, 1ull, row};
-      // The main path's kernel for one row (it also finds a tau, of rank 1
-      // here, which is not used), else the step-by-step one.
-      const Sampler form = choose_sampler(D, 1, static_cast<uint64_t>(n));
-      if (form == Sampler::Grid) {
-        PK_CHECK(cudaMemsetAsync(at<char>(c.ws, L.off_sctl), 0, sample_tau_ctl_bytes(), stream));
-        PK_CHECK(launch_sample_tau(sa, at<char>(c.ws, L.off_sctl), stream));
-      } else {
-        launch_sample_rows(sa, row, stream);
-      }
-      PK_CHECK(cudaGetLastError());
-      PK_CHECK(pinned(REPORT_BYTES, &hbuf));
-      PK_CHECK(cudaMemcpyAsync(hbuf, st, REPORT_BYTES, cudaMemcpyDeviceToHost, stream));
-      PK_CHECK(cudaStreamSynchronize(stream));
-      unsigned distinct = 0, errf = 0;
-      std::memcpy(&distinct, static_cast<char*>(hbuf) + offsetof(RowState, distinct), 4);
-      std::memcpy(&errf, static_cast<char*>(hbuf) + offsetof(RowState, error), 4);
-      if (errf) {
-        c.status = PROFK_ERR_CUDA;
-        goto done;
-      }
-      if (static_cast<int64_t>(distinct) >= S) {
-        const unsigned b = static_cast<unsigned>(std::min<int64_t>((S + 255) / 256, 1024));
-        launch_kernel(k_sample_out, b, 256, 0, stream, at<uint32_t>(c.ws, L.off_sidx), S, x, out_sidx, out_vals);
-        PK_CHECK(cudaGetLastError());
-        goto done;
-      }
+  PK_CHECK(ws_alloc(c, L.total));
+  {
+    RowState* st = at<RowState>(c.ws, L.off_state);
+    PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState), stream));
+    SampleArgs sa{x, n, static_cast<uint64_t>(n), S, seed, attempt, 1, nullptr, st, at<uint32_t>(c.ws, L.off_sidx),
+                  at<uint32_t>(c.ws, L.off_skeys), false, 1ull, row};
+    // The main path's kernel for one row (it also finds a tau, of rank 1
+    // here, which is not used), else the step-by-step one.
+    if (choose_sampler(S, 1) == Sampler::Grid) {
+      PK_CHECK(cudaMemsetAsync(at<char>(c.ws, L.off_sctl), 0, sample_tau_ctl_bytes(), stream));
+      PK_CHECK(launch_sample_tau(sa, at<char>(c.ws, L.off_sctl), 1, stream));
+    } else {
+      launch_sample_rows(sa, row, stream);
     }
-    ws_free(c);
-    D *= 2;
+    PK_CHECK(cudaGetLastError());
+    PK_CHECK(pinned(REPORT_BYTES, &hbuf));
+    PK_CHECK(cudaMemcpyAsync(hbuf, st, REPORT_BYTES, cudaMemcpyDeviceToHost, stream));
+    PK_CHECK(cudaStreamSynchronize(stream));
+    unsigned errf = 0;
+    std::memcpy(&errf, static_cast<char*>(hbuf) + offsetof(RowState, error), 4);
+    if (errf) {
+      c.status = (errf & 8u) ? PROFK_ERR_DEVICE_TIMEOUT : PROFK_ERR_CUDA;
+      goto done;
+    }
+    const unsigned b = static_cast<unsigned>(std::min<int64_t>((S + 255) / 256, 1024));
+    launch_kernel(k_sample_out, b, 256, 0, stream, at<uint32_t>(c.ws, L.off_sidx), S, x, out_sidx, out_vals);
+    PK_CHECK(cudaGetLastError());
   }
-  c.status = PROFK_ERR_CUDA;
 done:
   ws_free(c);
   return c.status;
@@ -1503,7 +1424,7 @@ int profk_exact(const float* x, int64_t n, int64_t k, float* out_vals, int64_t* 
   if (n > (1ll << 32)) return PROFK_ERR_UNSUPPORTED;
   Call c;
   c.stream = stream;
-  Layout L = make_layout(1, n, k, 0, 0, 0, false);
+  Layout L = make_layout(1, n, k, 0, 0, false);
   void* hbuf = nullptr;
   PK_CHECK(ws_alloc(c, L.total));
   {

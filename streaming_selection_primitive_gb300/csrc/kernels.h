@@ -62,50 +62,50 @@ struct SelectArgs {
   RowState* st;       // per-row state (indexed by row)
 };
 
-// Sampling: draws, first-occurrence marking and ordered compaction.
+// Sampling (sample.cu): the sample of each listed row is pi(0), ..., pi(S-1)
+// for the keyed permutation pi of [0, n) that sample.cu defines (a Feistel
+// network with Philox rounds, cycle-walked into [0, n)), key (seed, storage
+// row + key_row0) and the attempt number.
 struct SampleArgs {
   const float* x;
   int64_t ld;           // row stride of x
-  uint64_t n;           // row length
-  int64_t S;
-  int64_t D;            // draws examined (multiple of 4)
-  int log2H;            // hash table of 2^log2H slots per row
+  uint64_t n;           // row length, at most 2^32
+  int64_t S;            // sample size, 1 <= S <= n
   uint64_t seed;
   int attempt;
   int nrows;
   const int* rows;
   RowState* st;
-  unsigned long long* table;  // rows x 2^log2H, filled with ~0 by the host
-  uint32_t* draws;            // rows x D
-  uint32_t* blockcnt;         // rows x ceil(D / 1024)
-  uint32_t* sidx;             // rows x S (out)
-  uint32_t* skeys;            // rows x S (out)
+  uint32_t* sidx;   // rows x S (out): the indices in sample order
+  uint32_t* skeys;  // rows x S (out): their order keys
   // Optional: the first 11-bit pass of the tau selection (step 2, rank t)
-  // fused into the compaction; the selection state must have been reset
+  // fused into the sampling kernel; the selection state must have been reset
   // (RowState::hist zero, done_blocks 0).  The two remaining passes are
   // launch_select(..., first_pass = 1).
   bool tau_pass1 = false;
   unsigned long long t = 0;
-  // launch_sample_tau: Philox key word 1 = storage row + key_row0.
   int64_t key_row0 = 0;
   WaitCfg wait{};  // launch_sample_tau: test setting of its waits
 };
+// One thread per sample position: indices, keys and RowState::distinct (= S).
 void launch_sample(const SampleArgs& a, cudaStream_t stream);
 // Same, with Philox key word 1 = storage row + key_row0 (a single stored row
-// can then reproduce any row's stream).
+// can then reproduce any row's sample).
 void launch_sample_rows(const SampleArgs& a, int64_t key_row0, cudaStream_t stream);
 // Steps 1 and 2 of the main path in one persistent kernel: the sample (sidx,
-// skeys, RowState::distinct) and tau (RowState::tau_key, rank a.t) of each
-// listed row.  `ctl` holds rows x sample_tau_ctl_bytes(), indexed by row and
-// zero at launch; the hash tables must be empty.  a.draws and a.blockcnt
-// are not used.
+// skeys, RowState::distinct) and tau (RowState::tau_key, tau_copies; rank
+// a.t) of each listed row.  `scratch` holds sample_tau_scratch_bytes(
+// total_rows): first the per-row control blocks (sample_tau_ctl_bytes()
+// each, indexed by row, zero at launch), then candidate lists that need no
+// initialisation.
 size_t sample_tau_ctl_bytes();
-cudaError_t launch_sample_tau(const SampleArgs& a, void* ctl, cudaStream_t stream);
-// Whether launch_sample_tau takes these rows: each CTA's chunk of draws held
-// in registers (up to 1024 draws) or in shared memory (up to 49152, rows
-// shorter than 2^32); otherwise the step-by-step kernels (launch_sample with
+size_t sample_tau_scratch_bytes(int64_t rows);
+cudaError_t launch_sample_tau(const SampleArgs& a, void* scratch, int64_t total_rows, cudaStream_t stream);
+// Whether launch_sample_tau takes these rows: each CTA's chunk of the sample
+// (S split over the row's share of the SMs) held in registers, at most 1024
+// positions; otherwise the step-by-step kernels (launch_sample with
 // tau_pass1, then launch_select).
-bool sample_tau_fits(int64_t D, int nrows, uint64_t n);
+bool sample_tau_fits(int64_t S, int nrows);
 
 // Exact top-k of short rows, one CTA per row (rows.cu): outputs of each listed
 // row (or rows 0 .. nrows-1) sorted, RowState::sel_nan set to the row's NaN

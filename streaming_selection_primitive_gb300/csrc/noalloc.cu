@@ -11,8 +11,7 @@
 // The scratch is one file-scope device array of PROFK_NOALLOC_SCRATCH_BYTES.
 // Every GPU that loads the library holds it until the process exits.  All
 // calls share it, and it keeps whatever the previous call left there, so each
-// call clears what must start at zero (per-row counters, the sampler's hash
-// table).  Two calls whose GPU work overlaps (different streams, or different
+// call clears what must start at zero (the row's counters).  Two calls whose GPU work overlaps (different streams, or different
 // host threads, on the same device) race on the array and give wrong results:
 // order them on one stream or serialize them.
 //
@@ -57,26 +56,15 @@ size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 // Single-row layout inside the scratch array.
 struct ScratchLayout {
-  int64_t D = 0, kstride = 0;
-  int log2H = 0;
-  size_t off_table = 0, off_draws = 0, off_blockcnt = 0, off_sidx = 0, off_skeys = 0, off_buf = 0, off_sel = 0,
-         total = 0;
+  int64_t kstride = 0;
+  size_t off_sidx = 0, off_skeys = 0, off_buf = 0, off_sel = 0, total = 0;
 };
 
-ScratchLayout plan(int64_t S, int64_t D, int64_t M, int64_t k, bool sampling) {
+ScratchLayout plan(int64_t S, int64_t M, int64_t k, bool sampling) {
   ScratchLayout L;
-  L.D = D;
   L.kstride = sort_stride(k);
   size_t off = up256(sizeof(RowState));
   if (sampling) {
-    L.log2H = 1;
-    while ((1ll << L.log2H) < 2 * D) ++L.log2H;
-    L.off_table = off;
-    off = up256(off + sizeof(unsigned long long) * (static_cast<size_t>(1) << L.log2H));
-    L.off_draws = off;
-    off = up256(off + sizeof(uint32_t) * D);
-    L.off_blockcnt = off;
-    off = up256(off + sizeof(uint32_t) * ((D + 1023) / 1024));
     L.off_sidx = off;
     off = up256(off + sizeof(uint32_t) * S);
     L.off_skeys = off;
@@ -88,12 +76,6 @@ ScratchLayout plan(int64_t S, int64_t D, int64_t M, int64_t k, bool sampling) {
   off = up256(off + sizeof(unsigned long long) * L.kstride);
   L.total = off;
   return L;
-}
-
-int64_t draws_for(int64_t n, int64_t S) {
-  const double rep = static_cast<double>(S) * static_cast<double>(S) / (2.0 * static_cast<double>(n));
-  const int64_t D = S + static_cast<int64_t>(2.0 * rep + 8.0 * std::sqrt(rep) + 256.0);
-  return (D + 3) & ~3ll;
 }
 
 template <class T>
@@ -118,8 +100,7 @@ extern "C" int profk_topk_noalloc(const float* x, int64_t n, int64_t k, double e
   const bool tie_exit = profk_get_option(PROFK_OPT_TIE_EXIT) != 0;
   const Params P = compute_params(n, k, eps, mode);
   const bool sampling = uses_filter(P, n, k);
-  int64_t D = sampling ? draws_for(n, P.S) : 0;
-  ScratchLayout L = plan(P.S, D, P.M, k, sampling);
+  const ScratchLayout L = plan(P.S, P.M, k, sampling);
   if (L.total > PROFK_NOALLOC_SCRATCH_BYTES) return PROFK_ERR_SCRATCH;
 
   profk_stats s;
@@ -171,16 +152,12 @@ extern "C" int profk_topk_noalloc(const float* x, int64_t n, int64_t k, double e
   // Steps 1-4 per attempt; redraws with attempt + 1, up to max_attempts.
   for (int64_t a = 0; status == PROFK_OK && sampling && !ended && a < max_attempts;) {
     err = cudaMemsetAsync(st, 0, sizeof(RowState), stream);
-    if (err == cudaSuccess)
-      err = cudaMemsetAsync(in<void>(base, L.off_table), 0xff,
-                            sizeof(unsigned long long) * (static_cast<size_t>(1) << L.log2H), stream);
     if (err != cudaSuccess) {
       status = PROFK_ERR_CUDA;
       break;
     }
-    SampleArgs sa{x, n, static_cast<uint64_t>(n), P.S, L.D, L.log2H, seed, static_cast<int>(a), 1, nullptr, st,
-                  in<unsigned long long>(base, L.off_table), in<uint32_t>(base, L.off_draws),
-                  in<uint32_t>(base, L.off_blockcnt), in<uint32_t>(base, L.off_sidx), in<uint32_t>(base, L.off_skeys)};
+    SampleArgs sa{x, n, static_cast<uint64_t>(n), P.S, seed, static_cast<int>(a), 1, nullptr, st,
+                  in<uint32_t>(base, L.off_sidx), in<uint32_t>(base, L.off_skeys)};
     launch_sample(sa, stream);
     SelectArgs ta{KeySource::SampleKeys, in<uint32_t>(base, L.off_skeys), P.S, P.S, 1, nullptr, st};
     launch_select(ta, static_cast<uint64_t>(P.t), true, 0, stream);
@@ -203,16 +180,9 @@ extern "C" int profk_topk_noalloc(const float* x, int64_t n, int64_t k, double e
       status = error_status(errf);
       break;
     }
-    if (static_cast<int64_t>(word(offsetof(RowState, distinct))) < P.S) {  // more draws, same attempt
-      if (s.draw_doublings >= 24) {  // cannot happen for S <= n/2
-        status = PROFK_ERR_CUDA;
-        break;
-      }
-      s.draw_doublings += 1;
-      D *= 2;
-      L = plan(P.S, D, P.M, k, true);
-      if (L.total > PROFK_NOALLOC_SCRATCH_BYTES) status = PROFK_ERR_SCRATCH;
-      continue;
+    if (static_cast<int64_t>(word(offsetof(RowState, distinct))) != P.S) {  // always S (a consistency check)
+      status = PROFK_ERR_CUDA;
+      break;
     }
     s.attempts = static_cast<int32_t>(a + 1);
     const float tau = key_to_float(word(offsetof(RowState, tau_key)));

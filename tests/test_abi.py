@@ -91,7 +91,7 @@ def test_invalid_arguments_are_rejected_before_any_device_work(pk):
     assert lib.profk_topk_batched(fake, 2, 10, 9, 1, 1e-3, 0, fake, fake, None, None) == -1
     # x must be a float pointer (4-byte aligned); any row stride ld >= n is taken.
     assert lib.profk_topk_batched(C.c_void_p(258), 2, 10, 10, 1, 1e-3, 0, fake, fake, None, None) == -4
-    assert lib.profk_sample(fake, 10, 6, 0, 0, 0, fake, fake, None) == -1
+    assert lib.profk_sample(fake, 10, 11, 0, 0, 0, fake, fake, None) == -1  # S > n
     assert lib.profk_threshold(fake, 10, 11, fake, None) == -1
     assert lib.profk_refine(fake, 5, 6, fake, 10, fake, fake, None) == -1
     assert lib.profk_exact(fake, 10, 11, fake, fake, None) == -1

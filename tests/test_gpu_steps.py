@@ -17,12 +17,15 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("n,S,seed,row,attempt", [
     (1 << 22, 32768, 1, 0, 0), (1 << 22, 32768, 2, 5, 3), (1000003, 4099, 77, 1, 0), (64, 32, 9, 0, 0),
-    (1 << 30, 105985, 3, 0, 0), (3 * (1 << 20) + 17, 131072, 4, 2, 1),
-    # more than 1024 draws per CTA (the draws held in shared memory), many repeats
-    (1 << 24, 400_000, 5, 3, 2), (1 << 20, 1 << 19, 6, 0, 0), ((1 << 21) + 5, 300_001, 7, 1, 4)])
+    (1 << 30, 105985, 3, 0, 0), (3 * (1 << 20) + 17, 131072, 4, 2, 1), (50331648, 131072, 8, 0, 0),
+    # more than 1024 positions per CTA of the persistent form: the step-by-step kernel
+    (1 << 24, 400_000, 5, 3, 2), (1 << 20, 1 << 19, 6, 0, 0), ((1 << 21) + 5, 300_001, 7, 1, 4),
+    # the whole row (a permutation of it), tiny rows, and rows of one element
+    (5000, 5000, 10, 0, 0), (3, 2, 11, 1, 1), (1, 1, 12, 0, 0), ((1 << 32) - 5, 1000, 13, 0, 0)])
 @pytest.mark.parametrize("form", ["auto", "steps"])
 def test_sample_matches_oracle(pk, cuda_device, n, S, seed, row, attempt, form):
-    """Both kernel forms draw the same sample."""
+    """Both kernel forms draw the oracle's sample, index by index in order
+    (rows off the power-of-two grid walk the permutation's cycles)."""
     pk.set_option(pk.OPT_SAMPLER, {"auto": pk.SAMPLER_AUTO, "steps": pk.SAMPLER_STEPS}[form])
     x = workloads.uniform(n, seed, cuda_device)
     sidx, svals = pk.sample(x, S, seed, row, attempt)
