@@ -24,12 +24,13 @@
 //    finishes);
 //  * k_sample_tau (the main path, one 512-thread CTA per SM and contiguous
 //    chunk of at most 1024 sample positions, all CTAs of the launch resident
-//    together): the sample, then tau.  For t <= TAU_CAND every CTA selects
-//    its own t largest keys in shared memory and lists them; one CTA waits
-//    for every list (a bounded wait) and selects tau among them: the t-th
-//    largest of the sample is among the t largest of its own chunk.  For
-//    larger t, 11/11/10-bit MSD passes whose chunk histograms meet in global
-//    atomics, every CTA taking the same digit after each pass's barrier.
+//    together): the sample, then tau.  For t <= TAU_CAND (8) every CTA
+//    selects its own t largest keys (rounds of block maxima) and lists them;
+//    one CTA waits for every list (a bounded wait) and selects tau among
+//    them: the t-th largest of the sample is among the t largest of its own
+//    chunk.  For larger t, 11/11/10-bit MSD passes whose chunk histograms
+//    meet in global atomics, every CTA taking the same digit after each
+//    pass's barrier.
 #include "kernels.h"
 
 namespace profk {
@@ -40,7 +41,12 @@ constexpr int WALK_MAX = 1024;       // cycle-walking steps (each ends below n w
 constexpr int DRAW_THREADS = 1024;   // k_sample_draw
 constexpr int ST_THREADS = 512;      // k_sample_tau
 constexpr int ST_HELD = 2;           // sample positions per thread (keys kept in registers)
-constexpr int TAU_CAND = 128;        // largest t of the candidate-list selection
+// Largest t of the candidate-list selection (whose selections take rounds of
+// maxima).  For larger t the grid passes measured faster: at t = 93 the
+// candidate lists held G t ~ 12K keys for one CTA to select among (2^30,
+// k = 2^19: sampling stage 36.5 us against 23.5 us with the passes).
+constexpr int TAU_CAND = 8;
+constexpr int SMALL_T = TAU_CAND;
 constexpr int TAU_GATHER = ST_THREADS;  // a tau bucket this small is finished by one CTA (t > TAU_CAND)
 constexpr int MAX_CHUNKS = 256;
 
@@ -281,78 +287,60 @@ __device__ __forceinline__ void st_grid_sync(SampleCtl& c, unsigned target, int*
     return;                                     \
   }
 
-// Shared memory of the block selection below.
+// Shared memory of the selections (the passes of the t > TAU_CAND path, and
+// the rounds of maxima below).
 struct SelSmem {
   unsigned h[HIST_BINS];
   unsigned long long sw[33];
   unsigned digit;
   unsigned long long above, count;
+  unsigned wmax[ST_THREADS / 32], wcnt[ST_THREADS / 32];
 };
 
 // The want-th largest of the keys that each_key(fn) presents (fn(key,
-// valid), called the same number of times on every thread of the block):
-// three 11/11/10-bit MSD passes over shared-memory histograms.  Returns the
-// key; *above = keys strictly larger, *eq = keys equal to it.
+// valid), called the same number of times on every thread), for a small
+// want: rounds of "the largest key below the previous round's, and its
+// copies", a block maximum and a block count each, until the copies reach
+// the rank left (at most want rounds).  Returns the key; *above = keys
+// strictly larger, *eq = keys equal to it.  The block must hold at least
+// want valid keys.
 template <class EachKey>
-__device__ __forceinline__ uint32_t block_select(EachKey each_key, unsigned long long want, SelSmem& sm,
-                                                 unsigned long long* above, unsigned long long* eq) {
-  const int tid = threadIdx.x;
+__device__ __forceinline__ uint32_t block_select_small(EachKey each_key, unsigned long long want, SelSmem& sm,
+                                                       unsigned long long* above, unsigned long long* eq) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const unsigned long long want0 = want;
-  unsigned long long prefix = 0;
-  int bits = 0;
-#pragma unroll 1
-  for (int p = 0; p < 3; ++p) {
-    const int width = p == 2 ? 10 : 11;
-    const int shift = 32 - 11 * (p + 1) + (p == 2 ? 1 : 0);  // 21, 10, 0
-    const unsigned nb = 1u << width;
-    for (unsigned b = tid; b < nb; b += ST_THREADS) sm.h[b] = 0;
-    if (tid == 0) {
-      sm.digit = 0;
-      sm.above = 0;
-      sm.count = 0;
-    }
-    __syncthreads();
-    each_key([&](uint32_t key, bool valid) {
-      const bool m = valid && (bits == 0 || (static_cast<unsigned long long>(key) >> (shift + width)) == prefix);
-      hist_add(sm.h, (key >> shift) & (nb - 1), m);
+  uint32_t bound = 0xffffffffu;  // keys at or above it are taken (all keys remain in the first round)
+  bool first = true;
+  uint32_t result = 0;
+  for (int r = 0; r < SMALL_T; ++r) {
+    uint32_t m = 0;
+    each_key([&](uint32_t key, bool v) {
+      if (v && (first || key < bound) && key > m) m = key;
     });
+    m = __reduce_max_sync(FULL_MASK, m);
+    if (lane == 0) sm.wmax[warp] = m;
     __syncthreads();
-    // Bins counted down from the top: thread t owns nb / ST_THREADS of them.
-    const int per = static_cast<int>(nb) / ST_THREADS;
-    const int top = static_cast<int>(nb) - 1 - tid * per;
-    unsigned hv[4] = {0u, 0u, 0u, 0u};
-    unsigned long long local = 0;
+    m = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (q < per) {
-        hv[q] = sm.h[top - q];
-        local += hv[q];
-      }
-    }
-    unsigned long long tot;
-    const unsigned long long excl = excl_scan_block<ST_THREADS>(local, sm.sw, &tot);
-    if (excl < want && want <= excl + local) {
-      unsigned long long acc = excl;
+    for (int w = 0; w < ST_THREADS / 32; ++w) m = sm.wmax[w] > m ? sm.wmax[w] : m;
+    unsigned c = 0;
+    each_key([&](uint32_t key, bool v) { c += (v && (first || key < bound) && key == m) ? 1u : 0u; });
+    c = __reduce_add_sync(FULL_MASK, c);
+    if (lane == 0) sm.wcnt[warp] = c;
+    __syncthreads();
+    unsigned long long cnt = 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (q < per && want <= acc + hv[q]) {
-          sm.digit = static_cast<unsigned>(top - q);
-          sm.above = acc;
-          sm.count = hv[q];
-          break;
-        }
-        acc += hv[q];
-      }
-    }
-    __syncthreads();
-    prefix = (prefix << width) | sm.digit;
-    want -= sm.above;
-    bits += width;
-    *eq = sm.count;  // after the last pass: the keys equal to the result
-    __syncthreads();
+    for (int w = 0; w < ST_THREADS / 32; ++w) cnt += sm.wcnt[w];
+    __syncthreads();  // wmax and wcnt are rewritten by the next round
+    result = m;
+    *eq = cnt;
+    if (cnt >= want) break;
+    want -= cnt;
+    bound = m;
+    first = false;
   }
   *above = want0 - want;
-  return static_cast<uint32_t>(prefix);
+  return result;
 }
 
 template <bool CAND>
@@ -422,7 +410,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     uint32_t K = 0;
     unsigned long long above = 0, eq = 0;
     if (!short_chunk)
-      K = block_select(each_key, t, sm, &above, &eq);
+      K = block_select_small(each_key, t, sm, &above, &eq);
     else
       above = static_cast<unsigned long long>(cnt);  // every key goes to the list
     uint32_t* mine = cd.key + chunk * static_cast<int64_t>(t);
@@ -471,7 +459,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
       }
     };
     unsigned long long cabove = 0, ceq = 0;
-    const uint32_t tau = block_select(each_cand, t, sm, &cabove, &ceq);
+    const uint32_t tau = block_select_small(each_cand, t, sm, &cabove, &ceq);
     unsigned long long more = 0;
     for (int64_t ch = tid; ch < G; ch += ST_THREADS)
       if (__ldcg(&cd.kth[ch]) == tau) more += __ldcg(&cd.extra[ch]);
@@ -640,9 +628,7 @@ cudaError_t launch_sample_tau(const SampleArgs& a, void* scratch, int64_t total_
       reinterpret_cast<SampleCand*>(static_cast<char*>(scratch) + align256(sizeof(SampleCtl) * total_rows));
   const dim3 grid(static_cast<unsigned>(G), static_cast<unsigned>(a.nrows));
   if (a.t <= static_cast<unsigned long long>(TAU_CAND)) {
-    const size_t smem = sizeof(uint32_t) * static_cast<size_t>(G) * a.t;  // at most 128 KB
-    cudaFuncSetAttribute(k_sample_tau<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(sizeof(uint32_t) * MAX_CHUNKS * TAU_CAND));
+    const size_t smem = sizeof(uint32_t) * static_cast<size_t>(G) * a.t;  // at most 8 KB
     launch_kernel(k_sample_tau<true>, grid, ST_THREADS, smem, stream, a, ctl, cand);
   } else
     launch_kernel(k_sample_tau<false>, grid, ST_THREADS, 0, stream, a, ctl, cand);

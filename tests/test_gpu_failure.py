@@ -22,8 +22,9 @@ pytestmark = pytest.mark.gpu
 SENTINEL_V, SENTINEL_I = 12345.0, -7
 
 
-@pytest.mark.parametrize("which,n,k", [("sampler", 1 << 24, 1024), ("refine", 1 << 24, 1024),
-                                       ("sort", 1 << 24, 1 << 15)])
+@pytest.mark.parametrize("which,n,k", [("sampler", 1 << 24, 32),       # t = 3: the candidate lists' wait
+                                       ("sampler", 1 << 24, 1024),     # t = 9: the passes' grid barriers
+                                       ("refine", 1 << 24, 1024), ("sort", 1 << 24, 1 << 15)])
 @pytest.mark.parametrize("api", ["sync", "async"])
 def test_wait_that_runs_out_is_reported(pk, cuda_device, which, n, k, api):
     x = workloads.normal(n, 7, cuda_device)
