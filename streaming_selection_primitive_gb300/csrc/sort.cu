@@ -75,6 +75,7 @@ constexpr int RS_KMAX = 8;                                       // keys per thr
 constexpr int RS_SUB = RS_THREADS * RS_KMAX;                     // 8192 keys ranked at a time
 constexpr size_t RS_SMEM = sizeof(unsigned long long) * RS_SUB;  // staging of a piece (64 KB)
 constexpr int RUN_MAX = 256;   // runs up to this long are ordered by a warp
+constexpr int HI_POS = 5;      // step 1 counts byte positions HI_POS..7 (the value's top three bytes)
 constexpr int BK_BITS = 14;
 constexpr int BK = 1 << BK_BITS;           // buckets of the bucket stage
 constexpr unsigned BK_CAP = 4096;          // largest bucket the stage takes
@@ -399,6 +400,45 @@ __device__ __forceinline__ void radix_pass(const RadixSortArgs& a, int row, int6
   }
 }
 
+// The plan of byte positions [plo, phi), the same in every CTA: the row's
+// digit counts of each position (c.start, complete) into the start of each
+// digit (an exclusive scan), whether the position is the same in every key
+// (trivial), and how many digits occur (distinct).
+__device__ __forceinline__ void plan_positions(SortCtl& c, Smem& sm, int64_t len, int plo, int phi) {
+  for (int i = plo * 256 + threadIdx.x; i < phi * 256; i += RS_THREADS) {
+    const unsigned long long v = __ldcg(&c.start[0][0] + i);
+    (&sm.start[0][0])[i] = v;
+    if (static_cast<int64_t>(v) == len) sm.trivial[i >> 8] = 1;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pos = plo + warp;
+  if (pos < phi) {  // exclusive scan of position `pos`, 8 digits per lane
+    unsigned long long v[8], s = 0;
+    unsigned present = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = sm.start[pos][lane * 8 + j];
+      s += v[j];
+      present += v[j] != 0;
+    }
+    for (int o = 16; o >= 1; o >>= 1) present += __shfl_xor_sync(FULL_MASK, present, o);
+    if (lane == 0) sm.distinct[pos] = present;
+    unsigned long long incl = s;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += t;
+    }
+    unsigned long long run = incl - s;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sm.start[pos][lane * 8 + j] = run;
+      run += v[j];
+    }
+  }
+  __syncthreads();
+}
+
 // First position of the bucket starts st[0..BK) (nondecreasing) at or after
 // pos: the start of the first bucket beginning there, or len.
 __device__ __forceinline__ int64_t bucket_at(const unsigned* st, int64_t pos, int64_t len) {
@@ -694,8 +734,12 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
 
   unsigned* bkr = bk + static_cast<int64_t>(row) * 2 * BK;  // bucket counts, then cursors
 
-  // 1. Histograms of all positions (and this chunk's flags and share of the
-  // bucket counters zeroed).
+  // 1. Histograms of the value positions HI_POS..7 (and this chunk's flags
+  // and share of the bucket counters zeroed).  The other positions are
+  // counted later, only when the bucket stage cannot take the row (all keys
+  // share the top HI_POS bytes' values, or a bucket is too large): their
+  // digits are mostly the index bits, whose 256 bins are all populated in
+  // every chunk, and their global atomics cost more than the rest of step 1.
   {
     unsigned(*h)[256] = reinterpret_cast<unsigned(*)[256]>(s_keys);
     for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS) (&h[0][0])[i] = 0;
@@ -722,7 +766,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
         if (r * RS_THREADS >= cnt) break;  // uniform across the block
         const bool valid = j < cnt;
 #pragma unroll
-        for (int p = 0; p < 8; ++p) hist_add(h[p], digit_of(kv[r], p), valid);
+        for (int p = HI_POS; p < 8; ++p) hist_add(h[p], digit_of(kv[r], p), valid);
         if (valid) {
           kmx = kv[r] > kmx ? kv[r] : kmx;
           nkmx = ~kv[r] > nkmx ? ~kv[r] : nkmx;
@@ -745,57 +789,59 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
       atomicMax(&c.kmax, sm.kmax);
       atomicMax(&c.nkmax, sm.nkmax);
     }
-    for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS)
+    for (int i = HI_POS * 256 + threadIdx.x; i < 8 * 256; i += RS_THREADS)
       if ((&h[0][0])[i]) atomicAdd(&c.start[0][0] + i, static_cast<unsigned long long>((&h[0][0])[i]));
   }
   grid_sync(c, (target += G) + a.wait.skew, sm);
   RS_LEAVE_IF_GAVE_UP();
   // The plan, the same in every CTA.
-  if (threadIdx.x < 8) sm.trivial[threadIdx.x] = 0;
+  if (threadIdx.x < 8) sm.trivial[threadIdx.x] = 0;  // unknown positions count as varying
   if (threadIdx.x == 0) {
     sm.kmax = __ldcg(&c.kmax);
     sm.nkmax = __ldcg(&c.nkmax);
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 8 * 256; i += RS_THREADS) {
-    const unsigned long long v = __ldcg(&c.start[0][0] + i);
-    (&sm.start[0][0])[i] = v;
-    if (static_cast<int64_t>(v) == len) sm.trivial[i >> 8] = 1;
-  }
-  __syncthreads();
-  {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp < 8) {  // exclusive scan of position `warp`, 8 digits per lane
-      unsigned long long v[8], s = 0;
-      unsigned present = 0;
+  plan_positions(c, sm, len, HI_POS, 8);
+  // Positions 0 .. HI_POS-1 counted (a pass over the chunk, its atomics and
+  // one more barrier) and planned: for the bucket stage when the keys share
+  // the values of the top positions, and for the passes.
+  bool low_planned = false;
+  auto plan_low = [&]() {
+    unsigned(*h)[256] = reinterpret_cast<unsigned(*)[256]>(s_keys);
+    for (int i = threadIdx.x; i < HI_POS * 256; i += RS_THREADS) (&h[0][0])[i] = 0;
+    __syncthreads();
+    const unsigned long long* cst = s_keys + 2 * RS_SUB;  // the chunk, when step 1 kept it
+    const bool staged = hi - lo <= RS_SUB;
+    for (int64_t b0 = lo; b0 < hi; b0 += RS_THREADS) {
+      const int64_t i = b0 + threadIdx.x;
+      const bool valid = i < hi;
+      const unsigned long long kk = valid ? (staged ? cst[i - lo] : __ldcg(a.keys + row * a.key_stride + i)) : 0ull;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        v[j] = sm.start[warp][lane * 8 + j];
-        s += v[j];
-        present += v[j] != 0;
-      }
-      for (int o = 16; o >= 1; o >>= 1) present += __shfl_xor_sync(FULL_MASK, present, o);
-      if (lane == 0) sm.distinct[warp] = present;
-      unsigned long long incl = s;
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long t = __shfl_up_sync(FULL_MASK, incl, o);
-        if (lane >= o) incl += t;
-      }
-      unsigned long long run = incl - s;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        sm.start[warp][lane * 8 + j] = run;
-        run += v[j];
-      }
+      for (int q = 0; q < HI_POS; ++q) hist_add(h[q], digit_of(kk, q), valid);
     }
+    __syncthreads();
+    for (int i = threadIdx.x; i < HI_POS * 256; i += RS_THREADS)
+      if ((&h[0][0])[i]) atomicAdd(&c.start[0][0] + i, static_cast<unsigned long long>((&h[0][0])[i]));
+    grid_sync(c, target += G, sm);
+    if (!sm.err) plan_positions(c, sm, len, 0, HI_POS);
+    low_planned = true;
+  };
+  bool top_varies = false;
+  for (int q = HI_POS; q < 8; ++q) top_varies |= !sm.trivial[q];
+  if (!top_varies) {
+    plan_low();
+    RS_LEAVE_IF_GAVE_UP();
   }
-  __syncthreads();
 
   if (len >= BK_MIN_LEN && len < (int64_t(1) << 31) &&
       bucket_stage(a, row, len, lo, hi, c, target, bkr, tmp + row * a.key_stride, sm, s_keys)) {
     __syncthreads();
     RS_LEAVE_IF_GAVE_UP();
     return;
+  }
+  if (!low_planned) {
+    plan_low();
+    RS_LEAVE_IF_GAVE_UP();
   }
 
   // When the value bytes allow fewer than len / RUN_MAX distinct values,
