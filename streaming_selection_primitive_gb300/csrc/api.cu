@@ -549,9 +549,13 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
   unsigned* block_eq = tie_book ? reinterpret_cast<unsigned*>(at<char>(ws, L.off_tie) +
                                                               align_up(tie_ctl_bytes() * rows))
                                 : nullptr;
-  launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, gl, st, static_cast<unsigned long long>(P.t), ref_ctl,
-                ref_words, at<unsigned long long>(ws, L.off_sctl), static_cast<int>(sample_tau_ctl_bytes() / 8),
-                block_eq, nb);
+  // The grid sampler with the candidate lists (small t) does the attempt's
+  // set-up itself; the other forms get the reset kernel first.
+  const bool fused_setup = form == Sampler::Grid && P.t <= sample_tau_setup_max_t();
+  if (!fused_setup)
+    launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, gl, st, static_cast<unsigned long long>(P.t), ref_ctl,
+                  ref_words, at<unsigned long long>(ws, L.off_sctl), static_cast<int>(sample_tau_ctl_bytes() / 8),
+                  block_eq, nb);
   // Sampling and tau: one persistent kernel (its stage time is reported as
   // the sampling's, the threshold stage then being empty), or, when many rows
   // share the SMs, the step-by-step kernels with the first radix pass of tau
@@ -559,6 +563,12 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
   SampleArgs sa{x, ld, static_cast<uint64_t>(n), P.S, seed, a, ng, gl, st, at<uint32_t>(ws, L.off_sidx),
                 at<uint32_t>(ws, L.off_skeys), false, static_cast<unsigned long long>(P.t)};
   sa.wait = wait_cfg_for(PROFK_WAIT_TEST_SAMPLER);
+  if (fused_setup) {
+    sa.zero_ctl = ref_ctl;
+    sa.zero_words = ref_words;
+    sa.zero_eq = block_eq;
+    sa.zero_nb = nb;
+  }
   cudaError_t e = cudaSuccess;
   if (form == Sampler::Grid) {
     e = launch_sample_tau(sa, at<char>(ws, L.off_sctl), rows, stream);

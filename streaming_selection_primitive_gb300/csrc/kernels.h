@@ -86,6 +86,15 @@ struct SampleArgs {
   unsigned long long t = 0;
   int64_t key_row0 = 0;
   WaitCfg wait{};  // launch_sample_tau: test setting of its waits
+  // launch_sample_tau for t <= sample_tau_setup_max_t(): the attempt's set-up
+  // done by the sampler itself, in place of a reset kernel: the row state
+  // (counters, error word, selection state, histogram), the refinement's
+  // control block (zero_words 8-byte words per row, an even number) and
+  // the tie step's block counts (zero_nb per row) are zeroed.
+  unsigned long long* zero_ctl = nullptr;
+  int zero_words = 0;
+  unsigned* zero_eq = nullptr;
+  int64_t zero_nb = 0;
 };
 // One thread per sample position: indices, keys and RowState::distinct (= S).
 void launch_sample(const SampleArgs& a, cudaStream_t stream);
@@ -106,6 +115,9 @@ cudaError_t launch_sample_tau(const SampleArgs& a, void* scratch, int64_t total_
 // positions; otherwise the step-by-step kernels (launch_sample with
 // tau_pass1, then launch_select).
 bool sample_tau_fits(int64_t S, int nrows);
+// Largest t for which launch_sample_tau also does the attempt's set-up (and
+// needs no zeroed control block of its own).
+int64_t sample_tau_setup_max_t();
 
 // Exact top-k of short rows, one CTA per row (rows.cu): outputs of each listed
 // row (or rows 0 .. nrows-1) sorted, RowState::sel_nan set to the row's NaN

@@ -31,6 +31,11 @@
 //    chunk.  For larger t, 11/11/10-bit MSD passes whose chunk histograms
 //    meet in global atomics, every CTA taking the same digit after each
 //    pass's barrier.
+#include <atomic>
+#include <chrono>
+
+#include <unistd.h>
+
 #include "kernels.h"
 
 namespace profk {
@@ -257,11 +262,16 @@ static_assert(sizeof(SampleCtl) % 16 == 0, "SampleCtl is zeroed with 16-byte sto
 
 // Per-row candidate lists of the selection for t <= TAU_CAND (written whole
 // by every launch, so not zeroed): chunk c's t largest keys at key[c t ..],
-// and its t-th largest key with the number of its copies the list leaves out.
+// its t-th largest key with the number of its copies the list leaves out,
+// and its flag: (epoch << 1) | (a walk of the chunk did not end), written
+// once the list is complete.  The launch's epoch is unique to it (a process
+// nonce and a launch counter), so a flag left by an earlier launch, or any
+// other content of fresh memory, does not read as written.
 struct SampleCand {
   uint32_t key[MAX_CHUNKS * TAU_CAND];
   uint32_t kth[MAX_CHUNKS];
   uint32_t extra[MAX_CHUNKS];
+  unsigned long long flag[MAX_CHUNKS];
 };
 
 namespace {
@@ -344,26 +354,61 @@ __device__ __forceinline__ uint32_t block_select_small(EachKey each_key, unsigne
 }
 
 template <bool CAND>
-__global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, SampleCtl* ctl, SampleCand* cands) {
+__global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, SampleCtl* ctl, SampleCand* cands,
+                                                             unsigned long long epoch) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ uint32_t s_cand[];  // CAND: the G t candidates, in the first CTA
   __shared__ SelSmem sm;
-  __shared__ int s_err;
+  __shared__ int s_err, s_fail;
   __shared__ unsigned s_pos;
   __shared__ uint64_t s_keys[FEISTEL_ROUNDS];
   const int row = launch_row(a.rows);
   RowState& S = a.st[row];
   SampleCtl& c = ctl[row];
   const int tid = threadIdx.x;
+  const int64_t G = gridDim.x, chunk = blockIdx.x;
   if (tid == 0) {
     s_err = 0;
+    s_fail = 0;
     s_pos = 0;
+  }
+  if constexpr (CAND) {
+    // The attempt's set-up (see SampleArgs::zero_ctl): the first CTA the row
+    // state, every CTA its share of the refinement's control block and of
+    // the tie step's block counts.  The kernels that use them come later on
+    // the stream.
+    const int64_t gt = chunk * ST_THREADS + tid, gs = G * ST_THREADS;
+    if (a.zero_ctl) {
+      ulonglong2* zc = reinterpret_cast<ulonglong2*>(a.zero_ctl + static_cast<int64_t>(row) * a.zero_words);
+      for (int64_t i = gt; i < a.zero_words / 2; i += gs) zc[i] = make_ulonglong2(0ull, 0ull);
+    }
+    if (a.zero_eq) {
+      unsigned* ze = a.zero_eq + static_cast<int64_t>(row) * a.zero_nb;
+      for (int64_t i = gt; i < a.zero_nb; i += gs) ze[i] = 0u;
+    }
+    if (chunk == 0) {
+      for (int b = tid; b < HIST_BINS; b += ST_THREADS) S.hist[b] = 0u;
+      if (tid == 0) {
+        S.R_ge = 0;
+        S.R_gt = 0;
+        S.nan = 0;
+        S.error = 0;
+        S.sel_rank = a.t;
+        S.sel_above = 0;
+        S.sel_bucket = 0;
+        S.sel_thresh = 0;
+        S.sel_nan = 0;
+        S.done_blocks = 0;
+        S.compact_count = 0;
+        S.skip = 0;
+        S.tie_gt = 0;
+      }
+    }
   }
   round_keys(a.seed, static_cast<uint64_t>(row + a.key_row0), static_cast<uint64_t>(a.attempt), s_keys);
   __syncthreads();
   const int limit = wait_limit(a.wait);
-  const int64_t G = gridDim.x, chunk = blockIdx.x;
   const int64_t Cn = (((a.S + G - 1) / G) + 31) & ~int64_t(31);
   const int64_t lo = chunk * Cn < a.S ? chunk * Cn : a.S;
   const int64_t hi = lo + Cn < a.S ? lo + Cn : a.S;
@@ -379,7 +424,12 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     xs[h] = static_cast<uint64_t>(j);
     walk[h] = mh[h] = j < hi;
   }
-  if (!permute<ST_HELD>(xs, walk, a.n, domain_bits(a.n), s_keys)) atomicOr(&S.error, 1u);
+  if (!permute<ST_HELD>(xs, walk, a.n, domain_bits(a.n), s_keys)) {
+    if constexpr (CAND)
+      s_fail = 1;  // reported through the chunk's flag (the first CTA owns the error word)
+    else
+      atomicOr(&S.error, 1u);
+  }
   float vh[ST_HELD];
 #pragma unroll
   for (int h = 0; h < ST_HELD; ++h) vh[h] = mh[h] ? xr[xs[h]] : 0.f;  // the gathers, in flight together
@@ -424,15 +474,33 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
       cd.extra[chunk] = short_chunk ? 0u : static_cast<unsigned>(eq - (t - above));
     }
     __syncthreads();
-    if (tid == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&c.bar) : "memory");
+    if (tid == 0) {
+      const unsigned long long f = (epoch << 1) | (s_fail ? 1ull : 0ull);
+      asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(&cd.flag[chunk]), "l"(f) : "memory");
+    }
     if (chunk != 0) return;
-    // c. The first CTA waits for every list, then selects tau among the
-    // G t candidates.  The copies of tau in the sample are the listed ones
-    // plus those left out by the chunks whose t-th largest is tau (a chunk's
-    // t-th largest is at most tau, and below it every copy of tau is listed).
-    if (tid == 0 && !wait_count(&c.bar, static_cast<unsigned>(G) + a.wait.skew, &c.abort, limit)) s_err = 1;
+    // c. The first CTA waits for every list (thread c for chunk c's flag,
+    // bounded), then selects tau among the G t candidates.  The copies of
+    // tau in the sample are the listed ones plus those left out by the
+    // chunks whose t-th largest is tau (a chunk's t-th largest is at most
+    // tau, and below it every copy of tau is listed).
+    (void)c;
+    const int64_t nflags = G + a.wait.skew;  // a test setting waits for a flag no chunk writes
+    for (int64_t ch = tid; ch < nflags; ch += ST_THREADS) {
+      unsigned long long f;
+      for (int poll = 0;; ++poll) {
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(f) : "l"(&cd.flag[ch]) : "memory");
+        if ((f >> 1) == epoch) break;
+        if (poll >= limit) {
+          s_err = 1;
+          break;
+        }
+      }
+      if ((f >> 1) == epoch && (f & 1ull)) s_fail = 1;
+    }
     __syncthreads();
     ST_LEAVE_IF_GAVE_UP();
+    if (tid == 0 && s_fail) atomicOr(&S.error, 1u);
     // The lists into shared memory, eight independent loads per thread in
     // flight at a time, then the selection there.
     const int64_t total = G * static_cast<int64_t>(t);
@@ -599,7 +667,24 @@ int64_t sample_tau_chunks(int64_t S, int nrows) {
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// Epochs of the candidate lists' flags: a nonce drawn once per process (the
+// clock and the process id, mixed) in the high 31 bits, a launch counter in
+// the low 32.  Never 0.
+unsigned long long next_epoch() {
+  static const unsigned long long nonce = [] {
+    unsigned long long z = static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) ^
+                           (static_cast<unsigned long long>(getpid()) << 40);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return (z ^ (z >> 31)) & 0x7FFFFFFFull;
+  }();
+  static std::atomic<unsigned long long> count{0};
+  return (nonce << 32) | ((count.fetch_add(1) + 1) & 0xFFFFFFFFull);
+}
+
 }  // namespace
+
+int64_t sample_tau_setup_max_t() { return TAU_CAND; }
 
 void launch_sample_rows(const SampleArgs& a, int64_t key_row0, cudaStream_t stream) {
   const int64_t blocks = (a.S + DRAW_THREADS - 1) / DRAW_THREADS;
@@ -629,9 +714,10 @@ cudaError_t launch_sample_tau(const SampleArgs& a, void* scratch, int64_t total_
   const dim3 grid(static_cast<unsigned>(G), static_cast<unsigned>(a.nrows));
   if (a.t <= static_cast<unsigned long long>(TAU_CAND)) {
     const size_t smem = sizeof(uint32_t) * static_cast<size_t>(G) * a.t;  // at most 8 KB
-    launch_kernel(k_sample_tau<true>, grid, ST_THREADS, smem, stream, a, ctl, cand);
-  } else
-    launch_kernel(k_sample_tau<false>, grid, ST_THREADS, 0, stream, a, ctl, cand);
+    launch_kernel(k_sample_tau<true>, grid, ST_THREADS, smem, stream, a, ctl, cand, next_epoch());
+  } else {
+    launch_kernel(k_sample_tau<false>, grid, ST_THREADS, 0, stream, a, ctl, cand, 0ull);
+  }
   return cudaGetLastError();
 }
 
