@@ -232,7 +232,20 @@ typedef enum profk_option {
                                   2^22.  Every CTA of the row then gives up, writes nothing more, and
                                   the call returns PROFK_ERR_DEVICE_TIMEOUT with its outputs untouched;
                                   the next call is unaffected */
-  PROFK_OPT__COUNT = 12
+  PROFK_OPT_SPECULATIVE = 12,  /* redraws enqueued on the device [0]: 0 .. 8 attempts enqueued right
+                                  after the first one, before the host reads the run-time check.  Each
+                                  is attempt a of every row (the same sample, tau and result as the
+                                  host-driven attempt a), and its kernels leave alone every row that an
+                                  earlier attempt settled (its check passed, or it takes the tie exit,
+                                  or it met a NaN or an error): a row that fails the check is redrawn
+                                  without a host round trip, and the host reads the report once, after
+                                  the last of them (profk_wait, for the asynchronous calls).  Results and
+                                  statistics are those of the option's default.  Capped at
+                                  PROFK_OPT_MAX_ATTEMPTS - 1; taken only where the grid form of the
+                                  sampler takes the rows (see PROFK_OPT_SAMPLER) and
+                                  PROFK_OPT_TIMING is off.  A call whose rows all pass the first check
+                                  pays the empty attempts' launches (a few microseconds each) */
+  PROFK_OPT__COUNT = 13
 } profk_option;
 #define PROFK_WAIT_TEST_OFF 0
 #define PROFK_WAIT_TEST_SAMPLER 1
@@ -241,7 +254,7 @@ typedef enum profk_option {
 /* Forms of the sampling kernels (PROFK_OPT_SAMPLER); both give the same
  * sample and tau.  GRID: one persistent kernel (all CTAs resident), each CTA
  * taking up to 1024 sample positions; tau from per-CTA candidate lists that
- * one CTA waits for (t <= 128) or from passes whose CTAs meet at grid
+ * one CTA waits for (t <= 8) or from passes whose CTAs meet at grid
  * barriers (larger t).  STEPS: one thread per sample position, then a radix
  * selection of tau; taken when the rows' shares of the SMs are too small. */
 #define PROFK_SAMPLER_AUTO 0

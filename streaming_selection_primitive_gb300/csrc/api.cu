@@ -28,7 +28,7 @@ namespace {
 // ---------------------------------------------------------------------------
 // Options.
 std::atomic<int64_t> g_opt[PROFK_OPT__COUNT] = {
-    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}, {1}, {0}, {PROFK_SAMPLER_AUTO}, {PROFK_WAIT_TEST_OFF}};
+    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}, {1}, {0}, {PROFK_SAMPLER_AUTO}, {PROFK_WAIT_TEST_OFF}, {0}};
 
 // PROFK_OPT_WAIT_TEST: the wait setting of the persistent kernel it names
 // (one arrival more than the launch has at its first grid barrier, and a
@@ -163,13 +163,15 @@ __global__ void k_attempt_init(RowState* st, const int* rows) {
 // Start of an attempt for the listed rows: counters to zero and the
 // selection state ready for tau (rank t).  The control blocks of each row's
 // sampling (sample_ctl, sample_words 8-byte words per row) and refinement
-// (sort_ctl, ctl_words) are zeroed too.
+// (sort_ctl, ctl_words) are zeroed too.  A row that an earlier attempt
+// settled is left alone.
 __global__ void k_attempt_reset(const int* rows, RowState* st, unsigned long long t, unsigned long long* sort_ctl,
                                 int ctl_words, unsigned long long* sample_ctl, int sample_words, unsigned* block_eq,
-                                int64_t nblocks) {
+                                int64_t nblocks, int attempt) {
   pdl_trigger();
   pdl_wait();
   const int row = launch_row(rows);
+  if (settled_before(st[row], attempt)) return;
   // 16-byte stores, grid-strided over the row's CTAs: the control blocks (an
   // even number of words each) to zero.
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -205,6 +207,7 @@ __global__ void k_attempt_reset(const int* rows, RowState* st, unsigned long lon
     S.skip = 0;
     S.tie_gt = 0;
     S.tau_copies = 0;
+    S.settled = 0;
   }
 }
 
@@ -523,16 +526,30 @@ Sampler choose_sampler(int64_t S, int64_t ng) {
   return sample_tau_fits(S, static_cast<int>(ng)) ? Sampler::Grid : Sampler::Steps;
 }
 
+// Attempts enqueued after the first attempt of all `rows`, before the host
+// reads the check (PROFK_OPT_SPECULATIVE): within max_attempts, and only where
+// the grid sampler takes the rows (the step-by-step kernels do not leave
+// settled rows alone).
+int speculative_attempts(const Params& P, int64_t rows, int max_attempts) {
+  const int64_t want = g_opt[PROFK_OPT_SPECULATIVE].load();
+  if (want <= 0 || max_attempts <= 1 || choose_sampler(P.S, rows) != Sampler::Grid) return 0;
+  return static_cast<int>(std::min<int64_t>(want, max_attempts - 1));
+}
+
 // One attempt of the listed rows (gl, ng of them; all rows when gl is null):
 // reset, sampling and tau, filter, and the refinement, which is enqueued
 // before the host has seen the counts (a row whose count fails the check is
 // voided on the device and left untouched, so the host round trip of the
 // check is off the critical path of the likely successful attempt).  ev:
-// stage events e[1..4] (e[0] is the caller's), or nullptr.
+// stage events e[1..4] (e[0] is the caller's), or nullptr.  The refinement
+// also records the check's outcome in the row state (settle_row, with the
+// call's tie_exit), and every kernel of an attempt a > 0 leaves alone the
+// rows that an earlier one settled, so that attempts can follow one another
+// on the stream before the host has read any report.
 cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, int ng, const int* gl, int64_t rows,
                             const float* x, int64_t ld, int64_t n, int64_t k, uint64_t seed, int64_t cps,
                             float* out_vals, int64_t* out_idx, cudaStream_t stream, cudaEvent_t* ev,
-                            bool tie_book) {
+                            bool tie_book, bool tie_exit) {
   RowState* st = at<RowState>(ws, L.off_state);
   const Sampler form = choose_sampler(P.S, ng);
   // Reset CTAs per row: a few 16-byte stores per thread of 256.
@@ -555,7 +572,7 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
   if (!fused_setup)
     launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, gl, st, static_cast<unsigned long long>(P.t), ref_ctl,
                   ref_words, at<unsigned long long>(ws, L.off_sctl), static_cast<int>(sample_tau_ctl_bytes() / 8),
-                  block_eq, nb);
+                  block_eq, nb, a);
   // Sampling and tau: one persistent kernel (its stage time is reported as
   // the sampling's, the threshold stage then being empty), or, when many rows
   // share the SMs, the step-by-step kernels with the first radix pass of tau
@@ -583,18 +600,22 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
   }
   if (ev) cudaEventRecord(ev[2], stream);
   FilterArgs fa{x, ld, n, P.M, ng, gl, st, at<unsigned long long>(ws, L.off_buf), filter_grid(cps), block_eq, nb,
-                tie_book ? at<unsigned long long>(ws, L.off_sel) : nullptr, L.kstride, k};
+                tie_book ? at<unsigned long long>(ws, L.off_sel) : nullptr, L.kstride, k, a};
   launch_filter(fa, stream);
   if (ev) cudaEventRecord(ev[3], stream);
   if (!L.radix_refine) {
     RefineGridArgs ga{at<unsigned long long>(ws, L.off_buf), P.M, ng, gl, st, k, x, ld, n, out_vals, out_idx};
     ga.wait = wait_cfg_for(PROFK_WAIT_TEST_REFINE);
+    ga.attempt = a;
+    ga.tie_exit = tie_exit;
     e = launch_refine_grid(ga, at<char>(ws, L.off_refine), rows, stream);
   } else {
     // The whole buffer (R <= M keys) is sorted and its first k emitted.
     RadixSortArgs ra{at<unsigned long long>(ws, L.off_buf), P.M, k, SortCount::FromState, ng, gl, rows,
                      at<char>(ws, L.off_sort), true, x, ld, n, out_vals, out_idx, st};
     ra.wait = wait_cfg_for(PROFK_WAIT_TEST_SORT);
+    ra.attempt = a;
+    ra.tie_exit = tie_exit;
     e = launch_radix_sort(ra, stream);
   }
   if (e != cudaSuccess) return e;
@@ -617,10 +638,10 @@ cudaError_t enqueue_report(const RowState* st, int64_t rows, char* rep, unsigned
 }
 
 // The state an asynchronous call hands to the synchronous loop when its first
-// attempt did not clear the check: the workspace that attempt used (its layout
-// is run_topk's for the same arguments), its parameters and its report (the
-// heads of every row's state).  The loop continues from there instead of
-// repeating the attempt.
+// attempt (and the speculative ones after it) did not clear the check: the
+// workspace they used (its layout is run_topk's for the same arguments), the
+// parameters and the report (the heads of every row's state).  The loop
+// continues from there instead of repeating the attempts.
 struct Resume {
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -628,6 +649,7 @@ struct Resume {
   Params P{};
   int64_t launches = 0;  // kernels the first attempt launched
   bool tie_exit = true;  // PROFK_OPT_TIE_EXIT when the first attempt was enqueued
+  int extra = 0;         // attempts enqueued after the first (speculative_attempts)
 };
 
 int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, double eps, uint64_t seed,
@@ -814,6 +836,10 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
     // The first attempt of all rows already ran (asynchronous call): take its report.
     const bool resumed = resume && !resume_used && a == 0 && static_cast<int64_t>(ng) == rows;
     if (!resumed) PK_CHECK(upload_rows(L, c.ws, hbuf, 0, group, stream, &gl));
+    // Attempts a+1 .. a+extra, enqueued after attempt a of all rows before
+    // the report is read: a row's report is then that of the attempt that
+    // settled it (RowState::settled), or of the last one.
+    int extra = 0;
     {
       const bool time_it = timing && first_filter && !resumed;
       if (time_it) {
@@ -825,10 +851,15 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
       if (resumed) {
         std::memcpy(rep, resume->report, REPORT_BYTES * rows);
         resume_used = true;
+        extra = resume->extra;
       } else {
       PK_CHECK(enqueue_attempt(L, c.ws, P, a, ng, gl, rows, x, ld, n, k, seed, cps, out_vals, out_idx, stream,
-                               time_it ? t_events.e : nullptr, tie_exit && aligned_rows));
+                               time_it ? t_events.e : nullptr, tie_exit && aligned_rows, tie_exit));
       if (time_it) PK_CHECK(cudaEventRecord(t_events.e[4], stream));
+      if (a == 0 && static_cast<int64_t>(ng) == rows && !timing) extra = speculative_attempts(P, rows, max_attempts);
+      for (int q = 1; q <= extra; ++q)
+        PK_CHECK(enqueue_attempt(L, c.ws, P, q, ng, gl, rows, x, ld, n, k, seed, cps, out_vals, out_idx, stream,
+                                 nullptr, tie_exit && aligned_rows, tie_exit));
       PK_CHECK(cudaGetLastError());
       // Run-time check: read the exact counts of every row (written into
       // pinned memory by a kernel and waited for, or copied and synchronized
@@ -856,7 +887,8 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
       for (int r : group) {
         const char* h = rep + REPORT_BYTES * r;
         unsigned long long Rg = 0, Rt = 0, nanc = 0;
-        unsigned distinct = 0, tau_key = 0, errf = 0, copies = 0;
+        unsigned distinct = 0, tau_key = 0, errf = 0, copies = 0, settled = 0;
+        std::memcpy(&settled, h + offsetof(RowState, settled), 4);
         std::memcpy(&copies, h + offsetof(RowState, tau_copies), 4);
         std::memcpy(&Rg, h + offsetof(RowState, R_ge), 8);
         std::memcpy(&Rt, h + offsetof(RowState, R_gt), 8);
@@ -877,26 +909,43 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
           goto done;
         }
         profk_stats& s = st_host[r];
-        s.attempts = a + 1;
+        const int ar = extra == 0 ? a : (settled ? static_cast<int>(settled) - 1 : a + extra);  // the report's attempt
+        s.attempts = ar + 1;
         const float tau = key_to_float(tau_key);
         if (a == 0) {
-          s.R_first = static_cast<int64_t>(Rg);
-          s.R_gt_first = static_cast<int64_t>(Rt);
-          s.tau_first = tau;
+          // Attempt 0's counts: the report's own, or the copy that attempt
+          // kept when later ones ran before the report was read.
+          unsigned long long R1 = Rg, Rt1 = Rt;
+          unsigned tau1 = tau_key;
+          if (extra > 0) {
+            std::memcpy(&R1, h + offsetof(RowState, R_first), 8);
+            std::memcpy(&Rt1, h + offsetof(RowState, R_gt_first), 8);
+            std::memcpy(&tau1, h + offsetof(RowState, tau_first), 4);
+          }
+          s.R_first = static_cast<int64_t>(R1);
+          s.R_gt_first = static_cast<int64_t>(Rt1);
+          s.tau_first = key_to_float(tau1);
         }
         s.R_final = static_cast<int64_t>(Rg);
         s.R_gt_final = static_cast<int64_t>(Rt);
         s.tau_final = tau;
-        if (static_cast<uint64_t>(k) <= Rg && Rg <= static_cast<uint64_t>(P.M)) {
+        const bool pass = static_cast<uint64_t>(k) <= Rg && Rg <= static_cast<uint64_t>(P.M);
+        const bool tie_row = !pass && tie_exit && Rg > static_cast<uint64_t>(P.M) && Rt < static_cast<uint64_t>(k);
+        // The device took the same decision (settle_row): a mismatch is a fault.
+        if (extra > 0 && (settled != 0) != (pass || tie_row)) {
+          c.status = PROFK_ERR_CUDA;
+          goto done;
+        }
+        if (pass) {
           s.path = PROFK_PATH_FILTER;  // refined on the device already
-        } else if (tie_exit && Rg > static_cast<uint64_t>(P.M) && Rt < static_cast<uint64_t>(k)) {
+        } else if (tie_row) {
           s.path = PROFK_PATH_TIE;
           // The filter kept the tie step's counts for the rows whose sample
           // held tau more than once (aligned rows); the others need the
           // counting pass (or, unaligned, the selection-based step).
           (copies >= 2 && aligned_rows ? tie : tie_count).push_back(r);
         } else {
-          attempt[r] = a + 1;
+          attempt[r] = ar + 1;
           next.push_back(r);
         }
       }
@@ -999,10 +1048,11 @@ bool pdl_enabled() { return g_opt[PROFK_OPT_PDL].load(std::memory_order_relaxed)
 using namespace profk;
 
 // An asynchronous call (profk_topk_async / profk_topk_batched_async): its
-// first attempt is enqueued and the check's report is waited for later, in
-// profk_wait.  A call that the check does not clear is run again, whole and
-// synchronously, at that point (the same seed gives the same attempt, so the
-// outputs and statistics are those of the synchronous call).
+// first attempt (and the speculative attempts after it) is enqueued and the
+// check's report is waited for later, in profk_wait.  A call that the check
+// does not clear continues synchronously from that report at that point (the
+// same seed gives the same attempts, so the outputs and statistics are those
+// of the synchronous call); a call whose report never came is run again.
 struct profk_call {
   const float* x = nullptr;
   int64_t rows = 0, n = 0, ld = 0, k = 0;
@@ -1024,6 +1074,7 @@ struct profk_call {
   cudaEvent_t copied = nullptr;  // the report copy of more than REPORT_ROWS_MAPPED rows
   int64_t launches = 0;
   bool tie_exit = true;  // PROFK_OPT_TIE_EXIT at submission
+  int extra = 0;         // attempts enqueued after the first (PROFK_OPT_SPECULATIVE)
 };
 
 namespace {
@@ -1108,10 +1159,11 @@ int submit_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
     e = take_block(REPORT_BYTES * rows + 512, &call->host, &call->host_bytes);
   }
   call->tie_exit = g_opt[PROFK_OPT_TIE_EXIT].load() != 0;
-  if (e == cudaSuccess)
-    e = enqueue_attempt(L, call->ws, P, 0, static_cast<int>(rows), nullptr, rows, x, ld, n, k, seed,
+  call->extra = speculative_attempts(P, rows, static_cast<int>(g_opt[PROFK_OPT_MAX_ATTEMPTS].load()));
+  for (int a = 0; e == cudaSuccess && a <= call->extra; ++a)
+    e = enqueue_attempt(L, call->ws, P, a, static_cast<int>(rows), nullptr, rows, x, ld, n, k, seed,
                         g_opt[PROFK_OPT_FILTER_CTAS_PER_SM].load(), out_vals, out_idx, stream, nullptr,
-                        call->tie_exit && rows_aligned(x, rows, ld));
+                        call->tie_exit && rows_aligned(x, rows, ld), call->tie_exit);
   if (e == cudaSuccess) {
     call->flag = reinterpret_cast<unsigned long long*>(
         align_up(reinterpret_cast<uintptr_t>(call->host + REPORT_BYTES * rows)));
@@ -1145,24 +1197,33 @@ int finish_async(profk_call* call, profk_stats* stats) {
     const unsigned long long k = static_cast<unsigned long long>(call->k);
     for (int64_t r = 0; clear && r < call->rows; ++r) {
       const char* h = call->host + REPORT_BYTES * r;
-      unsigned long long Rg = 0, Rt = 0, nanc = 0;
-      unsigned distinct = 0, tau_key = 0, errf = 0;
+      unsigned long long Rg = 0, Rt = 0, nanc = 0, R1 = 0, Rt1 = 0;
+      unsigned distinct = 0, tau_key = 0, errf = 0, settled = 0, tau1 = 0;
+      std::memcpy(&settled, h + offsetof(RowState, settled), 4);
+      std::memcpy(&R1, h + offsetof(RowState, R_first), 8);
+      std::memcpy(&Rt1, h + offsetof(RowState, R_gt_first), 8);
+      std::memcpy(&tau1, h + offsetof(RowState, tau_first), 4);
       std::memcpy(&Rg, h + offsetof(RowState, R_ge), 8);
       std::memcpy(&Rt, h + offsetof(RowState, R_gt), 8);
       std::memcpy(&nanc, h + offsetof(RowState, nan), 8);
       std::memcpy(&distinct, h + offsetof(RowState, distinct), 4);
       std::memcpy(&tau_key, h + offsetof(RowState, tau_key), 4);
       std::memcpy(&errf, h + offsetof(RowState, error), 4);
+      // With attempts after the first, a passing row's report is that of
+      // the attempt that settled it, and attempt 0's counts are its copy.
       clear = nanc == 0 && errf == 0 && static_cast<int64_t>(distinct) >= call->P.S && k <= Rg &&
-              Rg <= static_cast<unsigned long long>(call->P.M);
+              Rg <= static_cast<unsigned long long>(call->P.M) && (call->extra == 0 || settled != 0);
       if (clear) {
         profk_stats& s = call->stats[static_cast<size_t>(r)];
         fill_stats_params(&s, call->P);
-        const float tau = key_to_float(tau_key);
-        s.R_first = s.R_final = static_cast<int64_t>(Rg);
-        s.R_gt_first = s.R_gt_final = static_cast<int64_t>(Rt);
-        s.tau_first = s.tau_final = tau;
-        s.attempts = 1;
+        const bool own = call->extra == 0;
+        s.R_first = static_cast<int64_t>(own ? Rg : R1);
+        s.R_gt_first = static_cast<int64_t>(own ? Rt : Rt1);
+        s.tau_first = key_to_float(own ? tau_key : tau1);
+        s.R_final = static_cast<int64_t>(Rg);
+        s.R_gt_final = static_cast<int64_t>(Rt);
+        s.tau_final = key_to_float(tau_key);
+        s.attempts = own ? 1 : static_cast<int32_t>(settled);
         s.path = PROFK_PATH_FILTER;
         s.aux_bytes = call->ws_bytes;
         s.launches = static_cast<int32_t>(call->launches);
@@ -1184,6 +1245,7 @@ int finish_async(profk_call* call, profk_stats* stats) {
       rs.P = call->P;
       rs.launches = call->launches;
       rs.tie_exit = call->tie_exit;
+      rs.extra = call->extra;
       status = run_topk(call->x, call->rows, call->n, call->ld, call->k, call->eps, call->seed, call->out_vals,
                         call->out_idx, call->stream, call->stats.data(), &rs);
     } else {
@@ -1282,6 +1344,7 @@ int profk_set_option(int option, int64_t value) {
     return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_WAIT_TEST && (value < PROFK_WAIT_TEST_OFF || value > PROFK_WAIT_TEST_SORT))
     return PROFK_ERR_INVALID;
+  if (option == PROFK_OPT_SPECULATIVE && value > 8) return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_MAX_SEGMENT && value != 0 && (value < (1 << 16) || value > (int64_t(1) << 32) || (value & 3)))
     return PROFK_ERR_INVALID;
   if (value < 0) return PROFK_ERR_INVALID;

@@ -81,18 +81,6 @@ __device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64
   }
 }
 
-// Lemire's multiply-shift bounded integer: accept w for range n unless the
-// low half of w*n falls in the (2^64 mod n) rejection zone.
-__device__ __forceinline__ bool lemire64(uint64_t w, uint64_t n, uint64_t* out) {
-  const uint64_t lo = w * n;
-  if (lo < n) {
-    const uint64_t thr = (0ull - n) % n;
-    if (lo < thr) return false;
-  }
-  *out = __umul64hi(w, n);
-  return true;
-}
-
 // ---------------------------------------------------------------------------
 // Per-row device state of one call.  Zeroed by the host before use.
 struct RowState {
@@ -101,6 +89,10 @@ struct RowState {
   unsigned long long R_ge;
   unsigned long long R_gt;
   unsigned long long nan;
+  // The first attempt's counts, kept for the statistics when later attempts
+  // run before the host reads the row (written by attempt 0's refinement).
+  unsigned long long R_first;
+  unsigned long long R_gt_first;
   // Sampling.
   unsigned int distinct;  // distinct draws among the D examined
   unsigned int tau_key;   // ord(tau)
@@ -119,8 +111,42 @@ struct RowState {
   unsigned int skip;              // 1: this row's refinement is void (its attempt failed the check)
   unsigned int tie_gt;            // x > tau appended to the tie list by the filter
   unsigned int tau_copies;        // copies of tau among the sample keys (2 or more: a tied top)
+  // 1 + the attempt whose check settled the row (it passed, or takes the tie
+  // exit, or met a NaN or an error), 0 while it is open.  The kernels of a
+  // later attempt leave a settled row alone.
+  unsigned int settled;
+  unsigned int tau_first;         // ord(tau) of the first attempt
   unsigned int hist[HIST_BINS];
 };
+
+// Whether an attempt before `attempt` settled the row: the kernels of this
+// attempt then leave it alone.  Every CTA of the row reads the same value
+// (only a refinement writes it, and those of earlier attempts have finished),
+// so the test is row-uniform.
+__device__ __forceinline__ bool settled_before(const RowState& S, int attempt) {
+  if (attempt == 0) return false;
+  const unsigned s = __ldcg(&S.settled);
+  return s != 0u && s <= static_cast<unsigned>(attempt);
+}
+
+// The run-time check of `attempt` for the row, taken on the device by its
+// refinement (one thread): the row is settled when k <= R <= M, or when the
+// tie exit takes it (R > M and R_gt < k, with the tie exit on), or when a
+// NaN or an error was counted; otherwise the next attempt redraws it.  The
+// host reads the same counts and takes the same decision.  Attempt 0 also
+// keeps its counts for the statistics.
+__device__ __forceinline__ void settle_row(RowState& S, int attempt, unsigned long long k, unsigned long long M,
+                                           bool tie_exit) {
+  const unsigned long long R = __ldcg(&S.R_ge), Rt = __ldcg(&S.R_gt);
+  const bool pass = k <= R && R <= M;
+  const bool tie = tie_exit && R > M && Rt < k;
+  if (pass || tie || __ldcg(&S.nan) != 0ull || __ldcg(&S.error) != 0u) S.settled = static_cast<unsigned>(attempt) + 1u;
+  if (attempt == 0) {
+    S.R_first = R;
+    S.R_gt_first = Rt;
+    S.tau_first = __ldcg(&S.tau_key);
+  }
+}
 
 // ---------------------------------------------------------------------------
 // Bounded waits of the persistent kernels (grid barriers and look-backs).

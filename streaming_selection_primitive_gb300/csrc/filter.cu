@@ -209,8 +209,9 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
       }
       cur = ri;
       const int nrow = a.rows ? a.rows[ri] : ri;
-      if (a.block_eq && (a.st[nrow].tau_copies >= 2) != TIE) {
-        // The other loop's row: on to this warp's first tile past it.
+      if ((a.block_eq && (a.st[nrow].tau_copies >= 2) != TIE) || settled_before(a.st[nrow], a.attempt)) {
+        // The other loop's row, or one that an earlier attempt settled: on
+        // to this warp's first tile past it.
         const int64_t next = static_cast<int64_t>(ri + 1) * tiles_per_row;
         tile += (next - tile + nwarps - 1) / nwarps * nwarps - nwarps;
         continue;

@@ -106,7 +106,8 @@ void launch_sample_rows(const SampleArgs& a, int64_t key_row0, cudaStream_t stre
 // a.t) of each listed row.  `scratch` holds sample_tau_scratch_bytes(
 // total_rows): first the per-row control blocks (sample_tau_ctl_bytes()
 // each, indexed by row, zero at launch), then candidate lists that need no
-// initialisation.
+// initialisation.  Rows that an attempt before a.attempt settled
+// (settled_before) are left alone.
 size_t sample_tau_ctl_bytes();
 size_t sample_tau_scratch_bytes(int64_t rows);
 cudaError_t launch_sample_tau(const SampleArgs& a, void* scratch, int64_t total_rows, cudaStream_t stream);
@@ -224,6 +225,11 @@ struct RadixSortArgs {
   int64_t* out_idx;
   RowState* st;  // skip / count source, and where a timed-out wait is reported
   WaitCfg wait{};  // test setting of its waits
+  // FromState: the attempt this refinement belongs to (rows settled by an
+  // earlier one are left alone; see settle_row) and whether the call's tie
+  // exit is on.
+  int attempt = 0;
+  bool tie_exit = false;
 };
 size_t radix_sort_scratch_bytes(int64_t key_stride, int64_t rows);
 void* radix_sort_ctl(void* scratch, int64_t key_stride, int64_t rows);  // per-row control blocks
@@ -250,6 +256,11 @@ struct RefineOneArgs {
   float* out_vals;
   int64_t* out_idx;
   WaitCfg wait{};  // launch_refine_grid: test setting of its waits
+  // launch_refine_grid: the attempt this refinement belongs to (rows settled
+  // by an earlier one are left alone; see settle_row) and whether the call's
+  // tie exit is on.
+  int attempt = 0;
+  bool tie_exit = false;
 };
 void launch_refine_one(const RefineOneArgs& a, cudaStream_t stream);
 int64_t refine_one_max_k();
@@ -290,6 +301,7 @@ struct FilterArgs {
   unsigned long long* tie_keys = nullptr;
   int64_t tie_stride = 0;
   int64_t k = 0;
+  int attempt = 0;  // rows settled by an earlier attempt are left alone (settled_before)
 };
 // The filter pass over the listed rows.  x must be 4-byte aligned.  When some
 // row does not start on a 16-byte boundary (x 4-byte aligned only, or a row

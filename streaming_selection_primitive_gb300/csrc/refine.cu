@@ -19,7 +19,9 @@
 // does not keep: it is read from x.
 //
 // The kernel is enqueued before the host has checked k <= R <= M; a row that
-// fails the check is marked skip and its outputs are not touched.
+// fails the check is marked skip and its outputs are not touched.  The check's
+// outcome is recorded in the row state (settle_row), so that the kernels of
+// an attempt enqueued after this one leave a settled row alone.
 #include "kernels.h"
 
 namespace profk {
@@ -97,12 +99,20 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
   const unsigned long long R = S.R_ge;
   const unsigned long long k = static_cast<unsigned long long>(a.k);
   // A row that fails the check, or whose earlier steps reported an error,
-  // is left alone (its outputs are not touched).  One thread decides for
-  // the block.
-  if (tid == 0) s_digit = !(k <= R && R <= static_cast<unsigned long long>(a.M)) || __ldcg(&S.error) != 0u;
+  // is left alone (its outputs are not touched); so is a row that an
+  // earlier attempt settled.  One thread decides for the block; the first
+  // CTA's also records the check's outcome (settle_row).
+  if (tid == 0) {
+    if (settled_before(S, a.attempt)) {
+      s_digit = 2;
+    } else {
+      s_digit = !(k <= R && R <= static_cast<unsigned long long>(a.M)) || __ldcg(&S.error) != 0u;
+      if (blockIdx.x == 0) settle_row(S, a.attempt, k, static_cast<unsigned long long>(a.M), a.tie_exit);
+    }
+  }
   __syncthreads();
   if (s_digit) {
-    if (blockIdx.x == 0 && tid == 0) S.skip = 1;
+    if (s_digit == 1 && blockIdx.x == 0 && tid == 0) S.skip = 1;
     return;  // every CTA of the row leaves: no barrier is met
   }
   const int limit = wait_limit(a.wait);

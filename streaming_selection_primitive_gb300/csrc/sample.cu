@@ -368,6 +368,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   SampleCtl& c = ctl[row];
   const int tid = threadIdx.x;
   const int64_t G = gridDim.x, chunk = blockIdx.x;
+  if (settled_before(S, a.attempt)) return;  // every CTA of the row leaves: nothing is waited for
   if (tid == 0) {
     s_err = 0;
     s_fail = 0;
@@ -403,6 +404,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
         S.compact_count = 0;
         S.skip = 0;
         S.tie_gt = 0;
+        S.settled = 0;
       }
     }
   }

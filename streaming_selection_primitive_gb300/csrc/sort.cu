@@ -710,7 +710,17 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_rs_sort(RadixSortArgs a, Sort
   __shared__ Smem sm;
   const int row = launch_row(a.rows);
   if (threadIdx.x == 0) {
-    sm.row_len = row_count(a, row);  // one thread decides for the block
+    // One thread decides for the block.  The refinement of the filter buffer
+    // leaves alone a row that an earlier attempt settled, and its first CTA
+    // records the check's outcome (settle_row).
+    if (a.mode == SortCount::FromState && settled_before(a.st[row], a.attempt)) {
+      sm.row_len = -1;
+    } else {
+      sm.row_len = row_count(a, row);
+      if (a.mode == SortCount::FromState && blockIdx.x == 0)
+        settle_row(a.st[row], a.attempt, static_cast<unsigned long long>(a.k),
+                   static_cast<unsigned long long>(a.key_stride), a.tie_exit);
+    }
     sm.err = 0;
     sm.limit = wait_limit(a.wait);
   }

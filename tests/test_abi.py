@@ -173,3 +173,14 @@ def test_wait_test_option(pk):
     for bad in (4, -1):
         with pytest.raises(pk.ProfkError):
             pk.set_option(pk.OPT_WAIT_TEST, bad)
+
+
+def test_speculative_option(pk):
+    # Attempts enqueued after the first: off by default, 0 .. 8.
+    assert pk.get_option(pk.OPT_SPECULATIVE) == 0
+    for v in (8, 1, 0):
+        pk.set_option(pk.OPT_SPECULATIVE, v)
+        assert pk.get_option(pk.OPT_SPECULATIVE) == v
+    for bad in (9, -1):
+        with pytest.raises(pk.ProfkError):
+            pk.set_option(pk.OPT_SPECULATIVE, bad)
