@@ -125,12 +125,22 @@ __device__ __forceinline__ void warp_sort_desc(unsigned long long (&v)[E]) {
 
 __device__ __forceinline__ void warp_sort256_desc(unsigned long long (&v)[8]) { warp_sort_desc<8>(v); }
 
-// Descending sort of P keys s[0..P) (P a multiple of 256, at most 256 x the
-// warps of the block) by a block of 1024 threads: every warp sorts one run of
-// 256 in registers, then runs are merged pairwise (merge path: each thread
-// finds where its P / 1024 outputs start by a binary search, then merges
-// them), alternating between s and t (P keys each).  Keys must be distinct.
-// Returns the buffer that holds the result; ends with a block barrier.
+// Shared-memory slot of key i in the buffers of block_merge_sort_desc: the
+// low four bits of i XORed with the next four.  A 64-bit key spans two of the
+// 32 banks, so 16 consecutive keys fill them once; with the swizzle, threads
+// that read or write keys 4 or 8 apart (the merge rounds' pattern, each thread
+// taking consecutive outputs) spread over all banks instead of piling onto
+// two or four of them (an 8- or 16-way conflict), and consecutive keys stay
+// conflict-free.  The map permutes each aligned group of 256 keys.
+__device__ __forceinline__ int mswz(int i) { return i ^ ((i >> 4) & 15); }
+
+// Descending sort of P keys (P a multiple of 256, at most 256 x the warps of
+// the block) by a block of 1024 threads, key i stored at s[mswz(i)]: every
+// warp sorts one run of 256 in registers, then runs are merged pairwise
+// (merge path: each thread finds where its P / 1024 outputs start by a binary
+// search, then merges them), alternating between s and t (P keys each, the
+// same layout).  Keys must be distinct.  Returns the buffer that holds the
+// result (key i at mswz(i)); ends with a block barrier.
 __device__ __forceinline__ unsigned long long* block_merge_sort_desc(unsigned long long* s, unsigned long long* t,
                                                                      int P) {
   constexpr int T = 1024;
@@ -138,10 +148,10 @@ __device__ __forceinline__ unsigned long long* block_merge_sort_desc(unsigned lo
   if (warp * 256 < P) {
     unsigned long long v[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) v[r] = s[warp * 256 + r * 32 + lane];
+    for (int r = 0; r < 8; ++r) v[r] = s[mswz(warp * 256 + r * 32 + lane)];
     warp_sort256_desc(v);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) s[warp * 256 + r * 32 + lane] = v[r];
+    for (int r = 0; r < 8; ++r) s[mswz(warp * 256 + r * 32 + lane)] = v[r];
   }
   __syncthreads();
   // Outputs per thread and round: a power of two, so that no thread's run of
@@ -154,22 +164,32 @@ __device__ __forceinline__ unsigned long long* block_merge_sort_desc(unsigned lo
       const int base = p0 / (2 * w) * (2 * w);  // this pair's first position
       const int na = w < P - base ? w : P - base;
       const int nb = P - base - na < w ? P - base - na : w;
-      const unsigned long long* A = s + base;
-      const unsigned long long* B = A + na;
+      auto A = [&](int q) { return s[mswz(base + q)]; };
+      auto B = [&](int q) { return s[mswz(base + na + q)]; };
       const int off = p0 - base;
       int lo = off > nb ? off - nb : 0, hi = off < na ? off : na;
       while (lo < hi) {  // how many of the first `off` outputs come from A
         const int mid = (lo + hi) >> 1;
-        if (A[mid] > B[off - mid - 1])
+        if (A(mid) > B(off - mid - 1))
           lo = mid + 1;
         else
           hi = mid;
       }
       int i = lo, j = off - lo;
       const int end = p0 + per < base + na + nb ? p0 + per : base + na + nb;
+      // The heads of both runs are kept in registers: one shared load per output.
+      unsigned long long ha = i < na ? A(i) : 0ull, hb = j < nb ? B(j) : 0ull;
       for (int p = p0; p < end; ++p) {
-        const bool takeA = j >= nb || (i < na && A[i] > B[j]);
-        t[p] = takeA ? A[i++] : B[j++];
+        const bool takeA = j >= nb || (i < na && ha > hb);
+        if (takeA) {
+          t[mswz(p)] = ha;
+          ++i;
+          ha = i < na ? A(i) : 0ull;
+        } else {
+          t[mswz(p)] = hb;
+          ++j;
+          hb = j < nb ? B(j) : 0ull;
+        }
       }
     }
     __syncthreads();

@@ -36,6 +36,8 @@
 // pass over those rows.  Each loop skips the other's rows whole; keeping the
 // bookkeeping out of the plain loop keeps its registers, and its speed, those
 // of a kernel without it.
+#include <type_traits>
+
 #include "kernels.h"
 
 namespace profk {
@@ -79,6 +81,14 @@ __device__ __forceinline__ void flush_row(RowState& S, unsigned long long& gt, u
 
 constexpr int STAGE = 128;  // staged passer keys per warp
 
+// A lane's mask over its 4U elements of a warp tile: 32 bits when they fit
+// (U <= 8, the shipped shape), else 64.
+template <int U>
+using LaneMask = std::conditional_t<(4 * U <= 32), uint32_t, uint64_t>;
+
+__device__ __forceinline__ unsigned popc_mask(uint32_t m) { return static_cast<unsigned>(__popc(m)); }
+__device__ __forceinline__ unsigned popc_mask(uint64_t m) { return static_cast<unsigned>(__popcll(m)); }
+
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -105,11 +115,11 @@ __device__ __forceinline__ void tie_append_one(RowState& S, unsigned long long* 
 // The same for the elements of a warp tile that bit e of each lane's mask m
 // selects (element e is component e % 4 of the lane's float4 v[e / 4]).
 template <int U>
-__device__ __forceinline__ void tie_append_tile(RowState& S, unsigned long long* tl, int64_t k, uint64_t m,
+__device__ __forceinline__ void tie_append_tile(RowState& S, unsigned long long* tl, int64_t k, LaneMask<U> m,
                                                 const float4 (&v)[U], int64_t base) {
   if (!__any_sync(FULL_MASK, m != 0)) return;
   const int lane = threadIdx.x & 31;
-  const unsigned c = static_cast<unsigned>(__popcll(m));
+  const unsigned c = popc_mask(m);
   unsigned incl = c;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -124,7 +134,7 @@ __device__ __forceinline__ void tie_append_tile(RowState& S, unsigned long long*
   for (int u = 0; u < U; ++u) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      if ((m >> (u * 4 + q)) & 1ull) {
+      if ((m >> (u * 4 + q)) & 1u) {
         if (pos < static_cast<unsigned long long>(k)) {
           const int64_t idx = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + q;
           tl[pos] = cand_key(comp(v[u], q), static_cast<uint32_t>(idx));
@@ -137,19 +147,23 @@ __device__ __forceinline__ void tie_append_tile(RowState& S, unsigned long long*
 
 // Moves a warp's staged keys into the buffer with one reservation; with the
 // tie bookkeeping (TIE), the keys above tau (key tkey) that fall beyond M go
-// to the tie list tl.
+// to the tie list tl.  Without it the staged keys above tau are counted here
+// into the lane's gt (the plain loop does not count them per tile).
 template <bool TIE>
 __device__ __forceinline__ void flush_stage(RowState& S, unsigned long long* stage, int& stage_n,
                                             unsigned long long* br, int64_t M, bool& over, unsigned long long* tl,
-                                            int64_t k, uint32_t tkey) {
+                                            int64_t k, uint32_t tkey, unsigned long long& gt) {
   if (stage_n == 0) return;
   const int lane = threadIdx.x & 31;
   unsigned long long gbase = 0;
   if (lane == 0) gbase = atomicAdd(&S.R_ge, static_cast<unsigned long long>(stage_n));
   gbase = __shfl_sync(FULL_MASK, gbase, 0);
   __syncwarp();
-  for (int j = lane; j < stage_n; j += 32)
-    if (gbase + j < static_cast<unsigned long long>(M)) br[gbase + j] = stage[j];
+  for (int j = lane; j < stage_n; j += 32) {
+    const unsigned long long key = stage[j];
+    if (gbase + j < static_cast<unsigned long long>(M)) br[gbase + j] = key;
+    if constexpr (!TIE) gt += static_cast<uint32_t>(key >> 32) > tkey;
+  }
   if (gbase + stage_n > static_cast<unsigned long long>(M)) {
     over = true;
     if constexpr (TIE) {
@@ -203,7 +217,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
     const int64_t base = (tile - static_cast<int64_t>(ri) * tiles_per_row) * WT;
     if (ri != cur) {
       if (active) {
-        flush_stage<TIE>(a.st[row], stage, stage_n, br, a.M, over, tl, a.k, tkey);
+        flush_stage<TIE>(a.st[row], stage, stage_n, br, a.M, over, tl, a.k, tkey, gt);
         flush_row(a.st[row], gt, nan, late);
         active = false;
       }
@@ -240,7 +254,8 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
       if (!over && lane == 0) rge = ld_relaxed_u64(&a.st[row].R_ge);
     }
     float4 v[U];
-    uint64_t valid = ~0ull;
+    using LM = LaneMask<U>;
+    LM valid = ~LM(0);
     // A full tile holds only the row's elements; the row's element index of
     // the tile's position 0 is ebase.
     auto full_tile = [&]() { return UNAL ? base >= head && base + WT <= a.n + head : base + WT <= a.n; };
@@ -259,7 +274,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
           const int64_t i = base + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
           const bool ok = UNAL ? i >= head && i < a.n + head : i < a.n;
           f[c] = ok ? xr[i] : -INFINITY;
-          valid |= static_cast<uint64_t>(ok) << (u * 4 + c);
+          valid |= static_cast<LM>(ok) << (u * 4 + c);
         }
         v[u] = make_float4(f[0], f[1], f[2], f[3]);
       }
@@ -280,7 +295,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const float f = comp(v[u], c);
-          nan += (((valid >> (u * 4 + c)) & 1ull) && f != f);
+          nan += (((valid >> (u * 4 + c)) & 1u) && f != f);
         }
     }
     // Copies of tau in this tile (per lane), added to the block's counter.
@@ -296,7 +311,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
     };
     // Per lane: the elements >= tau and those > tau (the rest of ge are
     // copies of tau); ok: element e of the lane is in the row.
-    auto masks = [&](uint64_t& ge, uint64_t& gtm) {
+    auto masks = [&](LM& ge, LM& gtm) {
       ge = 0;
       gtm = 0;
       if (!hit) return;
@@ -307,11 +322,32 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
         for (int c = 0; c < 4; ++c) {
           const int e = u * 4 + c;
           const float f = comp(v[u], c);
-          const bool ok = (valid >> e) & 1ull;
-          ge |= static_cast<uint64_t>(ok && f >= tau) << e;
-          gtm |= static_cast<uint64_t>(ok && f > tau) << e;
+          const bool ok = (valid >> e) & 1u;
+          ge |= static_cast<LM>(ok && f >= tau) << e;
+          gtm |= static_cast<LM>(ok && f > tau) << e;
         }
       }
+    };
+    // The elements >= tau alone (the plain loop counts the x > tau among the
+    // staged keys when it flushes them).
+    auto ge_mask = [&]() {
+      LM ge = 0;
+      if (!hit) return ge;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (mu[u] < tau) continue;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int e = u * 4 + c;
+          ge |= static_cast<LM>(((valid >> e) & 1u) && comp(v[u], c) >= tau) << e;
+        }
+      }
+      return ge;
+    };
+    auto gt_count = [&]() {
+      LM ge, gtm;
+      masks(ge, gtm);
+      return popc_mask(gtm);
     };
     if constexpr (TIE) {
       if (!over && __shfl_sync(FULL_MASK, rge, 0) >= static_cast<unsigned long long>(a.M)) over = true;
@@ -331,58 +367,76 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
             cgt += f > tau;
           }
       } else {
-        uint64_t ge, gtm;
+        LM ge, gtm;
         masks(ge, gtm);
-        cge = static_cast<unsigned>(__popcll(ge));
-        cgt = static_cast<unsigned>(__popcll(gtm));
+        cge = popc_mask(ge);
+        cgt = popc_mask(gtm);
       }
       late += cge;
       gt += cgt;
       count_ties(cge - cgt);
       if constexpr (TIE) {
         if (__any_sync(FULL_MASK, cgt != 0)) {
-          uint64_t ge, gtm;
+          LM ge, gtm;
           masks(ge, gtm);
           tie_append_tile<U>(a.st[row], tl, a.k, gtm, v, ebase);
         }
       }
       continue;
     }
-    uint64_t ge, gtm;
-    masks(ge, gtm);
-    gt += static_cast<unsigned long long>(__popcll(gtm));
-    count_ties(static_cast<unsigned>(__popcll(ge) - __popcll(gtm)));
+    LM ge, gtm = 0;
+    if constexpr (TIE) {
+      masks(ge, gtm);
+      gt += popc_mask(gtm);
+      count_ties(popc_mask(ge) - popc_mask(gtm));
+    } else {
+      ge = ge_mask();
+    }
     // With the tie bookkeeping: this tile's x > tau that the buffer does not
     // keep, appended to the row's tie list at the end of the tile.
-    uint64_t dropm = 0;
+    LM dropm = 0;
     {
-      const unsigned cnt = __popcll(ge);
-      unsigned incl = cnt;
+      // The lane's passers go after those of the lanes below it: with at
+      // most one per lane (the usual case, even for large k) two ballots
+      // give every lane its place, otherwise a warp scan of the counts.
+      const unsigned cnt = popc_mask(ge);
+      const unsigned some = __ballot_sync(FULL_MASK, cnt != 0);
+      unsigned excl, tot;
+      if (!__any_sync(FULL_MASK, cnt > 1)) {
+        excl = static_cast<unsigned>(__popc(some & ((1u << lane) - 1u)));
+        tot = static_cast<unsigned>(__popc(some));
+      } else {
+        unsigned incl = cnt;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
-        if (lane >= o) incl += t;
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned t = __shfl_up_sync(FULL_MASK, incl, o);
+          if (lane >= o) incl += t;
+        }
+        excl = incl - cnt;
+        tot = __shfl_sync(FULL_MASK, incl, 31);
       }
-      const unsigned tot = __shfl_sync(FULL_MASK, incl, 31);
       if (tot != 0 && tot <= STAGE) {
         if (stage_n + static_cast<int>(tot) > STAGE)
-          flush_stage<TIE>(a.st[row], stage, stage_n, br, a.M, over, tl, a.k, tkey);
+          flush_stage<TIE>(a.st[row], stage, stage_n, br, a.M, over, tl, a.k, tkey, gt);
         if (over) {  // the flush filled the buffer: this tile's passers are only counted
           if (lane == 0) late += tot;
-          dropm = gtm;
+          if constexpr (TIE)
+            dropm = gtm;
+          else
+            gt += gt_count();
         } else {
           if (cnt) {
-            int pos = stage_n + static_cast<int>(incl - cnt);
+            // Each group's passers in turn (usually one): the component by
+            // its bit, then the key.
+            int pos = stage_n + static_cast<int>(excl);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-              if (((ge >> (u * 4)) & 15ull) == 0) continue;  // sparse passers: skip empty groups
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const int e = u * 4 + c;
-                if ((ge >> e) & 1ull) {
-                  const int64_t idx = ebase + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
-                  stage[pos++] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
-                }
+              unsigned nib = static_cast<unsigned>(ge >> (u * 4)) & 15u;
+              while (nib) {
+                const int c = __ffs(nib) - 1;
+                nib &= nib - 1u;
+                const int64_t idx = ebase + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
+                stage[pos++] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
               }
             }
           }
@@ -394,19 +448,20 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
         unsigned long long gbase = 0;
         if (lane == 0) gbase = atomicAdd(&a.st[row].R_ge, static_cast<unsigned long long>(tot));
         gbase = __shfl_sync(FULL_MASK, gbase, 0);
+        if constexpr (!TIE) gt += gt_count();
         if (gbase + tot > static_cast<unsigned long long>(a.M)) over = true;
-        unsigned long long pos = gbase + incl - cnt;
+        unsigned long long pos = gbase + excl;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int e = u * 4 + c;
-            if ((ge >> e) & 1ull) {
+            if ((ge >> e) & 1u) {
               if (pos < static_cast<unsigned long long>(a.M)) {
                 const int64_t idx = ebase + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
                 br[pos] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
               } else if constexpr (TIE) {
-                dropm |= gtm & (1ull << e);
+                dropm |= gtm & (LM(1) << e);
               }
               ++pos;
             }
@@ -417,7 +472,7 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
     if constexpr (TIE) tie_append_tile<U>(a.st[row], tl, a.k, dropm, v, ebase);
   }
   if (active) {
-    flush_stage<TIE>(a.st[row], stage, stage_n, br, a.M, over, tl, a.k, tkey);
+    flush_stage<TIE>(a.st[row], stage, stage_n, br, a.M, over, tl, a.k, tkey, gt);
     flush_row(a.st[row], gt, nan, late);
   }
 }

@@ -525,9 +525,26 @@ __device__ bool bucket_stage(const RadixSortArgs& a, int row, int64_t len, int64
   const unsigned long long* cst = s_keys + 2 * RS_SUB;
   const bool staged = hi - lo <= RS_SUB;
   auto key_at = [&](int64_t i) { return staged ? cst[i - lo] : __ldcg(keys + i); };
+  // The chunk in pieces of RS_SUB keys, RS_KMAX per thread loaded together
+  // (their L2 round trips overlap), then handled.
+  auto each_piece = [&](auto&& fn) {
+    for (int64_t b0 = lo; b0 < hi; b0 += RS_SUB) {
+      unsigned long long kv[RS_KMAX];
+#pragma unroll
+      for (int r = 0; r < RS_KMAX; ++r) {
+        const int64_t i = b0 + r * RS_THREADS + threadIdx.x;
+        kv[r] = i < hi ? key_at(i) : 0ull;
+      }
+      fn(kv, b0);
+    }
+  };
   for (int i = threadIdx.x; i < BK; i += RS_THREADS) h[i] = 0;
   __syncthreads();
-  for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS) atomicAdd(&h[bucket_of(key_at(i))], 1u);
+  each_piece([&](const unsigned long long(&kv)[RS_KMAX], int64_t b0) {
+#pragma unroll
+    for (int r = 0; r < RS_KMAX; ++r)
+      if (b0 + r * RS_THREADS + threadIdx.x < hi) atomicAdd(&h[bucket_of(kv[r])], 1u);
+  });
   __syncthreads();
   for (int i = threadIdx.x; i < BK; i += RS_THREADS)
     if (h[i]) atomicAdd(&bkr[i], h[i]);
@@ -614,10 +631,15 @@ __device__ bool bucket_stage(const RadixSortArgs& a, int row, int64_t len, int64
     }
   }
   __syncthreads();
-  for (int64_t i = lo + threadIdx.x; i < hi; i += RS_THREADS) {
-    const unsigned long long kk = key_at(i);
-    tmp_row[atomicAdd(&h[bucket_of(kk)], 1u)] = kk;
-  }
+  each_piece([&](const unsigned long long(&kv)[RS_KMAX], int64_t b0) {
+    unsigned slot[RS_KMAX];
+#pragma unroll
+    for (int r = 0; r < RS_KMAX; ++r)
+      if (b0 + r * RS_THREADS + threadIdx.x < hi) slot[r] = atomicAdd(&h[bucket_of(kv[r])], 1u);
+#pragma unroll
+    for (int r = 0; r < RS_KMAX; ++r)
+      if (b0 + r * RS_THREADS + threadIdx.x < hi) tmp_row[slot[r]] = kv[r];
+  });
   grid_sync(c, target += G, sm);
   if (sm.err) return true;
 
@@ -683,13 +705,13 @@ __device__ bool bucket_stage(const RadixSortArgs& a, int row, int64_t len, int64
 #pragma unroll
       for (int r = 0; r < RS_KMAX; ++r) {
         const int i = r * RS_THREADS + threadIdx.x;
-        if (i < P) s_keys[i] = kv[r];
+        if (i < P) s_keys[mswz(i)] = kv[r];
       }
     }
     __syncthreads();
     const unsigned long long* srt = block_merge_sort_desc(s_keys, mbuf, P);
     for (int i = threadIdx.x; i < L; i += RS_THREADS)
-      if (rs + i < a.k) emit_key(a, row, rs + i, srt[i]);
+      if (rs + i < a.k) emit_key(a, row, rs + i, srt[mswz(i)]);
     __syncthreads();
   }
   return true;
