@@ -344,15 +344,12 @@ int profk_exact(const float* x, int64_t n, int64_t k, float* out_vals, int64_t* 
  *   Limits: n <= 2^32 (longer rows return PROFK_ERR_UNSUPPORTED) and x
  *     4-byte aligned (else PROFK_ERR_UNSUPPORTED).  The array must hold, at
  *     the parameters (S, t, M) that profk_params gives, each part rounded up
- *     to 256 bytes: the row state (8.3 KB); on the sampling route a hash table
- *     of 8 x (the power of two >= 2D) bytes with D = S + 2r + 8 sqrt(r) + 256
- *     draws (r = S^2 / 2n, rounded up to a multiple of 4), 4D bytes of draws,
- *     4 ceil(D / 1024) bytes of counts, 8S bytes of sample and 8M bytes of
- *     candidate buffer; and 8 K bytes of selected keys, K = k for k <= 8192,
- *     else the power of two >= k.  A problem that needs more returns
- *     PROFK_ERR_SCRATCH before any device work.  If D draws hold fewer than S
- *     distinct indices (practically never), D doubles and the need is checked
- *     again, so such a call can return PROFK_ERR_SCRATCH after device work.
+ *     to 256 bytes: the row state (8.4 KB); on the sampling route 4S bytes of
+ *     sample indices, 4S bytes of sample keys and 8M bytes of candidate
+ *     buffer; and 8 K bytes of selected keys, K = k for k <= 8192, else the
+ *     power of two >= k.  A problem that needs more returns
+ *     PROFK_ERR_SCRATCH before any device work (n = 2^30 with k = 2^19
+ *     needs about 14 MB).
  *   Errors: as profk_topk, including PROFK_ERR_CUDA / PROFK_ERR_DEVICE_TIMEOUT
  *     when a device-side check of any step fails.
  *   Statistics: S, t, M, the counts, tau, attempts and path as profk_topk;

@@ -148,18 +148,6 @@ thread_local float t_stage_ms[6] = {-1.f, -1.f, -1.f, -1.f, -1.f, -1.f};
 
 // ---------------------------------------------------------------------------
 // Small kernels of the control flow.
-__global__ void k_attempt_init(RowState* st, const int* rows) {
-  pdl_trigger();
-  pdl_wait();
-  const int row = rows ? rows[blockIdx.x] : static_cast<int>(blockIdx.x);
-  RowState& S = st[row];
-  S.R_ge = 0;
-  S.R_gt = 0;
-  S.nan = 0;
-  S.distinct = 0;
-  S.error = 0;
-}
-
 // Start of an attempt for the listed rows: counters to zero and the
 // selection state ready for tau (rank t).  The control blocks of each row's
 // sampling (sample_ctl, sample_words 8-byte words per row) and refinement

@@ -254,7 +254,7 @@ struct SampleCtl {
   unsigned hist[3][HIST_BINS];  // tau pass histograms, summed over the chunks (t > TAU_CAND)
   uint32_t bucket[TAU_GATHER];  // the sample keys of tau's final bucket (t > TAU_CAND)
   unsigned bucket_n;
-  unsigned bar;                 // grid-barrier arrivals (t > TAU_CAND) or finished lists (t <= TAU_CAND)
+  unsigned bar;                 // grid-barrier arrivals (t > TAU_CAND)
   unsigned abort;               // set by a CTA whose wait gave up
   unsigned pad[61];
 };
