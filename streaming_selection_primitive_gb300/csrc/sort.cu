@@ -654,13 +654,13 @@ __device__ bool bucket_stage(const RadixSortArgs& a, int row, int64_t len, int64
       const int sz = static_cast<int>(be - bs);
       auto sort_emit = [&](auto tagE) {
         constexpr int E = decltype(tagE)::value;
-        unsigned long long kv[E];
+        unsigned long long kv[E];  // key lane * E + r of the bucket in kv[r]
 #pragma unroll
-        for (int r = 0; r < E; ++r) kv[r] = r * 32 + lane < sz ? __ldcg(tmp_row + bs + r * 32 + lane) : 0ull;
+        for (int r = 0; r < E; ++r) kv[r] = lane * E + r < sz ? __ldcg(tmp_row + bs + lane * E + r) : 0ull;
         warp_sort_desc<E>(kv);
 #pragma unroll
         for (int r = 0; r < E; ++r) {
-          const int q = r * 32 + lane;
+          const int q = lane * E + r;
           if (q < sz && bs + q < a.k) emit_key(a, row, bs + q, kv[r]);
         }
       };
