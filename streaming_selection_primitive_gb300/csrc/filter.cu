@@ -5,7 +5,8 @@
 //
 // GB300 design.  The pass is a pure HBM read stream, so the kernel keeps as
 // many 16-byte loads in flight as the memory system wants and does almost
-// nothing else on the common path, with no block-wide barrier anywhere:
+// nothing else on the common path, with no block-wide barrier after the
+// start (where each CTA gathers its rows' tau into shared memory):
 //  * persistent grid of resident CTAs; every warp strides on its own over
 //    warp tiles of 32 lanes x U float4 (4U values per lane), issuing U
 //    independent 128-bit non-allocating loads per lane;
@@ -180,13 +181,31 @@ __device__ __forceinline__ void flush_stage(RowState& S, unsigned long long* sta
   __syncwarp();
 }
 
+// What a warp needs at each change of row, in one word: ord(tau) (bits
+// 0-31), whether the row's sample held tau twice or more (bit 32: the
+// bookkeeping loop's row), whether an earlier attempt settled it (bit 33) and
+// the storage row (bits 34-63).  The kernel gathers the words of its rows
+// into shared memory once per CTA (one round trip), so that a row change
+// costs a shared-memory read rather than two dependent L2 loads; with many
+// rows a warp changes row every few tiles.
+constexpr int INFO_ROWS = 4096;  // rows whose words are cached (32 KB)
+
+__device__ __forceinline__ unsigned long long row_info(const FilterArgs& a, int ri) {
+  const int r = a.rows ? a.rows[ri] : ri;
+  const RowState& S = a.st[r];
+  return static_cast<unsigned long long>(S.tau_key) | (static_cast<unsigned long long>(S.tau_copies >= 2) << 32) |
+         (static_cast<unsigned long long>(settled_before(S, a.attempt)) << 33) |
+         (static_cast<unsigned long long>(r) << 34);
+}
+
 // The pass over the rows this loop takes: with the tie bookkeeping on
 // (a.block_eq), the rows whose sample holds tau more than once (a heavily
 // tied top, RowState::tau_copies >= 2) go to the TIE loop and the others to
 // the plain one; with it off the plain loop takes every row.  A row of the
 // other loop is skipped whole.
 template <int T, int U, bool TIE, bool UNAL>
-__device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long long* stage) {
+__device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long long* stage,
+                                            const unsigned long long* info, int cached) {
   static_assert(!(TIE && UNAL), "the tie bookkeeping counts per aligned block");
   static_assert(4 * U <= 64, "at most 64 elements per lane");
   constexpr int64_t WT = 32 * 4 * U;  // elements per warp tile
@@ -222,17 +241,17 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
         active = false;
       }
       cur = ri;
-      const int nrow = a.rows ? a.rows[ri] : ri;
-      if ((a.block_eq && (a.st[nrow].tau_copies >= 2) != TIE) || settled_before(a.st[nrow], a.attempt)) {
+      const unsigned long long w = ri < cached ? info[ri] : row_info(a, ri);
+      if ((a.block_eq && static_cast<bool>((w >> 32) & 1ull) != TIE) || ((w >> 33) & 1ull)) {
         // The other loop's row, or one that an earlier attempt settled: on
         // to this warp's first tile past it.
         const int64_t next = static_cast<int64_t>(ri + 1) * tiles_per_row;
         tile += (next - tile + nwarps - 1) / nwarps * nwarps - nwarps;
         continue;
       }
-      row = nrow;
+      row = static_cast<int>(w >> 34);
       active = true;
-      tkey = a.st[row].tau_key;
+      tkey = static_cast<uint32_t>(w);
       tau = key_to_float(tkey);
       xr = a.x + static_cast<int64_t>(row) * a.ld;
       if constexpr (UNAL) {
@@ -483,10 +502,14 @@ template <int T, int U, bool UNAL>
 __global__ void __launch_bounds__(T, 3) k_filter(FilterArgs a) {
   pdl_wait();
   __shared__ unsigned long long s_stage[T / 32][STAGE];
+  extern __shared__ unsigned long long s_info[];  // the first `cached` rows' words (row_info)
+  const int cached = a.nrows < INFO_ROWS ? a.nrows : INFO_ROWS;
+  for (int i = threadIdx.x; i < cached; i += T) s_info[i] = row_info(a, i);
+  __syncthreads();
   unsigned long long* stage = s_stage[threadIdx.x >> 5];
-  filter_rows<T, U, false, UNAL>(a, stage);
+  filter_rows<T, U, false, UNAL>(a, stage, s_info, cached);
   if constexpr (!UNAL) {
-    if (a.block_eq) filter_rows<T, U, true, false>(a, stage);
+    if (a.block_eq) filter_rows<T, U, true, false>(a, stage, s_info, cached);
   }
 }
 
@@ -519,10 +542,11 @@ void launch_filter(const FilterArgs& args, cudaStream_t stream) {
   int grid = a.grid;
   if (ctas < grid) grid = static_cast<int>(ctas);
   if (grid < 1) grid = 1;
+  const size_t info = sizeof(unsigned long long) * static_cast<size_t>(a.nrows < INFO_ROWS ? a.nrows : INFO_ROWS);
   if (unaligned)
-    launch_kernel(k_filter<FT, FU, true>, grid, FT, 0, stream, a);
+    launch_kernel(k_filter<FT, FU, true>, grid, FT, info, stream, a);
   else
-    launch_kernel(k_filter<FT, FU, false>, grid, FT, 0, stream, a);
+    launch_kernel(k_filter<FT, FU, false>, grid, FT, info, stream, a);
 }
 
 }  // namespace profk
