@@ -230,10 +230,35 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
   unsigned* beq = nullptr;           // the row's per-block counts of tau
   uint32_t tkey = 0;
   unsigned long long gt = 0, nan = 0, late = 0;
-  for (int64_t tile = static_cast<int64_t>(blockIdx.x) * (T / 32) + (threadIdx.x >> 5); tile < total;
-       tile += nwarps) {
-    const int ri = static_cast<int>(tile / tiles_per_row);
-    const int64_t base = (tile - static_cast<int64_t>(ri) * tiles_per_row) * WT;
+  // The warps' tiles.  One row: warp w takes tiles w, w + nwarps, ...
+  // (the whole grid sweeps the row front to back).  Several rows: each warp
+  // takes one contiguous range of tiles (the rows in order), so that it
+  // changes row at most a few times however short the rows are (measured:
+  // 256 rows of 2^22, 0.719 -> 0.605 ms; a single 2^30 row sweeps 2.6 %
+  // faster with the strided order).
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * (T / 32) + (threadIdx.x >> 5);
+  const bool one = a.nrows == 1;
+  const int tpr = static_cast<int>(tiles_per_row);  // at most 2^22 + 1
+  const int step = one ? static_cast<int>(nwarps) : 1;
+  int64_t left;  // tiles still to take
+  int ri, tir;   // the tile's row (index in the launch) and its index in that row
+  if (one) {
+    left = wid < total ? (total - wid + nwarps - 1) / nwarps : 0;
+    ri = 0;
+    tir = static_cast<int>(wid);
+  } else {
+    const int64_t per = (total + nwarps - 1) / nwarps;
+    const int64_t t0 = wid * per < total ? wid * per : total;
+    left = (t0 + per < total ? t0 + per : total) - t0;
+    ri = static_cast<int>(t0 / tiles_per_row);
+    tir = static_cast<int>(t0 - static_cast<int64_t>(ri) * tiles_per_row);
+  }
+  for (; left > 0; --left, tir += step) {
+    if (tir >= tpr) {  // several rows only: on into the next row
+      ++ri;
+      tir = 0;
+    }
+    const int64_t base = static_cast<int64_t>(tir) * WT;
     if (ri != cur) {
       if (active) {
         flush_stage<TIE>(a.st[row], stage, stage_n, br, a.M, over, tl, a.k, tkey, gt);
@@ -244,9 +269,10 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
       const unsigned long long w = ri < cached ? info[ri] : row_info(a, ri);
       if ((a.block_eq && static_cast<bool>((w >> 32) & 1ull) != TIE) || ((w >> 33) & 1ull)) {
         // The other loop's row, or one that an earlier attempt settled: on
-        // to this warp's first tile past it.
-        const int64_t next = static_cast<int64_t>(ri + 1) * tiles_per_row;
-        tile += (next - tile + nwarps - 1) / nwarps * nwarps - nwarps;
+        // to the next row (the loop's step moves past this row's last tile).
+        if (one) break;
+        left -= tpr - 1 - tir;
+        tir = tpr - 1;
         continue;
       }
       row = static_cast<int>(w >> 34);
