@@ -222,8 +222,8 @@ typedef enum profk_option {
   PROFK_OPT_MAX_SEGMENT = 9,   /* rows longer than this are split into segments (see profk_topk);
                                   a multiple of 4, >= 2^16; 0 = 2^32 [0] */
   PROFK_OPT_SAMPLER = 10,      /* kernels of steps 1-2 (sample and tau): PROFK_SAMPLER_AUTO [0],
-                                  _GRID or _STEPS (GRID falls back to the automatic choice
-                                  where it cannot take the problem) */
+                                  _GRID, _STEPS or _LISTS (GRID and LISTS fall back to the
+                                  automatic choice where they cannot take the problem) */
   PROFK_OPT_WAIT_TEST = 11,    /* test of the path taken when a bounded device wait runs out [0]:
                                   PROFK_WAIT_TEST_SAMPLER, _REFINE or _SORT makes the first grid barrier
                                   of that persistent kernel (the sampler's grid form, the grid
@@ -251,15 +251,21 @@ typedef enum profk_option {
 #define PROFK_WAIT_TEST_SAMPLER 1
 #define PROFK_WAIT_TEST_REFINE 2
 #define PROFK_WAIT_TEST_SORT 3
-/* Forms of the sampling kernels (PROFK_OPT_SAMPLER); both give the same
+/* Forms of the sampling kernels (PROFK_OPT_SAMPLER); all give the same
  * sample and tau.  GRID: one persistent kernel (all CTAs resident), each CTA
  * taking up to 1024 sample positions; tau from per-CTA candidate lists that
  * one CTA waits for (t <= 8) or from passes whose CTAs meet at grid
- * barriers (larger t).  STEPS: one thread per sample position, then a radix
- * selection of tau; taken when the rows' shares of the SMs are too small. */
+ * barriers (larger t).  LISTS (t <= 8): CTAs of up to 2048 positions of one
+ * row, each listing its t largest sampled values; the row's last CTA to
+ * finish selects tau among the lists, and no CTA waits for another; taken
+ * for t <= 8 when the rows' shares of the SMs are too small for GRID.
+ * STEPS: one thread per sample position, then a radix selection of tau; the
+ * remaining cases.  A form that cannot take the problem falls back to the
+ * automatic choice. */
 #define PROFK_SAMPLER_AUTO 0
 #define PROFK_SAMPLER_GRID 1
 #define PROFK_SAMPLER_STEPS 2
+#define PROFK_SAMPLER_LISTS 3
 int profk_set_option(int option, int64_t value);
 int64_t profk_get_option(int option);
 

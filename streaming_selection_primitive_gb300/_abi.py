@@ -28,7 +28,7 @@ OPT_FILTER_CTAS_PER_SM = 7
 OPT_PDL = 8
 OPT_MAX_SEGMENT = 9
 OPT_SAMPLER = 10
-SAMPLER_AUTO, SAMPLER_GRID, SAMPLER_STEPS = 0, 1, 2
+SAMPLER_AUTO, SAMPLER_GRID, SAMPLER_STEPS, SAMPLER_LISTS = 0, 1, 2, 3
 OPT_WAIT_TEST = 11
 OPT_SPECULATIVE = 12
 WAIT_TEST_OFF, WAIT_TEST_SAMPLER, WAIT_TEST_REFINE, WAIT_TEST_SORT = 0, 1, 2, 3

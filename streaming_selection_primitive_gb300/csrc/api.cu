@@ -503,24 +503,29 @@ void fill_stats_params(profk_stats* s, const Params& P) {
 }
 
 
-// Kernels of steps 1-2 for ng rows of S sample positions each: the
-// step-by-step ones when PROFK_OPT_SAMPLER asks for them, else the
-// persistent grid kernel where its CTAs' shares of the sample fit their
-// registers, else the step-by-step ones.
-enum class Sampler { Grid, Steps };
+// Kernels of steps 1-2 for ng rows of S sample positions each and tau of
+// rank t: the form PROFK_OPT_SAMPLER asks for where it takes the problem;
+// otherwise the persistent grid kernel where its CTAs' shares of the sample
+// fit their registers, else the lists kernel for t <= 8, else the
+// step-by-step ones.
+enum class Sampler { Grid, Lists, Steps };
 
-Sampler choose_sampler(int64_t S, int64_t ng) {
-  if (g_opt[PROFK_OPT_SAMPLER].load() == PROFK_SAMPLER_STEPS) return Sampler::Steps;
-  return sample_tau_fits(S, static_cast<int>(ng)) ? Sampler::Grid : Sampler::Steps;
+Sampler choose_sampler(int64_t S, int64_t ng, unsigned long long t) {
+  const int64_t opt = g_opt[PROFK_OPT_SAMPLER].load();
+  if (opt == PROFK_SAMPLER_STEPS) return Sampler::Steps;
+  const bool lists = sample_lists_fits(S, t);
+  if (opt == PROFK_SAMPLER_LISTS && lists) return Sampler::Lists;
+  if (sample_tau_fits(S, static_cast<int>(ng))) return Sampler::Grid;
+  return lists ? Sampler::Lists : Sampler::Steps;
 }
 
 // Attempts enqueued after the first attempt of all `rows`, before the host
 // reads the check (PROFK_OPT_SPECULATIVE): within max_attempts, and only where
-// the grid sampler takes the rows (the step-by-step kernels do not leave
-// settled rows alone).
+// the grid or the lists sampler takes the rows (the step-by-step kernels do
+// not leave settled rows alone).
 int speculative_attempts(const Params& P, int64_t rows, int max_attempts) {
   const int64_t want = g_opt[PROFK_OPT_SPECULATIVE].load();
-  if (want <= 0 || max_attempts <= 1 || choose_sampler(P.S, rows) != Sampler::Grid) return 0;
+  if (want <= 0 || max_attempts <= 1 || choose_sampler(P.S, rows, P.t) == Sampler::Steps) return 0;
   return static_cast<int>(std::min<int64_t>(want, max_attempts - 1));
 }
 
@@ -539,7 +544,7 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
                             float* out_vals, int64_t* out_idx, cudaStream_t stream, cudaEvent_t* ev,
                             bool tie_book, bool tie_exit) {
   RowState* st = at<RowState>(ws, L.off_state);
-  const Sampler form = choose_sampler(P.S, ng);
+  const Sampler form = choose_sampler(P.S, ng, P.t);
   // Reset CTAs per row: a few 16-byte stores per thread of 256.
   constexpr unsigned rb = 8;
   // The refinement's control blocks start every attempt at zero.
@@ -556,7 +561,8 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
                                 : nullptr;
   // The grid sampler with the candidate lists (small t) does the attempt's
   // set-up itself; the other forms get the reset kernel first.
-  const bool fused_setup = form == Sampler::Grid && P.t <= sample_tau_setup_max_t();
+  const bool fused_setup =
+      form == Sampler::Lists || (form == Sampler::Grid && P.t <= static_cast<uint64_t>(sample_tau_setup_max_t()));
   if (!fused_setup)
     launch_kernel(k_attempt_reset, dim3(rb, ng), 256, 0, stream, gl, st, static_cast<unsigned long long>(P.t), ref_ctl,
                   ref_words, at<unsigned long long>(ws, L.off_sctl), static_cast<int>(sample_tau_ctl_bytes() / 8),
@@ -575,8 +581,10 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
     sa.zero_nb = nb;
   }
   cudaError_t e = cudaSuccess;
-  if (form == Sampler::Grid) {
-    e = launch_sample_tau(sa, at<char>(ws, L.off_sctl), rows, stream);
+  if (form != Sampler::Steps) {
+    sa.store_sample = false;  // nothing after this step reads the sample
+    e = form == Sampler::Grid ? launch_sample_tau(sa, at<char>(ws, L.off_sctl), rows, stream)
+                              : launch_sample_lists(sa, at<char>(ws, L.off_sctl), rows, stream);
     if (e != cudaSuccess) return e;
     if (ev) cudaEventRecord(ev[1], stream);
   } else {
@@ -1328,7 +1336,7 @@ size_t profk_workspace_size(int64_t rows, int64_t n, int64_t k, double eps) {
 int profk_set_option(int option, int64_t value) {
   if (option < 0 || option >= PROFK_OPT__COUNT) return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_PARAM_MODE && (value < 0 || value > 3)) return PROFK_ERR_INVALID;
-  if (option == PROFK_OPT_SAMPLER && (value < PROFK_SAMPLER_AUTO || value > PROFK_SAMPLER_STEPS))
+  if (option == PROFK_OPT_SAMPLER && (value < PROFK_SAMPLER_AUTO || value > PROFK_SAMPLER_LISTS))
     return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_WAIT_TEST && (value < PROFK_WAIT_TEST_OFF || value > PROFK_WAIT_TEST_SORT))
     return PROFK_ERR_INVALID;
@@ -1381,9 +1389,12 @@ int profk_sample(const float* x, int64_t n, int64_t S, uint64_t seed, int64_t ro
                   at<uint32_t>(c.ws, L.off_skeys), false, 1ull, row};
     // The main path's kernel for one row (it also finds a tau, of rank 1
     // here, which is not used), else the step-by-step one.
-    if (choose_sampler(S, 1) == Sampler::Grid) {
+    const Sampler form = choose_sampler(S, 1, 1);
+    if (form == Sampler::Grid) {
       PK_CHECK(cudaMemsetAsync(at<char>(c.ws, L.off_sctl), 0, sample_tau_ctl_bytes(), stream));
       PK_CHECK(launch_sample_tau(sa, at<char>(c.ws, L.off_sctl), 1, stream));
+    } else if (form == Sampler::Lists) {
+      PK_CHECK(launch_sample_lists(sa, at<char>(c.ws, L.off_sctl), 1, stream));
     } else {
       launch_sample_rows(sa, row, stream);
     }

@@ -82,6 +82,16 @@ __device__ __forceinline__ void flush_row(RowState& S, unsigned long long& gt, u
 
 constexpr int STAGE = 128;  // staged passer keys per warp
 
+// The L2 prefetch before tau (prefetch_first_tiles): about this many MB of
+// the tiles that the warps take first, every PF_STRIDE-th of a warp's tiles.
+#ifndef PROFK_FILTER_PREFETCH_MB
+#define PROFK_FILTER_PREFETCH_MB 64
+#endif
+#ifndef PROFK_FILTER_PREFETCH_STRIDE
+#define PROFK_FILTER_PREFETCH_STRIDE 2
+#endif
+constexpr int PF_STRIDE = PROFK_FILTER_PREFETCH_STRIDE;
+
 // A lane's mask over its 4U elements of a warp tile: 32 bits when they fit
 // (U <= 8, the shipped shape), else 64.
 template <int U>
@@ -522,10 +532,60 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
   }
 }
 
+__device__ __forceinline__ void prefetch_l2(const char* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Before tau is known.  With programmatic dependent launch the filter's
+// first CTAs become resident beside the sampler, whose work is a chain of
+// dependent steps that leaves HBM nearly idle; those CTAs (the first
+// pf_ctas) ask L2 for pf_tiles warp tiles of every warp of the grid, one
+// bulk prefetch per tile: every PF_STRIDE-th of the tiles filter_rows hands
+// the warp first, so that in the pass's first rounds each warp alternates a
+// tile on chip with one from HBM and HBM stays busy.  A prefetch is a hint:
+// nothing waits for it, and it covers only the row's own elements (rounded
+// inward to 16 bytes).  Measured on 2^26 inputs: 3-5 us less per call.
+template <int T, int U, bool UNAL>
+__device__ __forceinline__ void prefetch_first_tiles(const FilterArgs& a) {
+  constexpr int64_t WT = 32 * 4 * U;
+  const int64_t C = a.pf_ctas;
+  if (static_cast<int64_t>(blockIdx.x) >= C) return;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (T / 32);
+  const int64_t tpr = (a.n + (UNAL ? 3 : 0) + WT - 1) / WT;
+  const int64_t total = tpr * a.nrows;
+  const int64_t per = (total + nwarps - 1) / nwarps;
+  const int64_t F = a.pf_tiles;
+  const int64_t w0 = blockIdx.x * nwarps / C, w1 = (blockIdx.x + 1) * nwarps / C;
+  const int64_t items = (w1 - w0) * F;
+  for (int64_t it = threadIdx.x; it < items; it += T) {
+    const int64_t w = w0 + it / F, f = it % F;
+    int64_t tile;
+    if (a.nrows == 1) {
+      tile = w + f * PF_STRIDE * nwarps;
+    } else {
+      if (f * PF_STRIDE >= per) continue;
+      tile = w * per + f * PF_STRIDE;
+    }
+    if (tile >= total) continue;
+    const int64_t ri = tile / tpr, tir = tile - ri * tpr;
+    const int r = a.rows ? a.rows[ri] : static_cast<int>(ri);
+    const uintptr_t row0 = reinterpret_cast<uintptr_t>(a.x + static_cast<int64_t>(r) * a.ld);
+    const uintptr_t row1 = row0 + static_cast<uintptr_t>(a.n) * 4u;
+    const uintptr_t head = UNAL ? ((row0 >> 2) & 3u) : 0u;
+    uintptr_t lo = row0 - head * 4u + static_cast<uintptr_t>(tir) * WT * 4u;
+    uintptr_t hi = lo + WT * 4u;
+    const uintptr_t first = (row0 + 15u) & ~uintptr_t(15), last = row1 & ~uintptr_t(15);
+    if (lo < first) lo = first;
+    if (hi > last) hi = last;
+    if (hi > lo) prefetch_l2(reinterpret_cast<const char*>(lo), static_cast<unsigned>(hi - lo));
+  }
+}
+
 // UNAL: some row is off the 16-byte grid (its own instantiation, so that the
 // aligned kernel's code is that of a kernel without the head).
 template <int T, int U, bool UNAL>
 __global__ void __launch_bounds__(T, 3) k_filter(FilterArgs a) {
+  if (a.pf_tiles) prefetch_first_tiles<T, U, UNAL>(a);
   pdl_wait();
   __shared__ unsigned long long s_stage[T / 32][STAGE];
   extern __shared__ unsigned long long s_info[];  // the first `cached` rows' words (row_info)
@@ -568,6 +628,16 @@ void launch_filter(const FilterArgs& args, cudaStream_t stream) {
   int grid = a.grid;
   if (ctas < grid) grid = static_cast<int>(ctas);
   if (grid < 1) grid = 1;
+  // The L2 prefetch before tau (prefetch_first_tiles): the first CTAs, one
+  // per SM (those that fit beside the sampler's), warm about
+  // PROFK_FILTER_PREFETCH_MB of the tiles that every warp takes first
+  // (every PF_STRIDE-th of them).
+  const int64_t nwarps = static_cast<int64_t>(grid) * (FT / 32);
+  const int64_t per_warp = (warp_tiles + nwarps - 1) / nwarps;
+  int64_t pf = (static_cast<int64_t>(PROFK_FILTER_PREFETCH_MB) << 20) / (nwarps * WT * 4);
+  if (pf > (per_warp + PF_STRIDE - 1) / PF_STRIDE) pf = (per_warp + PF_STRIDE - 1) / PF_STRIDE;
+  a.pf_tiles = static_cast<int>(pf);
+  a.pf_ctas = sms() < grid ? sms() : grid;
   const size_t info = sizeof(unsigned long long) * static_cast<size_t>(a.nrows < INFO_ROWS ? a.nrows : INFO_ROWS);
   if (unaligned)
     launch_kernel(k_filter<FT, FU, true>, grid, FT, info, stream, a);

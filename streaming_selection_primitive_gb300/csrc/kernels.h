@@ -95,6 +95,10 @@ struct SampleArgs {
   int zero_words = 0;
   unsigned* zero_eq = nullptr;
   int64_t zero_nb = 0;
+  // Whether the persistent and the lists forms store sidx and skeys (the
+  // step-by-step form always does: its tau selection reads skeys); the main
+  // path needs neither.
+  bool store_sample = true;
 };
 // One thread per sample position: indices, keys and RowState::distinct (= S).
 void launch_sample(const SampleArgs& a, cudaStream_t stream);
@@ -119,6 +123,16 @@ bool sample_tau_fits(int64_t S, int nrows);
 // Largest t for which launch_sample_tau also does the attempt's set-up (and
 // needs no zeroed control block of its own).
 int64_t sample_tau_setup_max_t();
+// The lists form of steps 1 and 2, for t <= sample_tau_setup_max_t() and any
+// number of rows: CTAs of 256 threads take up to 2048 consecutive sample
+// positions of one row each, list their t largest keys, and the row's last
+// CTA to finish selects tau among the lists; no CTA waits for another, so
+// the launch needs no co-residency.  It does the attempt's set-up like the
+// persistent form (SampleArgs::zero_ctl), and uses the same scratch
+// (sample_tau_scratch_bytes), which needs no initialisation.  Rows that an
+// earlier attempt settled are left alone.
+bool sample_lists_fits(int64_t S, unsigned long long t);
+cudaError_t launch_sample_lists(const SampleArgs& a, void* scratch, int64_t total_rows, cudaStream_t stream);
 
 // Exact top-k of short rows, one CTA per row (rows.cu): outputs of each listed
 // row (or rows 0 .. nrows-1) sorted, RowState::sel_nan set to the row's NaN
@@ -302,6 +316,10 @@ struct FilterArgs {
   int64_t tie_stride = 0;
   int64_t k = 0;
   int attempt = 0;  // rows settled by an earlier attempt are left alone (settled_before)
+  // Set by launch_filter: the CTAs that warm L2 with the first tiles of every
+  // warp before tau is known, and how many tiles per warp.
+  int pf_ctas = 0;
+  int pf_tiles = 0;
 };
 // The filter pass over the listed rows.  x must be 4-byte aligned.  When some
 // row does not start on a 16-byte boundary (x 4-byte aligned only, or a row

@@ -17,11 +17,15 @@
 // therefore distinct by construction and each is computed on its own: no
 // table of drawn values, no repeat removal, no ordering across threads.
 //
-// Two forms:
+// Three forms:
 //  * k_sample_draw (one thread per sample position, all rows of a launch):
 //    the sample and its keys, optionally with the first 11-bit pass of the
 //    tau selection fused (the last block picks the digit; launch_select
 //    finishes);
+//  * k_sample_lists (t <= TAU_CAND, rows too many for the persistent form):
+//    CTAs of 256 threads take up to 2048 positions of one row, list their t
+//    largest keys, and the row's last CTA to finish selects tau among the
+//    lists, with no CTA waiting for another;
 //  * k_sample_tau (the main path, one 512-thread CTA per SM and contiguous
 //    chunk of at most 1024 sample positions, all CTAs of the launch resident
 //    together): the sample, then tau.  For t <= TAU_CAND (8) every CTA
@@ -272,6 +276,9 @@ struct SampleCand {
   uint32_t kth[MAX_CHUNKS];
   uint32_t extra[MAX_CHUNKS];
   unsigned long long flag[MAX_CHUNKS];
+  // The lists form: (launch tag << 32) | CTAs of the row arrived so far.
+  unsigned long long arrive;
+  unsigned long long pad;
 };
 
 namespace {
@@ -314,7 +321,7 @@ struct SelSmem {
 // the rank left (at most want rounds).  Returns the key; *above = keys
 // strictly larger, *eq = keys equal to it.  The block must hold at least
 // want valid keys.
-template <class EachKey>
+template <int NT = ST_THREADS, class EachKey>
 __device__ __forceinline__ uint32_t block_select_small(EachKey each_key, unsigned long long want, SelSmem& sm,
                                                        unsigned long long* above, unsigned long long* eq) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -332,7 +339,7 @@ __device__ __forceinline__ uint32_t block_select_small(EachKey each_key, unsigne
     __syncthreads();
     m = 0;
 #pragma unroll
-    for (int w = 0; w < ST_THREADS / 32; ++w) m = sm.wmax[w] > m ? sm.wmax[w] : m;
+    for (int w = 0; w < NT / 32; ++w) m = sm.wmax[w] > m ? sm.wmax[w] : m;
     unsigned c = 0;
     each_key([&](uint32_t key, bool v) { c += (v && (first || key < bound) && key == m) ? 1u : 0u; });
     c = __reduce_add_sync(FULL_MASK, c);
@@ -340,7 +347,7 @@ __device__ __forceinline__ uint32_t block_select_small(EachKey each_key, unsigne
     __syncthreads();
     unsigned long long cnt = 0;
 #pragma unroll
-    for (int w = 0; w < ST_THREADS / 32; ++w) cnt += sm.wcnt[w];
+    for (int w = 0; w < NT / 32; ++w) cnt += sm.wcnt[w];
     __syncthreads();  // wmax and wcnt are rewritten by the next round
     result = m;
     *eq = cnt;
@@ -351,6 +358,44 @@ __device__ __forceinline__ uint32_t block_select_small(EachKey each_key, unsigne
   }
   *above = want0 - want;
   return result;
+}
+
+// The attempt's set-up (see SampleArgs::zero_ctl), done by the sampler in
+// place of a reset kernel: the first CTA of the row zeroes the row state,
+// every CTA its share of the refinement's control block and of the tie
+// step's block counts.  The kernels that use them come later on the stream;
+// the CTA that writes tau does so after chunk 0 has published its list.
+template <int NT>
+__device__ __forceinline__ void attempt_setup(const SampleArgs& a, RowState& S, int row, int64_t chunk, int64_t G) {
+  const int tid = threadIdx.x;
+  const int64_t gt = chunk * NT + tid, gs = G * NT;
+  if (a.zero_ctl) {
+    ulonglong2* zc = reinterpret_cast<ulonglong2*>(a.zero_ctl + static_cast<int64_t>(row) * a.zero_words);
+    for (int64_t i = gt; i < a.zero_words / 2; i += gs) zc[i] = make_ulonglong2(0ull, 0ull);
+  }
+  if (a.zero_eq) {
+    unsigned* ze = a.zero_eq + static_cast<int64_t>(row) * a.zero_nb;
+    for (int64_t i = gt; i < a.zero_nb; i += gs) ze[i] = 0u;
+  }
+  if (chunk == 0) {
+    for (int b = tid; b < HIST_BINS; b += NT) S.hist[b] = 0u;
+    if (tid == 0) {
+      S.R_ge = 0;
+      S.R_gt = 0;
+      S.nan = 0;
+      S.error = 0;
+      S.sel_rank = a.t;
+      S.sel_above = 0;
+      S.sel_bucket = 0;
+      S.sel_thresh = 0;
+      S.sel_nan = 0;
+      S.done_blocks = 0;
+      S.compact_count = 0;
+      S.skip = 0;
+      S.tie_gt = 0;
+      S.settled = 0;
+    }
+  }
 }
 
 template <bool CAND>
@@ -374,40 +419,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     s_fail = 0;
     s_pos = 0;
   }
-  if constexpr (CAND) {
-    // The attempt's set-up (see SampleArgs::zero_ctl): the first CTA the row
-    // state, every CTA its share of the refinement's control block and of
-    // the tie step's block counts.  The kernels that use them come later on
-    // the stream.
-    const int64_t gt = chunk * ST_THREADS + tid, gs = G * ST_THREADS;
-    if (a.zero_ctl) {
-      ulonglong2* zc = reinterpret_cast<ulonglong2*>(a.zero_ctl + static_cast<int64_t>(row) * a.zero_words);
-      for (int64_t i = gt; i < a.zero_words / 2; i += gs) zc[i] = make_ulonglong2(0ull, 0ull);
-    }
-    if (a.zero_eq) {
-      unsigned* ze = a.zero_eq + static_cast<int64_t>(row) * a.zero_nb;
-      for (int64_t i = gt; i < a.zero_nb; i += gs) ze[i] = 0u;
-    }
-    if (chunk == 0) {
-      for (int b = tid; b < HIST_BINS; b += ST_THREADS) S.hist[b] = 0u;
-      if (tid == 0) {
-        S.R_ge = 0;
-        S.R_gt = 0;
-        S.nan = 0;
-        S.error = 0;
-        S.sel_rank = a.t;
-        S.sel_above = 0;
-        S.sel_bucket = 0;
-        S.sel_thresh = 0;
-        S.sel_nan = 0;
-        S.done_blocks = 0;
-        S.compact_count = 0;
-        S.skip = 0;
-        S.tie_gt = 0;
-        S.settled = 0;
-      }
-    }
-  }
+  if constexpr (CAND) attempt_setup<ST_THREADS>(a, S, row, chunk, G);
   round_keys(a.seed, static_cast<uint64_t>(row + a.key_row0), static_cast<uint64_t>(a.attempt), s_keys);
   __syncthreads();
   const int limit = wait_limit(a.wait);
@@ -439,7 +451,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
 #pragma unroll
   for (int h = 0; h < ST_HELD; ++h) {
     kh[h] = ord_key(vh[h]);
-    if (mh[h]) {
+    if (mh[h] && a.store_sample) {
       const int64_t o = orow + lo + static_cast<int64_t>(h) * ST_THREADS + tid;
       a.sidx[o] = static_cast<uint32_t>(xs[h]);
       a.skeys[o] = kh[h];
@@ -657,6 +669,150 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
 }
 #undef ST_LEAVE_IF_GAVE_UP
 
+// ---------------------------------------------------------------------------
+// The lists form (t <= TAU_CAND, any number of rows).  A CTA of LS_THREADS
+// threads takes LS_THREADS x H consecutive sample positions of one row
+// (thread tid: positions lo + h LS_THREADS + tid, so that the H Feistel
+// chains of a thread interleave), lists its t largest keys as the
+// persistent form's chunks do, and arrives on the row's arrival word; the
+// CTA that arrives last selects tau among the row's lists.  No CTA waits for
+// another.  The arrival word holds (launch tag << 32) | arrivals: the first
+// arrival of a launch finds another tag and starts the count at 1, so the
+// word needs no zeroing, and a CTA whose compare-and-swap fails has seen
+// another CTA's arrival succeed, which bounds its retries by the row's CTAs.
+constexpr int LS_THREADS = 256;
+constexpr int LS_MAX_H = 8;
+
+template <int H>
+__global__ void __launch_bounds__(LS_THREADS) k_sample_lists(SampleArgs a, SampleCand* cands,
+                                                            unsigned long long epoch) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ SelSmem sm;
+  __shared__ uint64_t s_keys[FEISTEL_ROUNDS];
+  __shared__ uint32_t s_cand[MAX_CHUNKS * TAU_CAND];  // the last CTA: every list of the row
+  __shared__ unsigned s_pos;
+  __shared__ int s_fail, s_last;
+  const int row = launch_row(a.rows);
+  RowState& S = a.st[row];
+  const int tid = threadIdx.x;
+  const int64_t G = gridDim.x, chunk = blockIdx.x;
+  if (settled_before(S, a.attempt)) return;  // every CTA of the row leaves before arriving
+  if (tid == 0) {
+    s_pos = 0;
+    s_fail = 0;
+    s_last = 0;
+  }
+  attempt_setup<LS_THREADS>(a, S, row, chunk, G);
+  round_keys(a.seed, static_cast<uint64_t>(row + a.key_row0), static_cast<uint64_t>(a.attempt), s_keys);
+  __syncthreads();
+  const int64_t lo = chunk * (static_cast<int64_t>(LS_THREADS) * H);
+  const float* xr = a.x + static_cast<int64_t>(row) * a.ld;
+  const int64_t orow = static_cast<int64_t>(row) * a.S;
+  uint64_t xs[H];
+  bool walk[H], mh[H];
+#pragma unroll
+  for (int h = 0; h < H; ++h) {
+    const int64_t j = lo + static_cast<int64_t>(h) * LS_THREADS + tid;
+    xs[h] = static_cast<uint64_t>(j);
+    walk[h] = mh[h] = j < a.S;
+  }
+  if (!permute<H>(xs, walk, a.n, domain_bits(a.n), s_keys)) s_fail = 1;
+  float vh[H];
+#pragma unroll
+  for (int h = 0; h < H; ++h) vh[h] = mh[h] ? xr[xs[h]] : 0.f;  // the gathers, in flight together
+  uint32_t kh[H];
+#pragma unroll
+  for (int h = 0; h < H; ++h) {
+    kh[h] = ord_key(vh[h]);
+    if (mh[h] && a.store_sample) {
+      const int64_t o = orow + lo + static_cast<int64_t>(h) * LS_THREADS + tid;
+      a.sidx[o] = static_cast<uint32_t>(xs[h]);
+      a.skeys[o] = kh[h];
+    }
+  }
+  if (chunk == 0 && tid == 0) S.distinct = static_cast<unsigned>(a.S < 0xffffffffll ? a.S : 0xffffffffll);
+  auto each_key = [&](auto&& fn) {
+#pragma unroll
+    for (int h = 0; h < H; ++h) fn(kh[h], mh[h]);
+  };
+  const unsigned long long t = a.t;
+  SampleCand& cd = cands[row];
+  // The chunk's t largest keys: those above its t-th largest K and copies of
+  // K to make t (all its keys, padded with zero keys, when it has fewer).
+  const int64_t cnt = (a.S - lo < static_cast<int64_t>(LS_THREADS) * H) ? a.S - lo : static_cast<int64_t>(LS_THREADS) * H;
+  const bool short_chunk = cnt < static_cast<int64_t>(t);
+  uint32_t K = 0;
+  unsigned long long above = 0, eq = 0;
+  if (!short_chunk)
+    K = block_select_small<LS_THREADS>(each_key, t, sm, &above, &eq);
+  else
+    above = static_cast<unsigned long long>(cnt);
+  uint32_t* mine = cd.key + chunk * static_cast<int64_t>(t);
+#pragma unroll
+  for (int h = 0; h < H; ++h) {
+    if (mh[h] && (short_chunk || kh[h] > K)) mine[atomicAdd(&s_pos, 1u)] = kh[h];
+  }
+  for (unsigned long long q = above + tid; q < t; q += LS_THREADS) mine[q] = short_chunk ? 0u : K;
+  __syncthreads();
+  if (tid == 0) {
+    cd.kth[chunk] = K;
+    cd.extra[chunk] = short_chunk ? 0u : static_cast<unsigned>(eq - (t - above));
+    cd.flag[chunk] = s_fail ? 1ull : 0ull;
+    // Arrival: the CTA's writes (ordered before it by the block barrier and
+    // the fence) are visible to the CTA that sees the last arrival.
+    __threadfence();
+    const unsigned long long tag = (epoch ^ (epoch >> 32)) & 0xFFFFFFFFull;
+    unsigned long long cur = __ldcg(&cd.arrive);
+    int tries = 0;
+    for (; tries <= G + 1; ++tries) {
+      const unsigned long long want = (cur >> 32) == tag ? cur + 1 : (tag << 32) | 1ull;
+      const unsigned long long prev = atomicCAS(&cd.arrive, cur, want);
+      if (prev == cur) {
+        s_last = (want & 0xFFFFFFFFull) == static_cast<unsigned long long>(G);
+        break;
+      }
+      cur = prev;
+    }
+    if (tries > G + 1) atomicOr(&S.error, ERR_WAIT);  // cannot happen: see the arrival word above
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // The last CTA: tau among the G t candidates.  The copies of tau in the
+  // sample are the listed ones plus those left out by the chunks whose t-th
+  // largest is tau.
+  for (int64_t ch = tid; ch < G; ch += LS_THREADS)
+    if (__ldcg(&cd.flag[ch])) s_fail = 1;
+  const int64_t total = G * static_cast<int64_t>(t);
+  for (int64_t e = tid; e < total; e += LS_THREADS) s_cand[e] = __ldcg(cd.key + e);
+  __syncthreads();
+  const int per = static_cast<int>((total + LS_THREADS - 1) / LS_THREADS);
+  auto each_cand = [&](auto&& fn) {
+    for (int q = 0; q < per; ++q) {
+      const int64_t e = static_cast<int64_t>(q) * LS_THREADS + tid;
+      const bool v = e < total;
+      fn(v ? s_cand[e] : 0u, v);
+    }
+  };
+  unsigned long long cabove = 0, ceq = 0;
+  const uint32_t tau = block_select_small<LS_THREADS>(each_cand, t, sm, &cabove, &ceq);
+  unsigned long long more = 0;
+  for (int64_t ch = tid; ch < G; ch += LS_THREADS)
+    if (__ldcg(&cd.kth[ch]) == tau) more += __ldcg(&cd.extra[ch]);
+  unsigned long long tot;
+  excl_scan_block<LS_THREADS>(more, sm.sw, &tot);
+  if (tid == 0) {
+    if (s_fail) atomicOr(&S.error, 1u);
+    const unsigned long long copies = ceq + tot;
+    S.tau_key = tau;
+    S.tau_copies = static_cast<unsigned>(copies < 0xffffffffull ? copies : 0xffffffffull);
+    S.sel_prefix = tau;
+    S.sel_bits = 32;
+    S.sel_done = 1;
+  }
+}
+
 // Chunks per row: all CTAs (chunks x rows) resident at once, one per SM, at
 // most MAX_CHUNKS, at least ST_THREADS sample positions per chunk.
 int64_t sample_tau_chunks(int64_t S, int nrows) {
@@ -719,6 +875,32 @@ cudaError_t launch_sample_tau(const SampleArgs& a, void* scratch, int64_t total_
     launch_kernel(k_sample_tau<true>, grid, ST_THREADS, smem, stream, a, ctl, cand, next_epoch());
   } else {
     launch_kernel(k_sample_tau<false>, grid, ST_THREADS, 0, stream, a, ctl, cand, 0ull);
+  }
+  return cudaGetLastError();
+}
+
+bool sample_lists_fits(int64_t S, unsigned long long t) {
+  return t >= 1 && t <= static_cast<unsigned long long>(TAU_CAND) &&
+         (S + LS_THREADS * LS_MAX_H - 1) / (LS_THREADS * LS_MAX_H) <= MAX_CHUNKS;
+}
+
+cudaError_t launch_sample_lists(const SampleArgs& a, void* scratch, int64_t total_rows, cudaStream_t stream) {
+  if (!sample_lists_fits(a.S, a.t)) return cudaErrorInvalidValue;
+  SampleCand* cand =
+      reinterpret_cast<SampleCand*>(static_cast<char*>(scratch) + align256(sizeof(SampleCtl) * total_rows));
+  // Positions per thread: the fewest that keep the launch within about four
+  // CTAs per SM (one wave), at most LS_MAX_H, and within MAX_CHUNKS chunks.
+  const int64_t wave = 4 * static_cast<int64_t>(sms());
+  int h = 1;
+  auto chunks = [&](int hh) { return (a.S + LS_THREADS * hh - 1) / (LS_THREADS * hh); };
+  while (h < LS_MAX_H && (chunks(h) > MAX_CHUNKS || chunks(h) * a.nrows > wave)) h *= 2;
+  const dim3 grid(static_cast<unsigned>(chunks(h)), static_cast<unsigned>(a.nrows));
+  const unsigned long long ep = next_epoch();
+  switch (h) {
+    case 1: launch_kernel(k_sample_lists<1>, grid, LS_THREADS, 0, stream, a, cand, ep); break;
+    case 2: launch_kernel(k_sample_lists<2>, grid, LS_THREADS, 0, stream, a, cand, ep); break;
+    case 4: launch_kernel(k_sample_lists<4>, grid, LS_THREADS, 0, stream, a, cand, ep); break;
+    default: launch_kernel(k_sample_lists<8>, grid, LS_THREADS, 0, stream, a, cand, ep); break;
   }
   return cudaGetLastError();
 }

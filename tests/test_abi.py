@@ -60,10 +60,10 @@ def test_options_roundtrip_and_validation(pk):
     with pytest.raises(pk.ProfkError):
         pk.set_option(pk.OPT_FORCE_S, -1)
     assert pk.get_option(pk.OPT_SAMPLER) == pk.SAMPLER_AUTO
-    for form in (pk.SAMPLER_GRID, pk.SAMPLER_STEPS, pk.SAMPLER_AUTO):
+    for form in (pk.SAMPLER_GRID, pk.SAMPLER_STEPS, pk.SAMPLER_LISTS, pk.SAMPLER_AUTO):
         pk.set_option(pk.OPT_SAMPLER, form)
         assert pk.get_option(pk.OPT_SAMPLER) == form
-    for bad in (-1, 3):
+    for bad in (-1, 4):
         with pytest.raises(pk.ProfkError):
             pk.set_option(pk.OPT_SAMPLER, bad)
 

@@ -22,11 +22,12 @@ pytestmark = pytest.mark.gpu
     (1 << 24, 400_000, 5, 3, 2), (1 << 20, 1 << 19, 6, 0, 0), ((1 << 21) + 5, 300_001, 7, 1, 4),
     # the whole row (a permutation of it), tiny rows, and rows of one element
     (5000, 5000, 10, 0, 0), (3, 2, 11, 1, 1), (1, 1, 12, 0, 0), ((1 << 32) - 5, 1000, 13, 0, 0)])
-@pytest.mark.parametrize("form", ["auto", "steps"])
+@pytest.mark.parametrize("form", ["auto", "steps", "lists"])
 def test_sample_matches_oracle(pk, cuda_device, n, S, seed, row, attempt, form):
-    """Both kernel forms draw the oracle's sample, index by index in order
-    (rows off the power-of-two grid walk the permutation's cycles)."""
-    pk.set_option(pk.OPT_SAMPLER, {"auto": pk.SAMPLER_AUTO, "steps": pk.SAMPLER_STEPS}[form])
+    """Every kernel form draws the oracle's sample, index by index in order
+    (rows off the power-of-two grid walk the permutation's cycles); the lists
+    form takes S up to 2^19."""
+    pk.set_option(pk.OPT_SAMPLER, {"auto": pk.SAMPLER_AUTO, "steps": pk.SAMPLER_STEPS, "lists": pk.SAMPLER_LISTS}[form])
     x = workloads.uniform(n, seed, cuda_device)
     sidx, svals = pk.sample(x, S, seed, row, attempt)
     ref = PX.sample_indices(n, S, seed, row, attempt)

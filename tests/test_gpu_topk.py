@@ -168,20 +168,21 @@ def test_batched(pk, cuda_device, rows, n, ld, k):
             assert sts[r]["tau_first"] == ost.taus[0]
 
 
-SAMPLER_FORMS = ("grid", "steps")
+SAMPLER_FORMS = ("grid", "steps", "lists")
 
 
 def sampler_option(pk, form):
-    return {"grid": pk.SAMPLER_GRID, "steps": pk.SAMPLER_STEPS}[form]
+    return {"grid": pk.SAMPLER_GRID, "steps": pk.SAMPLER_STEPS, "lists": pk.SAMPLER_LISTS}[form]
 
 
 @pytest.mark.parametrize("form", SAMPLER_FORMS)
 @pytest.mark.parametrize("rows,n,k", [(5, 1 << 20, 64), (12, (1 << 18) + 3, 700), (3, 3 * (1 << 20) + 8, 20_000),
                                       (2, 1 << 24, 32)])
 def test_batched_sampler_forms(pk, cuda_device, form, rows, n, k):
-    """Both forms of the sampling kernels (the persistent grid kernel, the
-    step-by-step kernels) give every row the oracle's sample: the same tau and
-    counts.  The third shape draws about 137,000 times per row."""
+    """Every form of the sampling kernels (the persistent grid kernel, the
+    step-by-step kernels, the lists kernel where t <= 8) gives every row the
+    oracle's sample: the same tau and counts.  The third shape draws about
+    137,000 times per row."""
     pk.set_option(pk.OPT_SAMPLER, sampler_option(pk, form))
     ld = (n + 3) // 4 * 4  # row stride a multiple of 4 elements
     x = workloads.normal_rows(rows, ld, 3 * rows + k, cuda_device)[:, :n]
