@@ -256,9 +256,10 @@ typedef enum profk_option {
  * taking up to 1024 sample positions; tau from per-CTA candidate lists that
  * one CTA waits for (t <= 8) or from passes whose CTAs meet at grid
  * barriers (larger t).  LISTS (t <= 8): CTAs of up to 2048 positions of one
- * row, each listing its t largest sampled values; the row's last CTA to
- * finish selects tau among the lists, and no CTA waits for another; taken
- * for t <= 8 when the rows' shares of the SMs are too small for GRID.
+ * row, each publishing a list of its t largest sampled values; a CTA that
+ * finds every list of its row published selects tau among them, and no CTA
+ * waits for another; taken for t <= 8 when the rows' shares of the SMs are
+ * too small for GRID.
  * STEPS: one thread per sample position, then a radix selection of tau; the
  * remaining cases.  A form that cannot take the problem falls back to the
  * automatic choice. */

@@ -125,9 +125,9 @@ bool sample_tau_fits(int64_t S, int nrows);
 int64_t sample_tau_setup_max_t();
 // The lists form of steps 1 and 2, for t <= sample_tau_setup_max_t() and any
 // number of rows: CTAs of 256 threads take up to 2048 consecutive sample
-// positions of one row each, list their t largest keys, and the row's last
-// CTA to finish selects tau among the lists; no CTA waits for another, so
-// the launch needs no co-residency.  It does the attempt's set-up like the
+// positions of one row each and publish lists of their t largest keys; a CTA
+// that finds every list of its row published selects tau among them.  No CTA
+// waits for another, so the launch needs no co-residency.  It does the attempt's set-up like the
 // persistent form (SampleArgs::zero_ctl), and uses the same scratch
 // (sample_tau_scratch_bytes), which needs no initialisation.  Rows that an
 // earlier attempt settled are left alone.

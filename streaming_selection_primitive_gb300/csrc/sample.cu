@@ -23,9 +23,9 @@
 //    tau selection fused (the last block picks the digit; launch_select
 //    finishes);
 //  * k_sample_lists (t <= TAU_CAND, rows too many for the persistent form):
-//    CTAs of 256 threads take up to 2048 positions of one row, list their t
-//    largest keys, and the row's last CTA to finish selects tau among the
-//    lists, with no CTA waiting for another;
+//    CTAs of 256 threads take up to 2048 positions of one row and publish
+//    lists of their t largest keys; a CTA that finds every list of its row
+//    published selects tau among them, with no CTA waiting for another;
 //  * k_sample_tau (the main path, one 512-thread CTA per SM and contiguous
 //    chunk of at most 1024 sample positions, all CTAs of the launch resident
 //    together): the sample, then tau.  For t <= TAU_CAND (8) every CTA
@@ -59,6 +59,11 @@ constexpr int SMALL_T = TAU_CAND;
 constexpr int TAU_GATHER = ST_THREADS;  // a tau bucket this small is finished by one CTA (t > TAU_CAND)
 constexpr int MAX_CHUNKS = 256;
 
+// A sampled value.  The positions are spread over the whole row, so no two
+// share a cache line: the load bypasses L1, whose misses fill whole lines,
+// and asks L2 for the one 32-byte sector that holds the value.
+__device__ __forceinline__ float gather_one(const float* p) { return __ldcg(p); }
+
 // b = max(2, ceil(log2 n)): the Feistel network permutes [0, 2^b), 2^b >= n.
 __device__ __forceinline__ int domain_bits(uint64_t n) { return n <= 4 ? 2 : 64 - __clzll(n - 1); }
 
@@ -80,14 +85,18 @@ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
   return z ^ (z >> 31);
 }
 
-__device__ __forceinline__ uint64_t feistel(uint64_t x, int b, const uint64_t* K) {
+// One pass of the network.  Rows hold at most 2^32 elements, so b <= 32: the
+// state and both halves (at most 16 bits each) are 32-bit words, and only the
+// round function works on 64 bits.
+__device__ __forceinline__ uint32_t feistel(uint32_t x, int b, const uint64_t* K) {
   int w = b >> 1;
 #pragma unroll
   for (int i = 0; i < FEISTEL_ROUNDS; ++i) {
     const int wl = b - w;
-    const uint64_t right = x & ((1ull << w) - 1ull);
-    const uint64_t left = x >> w;
-    x = (right << wl) | (left ^ (mix64(right ^ K[i]) & ((1ull << wl) - 1ull)));
+    const uint32_t right = x & ((1u << w) - 1u);
+    const uint32_t left = x >> w;
+    const uint32_t f = static_cast<uint32_t>(mix64(static_cast<uint64_t>(right) ^ K[i]));
+    x = (right << wl) | (left ^ (f & ((1u << wl) - 1u)));
     w = wl;
   }
   return x;
@@ -106,7 +115,7 @@ __device__ __forceinline__ bool permute(uint64_t (&x)[H], bool (&walk)[H], uint6
     if (!any) return true;
 #pragma unroll
     for (int h = 0; h < H; ++h) {
-      const uint64_t y = feistel(x[h], b, K);
+      const uint64_t y = feistel(static_cast<uint32_t>(x[h]), b, K);
       if (walk[h]) {
         x[h] = y;
         walk[h] = y >= n;
@@ -221,7 +230,7 @@ __global__ void __launch_bounds__(DRAW_THREADS) k_sample_draw(SampleArgs a, int6
     bool walk[1] = {true};
     if (!permute<1>(x, walk, a.n, domain_bits(a.n), s_keys)) atomicOr(&S.error, 1u);
     const uint32_t u = static_cast<uint32_t>(x[0]);
-    key = ord_key(a.x[static_cast<int64_t>(row) * a.ld + u]);
+    key = ord_key(gather_one(a.x + static_cast<int64_t>(row) * a.ld + u));
     const int64_t o = static_cast<int64_t>(row) * a.S + j;
     a.sidx[o] = u;
     a.skeys[o] = key;
@@ -276,9 +285,6 @@ struct SampleCand {
   uint32_t kth[MAX_CHUNKS];
   uint32_t extra[MAX_CHUNKS];
   unsigned long long flag[MAX_CHUNKS];
-  // The lists form: (launch tag << 32) | CTAs of the row arrived so far.
-  unsigned long long arrive;
-  unsigned long long pad;
 };
 
 namespace {
@@ -446,7 +452,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   }
   float vh[ST_HELD];
 #pragma unroll
-  for (int h = 0; h < ST_HELD; ++h) vh[h] = mh[h] ? xr[xs[h]] : 0.f;  // the gathers, in flight together
+  for (int h = 0; h < ST_HELD; ++h) vh[h] = mh[h] ? gather_one(xr + xs[h]) : 0.f;  // the gathers, in flight together
   uint32_t kh[ST_HELD];
 #pragma unroll
   for (int h = 0; h < ST_HELD; ++h) {
@@ -672,36 +678,139 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
 // ---------------------------------------------------------------------------
 // The lists form (t <= TAU_CAND, any number of rows).  A CTA of LS_THREADS
 // threads takes LS_THREADS x H consecutive sample positions of one row
-// (thread tid: positions lo + h LS_THREADS + tid, so that the H Feistel
-// chains of a thread interleave), lists its t largest keys as the
-// persistent form's chunks do, and arrives on the row's arrival word; the
-// CTA that arrives last selects tau among the row's lists.  No CTA waits for
-// another.  The arrival word holds (launch tag << 32) | arrivals: the first
-// arrival of a launch finds another tag and starts the count at 1, so the
-// word needs no zeroing, and a CTA whose compare-and-swap fails has seen
-// another CTA's arrival succeed, which bounds its retries by the row's CTAs.
+// (thread tid: positions lo + h LS_THREADS + tid), lists its t largest keys
+// as the persistent form's chunks do, and publishes the list with a flag
+// stamped with the launch's epoch (unique to the launch, so the flags need
+// no zeroing).  It then reads the row's flags: a CTA that finds every chunk
+// published selects tau among the lists.  No CTA waits for another.
+//
+// Selections of a few largest keys go warp by warp (reductions inside the
+// warp, no block barrier), then one warp merges the warps' lists: the t
+// largest of a set are among the union of the t largest of its parts.
 constexpr int LS_THREADS = 256;
+constexpr int LS_WARPS = LS_THREADS / 32;
 constexpr int LS_MAX_H = 8;
+
+// The want-th largest of the keys that each_key(fn) presents to the warp
+// (fn(key, valid), called the same number of times on every lane): rounds
+// of "the largest key below the previous round's, and its copies", at most
+// want rounds.  *above = keys strictly larger, *eq = keys equal to it.  The
+// warp must hold at least want valid keys.
+template <class EachKey>
+__device__ __forceinline__ uint32_t warp_select_small(EachKey each_key, unsigned want, unsigned* above,
+                                                      unsigned* eq) {
+  const unsigned want0 = want;
+  uint32_t bound = 0xffffffffu, result = 0;
+  bool first = true;
+  unsigned cnt = 0;
+  for (int r = 0; r < SMALL_T; ++r) {
+    uint32_t m = 0;
+    each_key([&](uint32_t key, bool v) {
+      if (v && (first || key < bound) && key > m) m = key;
+    });
+    m = __reduce_max_sync(FULL_MASK, m);
+    unsigned c = 0;
+    each_key([&](uint32_t key, bool v) { c += (v && (first || key < bound) && key == m) ? 1u : 0u; });
+    cnt = __reduce_add_sync(FULL_MASK, c);
+    result = m;
+    if (cnt >= want) break;
+    want -= cnt;
+    bound = m;
+    first = false;
+  }
+  *above = want0 - want;
+  *eq = cnt;
+  return result;
+}
+
+// The t largest keys of a warp's keys into out[0, t): those above the t-th
+// largest Kw, in lane order, then copies of Kw (a warp with fewer than t
+// keys lists them all, padded with zero keys, and Kw = 0).  Returns Kw;
+// *extra = the copies of Kw that the list leaves out.
+template <class EachKey>
+__device__ __forceinline__ uint32_t warp_list_t(EachKey each_key, unsigned t, uint32_t* out, unsigned* extra) {
+  const int lane = threadIdx.x & 31;
+  unsigned vc = 0;
+  each_key([&](uint32_t, bool v) { vc += v ? 1u : 0u; });
+  vc = __reduce_add_sync(FULL_MASK, vc);
+  const bool few = vc < t;
+  uint32_t K = 0;
+  unsigned above = vc, eq = 0;
+  if (!few) K = warp_select_small(each_key, t, &above, &eq);
+  unsigned pos = 0;
+  each_key([&](uint32_t key, bool v) {
+    const bool take = v && (few || key > K);
+    const unsigned m = __ballot_sync(FULL_MASK, take);
+    if (take) out[pos + __popc(m & ((1u << lane) - 1u))] = key;
+    pos += __popc(m);
+  });
+  for (unsigned q = above + lane; q < t; q += 32) out[q] = K;
+  *extra = few ? 0u : eq - (t - above);
+  return K;
+}
+
+struct ListsSmem {
+  uint32_t key[LS_WARPS * TAU_CAND];  // each warp's t largest
+  uint32_t kth[LS_WARPS];
+  unsigned extra[LS_WARPS];
+};
+
+// The t largest keys of the block (each warp's keys presented by each_key),
+// listed by warp 0 into out[0, t).  Returns the block's t-th largest K to
+// warp 0, with *extra = the block's copies of K that the list leaves out.
+// The block must hold at least t keys.  Ends with warp 0 alone (the other
+// warps return 0 and must not use the list before a block barrier).
+template <class EachKey>
+__device__ __forceinline__ uint32_t block_list_t(EachKey each_key, unsigned t, ListsSmem& sm, uint32_t* out,
+                                                 unsigned* extra) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned ex;
+  const uint32_t Kw = warp_list_t(each_key, t, sm.key + warp * t, &ex);
+  if (lane == 0) {
+    sm.kth[warp] = Kw;
+    sm.extra[warp] = ex;
+  }
+  __syncthreads();
+  if (warp != 0) return 0;
+  const unsigned total = LS_WARPS * t;
+  auto each_cand = [&](auto&& fn) {
+#pragma unroll
+    for (int q = 0; q < (LS_WARPS * TAU_CAND + 31) / 32; ++q) {
+      const unsigned e = q * 32 + lane;
+      const bool v = e < total;
+      fn(v ? sm.key[e] : 0u, v);
+    }
+  };
+  unsigned cex;
+  const uint32_t K = warp_list_t(each_cand, t, out, &cex);
+  // The copies of K outside the candidates: a warp whose t-th largest is
+  // above K cannot exist (its t keys would all be above K), and one whose
+  // t-th largest is below K listed all its copies of K.
+  unsigned more = (lane < LS_WARPS && sm.kth[lane] == K) ? sm.extra[lane] : 0u;
+  more = __reduce_add_sync(FULL_MASK, more);
+  *extra = cex + more;
+  return K;
+}
 
 template <int H>
 __global__ void __launch_bounds__(LS_THREADS) k_sample_lists(SampleArgs a, SampleCand* cands,
                                                             unsigned long long epoch) {
   pdl_trigger();
   pdl_wait();
-  __shared__ SelSmem sm;
+  __shared__ ListsSmem sm;
   __shared__ uint64_t s_keys[FEISTEL_ROUNDS];
-  __shared__ uint32_t s_cand[MAX_CHUNKS * TAU_CAND];  // the last CTA: every list of the row
+  __shared__ uint32_t s_cand[MAX_CHUNKS * TAU_CAND];  // a finishing CTA: every list of the row
+  __shared__ uint32_t s_final[TAU_CAND];
   __shared__ unsigned s_pos;
-  __shared__ int s_fail, s_last;
+  __shared__ int s_fail;
   const int row = launch_row(a.rows);
   RowState& S = a.st[row];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t G = gridDim.x, chunk = blockIdx.x;
-  if (settled_before(S, a.attempt)) return;  // every CTA of the row leaves before arriving
+  if (settled_before(S, a.attempt)) return;  // every CTA of the row leaves before publishing
   if (tid == 0) {
     s_pos = 0;
     s_fail = 0;
-    s_last = 0;
   }
   attempt_setup<LS_THREADS>(a, S, row, chunk, G);
   round_keys(a.seed, static_cast<uint64_t>(row + a.key_row0), static_cast<uint64_t>(a.attempt), s_keys);
@@ -709,18 +818,47 @@ __global__ void __launch_bounds__(LS_THREADS) k_sample_lists(SampleArgs a, Sampl
   const int64_t lo = chunk * (static_cast<int64_t>(LS_THREADS) * H);
   const float* xr = a.x + static_cast<int64_t>(row) * a.ld;
   const int64_t orow = static_cast<int64_t>(row) * a.S;
+  const int b = domain_bits(a.n);
+  // The positions in two halves: the first half's gathers are in flight
+  // while the second half's indices are computed.
+  constexpr int H1 = H > 1 ? H / 2 : 1, H2 = H - H1;
   uint64_t xs[H];
-  bool walk[H], mh[H];
-#pragma unroll
-  for (int h = 0; h < H; ++h) {
-    const int64_t j = lo + static_cast<int64_t>(h) * LS_THREADS + tid;
-    xs[h] = static_cast<uint64_t>(j);
-    walk[h] = mh[h] = j < a.S;
-  }
-  if (!permute<H>(xs, walk, a.n, domain_bits(a.n), s_keys)) s_fail = 1;
+  bool mh[H];
   float vh[H];
+  bool ok = true;
+  {
+    uint64_t x1[H1];
+    bool w1[H1];
 #pragma unroll
-  for (int h = 0; h < H; ++h) vh[h] = mh[h] ? xr[xs[h]] : 0.f;  // the gathers, in flight together
+    for (int h = 0; h < H1; ++h) {
+      const int64_t j = lo + static_cast<int64_t>(h) * LS_THREADS + tid;
+      x1[h] = static_cast<uint64_t>(j);
+      w1[h] = mh[h] = j < a.S;
+    }
+    ok &= permute<H1>(x1, w1, a.n, b, s_keys);
+#pragma unroll
+    for (int h = 0; h < H1; ++h) {
+      xs[h] = x1[h];
+      vh[h] = mh[h] ? gather_one(xr + x1[h]) : 0.f;
+    }
+  }
+  if constexpr (H2 > 0) {
+    uint64_t x2[H2 > 0 ? H2 : 1];
+    bool w2[H2 > 0 ? H2 : 1];
+#pragma unroll
+    for (int h = 0; h < H2; ++h) {
+      const int64_t j = lo + static_cast<int64_t>(H1 + h) * LS_THREADS + tid;
+      x2[h] = static_cast<uint64_t>(j);
+      w2[h] = mh[H1 + h] = j < a.S;
+    }
+    ok &= permute<H2>(x2, w2, a.n, b, s_keys);
+#pragma unroll
+    for (int h = 0; h < H2; ++h) {
+      xs[H1 + h] = x2[h];
+      vh[H1 + h] = mh[H1 + h] ? gather_one(xr + x2[h]) : 0.f;
+    }
+  }
+  if (!ok) s_fail = 1;
   uint32_t kh[H];
 #pragma unroll
   for (int h = 0; h < H; ++h) {
@@ -736,75 +874,87 @@ __global__ void __launch_bounds__(LS_THREADS) k_sample_lists(SampleArgs a, Sampl
 #pragma unroll
     for (int h = 0; h < H; ++h) fn(kh[h], mh[h]);
   };
-  const unsigned long long t = a.t;
+  const unsigned t = static_cast<unsigned>(a.t);
   SampleCand& cd = cands[row];
-  // The chunk's t largest keys: those above its t-th largest K and copies of
-  // K to make t (all its keys, padded with zero keys, when it has fewer).
-  const int64_t cnt = (a.S - lo < static_cast<int64_t>(LS_THREADS) * H) ? a.S - lo : static_cast<int64_t>(LS_THREADS) * H;
-  const bool short_chunk = cnt < static_cast<int64_t>(t);
-  uint32_t K = 0;
-  unsigned long long above = 0, eq = 0;
-  if (!short_chunk)
-    K = block_select_small<LS_THREADS>(each_key, t, sm, &above, &eq);
-  else
-    above = static_cast<unsigned long long>(cnt);
   uint32_t* mine = cd.key + chunk * static_cast<int64_t>(t);
+  // The chunk's t largest keys (all of them, padded with zero keys, when it
+  // has fewer than t).
+  const int64_t cnt = (a.S - lo < static_cast<int64_t>(LS_THREADS) * H) ? a.S - lo : static_cast<int64_t>(LS_THREADS) * H;
+  if (cnt < static_cast<int64_t>(t)) {
 #pragma unroll
-  for (int h = 0; h < H; ++h) {
-    if (mh[h] && (short_chunk || kh[h] > K)) mine[atomicAdd(&s_pos, 1u)] = kh[h];
-  }
-  for (unsigned long long q = above + tid; q < t; q += LS_THREADS) mine[q] = short_chunk ? 0u : K;
-  __syncthreads();
-  if (tid == 0) {
-    cd.kth[chunk] = K;
-    cd.extra[chunk] = short_chunk ? 0u : static_cast<unsigned>(eq - (t - above));
-    cd.flag[chunk] = s_fail ? 1ull : 0ull;
-    // Arrival: the CTA's writes (ordered before it by the block barrier and
-    // the fence) are visible to the CTA that sees the last arrival.
+    for (int h = 0; h < H; ++h)
+      if (mh[h]) mine[atomicAdd(&s_pos, 1u)] = kh[h];
     __threadfence();
-    const unsigned long long tag = (epoch ^ (epoch >> 32)) & 0xFFFFFFFFull;
-    unsigned long long cur = __ldcg(&cd.arrive);
-    int tries = 0;
-    for (; tries <= G + 1; ++tries) {
-      const unsigned long long want = (cur >> 32) == tag ? cur + 1 : (tag << 32) | 1ull;
-      const unsigned long long prev = atomicCAS(&cd.arrive, cur, want);
-      if (prev == cur) {
-        s_last = (want & 0xFFFFFFFFull) == static_cast<unsigned long long>(G);
-        break;
-      }
-      cur = prev;
+    __syncthreads();
+    if (tid == 0) {
+      for (unsigned q = static_cast<unsigned>(cnt); q < t; ++q) mine[q] = 0u;
+      cd.kth[chunk] = 0u;
+      cd.extra[chunk] = 0u;
     }
-    if (tries > G + 1) atomicOr(&S.error, ERR_WAIT);  // cannot happen: see the arrival word above
-    if (s_last) __threadfence();
+  } else {
+    unsigned ex;
+    const uint32_t K = block_list_t(each_key, t, sm, mine, &ex);
+    if (tid == 0) {
+      cd.kth[chunk] = K;
+      cd.extra[chunk] = ex;
+    }
+  }
+  // Publication: the chunk's flag, (epoch << 1) | (a walk did not end),
+  // stored with release semantics once its list is written (by warp 0, or by
+  // every thread before the block barrier above).  Then every CTA reads the
+  // row's flags; one that finds them all of this launch finishes the row.
+  // The fences between each CTA's flag store and its reads make sure that
+  // the last CTA to publish finds every flag; two CTAs that both do finish
+  // the row compute the same tau and write the same words.
+  if (warp == 0) {
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+      const unsigned long long f = (epoch << 1) | (s_fail ? 1ull : 0ull);
+      asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(&cd.flag[chunk]), "l"(f) : "memory");
+      __threadfence();
+    }
   }
   __syncthreads();
-  if (!s_last) return;
-  // The last CTA: tau among the G t candidates.  The copies of tau in the
-  // sample are the listed ones plus those left out by the chunks whose t-th
-  // largest is tau.
-  for (int64_t ch = tid; ch < G; ch += LS_THREADS)
-    if (__ldcg(&cd.flag[ch])) s_fail = 1;
-  const int64_t total = G * static_cast<int64_t>(t);
-  for (int64_t e = tid; e < total; e += LS_THREADS) s_cand[e] = __ldcg(cd.key + e);
+  __threadfence();
+  bool mine_ok = true;
+  for (int64_t ch = tid; ch < G; ch += LS_THREADS) {
+    unsigned long long f;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(f) : "l"(&cd.flag[ch]) : "memory");
+    if ((f >> 1) != epoch) mine_ok = false;
+    else if (f & 1ull) s_fail = 1;
+  }
+  if (!__syncthreads_and(mine_ok)) return;
+  // A CTA that finishes the row: tau among the G t candidates.  The copies
+  // of tau in the sample are those among the candidates plus those left out
+  // by the chunks whose t-th largest is tau.
+  const int total = static_cast<int>(G) * static_cast<int>(t);
+  for (int e = tid; e < total; e += LS_THREADS) s_cand[e] = __ldcg(cd.key + e);
   __syncthreads();
-  const int per = static_cast<int>((total + LS_THREADS - 1) / LS_THREADS);
+  // Warp w takes candidates w, w + LS_WARPS, ... (at most MAX_CHUNKS TAU_CAND / LS_THREADS a lane).
   auto each_cand = [&](auto&& fn) {
-    for (int q = 0; q < per; ++q) {
-      const int64_t e = static_cast<int64_t>(q) * LS_THREADS + tid;
+#pragma unroll
+    for (int q = 0; q < MAX_CHUNKS * TAU_CAND / LS_THREADS; ++q) {
+      const int e = (q * 32 + lane) * LS_WARPS + warp;
       const bool v = e < total;
       fn(v ? s_cand[e] : 0u, v);
     }
   };
-  unsigned long long cabove = 0, ceq = 0;
-  const uint32_t tau = block_select_small<LS_THREADS>(each_cand, t, sm, &cabove, &ceq);
-  unsigned long long more = 0;
-  for (int64_t ch = tid; ch < G; ch += LS_THREADS)
+  unsigned cex;
+  const uint32_t tau = block_list_t(each_cand, t, sm, s_final, &cex);
+  if (warp != 0) return;
+  unsigned more = 0;
+  for (int64_t ch = lane; ch < G; ch += 32)
     if (__ldcg(&cd.kth[ch]) == tau) more += __ldcg(&cd.extra[ch]);
-  unsigned long long tot;
-  excl_scan_block<LS_THREADS>(more, sm.sw, &tot);
-  if (tid == 0) {
+  more = __reduce_add_sync(FULL_MASK, more);
+  __syncwarp();  // s_final, written by the warp's lanes
+  if (lane == 0) {
     if (s_fail) atomicOr(&S.error, 1u);
-    const unsigned long long copies = ceq + tot;
+    // t listed keys are at or above tau; those equal to it, plus the copies
+    // left out of the candidates and out of the chunks' lists.
+    unsigned eq_listed = 0;
+    for (unsigned q = 0; q < t; ++q) eq_listed += s_final[q] == tau;
+    const unsigned long long copies = static_cast<unsigned long long>(eq_listed) + cex + more;
     S.tau_key = tau;
     S.tau_copies = static_cast<unsigned>(copies < 0xffffffffull ? copies : 0xffffffffull);
     S.sel_prefix = tau;

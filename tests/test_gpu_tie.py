@@ -41,8 +41,10 @@ def sample_copies_of_tau(h, S, t, seed, attempt, row=0):
     return int(np.count_nonzero(sv == tau))
 
 
-def run(pk, x, k, seed, force=None, eps=1e-3):
+def run(pk, x, k, seed, force=None, eps=1e-3, sampler=None):
     pk.reset_options()
+    if sampler is not None:
+        pk.set_option(pk.OPT_SAMPLER, sampler)
     if force:
         pk.set_option(pk.OPT_FORCE_S, force.get("S", 0))
         pk.set_option(pk.OPT_FORCE_T, force.get("t", 0))
@@ -156,3 +158,22 @@ def test_batched_rows_take_both_tie_forms_in_one_attempt(pk, cuda_device):
             copies = sample_copies_of_tau(hr, 256, 1, 17, ost.attempts - 1, row=r)
             forms_by_attempt.setdefault(ost.attempts, set()).add(copies >= 2)
     assert any(f == {False, True} for f in forms_by_attempt.values()), forms_by_attempt
+
+
+@pytest.mark.parametrize("force", [{"S": 256, "t": 1, "M": 400}, {"S": 4096, "t": 8, "M": 400},
+                                   {"S": 20_000, "t": 5, "M": 400}])
+def test_lists_sampler_routes_ties_like_the_grid_form(pk, cuda_device, force):
+    """The lists form of the sampler (forced) gives every seed the oracle's
+    result and the persistent form's statistics, kernel launches included.
+    The launches tell whether the row went through the filter's bookkeeping
+    (tau at least twice in the sample) or the counting pass, so both forms
+    count the copies of tau alike, across 1, 16 and 79 chunks."""
+    n, k = 1 << 20, 200
+    x = tied_top(n, 6000, 30, 11, cuda_device)
+    paths = set()
+    for seed in range(12):
+        st_grid, ost, h = run(pk, x, k, seed, force)
+        st_lists, _, _ = run(pk, x, k, seed, force, sampler=pk.SAMPLER_LISTS)
+        assert st_lists == st_grid, (seed, st_lists, st_grid)
+        paths.add(st_lists["path"])
+    assert pk.PATH_TIE in paths
