@@ -435,24 +435,28 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   const float* xr = a.x + static_cast<int64_t>(row) * a.ld;
   const int64_t orow = static_cast<int64_t>(row) * a.S;
 
-  // a. The chunk's sample positions: their indices, values and keys.
+  // a. The chunk's sample positions: their indices, values and keys (each
+  // position's gather is in flight while the next position is computed).
   uint64_t xs[ST_HELD];
-  bool walk[ST_HELD], mh[ST_HELD];
+  bool mh[ST_HELD];
+  float vh[ST_HELD];
+  bool ok = true;
 #pragma unroll
   for (int h = 0; h < ST_HELD; ++h) {
     const int64_t j = lo + static_cast<int64_t>(h) * ST_THREADS + tid;
-    xs[h] = static_cast<uint64_t>(j);
-    walk[h] = mh[h] = j < hi;
+    uint64_t x1[1] = {static_cast<uint64_t>(j)};
+    bool w1[1] = {j < hi};
+    mh[h] = w1[0];
+    ok &= permute<1>(x1, w1, a.n, domain_bits(a.n), s_keys);
+    xs[h] = x1[0];
+    vh[h] = mh[h] ? gather_one(xr + x1[0]) : 0.f;
   }
-  if (!permute<ST_HELD>(xs, walk, a.n, domain_bits(a.n), s_keys)) {
+  if (!ok) {
     if constexpr (CAND)
       s_fail = 1;  // reported through the chunk's flag (the first CTA owns the error word)
     else
       atomicOr(&S.error, 1u);
   }
-  float vh[ST_HELD];
-#pragma unroll
-  for (int h = 0; h < ST_HELD; ++h) vh[h] = mh[h] ? gather_one(xr + xs[h]) : 0.f;  // the gathers, in flight together
   uint32_t kh[ST_HELD];
 #pragma unroll
   for (int h = 0; h < ST_HELD; ++h) {

@@ -221,6 +221,23 @@ def test_large_k(pk, cuda_device, gen, n, k):
         check_call(pk, x, k, 1e-3, 90 + s)
 
 
+@pytest.mark.parametrize("gen,n,k,force", [
+    # tau's top buckets hold nearly every sample key (all three passes run)
+    ("ulps_below_one", 1 << 22, 4096, {"S": 131072, "t": 300}),
+    ("levels16", 1 << 22, 4096, {"S": 131072, "t": 300}),  # one level's copies: 1/16 of the sample
+    ("uniform", (1 << 22) + 3, 4096, {"S": 131072, "t": 300}),
+    ("normal", 1 << 22, 4096, {"S": 262144, "t": 9}),  # t just above the candidate lists' range
+    ("normal", 5000, 100, {"S": 1500, "t": 40}),  # a sample of a few chunks, the last one short
+])
+def test_sampler_passes_for_larger_t(pk, cuda_device, gen, n, k, force):
+    """For t > 8 the sampler selects tau by radix passes over the sample
+    keys; it finds the oracle's tau, and the oracle's counts and result
+    follow, for tau buckets of every size."""
+    x = workloads.GENERATORS[gen](n, 23, cuda_device)
+    for s in range(2):
+        check_call(pk, x, k, 1e-3, 40 + s, force=force)
+
+
 def test_large_k_fallback(pk, cuda_device):
     x = workloads.normal(1 << 22, 5, cuda_device)
     st = check_call(pk, x, 20_000, 1e-3, 3, force={"S": 32768, "t": 1}, max_attempts=2)
