@@ -408,7 +408,13 @@ template <bool CAND>
 __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, SampleCtl* ctl, SampleCand* cands,
                                                              unsigned long long epoch) {
   pdl_trigger();
-  pdl_wait();
+  // The first attempt of the candidate lists' form computes its first
+  // position (shared memory and registers only) before it waits for the
+  // preceding kernel, and reads or writes global memory only after.  Later
+  // attempts first read what earlier ones settled; the passes' form follows
+  // a reset kernel of its own attempt.
+  const bool early = CAND && a.attempt == 0;
+  if (!early) pdl_wait();
   extern __shared__ uint32_t s_cand[];  // CAND: the G t candidates, in the first CTA
   __shared__ SelSmem sm;
   __shared__ int s_err, s_fail;
@@ -425,7 +431,6 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     s_fail = 0;
     s_pos = 0;
   }
-  if constexpr (CAND) attempt_setup<ST_THREADS>(a, S, row, chunk, G);
   round_keys(a.seed, static_cast<uint64_t>(row + a.key_row0), static_cast<uint64_t>(a.attempt), s_keys);
   __syncthreads();
   const int limit = wait_limit(a.wait);
@@ -435,8 +440,9 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   const float* xr = a.x + static_cast<int64_t>(row) * a.ld;
   const int64_t orow = static_cast<int64_t>(row) * a.S;
 
-  // a. The chunk's sample positions: their indices, values and keys (each
-  // position's gather is in flight while the next position is computed).
+  // a. The chunk's sample positions, their values and keys (each position's
+  // gather is in flight while the next position is computed; the first
+  // position is computed before the wait, then the attempt's set-up).
   uint64_t xs[ST_HELD];
   bool mh[ST_HELD];
   float vh[ST_HELD];
@@ -448,26 +454,36 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
     bool w1[1] = {j < hi};
     mh[h] = w1[0];
     ok &= permute<1>(x1, w1, a.n, domain_bits(a.n), s_keys);
+    if (h == 0) {
+      if (early) pdl_wait();
+      if constexpr (CAND) attempt_setup<ST_THREADS>(a, S, row, chunk, G);
+    }
     xs[h] = x1[0];
     vh[h] = mh[h] ? gather_one(xr + x1[0]) : 0.f;
   }
-  if (!ok) {
-    if constexpr (CAND)
-      s_fail = 1;  // reported through the chunk's flag (the first CTA owns the error word)
-    else
-      atomicOr(&S.error, 1u);
-  }
+  // A walk that did not end: reported through the chunk's flag (the
+  // candidate lists' form, whose first CTA owns the error word) or the error
+  // word (the passes' form).
+  if (!ok) s_fail = 1;
   uint32_t kh[ST_HELD];
 #pragma unroll
-  for (int h = 0; h < ST_HELD; ++h) {
-    kh[h] = ord_key(vh[h]);
-    if (mh[h] && a.store_sample) {
-      const int64_t o = orow + lo + static_cast<int64_t>(h) * ST_THREADS + tid;
-      a.sidx[o] = static_cast<uint32_t>(xs[h]);
-      a.skeys[o] = kh[h];
+  for (int h = 0; h < ST_HELD; ++h) kh[h] = ord_key(vh[h]);
+  // The sample and RowState::distinct.  Called by every thread.
+  auto publish_sample = [&]() {
+#pragma unroll
+    for (int h = 0; h < ST_HELD; ++h) {
+      if (mh[h] && a.store_sample) {
+        const int64_t o = orow + lo + static_cast<int64_t>(h) * ST_THREADS + tid;
+        a.sidx[o] = static_cast<uint32_t>(xs[h]);
+        a.skeys[o] = kh[h];
+      }
     }
-  }
-  if (chunk == 0 && tid == 0) S.distinct = static_cast<unsigned>(a.S < 0xffffffffll ? a.S : 0xffffffffll);
+    if (chunk == 0 && tid == 0) S.distinct = static_cast<unsigned>(a.S < 0xffffffffll ? a.S : 0xffffffffll);
+    if constexpr (!CAND) {
+      __syncthreads();
+      if (tid == 0 && s_fail) atomicOr(&S.error, 1u);
+    }
+  };
   auto each_key = [&](auto&& fn) {
 #pragma unroll
     for (int h = 0; h < ST_HELD; ++h) fn(kh[h], mh[h]);
@@ -487,6 +503,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
       K = block_select_small(each_key, t, sm, &above, &eq);
     else
       above = static_cast<unsigned long long>(cnt);  // every key goes to the list
+    publish_sample();
     uint32_t* mine = cd.key + chunk * static_cast<int64_t>(t);
 #pragma unroll
     for (int h = 0; h < ST_HELD; ++h) {
@@ -568,6 +585,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_sample_tau(SampleArgs a, Samp
   } else {
     // b'. tau = the t-th largest sample key (and its copies among them) by
     // 11/11/10-bit passes whose chunk histograms meet in global atomics.
+    publish_sample();
     unsigned long long prefix = 0, want = t, copies = 0;
     int bits = 0;
     unsigned target = 0;
@@ -800,7 +818,10 @@ template <int H>
 __global__ void __launch_bounds__(LS_THREADS) k_sample_lists(SampleArgs a, SampleCand* cands,
                                                             unsigned long long epoch) {
   pdl_trigger();
-  pdl_wait();
+  // As in k_sample_tau: the first attempt computes its first positions
+  // before it waits for the preceding kernel.
+  const bool early = a.attempt == 0;
+  if (!early) pdl_wait();
   __shared__ ListsSmem sm;
   __shared__ uint64_t s_keys[FEISTEL_ROUNDS];
   __shared__ uint32_t s_cand[MAX_CHUNKS * TAU_CAND];  // a finishing CTA: every list of the row
@@ -816,7 +837,6 @@ __global__ void __launch_bounds__(LS_THREADS) k_sample_lists(SampleArgs a, Sampl
     s_pos = 0;
     s_fail = 0;
   }
-  attempt_setup<LS_THREADS>(a, S, row, chunk, G);
   round_keys(a.seed, static_cast<uint64_t>(row + a.key_row0), static_cast<uint64_t>(a.attempt), s_keys);
   __syncthreads();
   const int64_t lo = chunk * (static_cast<int64_t>(LS_THREADS) * H);
@@ -840,6 +860,8 @@ __global__ void __launch_bounds__(LS_THREADS) k_sample_lists(SampleArgs a, Sampl
       w1[h] = mh[h] = j < a.S;
     }
     ok &= permute<H1>(x1, w1, a.n, b, s_keys);
+    if (early) pdl_wait();
+    attempt_setup<LS_THREADS>(a, S, row, chunk, G);
 #pragma unroll
     for (int h = 0; h < H1; ++h) {
       xs[h] = x1[h];
