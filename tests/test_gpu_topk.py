@@ -452,3 +452,33 @@ def test_async_batched(pk, cuda_device, rows, n, k):
     v, i, sts = pk.topk_batched_async(x, k, 1e-3, 2).wait()
     assert torch.equal(v, ref[0]) and torch.equal(i, ref[1])
     assert [s["R_first"] for s in sts] == [s["R_first"] for s in ref[2]]
+
+
+@pytest.mark.parametrize("rows,zeros,k", [(1, 120, 40), (100, 120, 40), (100, 1500, 1000), (1, 3000, 2000)])
+def test_signed_zeros_at_the_top(pk, cuda_device, rows, zeros, k):
+    """Rows whose largest values are copies of +0.0 and -0.0 (equal as
+    values; the candidate key keeps no sign, so the refinement reads each
+    zero back from x): the output keeps every zero's own sign bit, in index
+    order.  The cases take the refinement's forms: few candidates placed at
+    once (one row; 100 rows), one CTA per row with its passes and its sorted
+    list (100 rows, 1500 zeros), the grid passes (one row, 3000 zeros)."""
+    n = 1 << 21
+    base = -torch.abs(workloads.normal_rows(rows, n, 12, "cpu")) - 1e-3
+    for r in range(rows):
+        g = torch.Generator().manual_seed(1000 + r)
+        pos = torch.randperm(n, generator=g)[:zeros]
+        base[r, pos[:zeros // 2]] = 0.0
+        base[r, pos[zeros // 2:]] = -0.0
+    x = base.to(cuda_device)
+    h = base.numpy()
+    if rows == 1:
+        vals, idx, st = pk.topk(x[0], k, 1e-3, 5)
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[0]), k, 1e-3, 5)
+        assert_same(vals, idx, ov, oi, "one row")
+        assert st["path"] == ost.path
+        return
+    vals, idx, sts = pk.topk_batched(x, k, 1e-3, 5)
+    for r in range(rows):
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 5, row=r, rows=rows)
+        assert_same(vals[r], idx[r], ov, oi, f"row {r}")
+        assert sts[r]["path"] == ost.path
