@@ -559,8 +559,9 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
   unsigned* block_eq = tie_book ? reinterpret_cast<unsigned*>(at<char>(ws, L.off_tie) +
                                                               align_up(tie_ctl_bytes() * rows))
                                 : nullptr;
-  // The grid sampler with the candidate lists (small t) does the attempt's
-  // set-up itself; the other forms get the reset kernel first.
+  // The candidate-list forms of the sampler (t <= 8: the grid kernel's and
+  // the lists kernel) do the attempt's set-up themselves; the other forms get
+  // the reset kernel first.
   const bool fused_setup =
       form == Sampler::Lists || (form == Sampler::Grid && P.t <= static_cast<uint64_t>(sample_tau_setup_max_t()));
   if (!fused_setup)

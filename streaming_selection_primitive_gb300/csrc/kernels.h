@@ -105,9 +105,9 @@ void launch_sample(const SampleArgs& a, cudaStream_t stream);
 // Same, with Philox key word 1 = storage row + key_row0 (a single stored row
 // can then reproduce any row's sample).
 void launch_sample_rows(const SampleArgs& a, int64_t key_row0, cudaStream_t stream);
-// Steps 1 and 2 of the main path in one persistent kernel: the sample (sidx,
-// skeys, RowState::distinct) and tau (RowState::tau_key, tau_copies; rank
-// a.t) of each listed row.  `scratch` holds sample_tau_scratch_bytes(
+// Steps 1 and 2 of the main path in one persistent kernel: the sample
+// (RowState::distinct; sidx and skeys when store_sample) and tau
+// (RowState::tau_key, tau_copies; rank a.t) of each listed row.  `scratch` holds sample_tau_scratch_bytes(
 // total_rows): first the per-row control blocks (sample_tau_ctl_bytes()
 // each, indexed by row, zero at launch), then candidate lists that need no
 // initialisation.  Rows that an attempt before a.attempt settled
@@ -126,11 +126,11 @@ int64_t sample_tau_setup_max_t();
 // The lists form of steps 1 and 2, for t <= sample_tau_setup_max_t() and any
 // number of rows: CTAs of 256 threads take up to 2048 consecutive sample
 // positions of one row each and publish lists of their t largest keys; a CTA
-// that finds every list of its row published selects tau among them.  No CTA
-// waits for another, so the launch needs no co-residency.  It does the attempt's set-up like the
-// persistent form (SampleArgs::zero_ctl), and uses the same scratch
-// (sample_tau_scratch_bytes), which needs no initialisation.  Rows that an
-// earlier attempt settled are left alone.
+// that finds every list of its row published selects tau among them.  No
+// CTA waits for another, so the launch needs no co-residency.  It does the
+// attempt's set-up like the persistent form (SampleArgs::zero_ctl) and uses
+// the same scratch (sample_tau_scratch_bytes), whose lists need no
+// initialisation.  Rows that an earlier attempt settled are left alone.
 bool sample_lists_fits(int64_t S, unsigned long long t);
 cudaError_t launch_sample_lists(const SampleArgs& a, void* scratch, int64_t total_rows, cudaStream_t stream);
 

@@ -18,6 +18,12 @@
 // from the keys (they hold them exactly), except zero, whose sign the key
 // does not keep: it is read from x.
 //
+// Two shortcuts take no barrier: a row of at most 2048 candidates (few
+// enough to place by counting) is placed at once by every CTA from the
+// buffer itself, and rows that would get two CTAs or fewer (many rows share
+// the SMs) get one CTA each, in their own instantiation (SOLO), whose
+// histograms and gather list stay in shared memory.
+//
 // The kernel is enqueued before the host has checked k <= R <= M; a row that
 // fails the check is marked skip and its outputs are not touched.  The check's
 // outcome is recorded in the row state (settle_row), so that the kernels of
@@ -138,10 +144,6 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
   const int64_t len = static_cast<int64_t>(R);
   const int64_t G = gridDim.x;
   const unsigned long long* keys = a.buf + static_cast<int64_t>(row) * a.M;
-  // Output positions: every CTA reads the list of cnt keys into shared
-  // memory, and each key's position is the number of listed keys above it
-  // (keys are distinct), counted by one warp per key, the keys spread over
-  // all warps of the launch; the first k are written.
   // A key's output slot e < k: (value, index).
   auto emit = [&](int64_t e, unsigned long long key) {
     const uint32_t idx = cand_index(key);
