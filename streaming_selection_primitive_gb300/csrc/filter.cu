@@ -620,7 +620,11 @@ int filter_default_grid(int sms) {
 
 void launch_filter(const FilterArgs& args, cudaStream_t stream) {
   FilterArgs a = args;
-  const bool unaligned = (reinterpret_cast<uintptr_t>(a.x) & 15u) != 0 || (a.nrows > 1 && (a.ld & 3) != 0);
+  // Some row off the 16-byte grid: x itself, or a row stride that is not a
+  // multiple of 4 elements whenever a row other than the first can be among
+  // those listed (several rows, or a row list, which may hold one later row).
+  const bool unaligned = (reinterpret_cast<uintptr_t>(a.x) & 15u) != 0 ||
+                         ((a.ld & 3) != 0 && (a.nrows > 1 || a.rows != nullptr));
   if (unaligned) a.block_eq = nullptr;  // the tie bookkeeping counts per aligned block
   const int64_t WT = 32 * 4 * FU;
   const int64_t warp_tiles = ((a.n + (unaligned ? 3 : 0) + WT - 1) / WT) * a.nrows;

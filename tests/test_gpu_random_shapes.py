@@ -1,0 +1,62 @@
+"""Seeded random shapes through the whole call, against the oracle.
+
+Each case draws a shape (rows, row length, row stride and start offset, k,
+eps, input distribution, seed) from a fixed generator, so the cases are the
+same on every run.  Together they reach every form of every step (the grid,
+lists and step-by-step samplers; the filter's aligned and unaligned
+instantiations and its tie bookkeeping; the refinement's shortcuts, its grid
+and one-CTA forms and the buffer sort; the tie exit, the exact routes, the
+redraws).  Every row's result must equal the oracle procedure's: values as
+bits, indices and order, and the path, attempts and first counts.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_helpers import assert_same
+from routing import oracle_profk
+
+pytestmark = pytest.mark.gpu
+
+GENS = ("uniform", "normal", "pareto", "ulps_below_one", "levels16", "sorted_normal")
+CASES = 40
+BUDGET = 1 << 24  # elements per case, rows x n, so that the oracle stays quick
+
+
+def draw(case):
+    rng = np.random.default_rng(90_000 + case)
+    rows = int(rng.choice([1, 1, 1, 1, 2, 3, 5, 9, 17, 40, 130]))
+    n_max = max(16, BUDGET // rows)
+    lo = 1 << 18 if rng.random() < 0.75 and n_max > (1 << 18) else 16  # mostly rows long enough to sample
+    n = int(min(n_max, np.exp(rng.uniform(np.log(lo), np.log(n_max)))))
+    off = int(rng.integers(0, 4)) if rng.random() < 0.3 else 0
+    ld = n + (int(rng.integers(0, 5)) if rows > 1 else 0)
+    k_max = min(n, 30_000)
+    k = int(min(k_max, max(1, np.exp(rng.uniform(0, np.log(k_max))))))
+    eps = float(rng.choice([1e-3, 1e-3, 1e-2, 0.2]))
+    gen = str(rng.choice(GENS))
+    seed = int(rng.integers(0, 2**31))
+    return rows, n, off, ld, k, eps, gen, seed
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_random_shape(pk, cuda_device, case):
+    rows, n, off, ld, k, eps, gen, seed = draw(case)
+    base = workloads.GENERATORS[gen](rows * ld + off + 4, case, cuda_device)
+    what = f"case {case}: rows={rows} n={n} ld={ld} off={off} k={k} eps={eps} {gen}"
+    if rows == 1:
+        x = base[off:off + n]
+        v, i, st = pk.topk(x, k, eps, seed)
+        ov, oi, ost = oracle_profk(x.cpu().numpy(), k, eps, seed)
+        assert_same(v, i, ov, oi, what)
+        assert (st["path"], st["attempts"], st["R_first"]) == (ost.path, ost.attempts, ost.R_first), (what, st)
+        return
+    x = base[off:off + rows * ld].view(rows, ld)[:, :n]
+    v, i, sts = pk.topk_batched(x, k, eps, seed)
+    h = x.cpu().numpy()
+    for r in range(rows):
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, eps / rows, seed, row=r, rows=rows)
+        assert_same(v[r], i[r], ov, oi, f"{what} row {r}")
+        assert (sts[r]["path"], sts[r]["attempts"], sts[r]["R_first"]) == (ost.path, ost.attempts, ost.R_first), \
+            (what, r, sts[r])

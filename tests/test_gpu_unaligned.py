@@ -113,3 +113,30 @@ def test_filter_step_unaligned(pk, cuda_device, off):
     assert counts.tolist() == [R, R_gt, 0]
     got = np.sort((~(keys[:R].cpu().numpy().view(np.uint64) & np.uint64(0xFFFFFFFF))).astype(np.uint32))
     assert np.array_equal(got, np.flatnonzero(h >= np.float32(tau)).astype(np.uint32))
+
+
+def test_one_later_row_redrawn_alone(pk, cuda_device):
+    """Two rows, the second off the 16-byte grid (odd row stride), with a
+    forced tiny sample (S = 2048, t = 1) that fails the check about a quarter
+    of the time: when the second row alone is redrawn, its attempt runs on a
+    list of one row, which must still take the filter's unaligned form.  Every
+    seed's result is compared with the oracle, and the seeds must include
+    one where the second row alone was redrawn."""
+    rows, n, ld, k = 2, 1 << 18, (1 << 18) + 1, 40
+    x = workloads.normal(rows * ld, 21, cuda_device).view(rows, ld)[:, :n]
+    assert x[1].data_ptr() % 16 != 0
+    force = {"S": 2048, "t": 1}
+    h = x.cpu().numpy()
+    alone = 0
+    for seed in range(30):
+        pk.reset_options()
+        pk.set_option(pk.OPT_FORCE_S, 2048)
+        pk.set_option(pk.OPT_FORCE_T, 1)
+        vals, idx, sts = pk.topk_batched(x, k, 1e-3, seed)
+        for r in range(rows):
+            ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, seed, row=r, rows=rows,
+                                       force=force)
+            assert_same(vals[r], idx[r], ov, oi, f"seed {seed} row {r}")
+            assert (sts[r]["path"], sts[r]["attempts"]) == (ost.path, ost.attempts)
+        alone += sts[0]["attempts"] == 1 and sts[1]["attempts"] > 1
+    assert alone > 0
