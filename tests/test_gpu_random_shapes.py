@@ -60,3 +60,59 @@ def test_random_shape(pk, cuda_device, case):
         assert_same(v[r], i[r], ov, oi, f"{what} row {r}")
         assert (sts[r]["path"], sts[r]["attempts"], sts[r]["R_first"]) == (ost.path, ost.attempts, ost.R_first), \
             (what, r, sts[r])
+
+
+OPTION_CASES = 30
+
+
+def draw_options(case):
+    rng = np.random.default_rng(95_000 + case)
+    rows = int(rng.choice([1, 1, 2, 5, 24]))
+    n_max = max(16, (1 << 23) // rows)
+    lo = 1 << 17 if rng.random() < 0.8 and n_max > (1 << 17) else 16
+    n = int(min(n_max, np.exp(rng.uniform(np.log(lo), np.log(n_max)))))
+    ld = n + (int(rng.integers(0, 3)) if rows > 1 else 0)
+    k = int(min(n, max(1, np.exp(rng.uniform(0, np.log(min(n, 20_000)))))))
+    eps = float(rng.choice([1e-3, 0.05, 0.3]))
+    gen = str(rng.choice(GENS))
+    seed = int(rng.integers(0, 2**31))
+    opts = {"sampler": int(rng.choice([0, 1, 2, 3])), "spec": int(rng.choice([0, 0, 2, 5])),
+            "tie_exit": bool(rng.random() < 0.8), "max_attempts": int(rng.choice([1, 2, 6, 6])),
+            "api": str(rng.choice(["sync", "async"]))}
+    return rows, n, ld, k, eps, gen, seed, opts
+
+
+@pytest.mark.parametrize("case", range(OPTION_CASES))
+def test_random_options(pk, cuda_device, case):
+    """Seeded shapes under seeded options: the sampler form forced, redraws
+    enqueued on the device, the tie exit off, few attempts before the exact
+    fallback, the asynchronous form.  None of them changes a row's result,
+    path or attempts from the oracle procedure's."""
+    rows, n, ld, k, eps, gen, seed, o = draw_options(case)
+    pk.set_option(pk.OPT_SAMPLER, o["sampler"])
+    pk.set_option(pk.OPT_SPECULATIVE, o["spec"])
+    pk.set_option(pk.OPT_TIE_EXIT, int(o["tie_exit"]))
+    pk.set_option(pk.OPT_MAX_ATTEMPTS, o["max_attempts"])
+    base = workloads.GENERATORS[gen](rows * ld + 4, 500 + case, cuda_device)
+    what = f"case {case}: rows={rows} n={n} ld={ld} k={k} eps={eps} {gen} {o}"
+    kw = {"tie_exit": o["tie_exit"], "max_attempts": o["max_attempts"]}
+    if rows == 1:
+        x = base[:n]
+        if o["api"] == "sync":
+            v, i, st = pk.topk(x, k, eps, seed)
+        else:
+            v, i, st = pk.topk_async(x, k, eps, seed).wait()
+        ov, oi, ost = oracle_profk(x.cpu().numpy(), k, eps, seed, **kw)
+        assert_same(v, i, ov, oi, what)
+        assert (st["path"], st["attempts"]) == (ost.path, ost.attempts), (what, st)
+        return
+    x = base[:rows * ld].view(rows, ld)[:, :n]
+    if o["api"] == "sync":
+        v, i, sts = pk.topk_batched(x, k, eps, seed)
+    else:
+        v, i, sts = pk.topk_batched_async(x, k, eps, seed).wait()
+    h = x.cpu().numpy()
+    for r in range(rows):
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, eps / rows, seed, row=r, rows=rows, **kw)
+        assert_same(v[r], i[r], ov, oi, f"{what} row {r}")
+        assert (sts[r]["path"], sts[r]["attempts"]) == (ost.path, ost.attempts), (what, r, sts[r])
