@@ -803,8 +803,10 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
   }
   st = at<RowState>(c.ws, L.off_state);
   // The sampling path starts every attempt with k_attempt_reset, which
-  // initialises the state of its rows; the exact path needs zeroed state.
-  if (!sampling) PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState) * rows, stream));
+  // initialises the state of its rows; the exact path needs zeroed state,
+  // and so does the fallback when no attempt is allowed (max_attempts 0):
+  // no reset then runs before it, and the workspace may hold anything.
+  if (!sampling || max_attempts == 0) PK_CHECK(cudaMemsetAsync(st, 0, sizeof(RowState) * rows, stream));
   PK_CHECK(pinned(sizeof(int) * rows * 4 + REPORT_BYTES * rows + 512, &hbuf));
 
   if (!sampling) {

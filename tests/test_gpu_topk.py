@@ -324,6 +324,25 @@ def test_caller_workspace(pk, cuda_device):
     assert torch.equal(again[1], ref[1])
 
 
+@pytest.mark.parametrize("rows,n,k", [(1, 1 << 20, 100), (16, 393712, 5937), (3, 1 << 20, 40)])
+def test_no_attempts_on_a_dirty_workspace(pk, cuda_device, rows, n, k):
+    """With no attempt allowed every row goes straight to the exact fallback,
+    before any attempt has set up its state: the call must not read whatever
+    the workspace held (a caller's buffer filled with ones here)."""
+    x = workloads.sorted_normal(rows * n, 324, cuda_device).view(rows, n)
+    buf = torch.full((pk.workspace_size(rows, n, k, 0.5),), 0xFF, dtype=torch.uint8, device=cuda_device)
+    pk.set_workspace(buf)
+    pk.set_option(pk.OPT_MAX_ATTEMPTS, 0)
+    try:
+        vals, idx, sts = pk.topk_batched(x, k, 0.5, 2064010536)
+    finally:
+        pk.set_workspace(None)
+    h = x.cpu().numpy()
+    for r in range(rows):
+        assert_same(vals[r], idx[r], *topk_sort(h[r], k), f"row {r}")
+        assert (sts[r]["path"], sts[r]["attempts"]) == (pk.PATH_FALLBACK, 0), sts[r]
+
+
 @pytest.mark.parametrize("rows,n,k", [(1024, 1 << 16, 16), (256, 1 << 20, 32), (512, (1 << 18) + 4, 100),
                                       (128, 1 << 21, 32), (160, (1 << 20) + 8, 2049)])
 def test_batched_many_rows(pk, cuda_device, rows, n, k):
