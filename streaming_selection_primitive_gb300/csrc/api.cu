@@ -196,6 +196,7 @@ __global__ void k_attempt_reset(const int* rows, RowState* st, unsigned long lon
     S.tie_gt = 0;
     S.tau_copies = 0;
     S.settled = 0;
+    S.vdiff = 0;
   }
 }
 
@@ -203,6 +204,7 @@ __global__ void k_set_tau(RowState* st, float tau) {
   pdl_trigger();
   pdl_wait();
   st->tau_key = ord_key(tau);
+  st->vdiff = 0;
   st->R_ge = 0;
   st->R_gt = 0;
   st->nan = 0;

@@ -117,6 +117,9 @@ struct RowState {
   unsigned int settled;
   unsigned int tau_first;         // ord(tau) of the first attempt
   unsigned int hist[HIST_BINS];
+  // OR of ord(x) ^ ord(tau) over the filter's passers: every passer's value
+  // key agrees with tau's above the highest set bit (0: all equal tau).
+  unsigned int vdiff;
 };
 
 // Whether an attempt before `attempt` settled the row: the kernels of this

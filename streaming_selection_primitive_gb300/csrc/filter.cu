@@ -26,7 +26,10 @@
 //  * R_gt, the NaN count and those late passers are per-lane registers,
 //    reduced once per row per warp.
 // A passer (v, i) is stored as the 64-bit key (ord(v) << 32) | ~i, the order
-// the refinement sorts by.
+// the refinement sorts by.  Each store of passers also ORs their
+// ord(v) ^ ord(tau) into the row's vdiff word (one warp reduction and one
+// atomic per flush), which tells the refinement the high bits that every
+// stored value shares with tau.
 //
 // Two loops over the tiles.  The plain one is all of the above.  With the
 // tie exit's bookkeeping requested, the rows whose sample held tau more than
@@ -170,11 +173,15 @@ __device__ __forceinline__ void flush_stage(RowState& S, unsigned long long* sta
   if (lane == 0) gbase = atomicAdd(&S.R_ge, static_cast<unsigned long long>(stage_n));
   gbase = __shfl_sync(FULL_MASK, gbase, 0);
   __syncwarp();
+  uint32_t dv = 0;  // the bits where these values differ from tau's
   for (int j = lane; j < stage_n; j += 32) {
     const unsigned long long key = stage[j];
     if (gbase + j < static_cast<unsigned long long>(M)) br[gbase + j] = key;
+    dv |= static_cast<uint32_t>(key >> 32) ^ tkey;
     if constexpr (!TIE) gt += static_cast<uint32_t>(key >> 32) > tkey;
   }
+  dv = __reduce_or_sync(FULL_MASK, dv);
+  if (lane == 0 && dv != 0u) atomicOr(&S.vdiff, dv);
   if (gbase + stage_n > static_cast<unsigned long long>(M)) {
     over = true;
     if constexpr (TIE) {
@@ -506,12 +513,14 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
         if constexpr (!TIE) gt += gt_count();
         if (gbase + tot > static_cast<unsigned long long>(a.M)) over = true;
         unsigned long long pos = gbase + excl;
+        uint32_t dv = 0;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int e = u * 4 + c;
             if ((ge >> e) & 1u) {
+              dv |= ord_key(comp(v[u], c)) ^ tkey;
               if (pos < static_cast<unsigned long long>(a.M)) {
                 const int64_t idx = ebase + (static_cast<int64_t>(u) * 32 + lane) * 4 + c;
                 br[pos] = cand_key(comp(v[u], c), static_cast<uint32_t>(idx));
@@ -522,6 +531,8 @@ __device__ __forceinline__ void filter_rows(const FilterArgs& a, unsigned long l
             }
           }
         }
+        dv = __reduce_or_sync(FULL_MASK, dv);
+        if (lane == 0 && dv != 0u) atomicOr(&a.st[row].vdiff, dv);
       }
     }
     if constexpr (TIE) tie_append_tile<U>(a.st[row], tl, a.k, dropm, v, ebase);

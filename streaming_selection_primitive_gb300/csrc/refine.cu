@@ -5,11 +5,14 @@
 // One persistent kernel, one 1024-thread CTA per SM and contiguous chunk of
 // the candidates; all CTAs of the launch are resident together (chunks x rows
 // <= the SM count), so that they can meet at grid barriers (bounded waits on
-// a per-row arrival counter).  11/11/10/11/11/10-bit MSD passes over the
-// 64-bit keys narrow the bucket that holds the k-th largest key: each CTA
-// histograms its chunk's keys inside the current bucket, the histograms meet
-// in global atomics, and after the barrier every CTA reads the same totals
-// and takes the same decision.  As soon as the keys above the bucket plus
+// a per-row arrival counter).  MSD passes of 11-bit digits over the 64-bit
+// keys narrow the bucket that holds the k-th largest key, starting at the
+// highest bit where the candidates may differ (the filter records which
+// value bits of its passers differ from tau's: above them every key is the
+// same, so a pass there would find one bucket).  Each CTA histograms its
+// chunk's keys inside the current bucket, the histograms meet in global
+// atomics, and after the barrier every CTA reads the same totals and takes
+// the same decision.  As soon as the keys above the bucket plus
 // the bucket fit the gather budget (at least 2k, at most 8192 keys), every
 // CTA appends its keys at or above the bucket's bound to a gather list.
 // After one more barrier every CTA reads the list, and each key's output
@@ -35,11 +38,12 @@ namespace profk {
 
 // Per-row control block, zeroed at the start of every attempt.
 struct RefineCtl {
-  unsigned hist[6][HIST_BINS];  // pass histograms, summed over the chunks
+  unsigned hist[7][HIST_BINS];  // pass histograms, summed over the chunks
   unsigned bar;                 // grid-barrier arrivals
   unsigned cursor;              // gather-list length
   unsigned abort;               // set by a CTA whose wait gave up
-  unsigned pad[61];
+  unsigned broken;              // set by a CTA that found a key outside the shared prefix
+  unsigned pad[60];
 };
 static_assert(sizeof(RefineCtl) % 16 == 0, "RefineCtl is zeroed with 16-byte stores");
 
@@ -200,47 +204,69 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
   // One CTA: a pass costs little, so the gather waits for a smaller bucket.
   const unsigned long long lo_budget = SOLO ? 256 : 2048;
   const unsigned long long budget = k * 2 < lo_budget ? lo_budget : (k * 2 > RG_OUT ? RG_OUT : k * 2);
-  unsigned long long prefix = 0, want = k, thresh = 0, total = k;
-  int bits = 0;
+  // The digits start at the highest bit where the candidates may differ.
+  // Every value the filter stored agrees with tau above the highest set bit
+  // of the row's vdiff word, so the keys share those bits (all 32 value bits
+  // when the word is 0: every value equals tau) and the first digit starts
+  // just below them.  The first pass checks every key against that prefix;
+  // if one breaks it (a buffer the filter did not fill), every CTA learns so
+  // at the pass's barrier and the passes start again from bit 63.
+  const uint32_t vd = __ldcg(&S.vdiff);
+  int hib = vd != 0u ? 63 - __clz(vd) : 31;  // the next digit's highest bit
+  unsigned long long prefix =
+      hib == 63 ? 0ull : (static_cast<unsigned long long>(__ldcg(&S.tau_key)) << 32) >> (hib + 1);
+  unsigned long long want = k, thresh = 0, total = k;
+  bool checking = hib < 63;
   unsigned target = 0;
 #pragma unroll 1
-  for (int p = 0; p < 6; ++p) {
-    // Digits from the top: 11, 11, 10 | 11, 11, 10 bits (shifts 53, 42, 32, 21, 10, 0).
-    const int width = p % 3 == 2 ? 10 : 11;
-    const int shift = (p < 3 ? 53 : 21) - 11 * (p % 3) + (p % 3 == 2 ? 1 : 0);
-    const int nb = 1 << width, hs = shift + width;
+  for (int p = 0; p < 7 && hib >= 0; ++p) {
+    // Digits of 11 bits down from hib (the last one narrower).
+    const int width = hib < 11 ? hib + 1 : 11;
+    const int hs = hib + 1, shift = hs - width, nb = 1 << width;
     for (int b = tid; b < nb; b += RG_THREADS) h[b] = 0;
     __syncthreads();
+    bool broken = false;
     for (int64_t base = lo; base < hi; base += RG_PIECE) {
 #pragma unroll
       for (int r = 0; r < RG_KPT; ++r) {
         const int64_t i = base + r * RG_THREADS + tid;
         const unsigned long long key = held ? kk[r] : (i < hi ? __ldcg(keys + i) : 0ull);
-        const bool m = i < hi && (bits == 0 || (key >> hs) == prefix);
+        const bool m = i < hi && (hs == 64 || (key >> hs) == prefix);
+        broken |= checking && i < hi && !m;
         hist_add(h, static_cast<uint32_t>(key >> shift) & (nb - 1), m);
       }
     }
-    __syncthreads();
+    const bool brk = __syncthreads_or(broken) != 0;
     if constexpr (!SOLO) {
+      if (brk && tid == 0) atomicOr(&c.broken, 1u);
       for (int b = tid; b < nb; b += RG_THREADS)
         if (h[b]) atomicAdd(&c.hist[p][b], h[b]);
       grid_sync(c, (target += static_cast<unsigned>(G)) + (p == 0 ? a.wait.skew : 0u), &s_err, limit);
       if (s_err) break;  // block-uniform (read after a block barrier)
     }
+    if (checking) {
+      checking = false;
+      if (SOLO ? brk : __ldcg(&c.broken) != 0u) {  // block-uniform: every CTA reads the same word
+        hib = 63;
+        prefix = 0;
+        __syncthreads();
+        continue;
+      }
+    }
     // Every CTA finds the same digit: the bins counted down from the top,
-    // thread t owning nb / 1024 of them.
+    // thread t owning max(nb / 1024, 1) of them.
     if (tid == 0) {
       s_digit = 0;
       s_above = 0;
       s_count = 0;
     }
-    const int per = nb / RG_THREADS;
+    const int per = nb > RG_THREADS ? nb / RG_THREADS : 1;
     const int top = nb - 1 - tid * per;
     unsigned hv[2] = {0u, 0u};
     unsigned long long local = 0;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      if (q < per) {
+      if (q < per && top - q >= 0) {
         hv[q] = SOLO ? h[top - q] : __ldcg(&c.hist[p][top - q]);
         local += hv[q];
       }
@@ -250,7 +276,7 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
       unsigned long long acc = excl;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        if (q < per && want <= acc + hv[q]) {
+        if (q < per && top - q >= 0 && want <= acc + hv[q]) {
           s_digit = top - q;
           s_above = acc;
           s_count = hv[q];
@@ -262,7 +288,7 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
     __syncthreads();
     prefix = (prefix << width) | static_cast<unsigned long long>(s_digit);
     want -= s_above;
-    bits += width;
+    hib = shift - 1;
     const unsigned long long above_all = k - want;  // keys above the bucket, all in the top-k
     if (s_count == want || shift == 0) {  // the whole bucket is in the top-k: keys >= its bound are exactly k
       thresh = prefix << shift;

@@ -400,6 +400,7 @@ __device__ __forceinline__ void attempt_setup(const SampleArgs& a, RowState& S, 
       S.skip = 0;
       S.tie_gt = 0;
       S.settled = 0;
+      S.vdiff = 0;
     }
   }
 }
