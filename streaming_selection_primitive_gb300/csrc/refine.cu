@@ -12,14 +12,19 @@
 // same, so a pass there would find one bucket).  Each CTA histograms its
 // chunk's keys inside the current bucket, the histograms meet in global
 // atomics, and after the barrier every CTA reads the same totals and takes
-// the same decision.  As soon as the keys above the bucket plus
-// the bucket fit the gather budget (at least 2k, at most 8192 keys), every
-// CTA appends its keys at or above the bucket's bound to a gather list.
-// After one more barrier every CTA reads the list, and each key's output
-// position is the number of listed keys above it, counted by one warp per key
-// over all warps of the launch; the first k are written.  Values are decoded
-// from the keys (they hold them exactly), except zero, whose sign the key
-// does not keep: it is read from x.
+// the same decision.  As soon as the keys above the bucket plus the bucket
+// fit the gather budget (at least 2k, at most 8192 keys), every CTA appends
+// its keys at or above the bucket's bound to a gather list.  Once every CTA
+// has gathered, every CTA reads the list, and each key's output position is
+// the number of listed keys above it, counted by one warp per key over all
+// warps of the launch; the first k are written.  The launch is sized by M,
+// before R is known: the passes and the gather run on only as many CTAs as
+// chunks of RG_KEYS_PER_CTA keys need, so that their barriers wait for fewer
+// arrivals; the other CTAs leave at once when those can count the list
+// alone, and otherwise wait for the gather and join the counting, whose cost
+// grows with the square of the list.  Values are
+// decoded from the keys (they hold them exactly), except zero, whose sign
+// the key does not keep: it is read from x.
 //
 // Two shortcuts take no barrier: a row of at most 2048 candidates (few
 // enough to place by counting) is placed at once by every CTA from the
@@ -43,7 +48,8 @@ struct RefineCtl {
   unsigned cursor;              // gather-list length
   unsigned abort;               // set by a CTA whose wait gave up
   unsigned broken;              // set by a CTA that found a key outside the shared prefix
-  unsigned pad[60];
+  unsigned gdone;               // CTAs whose passes and gather are done
+  unsigned pad[59];
 };
 static_assert(sizeof(RefineCtl) % 16 == 0, "RefineCtl is zeroed with 16-byte stores");
 
@@ -55,6 +61,11 @@ constexpr int RG_PIECE = RG_THREADS * RG_KPT;     // 4096
 constexpr int RG_OUT = 8192;                      // gather capacity (64 KB of shared memory)
 constexpr int RG_MAX_K = 8192;
 constexpr int64_t RG_MAX_M = int64_t(1) << 19;
+#ifndef PROFK_REFINE_KEYS_PER_CTA
+#define PROFK_REFINE_KEYS_PER_CTA 256
+#endif
+constexpr int64_t RG_KEYS_PER_CTA = PROFK_REFINE_KEYS_PER_CTA;  // fewest keys a pass chunk gets (0: one per CTA)
+constexpr int64_t RG_PLACE_CMP = 256;  // comparisons a thread may spend counting the list on fewer CTAs
 // Every CTA of the row arrives (a release: the CTA's writes, ordered before
 // it by the block barrier, become visible with it), then waits until all
 // have (target arrivals; acquire loads of the arrival count).  A wait that
@@ -146,7 +157,9 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
     if (blockIdx.x == 0) S.skip = 0;
   }
   const int64_t len = static_cast<int64_t>(R);
-  const int64_t G = gridDim.x;
+  const int64_t GA = gridDim.x;  // CTAs of the row: all of them place the gathered keys
+  int64_t G = GA;                // chunks of the passes (fewer below, once R is known)
+  int64_t PG = GA;               // CTAs that count the gathered list (the G alone below, if they can)
   const unsigned long long* keys = a.buf + static_cast<int64_t>(row) * a.M;
   // A key's output slot e < k: (value, index).
   auto emit = [&](int64_t e, unsigned long long key) {
@@ -173,7 +186,7 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
       for (int i = tid; i < cnt; i += RG_THREADS) s_out[i] = __ldcg(list + i);
     __syncthreads();
     const int warp = tid >> 5;
-    for (int e = blockIdx.x * (RG_THREADS / 32) + warp; e < cnt; e += G * (RG_THREADS / 32)) {
+    for (int e = blockIdx.x * (RG_THREADS / 32) + warp; e < cnt; e += PG * (RG_THREADS / 32)) {
       const unsigned long long key = s_out[e];
       unsigned above = 0;
       for (int j = lane; j < cnt; j += 32) above += s_out[j] > key;
@@ -185,9 +198,44 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
   // them all): no passes and no barrier; the list is the buffer's first R
   // slots (2^22, k = 32: 27.8 -> 22.8 us a call; at R ~ 4K the passes were
   // as fast).  (The test setting of the waits keeps the passes.)
-  if (R <= 2048ull && R * R <= 256ull * static_cast<unsigned long long>(G) * RG_THREADS && a.wait.skew == 0) {
+  if (R <= 2048ull && R * R <= 256ull * static_cast<unsigned long long>(GA) * RG_THREADS && a.wait.skew == 0) {
     place(keys, static_cast<int>(R));
     return;
+  }
+  // One CTA: a pass costs little, so the gather waits for a smaller bucket.
+  const unsigned long long lo_budget = SOLO ? 256 : 2048;
+  unsigned long long budget = k * 2 < lo_budget ? lo_budget : (k * 2 > RG_OUT ? RG_OUT : k * 2);
+  // The launch was sized by M before R was known: with fewer candidates,
+  // the passes and the gather take chunks of at least RG_KEYS_PER_CTA keys
+  // on the first G CTAs, so that their barriers wait only for those.  When
+  // those G can also count the gathered list alone (2k keys at most
+  // RG_PLACE_CMP comparisons a thread; the budget is then capped there), the
+  // other CTAs leave at once, which frees their SMs for the kernels that
+  // follow.  Otherwise they wait until the G have gathered (the row's gdone
+  // count) and help count.
+  if constexpr (!SOLO) {
+    if (RG_KEYS_PER_CTA > 0) {
+      const int64_t need = (len + RG_KEYS_PER_CTA - 1) / RG_KEYS_PER_CTA;
+      if (need < G) G = need < 1 ? 1 : need;
+    }
+    const unsigned long long cap =
+        static_cast<unsigned long long>(sqrtf(static_cast<float>(G * RG_THREADS * RG_PLACE_CMP)));
+    if (G < GA && 2 * k <= cap) {
+      if (budget > cap) budget = cap;
+      PG = G;
+      if (blockIdx.x >= G) return;
+    }
+    if (blockIdx.x >= G) {
+      if (tid == 0 && !wait_count(&c.gdone, static_cast<unsigned>(G), &c.abort, limit)) s_err = 1;
+      __syncthreads();
+      if (s_err) {
+        if (tid == 0) atomicOr(&S.error, ERR_WAIT);
+        return;
+      }
+      const unsigned cur = __ldcg(&c.cursor);
+      place(gather + static_cast<int64_t>(row) * RG_OUT, static_cast<int>(cur < RG_OUT ? cur : RG_OUT));
+      return;
+    }
   }
   const int64_t C = (((len + G - 1) / G) + 31) & ~int64_t(31);
   const int64_t lo = blockIdx.x * C < len ? blockIdx.x * C : len;
@@ -201,9 +249,6 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
       kk[r] = i < hi ? __ldcg(keys + i) : 0ull;
     }
   }
-  // One CTA: a pass costs little, so the gather waits for a smaller bucket.
-  const unsigned long long lo_budget = SOLO ? 256 : 2048;
-  const unsigned long long budget = k * 2 < lo_budget ? lo_budget : (k * 2 > RG_OUT ? RG_OUT : k * 2);
   // The digits start at the highest bit where the candidates may differ.
   // Every value the filter stored agrees with tau above the highest set bit
   // of the row's vdiff word, so the keys share those bits (all 32 value bits
@@ -349,12 +394,19 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
     for (int e = tid; e < static_cast<int>(k); e += RG_THREADS) emit(e, s_out[e]);
     return;
   }
-  grid_sync(c, target += static_cast<unsigned>(G), &s_err, limit);
+  // Every CTA of the row waits for the G gathers (its own included).
+  __syncthreads();
+  if (tid == 0) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&c.gdone) : "memory");
+    if (!wait_count(&c.gdone, static_cast<unsigned>(G), &c.abort, limit)) s_err = 1;
+  }
+  __syncthreads();
   if (s_err) {
     if (tid == 0) atomicOr(&S.error, ERR_WAIT);
     return;
   }
-  place(gr, static_cast<int>(total < RG_OUT ? total : RG_OUT));
+  const unsigned cur = __ldcg(&c.cursor);  // = total; read as the waiting CTAs read it
+  place(gr, static_cast<int>(cur < RG_OUT ? cur : RG_OUT));
 }
 
 }  // namespace
