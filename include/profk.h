@@ -245,7 +245,14 @@ typedef enum profk_option {
                                   sampler takes the rows (see PROFK_OPT_SAMPLER) and
                                   PROFK_OPT_TIMING is off.  A call whose rows all pass the first check
                                   pays the empty attempts' launches (a few microseconds each) */
-  PROFK_OPT__COUNT = 13
+  PROFK_OPT_PREFIX_TEST = 13,  /* test of the grid refinement's prefix check [0]: v in 1 .. 33 makes the
+                                  refinement (k <= 8192) trust only the low v - 1 bits of the filter's
+                                  record of the bits in which its passers' values differ from tau, so
+                                  that it takes a longer prefix as shared by every candidate than the
+                                  candidates share; its first pass finds a key outside that prefix and
+                                  every CTA of the row starts the passes again from the key's top bit.
+                                  Results and statistics are those of the default */
+  PROFK_OPT__COUNT = 14
 } profk_option;
 #define PROFK_WAIT_TEST_OFF 0
 #define PROFK_WAIT_TEST_SAMPLER 1

@@ -13,8 +13,8 @@ import ctypes as C
 
 from . import _abi
 from ._abi import (OPT_FILTER_CTAS_PER_SM, OPT_FORCE_M, OPT_FORCE_S, OPT_FORCE_T, OPT_MAX_ATTEMPTS,
-                   OPT_MAX_SEGMENT, OPT_PARAM_MODE, OPT_PDL, OPT_SAMPLER, OPT_SPECULATIVE, OPT_TIE_EXIT, OPT_TIMING,
-                   OPT_WAIT_TEST, WAIT_TEST_OFF, WAIT_TEST_REFINE, WAIT_TEST_SAMPLER, WAIT_TEST_SORT, PARAMS_CORRECTED,
+                   OPT_MAX_SEGMENT, OPT_PARAM_MODE, OPT_PDL, OPT_PREFIX_TEST, OPT_SAMPLER, OPT_SPECULATIVE, OPT_TIE_EXIT,
+                   OPT_TIMING, OPT_WAIT_TEST, WAIT_TEST_OFF, WAIT_TEST_REFINE, WAIT_TEST_SAMPLER, WAIT_TEST_SORT, PARAMS_CORRECTED,
                    PARAMS_DEFAULT, PARAMS_EXACT, SAMPLER_AUTO, SAMPLER_GRID, SAMPLER_LISTS, SAMPLER_STEPS,
                    PARAMS_OLD, PATH_EXACT, PATH_FALLBACK, PATH_FILTER, PATH_TIE, ProfkError, ProfkStats)
 

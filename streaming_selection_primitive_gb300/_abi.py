@@ -31,8 +31,9 @@ OPT_SAMPLER = 10
 SAMPLER_AUTO, SAMPLER_GRID, SAMPLER_STEPS, SAMPLER_LISTS = 0, 1, 2, 3
 OPT_WAIT_TEST = 11
 OPT_SPECULATIVE = 12
+OPT_PREFIX_TEST = 13
 WAIT_TEST_OFF, WAIT_TEST_SAMPLER, WAIT_TEST_REFINE, WAIT_TEST_SORT = 0, 1, 2, 3
-OPT_DEFAULTS = {0: 0, 1: 6, 2: 1, 3: 0, 4: 0, 5: 0, 6: 0, 7: 0, 8: 1, 9: 0, 10: 0, 11: 0, 12: 0}
+OPT_DEFAULTS = {0: 0, 1: 6, 2: 1, 3: 0, 4: 0, 5: 0, 6: 0, 7: 0, 8: 1, 9: 0, 10: 0, 11: 0, 12: 0, 13: 0}
 
 
 class ProfkStats(C.Structure):

@@ -28,7 +28,8 @@ namespace {
 // ---------------------------------------------------------------------------
 // Options.
 std::atomic<int64_t> g_opt[PROFK_OPT__COUNT] = {
-    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}, {1}, {0}, {PROFK_SAMPLER_AUTO}, {PROFK_WAIT_TEST_OFF}, {0}};
+    {PROFK_PARAMS_DEFAULT}, {6}, {1}, {0}, {0}, {0}, {0}, {0}, {1}, {0}, {PROFK_SAMPLER_AUTO}, {PROFK_WAIT_TEST_OFF}, {0},
+    {0}};
 
 // PROFK_OPT_WAIT_TEST: the wait setting of the persistent kernel it names
 // (one arrival more than the launch has at its first grid barrier, and a
@@ -605,6 +606,8 @@ cudaError_t enqueue_attempt(const Layout& L, void* ws, const Params& P, int a, i
   if (!L.radix_refine) {
     RefineGridArgs ga{at<unsigned long long>(ws, L.off_buf), P.M, ng, gl, st, k, x, ld, n, out_vals, out_idx};
     ga.wait = wait_cfg_for(PROFK_WAIT_TEST_REFINE);
+    const int64_t pt = g_opt[PROFK_OPT_PREFIX_TEST].load();
+    if (pt > 0) ga.vdiff_keep = pt > 32 ? 0xFFFFFFFFu : (1u << (pt - 1)) - 1u;
     ga.attempt = a;
     ga.tie_exit = tie_exit;
     e = launch_refine_grid(ga, at<char>(ws, L.off_refine), rows, stream);
@@ -1346,6 +1349,7 @@ int profk_set_option(int option, int64_t value) {
   if (option == PROFK_OPT_WAIT_TEST && (value < PROFK_WAIT_TEST_OFF || value > PROFK_WAIT_TEST_SORT))
     return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_SPECULATIVE && value > 8) return PROFK_ERR_INVALID;
+  if (option == PROFK_OPT_PREFIX_TEST && value > 33) return PROFK_ERR_INVALID;
   if (option == PROFK_OPT_MAX_SEGMENT && value != 0 && (value < (1 << 16) || value > (int64_t(1) << 32) || (value & 3)))
     return PROFK_ERR_INVALID;
   if (value < 0) return PROFK_ERR_INVALID;

@@ -275,6 +275,9 @@ struct RefineOneArgs {
   // tie exit is on.
   int attempt = 0;
   bool tie_exit = false;
+  // launch_refine_grid: the bits of the filter's RowState::vdiff it trusts
+  // (all but in the test of its prefix check).
+  uint32_t vdiff_keep = 0xFFFFFFFFu;
 };
 void launch_refine_one(const RefineOneArgs& a, cudaStream_t stream);
 int64_t refine_one_max_k();

@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(RG_THREADS, 1) k_refine_grid(RefineGridArgs a,
   // just below them.  The first pass checks every key against that prefix;
   // if one breaks it (a buffer the filter did not fill), every CTA learns so
   // at the pass's barrier and the passes start again from bit 63.
-  const uint32_t vd = __ldcg(&S.vdiff);
+  const uint32_t vd = __ldcg(&S.vdiff) & a.vdiff_keep;
   int hib = vd != 0u ? 63 - __clz(vd) : 31;  // the next digit's highest bit
   unsigned long long prefix =
       hib == 63 ? 0ull : (static_cast<unsigned long long>(__ldcg(&S.tau_key)) << 32) >> (hib + 1);

@@ -184,3 +184,15 @@ def test_speculative_option(pk):
     for bad in (9, -1):
         with pytest.raises(pk.ProfkError):
             pk.set_option(pk.OPT_SPECULATIVE, bad)
+
+
+def test_prefix_test_option(pk):
+    # The test setting of the grid refinement's prefix check: off by default,
+    # 1 .. 33 (the number of trusted low bits of the filter's record, plus one).
+    assert pk.get_option(pk.OPT_PREFIX_TEST) == 0
+    for v in (1, 9, 33, 0):
+        pk.set_option(pk.OPT_PREFIX_TEST, v)
+        assert pk.get_option(pk.OPT_PREFIX_TEST) == v
+    for bad in (34, -1):
+        with pytest.raises(pk.ProfkError):
+            pk.set_option(pk.OPT_PREFIX_TEST, bad)

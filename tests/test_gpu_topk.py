@@ -501,3 +501,39 @@ def test_signed_zeros_at_the_top(pk, cuda_device, rows, zeros, k):
         ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 5, row=r, rows=rows)
         assert_same(vals[r], idx[r], ov, oi, f"row {r}")
         assert sts[r]["path"] == ost.path
+
+
+# (generator, rows, n, k, M): the grid form of the refinement on one row and
+# on three, and its one-CTA-per-row form (80 rows); S and t forced so that R
+# (about n t / S) is far above the few-candidates shortcut, M above R.
+PREFIX_CASES = {"grid_row": ("normal", 1, 1 << 22, 1000, 100_000), "grid_rows": ("uniform", 3, 1 << 20, 500, 40_000),
+                "solo_rows": ("normal", 80, 1 << 18, 64, 10_000)}
+
+
+@pytest.mark.parametrize("keep", [1, 9, 20])
+@pytest.mark.parametrize("case", list(PREFIX_CASES))
+def test_refinement_prefix_check_restarts(pk, cuda_device, case, keep):
+    """The grid refinement's first digit starts below the high bits that the
+    filter records every candidate sharing with tau, and its first pass
+    checks that.  Told to trust only the low keep - 1 bits of the record, it
+    assumes a longer shared prefix than the candidates have (keep = 1: tau's
+    whole value), must find a key outside it and start the passes again from
+    the top bit; the result is the oracle's all the same."""
+    gen, rows, n, k, M = PREFIX_CASES[case]
+    force = {"S": 4096, "t": 64, "M": M}
+    x = workloads.GENERATORS[gen](rows * n, 17, cuda_device).view(rows, n)
+    pk.set_option(pk.OPT_FORCE_S, force["S"])
+    pk.set_option(pk.OPT_FORCE_T, force["t"])
+    pk.set_option(pk.OPT_FORCE_M, force["M"])
+    pk.set_option(pk.OPT_PREFIX_TEST, keep)
+    if rows == 1:
+        v, i, st = pk.topk(x[0], k, 1e-3, 8)
+        v, i, sts = v[None], i[None], [st]
+    else:
+        v, i, sts = pk.topk_batched(x, k, 1e-3, 8)
+    h = x.cpu().numpy()
+    for r in range(rows):
+        ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, 1e-3 / rows, 8, row=r, rows=rows, force=force)
+        assert_same(v[r], i[r], ov, oi, f"{case} keep={keep} row {r}")
+        assert (sts[r]["path"], sts[r]["attempts"], sts[r]["R_first"]) == (ost.path, ost.attempts, ost.R_first)
+        assert sts[r]["path"] == pk.PATH_FILTER and sts[r]["R_first"] > 2048
