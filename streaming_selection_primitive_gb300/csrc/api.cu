@@ -326,6 +326,16 @@ __global__ void __launch_bounds__(256) k_report(const RowState* st, int rows, un
 
 thread_local unsigned long long t_report_seq = 0;
 
+// The host buffers of the reports are reused from call to call, and where a
+// call's flag word lies depends on its row count: an earlier call's report
+// (a count, a rank, a key) may hold any value there, the new call's sequence
+// number included.  So the word is cleared before the kernel that writes it
+// is enqueued (sequence numbers start at 1).
+void clear_flag(unsigned long long* flag) {
+  *reinterpret_cast<volatile unsigned long long*>(flag) = 0ull;
+  std::atomic_thread_fence(std::memory_order_seq_cst);
+}
+
 // Waits for the report of sequence number `seq`.  A stream that fails or
 // finishes without it (or a wait of more than 10 s) ends the wait with the
 // stream synchronized, so that its error, if any, is returned.
@@ -872,6 +882,7 @@ int run_topk(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k, dou
         unsigned long long* flag =
             reinterpret_cast<unsigned long long*>(align_up(reinterpret_cast<uintptr_t>(rep + REPORT_BYTES * rows)));
         const unsigned long long seq = ++t_report_seq;
+        clear_flag(flag);
         PK_CHECK(enqueue_report(st, rows, rep, flag, seq, stream));
         if (time_it) PK_CHECK(cudaEventRecord(t_events.e[5], stream));
         if (rows <= REPORT_ROWS_MAPPED) {
@@ -1172,6 +1183,7 @@ int submit_async(const float* x, int64_t rows, int64_t n, int64_t ld, int64_t k,
     call->flag = reinterpret_cast<unsigned long long*>(
         align_up(reinterpret_cast<uintptr_t>(call->host + REPORT_BYTES * rows)));
     call->seq = ++g_async_seq;
+    clear_flag(call->flag);
     e = enqueue_report(at<RowState>(call->ws, L.off_state), rows, call->host, call->flag, call->seq, stream);
   }
   if (e == cudaSuccess && rows > REPORT_ROWS_MAPPED) {

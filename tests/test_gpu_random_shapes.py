@@ -15,6 +15,7 @@ import torch
 
 import workloads
 from gpu_helpers import assert_same
+from oracle.topk import topk_sort
 from routing import oracle_profk
 
 pytestmark = pytest.mark.gpu
@@ -116,3 +117,40 @@ def test_random_options(pk, cuda_device, case):
         ov, oi, ost = oracle_profk(np.ascontiguousarray(h[r]), k, eps / rows, seed, row=r, rows=rows, **kw)
         assert_same(v[r], i[r], ov, oi, f"{what} row {r}")
         assert (sts[r]["path"], sts[r]["attempts"]) == (ost.path, ost.attempts), (what, r, sts[r])
+
+
+SEGMENT_CASES = 16
+
+
+def draw_segmented(case):
+    rng = np.random.default_rng(97_000 + case)
+    rows = int(rng.choice([1, 1, 2, 3]))
+    n = int(rng.integers((1 << 16) + 1, 1 << 21))
+    seg = max(1 << 16, 4 * int(rng.integers(1 << 14, max((1 << 14) + 1, n // 8))))  # a multiple of 4, >= 2^16
+    off = int(rng.integers(0, 4)) if rng.random() < 0.4 else 0
+    ld = n + (int(rng.integers(0, 5)) if rows > 1 else 0)
+    k = int(min(n, max(1, np.exp(rng.uniform(0, np.log(min(n, 50_000)))))))
+    gen = str(rng.choice(GENS))
+    seed = int(rng.integers(0, 2**31))
+    return rows, n, off, ld, seg, k, gen, seed
+
+
+@pytest.mark.parametrize("case", range(SEGMENT_CASES))
+def test_random_segmented(pk, cuda_device, case):
+    """Seeded rows split into segments (the split point lowered to a random
+    multiple of 4), starting anywhere, with any row stride: each row's
+    merged result must be its exact top k (values as bits, indices, order)."""
+    rows, n, off, ld, seg, k, gen, seed = draw_segmented(case)
+    pk.set_option(pk.OPT_MAX_SEGMENT, seg)
+    base = workloads.GENERATORS[gen](rows * ld + off + 4, 700 + case, cuda_device)
+    what = f"case {case}: rows={rows} n={n} off={off} ld={ld} segment={seg} k={k} {gen}"
+    if rows == 1:
+        x = base[off:off + n]
+        v, i, _ = pk.topk(x, k, 1e-3, seed)
+        assert_same(v, i, *topk_sort(x.cpu().numpy(), k), what)
+        return
+    x = base[off:off + rows * ld].view(rows, ld)[:, :n]
+    v, i, _ = pk.topk_batched(x, k, 1e-3, seed)
+    h = x.cpu().numpy()
+    for r in range(rows):
+        assert_same(v[r], i[r], *topk_sort(np.ascontiguousarray(h[r]), k), f"{what} row {r}")
